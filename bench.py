@@ -1,0 +1,350 @@
+"""Benchmark of the EXL3 trellis-quantized linear on one GB300.
+
+Workload of a step: the dense decode sweep k = 5120, n in {5120, 17408,
+25600}, K = 4, M = 1 (three fused GEMV launches, fp16 out).  `value` is the
+aggregate algorithmic HBM traffic of those linears (packed weights + x + y +
+suh + svh) per second, with inputs resident on the device.  Three copies of
+the weights rotate between steps (3 x 123 MB > 2 x L2), so no step reads
+another's weights from L2.
+
+Extra objects on the same JSON line: `roofline` (the GEMV kernel against the
+measured HBM copy bandwidth), `cpu_baseline` (the CPU oracle on a bounded
+sample), `e2e` (the same metric through the C ABI with host buffers: x copied
+in and y copied out each step), `prefill` (M = 4096 TFLOP/s), and `clocks`.
+
+    python bench.py [--gpus 1] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import exl3_synth as synth  # noqa: E402
+
+METRIC = "EXL3 trellis GEMV HBM GB/s (M=1) & GEMM TFLOPS (M=4096), % of roofline"
+WORKLOAD = "dense decode GEMV sweep k=5120 n={5120,17408,25600} K=4 M=1 mul1, fp16 out"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+# dram bytes (read + write) per launch from an ncu capture of gemv_m1_kernel<4>
+# at k=5120 n=17408, with the hash of gemv.cu at capture time; a changed
+# kernel source makes the recorded traffic stale (reported as null).
+TRAFFIC = {"file": "trellis_quantized_gb300/csrc/gemv.cu", "sha1": None, "bytes_per_launch": None,
+           "workload": "k5120 n17408 K4 M1"}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def linear_bytes(case) -> int:
+    return case.trellis.nbytes + case.x.nbytes + case.suh.nbytes + case.svh.nbytes + case.M * case.n * 2
+
+
+def file_sha1(rel):
+    with open(os.path.join(ROOT, rel), "rb") as f:
+        return hashlib.sha1(f.read()).hexdigest()
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = max(mx, float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": mx or None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- ours
+
+def run_ours(args):
+    import torch
+    import trellis_quantized_gb300 as tq
+
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16
+                                     else np.ascontiguousarray(a)).cuda()
+    cases = [synth.config2(n, 1) for n in synth.CONFIG2_N]
+    copies = 3
+    dcases = []
+    for c in cases:
+        base_t = dev(c.trellis)
+        ts = [base_t] + [base_t.clone() for _ in range(copies - 1)]
+        ws = tq.workspace(tq.exl3_linear_workspace_size(1, c.k, c.n, c.K))
+        wsc = torch.zeros_like(ws)
+        dcases.append(dict(case=c, x=dev(c.x), t=ts, suh=dev(c.suh), svh=dev(c.svh),
+                           y=torch.empty((1, c.n), dtype=torch.float16, device="cuda"), ws=wsc))
+    stream = torch.cuda.current_stream()
+    L = tq.lib()
+
+    def launch(d, copy):
+        c = d["case"]
+        rc = L.exl3_linear(d["x"].data_ptr(), 1, c.k, c.n, d["t"][copy].data_ptr(), d["suh"].data_ptr(),
+                           d["svh"].data_ptr(), c.K, tq.EXL3_CB_MUL1, d["y"].data_ptr(), tq.EXL3_OUT_F16,
+                           d["ws"].data_ptr(), d["ws"].numel(), stream.cuda_stream)
+        if rc:
+            raise tq.Exl3Error(rc, L.exl3_last_error().decode())
+
+    step_bytes = sum(linear_bytes(d["case"]) for d in dcases)
+    for d in dcases:
+        tq.exl3_workspace_clear(d["ws"])
+    for i in range(args.warmup):
+        for d in dcases:
+            launch(d, i % copies)
+    torch.cuda.synchronize()
+
+    # per-launch CUDA events on the launching stream (for the roofline)
+    n_ev = args.steps * len(dcases)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_ev)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        time.sleep(0.3)
+        torch.cuda.synchronize()
+        t_start.record(stream)
+        e = 0
+        for i in range(args.steps):
+            for d in dcases:
+                evs[e][0].record(stream)
+                launch(d, i % copies)
+                evs[e][1].record(stream)
+                e += 1
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        time.sleep(0.2)
+    total_ms = t_start.elapsed_time(t_end)
+    per = np.array([a.elapsed_time(b) for a, b in evs]).reshape(args.steps, len(dcases))
+    ms_per_step = total_ms / args.steps
+    value = step_bytes / (ms_per_step * 1e-3) / 1e9
+
+    hbm, bf16, src = peaks()
+    kern_ms = per.mean(axis=0)                      # average duration per launch, per n
+    big = len(dcases) - 1                           # n = 25600, the largest launch
+    big_bytes = linear_bytes(dcases[big]["case"])
+    achieved = big_bytes / (kern_ms[big] * 1e-3) / 1e9
+    traffic = None
+    if TRAFFIC["sha1"] and TRAFFIC["sha1"] == file_sha1(TRAFFIC["file"]):
+        traffic = TRAFFIC["bytes_per_launch"]
+    roofline = {"bound": "hbm", "kernel": "gemv_m1_kernel<K=4> (k=5120 n=25600)", "achieved": round(achieved, 1),
+                "peak": hbm, "peak_source": src, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                "traffic": traffic,
+                "per_n": {str(d["case"].n): {"us": round(float(kern_ms[j]) * 1e3, 2),
+                                             "GBs": round(linear_bytes(d["case"]) / (kern_ms[j] * 1e-3) / 1e9, 1)}
+                          for j, d in enumerate(dcases)}}
+
+    # e2e: host x (pinned) -> device, linear, y -> host, every linear of the step
+    hx = [torch.from_numpy(d["case"].x).pin_memory() for d in dcases]
+    hy = [torch.empty((1, d["case"].n), dtype=torch.float16).pin_memory() for d in dcases]
+    e2e_steps = max(10, args.steps // 4)
+    for i in range(3):
+        for j, d in enumerate(dcases):
+            d["x"].copy_(hx[j], non_blocking=True)
+            launch(d, i % copies)
+            hy[j].copy_(d["y"], non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(e2e_steps):
+        for j, d in enumerate(dcases):
+            d["x"].copy_(hx[j], non_blocking=True)
+            launch(d, i % copies)
+            hy[j].copy_(d["y"], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e = {"value": round(step_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+           "h2d_bytes_per_step": int(sum(d["case"].x.nbytes for d in dcases)),
+           "d2h_bytes_per_step": int(sum(d["case"].n * 2 for d in dcases))}
+
+    prefill = bench_prefill(args, bf16, src) if not args.skip_prefill else None
+    for d in dcases:
+        assert tq.exl3_check_device_error(d["ws"]) == 0
+
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u16 trellis -> f32 accumulate, f16 out",
+        "data": "synthetic (seeded PCG64: uniform trellis, +-1 suh/svh, x ~ N(0,1) fp16)",
+        "config": {"workload": WORKLOAD, "K": 4, "k": 5120, "n": list(synth.CONFIG2_N), "M": 1,
+                   "l2": "3 rotating weight copies (369 MB > 2x L2), no flush",
+                   "parallelism": "single GPU; replicas only"},
+        "gpu_launches": int(args.steps * len(dcases)),
+        "roofline": roofline, "e2e": e2e, "clocks": clk.summary(), "prefill": prefill,
+    }
+    if not args.skip_cpu:
+        out["cpu_baseline"] = cpu_baseline(args)
+    return out
+
+
+def bench_prefill(args, bf16_peak, src):
+    """M = 4096, k = 5120, n = 17408, K = 4 (fp16 path): TFLOP/s of the whole call."""
+    import torch
+    import trellis_quantized_gb300 as tq
+    c = synth.config4()
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16
+                                     else np.ascontiguousarray(a)).cuda()
+    x, t, suh, svh = dev(c.x), dev(c.trellis), dev(c.suh), dev(c.svh)
+    ws = tq.workspace(tq.exl3_linear_workspace_size(c.M, c.k, c.n, c.K))
+    y = torch.empty((c.M, c.n), dtype=torch.float16, device="cuda")
+    for _ in range(3):
+        tq.exl3_linear(x, t, suh, svh, 4, y=y, workspace_buf=ws)
+    torch.cuda.synchronize()
+    reps = 10
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        tq.exl3_linear(x, t, suh, svh, 4, y=y, workspace_buf=ws)
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / reps
+    flops = 2.0 * c.M * c.k * c.n
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"workload": "M=4096 k=5120 n=17408 K=4 fp16 out", "ms": round(ms, 4), "tflops": round(tf, 1),
+            "peak_tflops": bf16_peak, "peak_source": src + " bf16 sustained", "frac": round(tf / bf16_peak, 4),
+            "path": "reconstruct + mma.sync GEMM (interim)"}
+
+
+# ------------------------------------------------------------------------- oracle
+
+def cpu_baseline(args):
+    """The CPU oracle, as it stands, on a bounded sample: the n = 5120 linear of
+    the sweep (decode + float64 contraction + transforms), timed in full."""
+    import oracle
+    oracle.build()
+    c = synth.config2(5120, 1)
+    oracle.linear(c.x[:1, :128], c.trellis[:8, :8], c.suh[:128], c.svh[:128], 4)   # load
+    reps = 1
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.linear(c.x, c.trellis, c.suh, c.svh, 4)
+    dt = (time.perf_counter() - t0) / reps
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": round(linear_bytes(c) / dt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"one k=5120 n=5120 K=4 M=1 linear ({linear_bytes(c)} algorithmic bytes) in {dt:.2f} s"}
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle timed as the reference arm."""
+    import oracle
+    oracle.build()
+    c = synth.config2(5120, 1)
+    for _ in range(args.warmup):
+        oracle.linear(c.x[:1, :128], c.trellis[:8, :8], c.suh[:128], c.svh[:128], 4)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.linear(c.x, c.trellis, c.suh, c.svh, 4)
+    dt = (time.perf_counter() - t0) / max(args.steps, 1)
+    value = linear_bytes(c) / dt / 1e9
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded PCG64)",
+            "config": {"workload": WORKLOAD + " (each step: the n=5120 linear, a bounded sample)", "K": 4,
+                       "k": 5120, "n": [5120], "M": 1, "parallelism": "CPU oracle"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": "one k=5120 n=5120 K=4 M=1 linear per step"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--skip-prefill", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if args.steps > 20:
+            args.steps = 3
+        if rank == 0:
+            print(json.dumps(run_reference(args)))
+        return
+    if args.gpus > 1 or int(os.environ.get("WORLD_SIZE", "1")) > 1:
+        # replicas only: every rank runs the same single-GPU workload
+        import torch
+        import torch.distributed as dist
+        local = int(os.environ.get("LOCAL_RANK", "0"))
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        out = run_ours(args)
+        t = torch.tensor([out["ms_per_step"]], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ws = dist.get_world_size()
+        step_bytes = out["value"] * 1e9 * out["ms_per_step"] * 1e-3      # this rank's bytes per step
+        out["ms_per_step"] = float(t.item())                             # slowest rank
+        out["value"] = round(step_bytes * ws / (out["ms_per_step"] * 1e-3) / 1e9, 1)
+        out["n_gpus"] = ws
+        if rank == 0:
+            print(json.dumps(out))
+        dist.destroy_process_group()
+        return
+    print(json.dumps(run_ours(args)))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,180 @@
+/*
+ * exl3.h -- C ABI of libexl3, the EXL3 trellis-quantized linear layer on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * What the layer computes (sources by page title and section):
+ *   - "exl3xpu" README, "Prefill: int8 linears and oneDNN fused attention":
+ *     the GEMM runs in the Hadamard domain; every mul1 codebook value is
+ *     bounded by 3.453125; the int8 variant has one activation scale per row
+ *     (fused into the input Hadamard) and one static weight scale (fused into
+ *     reconstruct), an s8 GEMM writing fp16.
+ *   - "exl3xpu" README, "Layout": Hadamard in/out, GEMV, reconstruct kernels.
+ *   - "exl3xpu" README, "MoE (routed experts)": the routed contribution in
+ *     fp32 with the routing weight on the down-projection output; codebook
+ *     ids (1 = MCG, 2 = mul1); unsupported width/codebook raises.
+ *   - "Bringing EXL3 Trellis Quantization to 35B MoE on Intel Arc 140V",
+ *     sections 1 and 2.A-2.D: trellis tensor [k/16, n/16, 16K]; packed expert
+ *     arenas [E, nslots, k/16, n/16, 16K]; one grouped launch for gate+up
+ *     (nslots = 2, shared input row) and one for down; device-side binning.
+ *   - "exl3xpu" README, "Adding a model": all dims multiples of 128.
+ *   - "EXL3 checkpoints on the native engine (tracker) #832": widths 1..8 per
+ *     tensor; fp32-output projections.
+ *
+ * Format (this library's reading where the pages are silent):
+ *   trellis  uint16 [k/16][n/16][16*K], tiles along n innermost.  Tile bit i
+ *            is bit (i mod 16) of word i/16.  Weight p = 16*r + c of a tile
+ *            (r along k, c along n) has the 16-bit state formed by stream bits
+ *            p*K .. p*K+15 (LSB first), wrapping around the tile's 256*K bits.
+ *   mul1     v(s) = fp16_RNE((B(s) - 510) * sigma), B(s) = sum of the bytes of
+ *            (s * 0x9E3779B1) mod 2^32, sigma = 1775 * 2^-18 (= fp16 of
+ *            3.453125/510).  |v| <= 3.453125, attained at s = 0.
+ *   RHT      x' = 2^-3.5 * H (x . suh) per aligned 128-block, H the Sylvester
+ *            Hadamard in natural order; y = (2^-3.5 * H y') . svh per block.
+ *   linear   y = RHT_out( RHT_in(x . suh) @ W ) . svh, W = decoded weights.
+ *
+ * Conventions for every entry point:
+ *   - All pointers are DEVICE pointers unless stated; the caller owns every
+ *     buffer.  The library allocates nothing and never synchronises the
+ *     stream; every call only enqueues work on `stream` (asynchronous).
+ *   - fp16 tensors are IEEE binary16 passed as uint16_t bits.
+ *   - Device buffers must be 16-byte aligned; row-major, densely packed.
+ *   - Return: EXL3_OK, or an error code with nothing enqueued (argument
+ *     errors) or with the CUDA launch error captured (EXL3_ERR_CUDA).
+ *     exl3_last_error() gives a message for the calling thread.
+ *   - Workspaces: size from the matching *_workspace_size(); must be zero
+ *     filled once before first use (exl3_workspace_clear); each call leaves
+ *     its counters at zero again.  One workspace must not be used by calls
+ *     that can run concurrently.
+ */
+#ifndef EXL3_H
+#define EXL3_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define EXL3_OK 0
+#define EXL3_ERR_ARG 1        /* null or misaligned pointer, bad enum value */
+#define EXL3_ERR_SHAPE 2      /* k or n not a multiple of 128, M < 1, bad tile range */
+#define EXL3_ERR_BITS 3       /* K outside 1..8 */
+#define EXL3_ERR_CODEBOOK 4   /* codebook other than mul1: fail closed, never guess */
+#define EXL3_ERR_WORKSPACE 5  /* workspace missing or too small */
+#define EXL3_ERR_CUDA 6       /* a CUDA call failed; message holds the CUDA error */
+#define EXL3_ERR_DEVICE 7     /* a kernel reported a violation in the error word */
+
+typedef enum { EXL3_CB_MCG = 1, EXL3_CB_MUL1 = 2, EXL3_CB_3INST = 3 } exl3_codebook;
+typedef enum { EXL3_OUT_F16 = 0, EXL3_OUT_F32 = 1 } exl3_out_dtype;
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *exl3_stream_t;
+
+/* Message for the last failed call on this thread ("" if none). */
+const char *exl3_last_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int exl3_version(void);
+
+/* Enqueue a zero fill of a workspace (cudaMemsetAsync; needed once before a
+ * workspace is first used). */
+int exl3_workspace_clear(void *workspace, size_t ws_bytes, exl3_stream_t stream);
+
+/* Test helper: waits for `stream`, then copies the device error word of a
+ * workspace to *err_out (0 = no violation recorded) and clears it. */
+int exl3_check_device_error(void *workspace, size_t ws_bytes, exl3_stream_t stream, int *err_out);
+
+/*
+ * exl3_decode_tile -- dequantise ("reconstruct", "exl3xpu" README, "Layout";
+ * bit-exact dequantised weights, "exl3xpu" README, "Correctness").
+ *   trellis  [k/16][n/16][16*K] uint16 (whole tensor)
+ *   tiles    [tk0, tk0+tk_cnt) x [tn0, tn0+tn_cnt) of the tile grid
+ *   w_out    fp16 bits; weight (16*tk + r, 16*tn + c) of the requested range
+ *            is written to w_out[(16*(tk-tk0) + r) * ld + 16*(tn-tn0) + c],
+ *            ld >= 16*tn_cnt elements, ld a multiple of 8.
+ *   Only k, n multiples of 16 are required here.  No workspace.
+ */
+int exl3_decode_tile(const uint16_t *trellis, int k, int n, int K, int codebook,
+                     int tk0, int tk_cnt, int tn0, int tn_cnt,
+                     uint16_t *w_out, int64_t ld, exl3_stream_t stream);
+
+/*
+ * exl3_input_rht -- the input transform alone (the "Hadamard in" kernel of
+ * "exl3xpu" README, "Layout"): x' = 2^-3.5 H (x . suh) per 128-block.
+ *   x [M][k] fp16, suh [k] fp16; out [M][k] as fp32 (out_dtype = EXL3_OUT_F32)
+ *   or fp16 (EXL3_OUT_F16).  fp32 results are bit-identical to the stated
+ *   butterfly order (stages 1, 2, ..., 64 of (a+b, a-b), then one multiply by
+ *   fp32(2^-3.5)).
+ */
+int exl3_input_rht(const uint16_t *x, int M, int k, const uint16_t *suh,
+                   void *out, int out_dtype, exl3_stream_t stream);
+
+/*
+ * exl3_linear -- y = RHT_out( RHT_in(x . suh) @ W ) . svh
+ * ("exl3xpu" README, "Prefill: int8 linears..." and "Layout"; fp32 outputs
+ * as the tracker #832 "decodeF32/promptF32" projections).
+ *   x        [M][k] fp16          trellis [k/16][n/16][16K] uint16
+ *   suh [k], svh [n] fp16         K in 1..8, codebook = EXL3_CB_MUL1
+ *   y        [M][n], fp16 (EXL3_OUT_F16) or fp32 (EXL3_OUT_F32)
+ *   workspace of exl3_linear_workspace_size(M, k, n, K) bytes.
+ *   M = 1 runs the fused CUDA-core GEMV; larger M runs the tensor-core paths.
+ */
+size_t exl3_linear_workspace_size(int M, int k, int n, int K);
+int exl3_linear(const uint16_t *x, int M, int k, int n,
+                const uint16_t *trellis, const uint16_t *suh, const uint16_t *svh,
+                int K, int codebook, void *y, int out_dtype,
+                void *workspace, size_t ws_bytes, exl3_stream_t stream);
+
+/*
+ * exl3_linear_int8 -- the int8 prefill variant ("exl3xpu" README, "Prefill:
+ * int8 linears and oneDNN fused attention").
+ *   a_r  = max_j |x'_rj| / 127 (fp32), x' the fp32 input transform above;
+ *   q_x  = clamp(RNE(x' * (127 / max|x'_r|)), -127, 127), int8;
+ *   q_w  = RNE(v * 127 / 3.453125) of each decoded weight v, int8;
+ *   acc  = sum_j q_x * q_w, exact int32;
+ *   y    = RHT_out(acc * a_r * weight_scale) . svh, fp16.
+ *   weight_scale must be 3.453125f/127 (the static weight scale) or > 0.
+ *   xq_out [M][k] int8, row_scale_out [M] fp32 and acc_out [M][n] int32 are
+ *   optional (NULL to skip) copies of the intermediate results.
+ */
+size_t exl3_linear_int8_workspace_size(int M, int k, int n, int K);
+int exl3_linear_int8(const uint16_t *x, int M, int k, int n,
+                     const uint16_t *trellis, const uint16_t *suh, const uint16_t *svh,
+                     int K, int codebook, float weight_scale, uint16_t *y,
+                     int8_t *xq_out, float *row_scale_out, int32_t *acc_out,
+                     void *workspace, size_t ws_bytes, exl3_stream_t stream);
+
+/*
+ * Routed experts ("exl3xpu" README, "MoE (routed experts)"; Arc 140V MoE
+ * post, sections 2.A, 2.B and 2.D).
+ *   One descriptor per projection kind, all E experts in contiguous arenas:
+ *   w13 (nslots = 2: slot 0 gate, slot 1 up; k = hidden, n = inter) and
+ *   w2 (nslots = 1; k = inter, n = hidden).  Per token t and slot s:
+ *     e = topk_ids[t][s]; g = lin(x_t; gate_e); u = lin(x_t; up_e);
+ *     h = SiLU(g) * u; y_t += topk_weights[t][s] * lin(h; down_e)
+ *   with the routing weight applied to the down output, in fp32.  Token to
+ *   expert binning happens on the device; there is no host synchronisation.
+ *   Expert ids outside [0, E) are recorded in the device error word and the
+ *   unit is skipped.
+ */
+typedef struct {
+  const uint16_t *trellis;  /* [E][nslots][k/16][n/16][16*K] */
+  const uint16_t *suh;      /* [E][nslots][k] fp16 */
+  const uint16_t *svh;      /* [E][nslots][n] fp16 */
+  int k, n, K, codebook, nslots;
+} exl3_expert_proj;
+
+size_t exl3_moe_workspace_size(int T, int topk, int E, const exl3_expert_proj *w13,
+                               const exl3_expert_proj *w2);
+int exl3_moe_grouped(const uint16_t *x, int T, int hidden,
+                     const int32_t *topk_ids, const float *topk_weights, int topk, int E,
+                     const exl3_expert_proj *w13, const exl3_expert_proj *w2,
+                     void *y, int out_dtype,
+                     void *workspace, size_t ws_bytes, exl3_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXL3_H */

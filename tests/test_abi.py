@@ -1,0 +1,95 @@
+"""The C ABI library loads, exports every entry point of include/exl3.h, and
+rejects bad arguments before launching anything (runs without a GPU).
+
+Every call below carries at least one argument that validation rejects, so
+no kernel is ever launched with the fake device addresses used here.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import trellis_quantized_gb300 as tq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FAKE = ctypes.c_void_p(0x10000)       # 16-byte aligned, never dereferenced
+FAKE_MIS = ctypes.c_void_p(0x10002)   # misaligned
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "exl3.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(exl3_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_library_builds_and_loads():
+    L = tq.lib()
+    assert os.path.exists(tq.lib_path())
+    assert L.exl3_version() >= 100
+
+
+def test_every_declared_symbol_is_exported():
+    L = tq.lib()
+    names = header_functions()
+    assert "exl3_linear" in names and "exl3_moe_grouped" in names and "exl3_decode_tile" in names
+    for name in names:
+        assert hasattr(L, name), f"{name} declared in exl3.h but not exported"
+
+
+def _err(L):
+    return L.exl3_last_error().decode()
+
+
+def test_decode_tile_argument_errors():
+    L = tq.lib()
+    assert L.exl3_decode_tile(None, 128, 128, 4, 2, 0, 8, 0, 8, FAKE, 128, None) == tq.EXL3_ERR_ARG
+    assert "trellis" in _err(L)
+    assert L.exl3_decode_tile(FAKE_MIS, 128, 128, 4, 2, 0, 8, 0, 8, FAKE, 128, None) == tq.EXL3_ERR_ARG
+    assert L.exl3_decode_tile(FAKE, 128, 128, 9, 2, 0, 8, 0, 8, FAKE, 128, None) == tq.EXL3_ERR_BITS
+    assert L.exl3_decode_tile(FAKE, 128, 128, 0, 2, 0, 8, 0, 8, FAKE, 128, None) == tq.EXL3_ERR_BITS
+    assert L.exl3_decode_tile(FAKE, 128, 128, 4, 1, 0, 8, 0, 8, FAKE, 128, None) == tq.EXL3_ERR_CODEBOOK
+    assert "refusing" in _err(L)
+    assert L.exl3_decode_tile(FAKE, 128, 128, 4, 3, 0, 8, 0, 8, FAKE, 128, None) == tq.EXL3_ERR_CODEBOOK
+    assert L.exl3_decode_tile(FAKE, 128, 128, 4, 7, 0, 8, 0, 8, FAKE, 128, None) == tq.EXL3_ERR_CODEBOOK
+    assert L.exl3_decode_tile(FAKE, 120, 128, 4, 2, 0, 7, 0, 8, FAKE, 128, None) == tq.EXL3_ERR_SHAPE
+    assert L.exl3_decode_tile(FAKE, 128, 128, 4, 2, 4, 8, 0, 8, FAKE, 128, None) == tq.EXL3_ERR_SHAPE
+    assert L.exl3_decode_tile(FAKE, 128, 128, 4, 2, 0, 8, 0, 8, FAKE, 100, None) == tq.EXL3_ERR_SHAPE
+    assert L.exl3_decode_tile(FAKE, 128, 128, 4, 2, 0, 8, 0, 8, FAKE, 132, None) == tq.EXL3_ERR_SHAPE
+
+
+def test_linear_argument_errors():
+    L = tq.lib()
+    ws = 1 << 20
+    args = lambda **kw: [kw.get("x", FAKE), kw.get("M", 1), kw.get("k", 256), kw.get("n", 256),
+                         kw.get("t", FAKE), kw.get("suh", FAKE), kw.get("svh", FAKE), kw.get("K", 4),
+                         kw.get("cb", 2), kw.get("y", FAKE), kw.get("od", 0), kw.get("ws", FAKE),
+                         kw.get("wsb", ws), None]
+    assert L.exl3_linear(*args(x=None)) == tq.EXL3_ERR_ARG
+    assert L.exl3_linear(*args(svh=FAKE_MIS)) == tq.EXL3_ERR_ARG
+    assert L.exl3_linear(*args(K=9)) == tq.EXL3_ERR_BITS
+    assert L.exl3_linear(*args(cb=1)) == tq.EXL3_ERR_CODEBOOK
+    assert L.exl3_linear(*args(M=0)) == tq.EXL3_ERR_SHAPE
+    assert L.exl3_linear(*args(k=200)) == tq.EXL3_ERR_SHAPE
+    assert L.exl3_linear(*args(n=64)) == tq.EXL3_ERR_SHAPE
+    assert L.exl3_linear(*args(od=5)) == tq.EXL3_ERR_ARG
+    assert L.exl3_linear(*args(ws=None)) == tq.EXL3_ERR_WORKSPACE
+    assert L.exl3_linear(*args(wsb=16)) == tq.EXL3_ERR_WORKSPACE
+    assert "workspace" in _err(L)
+
+
+def test_input_rht_argument_errors():
+    L = tq.lib()
+    assert L.exl3_input_rht(FAKE, 1, 100, FAKE, FAKE, 1, None) == tq.EXL3_ERR_SHAPE
+    assert L.exl3_input_rht(FAKE, 0, 128, FAKE, FAKE, 1, None) == tq.EXL3_ERR_SHAPE
+    assert L.exl3_input_rht(FAKE, 1, 128, None, FAKE, 1, None) == tq.EXL3_ERR_ARG
+    assert L.exl3_input_rht(FAKE, 1, 128, FAKE, FAKE, 3, None) == tq.EXL3_ERR_ARG
+
+
+@pytest.mark.parametrize("M,k,n,K", [(1, 5120, 17408, 4), (4, 5120, 5120, 4), (4096, 5120, 17408, 4),
+                                     (1, 128, 128, 1), (64, 4096, 4096, 7)])
+def test_workspace_sizes(M, k, n, K):
+    size = tq.exl3_linear_workspace_size(M, k, n, K)
+    assert size >= 256 and size % 256 == 0
+    assert tq.exl3_linear_workspace_size(M, k + 1, n, K) == 0
+    assert tq.exl3_linear_workspace_size(M, k, n, 0) == 0

@@ -1,0 +1,182 @@
+"""GPU parity of libexl3 against the CPU oracle: dequantisation, the input
+transform and the linear at M = 1 and above (through the C ABI).
+
+Dequantised weights and the fp32 input transform must match bit for bit;
+linear outputs must meet the tolerance in tests/gpu_util.py.  Inputs are the
+seeded synthetic workloads of exl3_synth (the shapes of the pages' dense 27B
+family: "exl3xpu" README; mixed widths: tracker #832).
+"""
+import numpy as np
+import pytest
+import torch
+
+import exl3_synth as synth
+import oracle
+import trellis_quantized_gb300 as tq
+from gpu_util import assert_close, dev, host
+
+pytestmark = pytest.mark.gpu
+
+BOUND = 3.453125
+
+
+# ------------------------------------------------------------- dequantise --
+
+@pytest.mark.parametrize("K", range(1, 9))
+def test_decode_tile_bit_exact(K):
+    case = synth.linear_case(10, K, 1, 256, 384, K)
+    ref = oracle.reconstruct(case.trellis, 256, 384, K).view(np.uint16)
+    got = host(tq.exl3_decode_tile(dev(case.trellis), 256, 384, K)).view(np.uint16)
+    assert np.array_equal(got, ref)
+
+
+def test_decode_tile_subrange_with_padded_rows():
+    K, k, n = 3, 256, 512
+    case = synth.linear_case(10, 20, 1, k, n, K)
+    ref = oracle.reconstruct(case.trellis, k, n, K).view(np.uint16)
+    tk0, tkc, tn0, tnc, ld = 3, 5, 7, 9, 160
+    out = torch.full((16 * tkc, ld), 7.0, dtype=torch.float16, device="cuda")
+    tq.exl3_decode_tile(dev(case.trellis), k, n, K, tk0=tk0, tk_cnt=tkc, tn0=tn0, tn_cnt=tnc, w_out=out, ld=ld)
+    got = host(out).view(np.uint16)
+    assert np.array_equal(got[:, :16 * tnc], ref[16 * tk0:16 * (tk0 + tkc), 16 * tn0:16 * (tn0 + tnc)])
+    assert np.all(host(out)[:, 16 * tnc:] == 7.0)      # padding untouched
+
+
+def _all_states_trellis():
+    """K = 8 tiles whose byte streams make every (lo, hi) byte pair a state.
+
+    For K = 8, state p is stream bytes p and p+1.  Tile (hi, half) holds bytes
+    b[2i] = 128 * half + i and b[2i+1] = hi, so its even states are
+    (128 * half + i) | hi << 8: 512 tiles cover all 65536 states."""
+    tiles = np.zeros((16, 32, 128), dtype=np.uint16)   # k = 256, n = 512: 512 tiles
+    for t in range(512):
+        hi, half = t >> 1, t & 1
+        b = np.zeros(256, dtype=np.uint8)
+        b[0::2] = 128 * half + np.arange(128)
+        b[1::2] = hi
+        tiles[t // 32, t % 32] = b.view(np.uint16)
+    return tiles
+
+
+def test_codebook_exhaustive_all_65536_states():
+    t = _all_states_trellis()
+    covered = set()
+    for tk in range(16):
+        for tn in range(32):
+            covered.update(oracle.tile_states(t[tk, tn], 8)[0::2].tolist())
+    assert len(covered) == 65536
+    ref = oracle.reconstruct(t, 256, 512, 8).view(np.uint16)
+    got = host(tq.exl3_decode_tile(dev(t), 256, 512, 8)).view(np.uint16)
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("K", [1, 5, 8])
+def test_decode_special_trellises(K):
+    zero = np.zeros((8, 8, 16 * K), dtype=np.uint16)
+    got = host(tq.exl3_decode_tile(dev(zero), 128, 128, K)).astype(np.float64)
+    assert np.all(got == -BOUND)
+    ones = np.full((8, 8, 16 * K), 0xFFFF, dtype=np.uint16)
+    got = host(tq.exl3_decode_tile(dev(ones), 128, 128, K)).view(np.uint16)
+    assert np.all(got == oracle.mul1_value_bits(0xFFFF))
+
+
+# --------------------------------------------------------------- transform --
+
+def test_input_rht_bit_exact():
+    case = synth.linear_case(11, 0, 7, 1024, 128, 2, outlier_rows=0.3)
+    ref = oracle.rht_in_f32(case.x, case.suh)
+    x, suh = dev(case.x), dev(case.suh)
+    got32 = host(tq.exl3_input_rht(x, suh, tq.EXL3_OUT_F32))
+    assert np.array_equal(got32.view(np.uint32), ref.view(np.uint32))
+    got16 = host(tq.exl3_input_rht(x, suh, tq.EXL3_OUT_F16))
+    assert np.array_equal(got16.view(np.uint16), ref.astype(np.float16).view(np.uint16))
+
+
+# ------------------------------------------------------------------ linear --
+
+def _run(case, out_dtype):
+    y = tq.exl3_linear(dev(case.x), dev(case.trellis), dev(case.suh), dev(case.svh), case.K,
+                       out_dtype=out_dtype)
+    return host(y).astype(np.float64)
+
+
+def _check_case(case, ref=None, rows=None):
+    if ref is None:
+        x = case.x if rows is None else case.x[rows]
+        ref = oracle.linear(x, case.trellis, case.suh, case.svh, case.K)
+    for od in (tq.EXL3_OUT_F16, tq.EXL3_OUT_F32):
+        y = _run(case, od)
+        if rows is not None:
+            y = y[rows]
+        assert_close(y, ref, f"{case.name} out={'f32' if od else 'f16'}")
+
+
+def test_linear_config1():
+    _check_case(synth.config1())
+
+
+@pytest.mark.parametrize("n", synth.CONFIG2_N)
+def test_linear_config2_m1(n):
+    _check_case(synth.config2(n, 1))
+
+
+@pytest.mark.parametrize("K", synth.CONFIG3_K)
+def test_linear_config3_m1(K):
+    _check_case(synth.config3(K, 1))
+
+
+@pytest.mark.parametrize("K", range(1, 9))
+@pytest.mark.parametrize("k,n", [(128, 128), (384, 384), (1152, 640)])
+def test_linear_m1_ragged_shapes(K, k, n):
+    """Smallest shape (one block), column counts that leave a CTA half empty,
+    and k-ranges that are not a power of two."""
+    _check_case(synth.linear_case(12, K * 10 + n // 128, 1, k, n, K))
+
+
+@pytest.mark.parametrize("M", [2, 4, 16])
+def test_linear_config2_small_m(M):
+    _check_case(synth.config2(5120, M))
+
+
+@pytest.mark.parametrize("K,M", [(2, 8), (5, 8), (8, 64), (3, 64)])
+def test_linear_config3_small_m(K, M):
+    _check_case(synth.config3(K, M))
+
+
+def test_linear_prefill_config4_sampled_rows():
+    """Full M = 4096 on the GPU; the oracle evaluates a seeded sample of rows
+    (rows are independent) including rows of every outlier channel."""
+    case = synth.config4()
+    rng = np.random.default_rng(4)
+    rows = np.unique(np.concatenate([[0, 1, 4095], rng.choice(4096, 13, replace=False)]))
+    W = oracle.reconstruct(case.trellis, case.k, case.n, case.K)
+    ref = oracle.linear_w(case.x[rows], W, case.suh, case.svh)
+    _check_case(case, ref=ref, rows=rows)
+
+
+def test_linear_odd_m_and_zero_rows():
+    case = synth.linear_case(13, 0, 37, 640, 384, 6)
+    case.x[5] = 0
+    _check_case(case)
+
+
+def test_linear_deterministic_and_workspace_clean():
+    case = synth.config2(17408, 1)
+    x, t, suh, svh = dev(case.x), dev(case.trellis), dev(case.suh), dev(case.svh)
+    need = tq.exl3_linear_workspace_size(1, case.k, case.n, case.K)
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    y1 = tq.exl3_linear(x, t, suh, svh, 4, workspace_buf=ws).clone()
+    y2 = tq.exl3_linear(x, t, suh, svh, 4, workspace_buf=ws).clone()
+    assert torch.equal(y1, y2)
+    assert tq.exl3_check_device_error(ws) == 0
+    # the arrival counters (right after the 256-byte control block) are back at zero
+    counters = host(ws[256:256 + 4 * (case.n // 128)]).view(np.int32)
+    assert np.all(counters == 0)
+
+
+def test_linear_rejects_small_workspace():
+    case = synth.linear_case(14, 0, 1, 256, 256, 4)
+    ws = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(tq.Exl3Error) as e:
+        tq.exl3_linear(dev(case.x), dev(case.trellis), dev(case.suh), dev(case.svh), 4, workspace_buf=ws)
+    assert e.value.code == tq.EXL3_ERR_WORKSPACE

@@ -1,0 +1,183 @@
+"""trellis_quantized_gb300 -- Python binding of libexl3 (the EXL3 trellis linear on GB300).
+
+A thin ctypes layer over the C ABI declared in include/exl3.h: every function
+here has the name of the C entry point it wraps and only marshals torch
+tensors into device pointers, sizes and the current CUDA stream.  All
+arithmetic runs in the library's CUDA kernels; there is no CPU path.  If
+libexl3.so cannot be built or loaded, importing a function raises.
+
+Tensors: fp16 data is passed as torch.float16 (or any 2-byte dtype holding
+binary16 bits), trellis words as a 2-byte integer tensor (torch.int16 or
+torch.uint16) shaped [k/16, n/16, 16K], all contiguous on the same CUDA
+device.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+import torch
+
+from . import _build
+
+EXL3_OK = 0
+EXL3_ERR_ARG = 1
+EXL3_ERR_SHAPE = 2
+EXL3_ERR_BITS = 3
+EXL3_ERR_CODEBOOK = 4
+EXL3_ERR_WORKSPACE = 5
+EXL3_ERR_CUDA = 6
+EXL3_ERR_DEVICE = 7
+
+EXL3_CB_MCG = 1
+EXL3_CB_MUL1 = 2
+EXL3_CB_3INST = 3
+EXL3_OUT_F16 = 0
+EXL3_OUT_F32 = 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+class Exl3Error(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"libexl3 error {code}: {msg}")
+        self.code = code
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """Load libexl3.so (building it first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        P, I, Z, L64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_int64
+        L.exl3_last_error.restype = ctypes.c_char_p
+        L.exl3_version.restype = I
+        L.exl3_workspace_clear.argtypes = [P, Z, P]
+        L.exl3_check_device_error.argtypes = [P, Z, P, ctypes.POINTER(I)]
+        L.exl3_decode_tile.argtypes = [P, I, I, I, I, I, I, I, I, P, L64, P]
+        L.exl3_input_rht.argtypes = [P, I, I, P, P, I, P]
+        L.exl3_linear_workspace_size.argtypes = [I, I, I, I]
+        L.exl3_linear_workspace_size.restype = Z
+        L.exl3_linear.argtypes = [P, I, I, I, P, P, P, I, I, P, I, P, Z, P]
+        L.exl3_linear_int8_workspace_size.argtypes = [I, I, I, I]
+        L.exl3_linear_int8_workspace_size.restype = Z
+        L.exl3_linear_int8.argtypes = [P, I, I, I, P, P, P, I, I, ctypes.c_float, P, P, P, P, P, Z, P]
+        L.exl3_moe_workspace_size.argtypes = [I, I, I, P, P]
+        L.exl3_moe_workspace_size.restype = Z
+        L.exl3_moe_grouped.argtypes = [P, I, I, P, P, I, I, P, P, P, I, P, Z, P]
+        _lib = L
+        return L
+
+
+def _check(rc: int):
+    if rc != EXL3_OK:
+        raise Exl3Error(rc, lib().exl3_last_error().decode())
+
+
+def _ptr(t, name: str, itemsize: int | None = None):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if itemsize is not None and t.element_size() != itemsize:
+        raise TypeError(f"{name} must have {itemsize}-byte elements, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+_ws_cache: dict = {}
+
+
+def workspace(nbytes: int, device=None, stream=None) -> torch.Tensor:
+    """A zero-initialised workspace of at least nbytes, cached per (device, stream).
+
+    Every libexl3 call leaves its counters at zero again, so one cleared
+    workspace serves any number of calls made in stream order."""
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    key = (dev.index, s.cuda_stream)
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+        exl3_workspace_clear(buf, stream=s)
+        _ws_cache[key] = buf
+    return buf
+
+
+# ------------------------------------------------------------------ entry points
+
+def exl3_version() -> int:
+    return lib().exl3_version()
+
+
+def exl3_workspace_clear(ws: torch.Tensor, stream=None):
+    _check(lib().exl3_workspace_clear(_ptr(ws, "workspace"), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def exl3_check_device_error(ws: torch.Tensor, stream=None) -> int:
+    err = ctypes.c_int(0)
+    _check(lib().exl3_check_device_error(_ptr(ws, "workspace"), ws.numel() * ws.element_size(),
+                                         _stream(stream), ctypes.byref(err)))
+    return err.value
+
+
+def exl3_decode_tile(trellis, k: int, n: int, K: int, codebook: int = EXL3_CB_MUL1, tk0: int = 0,
+                     tk_cnt: int | None = None, tn0: int = 0, tn_cnt: int | None = None,
+                     w_out=None, ld: int | None = None, stream=None) -> torch.Tensor:
+    """Dequantised fp16 weights of a tile range (the whole tensor by default)."""
+    tk_cnt = k // 16 - tk0 if tk_cnt is None else tk_cnt
+    tn_cnt = n // 16 - tn0 if tn_cnt is None else tn_cnt
+    if w_out is None:
+        ld = 16 * tn_cnt if ld is None else ld
+        w_out = torch.empty((16 * tk_cnt, ld), dtype=torch.float16, device=trellis.device)
+    elif ld is None:
+        ld = w_out.shape[-1]
+    _check(lib().exl3_decode_tile(_ptr(trellis, "trellis", 2), k, n, K, codebook, tk0, tk_cnt, tn0, tn_cnt,
+                                  _ptr(w_out, "w_out", 2), ld, _stream(stream)))
+    return w_out
+
+
+def exl3_input_rht(x, suh, out_dtype: int = EXL3_OUT_F32, out=None, stream=None) -> torch.Tensor:
+    M, k = x.shape
+    if out is None:
+        out = torch.empty((M, k), dtype=torch.float32 if out_dtype == EXL3_OUT_F32 else torch.float16,
+                          device=x.device)
+    _check(lib().exl3_input_rht(_ptr(x, "x", 2), M, k, _ptr(suh, "suh", 2), _ptr(out, "out"), out_dtype,
+                                _stream(stream)))
+    return out
+
+
+def exl3_linear_workspace_size(M: int, k: int, n: int, K: int) -> int:
+    return lib().exl3_linear_workspace_size(M, k, n, K)
+
+
+def exl3_linear(x, trellis, suh, svh, K: int, codebook: int = EXL3_CB_MUL1, out_dtype: int = EXL3_OUT_F16,
+                y=None, workspace_buf=None, stream=None) -> torch.Tensor:
+    """y = RHT_out(RHT_in(x . suh) @ W) . svh for x [M, k] fp16."""
+    M, k = x.shape
+    n = trellis.shape[1] * 16
+    if y is None:
+        y = torch.empty((M, n), dtype=torch.float32 if out_dtype == EXL3_OUT_F32 else torch.float16,
+                        device=x.device)
+    need = exl3_linear_workspace_size(M, k, n, K)
+    ws = workspace_buf if workspace_buf is not None else workspace(need, x.device, stream)
+    _check(lib().exl3_linear(_ptr(x, "x", 2), M, k, n, _ptr(trellis, "trellis", 2), _ptr(suh, "suh", 2),
+                             _ptr(svh, "svh", 2), K, codebook, _ptr(y, "y"), out_dtype, _ptr(ws, "workspace"),
+                             ws.numel() * ws.element_size(), _stream(stream)))
+    return y

@@ -1,0 +1,270 @@
+// api.cu -- the C ABI of libexl3 (declared in include/exl3.h): argument
+// validation, workspace layout and kernel dispatch.  No entry point
+// allocates device memory or synchronises the caller's stream (except the
+// test helper exl3_check_device_error).
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "exl3_common.cuh"
+
+// ---- kernels (other translation units)
+cudaError_t exl3_launch_decode_tile(const uint16_t *trellis, int n, int K, int tk0, int tk_cnt, int tn0,
+                                    int tn_cnt, uint16_t *w_out, int64_t ld, cudaStream_t s);
+cudaError_t exl3_launch_reconstruct_t(const uint16_t *trellis, int k, int n, int K, uint16_t *wt,
+                                      cudaStream_t s);
+cudaError_t exl3_launch_input_rht(const uint16_t *x, int M, int k, const uint16_t *suh, void *out,
+                                  bool f32out, cudaStream_t s);
+cudaError_t exl3_launch_output_rht(const float *yp, float pre, const uint16_t *svh, int M, int n, void *y,
+                                   bool f32out, cudaStream_t s);
+cudaError_t exl3_launch_gemv_m1(const uint16_t *x, const uint16_t *trellis, const uint16_t *suh,
+                                const uint16_t *svh, int k, int n, int K, void *y, bool f32out,
+                                float *partials, int *counters, int *err, int splits, cudaStream_t s);
+int exl3_gemv_cta_cols(int K);
+int exl3_gemv_splits(int k, int n, int K, int target_ctas);
+cudaError_t exl3_launch_gemm_mma(const uint16_t *xh, const uint16_t *wt, float *yp, int M, int n, int k,
+                                 cudaStream_t s);
+
+// ---------------------------------------------------------------- errors --
+
+static thread_local std::string g_last_error;
+
+int exl3_fail(int code, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int exl3_cuda_check(cudaError_t e, const char *what) {
+  if (e == cudaSuccess) return EXL3_OK;
+  return exl3_fail(EXL3_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+#define EXL3_TRY(expr)            \
+  do {                            \
+    int _rc = (expr);             \
+    if (_rc != EXL3_OK) return _rc; \
+  } while (0)
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr size_t kCtrlBytes = 256;   // device error word and reserved control words
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int sm_count() {
+  static int cached = 0;
+  if (cached) return cached;
+  int dev = 0, v = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+    cached = v;
+  else {
+    cudaGetLastError();
+    return 152;
+  }
+  return cached;
+}
+
+int check_ptr(const void *p, const char *name, bool required = true) {
+  if (!p) return required ? exl3_fail(EXL3_ERR_ARG, "%s is NULL", name) : EXL3_OK;
+  if (!aligned16(p)) return exl3_fail(EXL3_ERR_ARG, "%s is not 16-byte aligned", name);
+  return EXL3_OK;
+}
+
+int check_bits_codebook(int K, int codebook) {
+  if (codebook == EXL3_CB_MCG || codebook == EXL3_CB_3INST)
+    return exl3_fail(EXL3_ERR_CODEBOOK,
+                     "codebook %d is not implemented (only mul1 = %d); refusing rather than guessing",
+                     codebook, EXL3_CB_MUL1);
+  if (codebook != EXL3_CB_MUL1) return exl3_fail(EXL3_ERR_CODEBOOK, "unknown codebook id %d", codebook);
+  if (K < 1 || K > 8) return exl3_fail(EXL3_ERR_BITS, "K = %d outside 1..8", K);
+  return EXL3_OK;
+}
+
+int check_linear_shape(int M, int k, int n) {
+  if (M < 1) return exl3_fail(EXL3_ERR_SHAPE, "M = %d < 1", M);
+  if (k <= 0 || n <= 0 || k % 128 || n % 128)
+    return exl3_fail(EXL3_ERR_SHAPE, "k = %d and n = %d must be positive multiples of 128", k, n);
+  if ((int64_t)M * k > INT32_MAX || (int64_t)M * n > INT32_MAX || (int64_t)k * n > ((int64_t)1 << 40))
+    return exl3_fail(EXL3_ERR_SHAPE, "shape too large");
+  return EXL3_OK;
+}
+
+// ---- exl3_linear workspace layout
+struct LinearWs {
+  size_t ctrl = 0, counters = 0, partials = 0, xh = 0, wt = 0, yp = 0, total = 0;
+  int splits = 1;
+};
+
+LinearWs linear_ws(int M, int k, int n, int K) {
+  LinearWs w;
+  size_t off = kCtrlBytes;
+  if (M == 1) {
+    w.splits = exl3_gemv_splits(k, n, K, 4 * sm_count());
+    const int colblocks = (n + exl3_gemv_cta_cols(K) - 1) / exl3_gemv_cta_cols(K);
+    w.counters = off;
+    off = align_up(off + sizeof(int) * (size_t)colblocks);
+    w.partials = off;
+    off = align_up(off + (w.splits > 1 ? sizeof(float) * (size_t)w.splits * n : 0));
+  } else {
+    w.xh = off;
+    off = align_up(off + sizeof(uint16_t) * (size_t)M * k);
+    w.wt = off;
+    off = align_up(off + sizeof(uint16_t) * (size_t)k * n);
+    w.yp = off;
+    off = align_up(off + sizeof(float) * (size_t)M * n);
+  }
+  w.total = off;
+  return w;
+}
+
+int check_workspace(const void *ws, size_t have, size_t need) {
+  if (need == 0) return EXL3_OK;
+  if (!ws) return exl3_fail(EXL3_ERR_WORKSPACE, "workspace is NULL (%zu bytes needed)", need);
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0)
+    return exl3_fail(EXL3_ERR_WORKSPACE, "workspace must be %zu-byte aligned", kAlign);
+  if (have < need) return exl3_fail(EXL3_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", have, need);
+  return EXL3_OK;
+}
+
+template <typename T>
+T *at(void *base, size_t off) {
+  return reinterpret_cast<T *>(static_cast<char *>(base) + off);
+}
+
+}  // namespace
+
+// ================================================================== C ABI ==
+
+extern "C" {
+
+const char *exl3_last_error(void) { return g_last_error.c_str(); }
+
+int exl3_version(void) { return 100; }
+
+int exl3_workspace_clear(void *workspace, size_t ws_bytes, exl3_stream_t stream) {
+  g_last_error.clear();
+  if (!workspace || ws_bytes == 0) return EXL3_OK;
+  return exl3_cuda_check(cudaMemsetAsync(workspace, 0, ws_bytes, stream), "cudaMemsetAsync(workspace)");
+}
+
+int exl3_check_device_error(void *workspace, size_t ws_bytes, exl3_stream_t stream, int *err_out) {
+  g_last_error.clear();
+  if (!err_out) return exl3_fail(EXL3_ERR_ARG, "err_out is NULL");
+  *err_out = 0;
+  EXL3_TRY(check_workspace(workspace, ws_bytes, kCtrlBytes));
+  EXL3_TRY(exl3_cuda_check(cudaStreamSynchronize(stream), "cudaStreamSynchronize"));
+  int v = 0;
+  EXL3_TRY(exl3_cuda_check(cudaMemcpy(&v, workspace, sizeof v, cudaMemcpyDeviceToHost), "read error word"));
+  EXL3_TRY(exl3_cuda_check(cudaMemset(workspace, 0, sizeof v), "clear error word"));
+  *err_out = v;
+  return EXL3_OK;
+}
+
+int exl3_decode_tile(const uint16_t *trellis, int k, int n, int K, int codebook, int tk0, int tk_cnt,
+                     int tn0, int tn_cnt, uint16_t *w_out, int64_t ld, exl3_stream_t stream) {
+  g_last_error.clear();
+  EXL3_TRY(check_ptr(trellis, "trellis"));
+  EXL3_TRY(check_ptr(w_out, "w_out"));
+  EXL3_TRY(check_bits_codebook(K, codebook));
+  if (k <= 0 || n <= 0 || k % 16 || n % 16)
+    return exl3_fail(EXL3_ERR_SHAPE, "k = %d, n = %d must be positive multiples of 16", k, n);
+  if (tk0 < 0 || tn0 < 0 || tk_cnt < 0 || tn_cnt < 0 || tk0 + tk_cnt > k / 16 || tn0 + tn_cnt > n / 16)
+    return exl3_fail(EXL3_ERR_SHAPE, "tile range [%d,+%d) x [%d,+%d) outside the %d x %d tile grid", tk0,
+                     tk_cnt, tn0, tn_cnt, k / 16, n / 16);
+  if (ld < 16LL * tn_cnt || ld % 8)
+    return exl3_fail(EXL3_ERR_SHAPE, "ld = %lld must be >= 16 * tn_cnt and a multiple of 8", (long long)ld);
+  if (tk_cnt == 0 || tn_cnt == 0) return EXL3_OK;
+  if (tk_cnt * 2 > 65535) return exl3_fail(EXL3_ERR_SHAPE, "tk_cnt = %d too large for one call", tk_cnt);
+  return exl3_cuda_check(
+      exl3_launch_decode_tile(trellis, n, K, tk0, tk_cnt, tn0, tn_cnt, w_out, ld, stream), "decode_tile launch");
+}
+
+int exl3_input_rht(const uint16_t *x, int M, int k, const uint16_t *suh, void *out, int out_dtype,
+                   exl3_stream_t stream) {
+  g_last_error.clear();
+  EXL3_TRY(check_ptr(x, "x"));
+  EXL3_TRY(check_ptr(suh, "suh"));
+  EXL3_TRY(check_ptr(out, "out"));
+  if (out_dtype != EXL3_OUT_F16 && out_dtype != EXL3_OUT_F32)
+    return exl3_fail(EXL3_ERR_ARG, "out_dtype %d invalid", out_dtype);
+  if (M < 1 || k <= 0 || k % 128) return exl3_fail(EXL3_ERR_SHAPE, "M = %d, k = %d (k multiple of 128)", M, k);
+  return exl3_cuda_check(exl3_launch_input_rht(x, M, k, suh, out, out_dtype == EXL3_OUT_F32, stream),
+                         "input_rht launch");
+}
+
+size_t exl3_linear_workspace_size(int M, int k, int n, int K) {
+  if (M < 1 || k <= 0 || n <= 0 || k % 128 || n % 128 || K < 1 || K > 8) return 0;
+  return linear_ws(M, k, n, K).total;
+}
+
+int exl3_linear(const uint16_t *x, int M, int k, int n, const uint16_t *trellis, const uint16_t *suh,
+                const uint16_t *svh, int K, int codebook, void *y, int out_dtype, void *workspace,
+                size_t ws_bytes, exl3_stream_t stream) {
+  g_last_error.clear();
+  EXL3_TRY(check_ptr(x, "x"));
+  EXL3_TRY(check_ptr(trellis, "trellis"));
+  EXL3_TRY(check_ptr(suh, "suh"));
+  EXL3_TRY(check_ptr(svh, "svh"));
+  EXL3_TRY(check_ptr(y, "y"));
+  EXL3_TRY(check_bits_codebook(K, codebook));
+  EXL3_TRY(check_linear_shape(M, k, n));
+  if (out_dtype != EXL3_OUT_F16 && out_dtype != EXL3_OUT_F32)
+    return exl3_fail(EXL3_ERR_ARG, "out_dtype %d invalid", out_dtype);
+  const LinearWs L = linear_ws(M, k, n, K);
+  EXL3_TRY(check_workspace(workspace, ws_bytes, L.total));
+  const bool f32 = out_dtype == EXL3_OUT_F32;
+  int *err = at<int>(workspace, L.ctrl);
+  if (M == 1) {
+    return exl3_cuda_check(exl3_launch_gemv_m1(x, trellis, suh, svh, k, n, K, y, f32, at<float>(workspace, L.partials),
+                                               at<int>(workspace, L.counters), err, L.splits, stream),
+                           "gemv launch");
+  }
+  uint16_t *xh = at<uint16_t>(workspace, L.xh);
+  uint16_t *wt = at<uint16_t>(workspace, L.wt);
+  float *yp = at<float>(workspace, L.yp);
+  EXL3_TRY(exl3_cuda_check(exl3_launch_input_rht(x, M, k, suh, xh, false, stream), "input_rht launch"));
+  EXL3_TRY(exl3_cuda_check(exl3_launch_reconstruct_t(trellis, k, n, K, wt, stream), "reconstruct launch"));
+  EXL3_TRY(exl3_cuda_check(exl3_launch_gemm_mma(xh, wt, yp, M, n, k, stream), "gemm launch"));
+  return exl3_cuda_check(exl3_launch_output_rht(yp, 1.0f, svh, M, n, y, f32, stream), "output_rht launch");
+}
+
+size_t exl3_linear_int8_workspace_size(int M, int k, int n, int K) {
+  (void)M; (void)k; (void)n; (void)K;
+  return 0;
+}
+
+int exl3_linear_int8(const uint16_t *x, int M, int k, int n, const uint16_t *trellis, const uint16_t *suh,
+                     const uint16_t *svh, int K, int codebook, float weight_scale, uint16_t *y, int8_t *xq_out,
+                     float *row_scale_out, int32_t *acc_out, void *workspace, size_t ws_bytes,
+                     exl3_stream_t stream) {
+  (void)x; (void)M; (void)k; (void)n; (void)trellis; (void)suh; (void)svh; (void)K; (void)codebook;
+  (void)weight_scale; (void)y; (void)xq_out; (void)row_scale_out; (void)acc_out; (void)workspace;
+  (void)ws_bytes; (void)stream;
+  return exl3_fail(EXL3_ERR_ARG, "exl3_linear_int8 is not available in this build");
+}
+
+size_t exl3_moe_workspace_size(int T, int topk, int E, const exl3_expert_proj *w13,
+                               const exl3_expert_proj *w2) {
+  (void)T; (void)topk; (void)E; (void)w13; (void)w2;
+  return 0;
+}
+
+int exl3_moe_grouped(const uint16_t *x, int T, int hidden, const int32_t *topk_ids, const float *topk_weights,
+                     int topk, int E, const exl3_expert_proj *w13, const exl3_expert_proj *w2, void *y,
+                     int out_dtype, void *workspace, size_t ws_bytes, exl3_stream_t stream) {
+  (void)x; (void)T; (void)hidden; (void)topk_ids; (void)topk_weights; (void)topk; (void)E; (void)w13;
+  (void)w2; (void)y; (void)out_dtype; (void)workspace; (void)ws_bytes; (void)stream;
+  return exl3_fail(EXL3_ERR_ARG, "exl3_moe_grouped is not available in this build");
+}
+
+}  // extern "C"

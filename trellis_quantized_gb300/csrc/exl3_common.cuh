@@ -1,0 +1,100 @@
+// exl3_common.cuh -- device helpers shared by the libexl3 kernels.
+//
+// Format facts used here (this library's reading of the pages; sources by
+// page title and section):
+//  * trellis tensor [k/16][n/16][16K] ("Bringing EXL3 Trellis Quantization to
+//    35B MoE on Intel Arc 140V", section 2.A); tile bit i = bit (i % 16) of
+//    word i / 16; weight p = 16 r + c of a tile takes the 16-bit window of
+//    stream bits p*K .. p*K + 15, wrapping around the tile's 256 K bits.
+//  * mul1 codebook bounded by 3.453125 ("exl3xpu" README, "Prefill: int8
+//    linears and oneDNN fused attention"): B(s) = byte sum of
+//    (s * 0x9E3779B1) mod 2^32 (one IMAD and one DP4A), value =
+//    fp16_RNE((B - 510) * 1775 * 2^-18).
+//  * block Hadamard in and out ("exl3xpu" README, "Layout"): Sylvester order,
+//    scale 2^-3.5 per side, butterfly stages 1, 2, ..., 64 of (a+b, a-b).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/exl3.h"
+
+namespace exl3 {
+
+constexpr uint32_t kMul1 = 0x9E3779B1u;      // the mul1 multiplier
+constexpr float kSigma = 0x1.bbcp-8f;        // 1775 * 2^-18, an fp16 value
+constexpr float kRhtScale = 0x1.6a09e6p-4f;  // fp32 nearest 2^-3.5
+constexpr float kMagic = 8388608.0f;         // 2^23: float bits 0x4B000000
+constexpr float kBsumBias = 8389118.0f;      // 2^23 + 510
+
+// Device error word bits (workspace offset 0).
+constexpr int kErrDirtyCounter = 1;   // arrival counter found above its target
+constexpr int kErrExpertId = 2;       // routed expert id outside [0, E)
+constexpr int kErrBounds = 4;         // an index check failed
+
+// ---------------------------------------------------------------- codebook --
+
+// Byte sum B(s) of the mul1 hash of a 16-bit state (s must be < 2^16).
+__device__ __forceinline__ uint32_t mul1_bsum(uint32_t s) {
+  return __dp4a(s * kMul1, 0x01010101u, 0u);
+}
+
+// Exact fp16 codebook value: (B - 510) * 1775 is an integer below 2^24, so
+// the fp32 product is exact and __float2half_rn rounds it once.
+__device__ __forceinline__ __half mul1_half(uint32_t s) {
+  return __float2half_rn((float)((int)mul1_bsum(s) - 510) * kSigma);
+}
+
+// (B - 510) as an exact fp32 value, via the DP4A accumulator seeded with the
+// bit pattern of 2^23: the result's bits are those of the float 2^23 + B.
+__device__ __forceinline__ float mul1_centered(uint32_t s) {
+  return __int_as_float((int)__dp4a(s * kMul1, 0x01010101u, 0x4B000000u)) - kBsumBias;
+}
+
+// 16-bit window starting at bit `sh` (0..31) of the 64-bit pair (hi:lo).
+__device__ __forceinline__ uint32_t window16(uint32_t lo, uint32_t hi, uint32_t sh) {
+  return __funnelshift_r(lo, hi, sh) & 0xFFFFu;
+}
+
+// ------------------------------------------------------------------ FWHT-128 --
+
+// 128-point Sylvester Hadamard over one warp, lane l holding elements
+// 4l .. 4l+3.  Same per-element operation order as the definition: stage h,
+// pair (i, i+h) -> (a+b, a-b) with a the lower index.  Stages 1 and 2 are in
+// registers, stages 4..64 exchange with lane l ^ (h / 4).
+__device__ __forceinline__ void fwht128_warp(float v[4], int lane) {
+  float a, b;
+  // h = 1: pairs (0,1), (2,3)
+  a = v[0]; b = v[1]; v[0] = a + b; v[1] = a - b;
+  a = v[2]; b = v[3]; v[2] = a + b; v[3] = a - b;
+  // h = 2: pairs (0,2), (1,3)
+  a = v[0]; b = v[2]; v[0] = a + b; v[2] = a - b;
+  a = v[1]; b = v[3]; v[1] = a + b; v[3] = a - b;
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float other = __shfl_xor_sync(0xffffffffu, v[j], m);
+      v[j] = upper ? (other - v[j]) : (v[j] + other);
+    }
+  }
+}
+
+// ------------------------------------------------------------ small helpers --
+
+__device__ __forceinline__ void set_device_error(int *err, int bit) {
+  if (err) atomicOr(err, bit);
+}
+
+__host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+__host__ __device__ constexpr int gcd_c(int a, int b) { return b == 0 ? a : gcd_c(b, a % b); }
+
+}  // namespace exl3
+
+// ------------------------------------------------------------ host helpers --
+// Defined in api.cu: thread-local error message and CUDA error capture.
+int exl3_fail(int code, const char *fmt, ...);
+int exl3_cuda_check(cudaError_t e, const char *what);

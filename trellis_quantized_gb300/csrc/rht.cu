@@ -1,0 +1,99 @@
+// rht.cu -- the randomized block Hadamard transforms on activations and
+// outputs ("Hadamard in/out", "exl3xpu" README, "Layout"; randomized Hadamard
+// transforms, "Bringing EXL3 Trellis Quantization to 35B MoE on Intel Arc
+// 140V", section 1).
+//
+// One warp transforms one aligned 128-element block held as 4 elements per
+// lane (fwht128_warp); input side x' = 2^-3.5 H (x . suh), output side
+// y = (2^-3.5 H (pre * y')) . svh.
+#include "exl3_common.cuh"
+
+namespace exl3 {
+
+// x [M][k] fp16 -> out [M][k] fp32 (OUT_F32) or fp16.  One warp per block.
+template <bool F32OUT>
+__global__ void __launch_bounds__(256) input_rht_kernel(const __half *__restrict__ x,
+                                                        const __half *__restrict__ suh, int M, int k,
+                                                        void *__restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const long wid = (long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int blocks = k >> 7;
+  if (wid >= (long)M * blocks) return;
+  const long row = wid / blocks;
+  const int col = (int)(wid % blocks) * 128 + lane * 4;
+  const uint2 xv = *reinterpret_cast<const uint2 *>(x + row * k + col);
+  const uint2 sv = *reinterpret_cast<const uint2 *>(suh + col);
+  const __half2 *xh = reinterpret_cast<const __half2 *>(&xv);
+  const __half2 *sh = reinterpret_cast<const __half2 *>(&sv);
+  float v[4];
+  v[0] = __low2float(xh[0]) * __low2float(sh[0]);   // exact: 11-bit x 11-bit significands
+  v[1] = __high2float(xh[0]) * __high2float(sh[0]);
+  v[2] = __low2float(xh[1]) * __low2float(sh[1]);
+  v[3] = __high2float(xh[1]) * __high2float(sh[1]);
+  fwht128_warp(v, lane);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) v[j] = __fmul_rn(v[j], kRhtScale);
+  if (F32OUT) {
+    *reinterpret_cast<float4 *>(static_cast<float *>(out) + row * k + col) =
+        make_float4(v[0], v[1], v[2], v[3]);
+  } else {
+    __half2 o[2] = {__floats2half2_rn(v[0], v[1]), __floats2half2_rn(v[2], v[3])};
+    *reinterpret_cast<uint2 *>(static_cast<__half *>(out) + row * k + col) =
+        *reinterpret_cast<uint2 *>(o);
+  }
+}
+
+// yp [M][n] fp32 (Hadamard domain, times `pre`) -> y [M][n] fp16 or fp32.
+template <bool F32OUT>
+__global__ void __launch_bounds__(256) output_rht_kernel(const float *__restrict__ yp, float pre,
+                                                         const __half *__restrict__ svh, int M, int n,
+                                                         void *__restrict__ y) {
+  const int lane = threadIdx.x & 31;
+  const long wid = (long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int blocks = n >> 7;
+  if (wid >= (long)M * blocks) return;
+  const long row = wid / blocks;
+  const int col = (int)(wid % blocks) * 128 + lane * 4;
+  const float4 a = *reinterpret_cast<const float4 *>(yp + row * n + col);
+  float v[4] = {a.x * pre, a.y * pre, a.z * pre, a.w * pre};
+  fwht128_warp(v, lane);
+  const uint2 sv = *reinterpret_cast<const uint2 *>(svh + col);
+  const __half2 *sh = reinterpret_cast<const __half2 *>(&sv);
+  v[0] = v[0] * kRhtScale * __low2float(sh[0]);
+  v[1] = v[1] * kRhtScale * __high2float(sh[0]);
+  v[2] = v[2] * kRhtScale * __low2float(sh[1]);
+  v[3] = v[3] * kRhtScale * __high2float(sh[1]);
+  if (F32OUT) {
+    *reinterpret_cast<float4 *>(static_cast<float *>(y) + row * n + col) = make_float4(v[0], v[1], v[2], v[3]);
+  } else {
+    __half2 o[2] = {__floats2half2_rn(v[0], v[1]), __floats2half2_rn(v[2], v[3])};
+    *reinterpret_cast<uint2 *>(static_cast<__half *>(y) + row * n + col) = *reinterpret_cast<uint2 *>(o);
+  }
+}
+
+}  // namespace exl3
+
+using namespace exl3;
+
+cudaError_t exl3_launch_input_rht(const uint16_t *x, int M, int k, const uint16_t *suh, void *out,
+                                  bool f32out, cudaStream_t s) {
+  const long warps = (long)M * (k / 128);
+  const unsigned grid = (unsigned)((warps + 7) / 8);
+  if (grid == 0) return cudaSuccess;
+  const __half *xh = reinterpret_cast<const __half *>(x);
+  const __half *sh = reinterpret_cast<const __half *>(suh);
+  if (f32out) input_rht_kernel<true><<<grid, 256, 0, s>>>(xh, sh, M, k, out);
+  else input_rht_kernel<false><<<grid, 256, 0, s>>>(xh, sh, M, k, out);
+  return cudaGetLastError();
+}
+
+cudaError_t exl3_launch_output_rht(const float *yp, float pre, const uint16_t *svh, int M, int n,
+                                   void *y, bool f32out, cudaStream_t s) {
+  const long warps = (long)M * (n / 128);
+  const unsigned grid = (unsigned)((warps + 7) / 8);
+  if (grid == 0) return cudaSuccess;
+  const __half *sh = reinterpret_cast<const __half *>(svh);
+  if (f32out) output_rht_kernel<true><<<grid, 256, 0, s>>>(yp, pre, sh, M, n, y);
+  else output_rht_kernel<false><<<grid, 256, 0, s>>>(yp, pre, sh, M, n, y);
+  return cudaGetLastError();
+}
