@@ -261,7 +261,7 @@ def bench_prefill(args, bf16_peak, src):
     tf = flops / (ms * 1e-3) / 1e12
     return {"workload": "M=4096 k=5120 n=17408 K=4 fp16 out", "ms": round(ms, 4), "tflops": round(tf, 1),
             "peak_tflops": bf16_peak, "peak_source": src + " bf16 sustained", "frac": round(tf / bf16_peak, 4),
-            "path": "reconstruct + mma.sync GEMM (interim)"}
+            "path": "input RHT + transposed reconstruct + tcgen05/TMEM GEMM with fused output RHT"}
 
 
 # ------------------------------------------------------------------------- oracle

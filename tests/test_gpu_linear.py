@@ -133,9 +133,15 @@ def test_linear_m1_ragged_shapes(K, k, n):
     _check_case(synth.linear_case(12, K * 10 + n // 128, 1, k, n, K))
 
 
-@pytest.mark.parametrize("M", [2, 4, 16])
+@pytest.mark.parametrize("M", [4, 16])
 def test_linear_config2_small_m(M):
     _check_case(synth.config2(5120, M))
+
+
+@pytest.mark.parametrize("M", [2, 3, 31, 32, 33])
+def test_linear_small_m_around_path_switch(M):
+    """M = 2, 3 and 31 take the mma.sync GEMM, 32 and 33 the tcgen05 GEMM."""
+    _check_case(synth.linear_case(15, M, M, 1024, 768, 4))
 
 
 @pytest.mark.parametrize("K,M", [(2, 8), (5, 8), (8, 64), (3, 64)])

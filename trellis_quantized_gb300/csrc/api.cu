@@ -23,6 +23,8 @@ cudaError_t exl3_launch_gemv_m1(const uint16_t *x, const uint16_t *trellis, cons
                                 float *partials, int *counters, int *err, int splits, cudaStream_t s);
 int exl3_gemv_cta_cols(int K);
 int exl3_gemv_splits(int k, int n, int K, int target_ctas);
+int exl3_launch_gemm_tc(const uint16_t *xh, const uint16_t *wt, int M, int n, int k, const uint16_t *svh,
+                        void *y, bool f32out, const float *row_scale, float pre, int *err, cudaStream_t s);
 cudaError_t exl3_launch_gemm_mma(const uint16_t *xh, const uint16_t *wt, float *yp, int M, int n, int k,
                                  cudaStream_t s);
 
@@ -55,6 +57,13 @@ namespace {
 
 constexpr size_t kAlign = 256;
 constexpr size_t kCtrlBytes = 256;   // device error word and reserved control words
+// Arrival counters live at one fixed place of every workspace, right after
+// the control block, so calls of any shape find them zero (each call resets
+// the counters it used).  Capacity bounds n / 128 of one call.
+constexpr size_t kMaxCounters = 8192;
+constexpr size_t kCounterOff = kCtrlBytes;
+constexpr size_t kDataOff = kCounterOff + kMaxCounters * sizeof(int);
+constexpr int kTcMinM = 32;          // M >= this: tcgen05 GEMM, else the mma.sync GEMM
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
@@ -94,7 +103,8 @@ int check_linear_shape(int M, int k, int n) {
   if (M < 1) return exl3_fail(EXL3_ERR_SHAPE, "M = %d < 1", M);
   if (k <= 0 || n <= 0 || k % 128 || n % 128)
     return exl3_fail(EXL3_ERR_SHAPE, "k = %d and n = %d must be positive multiples of 128", k, n);
-  if ((int64_t)M * k > INT32_MAX || (int64_t)M * n > INT32_MAX || (int64_t)k * n > ((int64_t)1 << 40))
+  if ((int64_t)M * k > INT32_MAX || (int64_t)M * n > INT32_MAX || (int64_t)k * n > ((int64_t)1 << 40) ||
+      (size_t)(n / 128) > kMaxCounters)
     return exl3_fail(EXL3_ERR_SHAPE, "shape too large");
   return EXL3_OK;
 }
@@ -107,12 +117,10 @@ struct LinearWs {
 
 LinearWs linear_ws(int M, int k, int n, int K) {
   LinearWs w;
-  size_t off = kCtrlBytes;
+  size_t off = kDataOff;
+  w.counters = kCounterOff;
   if (M == 1) {
     w.splits = exl3_gemv_splits(k, n, K, 4 * sm_count());
-    const int colblocks = (n + exl3_gemv_cta_cols(K) - 1) / exl3_gemv_cta_cols(K);
-    w.counters = off;
-    off = align_up(off + sizeof(int) * (size_t)colblocks);
     w.partials = off;
     off = align_up(off + (w.splits > 1 ? sizeof(float) * (size_t)w.splits * n : 0));
   } else {
@@ -120,8 +128,10 @@ LinearWs linear_ws(int M, int k, int n, int K) {
     off = align_up(off + sizeof(uint16_t) * (size_t)M * k);
     w.wt = off;
     off = align_up(off + sizeof(uint16_t) * (size_t)k * n);
-    w.yp = off;
-    off = align_up(off + sizeof(float) * (size_t)M * n);
+    if (M < kTcMinM) {
+      w.yp = off;
+      off = align_up(off + sizeof(float) * (size_t)M * n);
+    }
   }
   w.total = off;
   return w;
@@ -234,6 +244,7 @@ int exl3_linear(const uint16_t *x, int M, int k, int n, const uint16_t *trellis,
   float *yp = at<float>(workspace, L.yp);
   EXL3_TRY(exl3_cuda_check(exl3_launch_input_rht(x, M, k, suh, xh, false, stream), "input_rht launch"));
   EXL3_TRY(exl3_cuda_check(exl3_launch_reconstruct_t(trellis, k, n, K, wt, stream), "reconstruct launch"));
+  if (M >= kTcMinM) return exl3_launch_gemm_tc(xh, wt, M, n, k, svh, y, f32, nullptr, 1.0f, err, stream);
   EXL3_TRY(exl3_cuda_check(exl3_launch_gemm_mma(xh, wt, yp, M, n, k, stream), "gemm launch"));
   return exl3_cuda_check(exl3_launch_output_rht(yp, 1.0f, svh, M, n, y, f32, stream), "output_rht launch");
 }

@@ -1,0 +1,295 @@
+// gemm_tc.cu -- prefill contraction on the 5th-generation tensor cores
+// (tcgen05 MMA, TMEM accumulators, TMA operand staging), with the output
+// Hadamard transform fused into the epilogue.
+//
+//   y[m, :] = ( 2^-3.5 H (pre * rs[m] * (x' W)[m, :]) per 128-block ) . svh
+//
+// x' fp16 [M][k] (K-major) and Wt fp16 [n][k] (the transposed reconstruct,
+// K-major) are read by TMA in 128-byte-swizzled boxes.  This is the
+// reconstruct-then-GEMM form of the prefill linear ("exl3xpu" README,
+// "Layout": large M goes through reconstruct + a dense GEMM; "Prefill: int8
+// linears and oneDNN fused attention": the GEMM runs in the Hadamard domain).
+//
+// Persistent kernel, one CTA per SM, 6 warps:
+//   warp 0     TMA producer (one thread): A box 128 x 64, B box 256 x 64 per stage
+//   warp 1     TMEM owner and MMA issuer (one thread): 4 x (M128 N256 K16) per stage
+//   warps 2-5  epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31, one output
+//              row per thread, two 128-column FWHTs in registers per tile
+// TMEM holds two 128 x 256 fp32 accumulators (512 columns) so the epilogue of
+// one tile overlaps the MMAs of the next.
+#include <cudaTypedefs.h>
+
+#include "exl3_common.cuh"
+#include "tc_ptx.cuh"
+
+namespace exl3 {
+namespace gtc {
+
+constexpr int BM = 128, BK = 64;
+
+// BN = 256: 4 stages of 48 KB; BN = 128: 6 stages of 32 KB.
+template <int BN>
+struct Cfg {
+  static constexpr int STAGES = BN == 256 ? 4 : 6;
+  static constexpr int A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2, STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*barriers*/ + 1024 /*alignment*/;
+  static constexpr uint32_t IDESC = tc::idesc_f16(BM, BN);
+  static constexpr uint32_t TMEM_COLS = 2 * BN;
+};
+
+struct Args {
+  int M, n, k;
+  const __half *svh;     // [n]
+  void *y;               // [M][n]
+  const float *row_scale;  // [M] or null
+  float pre;
+  int *err;
+};
+
+__device__ __forceinline__ void fwht128_regs(float (&v)[128]) {
+#pragma unroll
+  for (int h = 1; h < 128; h <<= 1)
+#pragma unroll
+    for (int i = 0; i < 128; i += 2 * h)
+#pragma unroll
+      for (int j = i; j < i + h; ++j) {
+        const float a = v[j], b = v[j + h];
+        v[j] = a + b;
+        v[j + h] = a - b;
+      }
+}
+
+template <int BN, bool F32OUT>
+__global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                                                         const __grid_constant__ CUtensorMap tmB, Args a) {
+  using C = Cfg<BN>;
+  constexpr int STAGES = C::STAGES, A_BYTES = C::A_BYTES, B_BYTES = C::B_BYTES, STAGE_BYTES = C::STAGE_BYTES;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = tc::smem_u32(smem_raw);
+  uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  uint8_t *sA = smem;                                   // [STAGES][A_BYTES]
+  uint8_t *sB = smem + STAGES * A_BYTES;                // [STAGES][B_BYTES]
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+  uint64_t *empty = full + STAGES;
+  uint64_t *tfull = empty + STAGES;
+  uint64_t *tempty = tfull + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int MT = (a.M + BM - 1) / BM, NT = a.n / BN, KB = a.k / BK;
+  const int num_tiles = MT * NT;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&tfull[b], 1);
+      tc::mbar_init(&tempty[b], 4);
+    }
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+    tc::prefetch_tmap(&tmA);
+    tc::prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x) {
+        const int mt = tile % MT, nt = tile / MT;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!tc::mbar_wait(&empty[stage], phase ^ 1)) {
+            set_device_error(a.err, kErrBounds);
+            *abort_flag = 1;
+            break;
+          }
+          tc::mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
+          tc::tma_load_2d(sA + stage * A_BYTES, &tmA, &full[stage], kb * BK, mt * BM);
+          tc::tma_load_2d(sB + stage * B_BYTES, &tmB, &full[stage], kb * BK, nt * BN);
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      for (int tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x) {
+        if (!tc::mbar_wait(&tempty[acc], acc_phase ^ 1)) {
+          set_device_error(a.err, kErrBounds);
+          *abort_flag = 1;
+          break;
+        }
+        tc::tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!tc::mbar_wait(&full[stage], phase)) {
+            set_device_error(a.err, kErrBounds);
+            *abort_flag = 1;
+            break;
+          }
+          tc::tc_fence_after();
+          const uint64_t ad = tc::sdesc_k_sw128(sA + stage * A_BYTES);
+          const uint64_t bd = tc::sdesc_k_sw128(sB + stage * B_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            tc::mma_f16(d, ad + 2 * kk, bd + 2 * kk, C::IDESC, (kb | kk) != 0);
+          tc::mma_commit(&empty[stage]);
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+        tc::mma_commit(&tfull[acc]);
+        if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+      }
+    }
+  } else {
+    // epilogue warps 2..5
+    const int lane_base = 32 * (warp & 3);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      const int mt = tile % MT, nt = tile / MT;
+      bool ok = tc::mbar_wait(&tfull[acc], acc_phase);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok || *abort_flag) {
+        if (lane == 0) set_device_error(a.err, kErrBounds);
+        *abort_flag = 1;
+        break;
+      }
+      tc::tc_fence_after();
+      const int row = mt * BM + lane_base + lane;
+      float rs = a.pre;
+      if (a.row_scale && row < a.M) rs *= a.row_scale[row];
+#pragma unroll 1
+      for (int blk = 0; blk < BN / 128; ++blk) {
+        float v[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float t[32];
+          tc::tmem_ld32(tmem_base + ((uint32_t)lane_base << 16) + (uint32_t)(acc * BN + blk * 128 + 32 * c), t);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[32 * c + i] = t[i];
+        }
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 128; ++i) v[i] *= rs;
+        fwht128_regs(v);
+        const int col0 = nt * BN + blk * 128;
+        if (row < a.M) {
+#pragma unroll
+          for (int c8 = 0; c8 < 16; ++c8) {
+            const uint4 sv = __ldg(reinterpret_cast<const uint4 *>(a.svh + col0 + 8 * c8));
+            const __half2 *sh = reinterpret_cast<const __half2 *>(&sv);
+            float o[8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              o[2 * j] = v[8 * c8 + 2 * j] * kRhtScale * __low2float(sh[j]);
+              o[2 * j + 1] = v[8 * c8 + 2 * j + 1] * kRhtScale * __high2float(sh[j]);
+            }
+            if (F32OUT) {
+              float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(a.y) + (long)row * a.n + col0 + 8 * c8);
+              dst[0] = make_float4(o[0], o[1], o[2], o[3]);
+              dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+            } else {
+              __half2 h[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) h[j] = __floats2half2_rn(o[2 * j], o[2 * j + 1]);
+              *reinterpret_cast<uint4 *>(static_cast<__half *>(a.y) + (long)row * a.n + col0 + 8 * c8) =
+                  *reinterpret_cast<uint4 *>(h);
+            }
+          }
+        }
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&tempty[acc]);
+      if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+    }
+  }
+
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+}  // namespace gtc
+}  // namespace exl3
+
+using namespace exl3;
+
+static PFN_cuTensorMapEncodeTiled_v12000 tmap_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D fp16 tensor [rows][cols] (cols contiguous), box [box_rows][64], 128-byte swizzle.
+static int make_tmap_f16(CUtensorMap *m, const void *base, int rows, int cols, int box_rows) {
+  auto fn = tmap_encode_fn();
+  if (!fn) return exl3_fail(EXL3_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return exl3_fail(EXL3_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return EXL3_OK;
+}
+
+// n must be a multiple of 128 and k of 64; rows of x' beyond M read as zero.
+int exl3_launch_gemm_tc(const uint16_t *xh, const uint16_t *wt, int M, int n, int k, const uint16_t *svh,
+                        void *y, bool f32out, const float *row_scale, float pre, int *err, cudaStream_t s) {
+  CUtensorMap ta, tb;
+  int rc = make_tmap_f16(&ta, xh, M, k, gtc::BM);
+  if (rc) return rc;
+  const bool wide = (n % 256) == 0;
+  rc = make_tmap_f16(&tb, wt, n, k, wide ? 256 : 128);
+  if (rc) return rc;
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 148;
+  }
+  gtc::Args a{M, n, k, reinterpret_cast<const __half *>(svh), y, row_scale, pre, err};
+  const int tiles = ((M + gtc::BM - 1) / gtc::BM) * (n / (wide ? 256 : 128));
+  const int grid = tiles < sms ? tiles : sms;
+#define EXL3_GTC(BNV, F32)                                                                              \
+  do {                                                                                                \
+    auto kfn = gtc::gemm_tc_kernel<BNV, F32>;                                                         \
+    cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, gtc::Cfg<BNV>::SMEM_BYTES); \
+    kfn<<<grid, 192, gtc::Cfg<BNV>::SMEM_BYTES, s>>>(ta, tb, a);                                      \
+  } while (0)
+  if (wide) {
+    if (f32out) EXL3_GTC(256, true); else EXL3_GTC(256, false);
+  } else {
+    if (f32out) EXL3_GTC(128, true); else EXL3_GTC(128, false);
+  }
+#undef EXL3_GTC
+  cudaError_t e = cudaGetLastError();
+  return exl3_cuda_check(e, "gemm_tc launch");
+}
