@@ -173,6 +173,31 @@ int exl3_moe_grouped(const uint16_t *x, int T, int hidden,
                      void *y, int out_dtype,
                      void *workspace, size_t ws_bytes, exl3_stream_t stream);
 
+/*
+ * exl3_linear_gemv_noalloc -- the M = 1 linear (the same fused GEMV, with
+ * the same result, as exl3_linear with M = 1) for callers that cannot
+ * allocate device memory.  The source pages have no counterpart: this is an
+ * addition of this library.
+ *   Who needs it: plugin hosts whose framework owns the device memory pool
+ *   and does not let a library call cudaMalloc, and latency-critical decode
+ *   loops that reserve all memory at start-up (cudaMalloc can synchronise the
+ *   device).  They pass only inputs and outputs; no workspace.
+ *   x [k] fp16 (one row), trellis [k/16][n/16][16K], suh [k], svh [n] fp16,
+ *   y [n] fp16 (EXL3_OUT_F16) or fp32 (EXL3_OUT_F32); K, codebook as above.
+ *   Scratch: one fixed 2 MiB array of library device memory per GPU that
+ *   loads the library, held until the process exits.  A shape whose k-split
+ *   partial sums do not fit is rejected with EXL3_ERR_SHAPE (use exl3_linear
+ *   with a workspace instead).  The first call on a device looks up the
+ *   array's device address (cudaGetSymbolAddress) with that device current;
+ *   make that first call before any stream capture.  Each call clears the
+ *   parts of the array that must start at zero.  All calls share the array:
+ *   calls that can overlap on the GPU (other streams, other host threads)
+ *   race with each other.  No cudaMalloc or cudaFree is ever called.
+ */
+int exl3_linear_gemv_noalloc(const uint16_t *x, int k, int n, const uint16_t *trellis,
+                             const uint16_t *suh, const uint16_t *svh, int K, int codebook,
+                             void *y, int out_dtype, exl3_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

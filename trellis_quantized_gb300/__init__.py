@@ -73,6 +73,7 @@ def lib():
         L.exl3_moe_workspace_size.argtypes = [I, I, I, P, P]
         L.exl3_moe_workspace_size.restype = Z
         L.exl3_moe_grouped.argtypes = [P, I, I, P, P, I, I, P, P, P, I, P, Z, P]
+        L.exl3_linear_gemv_noalloc.argtypes = [P, I, I, P, P, P, I, I, P, I, P]
         _lib = L
         return L
 
@@ -180,4 +181,19 @@ def exl3_linear(x, trellis, suh, svh, K: int, codebook: int = EXL3_CB_MUL1, out_
     _check(lib().exl3_linear(_ptr(x, "x", 2), M, k, n, _ptr(trellis, "trellis", 2), _ptr(suh, "suh", 2),
                              _ptr(svh, "svh", 2), K, codebook, _ptr(y, "y"), out_dtype, _ptr(ws, "workspace"),
                              ws.numel() * ws.element_size(), _stream(stream)))
+    return y
+
+
+def exl3_linear_gemv_noalloc(x, trellis, suh, svh, K: int, codebook: int = EXL3_CB_MUL1,
+                             out_dtype: int = EXL3_OUT_F16, y=None, stream=None) -> torch.Tensor:
+    """M = 1 linear without a caller workspace, for callers that may not allocate
+    device memory: the library's fixed scratch array is used instead."""
+    k = x.numel()
+    n = trellis.shape[1] * 16
+    if y is None:
+        y = torch.empty((1, n), dtype=torch.float32 if out_dtype == EXL3_OUT_F32 else torch.float16,
+                        device=x.device)
+    _check(lib().exl3_linear_gemv_noalloc(_ptr(x, "x", 2), k, n, _ptr(trellis, "trellis", 2),
+                                          _ptr(suh, "suh", 2), _ptr(svh, "svh", 2), K, codebook,
+                                          _ptr(y, "y"), out_dtype, _stream(stream)))
     return y

@@ -1,0 +1,116 @@
+// noalloc.cu -- the M = 1 linear for callers that cannot allocate device
+// memory.
+//
+// Some callers of this library are not allowed to call cudaMalloc: plugin
+// hosts whose framework owns the device memory pool, and latency-critical
+// decode loops that reserve every byte at start-up (cudaMalloc can
+// synchronise the device and take milliseconds).  exl3_linear_gemv_noalloc
+// serves them: the same fused GEMV as exl3_linear with M = 1, but its scratch
+// (the device error word, the arrival counters and the k-split partial sums)
+// lives in one fixed array that belongs to the library, so the caller passes
+// only inputs and outputs.
+//
+// The array is kNoAllocScratchBytes (2 MiB) of device memory on every GPU
+// that loads the library, held until the process exits.  In host code its
+// name is only a host-side stand-in, not a device address, so the first call
+// on each device (with that device current) looks the address up with
+// cudaGetSymbolAddress and caches it; that first call should come before any
+// stream capture.  All calls share the array and it keeps the last call's
+// contents: each call clears the error word and the counters it uses, and
+// calls that overlap on the GPU (different streams, or several host threads)
+// race on it.
+#include <mutex>
+
+#include "exl3_common.cuh"
+
+cudaError_t exl3_launch_gemv_m1(const uint16_t *x, const uint16_t *trellis, const uint16_t *suh,
+                                const uint16_t *svh, int k, int n, int K, void *y, bool f32out,
+                                float *partials, int *counters, int *err, int splits, cudaStream_t s);
+int exl3_gemv_cta_cols(int K);
+int exl3_gemv_splits(int k, int n, int K, int target_ctas);
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 2u << 20;   // the stated maximum
+constexpr size_t kCtrl = 256;                        // error word
+constexpr size_t kCounterBytes = 8192 * sizeof(int); // up to n / 128 = 8192 column blocks
+constexpr size_t kPartialsOff = kCtrl + kCounterBytes;
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_mutex;
+void *g_scratch_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (looked up once).
+int scratch_for_current_device(void **ptr, int *sms) {
+  int dev = 0;
+  int rc = exl3_cuda_check(cudaGetDevice(&dev), "cudaGetDevice");
+  if (rc) return rc;
+  if (dev < 0 || dev >= kMaxDevices) return exl3_fail(EXL3_ERR_ARG, "device ordinal %d not supported", dev);
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!g_scratch_ptr[dev]) {
+    void *p = nullptr;
+    rc = exl3_cuda_check(cudaGetSymbolAddress(&p, g_noalloc_scratch), "cudaGetSymbolAddress(scratch)");
+    if (rc) return rc;
+    int v = 0;
+    rc = exl3_cuda_check(cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev), "SM count");
+    if (rc) return rc;
+    g_sm_count[dev] = v > 0 ? v : 152;
+    g_scratch_ptr[dev] = p;
+  }
+  *ptr = g_scratch_ptr[dev];
+  *sms = g_sm_count[dev];
+  return EXL3_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" int exl3_linear_gemv_noalloc(const uint16_t *x, int k, int n, const uint16_t *trellis,
+                                        const uint16_t *suh, const uint16_t *svh, int K, int codebook, void *y,
+                                        int out_dtype, exl3_stream_t stream) {
+  const void *ptrs[] = {x, trellis, suh, svh, y};
+  const char *names[] = {"x", "trellis", "suh", "svh", "y"};
+  for (int i = 0; i < 5; ++i) {
+    if (!ptrs[i]) return exl3_fail(EXL3_ERR_ARG, "%s is NULL", names[i]);
+    if (!aligned16(ptrs[i])) return exl3_fail(EXL3_ERR_ARG, "%s is not 16-byte aligned", names[i]);
+  }
+  if (codebook != EXL3_CB_MUL1)
+    return exl3_fail(EXL3_ERR_CODEBOOK, "codebook %d is not implemented (only mul1 = %d); refusing rather than guessing",
+                     codebook, EXL3_CB_MUL1);
+  if (K < 1 || K > 8) return exl3_fail(EXL3_ERR_BITS, "K = %d outside 1..8", K);
+  if (k <= 0 || n <= 0 || k % 128 || n % 128)
+    return exl3_fail(EXL3_ERR_SHAPE, "k = %d and n = %d must be positive multiples of 128", k, n);
+  if (out_dtype != EXL3_OUT_F16 && out_dtype != EXL3_OUT_F32)
+    return exl3_fail(EXL3_ERR_ARG, "out_dtype %d invalid", out_dtype);
+
+  void *scratch = nullptr;
+  int sms = 0;
+  int rc = scratch_for_current_device(&scratch, &sms);
+  if (rc) return rc;
+
+  const int splits = exl3_gemv_splits(k, n, K, 4 * sms);
+  const size_t colblocks = (size_t)((n + exl3_gemv_cta_cols(K) - 1) / exl3_gemv_cta_cols(K));
+  const size_t partial_bytes = splits > 1 ? sizeof(float) * (size_t)splits * (size_t)n : 0;
+  const size_t need = kPartialsOff + partial_bytes;
+  if (colblocks * sizeof(int) > kCounterBytes || need > kNoAllocScratchBytes)
+    return exl3_fail(EXL3_ERR_SHAPE,
+                     "k = %d, n = %d needs %zu bytes of the fixed scratch; its limit is %zu bytes "
+                     "(use exl3_linear with a caller workspace)",
+                     k, n, need, kNoAllocScratchBytes);
+
+  char *base = static_cast<char *>(scratch);
+  int *err = reinterpret_cast<int *>(base);
+  int *counters = reinterpret_cast<int *>(base + kCtrl);
+  float *partials = reinterpret_cast<float *>(base + kPartialsOff);
+  // The error word and the counters must start at zero; a previous call that
+  // did not finish cleanly could have left them set.
+  rc = exl3_cuda_check(cudaMemsetAsync(base, 0, kCtrl + colblocks * sizeof(int), stream), "clear scratch");
+  if (rc) return rc;
+  return exl3_cuda_check(exl3_launch_gemv_m1(x, trellis, suh, svh, k, n, K, y, out_dtype == EXL3_OUT_F32,
+                                             partials, counters, err, splits, stream),
+                         "gemv launch");
+}
