@@ -47,9 +47,10 @@ def test_noalloc_matches_workspace_entry_point_twice(out_dtype):
 
 
 def test_noalloc_rejects_shapes_beyond_the_fixed_scratch():
-    """k = 128 * 641 (prime block count) forces 641 k-splits; with n = 1024 the
-    partial sums need 2.6 MB, beyond the 2 MiB array.  Rejected before any launch."""
-    k, n, K = 128 * 641, 1024, 2
+    """n = 2^20 columns (8192 column blocks of 128) needs more partial-sum slots
+    than the 2 MiB array holds, so the call is rejected before any launch.  The
+    buffers have their full sizes all the same (K = 1 keeps the trellis at 16 MiB)."""
+    k, n, K = 128, 1 << 20, 1
     x = torch.zeros(k, dtype=torch.float16, device="cuda")
     t = torch.zeros((k // 16, n // 16, 16 * K), dtype=torch.int16, device="cuda")
     suh = torch.ones(k, dtype=torch.float16, device="cuda")

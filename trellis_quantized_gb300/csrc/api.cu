@@ -20,9 +20,8 @@ cudaError_t exl3_launch_output_rht(const float *yp, float pre, const uint16_t *s
                                    bool f32out, cudaStream_t s);
 cudaError_t exl3_launch_gemv_m1(const uint16_t *x, const uint16_t *trellis, const uint16_t *suh,
                                 const uint16_t *svh, int k, int n, int K, void *y, bool f32out,
-                                float *partials, int *counters, int *err, int splits, cudaStream_t s);
-int exl3_gemv_cta_cols(int K);
-int exl3_gemv_splits(int k, int n, int K, int target_ctas);
+                                float *partials, int *counters, int *err, int grid, cudaStream_t s);
+void exl3_gemv_plan(int k, int n, int K, int *grid, size_t *partial_floats);
 int exl3_launch_gemm_tc(const uint16_t *xh, const uint16_t *wt, int M, int n, int k, const uint16_t *svh,
                         void *y, bool f32out, const float *row_scale, float pre, int *err, cudaStream_t s);
 cudaError_t exl3_launch_gemm_mma(const uint16_t *xh, const uint16_t *wt, float *yp, int M, int n, int k,
@@ -64,6 +63,7 @@ constexpr size_t kMaxCounters = 8192;
 constexpr size_t kCounterOff = kCtrlBytes;
 constexpr size_t kDataOff = kCounterOff + kMaxCounters * sizeof(int);
 constexpr int kTcMinM = 32;          // M >= this: tcgen05 GEMM, else the mma.sync GEMM
+constexpr int kMaxGemvK = 49152;     // the M = 1 GEMV keeps x' for all of k in shared memory
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
@@ -104,15 +104,16 @@ int check_linear_shape(int M, int k, int n) {
   if (k <= 0 || n <= 0 || k % 128 || n % 128)
     return exl3_fail(EXL3_ERR_SHAPE, "k = %d and n = %d must be positive multiples of 128", k, n);
   if ((int64_t)M * k > INT32_MAX || (int64_t)M * n > INT32_MAX || (int64_t)k * n > ((int64_t)1 << 40) ||
-      (size_t)(n / 128) > kMaxCounters)
-    return exl3_fail(EXL3_ERR_SHAPE, "shape too large");
+      (size_t)(n / 128) > kMaxCounters || (M == 1 && k > kMaxGemvK))
+    return exl3_fail(EXL3_ERR_SHAPE, "shape too large (n <= %zu, and k <= %d at M = 1)", 128 * kMaxCounters,
+                     kMaxGemvK);
   return EXL3_OK;
 }
 
 // ---- exl3_linear workspace layout
 struct LinearWs {
   size_t ctrl = 0, counters = 0, partials = 0, xh = 0, wt = 0, yp = 0, total = 0;
-  int splits = 1;
+  int grid = 1;
 };
 
 LinearWs linear_ws(int M, int k, int n, int K) {
@@ -120,9 +121,10 @@ LinearWs linear_ws(int M, int k, int n, int K) {
   size_t off = kDataOff;
   w.counters = kCounterOff;
   if (M == 1) {
-    w.splits = exl3_gemv_splits(k, n, K, 4 * sm_count());
+    size_t floats = 0;
+    exl3_gemv_plan(k, n, K, &w.grid, &floats);
     w.partials = off;
-    off = align_up(off + (w.splits > 1 ? sizeof(float) * (size_t)w.splits * n : 0));
+    off = align_up(off + sizeof(float) * floats);
   } else {
     w.xh = off;
     off = align_up(off + sizeof(uint16_t) * (size_t)M * k);
@@ -214,6 +216,7 @@ int exl3_input_rht(const uint16_t *x, int M, int k, const uint16_t *suh, void *o
 
 size_t exl3_linear_workspace_size(int M, int k, int n, int K) {
   if (M < 1 || k <= 0 || n <= 0 || k % 128 || n % 128 || K < 1 || K > 8) return 0;
+  if ((size_t)(n / 128) > kMaxCounters || (M == 1 && k > kMaxGemvK)) return 0;
   return linear_ws(M, k, n, K).total;
 }
 
@@ -236,7 +239,7 @@ int exl3_linear(const uint16_t *x, int M, int k, int n, const uint16_t *trellis,
   int *err = at<int>(workspace, L.ctrl);
   if (M == 1) {
     return exl3_cuda_check(exl3_launch_gemv_m1(x, trellis, suh, svh, k, n, K, y, f32, at<float>(workspace, L.partials),
-                                               at<int>(workspace, L.counters), err, L.splits, stream),
+                                               at<int>(workspace, L.counters), err, L.grid, stream),
                            "gemv launch");
   }
   uint16_t *xh = at<uint16_t>(workspace, L.xh);

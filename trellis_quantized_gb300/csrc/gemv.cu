@@ -5,19 +5,31 @@
 //   y = RHT_out( sigma * sum_k x'_k (B_kn - 510) ) . svh,  x' = RHT_in(x . suh)
 //
 // The contraction uses the exact codebook value (B - 510) * sigma, of which
-// the fp16 weight is the rounding; the difference (< 2^-11 relative per
-// weight) stays inside the output tolerance.
+// the fp16 weight is the rounding, and x' rounded to fp16 (as the tensor-core
+// paths do); both differences (< 2^-11 relative per term) stay inside the
+// output tolerance.  DP4A seeded with 0x6400 yields the fp16 value 1024 + B
+// in the low half of its result, which a mixed-precision FMA multiplies by
+// the fp16 x' into an fp32 accumulator: sum x' (1024 + B).  The offset is
+// removed once per lane, 1534 * sum x' (1024 + 510 = 1534), at the end.
 //
-// Work split.  A lane owns G = 8 / gcd(K, 8) consecutive rows of one tile:
+// Lane work.  A lane owns G = 8 / gcd(K, 8) consecutive rows of one tile:
 // 16 G weights whose states come from CPL = K / gcd(K, 8) contiguous 16-byte
 // chunks (128 CPL bits) plus the first 32 bits of the next row group (one
 // warp shuffle; the last group of a tile wraps to the first).  LPT = 16 / G
-// lanes cover a tile, a warp covers 2 G consecutive tiles along n, and the
-// lane keeps 16 column accumulators while the warp walks down k.  A CTA of 8
-// warps spans 128 (or 256) output columns and one k-range; CTAs on the same
-// columns split k.  The last CTA to arrive for a column block (atomic
-// counter, no waiting) sums the k-split partials in a fixed order, applies
-// the output transform and writes y, so results are deterministic.
+// lanes cover a tile and a warp covers 2 G consecutive tiles along n.  Each
+// window is cut out of byte-aligned (possibly pre-shifted) words with one
+// LOP/SHR/PRMT where it can, hashed (IMAD), byte-summed by DP4A and
+// accumulated by one mixed-precision FMA.
+//
+// Work split.  The work is the list of "rows" (column block c, tile row tk),
+// c-major; a column block is 128 (or 256) output columns.  A persistent grid
+// sized to the resident CTA slots takes equal contiguous ranges of that list,
+// so every SM gets the same amount of trellis.  A CTA's range crosses column
+// blocks; at each crossing it reduces its accumulators and either finishes
+// the block itself (it owned all of it) or stores a partial sum in a slot
+// fixed by (block, CTA).  The last CTA to arrive at a block (atomic counter,
+// no waiting) adds the partials in CTA order, applies the output transform
+// and writes y: the result does not depend on timing.
 #include "exl3_common.cuh"
 
 namespace exl3 {
@@ -37,16 +49,42 @@ struct GemvShape {
 };
 
 struct GemvArgs {
-  const __half *x;         // [k]
-  const uint16_t *trellis; // [k/16][n/16][16K]
-  const __half *suh;       // [k]
-  const __half *svh;       // [n]
-  void *y;                 // [n] fp16 or fp32
-  float *partials;         // [splits][n]
-  int *counters;           // [n / CTA_COLS]
-  int *err;                // device error word
-  int k, n, tk_per_split, splits;
+  const __half *x;          // [k]
+  const uint16_t *trellis;  // [k/16][n/16][16K]
+  const __half *suh;        // [k]
+  const __half *svh;        // [n]
+  void *y;                  // [n] fp16 or fp32
+  float *partials;          // [colblocks + grid][CTA_COLS]
+  int *counters;            // [colblocks]
+  int *err;                 // device error word
+  int k, n, tiles_k, colblocks;
+  long long total;          // colblocks * tiles_k
 };
+
+// acc += x * h, x and h binary16 (h = low half of r), acc binary32.
+__device__ __forceinline__ float fma_f16_f32(unsigned short x, uint32_t r, float acc) {
+  asm("{\n.reg .f16 hx, hh;\n.reg .b16 lo, hi;\nmov.b32 {lo, hi}, %1;\nmov.b16 hh, lo;\nmov.b16 hx, %2;\n"
+      "fma.rn.f32.f16 %0, hx, hh, %0;\n}\n"
+      : "+f"(acc)
+      : "r"(r), "h"(x));
+  return acc;
+}
+
+// 16-bit window at compile-time bit offset o of the word array w.  Windows on
+// byte offsets 0, 1, 2 of a word cost one instruction; other residues reuse a
+// word shifted by (o mod 8) bits, shared between windows of the same residue.
+template <int O, int N>
+__device__ __forceinline__ uint32_t window_at(const uint32_t (&w)[N]) {
+  constexpr int a = O & 7, base = O - a, j = base >> 5, b = base & 31;
+  if constexpr (b == 24) {
+    return __funnelshift_r(w[O >> 5], w[(O >> 5) + 1], O & 31) & 0xFFFFu;
+  } else {
+    const uint32_t src = a == 0 ? w[j] : __funnelshift_r(w[j], w[j + 1], a);
+    if constexpr (b == 0) return src & 0xFFFFu;
+    else if constexpr (b == 16) return src >> 16;
+    else return __byte_perm(src, 0u, 0x4421);   // bytes 1, 2 then zeros
+  }
+}
 
 template <int K>
 __device__ __forceinline__ void load_chunks(const uint4 *src, bool valid, uint32_t (&w)[GemvShape<K>::NW]) {
@@ -61,205 +99,267 @@ __device__ __forceinline__ void load_chunks(const uint4 *src, bool valid, uint32
   }
 }
 
+// Decode the lane's 16 G weights and accumulate x'_row * (1024 + B) into the
+// 16 column accumulators.
+template <int K, int J>
+__device__ __forceinline__ void decode_accumulate(const uint32_t (&w)[GemvShape<K>::NW + 1],
+                                                  const unsigned short (&xr)[GemvShape<K>::G],
+                                                  float (&acc)[16]) {
+  if constexpr (J < 16 * GemvShape<K>::G) {
+    const uint32_t s = window_at<J * K>(w);
+    const uint32_t h = __dp4a(s * kMul1, 0x01010101u, 0x6400u);   // fp16 bits of 1024 + B
+    acc[J & 15] = fma_f16_f32(xr[J >> 4], h, acc[J & 15]);
+    decode_accumulate<K, J + 1>(w, xr, acc);
+  }
+}
+
+__device__ __forceinline__ long long range_start(int i, long long total, int grid) {
+  return (long long)i * total / grid;
+}
+
+// Index of the CTA whose range holds row r.
+__device__ __forceinline__ int range_owner(long long r, long long total, int grid) {
+  int i = (int)((r * grid) / total);
+  while (i + 1 < grid && range_start(i + 1, total, grid) <= r) ++i;
+  while (i > 0 && range_start(i, total, grid) > r) --i;
+  return i;
+}
+
 template <int K, bool F32OUT>
 __global__ void __launch_bounds__(256) gemv_m1_kernel(GemvArgs a) {
   using S = GemvShape<K>;
   extern __shared__ __align__(16) float smem[];
-  const int kr = a.tk_per_split * 16;
-  float *xs = smem;                           // [kr] transformed input slice
-  float *red = xs + kr;                       // [WK][CTA_COLS]
+  float *red = smem;                          // [WK][CTA_COLS]
   float *ys = red + S::WK * S::CTA_COLS;      // [CTA_COLS]
+  __half *xs = reinterpret_cast<__half *>(ys + S::CTA_COLS);   // [k] fp16 x' (touched blocks)
   __shared__ int s_last;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int split = blockIdx.y;
-  const int tk_begin = split * a.tk_per_split;
-  const int tiles_n = a.n >> 4;
+  const int grid = gridDim.x, me = blockIdx.x;
+  const int TK = a.tiles_k, tiles_n = a.n >> 4;
+  const long long t0 = range_start(me, a.total, grid), t1 = range_start(me + 1, a.total, grid);
+  if (t0 >= t1) return;
 
-  // ---- prologue: x' = 2^-3.5 H (x . suh) for this CTA's k-range
-  for (int b = warp; b < kr / 128; b += 8) {
-    const int col = tk_begin * 16 + b * 128 + lane * 4;
-    const uint2 xv = *reinterpret_cast<const uint2 *>(a.x + col);
-    const uint2 sv = *reinterpret_cast<const uint2 *>(a.suh + col);
-    const __half2 *xh = reinterpret_cast<const __half2 *>(&xv);
-    const __half2 *sh = reinterpret_cast<const __half2 *>(&sv);
-    float v[4] = {__low2float(xh[0]) * __low2float(sh[0]), __high2float(xh[0]) * __high2float(sh[0]),
-                  __low2float(xh[1]) * __low2float(sh[1]), __high2float(xh[1]) * __high2float(sh[1])};
-    fwht128_warp(v, lane);
-    *reinterpret_cast<float4 *>(xs + b * 128 + lane * 4) =
-        make_float4(v[0] * kRhtScale, v[1] * kRhtScale, v[2] * kRhtScale, v[3] * kRhtScale);
+  // ---- prologue: x' = 2^-3.5 H (x . suh) for the 128-blocks this range touches
+  {
+    const int KB = a.k >> 7;
+    int b0 = 0, nb = KB;
+    if (t1 - t0 < TK) {   // fewer rows than one block: at most two column blocks
+      b0 = (int)(t0 % TK) >> 3;
+      const int b1 = (int)((t1 - 1) % TK) >> 3;
+      const bool wrap = (t0 / TK) != ((t1 - 1) / TK);
+      nb = !wrap ? b1 - b0 + 1 : (b1 >= b0 ? KB : KB - b0 + b1 + 1);
+    }
+    for (int i = warp; i < nb; i += 8) {
+      const int b = (b0 + i) % KB;
+      const int col = b * 128 + lane * 4;
+      const uint2 xv = *reinterpret_cast<const uint2 *>(a.x + col);
+      const uint2 sv = *reinterpret_cast<const uint2 *>(a.suh + col);
+      const __half2 *xh = reinterpret_cast<const __half2 *>(&xv);
+      const __half2 *sh = reinterpret_cast<const __half2 *>(&sv);
+      float v[4] = {__low2float(xh[0]) * __low2float(sh[0]), __high2float(xh[0]) * __high2float(sh[0]),
+                    __low2float(xh[1]) * __low2float(sh[1]), __high2float(xh[1]) * __high2float(sh[1])};
+      fwht128_warp(v, lane);
+      __half2 o[2] = {__floats2half2_rn(v[0] * kRhtScale, v[1] * kRhtScale),
+                      __floats2half2_rn(v[2] * kRhtScale, v[3] * kRhtScale)};
+      *reinterpret_cast<uint2 *>(xs + col) = *reinterpret_cast<uint2 *>(o);
+    }
   }
   __syncthreads();
 
-  // ---- main loop
   const int wc = warp % S::WC, wk = warp / S::WC;
   const int tile_in_warp = lane / S::LPT, q = lane % S::LPT;
-  const int tn = blockIdx.x * (S::CTA_COLS / 16) + wc * S::TPW + tile_in_warp;
-  const bool valid = tn < tiles_n;
   const int src_lane = (q == S::LPT - 1) ? lane - (S::LPT - 1) : lane + 1;
-  const long tile_stride = (long)tiles_n * 16 * K / 8;   // uint4 units per tk row
-  const uint4 *base = reinterpret_cast<const uint4 *>(a.trellis) +
-                      ((long)tk_begin * tiles_n + tn) * (2 * K) + q * S::CPL;
+  const long tile_stride = (long)tiles_n * 2 * K;        // uint4 per tile row
 
-  float acc[16];
-#pragma unroll
-  for (int c = 0; c < 16; ++c) acc[c] = 0.f;
+  for (long long t = t0; t < t1;) {
+    const int c = (int)(t / TK);
+    const long long seg_end = min(t1, (long long)(c + 1) * TK);
+    const int tk_first = (int)(t - (long long)c * TK), nrows = (int)(seg_end - t);
+    const int tn = c * (S::CTA_COLS / 16) + wc * S::TPW + tile_in_warp;
+    const bool valid = tn < tiles_n;
+    const uint4 *base = reinterpret_cast<const uint4 *>(a.trellis) + ((long)tk_first * tiles_n + tn) * (2 * K) +
+                        q * S::CPL;
 
-  const int iters = (a.tk_per_split - wk + S::WK - 1) / S::WK;   // tk = wk, wk + WK, ...
-  uint32_t buf[S::DEPTH][S::NW];
+    float acc[16];
 #pragma unroll
-  for (int d = 0; d < S::DEPTH; ++d)
-    if (d < iters) load_chunks<K>(base + (long)(wk + d * S::WK) * tile_stride, valid, buf[d]);
+    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+    float sx = 0.f;   // sum of the x' this lane used (for the 1024 + 510 offset)
 
-  for (int it0 = 0; it0 < iters; it0 += S::DEPTH) {
+    const int iters = nrows > wk ? (nrows - wk + S::WK - 1) / S::WK : 0;   // rows wk, wk + WK, ...
+    uint32_t buf[S::DEPTH][S::NW];
 #pragma unroll
-    for (int d = 0; d < S::DEPTH; ++d) {
-      const int it = it0 + d;
-      if (it < iters) {
-        uint32_t w[S::NW + 1];
+    for (int d = 0; d < S::DEPTH; ++d)
+      if (d < iters) load_chunks<K>(base + (long)(wk + d * S::WK) * tile_stride, valid, buf[d]);
+    for (int it0 = 0; it0 < iters; it0 += S::DEPTH) {
 #pragma unroll
-        for (int i = 0; i < S::NW; ++i) w[i] = buf[d][i];
-        w[S::NW] = __shfl_sync(0xffffffffu, w[0], src_lane);
-        const int nxt = it + S::DEPTH;
-        if (nxt < iters) load_chunks<K>(base + (long)(wk + nxt * S::WK) * tile_stride, valid, buf[d]);
-        const int tkl = wk + it * S::WK;                       // tk - tk_begin
-        float xr[S::G];
+      for (int d = 0; d < S::DEPTH; ++d) {
+        const int it = it0 + d;
+        if (it < iters) {
+          uint32_t w[S::NW + 1];
 #pragma unroll
-        for (int i = 0; i < S::G; ++i) xr[i] = xs[tkl * 16 + S::G * q + i];
+          for (int i = 0; i < S::NW; ++i) w[i] = buf[d][i];
+          w[S::NW] = __shfl_sync(0xffffffffu, w[0], src_lane);
+          const int nxt = it + S::DEPTH;
+          if (nxt < iters) load_chunks<K>(base + (long)(wk + nxt * S::WK) * tile_stride, valid, buf[d]);
+          const int tk = tk_first + wk + it * S::WK;
+          unsigned short xr[S::G];
 #pragma unroll
-        for (int j = 0; j < 16 * S::G; ++j) {
-          const int bit = j * K;
-          const uint32_t s = window16(w[bit >> 5], w[(bit >> 5) + 1], bit & 31);
-          acc[j & 15] = fmaf(xr[j >> 4], mul1_centered(s), acc[j & 15]);
+          for (int i = 0; i < S::G; ++i) {
+            const __half xv = xs[tk * 16 + S::G * q + i];
+            xr[i] = __half_as_ushort(xv);
+            sx += __half2float(xv);
+          }
+          decode_accumulate<K, 0>(w, xr, acc);
         }
       }
     }
-  }
 
-  // ---- reduce the LPT lanes of each tile, then the k-warps of the CTA
+    // ---- reduce: LPT lanes of a tile, then the k-warps of the CTA
+    float accf[16];
 #pragma unroll
-  for (int m = 1; m < S::LPT; m <<= 1)
+    for (int i = 0; i < 16; ++i) accf[i] = fmaf(-1534.0f, sx, acc[i]);
 #pragma unroll
-    for (int c = 0; c < 16; ++c) acc[c] += __shfl_xor_sync(0xffffffffu, acc[c], m);
-  if (q == 0) {
+    for (int m = 1; m < S::LPT; m <<= 1)
 #pragma unroll
-    for (int c = 0; c < 16; ++c) red[wk * S::CTA_COLS + wc * S::COLW + tile_in_warp * 16 + c] = acc[c];
-  }
-  __syncthreads();
-  const int col0 = blockIdx.x * S::CTA_COLS;
-  float part = 0.f;
-  if (tid < S::CTA_COLS) {
+      for (int i = 0; i < 16; ++i) accf[i] += __shfl_xor_sync(0xffffffffu, accf[i], m);
+    if (q == 0) {
 #pragma unroll
-    for (int w = 0; w < S::WK; ++w) part += red[w * S::CTA_COLS + tid];
-    part *= kSigma;
-  }
-
-  if (a.splits == 1) {
-    if (tid < S::CTA_COLS) ys[tid] = part;
-  } else {
-    if (tid < S::CTA_COLS && col0 + tid < a.n) a.partials[(long)split * a.n + col0 + tid] = part;
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-      const int old = atomicAdd(a.counters + blockIdx.x, 1);
-      if (old >= a.splits) set_device_error(a.err, kErrDirtyCounter);
-      s_last = (old == a.splits - 1);
+      for (int i = 0; i < 16; ++i) red[wk * S::CTA_COLS + wc * S::COLW + tile_in_warp * 16 + i] = accf[i];
     }
     __syncthreads();
-    if (!s_last) return;
-    __threadfence();
+    const int col0 = c * S::CTA_COLS;
+    float part = 0.f;
     if (tid < S::CTA_COLS) {
-      float sum = 0.f;
-      if (col0 + tid < a.n)
-        for (int s = 0; s < a.splits; ++s) sum += __ldcg(a.partials + (long)s * a.n + col0 + tid);
-      ys[tid] = sum;
+#pragma unroll
+      for (int w = 0; w < S::WK; ++w) part += red[w * S::CTA_COLS + tid];
+      part *= kSigma;
     }
-    if (tid == 0) a.counters[blockIdx.x] = 0;   // leave the workspace clean
-  }
-  __syncthreads();
-
-  // ---- output transform of the CTA's 128-column blocks
-  if (warp < S::CTA_COLS / 128 && col0 + warp * 128 < a.n) {
-    const int c = warp * 128 + lane * 4;
-    float v[4] = {ys[c], ys[c + 1], ys[c + 2], ys[c + 3]};
-    fwht128_warp(v, lane);
-    const int gc = col0 + c;
-    const uint2 sv = *reinterpret_cast<const uint2 *>(a.svh + gc);
-    const __half2 *sh = reinterpret_cast<const __half2 *>(&sv);
-    v[0] = v[0] * kRhtScale * __low2float(sh[0]);
-    v[1] = v[1] * kRhtScale * __high2float(sh[0]);
-    v[2] = v[2] * kRhtScale * __low2float(sh[1]);
-    v[3] = v[3] * kRhtScale * __high2float(sh[1]);
-    if (F32OUT) {
-      *reinterpret_cast<float4 *>(static_cast<float *>(a.y) + gc) = make_float4(v[0], v[1], v[2], v[3]);
+    const long long blk_first = (long long)c * TK, blk_last = min((long long)(c + 1) * TK, a.total) - 1;
+    const int i_first = range_owner(blk_first, a.total, grid), i_last = range_owner(blk_last, a.total, grid);
+    bool finish;
+    if (i_first == i_last) {
+      if (tid < S::CTA_COLS) ys[tid] = part;
+      finish = true;
     } else {
-      __half2 o[2] = {__floats2half2_rn(v[0], v[1]), __floats2half2_rn(v[2], v[3])};
-      *reinterpret_cast<uint2 *>(static_cast<__half *>(a.y) + gc) = *reinterpret_cast<uint2 *>(o);
+      if (tid < S::CTA_COLS) a.partials[(long)(c + me) * S::CTA_COLS + tid] = part;
+      __threadfence();
+      __syncthreads();
+      if (tid == 0) {
+        const int expected = i_last - i_first + 1;
+        const int old = atomicAdd(a.counters + c, 1);
+        if (old >= expected) set_device_error(a.err, kErrDirtyCounter);
+        s_last = (old == expected - 1);
+      }
+      __syncthreads();
+      finish = s_last != 0;
+      if (finish) {
+        __threadfence();
+        if (tid < S::CTA_COLS) {
+          float sum = 0.f;
+          for (int i = i_first; i <= i_last; ++i) sum += __ldcg(a.partials + (long)(c + i) * S::CTA_COLS + tid);
+          ys[tid] = sum;
+        }
+        if (tid == 0) a.counters[c] = 0;   // leave the workspace clean
+      }
     }
+    __syncthreads();
+
+    // ---- output transform of the block's 128-column groups
+    if (finish && warp < S::CTA_COLS / 128 && col0 + warp * 128 < a.n) {
+      const int cc = warp * 128 + lane * 4;
+      float v[4] = {ys[cc], ys[cc + 1], ys[cc + 2], ys[cc + 3]};
+      fwht128_warp(v, lane);
+      const int gc = col0 + cc;
+      const uint2 sv = *reinterpret_cast<const uint2 *>(a.svh + gc);
+      const __half2 *sh = reinterpret_cast<const __half2 *>(&sv);
+      v[0] = v[0] * kRhtScale * __low2float(sh[0]);
+      v[1] = v[1] * kRhtScale * __high2float(sh[0]);
+      v[2] = v[2] * kRhtScale * __low2float(sh[1]);
+      v[3] = v[3] * kRhtScale * __high2float(sh[1]);
+      if (F32OUT) {
+        *reinterpret_cast<float4 *>(static_cast<float *>(a.y) + gc) = make_float4(v[0], v[1], v[2], v[3]);
+      } else {
+        __half2 o[2] = {__floats2half2_rn(v[0], v[1]), __floats2half2_rn(v[2], v[3])};
+        *reinterpret_cast<uint2 *>(static_cast<__half *>(a.y) + gc) = *reinterpret_cast<uint2 *>(o);
+      }
+    }
+    __syncthreads();   // red / ys are reused by the next segment
+    t = seg_end;
   }
 }
 
-template <int K>
-int cta_cols() { return GemvShape<K>::CTA_COLS; }
-
-template <int K>
-size_t smem_bytes(int kr) {
-  return sizeof(float) * ((size_t)kr + (size_t)GemvShape<K>::WK * GemvShape<K>::CTA_COLS +
-                          GemvShape<K>::CTA_COLS);
-}
+template <int K, bool F32>
+struct Launcher {
+  static size_t smem(int k) {
+    return sizeof(float) * ((size_t)GemvShape<K>::WK * GemvShape<K>::CTA_COLS + GemvShape<K>::CTA_COLS) +
+           sizeof(__half) * (size_t)k;
+  }
+  static int grid(int k) {
+    static int cached_k = -1, cached = 0;
+    if (cached_k == k) return cached;
+    int dev = 0, sms = 0, occ = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const size_t sm = smem(k);
+    cudaFuncSetAttribute(gemv_m1_kernel<K, F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gemv_m1_kernel<K, F32>, 256, sm);
+    cudaGetLastError();
+    if (sms <= 0) sms = 152;
+    if (occ <= 0) occ = 1;
+    cached_k = k;
+    cached = sms * occ;
+    return cached;
+  }
+  static cudaError_t launch(const GemvArgs &a, int grid, cudaStream_t s) {
+    static int attr_k = -1;
+    const size_t sm = smem(a.k);
+    if (attr_k != a.k && sm > 48 * 1024) {
+      cudaFuncSetAttribute(gemv_m1_kernel<K, F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+      attr_k = a.k;
+    }
+    gemv_m1_kernel<K, F32><<<grid, 256, sm, s>>>(a);
+    return cudaGetLastError();
+  }
+};
 
 }  // namespace exl3
 
 using namespace exl3;
 
-// Columns covered by one CTA for width K (128 or 256).
+#define EXL3_K_SWITCH(K, ...)                         \
+  switch (K) {                                        \
+    case 1: { constexpr int KK = 1; __VA_ARGS__; } break; \
+    case 2: { constexpr int KK = 2; __VA_ARGS__; } break; \
+    case 3: { constexpr int KK = 3; __VA_ARGS__; } break; \
+    case 4: { constexpr int KK = 4; __VA_ARGS__; } break; \
+    case 5: { constexpr int KK = 5; __VA_ARGS__; } break; \
+    case 6: { constexpr int KK = 6; __VA_ARGS__; } break; \
+    case 7: { constexpr int KK = 7; __VA_ARGS__; } break; \
+    default: { constexpr int KK = 8; __VA_ARGS__; } break; \
+  }
+
+// Columns covered by one column block for width K (128 or 256).
 int exl3_gemv_cta_cols(int K) {
-  switch (K) {
-    case 1: return cta_cols<1>();
-    case 2: return cta_cols<2>();
-    case 3: return cta_cols<3>();
-    case 4: return cta_cols<4>();
-    case 5: return cta_cols<5>();
-    case 6: return cta_cols<6>();
-    case 7: return cta_cols<7>();
-    case 8: return cta_cols<8>();
-    default: return 128;
-  }
+  int r = 128;
+  EXL3_K_SWITCH(K, r = GemvShape<KK>::CTA_COLS);
+  return r;
 }
 
-// Number of k-splits: the smallest divisor of k/128 that gives at least
-// `target_ctas` CTAs, with at most 8192 k-elements of x' per CTA.
-int exl3_gemv_splits(int k, int n, int K, int target_ctas) {
-  const int kb = k / 128;
-  const int colblocks = ceil_div(n, exl3_gemv_cta_cols(K));
-  int best = kb;
-  for (int s = 1; s <= kb; ++s) {
-    if (kb % s) continue;
-    if ((kb / s) * 128 > 8192) continue;
-    best = s;
-    if (colblocks * s >= target_ctas) break;
-  }
-  return best;
-}
-
-size_t exl3_gemv_smem_bytes(int k, int K, int splits) {
-  const int kr = k / splits;
-  switch (K) {
-    case 1: return smem_bytes<1>(kr);
-    case 2: return smem_bytes<2>(kr);
-    case 3: return smem_bytes<3>(kr);
-    case 4: return smem_bytes<4>(kr);
-    case 5: return smem_bytes<5>(kr);
-    case 6: return smem_bytes<6>(kr);
-    case 7: return smem_bytes<7>(kr);
-    default: return smem_bytes<8>(kr);
-  }
+// Persistent grid size and the partial-sum slots (floats) the GEMV needs.
+void exl3_gemv_plan(int k, int n, int K, int *grid, size_t *partial_floats) {
+  int g = 0, cc = 128;
+  EXL3_K_SWITCH(K, (g = Launcher<KK, false>::grid(k), cc = GemvShape<KK>::CTA_COLS));
+  const long long colblocks = (n + cc - 1) / cc;
+  const long long total = colblocks * (k / 16);
+  if (g > total) g = (int)total;
+  *grid = g;
+  *partial_floats = (size_t)(colblocks + g) * (size_t)cc;
 }
 
 cudaError_t exl3_launch_gemv_m1(const uint16_t *x, const uint16_t *trellis, const uint16_t *suh,
                                 const uint16_t *svh, int k, int n, int K, void *y, bool f32out,
-                                float *partials, int *counters, int *err, int splits,
-                                cudaStream_t s) {
+                                float *partials, int *counters, int *err, int grid, cudaStream_t s) {
   GemvArgs a;
   a.x = reinterpret_cast<const __half *>(x);
   a.trellis = trellis;
@@ -271,27 +371,15 @@ cudaError_t exl3_launch_gemv_m1(const uint16_t *x, const uint16_t *trellis, cons
   a.err = err;
   a.k = k;
   a.n = n;
-  a.splits = splits;
-  a.tk_per_split = (k / 16) / splits;
-  const dim3 grid(ceil_div(n, exl3_gemv_cta_cols(K)), splits);
-  const size_t smem = exl3_gemv_smem_bytes(k, K, splits);
-  switch (K) {
-#define EXL3_CASE(KK)                                                                          \
-  case KK:                                                                                     \
-    if (f32out) {                                                                              \
-      cudaFuncSetAttribute(gemv_m1_kernel<KK, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                           (int)smem);                                                         \
-      gemv_m1_kernel<KK, true><<<grid, 256, smem, s>>>(a);                                     \
-    } else {                                                                                   \
-      cudaFuncSetAttribute(gemv_m1_kernel<KK, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                           (int)smem);                                                         \
-      gemv_m1_kernel<KK, false><<<grid, 256, smem, s>>>(a);                                    \
-    }                                                                                          \
-    break;
-    EXL3_CASE(1) EXL3_CASE(2) EXL3_CASE(3) EXL3_CASE(4) EXL3_CASE(5) EXL3_CASE(6) EXL3_CASE(7)
-    EXL3_CASE(8)
-#undef EXL3_CASE
-    default: return cudaErrorInvalidValue;
+  a.tiles_k = k / 16;
+  const int cc = exl3_gemv_cta_cols(K);
+  a.colblocks = (n + cc - 1) / cc;
+  a.total = (long long)a.colblocks * a.tiles_k;
+  cudaError_t e = cudaSuccess;
+  if (f32out) {
+    EXL3_K_SWITCH(K, e = Launcher<KK, true>::launch(a, grid, s));
+  } else {
+    EXL3_K_SWITCH(K, e = Launcher<KK, false>::launch(a, grid, s));
   }
-  return cudaGetLastError();
+  return e;
 }

@@ -25,9 +25,9 @@
 
 cudaError_t exl3_launch_gemv_m1(const uint16_t *x, const uint16_t *trellis, const uint16_t *suh,
                                 const uint16_t *svh, int k, int n, int K, void *y, bool f32out,
-                                float *partials, int *counters, int *err, int splits, cudaStream_t s);
+                                float *partials, int *counters, int *err, int grid, cudaStream_t s);
 int exl3_gemv_cta_cols(int K);
-int exl3_gemv_splits(int k, int n, int K, int target_ctas);
+void exl3_gemv_plan(int k, int n, int K, int *grid, size_t *partial_floats);
 
 namespace {
 
@@ -41,10 +41,8 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 
 std::mutex g_mutex;
 void *g_scratch_ptr[kMaxDevices] = {};
-int g_sm_count[kMaxDevices] = {};
-
 // Device address of the scratch array on the current device (looked up once).
-int scratch_for_current_device(void **ptr, int *sms) {
+int scratch_for_current_device(void **ptr) {
   int dev = 0;
   int rc = exl3_cuda_check(cudaGetDevice(&dev), "cudaGetDevice");
   if (rc) return rc;
@@ -54,14 +52,9 @@ int scratch_for_current_device(void **ptr, int *sms) {
     void *p = nullptr;
     rc = exl3_cuda_check(cudaGetSymbolAddress(&p, g_noalloc_scratch), "cudaGetSymbolAddress(scratch)");
     if (rc) return rc;
-    int v = 0;
-    rc = exl3_cuda_check(cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev), "SM count");
-    if (rc) return rc;
-    g_sm_count[dev] = v > 0 ? v : 152;
     g_scratch_ptr[dev] = p;
   }
   *ptr = g_scratch_ptr[dev];
-  *sms = g_sm_count[dev];
   return EXL3_OK;
 }
 
@@ -87,15 +80,16 @@ extern "C" int exl3_linear_gemv_noalloc(const uint16_t *x, int k, int n, const u
   if (out_dtype != EXL3_OUT_F16 && out_dtype != EXL3_OUT_F32)
     return exl3_fail(EXL3_ERR_ARG, "out_dtype %d invalid", out_dtype);
 
+  if (k > 49152) return exl3_fail(EXL3_ERR_SHAPE, "k = %d too large for the M = 1 GEMV (k <= 49152)", k);
   void *scratch = nullptr;
-  int sms = 0;
-  int rc = scratch_for_current_device(&scratch, &sms);
+  int rc = scratch_for_current_device(&scratch);
   if (rc) return rc;
 
-  const int splits = exl3_gemv_splits(k, n, K, 4 * sms);
+  int grid = 0;
+  size_t partial_floats = 0;
+  exl3_gemv_plan(k, n, K, &grid, &partial_floats);
   const size_t colblocks = (size_t)((n + exl3_gemv_cta_cols(K) - 1) / exl3_gemv_cta_cols(K));
-  const size_t partial_bytes = splits > 1 ? sizeof(float) * (size_t)splits * (size_t)n : 0;
-  const size_t need = kPartialsOff + partial_bytes;
+  const size_t need = kPartialsOff + sizeof(float) * partial_floats;
   if (colblocks * sizeof(int) > kCounterBytes || need > kNoAllocScratchBytes)
     return exl3_fail(EXL3_ERR_SHAPE,
                      "k = %d, n = %d needs %zu bytes of the fixed scratch; its limit is %zu bytes "
@@ -111,6 +105,6 @@ extern "C" int exl3_linear_gemv_noalloc(const uint16_t *x, int k, int n, const u
   rc = exl3_cuda_check(cudaMemsetAsync(base, 0, kCtrl + colblocks * sizeof(int), stream), "clear scratch");
   if (rc) return rc;
   return exl3_cuda_check(exl3_launch_gemv_m1(x, trellis, suh, svh, k, n, K, y, out_dtype == EXL3_OUT_F32,
-                                             partials, counters, err, splits, stream),
+                                             partials, counters, err, grid, stream),
                          "gemv launch");
 }
