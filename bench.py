@@ -259,9 +259,23 @@ def bench_prefill(args, bf16_peak, src):
     ms = a.elapsed_time(b) / reps
     flops = 2.0 * c.M * c.k * c.n
     tf = flops / (ms * 1e-3) / 1e12
+    # int8 variant: same shapes, q_x/q_w integer-exact on the f16 tensor path
+    ws8 = tq.workspace(tq.exl3_linear_int8_workspace_size(c.M, c.k, c.n, c.K))
+    for _ in range(3):
+        tq.exl3_linear_int8(x, t, suh, svh, 4, y=y, workspace_buf=ws8)
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(reps):
+        tq.exl3_linear_int8(x, t, suh, svh, 4, y=y, workspace_buf=ws8)
+    b.record()
+    torch.cuda.synchronize()
+    ms8 = a.elapsed_time(b) / reps
+    tf8 = flops / (ms8 * 1e-3) / 1e12
     return {"workload": "M=4096 k=5120 n=17408 K=4 fp16 out", "ms": round(ms, 4), "tflops": round(tf, 1),
             "peak_tflops": bf16_peak, "peak_source": src + " bf16 sustained", "frac": round(tf / bf16_peak, 4),
-            "path": "input RHT + transposed reconstruct + tcgen05/TMEM GEMM with fused output RHT"}
+            "path": "input RHT + transposed reconstruct + tcgen05/TMEM GEMM with fused output RHT",
+            "int8": {"ms": round(ms8, 4), "tops": round(tf8, 1), "frac_of_f16_peak": round(tf8 / bf16_peak, 4),
+                     "path": "quantise + q_w reconstruct + exact int32 on tcgen05 kind::f16 (no kind::i8 on sm_103a)"}}
 
 
 # ------------------------------------------------------------------------- oracle

@@ -184,6 +184,32 @@ def exl3_linear(x, trellis, suh, svh, K: int, codebook: int = EXL3_CB_MUL1, out_
     return y
 
 
+def exl3_linear_int8_workspace_size(M: int, k: int, n: int, K: int) -> int:
+    return lib().exl3_linear_int8_workspace_size(M, k, n, K)
+
+
+WEIGHT_SCALE = 3.453125 / 127.0
+
+
+def exl3_linear_int8(x, trellis, suh, svh, K: int, codebook: int = EXL3_CB_MUL1,
+                     weight_scale: float = WEIGHT_SCALE, y=None, xq_out=None, row_scale_out=None,
+                     acc_out=None, workspace_buf=None, stream=None) -> torch.Tensor:
+    """int8 prefill linear: y fp16 [M, n]; optional int8 q_x, fp32 row scales and
+    int32 accumulators are written to the given tensors."""
+    M, k = x.shape
+    n = trellis.shape[1] * 16
+    if y is None:
+        y = torch.empty((M, n), dtype=torch.float16, device=x.device)
+    need = exl3_linear_int8_workspace_size(M, k, n, K)
+    ws = workspace_buf if workspace_buf is not None else workspace(need, x.device, stream)
+    _check(lib().exl3_linear_int8(_ptr(x, "x", 2), M, k, n, _ptr(trellis, "trellis", 2), _ptr(suh, "suh", 2),
+                                  _ptr(svh, "svh", 2), K, codebook, weight_scale, _ptr(y, "y", 2),
+                                  _ptr(xq_out, "xq_out", 1), _ptr(row_scale_out, "row_scale_out", 4),
+                                  _ptr(acc_out, "acc_out", 4), _ptr(ws, "workspace"),
+                                  ws.numel() * ws.element_size(), _stream(stream)))
+    return y
+
+
 def exl3_linear_gemv_noalloc(x, trellis, suh, svh, K: int, codebook: int = EXL3_CB_MUL1,
                              out_dtype: int = EXL3_OUT_F16, y=None, stream=None) -> torch.Tensor:
     """M = 1 linear without a caller workspace, for callers that may not allocate

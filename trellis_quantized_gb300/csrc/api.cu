@@ -23,7 +23,12 @@ cudaError_t exl3_launch_gemv_m1(const uint16_t *x, const uint16_t *trellis, cons
                                 float *partials, int *counters, int *err, int grid, cudaStream_t s);
 void exl3_gemv_plan(int k, int n, int K, int *grid, size_t *partial_floats);
 int exl3_launch_gemm_tc(const uint16_t *xh, const uint16_t *wt, int M, int n, int k, const uint16_t *svh,
-                        void *y, bool f32out, const float *row_scale, float pre, int *err, cudaStream_t s);
+                        void *y, bool f32out, const float *row_scale, float pre, int *err, cudaStream_t s,
+                        bool q8 = false, int32_t *acc_out = nullptr);
+cudaError_t exl3_launch_quant_act(const uint16_t *x, int M, int k, const uint16_t *suh, uint16_t *qh,
+                                  int8_t *q8, float *row_scale, cudaStream_t s);
+cudaError_t exl3_launch_reconstruct_q8_t(const uint16_t *trellis, int k, int n, int K, uint16_t *wq,
+                                         cudaStream_t s);
 cudaError_t exl3_launch_gemm_mma(const uint16_t *xh, const uint16_t *wt, float *yp, int M, int n, int k,
                                  cudaStream_t s);
 
@@ -135,6 +140,24 @@ LinearWs linear_ws(int M, int k, int n, int K) {
       off = align_up(off + sizeof(float) * (size_t)M * n);
     }
   }
+  w.total = off;
+  return w;
+}
+
+// ---- exl3_linear_int8 workspace layout
+struct LinearInt8Ws {
+  size_t qh = 0, wq = 0, rs = 0, total = 0;
+};
+
+LinearInt8Ws linear_int8_ws(int M, int k, int n) {
+  LinearInt8Ws w;
+  size_t off = kDataOff;
+  w.qh = off;
+  off = align_up(off + sizeof(uint16_t) * (size_t)M * k);
+  w.wq = off;
+  off = align_up(off + sizeof(uint16_t) * (size_t)k * n);
+  w.rs = off;
+  off = align_up(off + sizeof(float) * (size_t)M);
   w.total = off;
   return w;
 }
@@ -253,18 +276,37 @@ int exl3_linear(const uint16_t *x, int M, int k, int n, const uint16_t *trellis,
 }
 
 size_t exl3_linear_int8_workspace_size(int M, int k, int n, int K) {
-  (void)M; (void)k; (void)n; (void)K;
-  return 0;
+  if (M < 1 || k <= 0 || n <= 0 || k % 128 || n % 128 || K < 1 || K > 8) return 0;
+  return linear_int8_ws(M, k, n).total;
 }
 
 int exl3_linear_int8(const uint16_t *x, int M, int k, int n, const uint16_t *trellis, const uint16_t *suh,
                      const uint16_t *svh, int K, int codebook, float weight_scale, uint16_t *y, int8_t *xq_out,
                      float *row_scale_out, int32_t *acc_out, void *workspace, size_t ws_bytes,
                      exl3_stream_t stream) {
-  (void)x; (void)M; (void)k; (void)n; (void)trellis; (void)suh; (void)svh; (void)K; (void)codebook;
-  (void)weight_scale; (void)y; (void)xq_out; (void)row_scale_out; (void)acc_out; (void)workspace;
-  (void)ws_bytes; (void)stream;
-  return exl3_fail(EXL3_ERR_ARG, "exl3_linear_int8 is not available in this build");
+  g_last_error.clear();
+  EXL3_TRY(check_ptr(x, "x"));
+  EXL3_TRY(check_ptr(trellis, "trellis"));
+  EXL3_TRY(check_ptr(suh, "suh"));
+  EXL3_TRY(check_ptr(svh, "svh"));
+  EXL3_TRY(check_ptr(y, "y"));
+  EXL3_TRY(check_ptr(xq_out, "xq_out", false));
+  EXL3_TRY(check_ptr(row_scale_out, "row_scale_out", false));
+  EXL3_TRY(check_ptr(acc_out, "acc_out", false));
+  EXL3_TRY(check_bits_codebook(K, codebook));
+  EXL3_TRY(check_linear_shape(M, k, n));
+  if (!(weight_scale > 0.0f) || weight_scale > 1e30f)
+    return exl3_fail(EXL3_ERR_ARG, "weight_scale must be positive and finite");
+  if (k > kMaxGemvK) return exl3_fail(EXL3_ERR_SHAPE, "k = %d too large for the int8 path (k <= %d)", k, kMaxGemvK);
+  const LinearInt8Ws L = linear_int8_ws(M, k, n);
+  EXL3_TRY(check_workspace(workspace, ws_bytes, L.total));
+  uint16_t *qh = at<uint16_t>(workspace, L.qh);
+  uint16_t *wq = at<uint16_t>(workspace, L.wq);
+  float *rs = row_scale_out ? row_scale_out : at<float>(workspace, L.rs);
+  int *err = at<int>(workspace, 0);
+  EXL3_TRY(exl3_cuda_check(exl3_launch_quant_act(x, M, k, suh, qh, xq_out, rs, stream), "quant_act launch"));
+  EXL3_TRY(exl3_cuda_check(exl3_launch_reconstruct_q8_t(trellis, k, n, K, wq, stream), "reconstruct_q8 launch"));
+  return exl3_launch_gemm_tc(qh, wq, M, n, k, svh, y, false, rs, weight_scale, err, stream, true, acc_out);
 }
 
 size_t exl3_moe_workspace_size(int T, int topk, int E, const exl3_expert_proj *w13,

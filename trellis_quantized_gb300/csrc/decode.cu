@@ -89,9 +89,75 @@ __global__ void __launch_bounds__(256) reconstruct_t_kernel(const uint16_t *__re
   }
 }
 
+// int8 weights ("exl3xpu" README, "Prefill: int8 linears and oneDNN fused
+// attention": one static weight scale, fused into reconstruct):
+// q_w = RNE(v * 127 / 3.453125) of the decoded fp16 weight v, an exact
+// rational.  v depends on the state only through the byte sum B, so each CTA
+// first fills a 1021-entry table q(B) in shared memory with exact integer
+// arithmetic: v = V * 2^-24 with V an integer and 3.453125 = 1768 * 2^-9, so
+// q = RNE(V * 127 / (1768 * 2^15)).
+__device__ __forceinline__ int quant_weight_of_bsum(int B) {
+  const float v = __half2float(__float2half_rn((float)(B - 510) * kSigma));
+  const long long V = __float2ll_rn(v * 16777216.0f);     // exact: v has 11 significant bits
+  const long long num = V * 127, den = 1768LL * 32768LL;
+  const long long an = num < 0 ? -num : num;
+  long long q = an / den;
+  const long long rem = an - q * den;
+  if (2 * rem > den || (2 * rem == den && (q & 1))) ++q;
+  return (int)(num < 0 ? -q : q);
+}
+
+// Transposed reconstruct of q_w as integer-valued fp16: Wq[16 tn + c][16 tk + r].
+template <int K>
+__global__ void __launch_bounds__(256) reconstruct_q8_t_kernel(const uint16_t *__restrict__ trellis,
+                                                               int tiles_k, int tiles_n,
+                                                               uint16_t *__restrict__ wq, int k) {
+  __shared__ __align__(16) __half sm[32][128 + 8];
+  __shared__ __half qtab[1024];
+  const int t = threadIdx.x;
+  for (int B = t; B < 1021; B += 256) qtab[B] = __int2half_rn(quant_weight_of_bsum(B));
+  __syncthreads();
+  const int tile_local = t >> 4, r = t & 15;
+  const int tkl = tile_local & 7, tnl = tile_local >> 3;
+  const int tk = blockIdx.y * 8 + tkl, tn = blockIdx.x * 2 + tnl;
+  if (tk < tiles_k && tn < tiles_n) {
+    uint32_t a[(K + 2) / 2 + 1];
+    load_row_words<K>(trellis + ((long)tk * tiles_n + tn) * 16 * K, r, a);
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const int bit = c * K;
+      const uint32_t s = window16(a[bit >> 5], a[(bit >> 5) + 1], bit & 31);
+      sm[tnl * 16 + c][tkl * 16 + r] = qtab[mul1_bsum(s)];
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    int chunk = t + i * 256;
+    int nrow = chunk >> 4, kc = (chunk & 15) * 8;
+    int ng = blockIdx.x * 32 + nrow, kg = blockIdx.y * 128 + kc;
+    if (ng < tiles_n * 16 && kg < k)
+      *reinterpret_cast<uint4 *>(wq + (long)ng * k + kg) = *reinterpret_cast<const uint4 *>(&sm[nrow][kc]);
+  }
+}
+
 }  // namespace exl3
 
 using namespace exl3;
+
+cudaError_t exl3_launch_reconstruct_q8_t(const uint16_t *trellis, int k, int n, int K, uint16_t *wq,
+                                         cudaStream_t s) {
+  dim3 grid(ceil_div(n / 16, 2), ceil_div(k / 16, 8));
+  switch (K) {
+#define EXL3_CASE(KK) \
+  case KK: reconstruct_q8_t_kernel<KK><<<grid, 256, 0, s>>>(trellis, k / 16, n / 16, wq, k); break;
+    EXL3_CASE(1) EXL3_CASE(2) EXL3_CASE(3) EXL3_CASE(4) EXL3_CASE(5) EXL3_CASE(6) EXL3_CASE(7)
+    EXL3_CASE(8)
+#undef EXL3_CASE
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
 
 // Launch helpers, called from api.cu after argument validation.
 cudaError_t exl3_launch_decode_tile(const uint16_t *trellis, int n, int K, int tk0, int tk_cnt,

@@ -15,8 +15,17 @@
 //   warp 1     TMEM owner and MMA issuer (one thread): 4 x (M128 N256 K16) per stage
 //   warps 2-5  epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31, one output
 //              row per thread, two 128-column FWHTs in registers per tile
-// TMEM holds two 128 x 256 fp32 accumulators (512 columns) so the epilogue of
-// one tile overlaps the MMAs of the next.
+// TMEM holds two 128 x BN fp32 accumulators so the epilogue of one tile
+// overlaps the MMAs of the next.
+//
+// Integer mode (the int8 variant of "exl3xpu" README, "Prefill: int8
+// linears and oneDNN fused attention").  GB300's tcgen05 has no int8 kind
+// (kind::i8 does not assemble for sm_103a), so the s8 x s8 -> s32 product is
+// computed exactly on the f16 kind: both operands hold integers in
+// [-127, 127] as fp16, every k-chunk of 512 accumulates in a fresh fp32
+// accumulator (|partial sum| <= 512 * 127^2 < 2^23, so every sum is exact),
+// and the epilogue converts each chunk to int32 and adds them in registers.
+// The output is y = RHT_out(acc * row_scale[m] * weight_scale) . svh.
 #include <cudaTypedefs.h>
 
 #include "exl3_common.cuh"
@@ -37,6 +46,8 @@ struct Cfg {
   static constexpr uint32_t TMEM_COLS = 2 * BN;
 };
 
+constexpr int Q8_CHUNK_KB = 8;   // k-blocks of 64 per exact fp32 chunk (512 elements)
+
 struct Args {
   int M, n, k;
   const __half *svh;     // [n]
@@ -44,6 +55,7 @@ struct Args {
   const float *row_scale;  // [M] or null
   float pre;
   int *err;
+  int32_t *acc_out;      // integer mode: optional [M][n] copy of the accumulators
 };
 
 __device__ __forceinline__ void fwht128_regs(float (&v)[128]) {
@@ -59,7 +71,35 @@ __device__ __forceinline__ void fwht128_regs(float (&v)[128]) {
       }
 }
 
-template <int BN, bool F32OUT>
+// y[row][col0 .. col0+127] = v * 2^-3.5 * svh (v already transformed).
+template <bool F32OUT>
+__device__ __forceinline__ void store_row(const float (&v)[128], const Args &a, int row, int col0) {
+  if (row >= a.M) return;
+#pragma unroll
+  for (int c8 = 0; c8 < 16; ++c8) {
+    const uint4 sv = __ldg(reinterpret_cast<const uint4 *>(a.svh + col0 + 8 * c8));
+    const __half2 *sh = reinterpret_cast<const __half2 *>(&sv);
+    float o[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      o[2 * j] = v[8 * c8 + 2 * j] * kRhtScale * __low2float(sh[j]);
+      o[2 * j + 1] = v[8 * c8 + 2 * j + 1] * kRhtScale * __high2float(sh[j]);
+    }
+    if (F32OUT) {
+      float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(a.y) + (long)row * a.n + col0 + 8 * c8);
+      dst[0] = make_float4(o[0], o[1], o[2], o[3]);
+      dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+    } else {
+      __half2 h[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) h[j] = __floats2half2_rn(o[2 * j], o[2 * j + 1]);
+      *reinterpret_cast<uint4 *>(static_cast<__half *>(a.y) + (long)row * a.n + col0 + 8 * c8) =
+          *reinterpret_cast<uint4 *>(h);
+    }
+  }
+}
+
+template <int BN, bool F32OUT, bool Q8>
 __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                                                          const __grid_constant__ CUtensorMap tmB, Args a) {
   using C = Cfg<BN>;
@@ -126,31 +166,35 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
     if (lane == 0) {
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
+      const int CH = Q8 ? Q8_CHUNK_KB : KB;       // k-blocks per accumulator hand-off
       for (int tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x) {
-        if (!tc::mbar_wait(&tempty[acc], acc_phase ^ 1)) {
-          set_device_error(a.err, kErrBounds);
-          *abort_flag = 1;
-          break;
-        }
-        tc::tc_fence_after();
-        const uint32_t d = tmem_base + (uint32_t)(acc * BN);
-        for (int kb = 0; kb < KB; ++kb) {
-          if (!tc::mbar_wait(&full[stage], phase)) {
+        for (int kb0 = 0; kb0 < KB && !*abort_flag; kb0 += CH) {
+          if (!tc::mbar_wait(&tempty[acc], acc_phase ^ 1)) {
             set_device_error(a.err, kErrBounds);
             *abort_flag = 1;
             break;
           }
           tc::tc_fence_after();
-          const uint64_t ad = tc::sdesc_k_sw128(sA + stage * A_BYTES);
-          const uint64_t bd = tc::sdesc_k_sw128(sB + stage * B_BYTES);
+          const uint32_t d = tmem_base + (uint32_t)(acc * BN);
+          const int kb1 = min(KB, kb0 + CH);
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!tc::mbar_wait(&full[stage], phase)) {
+              set_device_error(a.err, kErrBounds);
+              *abort_flag = 1;
+              break;
+            }
+            tc::tc_fence_after();
+            const uint64_t ad = tc::sdesc_k_sw128(sA + stage * A_BYTES);
+            const uint64_t bd = tc::sdesc_k_sw128(sB + stage * B_BYTES);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            tc::mma_f16(d, ad + 2 * kk, bd + 2 * kk, C::IDESC, (kb | kk) != 0);
-          tc::mma_commit(&empty[stage]);
-          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+            for (int kk = 0; kk < BK / 16; ++kk)
+              tc::mma_f16(d, ad + 2 * kk, bd + 2 * kk, C::IDESC, (kb != kb0 || kk != 0) ? 1u : 0u);
+            tc::mma_commit(&empty[stage]);
+            if (++stage == STAGES) { stage = 0; phase ^= 1; }
+          }
+          tc::mma_commit(&tfull[acc]);
+          if (++acc == 2) { acc = 0; acc_phase ^= 1; }
         }
-        tc::mma_commit(&tfull[acc]);
-        if (++acc == 2) { acc = 0; acc_phase ^= 1; }
       }
     }
   } else {
@@ -158,63 +202,87 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
     const int lane_base = 32 * (warp & 3);
     int acc = 0;
     uint32_t acc_phase = 0;
+    const int CH = Q8 ? Q8_CHUNK_KB : KB;
+    const int nchunks = (KB + CH - 1) / CH;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const int mt = tile % MT, nt = tile / MT;
-      bool ok = tc::mbar_wait(&tfull[acc], acc_phase);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok || *abort_flag) {
-        if (lane == 0) set_device_error(a.err, kErrBounds);
-        *abort_flag = 1;
-        break;
-      }
-      tc::tc_fence_after();
       const int row = mt * BM + lane_base + lane;
       float rs = a.pre;
       if (a.row_scale && row < a.M) rs *= a.row_scale[row];
-#pragma unroll 1
-      for (int blk = 0; blk < BN / 128; ++blk) {
+      bool failed = false;
+      if constexpr (Q8) {
+        // BN == 128: one 128-column block per tile, integer accumulation per
+        // chunk.  The int32 sums live in the same registers that later hold
+        // the float row (bit patterns), keeping one 128-entry array alive.
         float v[128];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float t[32];
-          tc::tmem_ld32(tmem_base + ((uint32_t)lane_base << 16) + (uint32_t)(acc * BN + blk * 128 + 32 * c), t);
+        for (int i = 0; i < 128; ++i) v[i] = __int_as_float(0);
+        for (int ch = 0; ch < nchunks; ++ch) {
+          bool ok = tc::mbar_wait(&tfull[acc], acc_phase);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok || *abort_flag) { failed = true; break; }
+          tc::tc_fence_after();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[32 * c + i] = t[i];
-        }
-        tc::tmem_ld_wait();
+          for (int c = 0; c < 4; ++c) {
+            float t[32];
+            tc::tmem_ld32(tmem_base + ((uint32_t)lane_base << 16) + (uint32_t)(acc * BN + 32 * c), t);
+            tc::tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 128; ++i) v[i] *= rs;
-        fwht128_regs(v);
-        const int col0 = nt * BN + blk * 128;
-        if (row < a.M) {
-#pragma unroll
-          for (int c8 = 0; c8 < 16; ++c8) {
-            const uint4 sv = __ldg(reinterpret_cast<const uint4 *>(a.svh + col0 + 8 * c8));
-            const __half2 *sh = reinterpret_cast<const __half2 *>(&sv);
-            float o[8];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              o[2 * j] = v[8 * c8 + 2 * j] * kRhtScale * __low2float(sh[j]);
-              o[2 * j + 1] = v[8 * c8 + 2 * j + 1] * kRhtScale * __high2float(sh[j]);
-            }
-            if (F32OUT) {
-              float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(a.y) + (long)row * a.n + col0 + 8 * c8);
-              dst[0] = make_float4(o[0], o[1], o[2], o[3]);
-              dst[1] = make_float4(o[4], o[5], o[6], o[7]);
-            } else {
-              __half2 h[4];
-#pragma unroll
-              for (int j = 0; j < 4; ++j) h[j] = __floats2half2_rn(o[2 * j], o[2 * j + 1]);
-              *reinterpret_cast<uint4 *>(static_cast<__half *>(a.y) + (long)row * a.n + col0 + 8 * c8) =
-                  *reinterpret_cast<uint4 *>(h);
-            }
+            for (int i = 0; i < 32; ++i)
+              v[32 * c + i] = __int_as_float(__float_as_int(v[32 * c + i]) + __float2int_rn(t[i]));
           }
+          tc::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&tempty[acc]);
+          if (++acc == 2) { acc = 0; acc_phase ^= 1; }
         }
+        if (failed) {
+          if (lane == 0) set_device_error(a.err, kErrBounds);
+          *abort_flag = 1;
+          break;
+        }
+        const int col0 = nt * BN;
+        if (a.acc_out && row < a.M) {
+#pragma unroll
+          for (int c4 = 0; c4 < 32; ++c4)
+            *reinterpret_cast<int4 *>(a.acc_out + (long)row * a.n + col0 + 4 * c4) =
+                make_int4(__float_as_int(v[4 * c4]), __float_as_int(v[4 * c4 + 1]), __float_as_int(v[4 * c4 + 2]),
+                          __float_as_int(v[4 * c4 + 3]));
+        }
+#pragma unroll
+        for (int i = 0; i < 128; ++i) v[i] = (float)__float_as_int(v[i]) * rs;
+        fwht128_regs(v);
+        store_row<F32OUT>(v, a, row, col0);
+      } else {
+        bool ok = tc::mbar_wait(&tfull[acc], acc_phase);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok || *abort_flag) {
+          if (lane == 0) set_device_error(a.err, kErrBounds);
+          *abort_flag = 1;
+          break;
+        }
+        tc::tc_fence_after();
+#pragma unroll 1
+        for (int blk = 0; blk < BN / 128; ++blk) {
+          float v[128];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            float t[32];
+            tc::tmem_ld32(tmem_base + ((uint32_t)lane_base << 16) + (uint32_t)(acc * BN + blk * 128 + 32 * c), t);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[32 * c + i] = t[i];
+          }
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 128; ++i) v[i] *= rs;
+          fwht128_regs(v);
+          store_row<F32OUT>(v, a, row, nt * BN + blk * 128);
+        }
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&tempty[acc]);
+        if (++acc == 2) { acc = 0; acc_phase ^= 1; }
       }
-      tc::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&tempty[acc]);
-      if (++acc == 2) { acc = 0; acc_phase ^= 1; }
     }
   }
 
@@ -260,12 +328,14 @@ static int make_tmap_f16(CUtensorMap *m, const void *base, int rows, int cols, i
 }
 
 // n must be a multiple of 128 and k of 64; rows of x' beyond M read as zero.
+// q8: integer mode (operands integer-valued fp16, exact int32 accumulation).
 int exl3_launch_gemm_tc(const uint16_t *xh, const uint16_t *wt, int M, int n, int k, const uint16_t *svh,
-                        void *y, bool f32out, const float *row_scale, float pre, int *err, cudaStream_t s) {
+                        void *y, bool f32out, const float *row_scale, float pre, int *err, cudaStream_t s,
+                        bool q8 = false, int32_t *acc_out = nullptr) {
   CUtensorMap ta, tb;
   int rc = make_tmap_f16(&ta, xh, M, k, gtc::BM);
   if (rc) return rc;
-  const bool wide = (n % 256) == 0;
+  const bool wide = !q8 && (n % 256) == 0;
   rc = make_tmap_f16(&tb, wt, n, k, wide ? 256 : 128);
   if (rc) return rc;
   static int sms = 0;
@@ -275,19 +345,21 @@ int exl3_launch_gemm_tc(const uint16_t *xh, const uint16_t *wt, int M, int n, in
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (sms <= 0) sms = 148;
   }
-  gtc::Args a{M, n, k, reinterpret_cast<const __half *>(svh), y, row_scale, pre, err};
+  gtc::Args a{M, n, k, reinterpret_cast<const __half *>(svh), y, row_scale, pre, err, acc_out};
   const int tiles = ((M + gtc::BM - 1) / gtc::BM) * (n / (wide ? 256 : 128));
   const int grid = tiles < sms ? tiles : sms;
-#define EXL3_GTC(BNV, F32)                                                                              \
+#define EXL3_GTC(BNV, F32, Q)                                                                           \
   do {                                                                                                \
-    auto kfn = gtc::gemm_tc_kernel<BNV, F32>;                                                         \
+    auto kfn = gtc::gemm_tc_kernel<BNV, F32, Q>;                                                      \
     cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, gtc::Cfg<BNV>::SMEM_BYTES); \
     kfn<<<grid, 192, gtc::Cfg<BNV>::SMEM_BYTES, s>>>(ta, tb, a);                                      \
   } while (0)
-  if (wide) {
-    if (f32out) EXL3_GTC(256, true); else EXL3_GTC(256, false);
+  if (q8) {
+    if (f32out) EXL3_GTC(128, true, true); else EXL3_GTC(128, false, true);
+  } else if (wide) {
+    if (f32out) EXL3_GTC(256, true, false); else EXL3_GTC(256, false, false);
   } else {
-    if (f32out) EXL3_GTC(128, true); else EXL3_GTC(128, false);
+    if (f32out) EXL3_GTC(128, true, false); else EXL3_GTC(128, false, false);
   }
 #undef EXL3_GTC
   cudaError_t e = cudaGetLastError();

@@ -97,3 +97,80 @@ cudaError_t exl3_launch_output_rht(const float *yp, float pre, const uint16_t *s
   else output_rht_kernel<false><<<grid, 256, 0, s>>>(yp, pre, sh, M, n, y);
   return cudaGetLastError();
 }
+
+// ---------------------------------------------------------------------------
+// int8 activations ("exl3xpu" README, "Prefill: int8 linears and oneDNN fused
+// attention": one int8 scale per activation row, fused into the input
+// Hadamard).  One CTA per row: x' in fp32 with the butterfly order above,
+// amax over the row, inv = 127 / amax (IEEE division), q = clamp(RNE(x' inv),
+// -127, 127), a = amax / 127; an all-zero row gives q = 0, a = 0.
+// q is written as integer-valued fp16 (the tensor-core operand) and, if
+// requested, as int8.
+namespace exl3 {
+
+__global__ void __launch_bounds__(256) quant_act_kernel(const __half *__restrict__ x,
+                                                        const __half *__restrict__ suh, int k,
+                                                        __half *__restrict__ qh, int8_t *__restrict__ q8,
+                                                        float *__restrict__ row_scale) {
+  extern __shared__ __align__(16) float xr[];   // [k]
+  __shared__ float wmax[8];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const long row = blockIdx.x;
+  const int blocks = k >> 7;
+  float m = 0.f;
+  for (int b = warp; b < blocks; b += 8) {
+    const int col = b * 128 + lane * 4;
+    const uint2 xv = *reinterpret_cast<const uint2 *>(x + row * k + col);
+    const uint2 sv = *reinterpret_cast<const uint2 *>(suh + col);
+    const __half2 *xh = reinterpret_cast<const __half2 *>(&xv);
+    const __half2 *sh = reinterpret_cast<const __half2 *>(&sv);
+    float v[4] = {__low2float(xh[0]) * __low2float(sh[0]), __high2float(xh[0]) * __high2float(sh[0]),
+                  __low2float(xh[1]) * __low2float(sh[1]), __high2float(xh[1]) * __high2float(sh[1])};
+    fwht128_warp(v, lane);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[j] = __fmul_rn(v[j], kRhtScale);
+      m = fmaxf(m, fabsf(v[j]));
+    }
+    *reinterpret_cast<float4 *>(xr + col) = make_float4(v[0], v[1], v[2], v[3]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) wmax[warp] = m;
+  __syncthreads();
+  float amax = wmax[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) amax = fmaxf(amax, wmax[w]);
+  const float inv = amax > 0.f ? __fdiv_rn(127.0f, amax) : 0.f;
+  if (threadIdx.x == 0 && row_scale) row_scale[row] = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 0.f;
+  for (int i = threadIdx.x * 4; i < k; i += 256 * 4) {
+    const float4 v = *reinterpret_cast<const float4 *>(xr + i);
+    const float vv[4] = {v.x, v.y, v.z, v.w};
+    int q[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      int t = amax > 0.f ? __float2int_rn(__fmul_rn(vv[j], inv)) : 0;
+      q[j] = t > 127 ? 127 : (t < -127 ? -127 : t);
+    }
+    __half2 h[2] = {__floats2half2_rn((float)q[0], (float)q[1]), __floats2half2_rn((float)q[2], (float)q[3])};
+    *reinterpret_cast<uint2 *>(qh + row * k + i) = *reinterpret_cast<uint2 *>(h);
+    if (q8) {
+      const uint32_t packed = (uint32_t)(q[0] & 255) | ((uint32_t)(q[1] & 255) << 8) |
+                              ((uint32_t)(q[2] & 255) << 16) | ((uint32_t)(q[3] & 255) << 24);
+      *reinterpret_cast<uint32_t *>(q8 + row * k + i) = packed;
+    }
+  }
+}
+
+}  // namespace exl3
+
+cudaError_t exl3_launch_quant_act(const uint16_t *x, int M, int k, const uint16_t *suh, uint16_t *qh,
+                                  int8_t *q8, float *row_scale, cudaStream_t s) {
+  const size_t smem = sizeof(float) * (size_t)k;
+  if (smem > 48 * 1024)
+    cudaFuncSetAttribute(exl3::quant_act_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  exl3::quant_act_kernel<<<M, 256, smem, s>>>(reinterpret_cast<const __half *>(x),
+                                              reinterpret_cast<const __half *>(suh), k,
+                                              reinterpret_cast<__half *>(qh), q8, row_scale);
+  return cudaGetLastError();
+}
