@@ -39,6 +39,13 @@ _lock = threading.Lock()
 _lib = None
 
 
+class ExpertProj(ctypes.Structure):
+    """exl3_expert_proj: one projection kind for all experts (device pointers)."""
+    _fields_ = [("trellis", ctypes.c_void_p), ("suh", ctypes.c_void_p), ("svh", ctypes.c_void_p),
+                ("k", ctypes.c_int), ("n", ctypes.c_int), ("K", ctypes.c_int), ("codebook", ctypes.c_int),
+                ("nslots", ctypes.c_int)]
+
+
 class Exl3Error(RuntimeError):
     def __init__(self, code: int, msg: str):
         super().__init__(f"libexl3 error {code}: {msg}")
@@ -206,6 +213,35 @@ def exl3_linear_int8(x, trellis, suh, svh, K: int, codebook: int = EXL3_CB_MUL1,
                                   _ptr(svh, "svh", 2), K, codebook, weight_scale, _ptr(y, "y", 2),
                                   _ptr(xq_out, "xq_out", 1), _ptr(row_scale_out, "row_scale_out", 4),
                                   _ptr(acc_out, "acc_out", 4), _ptr(ws, "workspace"),
+                                  ws.numel() * ws.element_size(), _stream(stream)))
+    return y
+
+
+def expert_proj(trellis, suh, svh, K: int, codebook: int = EXL3_CB_MUL1) -> ExpertProj:
+    """Descriptor of a projection arena: trellis [E, nslots, k/16, n/16, 16K], suh [E, nslots, k],
+    svh [E, nslots, n] (CUDA tensors kept alive by the caller)."""
+    E, nslots, tk, tn, _ = trellis.shape
+    return ExpertProj(_ptr(trellis, "trellis", 2).value, _ptr(suh, "suh", 2).value, _ptr(svh, "svh", 2).value,
+                      tk * 16, tn * 16, K, codebook, nslots)
+
+
+def exl3_moe_workspace_size(T: int, topk: int, E: int, w13: ExpertProj, w2: ExpertProj) -> int:
+    return lib().exl3_moe_workspace_size(T, topk, E, ctypes.byref(w13), ctypes.byref(w2))
+
+
+def exl3_moe_grouped(x, topk_ids, topk_weights, w13: ExpertProj, w2: ExpertProj, E: int,
+                     out_dtype: int = EXL3_OUT_F16, y=None, workspace_buf=None, stream=None) -> torch.Tensor:
+    """Routed-expert contribution y [T, hidden] (gate+up, SiLU, down, weighted combine)."""
+    T, hidden = x.shape
+    topk = topk_ids.shape[1]
+    if y is None:
+        y = torch.empty((T, hidden), dtype=torch.float32 if out_dtype == EXL3_OUT_F32 else torch.float16,
+                        device=x.device)
+    need = exl3_moe_workspace_size(T, topk, E, w13, w2)
+    ws = workspace_buf if workspace_buf is not None else workspace(need, x.device, stream)
+    _check(lib().exl3_moe_grouped(_ptr(x, "x", 2), T, hidden, _ptr(topk_ids, "topk_ids", 4),
+                                  _ptr(topk_weights, "topk_weights", 4), topk, E, ctypes.byref(w13),
+                                  ctypes.byref(w2), _ptr(y, "y"), out_dtype, _ptr(ws, "workspace"),
                                   ws.numel() * ws.element_size(), _stream(stream)))
     return y
 

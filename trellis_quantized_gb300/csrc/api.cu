@@ -32,6 +32,22 @@ cudaError_t exl3_launch_reconstruct_q8_t(const uint16_t *trellis, int k, int n, 
 cudaError_t exl3_launch_gemm_mma(const uint16_t *xh, const uint16_t *wt, float *yp, int M, int n, int k,
                                  cudaStream_t s);
 
+cudaError_t exl3_launch_moe_remap(const int32_t *ids, int U, int E, int *counts, int *offsets, int *perm, int *pos,
+                                  int *active, int *mtiles, int *n_mtiles, int max_mtiles, int *err, cudaStream_t s);
+cudaError_t exl3_launch_moe_reconstruct(const uint16_t *trellis, int nslots, int k, int n, int K, const int *active,
+                                        uint16_t *arena, bool interleave, int grid, cudaStream_t s);
+cudaError_t exl3_launch_moe_gather(const uint16_t *x, int U, int hidden, int topk, const int *perm, const int *offsets,
+                                   int E, const int32_t *ids, const uint16_t *suh13, uint16_t *xg, uint16_t *xu,
+                                   cudaStream_t s);
+cudaError_t exl3_launch_moe_combine(const float *d, const int *pos, int T, int topk, int hidden, void *y,
+                                    bool f32out, cudaStream_t s);
+int exl3_launch_moe_gateup(const uint16_t *xg, const uint16_t *xu, int U, int hidden, int inter, int E,
+                           const uint16_t *w13_arena, const int *mtiles, const int *n_mtiles, int max_mtiles,
+                           const uint16_t *svh13, const uint16_t *suh2, uint16_t *hout, int *err, cudaStream_t s);
+int exl3_launch_moe_down(const uint16_t *hin, int U, int hidden, int inter, int E, const uint16_t *w2_arena,
+                         const int *mtiles, const int *n_mtiles, int max_mtiles, const uint16_t *svh2,
+                         const float *weights, const int *perm, float *dout, int *err, cudaStream_t s);
+
 // ---------------------------------------------------------------- errors --
 
 static thread_local std::string g_last_error;
@@ -160,6 +176,58 @@ LinearInt8Ws linear_int8_ws(int M, int k, int n) {
   off = align_up(off + sizeof(float) * (size_t)M);
   w.total = off;
   return w;
+}
+
+// ---- exl3_moe_grouped workspace layout
+struct MoeWs {
+  size_t counts, offsets, pos, perm, active, mtiles, n_mtiles, xg, xu, h, d, w13, w2, total;
+  int max_mtiles;
+};
+
+MoeWs moe_ws(int T, int topk, int E, int hidden, int inter) {
+  MoeWs w{};
+  const size_t U = (size_t)T * topk;
+  w.max_mtiles = (int)(U / 128 + E + 1);
+  size_t off = kDataOff;
+  auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes); return o; };
+  w.counts = take(sizeof(int) * E);
+  w.offsets = take(sizeof(int) * (E + 1));
+  w.pos = take(sizeof(int) * U);
+  w.perm = take(sizeof(int) * U);
+  w.active = take(sizeof(int) * (E + 1));
+  w.mtiles = take(sizeof(int) * 4 * (size_t)w.max_mtiles);
+  w.n_mtiles = take(sizeof(int));
+  w.xg = take(sizeof(uint16_t) * U * hidden);
+  w.xu = take(sizeof(uint16_t) * U * hidden);
+  w.h = take(sizeof(uint16_t) * U * inter);
+  w.d = take(sizeof(float) * U * hidden);
+  w.w13 = take(sizeof(uint16_t) * (size_t)E * 2 * inter * hidden);
+  w.w2 = take(sizeof(uint16_t) * (size_t)E * hidden * inter);
+  w.total = off;
+  return w;
+}
+
+int check_moe(int T, int hidden, int topk, int E, const exl3_expert_proj *w13, const exl3_expert_proj *w2) {
+  if (!w13 || !w2) return exl3_fail(EXL3_ERR_ARG, "w13 / w2 descriptor is NULL");
+  if (T < 1 || topk < 1 || E < 1 || E > 1024 || (int64_t)T * topk > (1 << 24))
+    return exl3_fail(EXL3_ERR_SHAPE, "T = %d, topk = %d, E = %d out of range (E <= 1024)", T, topk, E);
+  EXL3_TRY(check_ptr(w13->trellis, "w13.trellis"));
+  EXL3_TRY(check_ptr(w13->suh, "w13.suh"));
+  EXL3_TRY(check_ptr(w13->svh, "w13.svh"));
+  EXL3_TRY(check_ptr(w2->trellis, "w2.trellis"));
+  EXL3_TRY(check_ptr(w2->suh, "w2.suh"));
+  EXL3_TRY(check_ptr(w2->svh, "w2.svh"));
+  EXL3_TRY(check_bits_codebook(w13->K, w13->codebook));
+  EXL3_TRY(check_bits_codebook(w2->K, w2->codebook));
+  if (w13->nslots != 2 || w2->nslots != 1)
+    return exl3_fail(EXL3_ERR_SHAPE, "w13 must have nslots = 2 (gate, up) and w2 nslots = 1");
+  const int inter = w13->n;
+  if (w13->k != hidden || w2->k != inter || w2->n != hidden)
+    return exl3_fail(EXL3_ERR_SHAPE, "projection shapes do not chain: w13 %d->%d, w2 %d->%d, hidden %d",
+                     w13->k, w13->n, w2->k, w2->n, hidden);
+  if (hidden <= 0 || inter <= 0 || hidden % 256 || inter % 128)
+    return exl3_fail(EXL3_ERR_SHAPE, "hidden = %d must be a multiple of 256 and inter = %d of 128", hidden, inter);
+  return EXL3_OK;
 }
 
 int check_workspace(const void *ws, size_t have, size_t need) {
@@ -311,16 +379,53 @@ int exl3_linear_int8(const uint16_t *x, int M, int k, int n, const uint16_t *tre
 
 size_t exl3_moe_workspace_size(int T, int topk, int E, const exl3_expert_proj *w13,
                                const exl3_expert_proj *w2) {
-  (void)T; (void)topk; (void)E; (void)w13; (void)w2;
-  return 0;
+  if (!w13 || !w2 || T < 1 || topk < 1 || E < 1 || E > 1024) return 0;
+  return moe_ws(T, topk, E, w13->k, w13->n).total;
 }
 
 int exl3_moe_grouped(const uint16_t *x, int T, int hidden, const int32_t *topk_ids, const float *topk_weights,
                      int topk, int E, const exl3_expert_proj *w13, const exl3_expert_proj *w2, void *y,
                      int out_dtype, void *workspace, size_t ws_bytes, exl3_stream_t stream) {
-  (void)x; (void)T; (void)hidden; (void)topk_ids; (void)topk_weights; (void)topk; (void)E; (void)w13;
-  (void)w2; (void)y; (void)out_dtype; (void)workspace; (void)ws_bytes; (void)stream;
-  return exl3_fail(EXL3_ERR_ARG, "exl3_moe_grouped is not available in this build");
+  g_last_error.clear();
+  EXL3_TRY(check_ptr(x, "x"));
+  EXL3_TRY(check_ptr(topk_ids, "topk_ids"));
+  EXL3_TRY(check_ptr(topk_weights, "topk_weights"));
+  EXL3_TRY(check_ptr(y, "y"));
+  EXL3_TRY(check_moe(T, hidden, topk, E, w13, w2));
+  if (out_dtype != EXL3_OUT_F16 && out_dtype != EXL3_OUT_F32)
+    return exl3_fail(EXL3_ERR_ARG, "out_dtype %d invalid", out_dtype);
+  const int inter = w13->n;
+  const int U = T * topk;
+  const MoeWs L = moe_ws(T, topk, E, hidden, inter);
+  EXL3_TRY(check_workspace(workspace, ws_bytes, L.total));
+  int *err = at<int>(workspace, 0);
+  int *counts = at<int>(workspace, L.counts), *offsets = at<int>(workspace, L.offsets);
+  int *pos = at<int>(workspace, L.pos), *perm = at<int>(workspace, L.perm);
+  int *active = at<int>(workspace, L.active), *mtiles = at<int>(workspace, L.mtiles);
+  int *n_mtiles = at<int>(workspace, L.n_mtiles);
+  uint16_t *xg = at<uint16_t>(workspace, L.xg), *xu = at<uint16_t>(workspace, L.xu);
+  uint16_t *h = at<uint16_t>(workspace, L.h), *w13a = at<uint16_t>(workspace, L.w13);
+  uint16_t *w2a = at<uint16_t>(workspace, L.w2);
+  float *d = at<float>(workspace, L.d);
+  const int grid = 4 * sm_count();
+  EXL3_TRY(exl3_cuda_check(exl3_launch_moe_remap(topk_ids, U, E, counts, offsets, perm, pos, active, mtiles,
+                                                 n_mtiles, L.max_mtiles, err, stream),
+                           "moe remap launch"));
+  EXL3_TRY(exl3_cuda_check(exl3_launch_moe_reconstruct(w13->trellis, 2, hidden, inter, w13->K, active, w13a, true,
+                                                       grid, stream),
+                           "moe w13 reconstruct launch"));
+  EXL3_TRY(exl3_cuda_check(exl3_launch_moe_reconstruct(w2->trellis, 1, inter, hidden, w2->K, active, w2a, false,
+                                                       grid, stream),
+                           "moe w2 reconstruct launch"));
+  EXL3_TRY(exl3_cuda_check(exl3_launch_moe_gather(x, U, hidden, topk, perm, offsets, E, topk_ids, w13->suh, xg, xu,
+                                                  stream),
+                           "moe gather launch"));
+  EXL3_TRY(exl3_launch_moe_gateup(xg, xu, U, hidden, inter, E, w13a, mtiles, n_mtiles, L.max_mtiles, w13->svh,
+                                  w2->suh, h, err, stream));
+  EXL3_TRY(exl3_launch_moe_down(h, U, hidden, inter, E, w2a, mtiles, n_mtiles, L.max_mtiles, w2->svh, topk_weights,
+                                perm, d, err, stream));
+  return exl3_cuda_check(exl3_launch_moe_combine(d, pos, T, topk, hidden, y, out_dtype == EXL3_OUT_F32, stream),
+                         "moe combine launch");
 }
 
 }  // extern "C"
