@@ -21,6 +21,12 @@
 // LOP/SHR/PRMT where it can, hashed (IMAD), byte-summed by DP4A and
 // accumulated by one mixed-precision FMA.
 //
+// Staging.  One producer warp streams the CTA's rows (the tiles of one
+// column block at one tile row, 0.5-3.5 KB of contiguous trellis each) into
+// a ring of shared-memory stages with bulk asynchronous copies completing on
+// mbarriers; eight consumer warps decode out of shared memory.  Every wait is
+// bounded; a wait that runs out sets the device error word.
+//
 // Work split.  The work is the list of "rows" (column block c, tile row tk),
 // c-major; a column block is 128 (or 256) output columns.  A persistent grid
 // sized to the resident CTA slots takes equal contiguous ranges of that list,
@@ -45,7 +51,11 @@ struct GemvShape {
   static constexpr int WK = 8 / WC;              // k warps per CTA
   static constexpr int CTA_COLS = WC * COLW;     // 128 or 256
   static constexpr int NW = 4 * CPL;             // 32-bit stream words per lane
-  static constexpr int DEPTH = CPL == 1 ? 4 : (CPL == 3 ? 2 : 1);  // loads in flight
+  static constexpr int ROWB = CTA_COLS * 2 * K;  // bytes of one row (CTA_COLS/16 tiles of 32K bytes)
+  static constexpr int R = ROWB >= 2048 ? WK : 2 * WK;   // rows per stage (one or two per k-warp)
+  static constexpr int STAGE_B = R * ROWB;
+  static constexpr int STAGES = (32 * 1024) / STAGE_B < 2 ? 2 : (32 * 1024) / STAGE_B;
+  static constexpr int RING_B = STAGES * STAGE_B;
 };
 
 struct GemvArgs {
@@ -86,18 +96,38 @@ __device__ __forceinline__ uint32_t window_at(const uint32_t (&w)[N]) {
   }
 }
 
-template <int K>
-__device__ __forceinline__ void load_chunks(const uint4 *src, bool valid, uint32_t (&w)[GemvShape<K>::NW]) {
-  constexpr int CPL = GemvShape<K>::CPL;
-#pragma unroll
-  for (int c = 0; c < CPL; ++c) {
-    uint4 t = valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-    w[4 * c + 0] = t.x;
-    w[4 * c + 1] = t.y;
-    w[4 * c + 2] = t.z;
-    w[4 * c + 3] = t.w;
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t n) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(b)), "r"(n));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(b)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive1(uint64_t *b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(b)) : "memory");
+}
+// Bounded wait for the phase of the given parity; false if it ran out.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *b, uint32_t parity) {
+  const long long t0 = clock64();
+  while (true) {
+    uint32_t ok;
+    asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+                 : "=r"(ok)
+                 : "r"(smem_addr(b)), "r"(parity)
+                 : "memory");
+    if (ok) return true;
+    if (clock64() - t0 > 2000000000LL) return false;
   }
 }
+__device__ __forceinline__ void bulk_copy(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_addr(dst)),
+               "l"(src), "r"(bytes), "r"(smem_addr(bar))
+               : "memory");
+}
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 // Decode the lane's 16 G weights and accumulate x'_row * (1024 + B) into the
 // 16 column accumulators.
@@ -126,13 +156,17 @@ __device__ __forceinline__ int range_owner(long long r, long long total, int gri
 }
 
 template <int K, bool F32OUT>
-__global__ void __launch_bounds__(256) gemv_m1_kernel(GemvArgs a) {
+__global__ void __launch_bounds__(288) gemv_m1_kernel(GemvArgs a) {
   using S = GemvShape<K>;
-  extern __shared__ __align__(16) float smem[];
-  float *red = smem;                          // [WK][CTA_COLS]
-  float *ys = red + S::WK * S::CTA_COLS;      // [CTA_COLS]
-  __half *xs = reinterpret_cast<__half *>(ys + S::CTA_COLS);   // [k] fp16 x' (touched blocks)
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  uint8_t *ring = smem_raw;                                         // [STAGES][R][ROWB]
+  float *red = reinterpret_cast<float *>(smem_raw + S::RING_B);    // [WK][CTA_COLS]
+  float *ys = red + S::WK * S::CTA_COLS;                           // [CTA_COLS]
+  uint64_t *full = reinterpret_cast<uint64_t *>(ys + S::CTA_COLS); // [STAGES]
+  uint64_t *empty = full + S::STAGES;                              // [STAGES]
+  __half *xs = reinterpret_cast<__half *>(empty + S::STAGES);      // [k] fp16 x' (touched blocks)
   __shared__ int s_last;
+  __shared__ volatile int s_abort;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int grid = gridDim.x, me = blockIdx.x;
@@ -140,7 +174,51 @@ __global__ void __launch_bounds__(256) gemv_m1_kernel(GemvArgs a) {
   const long long t0 = range_start(me, a.total, grid), t1 = range_start(me + 1, a.total, grid);
   if (t0 >= t1) return;
 
-  // ---- prologue: x' = 2^-3.5 H (x . suh) for the 128-blocks this range touches
+  if (tid == 0) {
+    for (int st = 0; st < S::STAGES; ++st) {
+      mbar_init(&full[st], 1);
+      mbar_init(&empty[st], 8);
+    }
+    s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  if (warp == 8) {
+    // ---------------- producer: one thread streams the rows into the ring
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (long long t = t0; t < t1 && !s_abort;) {
+        const int c = (int)(t / TK);
+        const long long seg_end = min(t1, (long long)(c + 1) * TK);
+        const int tk_first = (int)(t - (long long)c * TK), nrows = (int)(seg_end - t);
+        const int tn0 = c * (S::CTA_COLS / 16);
+        const int tiles_valid = min(S::CTA_COLS / 16, tiles_n - tn0);
+        const uint32_t bytes = (uint32_t)tiles_valid * 32u * K;
+        for (int r0 = 0; r0 < nrows && !s_abort; r0 += S::R) {
+          const int cnt = min(S::R, nrows - r0);
+          if (!mbar_wait_bounded(&empty[stage], phase ^ 1)) {
+            set_device_error(a.err, kErrBounds);
+            s_abort = 1;
+            break;
+          }
+          mbar_expect_tx(&full[stage], bytes * cnt);
+          for (int j = 0; j < cnt; ++j) {
+            const long tk = tk_first + r0 + j;
+            const uint16_t *src = a.trellis + ((long)tk * tiles_n + tn0) * 16 * K;
+            bulk_copy(ring + (size_t)stage * S::STAGE_B + (size_t)j * S::ROWB, src, bytes, &full[stage]);
+          }
+          if (++stage == S::STAGES) { stage = 0; phase ^= 1; }
+        }
+        t = seg_end;
+      }
+    }
+    return;
+  }
+
+  // ---------------- consumers (warps 0..7)
+  // prologue: x' = 2^-3.5 H (x . suh) for the 128-blocks this range touches
   {
     const int KB = a.k >> 7;
     int b0 = 0, nb = KB;
@@ -165,44 +243,55 @@ __global__ void __launch_bounds__(256) gemv_m1_kernel(GemvArgs a) {
       *reinterpret_cast<uint2 *>(xs + col) = *reinterpret_cast<uint2 *>(o);
     }
   }
-  __syncthreads();
+  consumer_sync();
 
   const int wc = warp % S::WC, wk = warp / S::WC;
   const int tile_in_warp = lane / S::LPT, q = lane % S::LPT;
-  const int src_lane = (q == S::LPT - 1) ? lane - (S::LPT - 1) : lane + 1;
-  const long tile_stride = (long)tiles_n * 2 * K;        // uint4 per tile row
+  const int tile_local = wc * S::TPW + tile_in_warp;                 // tile within the row
+  const int my_off = tile_local * 32 * K + q * 16 * S::CPL;          // byte offset in a row
+  const int next_off = tile_local * 32 * K + ((q + 1) % S::LPT) * 16 * S::CPL;  // next row group (wraps)
+  int stage = 0;
+  uint32_t phase = 0;
 
   for (long long t = t0; t < t1;) {
     const int c = (int)(t / TK);
     const long long seg_end = min(t1, (long long)(c + 1) * TK);
     const int tk_first = (int)(t - (long long)c * TK), nrows = (int)(seg_end - t);
-    const int tn = c * (S::CTA_COLS / 16) + wc * S::TPW + tile_in_warp;
-    const bool valid = tn < tiles_n;
-    const uint4 *base = reinterpret_cast<const uint4 *>(a.trellis) + ((long)tk_first * tiles_n + tn) * (2 * K) +
-                        q * S::CPL;
+    const bool valid = c * (S::CTA_COLS / 16) + tile_local < tiles_n;
 
     float acc[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) acc[i] = 0.f;
     float sx = 0.f;   // sum of the x' this lane used (for the 1024 + 510 offset)
 
-    const int iters = nrows > wk ? (nrows - wk + S::WK - 1) / S::WK : 0;   // rows wk, wk + WK, ...
-    uint32_t buf[S::DEPTH][S::NW];
+    for (int r0 = 0; r0 < nrows; r0 += S::R) {
+      const int cnt = min(S::R, nrows - r0);
+      if (!s_abort && !mbar_wait_bounded(&full[stage], phase)) {
+        if (lane == 0) set_device_error(a.err, kErrBounds);
+        s_abort = 1;
+      }
+      const uint8_t *sbase = ring + (size_t)stage * S::STAGE_B;
 #pragma unroll
-    for (int d = 0; d < S::DEPTH; ++d)
-      if (d < iters) load_chunks<K>(base + (long)(wk + d * S::WK) * tile_stride, valid, buf[d]);
-    for (int it0 = 0; it0 < iters; it0 += S::DEPTH) {
-#pragma unroll
-      for (int d = 0; d < S::DEPTH; ++d) {
-        const int it = it0 + d;
-        if (it < iters) {
+      for (int jj = 0; jj < S::R / S::WK; ++jj) {
+        const int j = wk + jj * S::WK;
+        if (j < cnt) {
           uint32_t w[S::NW + 1];
+          const uint8_t *rowp = sbase + (size_t)j * S::ROWB;
+          if (valid) {
 #pragma unroll
-          for (int i = 0; i < S::NW; ++i) w[i] = buf[d][i];
-          w[S::NW] = __shfl_sync(0xffffffffu, w[0], src_lane);
-          const int nxt = it + S::DEPTH;
-          if (nxt < iters) load_chunks<K>(base + (long)(wk + nxt * S::WK) * tile_stride, valid, buf[d]);
-          const int tk = tk_first + wk + it * S::WK;
+            for (int cc = 0; cc < S::CPL; ++cc) {
+              const uint4 v4 = *reinterpret_cast<const uint4 *>(rowp + my_off + 16 * cc);
+              w[4 * cc + 0] = v4.x;
+              w[4 * cc + 1] = v4.y;
+              w[4 * cc + 2] = v4.z;
+              w[4 * cc + 3] = v4.w;
+            }
+            w[S::NW] = *reinterpret_cast<const uint32_t *>(rowp + next_off);
+          } else {
+#pragma unroll
+            for (int i = 0; i <= S::NW; ++i) w[i] = 0u;
+          }
+          const int tk = tk_first + r0 + j;
           unsigned short xr[S::G];
 #pragma unroll
           for (int i = 0; i < S::G; ++i) {
@@ -213,6 +302,9 @@ __global__ void __launch_bounds__(256) gemv_m1_kernel(GemvArgs a) {
           decode_accumulate<K, 0>(w, xr, acc);
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive1(&empty[stage]);
+      if (++stage == S::STAGES) { stage = 0; phase ^= 1; }
     }
 
     // ---- reduce: LPT lanes of a tile, then the k-warps of the CTA
@@ -227,7 +319,7 @@ __global__ void __launch_bounds__(256) gemv_m1_kernel(GemvArgs a) {
 #pragma unroll
       for (int i = 0; i < 16; ++i) red[wk * S::CTA_COLS + wc * S::COLW + tile_in_warp * 16 + i] = accf[i];
     }
-    __syncthreads();
+    consumer_sync();
     const int col0 = c * S::CTA_COLS;
     float part = 0.f;
     if (tid < S::CTA_COLS) {
@@ -242,16 +334,18 @@ __global__ void __launch_bounds__(256) gemv_m1_kernel(GemvArgs a) {
       if (tid < S::CTA_COLS) ys[tid] = part;
       finish = true;
     } else {
-      if (tid < S::CTA_COLS) a.partials[(long)(c + me) * S::CTA_COLS + tid] = part;
-      __threadfence();
-      __syncthreads();
+      if (tid < S::CTA_COLS) {
+        a.partials[(long)(c + me) * S::CTA_COLS + tid] = part;
+        __threadfence();
+      }
+      consumer_sync();
       if (tid == 0) {
         const int expected = i_last - i_first + 1;
         const int old = atomicAdd(a.counters + c, 1);
         if (old >= expected) set_device_error(a.err, kErrDirtyCounter);
         s_last = (old == expected - 1);
       }
-      __syncthreads();
+      consumer_sync();
       finish = s_last != 0;
       if (finish) {
         __threadfence();
@@ -263,7 +357,7 @@ __global__ void __launch_bounds__(256) gemv_m1_kernel(GemvArgs a) {
         if (tid == 0) a.counters[c] = 0;   // leave the workspace clean
       }
     }
-    __syncthreads();
+    consumer_sync();
 
     // ---- output transform of the block's 128-column groups
     if (finish && warp < S::CTA_COLS / 128 && col0 + warp * 128 < a.n) {
@@ -284,7 +378,7 @@ __global__ void __launch_bounds__(256) gemv_m1_kernel(GemvArgs a) {
         *reinterpret_cast<uint2 *>(static_cast<__half *>(a.y) + gc) = *reinterpret_cast<uint2 *>(o);
       }
     }
-    __syncthreads();   // red / ys are reused by the next segment
+    consumer_sync();   // red / ys are reused by the next segment
     t = seg_end;
   }
 }
@@ -292,8 +386,9 @@ __global__ void __launch_bounds__(256) gemv_m1_kernel(GemvArgs a) {
 template <int K, bool F32>
 struct Launcher {
   static size_t smem(int k) {
-    return sizeof(float) * ((size_t)GemvShape<K>::WK * GemvShape<K>::CTA_COLS + GemvShape<K>::CTA_COLS) +
-           sizeof(__half) * (size_t)k;
+    using S = GemvShape<K>;
+    return (size_t)S::RING_B + sizeof(float) * ((size_t)S::WK * S::CTA_COLS + S::CTA_COLS) +
+           sizeof(uint64_t) * 2 * S::STAGES + sizeof(__half) * (size_t)k;
   }
   static int grid(int k) {
     static int cached_k = -1, cached = 0;
@@ -303,7 +398,7 @@ struct Launcher {
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const size_t sm = smem(k);
     cudaFuncSetAttribute(gemv_m1_kernel<K, F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gemv_m1_kernel<K, F32>, 256, sm);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gemv_m1_kernel<K, F32>, 288, sm);
     cudaGetLastError();
     if (sms <= 0) sms = 152;
     if (occ <= 0) occ = 1;
@@ -314,11 +409,11 @@ struct Launcher {
   static cudaError_t launch(const GemvArgs &a, int grid, cudaStream_t s) {
     static int attr_k = -1;
     const size_t sm = smem(a.k);
-    if (attr_k != a.k && sm > 48 * 1024) {
+    if (attr_k != a.k) {
       cudaFuncSetAttribute(gemv_m1_kernel<K, F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
       attr_k = a.k;
     }
-    gemv_m1_kernel<K, F32><<<grid, 256, sm, s>>>(a);
+    gemv_m1_kernel<K, F32><<<grid, 288, sm, s>>>(a);
     return cudaGetLastError();
   }
 };
