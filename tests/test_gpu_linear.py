@@ -138,10 +138,17 @@ def test_linear_config2_small_m(M):
     _check_case(synth.config2(5120, M))
 
 
-@pytest.mark.parametrize("M", [2, 3, 31, 32, 33])
+@pytest.mark.parametrize("M", [2, 3, 31, 127, 128, 129, 200])
 def test_linear_small_m_around_path_switch(M):
-    """M = 2, 3 and 31 take the mma.sync GEMM, 32 and 33 the tcgen05 GEMM."""
+    """2 <= M <= 128 take the fused decode + tcgen05 kernel, larger M the
+    reconstruct + tcgen05 GEMM."""
     _check_case(synth.linear_case(15, M, M, 1024, 768, 4))
+
+
+@pytest.mark.parametrize("K", range(1, 9))
+def test_linear_fused_small_m_all_widths(K):
+    """Every K through the fused kernel, with a k that splits unevenly (k/64 = 18)."""
+    _check_case(synth.linear_case(16, K, 5, 1152, 384, K, outlier_rows=0.2))
 
 
 @pytest.mark.parametrize("K,M", [(2, 8), (5, 8), (8, 64), (3, 64)])

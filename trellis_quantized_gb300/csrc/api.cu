@@ -16,8 +16,6 @@ cudaError_t exl3_launch_reconstruct_t(const uint16_t *trellis, int k, int n, int
                                       cudaStream_t s);
 cudaError_t exl3_launch_input_rht(const uint16_t *x, int M, int k, const uint16_t *suh, void *out,
                                   bool f32out, cudaStream_t s);
-cudaError_t exl3_launch_output_rht(const float *yp, float pre, const uint16_t *svh, int M, int n, void *y,
-                                   bool f32out, cudaStream_t s);
 cudaError_t exl3_launch_gemv_m1(const uint16_t *x, const uint16_t *trellis, const uint16_t *suh,
                                 const uint16_t *svh, int k, int n, int K, void *y, bool f32out,
                                 float *partials, int *counters, int *err, int grid, cudaStream_t s);
@@ -29,8 +27,10 @@ cudaError_t exl3_launch_quant_act(const uint16_t *x, int M, int k, const uint16_
                                   int8_t *q8, float *row_scale, cudaStream_t s);
 cudaError_t exl3_launch_reconstruct_q8_t(const uint16_t *trellis, int k, int n, int K, uint16_t *wq,
                                          cudaStream_t s);
-cudaError_t exl3_launch_gemm_mma(const uint16_t *xh, const uint16_t *wt, float *yp, int M, int n, int k,
-                                 cudaStream_t s);
+int exl3_fused_tc_splits(int k, int n);
+int exl3_launch_fused_tc(const uint16_t *xh, const uint16_t *trellis, const uint16_t *svh, int M, int k, int n,
+                         int K, void *y, bool f32out, float *partials, int *counters, int *err, int splits,
+                         cudaStream_t s);
 
 cudaError_t exl3_launch_moe_remap(const int32_t *ids, int U, int E, int *counts, int *offsets, int *perm, int *pos,
                                   int *active, int *mtiles, int *n_mtiles, int max_mtiles, int *err, cudaStream_t s);
@@ -83,7 +83,7 @@ constexpr size_t kCtrlBytes = 256;   // device error word and reserved control w
 constexpr size_t kMaxCounters = 8192;
 constexpr size_t kCounterOff = kCtrlBytes;
 constexpr size_t kDataOff = kCounterOff + kMaxCounters * sizeof(int);
-constexpr int kTcMinM = 32;          // M >= this: tcgen05 GEMM, else the mma.sync GEMM
+constexpr int kFusedMaxM = 128;      // 2 <= M <= this: fused decode + tcgen05; above: reconstruct + tcgen05
 constexpr int kMaxGemvK = 49152;     // the M = 1 GEMV keeps x' for all of k in shared memory
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
@@ -133,8 +133,8 @@ int check_linear_shape(int M, int k, int n) {
 
 // ---- exl3_linear workspace layout
 struct LinearWs {
-  size_t ctrl = 0, counters = 0, partials = 0, xh = 0, wt = 0, yp = 0, total = 0;
-  int grid = 1;
+  size_t ctrl = 0, counters = 0, partials = 0, xh = 0, wt = 0, total = 0;
+  int grid = 1, splits = 1;
 };
 
 LinearWs linear_ws(int M, int k, int n, int K) {
@@ -146,15 +146,17 @@ LinearWs linear_ws(int M, int k, int n, int K) {
     exl3_gemv_plan(k, n, K, &w.grid, &floats);
     w.partials = off;
     off = align_up(off + sizeof(float) * floats);
+  } else if (M <= kFusedMaxM) {
+    w.xh = off;
+    off = align_up(off + sizeof(uint16_t) * (size_t)M * k);
+    w.splits = exl3_fused_tc_splits(k, n);
+    w.partials = off;
+    off = align_up(off + (w.splits > 1 ? sizeof(float) * (size_t)w.splits * M * n : 0));
   } else {
     w.xh = off;
     off = align_up(off + sizeof(uint16_t) * (size_t)M * k);
     w.wt = off;
     off = align_up(off + sizeof(uint16_t) * (size_t)k * n);
-    if (M < kTcMinM) {
-      w.yp = off;
-      off = align_up(off + sizeof(float) * (size_t)M * n);
-    }
   }
   w.total = off;
   return w;
@@ -334,13 +336,13 @@ int exl3_linear(const uint16_t *x, int M, int k, int n, const uint16_t *trellis,
                            "gemv launch");
   }
   uint16_t *xh = at<uint16_t>(workspace, L.xh);
-  uint16_t *wt = at<uint16_t>(workspace, L.wt);
-  float *yp = at<float>(workspace, L.yp);
   EXL3_TRY(exl3_cuda_check(exl3_launch_input_rht(x, M, k, suh, xh, false, stream), "input_rht launch"));
+  if (M <= kFusedMaxM)
+    return exl3_launch_fused_tc(xh, trellis, svh, M, k, n, K, y, f32, at<float>(workspace, L.partials),
+                                at<int>(workspace, L.counters), err, L.splits, stream);
+  uint16_t *wt = at<uint16_t>(workspace, L.wt);
   EXL3_TRY(exl3_cuda_check(exl3_launch_reconstruct_t(trellis, k, n, K, wt, stream), "reconstruct launch"));
-  if (M >= kTcMinM) return exl3_launch_gemm_tc(xh, wt, M, n, k, svh, y, f32, nullptr, 1.0f, err, stream);
-  EXL3_TRY(exl3_cuda_check(exl3_launch_gemm_mma(xh, wt, yp, M, n, k, stream), "gemm launch"));
-  return exl3_cuda_check(exl3_launch_output_rht(yp, 1.0f, svh, M, n, y, f32, stream), "output_rht launch");
+  return exl3_launch_gemm_tc(xh, wt, M, n, k, svh, y, f32, nullptr, 1.0f, err, stream);
 }
 
 size_t exl3_linear_int8_workspace_size(int M, int k, int n, int K) {

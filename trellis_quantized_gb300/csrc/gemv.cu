@@ -37,6 +37,7 @@
 // no waiting) adds the partials in CTA order, applies the output transform
 // and writes y: the result does not depend on timing.
 #include "exl3_common.cuh"
+#include "trellis_window.cuh"
 
 namespace exl3 {
 
@@ -78,22 +79,6 @@ __device__ __forceinline__ float fma_f16_f32(unsigned short x, uint32_t r, float
       : "+f"(acc)
       : "r"(r), "h"(x));
   return acc;
-}
-
-// 16-bit window at compile-time bit offset o of the word array w.  Windows on
-// byte offsets 0, 1, 2 of a word cost one instruction; other residues reuse a
-// word shifted by (o mod 8) bits, shared between windows of the same residue.
-template <int O, int N>
-__device__ __forceinline__ uint32_t window_at(const uint32_t (&w)[N]) {
-  constexpr int a = O & 7, base = O - a, j = base >> 5, b = base & 31;
-  if constexpr (b == 24) {
-    return __funnelshift_r(w[O >> 5], w[(O >> 5) + 1], O & 31) & 0xFFFFu;
-  } else {
-    const uint32_t src = a == 0 ? w[j] : __funnelshift_r(w[j], w[j + 1], a);
-    if constexpr (b == 0) return src & 0xFFFFu;
-    else if constexpr (b == 16) return src >> 16;
-    else return __byte_perm(src, 0u, 0x4421);   // bytes 1, 2 then zeros
-  }
 }
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {

@@ -4,8 +4,8 @@
 // 140V", section 1).
 //
 // One warp transforms one aligned 128-element block held as 4 elements per
-// lane (fwht128_warp); input side x' = 2^-3.5 H (x . suh), output side
-// y = (2^-3.5 H (pre * y')) . svh.
+// lane (fwht128_warp): x' = 2^-3.5 H (x . suh).  The output side is fused
+// into the epilogues of the GEMV and GEMM kernels.
 #include "exl3_common.cuh"
 
 namespace exl3 {
@@ -43,34 +43,6 @@ __global__ void __launch_bounds__(256) input_rht_kernel(const __half *__restrict
   }
 }
 
-// yp [M][n] fp32 (Hadamard domain, times `pre`) -> y [M][n] fp16 or fp32.
-template <bool F32OUT>
-__global__ void __launch_bounds__(256) output_rht_kernel(const float *__restrict__ yp, float pre,
-                                                         const __half *__restrict__ svh, int M, int n,
-                                                         void *__restrict__ y) {
-  const int lane = threadIdx.x & 31;
-  const long wid = (long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int blocks = n >> 7;
-  if (wid >= (long)M * blocks) return;
-  const long row = wid / blocks;
-  const int col = (int)(wid % blocks) * 128 + lane * 4;
-  const float4 a = *reinterpret_cast<const float4 *>(yp + row * n + col);
-  float v[4] = {a.x * pre, a.y * pre, a.z * pre, a.w * pre};
-  fwht128_warp(v, lane);
-  const uint2 sv = *reinterpret_cast<const uint2 *>(svh + col);
-  const __half2 *sh = reinterpret_cast<const __half2 *>(&sv);
-  v[0] = v[0] * kRhtScale * __low2float(sh[0]);
-  v[1] = v[1] * kRhtScale * __high2float(sh[0]);
-  v[2] = v[2] * kRhtScale * __low2float(sh[1]);
-  v[3] = v[3] * kRhtScale * __high2float(sh[1]);
-  if (F32OUT) {
-    *reinterpret_cast<float4 *>(static_cast<float *>(y) + row * n + col) = make_float4(v[0], v[1], v[2], v[3]);
-  } else {
-    __half2 o[2] = {__floats2half2_rn(v[0], v[1]), __floats2half2_rn(v[2], v[3])};
-    *reinterpret_cast<uint2 *>(static_cast<__half *>(y) + row * n + col) = *reinterpret_cast<uint2 *>(o);
-  }
-}
-
 }  // namespace exl3
 
 using namespace exl3;
@@ -84,17 +56,6 @@ cudaError_t exl3_launch_input_rht(const uint16_t *x, int M, int k, const uint16_
   const __half *sh = reinterpret_cast<const __half *>(suh);
   if (f32out) input_rht_kernel<true><<<grid, 256, 0, s>>>(xh, sh, M, k, out);
   else input_rht_kernel<false><<<grid, 256, 0, s>>>(xh, sh, M, k, out);
-  return cudaGetLastError();
-}
-
-cudaError_t exl3_launch_output_rht(const float *yp, float pre, const uint16_t *svh, int M, int n,
-                                   void *y, bool f32out, cudaStream_t s) {
-  const long warps = (long)M * (n / 128);
-  const unsigned grid = (unsigned)((warps + 7) / 8);
-  if (grid == 0) return cudaSuccess;
-  const __half *sh = reinterpret_cast<const __half *>(svh);
-  if (f32out) output_rht_kernel<true><<<grid, 256, 0, s>>>(yp, pre, sh, M, n, y);
-  else output_rht_kernel<false><<<grid, 256, 0, s>>>(yp, pre, sh, M, n, y);
   return cudaGetLastError();
 }
 
