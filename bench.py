@@ -299,27 +299,35 @@ def bench_prefill(args, bf16_peak, src):
 
 
 def _timed(fn, reps=10, warm=3):
+    """Device time per call: the call is captured in a CUDA graph of `reps`
+    back-to-back calls, replayed and timed with CUDA events."""
     import torch
     for _ in range(warm):
         fn()
     torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(reps):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record()
-    for _ in range(reps):
-        fn()
+    for _ in range(3):
+        g.replay()
     b.record()
     torch.cuda.synchronize()
-    return a.elapsed_time(b) / reps
+    return a.elapsed_time(b) / (3 * reps)
 
 
-def bench_extras():
+def bench_extras(only=None):
     """Small-M linears (config 2 shapes) and the grouped MoE (config 5) per call."""
     import torch
     import trellis_quantized_gb300 as tq
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16
                                      else np.ascontiguousarray(a)).cuda()
     small = {}
-    for M in (4, 16):
+    for M in ((4, 16) if only in (None, "small") else ()):
         c = synth.config2(17408, M)
         x, t, suh, svh = dev(c.x), dev(c.trellis), dev(c.suh), dev(c.svh)
         ws = tq.workspace(tq.exl3_linear_workspace_size(M, c.k, c.n, c.K))
@@ -328,7 +336,7 @@ def bench_extras():
         small[f"M{M}"] = {"ms": round(ms, 4), "GBs": round(linear_bytes(c) / (ms * 1e-3) / 1e9, 1),
                           "tflops": round(2.0 * M * c.k * c.n / (ms * 1e-3) / 1e12, 2)}
     moe = {}
-    for T in synth.CONFIG5_T:
+    for T in (synth.CONFIG5_T if only in (None, "moe") else ()):
         c = synth.config5(T)
         d = dict(x=dev(c.x), ids=dev(c.ids), w=dev(c.weights), t13=dev(c.w13.trellis), s13=dev(c.w13.suh),
                  v13=dev(c.w13.svh), t2=dev(c.w2.trellis), s2=dev(c.w2.suh), v2=dev(c.w2.svh))
@@ -337,7 +345,7 @@ def bench_extras():
         ws = tq.workspace(tq.exl3_moe_workspace_size(T, c.topk, c.E, w13, w2))
         y = torch.empty((T, c.hidden), dtype=torch.float16, device="cuda")
         ms = _timed(lambda: tq.exl3_moe_grouped(d["x"], d["ids"], d["w"], w13, w2, c.E, y=y, workspace_buf=ws),
-                    reps=5)
+                    reps=3)
         used = len(np.unique(c.ids))
         per_expert = (c.w13.trellis.nbytes + c.w2.trellis.nbytes) // c.E
         flops = 2.0 * T * c.topk * (2 * c.hidden * c.inter + c.inter * c.hidden)
@@ -401,7 +409,16 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-prefill", action="store_true")
+    ap.add_argument("--only", choices=["small", "moe", "prefill"], default=None,
+                    help="run one extra section alone and print its JSON (for profiling)")
     args = ap.parse_args()
+    if args.only:
+        import torch
+        if args.only == "prefill":
+            print(json.dumps(bench_prefill(args, *peaks()[1:])))
+        else:
+            print(json.dumps(bench_extras(args.only)))
+        return
     args.warmup = max(args.warmup, 3)
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":

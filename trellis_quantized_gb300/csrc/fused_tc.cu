@@ -5,20 +5,30 @@
 //
 //   y[m, :] = RHT_out( sigma * x'[m, :] (B - 510) ) . svh      per 128-column tile
 //
+// The MMA computes the transposed product D[n][m] = sum_k W[k][n] x'[m][k]:
+// the decoded weights are the A operand (M = 128 output columns, MN-major)
+// and x' is the narrow B operand (N = M rounded up to 16, K-major), so an
+// operand slot stays small and many fit in shared memory.
+//
 // Per CTA: one 128-column tile of y and one k-range (k splits over CTAs).
-//   warp 0     producer: TMA of the x' tile (128 rows x 64 k, rows >= M read as
-//              zero) and bulk copies of the four trellis rows (8 tiles each) of
-//              every 64-deep k step into a ring of shared-memory stages
-//   warp 1     MMA issuer: 4 x tcgen05.mma M128 N128 K16 per stage into TMEM
-//   warps 2-9  decoders: each lane cuts 16 G trellis states out of its stage
-//              chunk, hashes them (IMAD + DP4A seeded with 0x6400 gives the
-//              fp16 value 1024 + B), subtracts 1534 in half2 (exact) and stores
-//              the integers B - 510 as the MN-major, 128-byte-swizzled fp16
-//              operand (row k, 64 n per 128-byte row; 8-row k groups 2 KB
-//              apart, 64-wide n atoms 1 KB apart).  They then run the
-//              epilogue: TMEM rows to a shared scratch, the fixed-order split-k
-//              combine (last CTA to arrive, no waiting) and a warp-level
-//              FWHT-128 per token row.
+//   warp 0       trellis producer: bulk copies of the four trellis rows (8
+//                tiles each) of every 64-deep k step into a deep ring
+//   warp 1       MMA issuer: 4 x tcgen05.mma M128 N(M) K16 per step into TMEM
+//   warp 2       operand producer: TMA of the x' tile (M rows x 64 k) into the
+//                operand ring
+//   warps 3-18   decoders, two groups of eight taking alternate k steps: each
+//                lane cuts 16 G trellis states out of its chunk, hashes them
+//                (IMAD + DP4A seeded with 0x6400 gives the fp16 value
+//                1024 + B), subtracts 1534 in half2 (exact) and stores the
+//                integers B - 510 as the MN-major, 128-byte-swizzled fp16
+//                operand (row k, 64 n per 128-byte row; 8-row k groups 2 KB
+//                apart, 64-wide n atoms 1 KB apart).  The lane-to-chunk
+//                mapping keeps both the 16-byte chunk loads and the swizzled
+//                stores free of bank conflicts where the width allows.  The
+//                decoders then run the epilogue: the TMEM accumulator
+//                (lane = output column, column = token) transposed into a
+//                shared scratch, the fixed-order split-k combine (last CTA to
+//                arrive, no waiting) and a warp-level FWHT-128 per token row.
 // Every wait is bounded and reports through the device error word.
 #include <cudaTypedefs.h>
 
@@ -29,20 +39,26 @@
 namespace exl3 {
 namespace ftc {
 
-constexpr int BM = 128, BN = 128, BK = 64;
-constexpr int A_BYTES = BM * BK * 2, B_BYTES = BK * BN * 2;
-constexpr int NDEC = 8;   // decoder warps
+constexpr int BN = 128, BK = 64;             // output columns per CTA, k per step
+constexpr int W_BYTES = BK * BN * 2;         // decoded weight operand of one step
+constexpr int NGRP = 2;   // decoder groups (alternate k steps)
+constexpr int NDEC = 8;   // decoder warps per group
+constexpr int NWARPS = 3 + NGRP * NDEC;
 
-template <int K>
+template <int K, int NMAX>
 struct Shape {
   static constexpr int G = 8 / gcd_c(K, 8);      // rows per lane item
   static constexpr int CPL = K / gcd_c(K, 8);    // 16-byte chunks per item
   static constexpr int LPT = 16 / G;             // items per tile
   static constexpr int ROWB = (BN / 16) * 32 * K;   // one tile row of the CTA: 8 tiles
   static constexpr int T_BYTES = 4 * ROWB;          // 4 tile rows per 64-deep k step
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + T_BYTES;
-  static constexpr int STAGES = 3;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 1024;
+  static constexpr int X_BYTES = NMAX * BK * 2;     // x' operand of one step (up to NMAX tokens)
+  static constexpr int WS = 4;                      // decoded-weight ring depth
+  static constexpr int XS = NMAX <= 32 ? 16 : 4;    // x' ring depth (runs ahead of the MMA)
+  // trellis ring: the shared memory the two operand rings leave
+  static constexpr int TS_FIT = (220 * 1024 - WS * W_BYTES - XS * X_BYTES) / T_BYTES;
+  static constexpr int TS = TS_FIT > 32 ? 32 : TS_FIT;
+  static constexpr int SMEM_BYTES = WS * W_BYTES + XS * X_BYTES + TS * T_BYTES + 1024 + 1024;
   static constexpr int ITEMS = 32 * LPT;         // (tile, group) items per stage
   static constexpr int NW = 4 * CPL;
 };
@@ -59,8 +75,8 @@ __device__ __forceinline__ uint64_t sdesc_mn_sw128(const void *base, uint32_t lb
   return d;
 }
 
-__host__ __device__ constexpr uint32_t idesc_f16_bmn(int M, int N) {
-  return tc::idesc_f16(M, N) | (1u << 16);   // B is MN-major
+__host__ __device__ constexpr uint32_t idesc_f16_amn(int M, int N) {
+  return tc::idesc_f16(M, N) | (1u << 15);   // A is MN-major
 }
 
 struct Args {
@@ -83,7 +99,7 @@ __device__ __forceinline__ void bulk_copy(void *dst, const void *src, uint32_t b
 // Two adjacent weights (columns C, C + 1 of row R) as the half2 (B0 - 510, B1 - 510):
 // DP4A seeded with 0x6400 gives the fp16 bits of 1024 + B; 1024 + B - 1534 is exact.
 template <int K, int R, int C>
-__device__ __forceinline__ uint32_t decode_pair(const uint32_t (&w)[Shape<K>::NW + 1]) {
+__device__ __forceinline__ uint32_t decode_pair(const uint32_t (&w)[Shape<K, 32>::NW + 1]) {
   const uint32_t s0 = window_at<(16 * R + C) * K>(w), s1 = window_at<(16 * R + C + 1) * K>(w);
   const uint32_t h0 = __dp4a(s0 * kMul1, 0x01010101u, 0x6400u);
   const uint32_t h1 = __dp4a(s1 * kMul1, 0x01010101u, 0x6400u);
@@ -95,9 +111,9 @@ __device__ __forceinline__ uint32_t decode_pair(const uint32_t (&w)[Shape<K>::NW
 // Decode one (tile, row group) item: rows G q .. G q + G - 1 of the tile,
 // 16 columns each, into the operand stage.
 template <int K, int R>
-__device__ __forceinline__ void decode_rows(const uint32_t (&w)[Shape<K>::NW + 1], uint8_t *bstage, int k0,
-                                            int nn0) {
-  if constexpr (R < Shape<K>::G) {
+__device__ __forceinline__ void decode_rows(const uint32_t (&w)[Shape<K, 32>::NW + 1], uint8_t *bstage, int k0,
+                                            int nn0, int swap) {
+  if constexpr (R < Shape<K, 32>::G) {
     const uint4 lo = make_uint4(decode_pair<K, R, 0>(w), decode_pair<K, R, 2>(w), decode_pair<K, R, 4>(w),
                                 decode_pair<K, R, 6>(w));
     const uint4 hi = make_uint4(decode_pair<K, R, 8>(w), decode_pair<K, R, 10>(w), decode_pair<K, R, 12>(w),
@@ -106,48 +122,92 @@ __device__ __forceinline__ void decode_rows(const uint32_t (&w)[Shape<K>::NW + 1
     const int kg = kk >> 3, kr = kk & 7;
     const int na = nn0 >> 6, ch = (nn0 & 63) >> 3;  // 16 columns = chunks ch, ch + 1 of a 64-wide atom
     uint8_t *row = bstage + kg * 2048 + na * 1024 + kr * 128;
-    *reinterpret_cast<uint4 *>(row + ((ch ^ kr) << 4)) = lo;
-    *reinterpret_cast<uint4 *>(row + (((ch + 1) ^ kr) << 4)) = hi;
-    decode_rows<K, R + 1>(w, bstage, k0, nn0);
+    if (swap) {
+      *reinterpret_cast<uint4 *>(row + (((ch + 1) ^ kr) << 4)) = hi;
+      *reinterpret_cast<uint4 *>(row + ((ch ^ kr) << 4)) = lo;
+    } else {
+      *reinterpret_cast<uint4 *>(row + ((ch ^ kr) << 4)) = lo;
+      *reinterpret_cast<uint4 *>(row + (((ch + 1) ^ kr) << 4)) = hi;
+    }
+    decode_rows<K, R + 1>(w, bstage, k0, nn0, swap);
   }
 }
 
-template <int K, bool F32OUT>
-__global__ void __launch_bounds__(320, 2) fused_tc_kernel(const __grid_constant__ CUtensorMap tmA, Args a) {
-  using S = Shape<K>;
-  constexpr int STAGES = S::STAGES;
+// Item -> (tile 0..31 of the step, row group q, which chunk is stored first).
+// 32 consecutive items form one warp instruction; each 8-lane phase should
+// touch 8 distinct 16-byte bank groups for the chunk loads and the stores.
+template <int K>
+__device__ __forceinline__ void item_map(int it, int &ti, int &q, int &swap) {
+  constexpr int LPT = Shape<K, 32>::LPT;
+  if constexpr (LPT == 8) {
+    // two tiles per phase pair: lanes 0-3 of a phase take groups 0-3 of one
+    // tile, lanes 4-7 groups 4-7 of the other; the halves store opposite
+    // chunk parities first
+    const int w = it >> 5, l = it & 31, p = l >> 3, i = l & 7;
+    ti = w * 4 + 2 * (p >> 1) + ((i >> 2) ^ (p & 1));
+    q = i;
+    swap = i >> 2;
+  } else if constexpr (LPT == 2) {
+    // tiles fastest (8 per phase), the second half of the phase stores the odd chunk first
+    const int w = it >> 5, l = it & 31, p = l >> 3, i = l & 7;
+    ti = (w * 16) + ((p & 1) << 3) + i;
+    q = p >> 1;
+    swap = i >> 2;
+  } else {
+    ti = it / LPT;
+    q = it % LPT;
+    swap = 0;
+  }
+}
+
+template <int K, bool F32OUT, int NMAX>
+__global__ void __launch_bounds__(NWARPS * 32, 1) fused_tc_kernel(const __grid_constant__ CUtensorMap tmX, Args a) {
+  using S = Shape<K, NMAX>;
+  constexpr int WS = S::WS, XS = S::XS, TS = S::TS;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = tc::smem_u32(smem_raw);
   uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  uint8_t *sA = smem;                                   // [STAGES][A_BYTES]
-  uint8_t *sB = smem + STAGES * A_BYTES;                // [STAGES][B_BYTES]
-  uint8_t *sT = sB + STAGES * B_BYTES;                  // [STAGES][T_BYTES]
-  uint64_t *full = reinterpret_cast<uint64_t *>(sT + STAGES * S::T_BYTES);
-  uint64_t *bfull = full + STAGES;
-  uint64_t *empty = bfull + STAGES;
-  uint64_t *tfull = empty + STAGES;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tfull + 1);
+  uint8_t *sW = smem;                                   // [WS][W_BYTES] decoded weights (A operand)
+  uint8_t *sX = smem + WS * W_BYTES;                    // [XS][X_BYTES] x' rows (B operand)
+  uint8_t *sT = sX + XS * S::X_BYTES;                   // [TS][T_BYTES]
+  uint64_t *tfull = reinterpret_cast<uint64_t *>(sT + TS * S::T_BYTES);   // [TS] trellis landed
+  uint64_t *tempty = tfull + TS;                        // [TS] trellis decoded
+  uint64_t *xfull = tempty + TS;                        // [XS] x' tile landed
+  uint64_t *xempty = xfull + XS;                        // [XS] MMA done with the x' slot
+  uint64_t *wfull = xempty + XS;                        // [WS] weights decoded
+  uint64_t *wempty = wfull + WS;                        // [WS] MMA done with the weight slot
+  uint64_t *accum = wempty + WS;                        // accumulator complete
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accum + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   int *s_last = const_cast<int *>(abort_flag + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nt = blockIdx.x, split = blockIdx.y;
-  const int kb0 = split * a.kb_per_split, nkb = a.kb_per_split;
+  const int kb0 = (int)((long)split * (a.k / BK) / a.splits);
+  const int nkb = (int)((long)(split + 1) * (a.k / BK) / a.splits) - kb0;
   const int tn0 = nt * (BN / 16);
+  const int npad = (a.M + 15) & ~15;                    // MMA N: tokens rounded up to 16
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      tc::mbar_init(&full[s], 1);
-      tc::mbar_init(&bfull[s], NDEC);
-      tc::mbar_init(&empty[s], 1);
+    for (int s = 0; s < TS; ++s) {
+      tc::mbar_init(&tfull[s], 1);
+      tc::mbar_init(&tempty[s], NDEC);
     }
-    tc::mbar_init(tfull, 1);
+    for (int s = 0; s < XS; ++s) {
+      tc::mbar_init(&xfull[s], 1);
+      tc::mbar_init(&xempty[s], 1);
+    }
+    for (int s = 0; s < WS; ++s) {
+      tc::mbar_init(&wfull[s], NDEC);
+      tc::mbar_init(&wempty[s], 1);
+    }
+    tc::mbar_init(accum, 1);
     *abort_flag = 0;
     tc::fence_mbar_init();
-    tc::prefetch_tmap(&tmA);
+    tc::prefetch_tmap(&tmX);
   }
   if (warp == 1) {
-    tc::tmem_alloc(tmem_slot, 128);
+    tc::tmem_alloc(tmem_slot, NMAX);
     tc::tmem_relinquish();
   }
   tc::tc_fence_before();
@@ -156,65 +216,78 @@ __global__ void __launch_bounds__(320, 2) fused_tc_kernel(const __grid_constant_
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
+    // ---------------- trellis producer
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
       for (int i = 0; i < nkb && !*abort_flag; ++i) {
-        const int kb = kb0 + i;
-        if (!tc::mbar_wait(&empty[stage], phase ^ 1)) {
+        const int st = i % TS;
+        if (!tc::mbar_wait(&tempty[st], ((i / TS) & 1) ^ 1)) {
           set_device_error(a.err, kErrBounds);
           *abort_flag = 1;
           break;
         }
-        tc::mbar_arrive_expect_tx(&full[stage], A_BYTES + S::T_BYTES);
-        tc::tma_load_2d(sA + stage * A_BYTES, &tmA, &full[stage], kb * BK, 0);
+        tc::mbar_arrive_expect_tx(&tfull[st], S::T_BYTES);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const long tk = (long)kb * 4 + j;
-          bulk_copy(sT + stage * S::T_BYTES + j * S::ROWB, a.trellis + (tk * a.tiles_n + tn0) * 16 * K, S::ROWB,
-                    &full[stage]);
+          const long tk = (long)(kb0 + i) * 4 + j;
+          bulk_copy(sT + st * S::T_BYTES + j * S::ROWB, a.trellis + (tk * a.tiles_n + tn0) * 16 * K, S::ROWB,
+                    &tfull[st]);
         }
-        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+      }
+    }
+  } else if (warp == 2) {
+    // ---------------- x' operand producer
+    if (lane == 0) {
+      for (int i = 0; i < nkb && !*abort_flag; ++i) {
+        const int st = i % XS;
+        if (!tc::mbar_wait(&xempty[st], ((i / XS) & 1) ^ 1)) {
+          set_device_error(a.err, kErrBounds);
+          *abort_flag = 1;
+          break;
+        }
+        tc::mbar_arrive_expect_tx(&xfull[st], (uint32_t)npad * BK * 2);
+        tc::tma_load_2d(sX + st * S::X_BYTES, &tmX, &xfull[st], (kb0 + i) * BK, 0);
       }
     }
   } else if (warp == 1) {
+    // ---------------- MMA issuer
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      for (int i = 0; i < nkb && ok; ++i) {
-        ok = tc::mbar_wait(&full[stage], phase) && tc::mbar_wait(&bfull[stage], phase);
+      for (int i = 0; i < nkb; ++i) {
+        const int xs = i % XS, ws = i % WS;
+        const bool ok = tc::mbar_wait(&xfull[xs], (i / XS) & 1) && tc::mbar_wait(&wfull[ws], (i / WS) & 1);
         if (!ok || *abort_flag) {
           set_device_error(a.err, kErrBounds);
           *abort_flag = 1;
           break;
         }
         tc::tc_fence_after();
-        const uint64_t ad = tc::sdesc_k_sw128(sA + stage * A_BYTES);
-        const uint64_t bd = sdesc_mn_sw128(sB + stage * B_BYTES, 1024, 2048);
+        const uint64_t ad = sdesc_mn_sw128(sW + ws * W_BYTES, 1024, 2048);
+        const uint64_t bd = tc::sdesc_k_sw128(sX + xs * S::X_BYTES);
+        const uint32_t idesc = idesc_f16_amn(BN, npad);
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
-          tc::mma_f16(tmem_base, ad + 2 * kk, bd + (uint64_t)((2 * 2048 * kk) >> 4), idesc_f16_bmn(BM, BN),
-                      (i | kk) != 0 ? 1u : 0u);
-        tc::mma_commit(&empty[stage]);
-        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+          tc::mma_f16(tmem_base, ad + (uint64_t)((2 * 2048 * kk) >> 4), bd + 2 * kk, idesc, (i | kk) != 0 ? 1u : 0u);
+        tc::mma_commit(&wempty[ws]);
+        tc::mma_commit(&xempty[xs]);
       }
-      tc::mma_commit(tfull);
+      tc::mma_commit(accum);
     }
   } else {
-    // ---------------- decoders (warps 2..9)
-    const int dt = threadIdx.x - 64;   // 0..255
-    int stage = 0;
-    uint32_t phase = 0;
-    for (int i = 0; i < nkb; ++i) {
-      if (!*abort_flag && !tc::mbar_wait(&full[stage], phase)) {
+    // ---------------- decoders: group g takes k steps i = g, g + 2, ...
+    const int dw = warp - 3;                 // 0..15
+    const int grp = dw / NDEC, dt = (dw % NDEC) * 32 + lane;
+    for (int i = grp; i < nkb; i += NGRP) {
+      const int ts = i % TS, bs = i % WS;
+      const bool ok = (*abort_flag) || (tc::mbar_wait(&tfull[ts], (i / TS) & 1) &&
+                                        tc::mbar_wait(&wempty[bs], ((i / WS) & 1) ^ 1));
+      if (!ok) {
         if (lane == 0) set_device_error(a.err, kErrBounds);
         *abort_flag = 1;
       }
-      const uint8_t *tst = sT + stage * S::T_BYTES;
-      uint8_t *bst = sB + stage * B_BYTES;
+      const uint8_t *tst = sT + ts * S::T_BYTES;
+      uint8_t *bst = sW + bs * W_BYTES;
       for (int it = dt; it < S::ITEMS; it += NDEC * 32) {
-        const int ti = it / S::LPT, q = it % S::LPT;
+        int ti, q, swp;
+        item_map<K>(it, ti, q, swp);
         const int tkl = ti >> 3, tnl = ti & 7;
         const uint8_t *tile = tst + tkl * S::ROWB + tnl * 32 * K;
         uint32_t w[S::NW + 1];
@@ -227,68 +300,66 @@ __global__ void __launch_bounds__(320, 2) fused_tc_kernel(const __grid_constant_
           w[4 * cc + 3] = v4.w;
         }
         w[S::NW] = *reinterpret_cast<const uint32_t *>(tile + ((q + 1) % S::LPT) * 16 * S::CPL);
-        decode_rows<K, 0>(w, bst, tkl * 16 + S::G * q, tnl * 16);
+        decode_rows<K, 0>(w, bst, tkl * 16 + S::G * q, tnl * 16, swp);
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic stores -> tensor-core reads
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&bfull[stage]);
-      if (++stage == STAGES) { stage = 0; phase ^= 1; }
+      if (lane == 0) {
+        tc::mbar_arrive(&wfull[bs]);
+        tc::mbar_arrive(&tempty[ts]);
+      }
     }
 
     // ---------------- epilogue
-    // (1) warps 2..5 (TMEM lanes 64-95, 96-127, 0-31, 32-63) copy the valid
-    // token rows, times sigma, into a scratch [M][128] fp32 that reuses the
-    // operand ring (free once every MMA has completed).
+    // (1) warps 3..6 (TMEM lanes 96-127, 0-31, 32-63, 64-95 = output columns)
+    // write the accumulator, times sigma, transposed into a scratch [M][128]
+    // fp32 that reuses the operand ring (free once every MMA has completed).
     float *scratch = reinterpret_cast<float *>(smem);
-    {
-      bool ok = true;
-      if (warp < 6) {
-        ok = tc::mbar_wait(tfull, 0);
-        ok = __all_sync(0xffffffffu, ok) && !*abort_flag;
-        if (!ok && lane == 0) set_device_error(a.err, kErrBounds);
-        tc::tc_fence_after();
-        const int lane_base = 32 * (warp & 3);
-        const int m = lane_base + lane;
+    if (warp < 7) {
+      bool ok = tc::mbar_wait(accum, 0);
+      ok = __all_sync(0xffffffffu, ok) && !*abort_flag;
+      if (!ok && lane == 0) set_device_error(a.err, kErrBounds);
+      tc::tc_fence_after();
+      const int lane_base = 32 * (warp & 3);
+      const int ncol = lane_base + lane;
+      for (int m0 = 0; m0 < a.M; m0 += 8) {
+        uint32_t r[8];
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                     : "r"(tmem_base + ((uint32_t)lane_base << 16) + (uint32_t)m0));
+        tc::tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float t[32];
-          tc::tmem_ld32(tmem_base + ((uint32_t)lane_base << 16) + 32 * c, t);
-          tc::tmem_ld_wait();
-          if (m < a.M) {
-#pragma unroll
-            for (int j = 0; j < 32; j += 4)
-              *reinterpret_cast<float4 *>(scratch + m * 128 + 32 * c + j) =
-                  make_float4(t[j] * kSigma, t[j + 1] * kSigma, t[j + 2] * kSigma, t[j + 3] * kSigma);
-          }
-        }
-        tc::tc_fence_before();
+        for (int j = 0; j < 8; ++j)
+          if (m0 + j < a.M) scratch[(m0 + j) * 128 + ncol] = __uint_as_float(r[j]) * kSigma;
       }
+      tc::tc_fence_before();
     }
-    asm volatile("bar.sync 1, 256;" ::: "memory");   // the eight decoder warps
+    asm volatile("bar.sync 1, %0;" ::"n"(NGRP * NDEC * 32) : "memory");   // all decoder warps
     const int col0 = nt * BN;
-    const int ew = warp - 2;                          // 0..7
+    const int ew = dw;                                // 0..15
+    constexpr int NEW = NGRP * NDEC;
     bool finish = true;
     if (a.splits > 1) {
       // (2) partial sums of this split; the last CTA of the column tile adds all
       // splits in order.
-      for (int m = ew; m < a.M; m += NDEC) {
+      for (int m = ew; m < a.M; m += NEW) {
         const float4 v = *reinterpret_cast<const float4 *>(scratch + m * 128 + 4 * lane);
         *reinterpret_cast<float4 *>(a.partials + ((long)split * a.M + m) * a.n + col0 + 4 * lane) = v;
       }
       __threadfence();
-      asm volatile("bar.sync 1, 256;" ::: "memory");
-      if (threadIdx.x == 64) {
+      asm volatile("bar.sync 1, %0;" ::"n"(NEW * 32) : "memory");
+      if (dw == 0 && lane == 0) {
         const int old = atomicAdd(a.counters + nt, 1);
         if (old >= a.splits) set_device_error(a.err, kErrDirtyCounter);
         *s_last = (old == a.splits - 1);
       }
-      asm volatile("bar.sync 1, 256;" ::: "memory");
+      asm volatile("bar.sync 1, %0;" ::"n"(NEW * 32) : "memory");
       finish = *s_last != 0;
       if (finish) __threadfence();
     }
     // (3) one warp per token row: sum the splits, FWHT-128, 2^-3.5, svh, store
     if (finish) {
-      for (int m = ew; m < a.M; m += NDEC) {
+      for (int m = ew; m < a.M; m += NEW) {
         float v[4];
         if (a.splits > 1) {
           float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -320,7 +391,7 @@ __global__ void __launch_bounds__(320, 2) fused_tc_kernel(const __grid_constant_
           *reinterpret_cast<uint2 *>(static_cast<__half *>(a.y) + (long)m * a.n + gc) = *reinterpret_cast<uint2 *>(o);
         }
       }
-      if (a.splits > 1 && threadIdx.x == 64) a.counters[nt] = 0;   // leave the workspace clean
+      if (a.splits > 1 && dw == 0 && lane == 0) a.counters[nt] = 0;   // leave the workspace clean
     }
   }
 
@@ -328,7 +399,7 @@ __global__ void __launch_bounds__(320, 2) fused_tc_kernel(const __grid_constant_
   __syncthreads();
   if (warp == 1) {
     tc::tc_fence_after();
-    tc::tmem_dealloc(tmem_base, 128);
+    tc::tmem_dealloc(tmem_base, NMAX);
   }
 }
 
@@ -350,7 +421,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 ftc_tmap_fn() {
   return fn;
 }
 
-// Number of k splits: the smallest divisor of k/64 giving at least 2 CTAs per SM.
+// Number of k splits (one CTA per SM): the split count whose CTAs fill whole
+// waves best, keeping at least 16 k steps of 64 per CTA (fewer on ties).
 int exl3_fused_tc_splits(int k, int n) {
   static int sms = 0;
   if (!sms) {
@@ -360,11 +432,16 @@ int exl3_fused_tc_splits(int k, int n) {
     cudaGetLastError();
   }
   const int kb = k / 64, tiles = n / 128;
-  int best = kb;
-  for (int s = 1; s <= kb; ++s) {
-    if (kb % s) continue;
-    best = s;
-    if (tiles * s >= 2 * sms) break;
+  int best = 1;
+  double best_eff = 0.0;
+  for (int s = 1; s <= kb && (s == 1 || kb / s >= 16); ++s) {
+    const long ctas = (long)tiles * s;
+    const long waves = (ctas + sms - 1) / sms;
+    const double eff = (double)ctas / (double)(waves * sms);
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      best = s;
+    }
   }
   return best;
 }
@@ -378,25 +455,32 @@ int exl3_launch_fused_tc(const uint16_t *xh, const uint16_t *trellis, const uint
   CUtensorMap ta;
   cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)M};
   cuuint64_t strides[1] = {(cuuint64_t)k * 2};
-  cuuint32_t box[2] = {64, 128};
+  const int npad = (M + 15) & ~15;
+  cuuint32_t box[2] = {64, (cuuint32_t)npad};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t *>(xh), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return exl3_fail(EXL3_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
   ftc::Args a{trellis, reinterpret_cast<const __half *>(svh), y, partials, counters, err, M, k, n, n / 16,
-              (k / 64) / splits, splits};
+              0, splits};
   dim3 grid(n / 128, splits);
   cudaError_t e = cudaSuccess;
-#define EXL3_FTC(KK, F32)                                                                                    \
+#define EXL3_FTC(KK, F32, NM)                                                                                \
   do {                                                                                                      \
-    auto kfn = ftc::fused_tc_kernel<KK, F32>;                                                               \
-    cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, ftc::Shape<KK>::SMEM_BYTES);      \
-    kfn<<<grid, 320, ftc::Shape<KK>::SMEM_BYTES, s>>>(ta, a);                                               \
+    auto kfn = ftc::fused_tc_kernel<KK, F32, NM>;                                                           \
+    cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, ftc::Shape<KK, NM>::SMEM_BYTES);  \
+    kfn<<<grid, ftc::NWARPS * 32, ftc::Shape<KK, NM>::SMEM_BYTES, s>>>(ta, a);                              \
     e = cudaGetLastError();                                                                                 \
   } while (0)
-#define EXL3_FTC_K(KK) \
-  case KK: if (f32out) EXL3_FTC(KK, true); else EXL3_FTC(KK, false); break;
+#define EXL3_FTC_K(KK)                                          \
+  case KK:                                                      \
+    if (npad <= 32) {                                           \
+      if (f32out) EXL3_FTC(KK, true, 32); else EXL3_FTC(KK, false, 32); \
+    } else {                                                    \
+      if (f32out) EXL3_FTC(KK, true, 128); else EXL3_FTC(KK, false, 128); \
+    }                                                           \
+    break;
   switch (K) {
     EXL3_FTC_K(1) EXL3_FTC_K(2) EXL3_FTC_K(3) EXL3_FTC_K(4) EXL3_FTC_K(5) EXL3_FTC_K(6) EXL3_FTC_K(7)
     EXL3_FTC_K(8)
