@@ -320,7 +320,7 @@ def _timed(fn, reps=10, warm=3):
     return a.elapsed_time(b) / (3 * reps)
 
 
-def bench_extras(only=None):
+def bench_extras(only=None, moe_tokens=None):
     """Small-M linears (config 2 shapes) and the grouped MoE (config 5) per call."""
     import torch
     import trellis_quantized_gb300 as tq
@@ -336,7 +336,7 @@ def bench_extras(only=None):
         small[f"M{M}"] = {"ms": round(ms, 4), "GBs": round(linear_bytes(c) / (ms * 1e-3) / 1e9, 1),
                           "tflops": round(2.0 * M * c.k * c.n / (ms * 1e-3) / 1e12, 2)}
     moe = {}
-    for T in (synth.CONFIG5_T if only in (None, "moe") else ()):
+    for T in ((moe_tokens or synth.CONFIG5_T) if only in (None, "moe") else ()):
         c = synth.config5(T)
         d = dict(x=dev(c.x), ids=dev(c.ids), w=dev(c.weights), t13=dev(c.w13.trellis), s13=dev(c.w13.suh),
                  v13=dev(c.w13.svh), t2=dev(c.w2.trellis), s2=dev(c.w2.suh), v2=dev(c.w2.svh))
@@ -354,8 +354,9 @@ def bench_extras(only=None):
                         "tflops": round(flops / (ms * 1e-3) / 1e12, 2)}
         del d
     return {"small_m_k5120_n17408": small, "moe_E256_top8_h2048_i512_K3": moe,
-            "note": "small M: reconstruct + mma.sync/tcgen05 two-phase; MoE: remap + active-expert reconstruct + "
-                    "two grouped tcgen05 GEMMs + combine"}
+            "note": "small M: trellis decoded into tcgen05 operands (one fused kernel after the input RHT); "
+                    "MoE: device remap + gather/RHT + two grouped tcgen05 kernels decoding the experts' trellis "
+                    "on the fly + fixed-order combine"}
 
 
 # ------------------------------------------------------------------------- oracle
@@ -411,13 +412,15 @@ def main():
     ap.add_argument("--skip-prefill", action="store_true")
     ap.add_argument("--only", choices=["small", "moe", "prefill"], default=None,
                     help="run one extra section alone and print its JSON (for profiling)")
+    ap.add_argument("--moe-tokens", type=int, nargs="*", default=None,
+                    help="token counts of the MoE section (default: all of the MoE workload's)")
     args = ap.parse_args()
     if args.only:
         import torch
         if args.only == "prefill":
             print(json.dumps(bench_prefill(args, *peaks()[1:])))
         else:
-            print(json.dumps(bench_extras(args.only)))
+            print(json.dumps(bench_extras(args.only, args.moe_tokens)))
         return
     args.warmup = max(args.warmup, 3)
     rank = int(os.environ.get("RANK", "0"))

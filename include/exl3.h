@@ -156,7 +156,9 @@ int exl3_linear_int8(const uint16_t *x, int M, int k, int n,
  *   with the routing weight applied to the down output, in fp32.  Token to
  *   expert binning happens on the device; there is no host synchronisation.
  *   Expert ids outside [0, E) are recorded in the device error word and the
- *   unit is skipped.
+ *   unit is skipped.  Expert weights are decoded from the trellis inside the
+ *   two grouped tensor-core launches; the workspace holds only routing
+ *   tables and per-row activations (T * topk rows of hidden and inter).
  */
 typedef struct {
   const uint16_t *trellis;  /* [E][nslots][k/16][n/16][16*K] */

@@ -33,20 +33,19 @@ int exl3_launch_fused_tc(const uint16_t *xh, const uint16_t *trellis, const uint
                          cudaStream_t s);
 
 cudaError_t exl3_launch_moe_remap(const int32_t *ids, int U, int E, int *counts, int *offsets, int *perm, int *pos,
-                                  int *active, int *mtiles, int *n_mtiles, int max_mtiles, int *err, cudaStream_t s);
-cudaError_t exl3_launch_moe_reconstruct(const uint16_t *trellis, int nslots, int k, int n, int K, const int *active,
-                                        uint16_t *arena, bool interleave, int grid, cudaStream_t s);
+                                  int *mtiles, int *n_mtiles, int max_mtiles, int *err, cudaStream_t s);
 cudaError_t exl3_launch_moe_gather(const uint16_t *x, int U, int hidden, int topk, const int *perm, const int *offsets,
                                    int E, const int32_t *ids, const uint16_t *suh13, uint16_t *xg, uint16_t *xu,
                                    cudaStream_t s);
 cudaError_t exl3_launch_moe_combine(const float *d, const int *pos, int T, int topk, int hidden, void *y,
                                     bool f32out, cudaStream_t s);
-int exl3_launch_moe_gateup(const uint16_t *xg, const uint16_t *xu, int U, int hidden, int inter, int E,
-                           const uint16_t *w13_arena, const int *mtiles, const int *n_mtiles, int max_mtiles,
-                           const uint16_t *svh13, const uint16_t *suh2, uint16_t *hout, int *err, cudaStream_t s);
-int exl3_launch_moe_down(const uint16_t *hin, int U, int hidden, int inter, int E, const uint16_t *w2_arena,
-                         const int *mtiles, const int *n_mtiles, int max_mtiles, const uint16_t *svh2,
-                         const float *weights, const int *perm, float *dout, int *err, cudaStream_t s);
+int exl3_launch_moe_fused_gateup(const uint16_t *xg, const uint16_t *xu, int U, int hidden, int inter, int K,
+                                 const uint16_t *w13_trellis, const int *mtiles, const int *n_mtiles, int max_mtiles,
+                                 const uint16_t *svh13, const uint16_t *suh2, uint16_t *hout, int *err,
+                                 cudaStream_t s);
+int exl3_launch_moe_fused_down(const uint16_t *hin, int U, int hidden, int inter, int K, const uint16_t *w2_trellis,
+                               const int *mtiles, const int *n_mtiles, int max_mtiles, const uint16_t *svh2,
+                               const float *weights, const int *perm, float *dout, int *err, cudaStream_t s);
 
 // ---------------------------------------------------------------- errors --
 
@@ -182,7 +181,7 @@ LinearInt8Ws linear_int8_ws(int M, int k, int n) {
 
 // ---- exl3_moe_grouped workspace layout
 struct MoeWs {
-  size_t counts, offsets, pos, perm, active, mtiles, n_mtiles, xg, xu, h, d, w13, w2, total;
+  size_t counts, offsets, pos, perm, mtiles, n_mtiles, xg, xu, h, d, total;
   int max_mtiles;
 };
 
@@ -196,15 +195,12 @@ MoeWs moe_ws(int T, int topk, int E, int hidden, int inter) {
   w.offsets = take(sizeof(int) * (E + 1));
   w.pos = take(sizeof(int) * U);
   w.perm = take(sizeof(int) * U);
-  w.active = take(sizeof(int) * (E + 1));
   w.mtiles = take(sizeof(int) * 4 * (size_t)w.max_mtiles);
   w.n_mtiles = take(sizeof(int));
   w.xg = take(sizeof(uint16_t) * U * hidden);
   w.xu = take(sizeof(uint16_t) * U * hidden);
   w.h = take(sizeof(uint16_t) * U * inter);
   w.d = take(sizeof(float) * U * hidden);
-  w.w13 = take(sizeof(uint16_t) * (size_t)E * 2 * inter * hidden);
-  w.w2 = take(sizeof(uint16_t) * (size_t)E * hidden * inter);
   w.total = off;
   return w;
 }
@@ -403,29 +399,21 @@ int exl3_moe_grouped(const uint16_t *x, int T, int hidden, const int32_t *topk_i
   int *err = at<int>(workspace, 0);
   int *counts = at<int>(workspace, L.counts), *offsets = at<int>(workspace, L.offsets);
   int *pos = at<int>(workspace, L.pos), *perm = at<int>(workspace, L.perm);
-  int *active = at<int>(workspace, L.active), *mtiles = at<int>(workspace, L.mtiles);
+  int *mtiles = at<int>(workspace, L.mtiles);
   int *n_mtiles = at<int>(workspace, L.n_mtiles);
   uint16_t *xg = at<uint16_t>(workspace, L.xg), *xu = at<uint16_t>(workspace, L.xu);
-  uint16_t *h = at<uint16_t>(workspace, L.h), *w13a = at<uint16_t>(workspace, L.w13);
-  uint16_t *w2a = at<uint16_t>(workspace, L.w2);
+  uint16_t *h = at<uint16_t>(workspace, L.h);
   float *d = at<float>(workspace, L.d);
-  const int grid = 4 * sm_count();
-  EXL3_TRY(exl3_cuda_check(exl3_launch_moe_remap(topk_ids, U, E, counts, offsets, perm, pos, active, mtiles,
+  EXL3_TRY(exl3_cuda_check(exl3_launch_moe_remap(topk_ids, U, E, counts, offsets, perm, pos, mtiles,
                                                  n_mtiles, L.max_mtiles, err, stream),
                            "moe remap launch"));
-  EXL3_TRY(exl3_cuda_check(exl3_launch_moe_reconstruct(w13->trellis, 2, hidden, inter, w13->K, active, w13a, true,
-                                                       grid, stream),
-                           "moe w13 reconstruct launch"));
-  EXL3_TRY(exl3_cuda_check(exl3_launch_moe_reconstruct(w2->trellis, 1, inter, hidden, w2->K, active, w2a, false,
-                                                       grid, stream),
-                           "moe w2 reconstruct launch"));
   EXL3_TRY(exl3_cuda_check(exl3_launch_moe_gather(x, U, hidden, topk, perm, offsets, E, topk_ids, w13->suh, xg, xu,
                                                   stream),
                            "moe gather launch"));
-  EXL3_TRY(exl3_launch_moe_gateup(xg, xu, U, hidden, inter, E, w13a, mtiles, n_mtiles, L.max_mtiles, w13->svh,
-                                  w2->suh, h, err, stream));
-  EXL3_TRY(exl3_launch_moe_down(h, U, hidden, inter, E, w2a, mtiles, n_mtiles, L.max_mtiles, w2->svh, topk_weights,
-                                perm, d, err, stream));
+  EXL3_TRY(exl3_launch_moe_fused_gateup(xg, xu, U, hidden, inter, w13->K, w13->trellis, mtiles, n_mtiles,
+                                        L.max_mtiles, w13->svh, w2->suh, h, err, stream));
+  EXL3_TRY(exl3_launch_moe_fused_down(h, U, hidden, inter, w2->K, w2->trellis, mtiles, n_mtiles, L.max_mtiles,
+                                      w2->svh, topk_weights, perm, d, err, stream));
   return exl3_cuda_check(exl3_launch_moe_combine(d, pos, T, topk, hidden, y, out_dtype == EXL3_OUT_F32, stream),
                          "moe combine launch");
 }

@@ -34,50 +34,10 @@
 
 #include "exl3_common.cuh"
 #include "tc_ptx.cuh"
-#include "trellis_window.cuh"
+#include "fused_decode.cuh"
 
 namespace exl3 {
 namespace ftc {
-
-constexpr int BN = 128, BK = 64;             // output columns per CTA, k per step
-constexpr int W_BYTES = BK * BN * 2;         // decoded weight operand of one step
-constexpr int NGRP = 2;   // decoder groups (alternate k steps)
-constexpr int NDEC = 8;   // decoder warps per group
-constexpr int NWARPS = 3 + NGRP * NDEC;
-
-template <int K, int NMAX>
-struct Shape {
-  static constexpr int G = 8 / gcd_c(K, 8);      // rows per lane item
-  static constexpr int CPL = K / gcd_c(K, 8);    // 16-byte chunks per item
-  static constexpr int LPT = 16 / G;             // items per tile
-  static constexpr int ROWB = (BN / 16) * 32 * K;   // one tile row of the CTA: 8 tiles
-  static constexpr int T_BYTES = 4 * ROWB;          // 4 tile rows per 64-deep k step
-  static constexpr int X_BYTES = NMAX * BK * 2;     // x' operand of one step (up to NMAX tokens)
-  static constexpr int WS = 4;                      // decoded-weight ring depth
-  static constexpr int XS = NMAX <= 32 ? 16 : 4;    // x' ring depth (runs ahead of the MMA)
-  // trellis ring: the shared memory the two operand rings leave
-  static constexpr int TS_FIT = (220 * 1024 - WS * W_BYTES - XS * X_BYTES) / T_BYTES;
-  static constexpr int TS = TS_FIT > 32 ? 32 : TS_FIT;
-  static constexpr int SMEM_BYTES = WS * W_BYTES + XS * X_BYTES + TS * T_BYTES + 1024 + 1024;
-  static constexpr int ITEMS = 32 * LPT;         // (tile, group) items per stage
-  static constexpr int NW = 4 * CPL;
-};
-
-// MN-major 128B-swizzle descriptor: LBO = n-atom stride, SBO = k-group stride.
-__device__ __forceinline__ uint64_t sdesc_mn_sw128(const void *base, uint32_t lbo, uint32_t sbo) {
-  const uint64_t addr = tc::smem_u32(base);
-  uint64_t d = 0;
-  d |= (addr >> 4) & 0x3FFFull;
-  d |= (uint64_t)(lbo >> 4) << 16;
-  d |= (uint64_t)(sbo >> 4) << 32;
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
-  return d;
-}
-
-__host__ __device__ constexpr uint32_t idesc_f16_amn(int M, int N) {
-  return tc::idesc_f16(M, N) | (1u << 15);   // A is MN-major
-}
 
 struct Args {
   const uint16_t *trellis;
@@ -88,77 +48,6 @@ struct Args {
   int *err;
   int M, k, n, tiles_n, kb_per_split, splits;
 };
-
-__device__ __forceinline__ void bulk_copy(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   tc::smem_u32(dst)),
-               "l"(src), "r"(bytes), "r"(tc::smem_u32(bar))
-               : "memory");
-}
-
-// Two adjacent weights (columns C, C + 1 of row R) as the half2 (B0 - 510, B1 - 510):
-// DP4A seeded with 0x6400 gives the fp16 bits of 1024 + B; 1024 + B - 1534 is exact.
-template <int K, int R, int C>
-__device__ __forceinline__ uint32_t decode_pair(const uint32_t (&w)[Shape<K, 32>::NW + 1]) {
-  const uint32_t s0 = window_at<(16 * R + C) * K>(w), s1 = window_at<(16 * R + C + 1) * K>(w);
-  const uint32_t h0 = __dp4a(s0 * kMul1, 0x01010101u, 0x6400u);
-  const uint32_t h1 = __dp4a(s1 * kMul1, 0x01010101u, 0x6400u);
-  const uint32_t pr = __byte_perm(h0, h1, 0x5410);
-  const __half2 d = __hsub2(*reinterpret_cast<const __half2 *>(&pr), __half2half2(__ushort_as_half(0x65FE)));
-  return *reinterpret_cast<const uint32_t *>(&d);
-}
-
-// Decode one (tile, row group) item: rows G q .. G q + G - 1 of the tile,
-// 16 columns each, into the operand stage.
-template <int K, int R>
-__device__ __forceinline__ void decode_rows(const uint32_t (&w)[Shape<K, 32>::NW + 1], uint8_t *bstage, int k0,
-                                            int nn0, int swap) {
-  if constexpr (R < Shape<K, 32>::G) {
-    const uint4 lo = make_uint4(decode_pair<K, R, 0>(w), decode_pair<K, R, 2>(w), decode_pair<K, R, 4>(w),
-                                decode_pair<K, R, 6>(w));
-    const uint4 hi = make_uint4(decode_pair<K, R, 8>(w), decode_pair<K, R, 10>(w), decode_pair<K, R, 12>(w),
-                                decode_pair<K, R, 14>(w));
-    const int kk = k0 + R;                         // k within the 64-deep step
-    const int kg = kk >> 3, kr = kk & 7;
-    const int na = nn0 >> 6, ch = (nn0 & 63) >> 3;  // 16 columns = chunks ch, ch + 1 of a 64-wide atom
-    uint8_t *row = bstage + kg * 2048 + na * 1024 + kr * 128;
-    if (swap) {
-      *reinterpret_cast<uint4 *>(row + (((ch + 1) ^ kr) << 4)) = hi;
-      *reinterpret_cast<uint4 *>(row + ((ch ^ kr) << 4)) = lo;
-    } else {
-      *reinterpret_cast<uint4 *>(row + ((ch ^ kr) << 4)) = lo;
-      *reinterpret_cast<uint4 *>(row + (((ch + 1) ^ kr) << 4)) = hi;
-    }
-    decode_rows<K, R + 1>(w, bstage, k0, nn0, swap);
-  }
-}
-
-// Item -> (tile 0..31 of the step, row group q, which chunk is stored first).
-// 32 consecutive items form one warp instruction; each 8-lane phase should
-// touch 8 distinct 16-byte bank groups for the chunk loads and the stores.
-template <int K>
-__device__ __forceinline__ void item_map(int it, int &ti, int &q, int &swap) {
-  constexpr int LPT = Shape<K, 32>::LPT;
-  if constexpr (LPT == 8) {
-    // two tiles per phase pair: lanes 0-3 of a phase take groups 0-3 of one
-    // tile, lanes 4-7 groups 4-7 of the other; the halves store opposite
-    // chunk parities first
-    const int w = it >> 5, l = it & 31, p = l >> 3, i = l & 7;
-    ti = w * 4 + 2 * (p >> 1) + ((i >> 2) ^ (p & 1));
-    q = i;
-    swap = i >> 2;
-  } else if constexpr (LPT == 2) {
-    // tiles fastest (8 per phase), the second half of the phase stores the odd chunk first
-    const int w = it >> 5, l = it & 31, p = l >> 3, i = l & 7;
-    ti = (w * 16) + ((p & 1) << 3) + i;
-    q = p >> 1;
-    swap = i >> 2;
-  } else {
-    ti = it / LPT;
-    q = it % LPT;
-    swap = 0;
-  }
-}
 
 template <int K, bool F32OUT, int NMAX>
 __global__ void __launch_bounds__(NWARPS * 32, 1) fused_tc_kernel(const __grid_constant__ CUtensorMap tmX, Args a) {

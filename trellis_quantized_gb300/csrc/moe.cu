@@ -1,8 +1,9 @@
 // moe.cu -- routed experts ("exl3xpu" README, "MoE (routed experts)";
 // "Bringing EXL3 Trellis Quantization to 35B MoE on Intel Arc 140V",
-// sections 2.A-2.D): device-side token-to-expert binning, reconstruct of the
-// experts that received tokens, and the final weighted combine.  The two
-// grouped projections run on the tensor cores (moe_gemm.cu).
+// sections 2.A-2.D): device-side token-to-expert binning, the gather and
+// input transform of the routed rows, and the final weighted combine.  The
+// two grouped projections, with the trellis decoded on the fly, are in
+// moe_fused.cu.
 //
 // Units are (token t, slot s) pairs, u = t * topk + s.  Every step runs on the
 // device; the host never waits for routing results.
@@ -16,12 +17,11 @@ struct Plan {       // device-side routing results (workspace)
   int *offsets;     // [E + 1] exclusive scan of counts (rows in sorted order)
   int *perm;        // [U] sorted row -> unit
   int *pos;         // [U] unit -> sorted row (-1 for an invalid expert id)
-  int *active;      // [1 + E]: number of experts with tokens, then their ids
   int4 *mtiles;     // [max_mtiles]: (expert, first row, rows, 0) per 128-row tile
   int *n_mtiles;    // [1]
 };
 
-// Counts, offsets, the active-expert list and the 128-row tile list.
+// Counts, offsets and the 128-row tile list.
 // One CTA of 1024 threads; E <= 1024.
 __global__ void __launch_bounds__(1024) remap_count_kernel(const int32_t *__restrict__ ids, int U, int E,
                                                            Plan p, int max_mtiles, int *err) {
@@ -39,13 +39,12 @@ __global__ void __launch_bounds__(1024) remap_count_kernel(const int32_t *__rest
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    int off = 0, na = 0, nt = 0;
+    int off = 0, nt = 0;
     for (int e = 0; e < E; ++e) {
       const int c = sh[e];
       p.counts[e] = c;
       p.offsets[e] = off;
       if (c > 0) {
-        p.active[1 + na++] = e;
         for (int r = 0; r < c; r += 128) {
           if (nt < max_mtiles) p.mtiles[nt] = make_int4(e, off + r, min(128, c - r), 0);
           ++nt;
@@ -54,7 +53,6 @@ __global__ void __launch_bounds__(1024) remap_count_kernel(const int32_t *__rest
       off += c;
     }
     p.offsets[E] = off;
-    p.active[0] = na;
     if (nt > max_mtiles) set_device_error(err, kErrBounds);
     *p.n_mtiles = min(nt, max_mtiles);
   }
@@ -78,62 +76,6 @@ __global__ void __launch_bounds__(256) remap_place_kernel(const int32_t *__restr
       p.pos[u] = r;
     }
     base += __popc(m);
-  }
-}
-
-// Transposed reconstruct of the active experts' weights into fp16 K-major
-// arenas.  w13: row (2 j + slot) * 128 + c of expert e's [2 inter][hidden]
-// block holds output column 128 j + c of slot `slot` (gate 0, up 1), so a
-// 256-row operand tile is gate block j followed by up block j.  w2: plain
-// [hidden][inter].  Work unit: 8 tk x 2 tn tiles of one (expert, slot).
-template <int K>
-__global__ void __launch_bounds__(256) reconstruct_experts_kernel(const uint16_t *__restrict__ trellis, int nslots,
-                                                                  int k, int n, const int *__restrict__ active,
-                                                                  uint16_t *__restrict__ arena, bool interleave) {
-  __shared__ __align__(16) __half sm[32][128 + 8];
-  const int tiles_k = k / 16, tiles_n = n / 16;
-  const int units_per_slot = (tiles_n / 2) * (tiles_k / 8);
-  const int units_per_expert = units_per_slot * nslots;
-  const long total = (long)active[0] * units_per_expert;
-  const int t = threadIdx.x;
-  for (long w = blockIdx.x; w < total; w += gridDim.x) {
-    const int ai = (int)(w / units_per_expert), rem = (int)(w % units_per_expert);
-    const int e = active[1 + ai];
-    const int slot = rem / units_per_slot, u = rem % units_per_slot;
-    const int bx = u % (tiles_n / 2), by = u / (tiles_n / 2);
-    const uint16_t *tr = trellis + ((long)e * nslots + slot) * (long)tiles_k * tiles_n * 16 * K;
-    const int tile_local = t >> 4, r = t & 15;
-    const int tkl = tile_local & 7, tnl = tile_local >> 3;
-    const int tk = by * 8 + tkl, tn = bx * 2 + tnl;
-    uint32_t a[(K + 2) / 2 + 1];
-    {
-      constexpr int NW = 16 * K;
-      const uint16_t *tile = tr + ((long)tk * tiles_n + tn) * 16 * K;
-#pragma unroll
-      for (int i = 0; i < (K + 2) / 2 + 1; ++i) {
-        int w0 = r * K + 2 * i, w1 = w0 + 1;
-        uint32_t lo = (2 * i <= K) ? (uint32_t)__ldg(tile + (w0 % NW)) : 0u;
-        uint32_t hi = (2 * i + 1 <= K) ? (uint32_t)__ldg(tile + (w1 % NW)) : 0u;
-        a[i] = lo | (hi << 16);
-      }
-    }
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      const int bit = c * K;
-      sm[tnl * 16 + c][tkl * 16 + r] = mul1_half(window16(a[bit >> 5], a[(bit >> 5) + 1], bit & 31));
-    }
-    __syncthreads();
-    uint16_t *dst_e = arena + (long)e * (long)nslots * n * k;
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int chunk = t + i * 256;
-      const int nrow = chunk >> 4, kc = (chunk & 15) * 8;
-      const int col = bx * 32 + nrow;               // output column of this slot
-      const int kg = by * 128 + kc;
-      const long drow = interleave ? (long)((2 * (col >> 7) + slot) * 128 + (col & 127)) : (long)slot * n + col;
-      *reinterpret_cast<uint4 *>(dst_e + drow * k + kg) = *reinterpret_cast<const uint4 *>(&sm[nrow][kc]);
-    }
-    __syncthreads();
   }
 }
 
@@ -201,27 +143,13 @@ __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ 
 using namespace exl3;
 
 cudaError_t exl3_launch_moe_remap(const int32_t *ids, int U, int E, int *counts, int *offsets, int *perm, int *pos,
-                                  int *active, int *mtiles, int *n_mtiles, int max_mtiles, int *err,
+                                  int *mtiles, int *n_mtiles, int max_mtiles, int *err,
                                   cudaStream_t s) {
-  moe::Plan p{counts, offsets, perm, pos, active, reinterpret_cast<int4 *>(mtiles), n_mtiles};
+  moe::Plan p{counts, offsets, perm, pos, reinterpret_cast<int4 *>(mtiles), n_mtiles};
   moe::remap_count_kernel<<<1, 1024, sizeof(int) * E, s>>>(ids, U, E, p, max_mtiles, err);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   moe::remap_place_kernel<<<(E + 7) / 8, 256, 0, s>>>(ids, U, E, p);
-  return cudaGetLastError();
-}
-
-cudaError_t exl3_launch_moe_reconstruct(const uint16_t *trellis, int nslots, int k, int n, int K,
-                                        const int *active, uint16_t *arena, bool interleave, int grid,
-                                        cudaStream_t s) {
-  switch (K) {
-#define EXL3_CASE(KK) \
-  case KK: moe::reconstruct_experts_kernel<KK><<<grid, 256, 0, s>>>(trellis, nslots, k, n, active, arena, interleave); break;
-    EXL3_CASE(1) EXL3_CASE(2) EXL3_CASE(3) EXL3_CASE(4) EXL3_CASE(5) EXL3_CASE(6) EXL3_CASE(7)
-    EXL3_CASE(8)
-#undef EXL3_CASE
-    default: return cudaErrorInvalidValue;
-  }
   return cudaGetLastError();
 }
 
