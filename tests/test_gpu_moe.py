@@ -59,9 +59,10 @@ def test_moe_config5_t4096_sampled_tokens():
     assert_close(y[tokens], ref, c.name + " sampled")
 
 
-@pytest.mark.parametrize("E,topk,T", [(4, 2, 3), (1, 1, 5), (8, 8, 37)])
+@pytest.mark.parametrize("E,topk,T", [(4, 2, 3), (1, 1, 5), (8, 8, 37), (1000, 4, 300)])
 def test_moe_small_shapes(E, topk, T):
-    """Few experts (many rows per expert), a single expert, all experts hit."""
+    """Few experts (many rows per expert), a single expert, all experts hit,
+    and 1000 experts (the routing step bins units in several chunks)."""
     c = synth.moe_case(51, E * 10 + topk, T, E=E, topk=topk, hidden=256, inter=128, K=4)
     d = _dev_case(c)
     assert_close(_run(c, d), _oracle(c), f"moe E{E} top{topk} T{T}")

@@ -33,7 +33,9 @@ int exl3_launch_fused_tc(const uint16_t *xh, const uint16_t *trellis, const uint
                          cudaStream_t s);
 
 cudaError_t exl3_launch_moe_remap(const int32_t *ids, int U, int E, int *counts, int *offsets, int *perm, int *pos,
-                                  int *mtiles, int *n_mtiles, int max_mtiles, int *err, cudaStream_t s);
+                                  int *mtiles, int *n_mtiles, int max_mtiles, int *chunk_tab, int *err,
+                                  cudaStream_t s);
+int exl3_moe_remap_chunk(int E);
 cudaError_t exl3_launch_moe_gather(const uint16_t *x, int U, int hidden, int topk, const int *perm, const int *offsets,
                                    int E, const int32_t *ids, const uint16_t *suh13, uint16_t *xg, uint16_t *xu,
                                    cudaStream_t s);
@@ -181,7 +183,7 @@ LinearInt8Ws linear_int8_ws(int M, int k, int n) {
 
 // ---- exl3_moe_grouped workspace layout
 struct MoeWs {
-  size_t counts, offsets, pos, perm, mtiles, n_mtiles, xg, xu, h, d, total;
+  size_t counts, offsets, pos, perm, mtiles, n_mtiles, chunk, xg, xu, h, d, total;
   int max_mtiles;
 };
 
@@ -197,6 +199,8 @@ MoeWs moe_ws(int T, int topk, int E, int hidden, int inter) {
   w.perm = take(sizeof(int) * U);
   w.mtiles = take(sizeof(int) * 4 * (size_t)w.max_mtiles);
   w.n_mtiles = take(sizeof(int));
+  const size_t ch = (size_t)exl3_moe_remap_chunk(E);
+  w.chunk = take(sizeof(int) * ((U + ch - 1) / ch) * (size_t)E);
   w.xg = take(sizeof(uint16_t) * U * hidden);
   w.xu = take(sizeof(uint16_t) * U * hidden);
   w.h = take(sizeof(uint16_t) * U * inter);
@@ -399,13 +403,13 @@ int exl3_moe_grouped(const uint16_t *x, int T, int hidden, const int32_t *topk_i
   int *err = at<int>(workspace, 0);
   int *counts = at<int>(workspace, L.counts), *offsets = at<int>(workspace, L.offsets);
   int *pos = at<int>(workspace, L.pos), *perm = at<int>(workspace, L.perm);
-  int *mtiles = at<int>(workspace, L.mtiles);
+  int *mtiles = at<int>(workspace, L.mtiles), *chunk_tab = at<int>(workspace, L.chunk);
   int *n_mtiles = at<int>(workspace, L.n_mtiles);
   uint16_t *xg = at<uint16_t>(workspace, L.xg), *xu = at<uint16_t>(workspace, L.xu);
   uint16_t *h = at<uint16_t>(workspace, L.h);
   float *d = at<float>(workspace, L.d);
   EXL3_TRY(exl3_cuda_check(exl3_launch_moe_remap(topk_ids, U, E, counts, offsets, perm, pos, mtiles,
-                                                 n_mtiles, L.max_mtiles, err, stream),
+                                                 n_mtiles, L.max_mtiles, chunk_tab, err, stream),
                            "moe remap launch"));
   EXL3_TRY(exl3_cuda_check(exl3_launch_moe_gather(x, U, hidden, topk, perm, offsets, E, topk_ids, w13->suh, xg, xu,
                                                   stream),

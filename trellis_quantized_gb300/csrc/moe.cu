@@ -19,68 +19,133 @@ struct Plan {       // device-side routing results (workspace)
   int *pos;         // [U] unit -> sorted row (-1 for an invalid expert id)
   int4 *mtiles;     // [max_mtiles]: (expert, first row, rows, 0) per 128-row tile
   int *n_mtiles;    // [1]
+  int *chunk;       // [nchunks][E]: units of each expert per chunk, then the
+                    // expert's rows before the chunk (exclusive scan over chunks)
 };
 
-// Counts, offsets and the 128-row tile list.
-// One CTA of 1024 threads; E <= 1024.
-__global__ void __launch_bounds__(1024) remap_count_kernel(const int32_t *__restrict__ ids, int U, int E,
-                                                           Plan p, int max_mtiles, int *err) {
-  extern __shared__ int sh[];   // cnt[E]
-  for (int e = threadIdx.x; e < E; e += blockDim.x) sh[e] = 0;
+// Units are binned in chunks of 32 W consecutive units (one CTA, W warps);
+// W is chosen on the host so that a [W][E] int table fits 32 KB.
+__device__ __forceinline__ unsigned lanemask_lt() {
+  unsigned m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// (1) per-chunk histogram.  Lanes holding the same expert id elect one
+// leader, which adds the group size: one shared atomic per distinct id per
+// warp.  Invalid ids are reported, their unit gets pos = -1.
+__global__ void remap_hist_kernel(const int32_t *__restrict__ ids, int U, int E, Plan p, int *err) {
+  extern __shared__ int hist[];   // [E]
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
-  for (int u = threadIdx.x; u < U; u += blockDim.x) {
-    const int e = ids[u];
-    if (e >= 0 && e < E) {
-      atomicAdd(&sh[e], 1);
-    } else {
-      set_device_error(err, kErrExpertId);
-      p.pos[u] = -1;   // skipped: contributes nothing
+  const int u = blockIdx.x * blockDim.x + threadIdx.x;
+  const int id = u < U ? ids[u] : -1;
+  const bool valid = id >= 0 && id < E;
+  if (u < U && !valid) {
+    set_device_error(err, kErrExpertId);
+    p.pos[u] = -1;
+  }
+  const unsigned peers = __match_any_sync(0xffffffffu, valid ? id : -1);
+  if (valid && (peers & lanemask_lt()) == 0) atomicAdd(&hist[id], __popc(peers));
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) p.chunk[(long)blockIdx.x * E + e] = hist[e];
+}
+
+// Block-wide exclusive scan of one int per thread (1024 threads); returns
+// the prefix and writes the block total to *total.
+__device__ __forceinline__ int block_exclusive_scan(int v, int *warp_sums, int *total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) warp_sums[w] = incl;
+  __syncthreads();
+  if (w == 0) {
+    int ws = warp_sums[lane];
+    int wi = ws;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += t;
     }
+    warp_sums[lane] = wi - ws;   // exclusive prefix of the warps
+    if (lane == 31) *total = wi;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int off = 0, nt = 0;
-    for (int e = 0; e < E; ++e) {
-      const int c = sh[e];
-      p.counts[e] = c;
-      p.offsets[e] = off;
-      if (c > 0) {
-        for (int r = 0; r < c; r += 128) {
-          if (nt < max_mtiles) p.mtiles[nt] = make_int4(e, off + r, min(128, c - r), 0);
-          ++nt;
-        }
+  const int r = warp_sums[w] + incl - v;
+  __syncthreads();   // warp_sums may be reused by the caller
+  return r;
+}
+
+// (2) one CTA of 1024 threads, thread e = expert e (E <= 1024): per-chunk
+// counts become the expert's rows before each chunk; counts, offsets and the
+// 128-row tile list follow from two block scans.
+__global__ void __launch_bounds__(1024) remap_scan_kernel(int E, int nchunks, Plan p, int max_mtiles, int *err) {
+  __shared__ int warp_sums[32];
+  __shared__ int total;
+  const int e = threadIdx.x;
+  int c = 0;
+  if (e < E) {
+    int *col = p.chunk + e;
+    int ch = 0;
+    for (; ch + 8 <= nchunks; ch += 8) {
+      int v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = col[(long)(ch + j) * E];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        col[(long)(ch + j) * E] = c;
+        c += v[j];
       }
-      off += c;
     }
-    p.offsets[E] = off;
-    if (nt > max_mtiles) set_device_error(err, kErrBounds);
-    *p.n_mtiles = min(nt, max_mtiles);
+    for (; ch < nchunks; ++ch) {
+      const int v = col[(long)ch * E];
+      col[(long)ch * E] = c;
+      c += v;
+    }
+    p.counts[e] = c;
+  }
+  const int off = block_exclusive_scan(c, warp_sums, &total);
+  if (e < E) p.offsets[e] = off;
+  if (e == 0) p.offsets[E] = total;
+  const int nt = (c + 127) >> 7;
+  const int tb = block_exclusive_scan(nt, warp_sums, &total);
+  for (int j = 0; j < nt; ++j)
+    if (tb + j < max_mtiles) p.mtiles[tb + j] = make_int4(e, off + 128 * j, min(128, c - 128 * j), 0);
+  if (e == 0) {
+    if (total > max_mtiles) set_device_error(err, kErrBounds);
+    *p.n_mtiles = min(total, max_mtiles);
   }
 }
 
-// Stable placement: warp e scans all units in order with ballots; the unit's
-// row is offsets[e] + (number of earlier units routed to e).
-__global__ void __launch_bounds__(256) remap_place_kernel(const int32_t *__restrict__ ids, int U, int E,
-                                                          Plan p) {
-  const int lane = threadIdx.x & 31;
-  const int e = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (e >= E || p.counts[e] == 0) return;
-  int base = p.offsets[e];
-  for (int u0 = 0; u0 < U; u0 += 32) {
-    const int u = u0 + lane;
-    const int id = u < U ? ids[u] : -1;
-    const unsigned m = __ballot_sync(0xffffffffu, id == e);
-    if (id == e) {
-      const int r = base + __popc(m & ((1u << lane) - 1u));
-      p.perm[r] = u;
-      p.pos[u] = r;
-    }
-    base += __popc(m);
-  }
+// (3) stable placement: the unit's row is offsets[e] + (rows of e before the
+// chunk) + (units of e in earlier warps of the chunk) + (earlier lanes of
+// the same warp with e), so rows of an expert follow unit order.
+__global__ void remap_place_kernel(const int32_t *__restrict__ ids, int U, int E, Plan p) {
+  extern __shared__ int wc[];   // [W][E]
+  const int W = blockDim.x >> 5, w = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < W * E; i += blockDim.x) wc[i] = 0;
+  __syncthreads();
+  const int u = blockIdx.x * blockDim.x + threadIdx.x;
+  const int id = u < U ? ids[u] : -1;
+  const bool valid = id >= 0 && id < E;
+  const unsigned peers = __match_any_sync(0xffffffffu, valid ? id : -1);
+  const unsigned lt = lanemask_lt();
+  if (valid && (peers & lt) == 0) wc[w * E + id] = __popc(peers);
+  __syncthreads();
+  if (!valid) return;
+  int r = p.offsets[id] + p.chunk[(long)blockIdx.x * E + id] + __popc(peers & lt);
+  for (int j = 0; j < w; ++j) r += wc[j * E + id];
+  p.perm[r] = u;
+  p.pos[u] = r;
 }
 
 // Sorted rows of the transformed token inputs for gate and up:
 // xg[i] = RHT(x_t . suh_gate[e]), xu[i] = RHT(x_t . suh_up[e]), t = perm[i] / topk.
+// One warp per sorted row: both slots, every 128-block of the row.
 __global__ void __launch_bounds__(256) gather_rht_kernel(const __half *__restrict__ x, int hidden, int topk,
                                                          const int *__restrict__ perm,
                                                          const int *__restrict__ offsets, int E,
@@ -88,27 +153,36 @@ __global__ void __launch_bounds__(256) gather_rht_kernel(const __half *__restric
                                                          const __half *__restrict__ suh13,  // [E][2][hidden]
                                                          __half *__restrict__ xg, __half *__restrict__ xu) {
   const int lane = threadIdx.x & 31;
-  const int blocks = hidden >> 7;
-  const long wid = (long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int U = offsets[E];
-  if (wid >= (long)U * blocks * 2) return;
-  const int slot = (int)(wid & 1);
-  const long rb = wid >> 1;
-  const int i = (int)(rb / blocks), b = (int)(rb % blocks);
+  const int i = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (i >= offsets[E]) return;
   const int u = perm[i];
   const int t = u / topk, e = ids[u];
-  const int col = b * 128 + lane * 4;
-  const uint2 xv = *reinterpret_cast<const uint2 *>(x + (long)t * hidden + col);
-  const uint2 sv = *reinterpret_cast<const uint2 *>(suh13 + ((long)e * 2 + slot) * hidden + col);
-  const __half2 *xh = reinterpret_cast<const __half2 *>(&xv);
-  const __half2 *sh = reinterpret_cast<const __half2 *>(&sv);
-  float v[4] = {__low2float(xh[0]) * __low2float(sh[0]), __high2float(xh[0]) * __high2float(sh[0]),
-                __low2float(xh[1]) * __low2float(sh[1]), __high2float(xh[1]) * __high2float(sh[1])};
-  fwht128_warp(v, lane);
-  __half2 o[2] = {__floats2half2_rn(v[0] * kRhtScale, v[1] * kRhtScale),
-                  __floats2half2_rn(v[2] * kRhtScale, v[3] * kRhtScale)};
-  __half *dst = (slot == 0 ? xg : xu) + (long)i * hidden + col;
-  *reinterpret_cast<uint2 *>(dst) = *reinterpret_cast<uint2 *>(o);
+  const __half *xr = x + (long)t * hidden;
+  const __half *sg = suh13 + (long)e * 2 * hidden, *su = sg + hidden;
+  __half *dg = xg + (long)i * hidden, *du = xu + (long)i * hidden;
+#pragma unroll 4
+  for (int col = lane * 4; col < hidden; col += 128) {
+    const uint2 xv = *reinterpret_cast<const uint2 *>(xr + col);
+    const uint2 gv = __ldg(reinterpret_cast<const uint2 *>(sg + col));
+    const uint2 uv = __ldg(reinterpret_cast<const uint2 *>(su + col));
+    const __half2 *xh = reinterpret_cast<const __half2 *>(&xv);
+    const __half2 *gh = reinterpret_cast<const __half2 *>(&gv);
+    const __half2 *uh = reinterpret_cast<const __half2 *>(&uv);
+    const float x0 = __low2float(xh[0]), x1 = __high2float(xh[0]), x2 = __low2float(xh[1]),
+                x3 = __high2float(xh[1]);
+    float a[4] = {x0 * __low2float(gh[0]), x1 * __high2float(gh[0]), x2 * __low2float(gh[1]),
+                  x3 * __high2float(gh[1])};
+    float b[4] = {x0 * __low2float(uh[0]), x1 * __high2float(uh[0]), x2 * __low2float(uh[1]),
+                  x3 * __high2float(uh[1])};
+    fwht128_warp(a, lane);
+    fwht128_warp(b, lane);
+    __half2 og[2] = {__floats2half2_rn(a[0] * kRhtScale, a[1] * kRhtScale),
+                     __floats2half2_rn(a[2] * kRhtScale, a[3] * kRhtScale)};
+    __half2 ou[2] = {__floats2half2_rn(b[0] * kRhtScale, b[1] * kRhtScale),
+                     __floats2half2_rn(b[2] * kRhtScale, b[3] * kRhtScale)};
+    *reinterpret_cast<uint2 *>(dg + col) = *reinterpret_cast<uint2 *>(og);
+    *reinterpret_cast<uint2 *>(du + col) = *reinterpret_cast<uint2 *>(ou);
+  }
 }
 
 // y_t = sum over slots s (in order) of d[pos(t, s)]; d already carries the
@@ -142,22 +216,37 @@ __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ 
 
 using namespace exl3;
 
+// Units per binning chunk: 32 W with W warps, the [W][E] placement table
+// within 32 KB of shared memory (E <= 1024 gives W >= 8).
+int exl3_moe_remap_chunk(int E) {
+  const int W = E > 0 ? 8192 / E : 32;
+  return 32 * (W > 32 ? 32 : W);
+}
+
+// chunk_tab: [ceil(U / exl3_moe_remap_chunk(E))][E] ints of workspace.
 cudaError_t exl3_launch_moe_remap(const int32_t *ids, int U, int E, int *counts, int *offsets, int *perm, int *pos,
-                                  int *mtiles, int *n_mtiles, int max_mtiles, int *err,
+                                  int *mtiles, int *n_mtiles, int max_mtiles, int *chunk_tab, int *err,
                                   cudaStream_t s) {
-  moe::Plan p{counts, offsets, perm, pos, reinterpret_cast<int4 *>(mtiles), n_mtiles};
-  moe::remap_count_kernel<<<1, 1024, sizeof(int) * E, s>>>(ids, U, E, p, max_mtiles, err);
+  if (E < 1 || E > 1024) return cudaErrorInvalidValue;
+  moe::Plan p{counts, offsets, perm, pos, reinterpret_cast<int4 *>(mtiles), n_mtiles, chunk_tab};
+  const int CH = exl3_moe_remap_chunk(E);
+  const int nchunks = (U + CH - 1) / CH;
+  if (nchunks > 0) {
+    moe::remap_hist_kernel<<<nchunks, CH, sizeof(int) * E, s>>>(ids, U, E, p, err);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  moe::remap_scan_kernel<<<1, 1024, 0, s>>>(E, nchunks, p, max_mtiles, err);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  moe::remap_place_kernel<<<(E + 7) / 8, 256, 0, s>>>(ids, U, E, p);
+  if (e != cudaSuccess || nchunks == 0) return e;
+  moe::remap_place_kernel<<<nchunks, CH, sizeof(int) * (CH / 32) * E, s>>>(ids, U, E, p);
   return cudaGetLastError();
 }
 
 cudaError_t exl3_launch_moe_gather(const uint16_t *x, int U, int hidden, int topk, const int *perm,
                                    const int *offsets, int E, const int32_t *ids, const uint16_t *suh13,
                                    uint16_t *xg, uint16_t *xu, cudaStream_t s) {
-  const long warps = (long)U * (hidden / 128) * 2;   // upper bound: all units valid
-  const unsigned grid = (unsigned)((warps + 7) / 8);
+  const unsigned grid = (unsigned)(((long)U + 7) / 8);   // one warp per row; rows <= U
   if (grid == 0) return cudaSuccess;
   moe::gather_rht_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const __half *>(x), hidden, topk, perm, offsets, E,
                                                ids, reinterpret_cast<const __half *>(suh13),

@@ -200,6 +200,31 @@ __global__ void __launch_bounds__(NWARPS * 32, 1) moe_fused_kernel(const __grid_
     const int dw = warp - 3;
     const int grp = dw / NDEC, dt = (dw % NDEC) * 32 + lane;
     constexpr int PER_P = 32 * S::LPT;
+    // Epilogue operands, loaded now so that their latency hides behind the
+    // decode: this lane's 4 columns of svh (gate, up) and suh (down), or of
+    // svh (down) and the routing weights of the warp's rows (lane q holds
+    // row dw + 16 q).
+    const int col0 = nt * BN;
+    float ep_a[4], ep_b[4], ep_c[4], row_w = 0.f;
+    {
+      auto ld4 = [&](const __half *src, float (&o)[4]) {
+        const uint2 r = __ldg(reinterpret_cast<const uint2 *>(src + col0 + 4 * lane));
+        const __half2 *h = reinterpret_cast<const __half2 *>(&r);
+        o[0] = __low2float(h[0]);
+        o[1] = __high2float(h[0]);
+        o[2] = __low2float(h[1]);
+        o[3] = __high2float(h[1]);
+      };
+      if (PHASE == 1) {
+        ld4(a.svh13 + ((long)e * 2 + 0) * a.inter, ep_a);
+        ld4(a.svh13 + ((long)e * 2 + 1) * a.inter, ep_b);
+        ld4(a.suh2 + (long)e * a.inter, ep_c);
+      } else {
+        ld4(a.svh2 + (long)e * a.hidden, ep_a);
+        const int m = dw + NGRP * NDEC * lane;
+        if (lane < XROWS / (NGRP * NDEC) && m < rows) row_w = a.weights[a.perm[row0 + m]];
+      }
+    }
     for (int i = grp; i < KB; i += NGRP) {
       const int ts = i % TS, bs = i % WS;
       const bool ok = (*abort_flag) || (tc::mbar_wait(&tfull[ts], (i / TS) & 1) &&
@@ -263,37 +288,32 @@ __global__ void __launch_bounds__(NWARPS * 32, 1) moe_fused_kernel(const __grid_
     }
     asm volatile("bar.sync 1, %0;" ::"n"(NGRP * NDEC * 32) : "memory");
     // (2) one warp per row of the tile
-    const int col0 = nt * BN;
     for (int m = dw; m < rows; m += NGRP * NDEC) {
       const long row = (long)row0 + m;
       const float4 g4 = *reinterpret_cast<const float4 *>(scratch + m * 128 + 4 * lane);
       float v[4] = {g4.x, g4.y, g4.z, g4.w};
       fwht128_warp(v, lane);
       if (PHASE == 1) {
-        const __half *sg = a.svh13 + ((long)e * 2 + 0) * a.inter + col0 + 4 * lane;
-        const __half *su = a.svh13 + ((long)e * 2 + 1) * a.inter + col0 + 4 * lane;
-        const __half *sd = a.suh2 + (long)e * a.inter + col0 + 4 * lane;
         const float4 u4 = *reinterpret_cast<const float4 *>(scratch + (XROWS + m) * 128 + 4 * lane);
         float u[4] = {u4.x, u4.y, u4.z, u4.w};
         fwht128_warp(u, lane);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float g = v[j] * kRhtScale * __half2float(sg[j]);
-          const float uu = u[j] * kRhtScale * __half2float(su[j]);
-          v[j] = g / (1.0f + expf(-g)) * uu * __half2float(sd[j]);   // h . suh_down
+        for (int q = 0; q < 4; ++q) {
+          const float g = v[q] * kRhtScale * ep_a[q];
+          const float uu = u[q] * kRhtScale * ep_b[q];
+          v[q] = g / (1.0f + expf(-g)) * uu * ep_c[q];   // h . suh_down
         }
         fwht128_warp(v, lane);
         __half2 o[2] = {__floats2half2_rn(v[0] * kRhtScale, v[1] * kRhtScale),
                         __floats2half2_rn(v[2] * kRhtScale, v[3] * kRhtScale)};
         *reinterpret_cast<uint2 *>(a.hout + row * a.inter + col0 + 4 * lane) = *reinterpret_cast<uint2 *>(o);
       } else {
-        const __half *sv = a.svh2 + (long)e * a.hidden + col0 + 4 * lane;
-        const float w = a.weights[a.perm[row]];
+        const float w = __shfl_sync(0xffffffffu, row_w, m / (NGRP * NDEC));
         float4 o;
-        o.x = v[0] * kRhtScale * __half2float(sv[0]) * w;
-        o.y = v[1] * kRhtScale * __half2float(sv[1]) * w;
-        o.z = v[2] * kRhtScale * __half2float(sv[2]) * w;
-        o.w = v[3] * kRhtScale * __half2float(sv[3]) * w;
+        o.x = v[0] * kRhtScale * ep_a[0] * w;
+        o.y = v[1] * kRhtScale * ep_a[1] * w;
+        o.z = v[2] * kRhtScale * ep_a[2] * w;
+        o.w = v[3] * kRhtScale * ep_a[3] * w;
         *reinterpret_cast<float4 *>(a.dout + row * a.hidden + col0 + 4 * lane) = o;
       }
     }
