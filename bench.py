@@ -40,8 +40,8 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # dram bytes (read + write) per launch from an ncu capture of gemv_m1_kernel<4>
 # at k=5120 n=17408, with the hash of gemv.cu at capture time; a changed
 # kernel source makes the recorded traffic stale (reported as null).
-TRAFFIC = {"file": "trellis_quantized_gb300/csrc/gemv.cu", "sha1": None, "bytes_per_launch": None,
-           "workload": "k5120 n17408 K4 M1"}
+TRAFFIC = {"file": "trellis_quantized_gb300/csrc/gemv.cu", "sha1": "7c1e1bba22245b6c6ac5c678385db99d403df8a2",
+           "bytes_per_launch": 65939456, "workload": "k5120 n25600 K4 M1"}
 
 
 def peaks():
@@ -49,7 +49,8 @@ def peaks():
     try:
         with open(path) as f:
             p = json.load(f)
-        return float(p["hbm_gbs"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+        # burst figure: the prefill GEMM is timed alone (a graph of back-to-back calls)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
@@ -292,7 +293,7 @@ def bench_prefill(args, bf16_peak, src):
     ms8 = a.elapsed_time(b) / reps
     tf8 = flops / (ms8 * 1e-3) / 1e12
     return {"workload": "M=4096 k=5120 n=17408 K=4 fp16 out", "ms": round(ms, 4), "tflops": round(tf, 1),
-            "peak_tflops": bf16_peak, "peak_source": src + " bf16 sustained", "frac": round(tf / bf16_peak, 4),
+            "peak_tflops": bf16_peak, "peak_source": src + " bf16 burst (fp16 dense rate = bf16)", "frac": round(tf / bf16_peak, 4),
             "path": "input RHT + transposed reconstruct + tcgen05/TMEM GEMM with fused output RHT",
             "int8": {"ms": round(ms8, 4), "tops": round(tf8, 1), "frac_of_f16_peak": round(tf8 / bf16_peak, 4),
                      "path": "quantise + q_w reconstruct + exact int32 on tcgen05 kind::f16 (no kind::i8 on sm_103a)"}}
