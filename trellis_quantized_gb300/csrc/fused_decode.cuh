@@ -33,14 +33,21 @@ struct Shape {
   static constexpr int ROWB = (BN / 16) * 32 * K;   // one tile row of the CTA: 8 tiles
   static constexpr int T_BYTES = 4 * ROWB;          // 4 tile rows per 64-deep k step
   static constexpr int X_BYTES = NMAX * BK * 2;     // x' operand of one step (up to NMAX tokens)
-  static constexpr int WS = 4;                      // decoded-weight ring depth
-  static constexpr int XS = NMAX <= 32 ? 16 : 4;    // x' ring depth (runs ahead of the MMA)
-  // trellis ring: the shared memory the two operand rings leave
-  static constexpr int TS_FIT = (220 * 1024 - WS * W_BYTES - XS * X_BYTES) / T_BYTES;
-  static constexpr int TS = TS_FIT > 32 ? 32 : TS_FIT;
-  static constexpr int SMEM_BYTES = WS * W_BYTES + XS * X_BYTES + TS * T_BYTES + 1024 + 1024;
   static constexpr int ITEMS = 32 * LPT;         // (tile, group) items per stage
   static constexpr int NW = 4 * CPL;
+  // Streaming: a trellis stage is TSTEPS k steps (16 tile rows) fetched by one
+  // tensor load; an x' stage is XSTEPS k steps, also one tensor load.  Few,
+  // large copies keep one producer thread from limiting the feed.
+  static constexpr int TSTEPS = 4;
+  static constexpr int T_STAGE = TSTEPS * T_BYTES;
+  static constexpr int XSTEPS = NMAX <= 32 ? 4 : 2;
+  static constexpr int X_STAGE = XSTEPS * X_BYTES;
+  static constexpr int WS = 4;                      // decoded-weight ring depth (steps)
+  static constexpr int XS = 2;                      // x' ring depth (stages)
+  static constexpr int TS_FIT = (220 * 1024 - WS * W_BYTES - XS * X_STAGE) / T_STAGE;
+  static constexpr int TS = TS_FIT > 8 ? 8 : TS_FIT;   // trellis ring depth (stages)
+  static constexpr int SMEM_BYTES = WS * W_BYTES + XS * X_STAGE + TS * T_STAGE + 1024 + 1024;
+  static_assert(TS >= 2, "trellis ring too shallow");
 };
 
 // MN-major 128B-swizzle descriptor: LBO = n-atom stride, SBO = k-group stride.

@@ -11,11 +11,14 @@
 // operand slot stays small and many fit in shared memory.
 //
 // Per CTA: one 128-column tile of y and one k-range (k splits over CTAs).
-//   warp 0       trellis producer: bulk copies of the four trellis rows (8
-//                tiles each) of every 64-deep k step into a deep ring
-//   warp 1       MMA issuer: 4 x tcgen05.mma M128 N(M) K16 per step into TMEM
-//   warp 2       operand producer: TMA of the x' tile (M rows x 64 k) into the
-//                operand ring
+//   warp 0       trellis producer: one tensor load per stage of 16 tile rows
+//                (8 tiles each, four 64-deep k steps) into a ring
+//   warps 1, 2   MMA issuers, one per decoder group: 4 x tcgen05.mma M128
+//                N(M) K16 per step into the group's own TMEM accumulator (a
+//                single issuer, with its barrier waits, could not keep up
+//                with the decoders)
+//   warp 19      operand producer: one tensor load of the x' tiles of 2-4 k
+//                steps (M rows x 64 k each, 128-byte swizzled)
 //   warps 3-18   decoders, two groups of eight taking alternate k steps: each
 //                lane cuts 16 G trellis states out of its chunk, hashes them
 //                (IMAD + DP4A seeded with 0x6400 gives the fp16 value
@@ -39,6 +42,9 @@
 namespace exl3 {
 namespace ftc {
 
+constexpr int kXWarp = NWARPS;            // the x' producer follows the decoder warps
+constexpr int kFtcWarps = NWARPS + 1;
+
 struct Args {
   const uint16_t *trellis;
   const __half *svh;
@@ -50,16 +56,17 @@ struct Args {
 };
 
 template <int K, bool F32OUT, int NMAX>
-__global__ void __launch_bounds__(NWARPS * 32, 1) fused_tc_kernel(const __grid_constant__ CUtensorMap tmX, Args a) {
+__global__ void __launch_bounds__(kFtcWarps * 32, 1) fused_tc_kernel(const __grid_constant__ CUtensorMap tmX,
+                                                                  const __grid_constant__ CUtensorMap tmT, Args a) {
   using S = Shape<K, NMAX>;
   constexpr int WS = S::WS, XS = S::XS, TS = S::TS;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = tc::smem_u32(smem_raw);
   uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   uint8_t *sW = smem;                                   // [WS][W_BYTES] decoded weights (A operand)
-  uint8_t *sX = smem + WS * W_BYTES;                    // [XS][X_BYTES] x' rows (B operand)
-  uint8_t *sT = sX + XS * S::X_BYTES;                   // [TS][T_BYTES]
-  uint64_t *tfull = reinterpret_cast<uint64_t *>(sT + TS * S::T_BYTES);   // [TS] trellis landed
+  uint8_t *sX = smem + WS * W_BYTES;                    // [XS][X_STAGE] x' rows (B operand)
+  uint8_t *sT = sX + XS * S::X_STAGE;                   // [TS][T_STAGE]
+  uint64_t *tfull = reinterpret_cast<uint64_t *>(sT + TS * S::T_STAGE);   // [TS] trellis landed
   uint64_t *tempty = tfull + TS;                        // [TS] trellis decoded
   uint64_t *xfull = tempty + TS;                        // [XS] x' tile landed
   uint64_t *xempty = xfull + XS;                        // [XS] MMA done with the x' slot
@@ -72,31 +79,37 @@ __global__ void __launch_bounds__(NWARPS * 32, 1) fused_tc_kernel(const __grid_c
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nt = blockIdx.x, split = blockIdx.y;
-  const int kb0 = (int)((long)split * (a.k / BK) / a.splits);
-  const int nkb = (int)((long)(split + 1) * (a.k / BK) / a.splits) - kb0;
+  // k range of this split: whole trellis stages (the last stage of the
+  // tensor may hold only two steps; k is a multiple of 128, so nkb is even)
+  const int kbt = a.k / BK, kst = (kbt + S::TSTEPS - 1) / S::TSTEPS;
+  const int kb0 = (int)((long)split * kst / a.splits) * S::TSTEPS;
+  const int nkb = min(kbt, (int)((long)(split + 1) * kst / a.splits) * S::TSTEPS) - kb0;
+  const int ntst = (nkb + S::TSTEPS - 1) / S::TSTEPS;   // trellis stages
+  const int nxst = (nkb + S::XSTEPS - 1) / S::XSTEPS;   // x' stages
   const int tn0 = nt * (BN / 16);
   const int npad = (a.M + 15) & ~15;                    // MMA N: tokens rounded up to 16
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < TS; ++s) {
       tc::mbar_init(&tfull[s], 1);
-      tc::mbar_init(&tempty[s], NDEC);
+      tc::mbar_init(&tempty[s], NGRP * NDEC);   // every decoder warp, once per stage
     }
     for (int s = 0; s < XS; ++s) {
       tc::mbar_init(&xfull[s], 1);
-      tc::mbar_init(&xempty[s], 1);
+      tc::mbar_init(&xempty[s], NGRP);          // both MMA issuers
     }
     for (int s = 0; s < WS; ++s) {
       tc::mbar_init(&wfull[s], NDEC);
       tc::mbar_init(&wempty[s], 1);
     }
-    tc::mbar_init(accum, 1);
+    tc::mbar_init(accum, NGRP);
     *abort_flag = 0;
     tc::fence_mbar_init();
     tc::prefetch_tmap(&tmX);
+    tc::prefetch_tmap(&tmT);
   }
   if (warp == 1) {
-    tc::tmem_alloc(tmem_slot, NMAX);
+    tc::tmem_alloc(tmem_slot, NGRP * NMAX);   // one accumulator per decoder group
     tc::tmem_relinquish();
   }
   tc::tc_fence_before();
@@ -105,74 +118,85 @@ __global__ void __launch_bounds__(NWARPS * 32, 1) fused_tc_kernel(const __grid_c
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
-    // ---------------- trellis producer
+    // ---------------- trellis producer: one tensor load per stage (16 tile
+    // rows x the CTA's 8 tiles)
     if (lane == 0) {
-      for (int i = 0; i < nkb && !*abort_flag; ++i) {
-        const int st = i % TS;
-        if (!tc::mbar_wait(&tempty[st], ((i / TS) & 1) ^ 1)) {
+      for (int j = 0; j < ntst && !*abort_flag; ++j) {
+        const int st = j % TS;
+        if (!tc::mbar_wait(&tempty[st], ((j / TS) & 1) ^ 1)) {
           set_device_error(a.err, kErrBounds);
           *abort_flag = 1;
           break;
         }
-        tc::mbar_arrive_expect_tx(&tfull[st], S::T_BYTES);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const long tk = (long)(kb0 + i) * 4 + j;
-          bulk_copy(sT + st * S::T_BYTES + j * S::ROWB, a.trellis + (tk * a.tiles_n + tn0) * 16 * K, S::ROWB,
-                    &tfull[st]);
-        }
+        tc::mbar_arrive_expect_tx(&tfull[st], S::T_STAGE);
+        tc::tma_load_2d(sT + st * S::T_STAGE, &tmT, &tfull[st], tn0 * (4 * K), (kb0 + j * S::TSTEPS) * 4);
       }
     }
-  } else if (warp == 2) {
-    // ---------------- x' operand producer
+  } else if (warp == kXWarp) {
+    // ---------------- x' producer: XSTEPS k blocks of every token per tensor load
     if (lane == 0) {
-      for (int i = 0; i < nkb && !*abort_flag; ++i) {
-        const int st = i % XS;
-        if (!tc::mbar_wait(&xempty[st], ((i / XS) & 1) ^ 1)) {
+      const uint32_t xbytes = (uint32_t)S::XSTEPS * npad * BK * 2;
+      for (int j = 0; j < nxst && !*abort_flag; ++j) {
+        const int st = j % XS;
+        if (!tc::mbar_wait(&xempty[st], ((j / XS) & 1) ^ 1)) {
           set_device_error(a.err, kErrBounds);
           *abort_flag = 1;
           break;
         }
-        tc::mbar_arrive_expect_tx(&xfull[st], (uint32_t)npad * BK * 2);
-        tc::tma_load_2d(sX + st * S::X_BYTES, &tmX, &xfull[st], (kb0 + i) * BK, 0);
+        tc::mbar_arrive_expect_tx(&xfull[st], xbytes);
+        tc::tma_load_3d(sX + st * S::X_STAGE, &tmX, &xfull[st], 0, 0, kb0 + j * S::XSTEPS);
       }
     }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer
+  } else if (warp <= NGRP) {
+    // ---------------- MMA issuers: warp 1 + g takes decoder group g's k
+    // steps (i = g, g + 2, ...) into its own accumulator (TMEM columns
+    // g * NMAX ...), so neither issuer limits the decode rate
     if (lane == 0) {
-      for (int i = 0; i < nkb; ++i) {
-        const int xs = i % XS, ws = i % WS;
-        const bool ok = tc::mbar_wait(&xfull[xs], (i / XS) & 1) && tc::mbar_wait(&wfull[ws], (i / WS) & 1);
+      const int g = warp - 1;
+      const uint32_t dcol = tmem_base + (uint32_t)(g * NMAX);
+      const uint32_t idesc = idesc_f16_amn(BN, npad);
+      int xwaited = -1;
+      bool stop = false;
+      for (int i = g; i < nkb; i += NGRP) {
+        const int xj = i / S::XSTEPS, xs = xj % XS, ws = i % WS;
+        bool ok = true;
+        if (xj != xwaited) {            // once per x' stage
+          ok = tc::mbar_wait(&xfull[xs], (xj / XS) & 1);
+          xwaited = xj;
+        }
+        ok = ok && tc::mbar_wait(&wfull[ws], (i / WS) & 1);
         if (!ok || *abort_flag) {
           set_device_error(a.err, kErrBounds);
           *abort_flag = 1;
+          stop = true;
           break;
         }
         tc::tc_fence_after();
         const uint64_t ad = sdesc_mn_sw128(sW + ws * W_BYTES, 1024, 2048);
-        const uint64_t bd = tc::sdesc_k_sw128(sX + xs * S::X_BYTES);
-        const uint32_t idesc = idesc_f16_amn(BN, npad);
+        const uint64_t bd = tc::sdesc_k_sw128(sX + xs * S::X_STAGE + (i % S::XSTEPS) * npad * (BK * 2));
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
-          tc::mma_f16(tmem_base, ad + (uint64_t)((2 * 2048 * kk) >> 4), bd + 2 * kk, idesc, (i | kk) != 0 ? 1u : 0u);
+          tc::mma_f16(dcol, ad + (uint64_t)((2 * 2048 * kk) >> 4), bd + 2 * kk, idesc, (i != g || kk != 0) ? 1u : 0u);
         tc::mma_commit(&wempty[ws]);
-        tc::mma_commit(&xempty[xs]);
+        // this issuer's last step in the x' stage releases it
+        if (i + NGRP >= min(nkb, (xj + 1) * S::XSTEPS)) tc::mma_commit(&xempty[xs]);
       }
-      tc::mma_commit(accum);
+      if (!stop) tc::mma_commit(accum);
     }
   } else {
     // ---------------- decoders: group g takes k steps i = g, g + 2, ...
     const int dw = warp - 3;                 // 0..15
     const int grp = dw / NDEC, dt = (dw % NDEC) * 32 + lane;
     for (int i = grp; i < nkb; i += NGRP) {
-      const int ts = i % TS, bs = i % WS;
-      const bool ok = (*abort_flag) || (tc::mbar_wait(&tfull[ts], (i / TS) & 1) &&
+      const int tj = i / S::TSTEPS, ts = tj % TS, bs = i % WS;
+      const bool first_in_stage = (i % S::TSTEPS) < NGRP;   // the stage is waited once per group
+      const bool ok = (*abort_flag) || ((!first_in_stage || tc::mbar_wait(&tfull[ts], (tj / TS) & 1)) &&
                                         tc::mbar_wait(&wempty[bs], ((i / WS) & 1) ^ 1));
       if (!ok) {
         if (lane == 0) set_device_error(a.err, kErrBounds);
         *abort_flag = 1;
       }
-      const uint8_t *tst = sT + ts * S::T_BYTES;
+      const uint8_t *tst = sT + ts * S::T_STAGE + (i % S::TSTEPS) * S::T_BYTES;
       uint8_t *bst = sW + bs * W_BYTES;
       for (int it = dt; it < S::ITEMS; it += NDEC * 32) {
         int ti, q, swp;
@@ -195,14 +219,16 @@ __global__ void __launch_bounds__(NWARPS * 32, 1) fused_tc_kernel(const __grid_c
       __syncwarp();
       if (lane == 0) {
         tc::mbar_arrive(&wfull[bs]);
-        tc::mbar_arrive(&tempty[ts]);
+        // this group's last step in the trellis stage releases it
+        if (i + NGRP >= min(nkb, (tj + 1) * S::TSTEPS)) tc::mbar_arrive(&tempty[ts]);
       }
     }
 
     // ---------------- epilogue
     // (1) warps 3..6 (TMEM lanes 96-127, 0-31, 32-63, 64-95 = output columns)
-    // write the accumulator, times sigma, transposed into a scratch [M][128]
-    // fp32 that reuses the operand ring (free once every MMA has completed).
+    // write the sum of the two groups' accumulators (group 0 + group 1, in
+    // that order), times sigma, transposed into a scratch [M][128] fp32 that
+    // reuses the operand ring (free once every MMA has completed).
     float *scratch = reinterpret_cast<float *>(smem);
     if (warp < 7) {
       bool ok = tc::mbar_wait(accum, 0);
@@ -212,14 +238,19 @@ __global__ void __launch_bounds__(NWARPS * 32, 1) fused_tc_kernel(const __grid_c
       const int lane_base = 32 * (warp & 3);
       const int ncol = lane_base + lane;
       for (int m0 = 0; m0 < a.M; m0 += 8) {
-        uint32_t r[8];
+        uint32_t r[8], u[8];
+        const uint32_t taddr = tmem_base + ((uint32_t)lane_base << 16) + (uint32_t)m0;
         asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
                      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-                     : "r"(tmem_base + ((uint32_t)lane_base << 16) + (uint32_t)m0));
+                     : "r"(taddr));
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+                     : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7])
+                     : "r"(taddr + (uint32_t)NMAX));
         tc::tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          if (m0 + j < a.M) scratch[(m0 + j) * 128 + ncol] = __uint_as_float(r[j]) * kSigma;
+          if (m0 + j < a.M)
+            scratch[(m0 + j) * 128 + ncol] = (__uint_as_float(r[j]) + __uint_as_float(u[j])) * kSigma;
       }
       tc::tc_fence_before();
     }
@@ -288,7 +319,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 1) fused_tc_kernel(const __grid_c
   __syncthreads();
   if (warp == 1) {
     tc::tc_fence_after();
-    tc::tmem_dealloc(tmem_base, NMAX);
+    tc::tmem_dealloc(tmem_base, NGRP * NMAX);
   }
 }
 
@@ -311,7 +342,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 ftc_tmap_fn() {
 }
 
 // Number of k splits (one CTA per SM): the split count whose CTAs fill whole
-// waves best, keeping at least 16 k steps of 64 per CTA (fewer on ties).
+// waves best, keeping at least 4 trellis stages (16 k steps of 64) per CTA
+// (fewer splits on ties).  Splits fall on stage boundaries.
 int exl3_fused_tc_splits(int k, int n) {
   static int sms = 0;
   if (!sms) {
@@ -320,10 +352,10 @@ int exl3_fused_tc_splits(int k, int n) {
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 152;
     cudaGetLastError();
   }
-  const int kb = k / 64, tiles = n / 128;
+  const int kst = (k / 64 + 3) / 4, tiles = n / 128;
   int best = 1;
   double best_eff = 0.0;
-  for (int s = 1; s <= kb && (s == 1 || kb / s >= 16); ++s) {
+  for (int s = 1; s <= kst && (s == 1 || kst / s >= 4); ++s) {
     const long ctas = (long)tiles * s;
     const long waves = (ctas + sms - 1) / sms;
     const double eff = (double)ctas / (double)(waves * sms);
@@ -341,16 +373,33 @@ int exl3_launch_fused_tc(const uint16_t *xh, const uint16_t *trellis, const uint
                          cudaStream_t s) {
   auto fn = ftc_tmap_fn();
   if (!fn) return exl3_fail(EXL3_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
-  CUtensorMap ta;
-  cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)M};
-  cuuint64_t strides[1] = {(cuuint64_t)k * 2};
+  // x' [M][k] as (64 k, M rows, k/64 blocks): one load brings XSTEPS k blocks
+  // of every token, each block a 128-byte-swizzled K-major operand.
   const int npad = (M + 15) & ~15;
-  cuuint32_t box[2] = {64, (cuuint32_t)npad};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<uint16_t *>(xh), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return exl3_fail(EXL3_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  const int xsteps = npad <= 32 ? ftc::Shape<1, 32>::XSTEPS : ftc::Shape<1, 128>::XSTEPS;
+  CUtensorMap ta, tt;
+  {
+    cuuint64_t dims[3] = {64, (cuuint64_t)M, (cuuint64_t)(k / 64)};
+    cuuint64_t strides[2] = {(cuuint64_t)k * 2, 128};
+    cuuint32_t box[3] = {64, (cuuint32_t)npad, (cuuint32_t)xsteps};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<uint16_t *>(xh), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return exl3_fail(EXL3_ERR_CUDA, "cuTensorMapEncodeTiled (x') failed (%d)", (int)r);
+  }
+  // trellis [k/16][n/16 * 32K bytes] as u64: one load brings 16 tile rows of
+  // the CTA's 8 tiles (4K u64 per tile).
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)(n / 16) * 4 * K, (cuuint64_t)(k / 16)};
+    cuuint64_t strides[1] = {(cuuint64_t)(n / 16) * 32 * K};
+    cuuint32_t box[2] = {(cuuint32_t)(8 * 4 * K), 16};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(&tt, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<uint16_t *>(trellis), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return exl3_fail(EXL3_ERR_CUDA, "cuTensorMapEncodeTiled (trellis) failed (%d)", (int)r);
+  }
   ftc::Args a{trellis, reinterpret_cast<const __half *>(svh), y, partials, counters, err, M, k, n, n / 16,
               0, splits};
   dim3 grid(n / 128, splits);
@@ -359,7 +408,7 @@ int exl3_launch_fused_tc(const uint16_t *xh, const uint16_t *trellis, const uint
   do {                                                                                                      \
     auto kfn = ftc::fused_tc_kernel<KK, F32, NM>;                                                           \
     cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, ftc::Shape<KK, NM>::SMEM_BYTES);  \
-    kfn<<<grid, ftc::NWARPS * 32, ftc::Shape<KK, NM>::SMEM_BYTES, s>>>(ta, a);                              \
+    kfn<<<grid, ftc::kFtcWarps * 32, ftc::Shape<KK, NM>::SMEM_BYTES, s>>>(ta, tt, a);                              \
     e = cudaGetLastError();                                                                                 \
   } while (0)
 #define EXL3_FTC_K(KK)                                          \
