@@ -42,9 +42,11 @@ struct Shape {
   static constexpr int T_STAGE = TSTEPS * T_BYTES;
   static constexpr int XSTEPS = NMAX <= 32 ? 4 : 2;
   static constexpr int X_STAGE = XSTEPS * X_BYTES;
-  static constexpr int WS = 4;                      // decoded-weight ring depth (steps)
+  // decoded-weight ring depth (steps; even, so each decoder group owns WS / 2
+  // slots and reuses one only after its MMA of WS steps earlier)
+  static constexpr int WS = NMAX <= 32 ? 8 : 6;
   static constexpr int XS = 2;                      // x' ring depth (stages)
-  static constexpr int TS_FIT = (220 * 1024 - WS * W_BYTES - XS * X_STAGE) / T_STAGE;
+  static constexpr int TS_FIT = (227 * 1024 - 2048 - WS * W_BYTES - XS * X_STAGE) / T_STAGE;
   static constexpr int TS = TS_FIT > 8 ? 8 : TS_FIT;   // trellis ring depth (stages)
   static constexpr int SMEM_BYTES = WS * W_BYTES + XS * X_STAGE + TS * T_STAGE + 1024 + 1024;
   static_assert(TS >= 2, "trellis ring too shallow");

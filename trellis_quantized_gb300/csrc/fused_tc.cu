@@ -19,7 +19,8 @@
 //                with the decoders)
 //   warp 19      operand producer: one tensor load of the x' tiles of 2-4 k
 //                steps (M rows x 64 k each, 128-byte swizzled)
-//   warps 3-18   decoders, two groups of eight taking alternate k steps: each
+//   warps 3-18   decoders, two groups of eight taking alternate pairs of k
+//                steps (one fence and one signal per pair): each
 //                lane cuts 16 G trellis states out of its chunk, hashes them
 //                (IMAD + DP4A seeded with 0x6400 gives the fp16 value
 //                1024 + B), subtracts 1534 in half2 (exact) and stores the
@@ -70,8 +71,8 @@ __global__ void __launch_bounds__(kFtcWarps * 32, 1) fused_tc_kernel(const __gri
   uint64_t *tempty = tfull + TS;                        // [TS] trellis decoded
   uint64_t *xfull = tempty + TS;                        // [XS] x' tile landed
   uint64_t *xempty = xfull + XS;                        // [XS] MMA done with the x' slot
-  uint64_t *wfull = xempty + XS;                        // [WS] weights decoded
-  uint64_t *wempty = wfull + WS;                        // [WS] MMA done with the weight slot
+  uint64_t *wfull = xempty + XS;                        // [WS / 2] a pair of weight slots decoded
+  uint64_t *wempty = wfull + WS;                        // [WS / 2] MMA done with the pair of slots
   uint64_t *accum = wempty + WS;                        // accumulator complete
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accum + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -86,6 +87,11 @@ __global__ void __launch_bounds__(kFtcWarps * 32, 1) fused_tc_kernel(const __gri
   const int nkb = min(kbt, (int)((long)(split + 1) * kst / a.splits) * S::TSTEPS) - kb0;
   const int ntst = (nkb + S::TSTEPS - 1) / S::TSTEPS;   // trellis stages
   const int nxst = (nkb + S::XSTEPS - 1) / S::XSTEPS;   // x' stages
+  // Work is handed over in pairs of k steps: pair P = steps 2P, 2P + 1 (half
+  // a trellis stage), decoder group and MMA issuer P mod 2, weight slots
+  // 2 (P mod NPS) and 2 (P mod NPS) + 1.
+  constexpr int NPS = WS / 2;
+  const int npairs = nkb / 2;
   const int tn0 = nt * (BN / 16);
   const int npad = (a.M + 15) & ~15;                    // MMA N: tokens rounded up to 16
 
@@ -96,10 +102,10 @@ __global__ void __launch_bounds__(kFtcWarps * 32, 1) fused_tc_kernel(const __gri
     }
     for (int s = 0; s < XS; ++s) {
       tc::mbar_init(&xfull[s], 1);
-      tc::mbar_init(&xempty[s], NGRP);          // both MMA issuers
+      tc::mbar_init(&xempty[s], S::XSTEPS / 2);  // the issuers of the stage's pairs
     }
-    for (int s = 0; s < WS; ++s) {
-      tc::mbar_init(&wfull[s], NDEC);
+    for (int s = 0; s < NPS; ++s) {
+      tc::mbar_init(&wfull[s], NDEC);            // one group's warps, once per pair
       tc::mbar_init(&wempty[s], 1);
     }
     tc::mbar_init(accum, NGRP);
@@ -148,8 +154,8 @@ __global__ void __launch_bounds__(kFtcWarps * 32, 1) fused_tc_kernel(const __gri
       }
     }
   } else if (warp <= NGRP) {
-    // ---------------- MMA issuers: warp 1 + g takes decoder group g's k
-    // steps (i = g, g + 2, ...) into its own accumulator (TMEM columns
+    // ---------------- MMA issuers: warp 1 + g takes the pairs P = g, g + 2,
+    // ... (8 MMAs after one wait) into its own accumulator (TMEM columns
     // g * NMAX ...), so neither issuer limits the decode rate
     if (lane == 0) {
       const int g = warp - 1;
@@ -157,14 +163,14 @@ __global__ void __launch_bounds__(kFtcWarps * 32, 1) fused_tc_kernel(const __gri
       const uint32_t idesc = idesc_f16_amn(BN, npad);
       int xwaited = -1;
       bool stop = false;
-      for (int i = g; i < nkb; i += NGRP) {
-        const int xj = i / S::XSTEPS, xs = xj % XS, ws = i % WS;
+      for (int P = g; P < npairs; P += NGRP) {
+        const int xj = (2 * P) / S::XSTEPS, xs = xj % XS, ps = P % NPS;
         bool ok = true;
         if (xj != xwaited) {            // once per x' stage
           ok = tc::mbar_wait(&xfull[xs], (xj / XS) & 1);
           xwaited = xj;
         }
-        ok = ok && tc::mbar_wait(&wfull[ws], (i / WS) & 1);
+        ok = ok && tc::mbar_wait(&wfull[ps], (P / NPS) & 1);
         if (!ok || *abort_flag) {
           set_device_error(a.err, kErrBounds);
           *abort_flag = 1;
@@ -172,14 +178,18 @@ __global__ void __launch_bounds__(kFtcWarps * 32, 1) fused_tc_kernel(const __gri
           break;
         }
         tc::tc_fence_after();
-        const uint64_t ad = sdesc_mn_sw128(sW + ws * W_BYTES, 1024, 2048);
-        const uint64_t bd = tc::sdesc_k_sw128(sX + xs * S::X_STAGE + (i % S::XSTEPS) * npad * (BK * 2));
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)
-          tc::mma_f16(dcol, ad + (uint64_t)((2 * 2048 * kk) >> 4), bd + 2 * kk, idesc, (i != g || kk != 0) ? 1u : 0u);
-        tc::mma_commit(&wempty[ws]);
-        // this issuer's last step in the x' stage releases it
-        if (i + NGRP >= min(nkb, (xj + 1) * S::XSTEPS)) tc::mma_commit(&xempty[xs]);
+        for (int h = 0; h < 2; ++h) {
+          const int i = 2 * P + h;
+          const uint64_t ad = sdesc_mn_sw128(sW + (2 * ps + h) * W_BYTES, 1024, 2048);
+          const uint64_t bd = tc::sdesc_k_sw128(sX + xs * S::X_STAGE + (i % S::XSTEPS) * npad * (BK * 2));
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            tc::mma_f16(dcol, ad + (uint64_t)((2 * 2048 * kk) >> 4), bd + 2 * kk, idesc,
+                        (P != g || h != 0 || kk != 0) ? 1u : 0u);
+        }
+        tc::mma_commit(&wempty[ps]);
+        tc::mma_commit(&xempty[xs]);    // each issuer uses an x' stage for one pair
       }
       if (!stop) tc::mma_commit(accum);
     }
@@ -187,40 +197,42 @@ __global__ void __launch_bounds__(kFtcWarps * 32, 1) fused_tc_kernel(const __gri
     // ---------------- decoders: group g takes k steps i = g, g + 2, ...
     const int dw = warp - 3;                 // 0..15
     const int grp = dw / NDEC, dt = (dw % NDEC) * 32 + lane;
-    for (int i = grp; i < nkb; i += NGRP) {
-      const int tj = i / S::TSTEPS, ts = tj % TS, bs = i % WS;
-      const bool first_in_stage = (i % S::TSTEPS) < NGRP;   // the stage is waited once per group
-      const bool ok = (*abort_flag) || ((!first_in_stage || tc::mbar_wait(&tfull[ts], (tj / TS) & 1)) &&
-                                        tc::mbar_wait(&wempty[bs], ((i / WS) & 1) ^ 1));
+    for (int P = grp; P < npairs; P += NGRP) {
+      const int tj = P / 2, ts = tj % TS, ps = P % NPS;   // a trellis stage holds two pairs
+      const bool ok = (*abort_flag) || (tc::mbar_wait(&tfull[ts], (tj / TS) & 1) &&
+                                        tc::mbar_wait(&wempty[ps], ((P / NPS) & 1) ^ 1));
       if (!ok) {
         if (lane == 0) set_device_error(a.err, kErrBounds);
         *abort_flag = 1;
       }
-      const uint8_t *tst = sT + ts * S::T_STAGE + (i % S::TSTEPS) * S::T_BYTES;
-      uint8_t *bst = sW + bs * W_BYTES;
-      for (int it = dt; it < S::ITEMS; it += NDEC * 32) {
-        int ti, q, swp;
-        item_map<K>(it, ti, q, swp);
-        const int tkl = ti >> 3, tnl = ti & 7;
-        const uint8_t *tile = tst + tkl * S::ROWB + tnl * 32 * K;
-        uint32_t w[S::NW + 1];
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        const int i = 2 * P + h;
+        const uint8_t *tst = sT + ts * S::T_STAGE + (i % S::TSTEPS) * S::T_BYTES;
+        uint8_t *bst = sW + (2 * ps + h) * W_BYTES;
+        for (int it = dt; it < S::ITEMS; it += NDEC * 32) {
+          int ti, q, swp;
+          item_map<K>(it, ti, q, swp);
+          const int tkl = ti >> 3, tnl = ti & 7;
+          const uint8_t *tile = tst + tkl * S::ROWB + tnl * 32 * K;
+          uint32_t w[S::NW + 1];
 #pragma unroll
-        for (int cc = 0; cc < S::CPL; ++cc) {
-          const uint4 v4 = *reinterpret_cast<const uint4 *>(tile + q * 16 * S::CPL + 16 * cc);
-          w[4 * cc + 0] = v4.x;
-          w[4 * cc + 1] = v4.y;
-          w[4 * cc + 2] = v4.z;
-          w[4 * cc + 3] = v4.w;
+          for (int cc = 0; cc < S::CPL; ++cc) {
+            const uint4 v4 = *reinterpret_cast<const uint4 *>(tile + q * 16 * S::CPL + 16 * cc);
+            w[4 * cc + 0] = v4.x;
+            w[4 * cc + 1] = v4.y;
+            w[4 * cc + 2] = v4.z;
+            w[4 * cc + 3] = v4.w;
+          }
+          w[S::NW] = *reinterpret_cast<const uint32_t *>(tile + ((q + 1) % S::LPT) * 16 * S::CPL);
+          decode_rows<K, 0>(w, bst, tkl * 16 + S::G * q, tnl * 16, swp);
         }
-        w[S::NW] = *reinterpret_cast<const uint32_t *>(tile + ((q + 1) % S::LPT) * 16 * S::CPL);
-        decode_rows<K, 0>(w, bst, tkl * 16 + S::G * q, tnl * 16, swp);
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic stores -> tensor-core reads
       __syncwarp();
       if (lane == 0) {
-        tc::mbar_arrive(&wfull[bs]);
-        // this group's last step in the trellis stage releases it
-        if (i + NGRP >= min(nkb, (tj + 1) * S::TSTEPS)) tc::mbar_arrive(&tempty[ts]);
+        tc::mbar_arrive(&wfull[ps]);
+        tc::mbar_arrive(&tempty[ts]);   // the group's only pair in the stage
       }
     }
 
@@ -247,6 +259,10 @@ __global__ void __launch_bounds__(kFtcWarps * 32, 1) fused_tc_kernel(const __gri
                      : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7])
                      : "r"(taddr + (uint32_t)NMAX));
         tc::tmem_ld_wait();
+        if (npairs < 2) {                // group 1 had no pair: its accumulator was never written
+#pragma unroll
+          for (int j = 0; j < 8; ++j) u[j] = 0u;
+        }
 #pragma unroll
         for (int j = 0; j < 8; ++j)
           if (m0 + j < a.M)
