@@ -27,14 +27,19 @@ constexpr int NWARPS = 3 + NGRP * NDEC;
 
 template <int K, int NMAX>
 struct Shape {
-  static constexpr int G = 8 / gcd_c(K, 8);      // rows per lane item
-  static constexpr int CPL = K / gcd_c(K, 8);    // 16-byte chunks per item
+  // Items.  K = 4 and 8: an item is G = 8 / gcd(K, 8) rows of a tile, read as
+  // CPL 16-byte chunks.  Other widths (RP): an item is one row pair of a tile,
+  // the K + 1 stream words starting at word K * rp, so every width gives 256
+  // or more items per k step (all decoder threads busy).
+  static constexpr bool RP = (K != 4 && K != 8);
+  static constexpr int G = RP ? 2 : 8 / gcd_c(K, 8);    // rows per lane item
+  static constexpr int CPL = RP ? 0 : K / gcd_c(K, 8);  // 16-byte chunks per item
   static constexpr int LPT = 16 / G;             // items per tile
   static constexpr int ROWB = (BN / 16) * 32 * K;   // one tile row of the CTA: 8 tiles
   static constexpr int T_BYTES = 4 * ROWB;          // 4 tile rows per 64-deep k step
   static constexpr int X_BYTES = NMAX * BK * 2;     // x' operand of one step (up to NMAX tokens)
   static constexpr int ITEMS = 32 * LPT;         // (tile, group) items per stage
-  static constexpr int NW = 4 * CPL;
+  static constexpr int NW = RP ? K : 4 * CPL;    // stream words per item (one more is read)
   // Streaming: a trellis stage is TSTEPS k steps (16 tile rows) fetched by one
   // tensor load; an x' stage is XSTEPS k steps, also one tensor load.  Few,
   // large copies keep one producer thread from limiting the feed.
@@ -113,13 +118,54 @@ __device__ __forceinline__ void decode_rows(const uint32_t (&w)[Shape<K, 32>::NW
   }
 }
 
+// The item's stream words w[0..NW] (w[NW] is the first word of the next item
+// of the tile, wrapping at the tile end) from the tile at `tile` in shared
+// memory.
+template <int K>
+__device__ __forceinline__ void load_item(const uint8_t *tile, int q, uint32_t (&w)[Shape<K, 32>::NW + 1]) {
+  using S = Shape<K, 32>;
+  if constexpr (S::RP) {
+    const uint32_t *tw = reinterpret_cast<const uint32_t *>(tile);
+    if constexpr ((K & 1) == 0) {
+#pragma unroll
+      for (int j = 0; j < K / 2; ++j) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(tw + K * q + 2 * j);
+        w[2 * j] = v.x;
+        w[2 * j + 1] = v.y;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < K; ++j) w[j] = tw[K * q + j];
+    }
+    w[K] = tw[K * ((q + 1) & 7)];
+  } else {
+#pragma unroll
+    for (int cc = 0; cc < S::CPL; ++cc) {
+      const uint4 v4 = *reinterpret_cast<const uint4 *>(tile + q * 16 * S::CPL + 16 * cc);
+      w[4 * cc + 0] = v4.x;
+      w[4 * cc + 1] = v4.y;
+      w[4 * cc + 2] = v4.z;
+      w[4 * cc + 3] = v4.w;
+    }
+    w[S::NW] = *reinterpret_cast<const uint32_t *>(tile + ((q + 1) % S::LPT) * 16 * S::CPL);
+  }
+}
+
 // Item -> (tile 0..31 of the step, row group q, which chunk is stored first).
 // 32 consecutive items form one warp instruction; each 8-lane phase should
 // touch 8 distinct 16-byte bank groups for the chunk loads and the stores.
 template <int K>
 __device__ __forceinline__ void item_map(int it, int &ti, int &q, int &swap) {
   constexpr int LPT = Shape<K, 32>::LPT;
-  if constexpr (LPT == 8) {
+  if constexpr (Shape<K, 32>::RP) {
+    // four tiles per warp, lane = 8 tile + row pair: the words K (8 tile + rp)
+    // + j of one load fall in 32 distinct banks (odd K) or 16 distinct 8-byte
+    // units per half warp (K = 2, 6); row pairs 4..7 store the odd chunk first
+    const int w = it >> 5, l = it & 31;
+    ti = 4 * w + (l >> 3);
+    q = l & 7;
+    swap = q >> 2;
+  } else if constexpr (LPT == 8) {
     // two tiles per phase pair: lanes 0-3 of a phase take groups 0-3 of one
     // tile, lanes 4-7 groups 4-7 of the other; the halves store opposite
     // chunk parities first

@@ -216,15 +216,7 @@ __global__ void __launch_bounds__(kFtcWarps * 32, 1) fused_tc_kernel(const __gri
           const int tkl = ti >> 3, tnl = ti & 7;
           const uint8_t *tile = tst + tkl * S::ROWB + tnl * 32 * K;
           uint32_t w[S::NW + 1];
-#pragma unroll
-          for (int cc = 0; cc < S::CPL; ++cc) {
-            const uint4 v4 = *reinterpret_cast<const uint4 *>(tile + q * 16 * S::CPL + 16 * cc);
-            w[4 * cc + 0] = v4.x;
-            w[4 * cc + 1] = v4.y;
-            w[4 * cc + 2] = v4.z;
-            w[4 * cc + 3] = v4.w;
-          }
-          w[S::NW] = *reinterpret_cast<const uint32_t *>(tile + ((q + 1) % S::LPT) * 16 * S::CPL);
+          ftc::load_item<K>(tile, q, w);
           decode_rows<K, 0>(w, bst, tkl * 16 + S::G * q, tnl * 16, swp);
         }
       }
