@@ -41,11 +41,12 @@ cudaError_t exl3_launch_moe_gather(const uint16_t *x, int U, int hidden, int top
                                    cudaStream_t s);
 cudaError_t exl3_launch_moe_combine(const float *d, const int *pos, int T, int topk, int hidden, void *y,
                                     bool f32out, cudaStream_t s);
-int exl3_launch_moe_fused_gateup(const uint16_t *xg, const uint16_t *xu, int U, int hidden, int inter, int K,
+int exl3_launch_moe_fused_gateup(const uint16_t *xg, const uint16_t *xu, int U, int hidden, int inter, int K, int E,
                                  const uint16_t *w13_trellis, const int *mtiles, const int *n_mtiles, int max_mtiles,
                                  const uint16_t *svh13, const uint16_t *suh2, uint16_t *hout, int *err,
                                  cudaStream_t s);
-int exl3_launch_moe_fused_down(const uint16_t *hin, int U, int hidden, int inter, int K, const uint16_t *w2_trellis,
+int exl3_launch_moe_fused_down(const uint16_t *hin, int U, int hidden, int inter, int K, int E,
+                               const uint16_t *w2_trellis,
                                const int *mtiles, const int *n_mtiles, int max_mtiles, const uint16_t *svh2,
                                const float *weights, const int *perm, float *dout, int *err, cudaStream_t s);
 
@@ -414,9 +415,9 @@ int exl3_moe_grouped(const uint16_t *x, int T, int hidden, const int32_t *topk_i
   EXL3_TRY(exl3_cuda_check(exl3_launch_moe_gather(x, U, hidden, topk, perm, offsets, E, topk_ids, w13->suh, xg, xu,
                                                   stream),
                            "moe gather launch"));
-  EXL3_TRY(exl3_launch_moe_fused_gateup(xg, xu, U, hidden, inter, w13->K, w13->trellis, mtiles, n_mtiles,
+  EXL3_TRY(exl3_launch_moe_fused_gateup(xg, xu, U, hidden, inter, w13->K, E, w13->trellis, mtiles, n_mtiles,
                                         L.max_mtiles, w13->svh, w2->suh, h, err, stream));
-  EXL3_TRY(exl3_launch_moe_fused_down(h, U, hidden, inter, w2->K, w2->trellis, mtiles, n_mtiles, L.max_mtiles,
+  EXL3_TRY(exl3_launch_moe_fused_down(h, U, hidden, inter, w2->K, E, w2->trellis, mtiles, n_mtiles, L.max_mtiles,
                                       w2->svh, topk_weights, perm, d, err, stream));
   return exl3_cuda_check(exl3_launch_moe_combine(d, pos, T, topk, hidden, y, out_dtype == EXL3_OUT_F32, stream),
                          "moe combine launch");

@@ -98,7 +98,9 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *b, uint32_t parity) 
   const long long t0 = clock64();
   while (true) {
     uint32_t ok;
-    asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+    // the suspend-time hint (ns) lets the thread sleep until the phase
+    // completes instead of spinning through issue slots
+    asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 10000;\nselp.u32 %0, 1, 0, p;\n}\n"
                  : "=r"(ok)
                  : "r"(smem_addr(b)), "r"(parity)
                  : "memory");

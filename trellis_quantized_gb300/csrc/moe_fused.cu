@@ -6,14 +6,19 @@
 // anywhere).
 //
 // A CTA handles one (128-row expert tile, 128-column output tile) pair of the
-// device-side tile list; the MMA computes the transposed product (decoded
+// device-side tile list.  The MMA computes the transposed product (decoded
 // weights as the MN-major A operand, M = 128 output columns; the tile's x'
-// rows as the K-major B operand, N = 128), with the warp roles of the
-// small-M linear: trellis producer, MMA issuer, x' producer, two groups of
-// eight decoder warps on alternate k steps.
+// rows as the K-major B operand, N = 128).  Roles (20 warps):
+//   warp 0       trellis producer: one tensor load per projection and stage
+//                over all experts' trellis (16 tile rows per stage)
+//   warps 1, 2   MMA issuers, one per decoder group, each with its own
+//                accumulators (summed in a fixed order by the epilogue)
+//   warps 3-18   decoders in two groups of eight, taking alternate "pairs":
+//                phase 1 a pair is the gate and up weights of one k step,
+//                phase 2 two k steps of down; one fence and one signal per pair
+//   warp 19      x' producer: one 32 KB stage (the pair's B operands) per load
 //
-// Phase 1 (gate + up): both projections of the expert are decoded per k step
-//   into two accumulators; per token row the epilogue forms
+// Phase 1 (gate + up): per token row the epilogue forms
 //   g = RHT_out(gate) . svh_gate, u = RHT_out(up) . svh_up, h = SiLU(g) u and
 //   the down projection's input transform h' = 2^-3.5 H (h . suh_down).
 // Phase 2 (down): d = RHT_out(h' Wdown) . svh_down * routing weight (fp32).
@@ -28,36 +33,39 @@ using ftc::BK;
 using ftc::BN;
 using ftc::NDEC;
 using ftc::NGRP;
-using ftc::NWARPS;
 using ftc::W_BYTES;
 
-constexpr int XROWS = 128;
-constexpr int X_BYTES = XROWS * BK * 2;
+constexpr int XROWS = 128;                  // rows of a tile (MMA N)
+constexpr int X_STEP = XROWS * BK * 2;      // B operand of one k step (16 KB)
+constexpr int kWarps = 3 + NGRP * NDEC + 1;
+constexpr int kXWarp = kWarps - 1;
 
 template <int K, int PHASE>
 struct Cfg {
-  static constexpr int NP = PHASE == 1 ? 2 : 1;                 // projections decoded per k step
-  static constexpr int T_ONE = 4 * (BN / 16) * 32 * K;          // trellis of one projection per k step
-  static constexpr int T_BYTES = NP * T_ONE;
-  static constexpr int XS = PHASE == 1 ? 3 : 4;
-  static constexpr int WS = PHASE == 1 ? 2 : 4;
-  static constexpr int TS_FIT = (220 * 1024 - XS * NP * X_BYTES - WS * NP * W_BYTES) / T_BYTES;
-  static constexpr int TS = TS_FIT > 24 ? 24 : TS_FIT;
-  static constexpr int SMEM_BYTES = XS * NP * X_BYTES + WS * NP * W_BYTES + TS * T_BYTES + 1024 + 1024;
-  static constexpr int ITEMS = NP * 32 * ftc::Shape<K, 32>::LPT;
-  static constexpr uint32_t TMEM_COLS = NP == 2 ? 256 : 128;
-  static_assert(TS >= 2, "trellis ring too shallow");
-  static_assert(NP * XROWS * 128 * 4 <= XS * NP * X_BYTES + WS * NP * W_BYTES, "epilogue scratch overlaps the trellis ring");
+  static constexpr int NP = PHASE == 1 ? 2 : 1;         // projections (accumulators per issuer)
+  static constexpr int ROWB = (BN / 16) * 32 * K;       // one tile row of the CTA's 8 tiles
+  static constexpr int T_STAGE = 16 * ROWB;             // two pairs
+  static constexpr int NPS = 3;                         // pair slots of the weight ring
+  static constexpr int W_RING = 2 * NPS * W_BYTES;
+  static constexpr int X_STAGE = 2 * X_STEP;            // one pair
+  // x' ring: as deep as the budget allows after two trellis stages (the
+  // loads come from L2 or HBM and must run several pairs ahead)
+  static constexpr int XS_FIT = (227 * 1024 - 2048 - W_RING - 2 * T_STAGE) / X_STAGE;
+  static constexpr int XS = XS_FIT > 4 ? 4 : XS_FIT;
+  static constexpr int TS_FIT = (227 * 1024 - 2048 - W_RING - XS * X_STAGE) / T_STAGE;
+  static constexpr int TS = TS_FIT > 8 ? 8 : TS_FIT;
+  static constexpr int SMEM_BYTES = XS * X_STAGE + W_RING + TS * T_STAGE + 2048;
+  static constexpr int ITEMS = 32 * ftc::Shape<K, 32>::LPT;  // items per (k step, projection)
+  static constexpr uint32_t TMEM_COLS = NGRP * NP * XROWS;
+  static_assert(TS >= 2 && XS >= 2, "operand rings too shallow");
+  static_assert(NP * XROWS * 128 * 4 <= XS * X_STAGE + W_RING, "epilogue scratch exceeds the operand rings");
 };
 
 struct Args {
   const int4 *mtiles;       // (expert, first row, rows, 0)
   const int *n_mtiles;
   int NT, KB;               // output tiles per m-tile, k steps
-  const uint16_t *trellis;  // [E][nslots][k/16][n/16][16K]
-  int tiles_n;              // n / 16 of one projection
-  long slot_words;          // words of one (expert, slot) trellis
-  int nslots;
+  int tiles_k, nslots;      // trellis rows of one projection, projections per expert
   const __half *svh13;      // [E][2][inter]
   const __half *suh2;       // [E][inter]
   __half *hout;             // [U][inter]
@@ -71,55 +79,58 @@ struct Args {
 };
 
 template <int K, int PHASE>
-__global__ void __launch_bounds__(NWARPS * 32, 1) moe_fused_kernel(const __grid_constant__ CUtensorMap tmX0,
+__global__ void __launch_bounds__(kWarps * 32, 1) moe_fused_kernel(const __grid_constant__ CUtensorMap tmX0,
                                                                    const __grid_constant__ CUtensorMap tmX1,
-                                                                   Args a) {
+                                                                   const __grid_constant__ CUtensorMap tmT, Args a) {
   using C = Cfg<K, PHASE>;
   using S = ftc::Shape<K, 32>;
-  constexpr int NP = C::NP, XS = C::XS, WS = C::WS, TS = C::TS;
+  constexpr int NP = C::NP, XS = C::XS, TS = C::TS, NPS = C::NPS;
   const int tile = blockIdx.x;
   if (tile >= *a.n_mtiles * a.NT) return;   // uniform per CTA: the tile list is device-side
   const int4 mt = a.mtiles[tile / a.NT];
   const int nt = tile % a.NT, e = mt.x, row0 = mt.y, rows = mt.z;
   const int tn0 = nt * (BN / 16);
+  const int KB = a.KB;
+  const int npairs = PHASE == 1 ? KB : KB / 2;       // KB is even
+  const int ntst = (npairs + 1) / 2;                 // a trellis stage holds two pairs
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = tc::smem_u32(smem_raw);
   uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-  uint8_t *sX = smem;                                   // [XS][NP][X_BYTES]
-  uint8_t *sW = sX + XS * NP * X_BYTES;                 // [WS][NP][W_BYTES]
-  uint8_t *sT = sW + WS * NP * W_BYTES;                 // [TS][T_BYTES]
-  uint64_t *tfull = reinterpret_cast<uint64_t *>(sT + TS * C::T_BYTES);
+  uint8_t *sX = smem;                                   // [XS][X_STAGE]
+  uint8_t *sW = sX + XS * C::X_STAGE;                   // [2 NPS][W_BYTES]
+  uint8_t *sT = sW + C::W_RING;                         // [TS][T_STAGE]
+  uint64_t *tfull = reinterpret_cast<uint64_t *>(sT + TS * C::T_STAGE);
   uint64_t *tempty = tfull + TS;
   uint64_t *xfull = tempty + TS;
   uint64_t *xempty = xfull + XS;
   uint64_t *wfull = xempty + XS;
-  uint64_t *wempty = wfull + WS;
-  uint64_t *accum = wempty + WS;
+  uint64_t *wempty = wfull + NPS;
+  uint64_t *accum = wempty + NPS;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accum + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int KB = a.KB;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < TS; ++s) {
       tc::mbar_init(&tfull[s], 1);
-      tc::mbar_init(&tempty[s], NDEC);
+      tc::mbar_init(&tempty[s], NGRP * NDEC);   // every decoder warp, once per stage
     }
     for (int s = 0; s < XS; ++s) {
       tc::mbar_init(&xfull[s], 1);
-      tc::mbar_init(&xempty[s], 1);
+      tc::mbar_init(&xempty[s], 1);             // the issuer of the stage's pair
     }
-    for (int s = 0; s < WS; ++s) {
-      tc::mbar_init(&wfull[s], NDEC);
+    for (int s = 0; s < NPS; ++s) {
+      tc::mbar_init(&wfull[s], NDEC);           // one group's warps, once per pair
       tc::mbar_init(&wempty[s], 1);
     }
-    tc::mbar_init(accum, 1);
+    tc::mbar_init(accum, NGRP);
     *abort_flag = 0;
     tc::fence_mbar_init();
     tc::prefetch_tmap(&tmX0);
-    if (NP == 2) tc::prefetch_tmap(&tmX1);
+    if (PHASE == 1) tc::prefetch_tmap(&tmX1);
+    tc::prefetch_tmap(&tmT);
   }
   if (warp == 1) {
     tc::tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -131,75 +142,85 @@ __global__ void __launch_bounds__(NWARPS * 32, 1) moe_fused_kernel(const __grid_
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
-    // ---------------- trellis producer
+    // ---------------- trellis producer.  Phase 1: per projection 8 tile rows
+    // (two k steps); phase 2: 16 tile rows (four k steps).
     if (lane == 0) {
-      for (int i = 0; i < KB && !*abort_flag; ++i) {
-        const int st = i % TS;
-        if (!tc::mbar_wait(&tempty[st], ((i / TS) & 1) ^ 1)) {
+      for (int j = 0; j < ntst && !*abort_flag; ++j) {
+        const int st = j % TS;
+        if (!tc::mbar_wait(&tempty[st], ((j / TS) & 1) ^ 1)) {
           set_device_error(a.err, kErrBounds);
           *abort_flag = 1;
           break;
         }
-        tc::mbar_arrive_expect_tx(&tfull[st], C::T_BYTES);
+        tc::mbar_arrive_expect_tx(&tfull[st], C::T_STAGE);
+        if (PHASE == 1) {
 #pragma unroll
-        for (int p = 0; p < NP; ++p) {
-          const uint16_t *tr = a.trellis + ((long)e * a.nslots + p) * a.slot_words;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const long tk = (long)i * 4 + j;
-            ftc::bulk_copy(sT + st * C::T_BYTES + p * C::T_ONE + j * S::ROWB, tr + (tk * a.tiles_n + tn0) * 16 * K,
-                           S::ROWB, &tfull[st]);
-          }
+          for (int p = 0; p < 2; ++p)
+            tc::tma_load_2d(sT + st * C::T_STAGE + p * 8 * C::ROWB, &tmT, &tfull[st], tn0 * (4 * K),
+                            (e * a.nslots + p) * a.tiles_k + 8 * j);
+        } else {
+          tc::tma_load_2d(sT + st * C::T_STAGE, &tmT, &tfull[st], tn0 * (4 * K), e * a.tiles_k + 16 * j);
         }
       }
     }
-  } else if (warp == 2) {
-    // ---------------- x' producer: the tile's sorted rows
+  } else if (warp == kXWarp) {
+    // ---------------- x' producer: the pair's two B operands (phase 1: x'g
+    // and x'u of k step P; phase 2: h' of k steps 2P, 2P + 1), 32 KB per load
     if (lane == 0) {
-      for (int i = 0; i < KB && !*abort_flag; ++i) {
-        const int st = i % XS;
-        if (!tc::mbar_wait(&xempty[st], ((i / XS) & 1) ^ 1)) {
+      for (int P = 0; P < npairs && !*abort_flag; ++P) {
+        const int st = P % XS;
+        if (!tc::mbar_wait(&xempty[st], ((P / XS) & 1) ^ 1)) {
           set_device_error(a.err, kErrBounds);
           *abort_flag = 1;
           break;
         }
-        tc::mbar_arrive_expect_tx(&xfull[st], NP * X_BYTES);
-        tc::tma_load_2d(sX + st * NP * X_BYTES, &tmX0, &xfull[st], i * BK, row0);
-        if (NP == 2) tc::tma_load_2d(sX + st * NP * X_BYTES + X_BYTES, &tmX1, &xfull[st], i * BK, row0);
+        tc::mbar_arrive_expect_tx(&xfull[st], C::X_STAGE);
+        if (PHASE == 1) {
+          tc::tma_load_2d(sX + st * C::X_STAGE, &tmX0, &xfull[st], P * BK, row0);
+          tc::tma_load_2d(sX + st * C::X_STAGE + X_STEP, &tmX1, &xfull[st], P * BK, row0);
+        } else {
+          tc::tma_load_3d(sX + st * C::X_STAGE, &tmX0, &xfull[st], 0, row0, 2 * P);
+        }
       }
     }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer
+  } else if (warp <= NGRP) {
+    // ---------------- MMA issuers: warp 1 + g takes the pairs P = g, g + 2, ...
+    // into accumulators (g NP + p) * 128 (phase 1: p = gate, up)
     if (lane == 0) {
+      const int g = warp - 1;
       const uint32_t idesc = ftc::idesc_f16_amn(BN, XROWS);
-      for (int i = 0; i < KB; ++i) {
-        const int xs = i % XS, ws = i % WS;
-        const bool ok = tc::mbar_wait(&xfull[xs], (i / XS) & 1) && tc::mbar_wait(&wfull[ws], (i / WS) & 1);
+      bool stop = false;
+      for (int P = g; P < npairs; P += NGRP) {
+        const int xs = P % XS, ps = P % NPS;
+        const bool ok = tc::mbar_wait(&xfull[xs], (P / XS) & 1) && tc::mbar_wait(&wfull[ps], (P / NPS) & 1);
         if (!ok || *abort_flag) {
           set_device_error(a.err, kErrBounds);
           *abort_flag = 1;
+          stop = true;
           break;
         }
         tc::tc_fence_after();
 #pragma unroll
-        for (int p = 0; p < NP; ++p) {
-          const uint64_t ad = ftc::sdesc_mn_sw128(sW + (ws * NP + p) * W_BYTES, 1024, 2048);
-          const uint64_t bd = tc::sdesc_k_sw128(sX + (xs * NP + p) * X_BYTES);
+        for (int h = 0; h < 2; ++h) {
+          const int p = PHASE == 1 ? h : 0;
+          const uint32_t dcol = tmem_base + (uint32_t)((g * NP + p) * XROWS);
+          const uint64_t ad = ftc::sdesc_mn_sw128(sW + (2 * ps + h) * W_BYTES, 1024, 2048);
+          const uint64_t bd = tc::sdesc_k_sw128(sX + xs * C::X_STAGE + h * X_STEP);
+          const bool first = (P == g) && (PHASE == 1 || h == 0);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
-            tc::mma_f16(tmem_base + p * XROWS, ad + (uint64_t)((2 * 2048 * kk) >> 4), bd + 2 * kk, idesc,
-                        (i | kk) != 0 ? 1u : 0u);
+            tc::mma_f16(dcol, ad + (uint64_t)((2 * 2048 * kk) >> 4), bd + 2 * kk, idesc,
+                        (!first || kk != 0) ? 1u : 0u);
         }
-        tc::mma_commit(&wempty[ws]);
+        tc::mma_commit(&wempty[ps]);
         tc::mma_commit(&xempty[xs]);
       }
-      tc::mma_commit(accum);
+      if (!stop) tc::mma_commit(accum);
     }
   } else {
-    // ---------------- decoders: group g takes k steps i = g, g + 2, ...
+    // ---------------- decoders: group g takes the pairs P = g, g + 2, ...
     const int dw = warp - 3;
     const int grp = dw / NDEC, dt = (dw % NDEC) * 32 + lane;
-    constexpr int PER_P = 32 * S::LPT;
     // Epilogue operands, loaded now so that their latency hides behind the
     // decode: this lane's 4 columns of svh (gate, up) and suh (down), or of
     // svh (down) and the routing weights of the warp's rows (lane q holds
@@ -209,11 +230,11 @@ __global__ void __launch_bounds__(NWARPS * 32, 1) moe_fused_kernel(const __grid_
     {
       auto ld4 = [&](const __half *src, float (&o)[4]) {
         const uint2 r = __ldg(reinterpret_cast<const uint2 *>(src + col0 + 4 * lane));
-        const __half2 *h = reinterpret_cast<const __half2 *>(&r);
-        o[0] = __low2float(h[0]);
-        o[1] = __high2float(h[0]);
-        o[2] = __low2float(h[1]);
-        o[3] = __high2float(h[1]);
+        const __half2 *hh = reinterpret_cast<const __half2 *>(&r);
+        o[0] = __low2float(hh[0]);
+        o[1] = __high2float(hh[0]);
+        o[2] = __low2float(hh[1]);
+        o[3] = __high2float(hh[1]);
       };
       if (PHASE == 1) {
         ld4(a.svh13 + ((long)e * 2 + 0) * a.inter, ep_a);
@@ -225,55 +246,74 @@ __global__ void __launch_bounds__(NWARPS * 32, 1) moe_fused_kernel(const __grid_
         if (lane < XROWS / (NGRP * NDEC) && m < rows) row_w = a.weights[a.perm[row0 + m]];
       }
     }
-    for (int i = grp; i < KB; i += NGRP) {
-      const int ts = i % TS, bs = i % WS;
-      const bool ok = (*abort_flag) || (tc::mbar_wait(&tfull[ts], (i / TS) & 1) &&
-                                        tc::mbar_wait(&wempty[bs], ((i / WS) & 1) ^ 1));
+    for (int P = grp; P < npairs; P += NGRP) {
+      const int tj = P / 2, ts = tj % TS, ps = P % NPS;
+      const bool ok = (*abort_flag) || (tc::mbar_wait(&tfull[ts], (tj / TS) & 1) &&
+                                        tc::mbar_wait(&wempty[ps], ((P / NPS) & 1) ^ 1));
       if (!ok) {
         if (lane == 0) set_device_error(a.err, kErrBounds);
         *abort_flag = 1;
       }
-      for (int it = dt; it < C::ITEMS; it += NDEC * 32) {
-        const int p = it / PER_P;
-        int ti, q, swp;
-        ftc::item_map<K>(it % PER_P, ti, q, swp);
-        const int tkl = ti >> 3, tnl = ti & 7;
-        const uint8_t *tilep = sT + ts * C::T_BYTES + p * C::T_ONE + tkl * S::ROWB + tnl * 32 * K;
-        uint32_t w[S::NW + 1];
-        ftc::load_item<K>(tilep, q, w);
-        ftc::decode_rows<K, 0>(w, sW + (bs * NP + p) * W_BYTES, tkl * 16 + S::G * q, tnl * 16, swp);
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        // phase 1: projection h of k step P (stage rows h * 8 + (P % 2) * 4);
+        // phase 2: k step 2P + h (stage rows ((2P + h) % 4) * 4)
+        const int r0 = PHASE == 1 ? h * 8 + (P % 2) * 4 : ((2 * P + h) % 4) * 4;
+        const uint8_t *tst = sT + ts * C::T_STAGE + r0 * C::ROWB;
+        uint8_t *bst = sW + (2 * ps + h) * W_BYTES;
+        for (int it = dt; it < C::ITEMS; it += NDEC * 32) {
+          int ti, q, swp;
+          ftc::item_map<K>(it, ti, q, swp);
+          const int tkl = ti >> 3, tnl = ti & 7;
+          const uint8_t *tilep = tst + tkl * C::ROWB + tnl * 32 * K;
+          uint32_t w[S::NW + 1];
+          ftc::load_item<K>(tilep, q, w);
+          ftc::decode_rows<K, 0>(w, bst, tkl * 16 + S::G * q, tnl * 16, swp);
+        }
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic stores -> tensor-core reads
       __syncwarp();
       if (lane == 0) {
-        tc::mbar_arrive(&wfull[bs]);
-        tc::mbar_arrive(&tempty[ts]);
+        tc::mbar_arrive(&wfull[ps]);
+        tc::mbar_arrive(&tempty[ts]);   // the group's only pair in the stage
       }
     }
 
     // ---------------- epilogue
-    // (1) accumulators (lane = output column, column = row of the tile),
-    // times sigma, transposed into scratch [NP][rows][128] over the rings.
+    // (1) warps 3..6 (TMEM lanes 96-127, 0-31, 32-63, 64-95 = output columns)
+    // write issuer 0's plus issuer 1's accumulator of each projection, times
+    // sigma, transposed into a scratch [NP][rows][128] over the x' and weight
+    // rings (idle once every MMA has completed).
     float *scratch = reinterpret_cast<float *>(smem);
     if (warp < 7) {
-      bool ok = tc::mbar_wait(accum, 0);
-      ok = __all_sync(0xffffffffu, ok) && !*abort_flag;
-      if (!ok && lane == 0) set_device_error(a.err, kErrBounds);
+      bool okw = tc::mbar_wait(accum, 0);
+      okw = __all_sync(0xffffffffu, okw) && !*abort_flag;
+      if (!okw && lane == 0) set_device_error(a.err, kErrBounds);
       tc::tc_fence_after();
       const int lane_base = 32 * (warp & 3);
       const int ncol = lane_base + lane;
 #pragma unroll
       for (int p = 0; p < NP; ++p) {
         for (int m0 = 0; m0 < rows; m0 += 8) {
-          uint32_t r[8];
+          uint32_t r[8], u[8];
+          const uint32_t taddr = tmem_base + ((uint32_t)lane_base << 16) + (uint32_t)(p * XROWS + m0);
           asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
                        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
                          "=r"(r[7])
-                       : "r"(tmem_base + ((uint32_t)lane_base << 16) + (uint32_t)(p * XROWS + m0)));
+                       : "r"(taddr));
+          asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+                       : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]),
+                         "=r"(u[7])
+                       : "r"(taddr + (uint32_t)(NP * XROWS)));
           tc::tmem_ld_wait();
+          if (npairs < 2) {            // issuer 1 had no pair: its accumulators were never written
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            if (m0 + j < rows) scratch[(p * XROWS + m0 + j) * 128 + ncol] = __uint_as_float(r[j]) * kSigma;
+            for (int q = 0; q < 8; ++q) u[q] = 0u;
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            if (m0 + q < rows)
+              scratch[(p * XROWS + m0 + q) * 128 + ncol] = (__uint_as_float(r[q]) + __uint_as_float(u[q])) * kSigma;
         }
       }
       tc::tc_fence_before();
@@ -291,9 +331,9 @@ __global__ void __launch_bounds__(NWARPS * 32, 1) moe_fused_kernel(const __grid_
         fwht128_warp(u, lane);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const float g = v[q] * kRhtScale * ep_a[q];
+          const float gg = v[q] * kRhtScale * ep_a[q];
           const float uu = u[q] * kRhtScale * ep_b[q];
-          v[q] = g / (1.0f + expf(-g)) * uu * ep_c[q];   // h . suh_down
+          v[q] = gg / (1.0f + expf(-gg)) * uu * ep_c[q];   // h . suh_down
         }
         fwht128_warp(v, lane);
         __half2 o[2] = {__floats2half2_rn(v[0] * kRhtScale, v[1] * kRhtScale),
@@ -337,31 +377,45 @@ static PFN_cuTensorMapEncodeTiled_v12000 mf_tmap_fn() {
   return fn;
 }
 
-// rows x cols fp16 (cols contiguous), box 128 rows x 64, 128-byte swizzle.
-static int mf_tmap(CUtensorMap *m, const void *base, int rows, int cols) {
+static int mf_encode(CUtensorMap *m, CUtensorMapDataType dt, int rank, const void *base, const cuuint64_t *dims,
+                     const cuuint64_t *strides, const cuuint32_t *box, CUtensorMapSwizzle sw, const char *what) {
   auto fn = mf_tmap_fn();
   if (!fn) return exl3_fail(EXL3_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)mf::XROWS};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return exl3_fail(EXL3_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, dt, rank, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return exl3_fail(EXL3_ERR_CUDA, "cuTensorMapEncodeTiled (%s) failed (%d)", what, (int)r);
   return EXL3_OK;
 }
 
+// rows x cols fp16 (cols contiguous), box 128 rows x 64, 128-byte swizzle.
+static int mf_xmap(CUtensorMap *m, const void *base, int rows, int cols) {
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)mf::XROWS};
+  return mf_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, "x'");
+}
+
+// All experts' trellis of one projection kind, [E * nslots * (k/16)][(n/16) * 32K bytes] as u64:
+// one load brings box_rows tile rows of 8 tiles.
+static int mf_tmap(CUtensorMap *m, const uint16_t *trellis, long rows, int n, int K, int box_rows) {
+  cuuint64_t dims[2] = {(cuuint64_t)(n / 16) * 4 * K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(n / 16) * 32 * K};
+  cuuint32_t box[2] = {(cuuint32_t)(8 * 4 * K), (cuuint32_t)box_rows};
+  return mf_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, trellis, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   "trellis");
+}
+
 template <int PHASE>
-static int mf_launch(int K, const CUtensorMap &t0, const CUtensorMap &t1, const mf::Args &a, int grid,
-                     cudaStream_t s) {
+static int mf_launch(int K, const CUtensorMap &t0, const CUtensorMap &t1, const CUtensorMap &tt, const mf::Args &a,
+                     int grid, cudaStream_t s) {
   cudaError_t e = cudaSuccess;
-#define EXL3_MF(KK)                                                                                      \
-  case KK: {                                                                                             \
-    auto kfn = mf::moe_fused_kernel<KK, PHASE>;                                                          \
+#define EXL3_MF(KK)                                                                                         \
+  case KK: {                                                                                                \
+    auto kfn = mf::moe_fused_kernel<KK, PHASE>;                                                             \
     cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, mf::Cfg<KK, PHASE>::SMEM_BYTES); \
-    kfn<<<grid, mf::NWARPS * 32, mf::Cfg<KK, PHASE>::SMEM_BYTES, s>>>(t0, t1, a);                        \
-    e = cudaGetLastError();                                                                              \
+    kfn<<<grid, mf::kWarps * 32, mf::Cfg<KK, PHASE>::SMEM_BYTES, s>>>(t0, t1, tt, a);                       \
+    e = cudaGetLastError();                                                                                 \
   } break;
   switch (K) {
     EXL3_MF(1) EXL3_MF(2) EXL3_MF(3) EXL3_MF(4) EXL3_MF(5) EXL3_MF(6) EXL3_MF(7) EXL3_MF(8)
@@ -372,47 +426,50 @@ static int mf_launch(int K, const CUtensorMap &t0, const CUtensorMap &t1, const 
 }
 
 // Phase 1: xg, xu [U][hidden] fp16 sorted rows; w13 trellis [E][2][hidden/16][inter/16][16K].
-int exl3_launch_moe_fused_gateup(const uint16_t *xg, const uint16_t *xu, int U, int hidden, int inter, int K,
+int exl3_launch_moe_fused_gateup(const uint16_t *xg, const uint16_t *xu, int U, int hidden, int inter, int K, int E,
                                  const uint16_t *w13_trellis, const int *mtiles, const int *n_mtiles, int max_mtiles,
                                  const uint16_t *svh13, const uint16_t *suh2, uint16_t *hout, int *err,
                                  cudaStream_t s) {
-  CUtensorMap t0, t1;
-  int rc = mf_tmap(&t0, xg, U, hidden);
-  if (rc) return rc;
-  rc = mf_tmap(&t1, xu, U, hidden);
+  CUtensorMap t0, t1, tt;
+  int rc = mf_xmap(&t0, xg, U, hidden);
+  if (!rc) rc = mf_xmap(&t1, xu, U, hidden);
+  if (!rc) rc = mf_tmap(&tt, w13_trellis, (long)E * 2 * (hidden / 16), inter, K, 8);
   if (rc) return rc;
   mf::Args a{};
   a.mtiles = reinterpret_cast<const int4 *>(mtiles);
   a.n_mtiles = n_mtiles;
   a.NT = inter / 128;
   a.KB = hidden / 64;
-  a.trellis = w13_trellis;
-  a.tiles_n = inter / 16;
-  a.slot_words = (long)(hidden / 16) * (inter / 16) * 16 * K;
+  a.tiles_k = hidden / 16;
   a.nslots = 2;
   a.svh13 = reinterpret_cast<const __half *>(svh13);
   a.suh2 = reinterpret_cast<const __half *>(suh2);
   a.hout = reinterpret_cast<__half *>(hout);
   a.inter = inter;
   a.err = err;
-  return mf_launch<1>(K, t0, t1, a, max_mtiles * a.NT, s);
+  return mf_launch<1>(K, t0, t1, tt, a, max_mtiles * a.NT, s);
 }
 
 // Phase 2: h' [U][inter] fp16 sorted rows; w2 trellis [E][1][inter/16][hidden/16][16K]; d [U][hidden] fp32.
-int exl3_launch_moe_fused_down(const uint16_t *hin, int U, int hidden, int inter, int K, const uint16_t *w2_trellis,
-                               const int *mtiles, const int *n_mtiles, int max_mtiles, const uint16_t *svh2,
-                               const float *weights, const int *perm, float *dout, int *err, cudaStream_t s) {
-  CUtensorMap t0;
-  int rc = mf_tmap(&t0, hin, U, inter);
+int exl3_launch_moe_fused_down(const uint16_t *hin, int U, int hidden, int inter, int K, int E,
+                               const uint16_t *w2_trellis, const int *mtiles, const int *n_mtiles, int max_mtiles,
+                               const uint16_t *svh2, const float *weights, const int *perm, float *dout, int *err,
+                               cudaStream_t s) {
+  CUtensorMap t0, tt;
+  // h' as (64 k, U rows, inter/64 blocks): one load brings two k steps of the tile's rows
+  cuuint64_t dims[3] = {64, (cuuint64_t)U, (cuuint64_t)(inter / 64)};
+  cuuint64_t strides[2] = {(cuuint64_t)inter * 2, 128};
+  cuuint32_t box[3] = {64, (cuuint32_t)mf::XROWS, 2};
+  int rc = mf_encode(&t0, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, hin, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
+                     "h'");
+  if (!rc) rc = mf_tmap(&tt, w2_trellis, (long)E * (inter / 16), hidden, K, 16);
   if (rc) return rc;
   mf::Args a{};
   a.mtiles = reinterpret_cast<const int4 *>(mtiles);
   a.n_mtiles = n_mtiles;
   a.NT = hidden / 128;
   a.KB = inter / 64;
-  a.trellis = w2_trellis;
-  a.tiles_n = hidden / 16;
-  a.slot_words = (long)(inter / 16) * (hidden / 16) * 16 * K;
+  a.tiles_k = inter / 16;
   a.nslots = 1;
   a.svh2 = reinterpret_cast<const __half *>(svh2);
   a.weights = weights;
@@ -420,5 +477,5 @@ int exl3_launch_moe_fused_down(const uint16_t *hin, int U, int hidden, int inter
   a.dout = dout;
   a.hidden = hidden;
   a.err = err;
-  return mf_launch<2>(K, t0, t0, a, max_mtiles * a.NT, s);
+  return mf_launch<2>(K, t0, t0, tt, a, max_mtiles * a.NT, s);
 }
