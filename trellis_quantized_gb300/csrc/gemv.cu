@@ -53,9 +53,14 @@ struct GemvShape {
   static constexpr int CTA_COLS = WC * COLW;     // 128 or 256
   static constexpr int NW = 4 * CPL;             // 32-bit stream words per lane
   static constexpr int ROWB = CTA_COLS * 2 * K;  // bytes of one row (CTA_COLS/16 tiles of 32K bytes)
-  static constexpr int R = ROWB >= 2048 ? WK : 2 * WK;   // rows per stage (one or two per k-warp)
+  // rows per stage: each k-warp takes RPW rows per wait, aiming at 16 KB
+  // stages (at least the one or two rows of a wide or narrow row, at most 4)
+  static constexpr int RPW_MIN = ROWB >= 2048 ? 1 : 2;
+  static constexpr int RPW_FIT = 16384 / (WK * ROWB);
+  static constexpr int RPW = RPW_FIT > 4 ? 4 : (RPW_FIT < RPW_MIN ? RPW_MIN : RPW_FIT);
+  static constexpr int R = RPW * WK;
   static constexpr int STAGE_B = R * ROWB;
-  static constexpr int STAGES = (32 * 1024) / STAGE_B < 2 ? 2 : (32 * 1024) / STAGE_B;
+  static constexpr int STAGES = (48 * 1024) / STAGE_B < 2 ? 2 : (48 * 1024) / STAGE_B;
   static constexpr int RING_B = STAGES * STAGE_B;
 };
 
@@ -389,6 +394,10 @@ struct Launcher {
     cudaGetLastError();
     if (sms <= 0) sms = 152;
     if (occ <= 0) occ = 1;
+    // three resident CTAs per SM: more rows per CTA between column-block
+    // flushes, still enough warps to hide the decode latencies (measured
+    // faster than four at k = 5120, n = 5120 ... 25600)
+    if (occ > 3) occ = 3;
     cached_k = k;
     cached = sms * occ;
     return cached;
