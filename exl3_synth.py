@@ -186,11 +186,12 @@ CONFIG5_T = (1, 128, 4096)
 
 
 def moe_case(config: int, sub: int, T: int, *, E: int = 256, topk: int = 8, hidden: int = 2048,
-             inter: int = 512, K: int = 3, name: str = "") -> MoECase:
-    """Routed experts: gate+up (nslots=2, hidden->inter each) and down (inter->hidden)."""
+             inter: int = 512, K: int = 3, K2: int = 0, name: str = "") -> MoECase:
+    """Routed experts: gate+up (nslots=2, hidden->inter each, K bits) and down
+    (inter->hidden, K2 bits; K2 = 0 means K)."""
     rng = rng_for(config, sub)
     w13 = expert_proj(rng, E, 2, hidden, inter, K)
-    w2 = expert_proj(rng, E, 1, inter, hidden, K)
+    w2 = expert_proj(rng, E, 1, inter, hidden, K2 or K)
     ids, w = routing(rng, T, E, topk)
     x = activations(rng, T, hidden)
     return MoECase(name or f"moe{config}.{sub}", T, hidden, inter, E, topk, K, x, ids, w, w13, w2)

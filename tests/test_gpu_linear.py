@@ -151,6 +151,14 @@ def test_linear_fused_small_m_all_widths(K):
     _check_case(synth.linear_case(16, K, 5, 1152, 384, K, outlier_rows=0.2))
 
 
+@pytest.mark.parametrize("K,k,M", [(3, 128, 4), (4, 128, 16), (8, 128, 100), (1, 256, 33), (6, 384, 17)])
+def test_linear_fused_small_m_short_k(K, k, M):
+    """k = 128 is a single pair of k steps (the second decoder group and its
+    accumulator stay idle); k = 256 and 384 give one and a half trellis stages;
+    M = 33 and 100 use the wide x' layout."""
+    _check_case(synth.linear_case(17, K * 1000 + k, M, k, 256, K, outlier_rows=0.1))
+
+
 @pytest.mark.parametrize("K,M", [(2, 8), (5, 8), (8, 64), (3, 64)])
 def test_linear_config3_small_m(K, M):
     _check_case(synth.config3(K, M))

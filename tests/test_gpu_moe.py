@@ -68,6 +68,16 @@ def test_moe_small_shapes(E, topk, T):
     assert_close(_run(c, d), _oracle(c), f"moe E{E} top{topk} T{T}")
 
 
+@pytest.mark.parametrize("K,K2,hidden,inter", [(8, 8, 256, 128), (5, 5, 512, 256), (1, 7, 256, 384), (6, 2, 768, 128)])
+def test_moe_widths_and_shapes(K, K2, hidden, inter):
+    """Every width on both projections (different widths for gate+up and down),
+    down projections of one and several k-step pairs, odd numbers of 128-row
+    output tiles."""
+    c = synth.moe_case(55, K * 10 + K2, 40, E=6, topk=3, hidden=hidden, inter=inter, K=K, K2=K2)
+    d = _dev_case(c)
+    assert_close(_run(c, d), _oracle(c), f"moe K{K}/{K2} h{hidden} i{inter}")
+
+
 def test_moe_many_rows_one_expert_spans_tiles():
     """300 rows on one expert: its rows cross two 128-row tiles plus a partial one."""
     c = synth.moe_case(52, 0, 150, E=3, topk=2, hidden=512, inter=256, K=2)
