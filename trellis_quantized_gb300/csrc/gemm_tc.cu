@@ -15,6 +15,7 @@
 //   warp 1     TMEM owner and MMA issuer (one thread): 4 x (M128 N256 K16) per stage
 //   warps 2-5  epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31, one output
 //              row per thread, two 128-column FWHTs in registers per tile
+//              (integer mode with 256-column tiles: warps 2-9, see below)
 // TMEM holds two 128 x BN fp32 accumulators so the epilogue of one tile
 // overlaps the MMAs of the next.
 //
@@ -25,6 +26,10 @@
 // [-127, 127] as fp16, every k-chunk of 512 accumulates in a fresh fp32
 // accumulator (|partial sum| <= 512 * 127^2 < 2^23, so every sum is exact),
 // and the epilogue converts each chunk to int32 and adds them in registers.
+// With 256-column tiles the epilogue has 8 warps (two per TMEM lane quarter,
+// 128 columns each), so the MMA reads 48 KB of operands per 512 tensor cycles
+// rather than 32 KB per 256 (the 128-column tile needed more shared-memory
+// bandwidth than the SM has).
 // The output is y = RHT_out(acc * row_scale[m] * weight_scale) . svh.
 #include <cudaTypedefs.h>
 
@@ -47,6 +52,12 @@ struct Cfg {
 };
 
 constexpr int Q8_CHUNK_KB = 8;   // k-blocks of 64 per exact fp32 chunk (512 elements)
+
+// Epilogue warps: the integer mode with 256-column tiles keeps each row's 256
+// running int32 sums in two warps of 128 registers (two warps per TMEM lane
+// quarter); otherwise four warps, one per lane quarter.
+template <int BN, bool Q8>
+constexpr int epi_warps() { return (Q8 && BN == 256) ? 8 : 4; }
 
 struct Args {
   int M, n, k;
@@ -100,7 +111,7 @@ __device__ __forceinline__ void store_row(const float (&v)[128], const Args &a, 
 }
 
 template <int BN, bool F32OUT, bool Q8>
-__global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+__global__ void __launch_bounds__((2 + epi_warps<BN, Q8>()) * 32, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                                                          const __grid_constant__ CUtensorMap tmB, Args a) {
   using C = Cfg<BN>;
   constexpr int STAGES = C::STAGES, A_BYTES = C::A_BYTES, B_BYTES = C::B_BYTES, STAGE_BYTES = C::STAGE_BYTES;
@@ -127,7 +138,7 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&tfull[b], 1);
-      tc::mbar_init(&tempty[b], 4);
+      tc::mbar_init(&tempty[b], epi_warps<BN, Q8>());
     }
     *abort_flag = 0;
     tc::fence_mbar_init();
@@ -198,8 +209,9 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
       }
     }
   } else {
-    // epilogue warps 2..5
+    // epilogue warps 2 .. 2 + epi_warps - 1
     const int lane_base = 32 * (warp & 3);
+    const int half = (Q8 && BN == 256) ? (warp - 2) / 4 : 0;   // integer mode: 128-column half
     int acc = 0;
     uint32_t acc_phase = 0;
     const int CH = Q8 ? Q8_CHUNK_KB : KB;
@@ -211,9 +223,10 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
       if (a.row_scale && row < a.M) rs *= a.row_scale[row];
       bool failed = false;
       if constexpr (Q8) {
-        // BN == 128: one 128-column block per tile, integer accumulation per
-        // chunk.  The int32 sums live in the same registers that later hold
-        // the float row (bit patterns), keeping one 128-entry array alive.
+        // One 128-column block per warp (BN == 256: two warps per row),
+        // integer accumulation per chunk.  The int32 sums live in the same
+        // registers that later hold the float row (bit patterns), keeping one
+        // 128-entry array alive.
         float v[128];
 #pragma unroll
         for (int i = 0; i < 128; ++i) v[i] = __int_as_float(0);
@@ -225,7 +238,7 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             float t[32];
-            tc::tmem_ld32(tmem_base + ((uint32_t)lane_base << 16) + (uint32_t)(acc * BN + 32 * c), t);
+            tc::tmem_ld32(tmem_base + ((uint32_t)lane_base << 16) + (uint32_t)(acc * BN + half * 128 + 32 * c), t);
             tc::tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 32; ++i)
@@ -241,7 +254,7 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
           *abort_flag = 1;
           break;
         }
-        const int col0 = nt * BN;
+        const int col0 = nt * BN + half * 128;
         if (a.acc_out && row < a.M) {
 #pragma unroll
           for (int c4 = 0; c4 < 32; ++c4)
@@ -335,7 +348,7 @@ int exl3_launch_gemm_tc(const uint16_t *xh, const uint16_t *wt, int M, int n, in
   CUtensorMap ta, tb;
   int rc = make_tmap_f16(&ta, xh, M, k, gtc::BM);
   if (rc) return rc;
-  const bool wide = !q8 && (n % 256) == 0;
+  const bool wide = (n % 256) == 0;
   rc = make_tmap_f16(&tb, wt, n, k, wide ? 256 : 128);
   if (rc) return rc;
   static int sms = 0;
@@ -352,9 +365,11 @@ int exl3_launch_gemm_tc(const uint16_t *xh, const uint16_t *wt, int M, int n, in
   do {                                                                                                \
     auto kfn = gtc::gemm_tc_kernel<BNV, F32, Q>;                                                      \
     cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, gtc::Cfg<BNV>::SMEM_BYTES); \
-    kfn<<<grid, 192, gtc::Cfg<BNV>::SMEM_BYTES, s>>>(ta, tb, a);                                      \
+    kfn<<<grid, (2 + gtc::epi_warps<BNV, Q>()) * 32, gtc::Cfg<BNV>::SMEM_BYTES, s>>>(ta, tb, a);       \
   } while (0)
-  if (q8) {
+  if (q8 && wide) {
+    if (f32out) EXL3_GTC(256, true, true); else EXL3_GTC(256, false, true);
+  } else if (q8) {
     if (f32out) EXL3_GTC(128, true, true); else EXL3_GTC(128, false, true);
   } else if (wide) {
     if (f32out) EXL3_GTC(256, true, false); else EXL3_GTC(256, false, false);
