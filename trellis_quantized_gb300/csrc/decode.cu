@@ -92,19 +92,13 @@ __global__ void __launch_bounds__(256) reconstruct_t_kernel(const uint16_t *__re
 // int8 weights ("exl3xpu" README, "Prefill: int8 linears and oneDNN fused
 // attention": one static weight scale, fused into reconstruct):
 // q_w = RNE(v * 127 / 3.453125) of the decoded fp16 weight v, an exact
-// rational.  v depends on the state only through the byte sum B, so each CTA
-// first fills a 1021-entry table q(B) in shared memory with exact integer
-// arithmetic: v = V * 2^-24 with V an integer and 3.453125 = 1768 * 2^-9, so
-// q = RNE(V * 127 / (1768 * 2^15)).
-__device__ __forceinline__ int quant_weight_of_bsum(int B) {
-  const float v = __half2float(__float2half_rn((float)(B - 510) * kSigma));
-  const long long V = __float2ll_rn(v * 16777216.0f);     // exact: v has 11 significant bits
-  const long long num = V * 127, den = 1768LL * 32768LL;
-  const long long an = num < 0 ? -num : num;
-  long long q = an / den;
-  const long long rem = an - q * den;
-  if (2 * rem > den || (2 * rem == den && (q & 1))) ++q;
-  return (int)(num < 0 ? -q : q);
+// rational.  One fp32 product v * fp32(127 / 3.453125) rounded to nearest
+// even gives that integer for every one of the 1021 codebook values (checked
+// exhaustively against exact rational arithmetic), so no table is needed.
+constexpr float kQ8Scale = 127.0f / 3.453125f;
+
+__device__ __forceinline__ __half mul1_q8(uint32_t s) {
+  return __int2half_rn(__float2int_rn(__half2float(mul1_half(s)) * kQ8Scale));
 }
 
 // Transposed reconstruct of q_w as integer-valued fp16: Wq[16 tn + c][16 tk + r].
@@ -113,10 +107,7 @@ __global__ void __launch_bounds__(256) reconstruct_q8_t_kernel(const uint16_t *_
                                                                int tiles_k, int tiles_n,
                                                                uint16_t *__restrict__ wq, int k) {
   __shared__ __align__(16) __half sm[32][128 + 8];
-  __shared__ __half qtab[1024];
   const int t = threadIdx.x;
-  for (int B = t; B < 1021; B += 256) qtab[B] = __int2half_rn(quant_weight_of_bsum(B));
-  __syncthreads();
   const int tile_local = t >> 4, r = t & 15;
   const int tkl = tile_local & 7, tnl = tile_local >> 3;
   const int tk = blockIdx.y * 8 + tkl, tn = blockIdx.x * 2 + tnl;
@@ -126,8 +117,7 @@ __global__ void __launch_bounds__(256) reconstruct_q8_t_kernel(const uint16_t *_
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
       const int bit = c * K;
-      const uint32_t s = window16(a[bit >> 5], a[(bit >> 5) + 1], bit & 31);
-      sm[tnl * 16 + c][tkl * 16 + r] = qtab[mul1_bsum(s)];
+      sm[tnl * 16 + c][tkl * 16 + r] = mul1_q8(window16(a[bit >> 5], a[(bit >> 5) + 1], bit & 31));
     }
   }
   __syncthreads();

@@ -10,36 +10,54 @@
 
 namespace exl3 {
 
-// x [M][k] fp16 -> out [M][k] fp32 (OUT_F32) or fp16.  One warp per block.
+// x [M][k] fp16 -> out [M][k] fp32 (OUT_F32) or fp16.  One warp per group of
+// up to four blocks of a row: all loads are issued before the transforms, so
+// each warp keeps 1 KB in flight.
+constexpr int kRhtGroup = 4;
+
 template <bool F32OUT>
 __global__ void __launch_bounds__(256) input_rht_kernel(const __half *__restrict__ x,
                                                         const __half *__restrict__ suh, int M, int k,
                                                         void *__restrict__ out) {
   const int lane = threadIdx.x & 31;
   const long wid = (long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int blocks = k >> 7;
-  if (wid >= (long)M * blocks) return;
-  const long row = wid / blocks;
-  const int col = (int)(wid % blocks) * 128 + lane * 4;
-  const uint2 xv = *reinterpret_cast<const uint2 *>(x + row * k + col);
-  const uint2 sv = *reinterpret_cast<const uint2 *>(suh + col);
-  const __half2 *xh = reinterpret_cast<const __half2 *>(&xv);
-  const __half2 *sh = reinterpret_cast<const __half2 *>(&sv);
-  float v[4];
-  v[0] = __low2float(xh[0]) * __low2float(sh[0]);   // exact: 11-bit x 11-bit significands
-  v[1] = __high2float(xh[0]) * __high2float(sh[0]);
-  v[2] = __low2float(xh[1]) * __low2float(sh[1]);
-  v[3] = __high2float(xh[1]) * __high2float(sh[1]);
-  fwht128_warp(v, lane);
+  const int blocks = k >> 7, groups = (blocks + kRhtGroup - 1) / kRhtGroup;
+  if (wid >= (long)M * groups) return;
+  const long row = wid / groups;
+  const int b0 = (int)(wid % groups) * kRhtGroup;
+  const int nb = min(kRhtGroup, blocks - b0);
+  uint2 xv[kRhtGroup], sv[kRhtGroup];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) v[j] = __fmul_rn(v[j], kRhtScale);
-  if (F32OUT) {
-    *reinterpret_cast<float4 *>(static_cast<float *>(out) + row * k + col) =
-        make_float4(v[0], v[1], v[2], v[3]);
-  } else {
-    __half2 o[2] = {__floats2half2_rn(v[0], v[1]), __floats2half2_rn(v[2], v[3])};
-    *reinterpret_cast<uint2 *>(static_cast<__half *>(out) + row * k + col) =
-        *reinterpret_cast<uint2 *>(o);
+  for (int j = 0; j < kRhtGroup; ++j) {
+    if (j < nb) {
+      const int col = (b0 + j) * 128 + lane * 4;
+      xv[j] = *reinterpret_cast<const uint2 *>(x + row * k + col);
+      sv[j] = __ldg(reinterpret_cast<const uint2 *>(suh + col));
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kRhtGroup; ++j) {
+    if (j < nb) {
+      const int col = (b0 + j) * 128 + lane * 4;
+      const __half2 *xh = reinterpret_cast<const __half2 *>(&xv[j]);
+      const __half2 *sh = reinterpret_cast<const __half2 *>(&sv[j]);
+      float v[4];
+      v[0] = __low2float(xh[0]) * __low2float(sh[0]);   // exact: 11-bit x 11-bit significands
+      v[1] = __high2float(xh[0]) * __high2float(sh[0]);
+      v[2] = __low2float(xh[1]) * __low2float(sh[1]);
+      v[3] = __high2float(xh[1]) * __high2float(sh[1]);
+      fwht128_warp(v, lane);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) v[q] = __fmul_rn(v[q], kRhtScale);
+      if (F32OUT) {
+        *reinterpret_cast<float4 *>(static_cast<float *>(out) + row * k + col) =
+            make_float4(v[0], v[1], v[2], v[3]);
+      } else {
+        __half2 o[2] = {__floats2half2_rn(v[0], v[1]), __floats2half2_rn(v[2], v[3])};
+        *reinterpret_cast<uint2 *>(static_cast<__half *>(out) + row * k + col) =
+            *reinterpret_cast<uint2 *>(o);
+      }
+    }
   }
 }
 
@@ -49,7 +67,7 @@ using namespace exl3;
 
 cudaError_t exl3_launch_input_rht(const uint16_t *x, int M, int k, const uint16_t *suh, void *out,
                                   bool f32out, cudaStream_t s) {
-  const long warps = (long)M * (k / 128);
+  const long warps = (long)M * ((k / 128 + kRhtGroup - 1) / kRhtGroup);
   const unsigned grid = (unsigned)((warps + 7) / 8);
   if (grid == 0) return cudaSuccess;
   const __half *xh = reinterpret_cast<const __half *>(x);
