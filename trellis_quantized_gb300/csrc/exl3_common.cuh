@@ -82,6 +82,34 @@ __device__ __forceinline__ void fwht128_warp(float v[4], int lane) {
   }
 }
 
+// The same transform with 16 contiguous values per lane: lanes 8j .. 8j + 7
+// of the warp hold one 128-block (lane l: elements 16 (l mod 8) + i), so a
+// warp transforms four blocks at once.  Stages h = 1, 2, 4, 8 stay in
+// registers, h = 16, 32, 64 exchange with lane l ^ 1, ^ 2, ^ 4 (three shuffle
+// stages instead of five).  The stage order and every rounding are those of
+// fwht128_warp: fma(+-1, v, partner) is the single-rounded sum or difference.
+__device__ __forceinline__ void fwht128_x8(float (&v)[16], int lane) {
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1)
+#pragma unroll
+    for (int i = 0; i < 16; i += 2 * h)
+#pragma unroll
+      for (int j = i; j < i + h; ++j) {
+        const float a = v[j], b = v[j + h];
+        v[j] = a + b;
+        v[j + h] = a - b;
+      }
+#pragma unroll
+  for (int m = 1; m < 8; m <<= 1) {
+    const float sgn = (lane & m) ? -1.0f : 1.0f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float other = __shfl_xor_sync(0xffffffffu, v[j], m);
+      v[j] = fmaf(sgn, v[j], other);
+    }
+  }
+}
+
 // ------------------------------------------------------------ small helpers --
 
 __device__ __forceinline__ void set_device_error(int *err, int bit) {

@@ -160,28 +160,45 @@ __global__ void __launch_bounds__(256) gather_rht_kernel(const __half *__restric
   const __half *xr = x + (long)t * hidden;
   const __half *sg = suh13 + (long)e * 2 * hidden, *su = sg + hidden;
   __half *dg = xg + (long)i * hidden, *du = xu + (long)i * hidden;
-#pragma unroll 4
-  for (int col = lane * 4; col < hidden; col += 128) {
-    const uint2 xv = *reinterpret_cast<const uint2 *>(xr + col);
-    const uint2 gv = __ldg(reinterpret_cast<const uint2 *>(sg + col));
-    const uint2 uv = __ldg(reinterpret_cast<const uint2 *>(su + col));
-    const __half2 *xh = reinterpret_cast<const __half2 *>(&xv);
-    const __half2 *gh = reinterpret_cast<const __half2 *>(&gv);
-    const __half2 *uh = reinterpret_cast<const __half2 *>(&uv);
-    const float x0 = __low2float(xh[0]), x1 = __high2float(xh[0]), x2 = __low2float(xh[1]),
-                x3 = __high2float(xh[1]);
-    float a[4] = {x0 * __low2float(gh[0]), x1 * __high2float(gh[0]), x2 * __low2float(gh[1]),
-                  x3 * __high2float(gh[1])};
-    float b[4] = {x0 * __low2float(uh[0]), x1 * __high2float(uh[0]), x2 * __low2float(uh[1]),
-                  x3 * __high2float(uh[1])};
-    fwht128_warp(a, lane);
-    fwht128_warp(b, lane);
-    __half2 og[2] = {__floats2half2_rn(a[0] * kRhtScale, a[1] * kRhtScale),
-                     __floats2half2_rn(a[2] * kRhtScale, a[3] * kRhtScale)};
-    __half2 ou[2] = {__floats2half2_rn(b[0] * kRhtScale, b[1] * kRhtScale),
-                     __floats2half2_rn(b[2] * kRhtScale, b[3] * kRhtScale)};
-    *reinterpret_cast<uint2 *>(dg + col) = *reinterpret_cast<uint2 *>(og);
-    *reinterpret_cast<uint2 *>(du + col) = *reinterpret_cast<uint2 *>(ou);
+  // a pass covers 512 elements (four 128-blocks): lane l holds 16 contiguous
+  // elements, col = 512 p + 16 l (fwht128_x8 layout)
+  for (int c0 = 0; c0 < hidden; c0 += 512) {
+    const int col = c0 + 16 * lane;
+    const bool in = col < hidden;      // whole 128-blocks are in or out (hidden % 128 == 0)
+    uint4 xv[2] = {}, gv[2] = {}, uv[2] = {};
+    if (in) {
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        xv[q] = *reinterpret_cast<const uint4 *>(xr + col + 8 * q);
+        gv[q] = __ldg(reinterpret_cast<const uint4 *>(sg + col + 8 * q));
+        uv[q] = __ldg(reinterpret_cast<const uint4 *>(su + col + 8 * q));
+      }
+    }
+    const __half *xh = reinterpret_cast<const __half *>(xv);
+    const __half *gh = reinterpret_cast<const __half *>(gv);
+    const __half *uh = reinterpret_cast<const __half *>(uv);
+    float a[16], b[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float xx = __half2float(xh[j]);
+      a[j] = xx * __half2float(gh[j]);
+      b[j] = xx * __half2float(uh[j]);
+    }
+    fwht128_x8(a, lane);
+    fwht128_x8(b, lane);
+    if (in) {
+      __align__(16) __half2 og[8], ou[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        og[j] = __floats2half2_rn(a[2 * j] * kRhtScale, a[2 * j + 1] * kRhtScale);
+        ou[j] = __floats2half2_rn(b[2 * j] * kRhtScale, b[2 * j + 1] * kRhtScale);
+      }
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        *reinterpret_cast<uint4 *>(dg + col + 8 * q) = reinterpret_cast<const uint4 *>(og)[q];
+        *reinterpret_cast<uint4 *>(du + col + 8 * q) = reinterpret_cast<const uint4 *>(ou)[q];
+      }
+    }
   }
 }
 

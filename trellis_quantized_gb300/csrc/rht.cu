@@ -11,9 +11,8 @@
 namespace exl3 {
 
 // x [M][k] fp16 -> out [M][k] fp32 (OUT_F32) or fp16.  One warp per group of
-// up to four blocks of a row: all loads are issued before the transforms, so
-// each warp keeps 1 KB in flight.
-constexpr int kRhtGroup = 4;
+// four 128-blocks of a row (512 elements, 16 contiguous per lane: the
+// fwht128_x8 layout).
 
 template <bool F32OUT>
 __global__ void __launch_bounds__(256) input_rht_kernel(const __half *__restrict__ x,
@@ -21,43 +20,39 @@ __global__ void __launch_bounds__(256) input_rht_kernel(const __half *__restrict
                                                         void *__restrict__ out) {
   const int lane = threadIdx.x & 31;
   const long wid = (long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int blocks = k >> 7, groups = (blocks + kRhtGroup - 1) / kRhtGroup;
-  if (wid >= (long)M * groups) return;
+  const int groups = (k + 511) / 512;
+  if (wid >= (long)M * groups) return;            // uniform per warp
   const long row = wid / groups;
-  const int b0 = (int)(wid % groups) * kRhtGroup;
-  const int nb = min(kRhtGroup, blocks - b0);
-  uint2 xv[kRhtGroup], sv[kRhtGroup];
+  const int col = (int)(wid % groups) * 512 + 16 * lane;
+  const bool in = col < k;                        // whole 128-blocks are in or out
+  uint4 xv[2] = {}, sv[2] = {};
+  if (in) {
 #pragma unroll
-  for (int j = 0; j < kRhtGroup; ++j) {
-    if (j < nb) {
-      const int col = (b0 + j) * 128 + lane * 4;
-      xv[j] = *reinterpret_cast<const uint2 *>(x + row * k + col);
-      sv[j] = __ldg(reinterpret_cast<const uint2 *>(suh + col));
+    for (int q = 0; q < 2; ++q) {
+      xv[q] = *reinterpret_cast<const uint4 *>(x + row * k + col + 8 * q);
+      sv[q] = __ldg(reinterpret_cast<const uint4 *>(suh + col + 8 * q));
     }
   }
+  const __half *xh = reinterpret_cast<const __half *>(xv);
+  const __half *sh = reinterpret_cast<const __half *>(sv);
+  float v[16];
 #pragma unroll
-  for (int j = 0; j < kRhtGroup; ++j) {
-    if (j < nb) {
-      const int col = (b0 + j) * 128 + lane * 4;
-      const __half2 *xh = reinterpret_cast<const __half2 *>(&xv[j]);
-      const __half2 *sh = reinterpret_cast<const __half2 *>(&sv[j]);
-      float v[4];
-      v[0] = __low2float(xh[0]) * __low2float(sh[0]);   // exact: 11-bit x 11-bit significands
-      v[1] = __high2float(xh[0]) * __high2float(sh[0]);
-      v[2] = __low2float(xh[1]) * __low2float(sh[1]);
-      v[3] = __high2float(xh[1]) * __high2float(sh[1]);
-      fwht128_warp(v, lane);
+  for (int j = 0; j < 16; ++j) v[j] = __half2float(xh[j]) * __half2float(sh[j]);   // exact
+  fwht128_x8(v, lane);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) v[q] = __fmul_rn(v[q], kRhtScale);
-      if (F32OUT) {
-        *reinterpret_cast<float4 *>(static_cast<float *>(out) + row * k + col) =
-            make_float4(v[0], v[1], v[2], v[3]);
-      } else {
-        __half2 o[2] = {__floats2half2_rn(v[0], v[1]), __floats2half2_rn(v[2], v[3])};
-        *reinterpret_cast<uint2 *>(static_cast<__half *>(out) + row * k + col) =
-            *reinterpret_cast<uint2 *>(o);
-      }
-    }
+  for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], kRhtScale);
+  if (!in) return;
+  if (F32OUT) {
+    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(out) + row * k + col);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+  } else {
+    __align__(16) __half2 o[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) o[j] = __floats2half2_rn(v[2 * j], v[2 * j + 1]);
+    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__half *>(out) + row * k + col);
+    dst[0] = reinterpret_cast<const uint4 *>(o)[0];
+    dst[1] = reinterpret_cast<const uint4 *>(o)[1];
   }
 }
 
@@ -67,7 +62,7 @@ using namespace exl3;
 
 cudaError_t exl3_launch_input_rht(const uint16_t *x, int M, int k, const uint16_t *suh, void *out,
                                   bool f32out, cudaStream_t s) {
-  const long warps = (long)M * ((k / 128 + kRhtGroup - 1) / kRhtGroup);
+  const long warps = (long)M * ((k + 511) / 512);
   const unsigned grid = (unsigned)((warps + 7) / 8);
   if (grid == 0) return cudaSuccess;
   const __half *xh = reinterpret_cast<const __half *>(x);
@@ -95,23 +90,35 @@ __global__ void __launch_bounds__(256) quant_act_kernel(const __half *__restrict
   __shared__ float wmax[8];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const long row = blockIdx.x;
-  const int blocks = k >> 7;
   float m = 0.f;
-  for (int b = warp; b < blocks; b += 8) {
-    const int col = b * 128 + lane * 4;
-    const uint2 xv = *reinterpret_cast<const uint2 *>(x + row * k + col);
-    const uint2 sv = *reinterpret_cast<const uint2 *>(suh + col);
-    const __half2 *xh = reinterpret_cast<const __half2 *>(&xv);
-    const __half2 *sh = reinterpret_cast<const __half2 *>(&sv);
-    float v[4] = {__low2float(xh[0]) * __low2float(sh[0]), __high2float(xh[0]) * __high2float(sh[0]),
-                  __low2float(xh[1]) * __low2float(sh[1]), __high2float(xh[1]) * __high2float(sh[1])};
-    fwht128_warp(v, lane);
+  // warp w takes the 512-element groups w, w + 8, ... (fwht128_x8 layout)
+  for (int c0 = warp * 512; c0 < k; c0 += 8 * 512) {
+    const int col = c0 + 16 * lane;
+    const bool in = col < k;
+    uint4 xv[2] = {}, sv[2] = {};
+    if (in) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+      for (int q = 0; q < 2; ++q) {
+        xv[q] = *reinterpret_cast<const uint4 *>(x + row * k + col + 8 * q);
+        sv[q] = __ldg(reinterpret_cast<const uint4 *>(suh + col + 8 * q));
+      }
+    }
+    const __half *xh = reinterpret_cast<const __half *>(xv);
+    const __half *sh = reinterpret_cast<const __half *>(sv);
+    float v[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = __half2float(xh[j]) * __half2float(sh[j]);
+    fwht128_x8(v, lane);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
       v[j] = __fmul_rn(v[j], kRhtScale);
       m = fmaxf(m, fabsf(v[j]));
     }
-    *reinterpret_cast<float4 *>(xr + col) = make_float4(v[0], v[1], v[2], v[3]);
+    if (in) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<float4 *>(xr + col + 4 * q) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
