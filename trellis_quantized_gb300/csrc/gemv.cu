@@ -43,8 +43,11 @@ namespace exl3 {
 
 template <int K>
 struct GemvShape {
-  static constexpr int G = 8 / gcd_c(K, 8);      // rows per lane
-  static constexpr int CPL = K / gcd_c(K, 8);    // 16-byte chunks per lane
+  // rows per lane item: a whole number of 16-byte chunks, and at least four
+  // rows so that per-item costs (loads, x', loop) are shared by 64+ weights
+  static constexpr int G0 = 8 / gcd_c(K, 8);
+  static constexpr int G = G0 < 4 ? 4 : G0;
+  static constexpr int CPL = K * G / 8;          // 16-byte chunks per lane
   static constexpr int LPT = 16 / G;             // lanes per tile
   static constexpr int TPW = 32 / LPT;           // tiles per warp
   static constexpr int COLW = TPW * 16;          // columns per warp
