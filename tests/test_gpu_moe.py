@@ -112,3 +112,21 @@ def test_moe_slot_order_does_not_matter():
     y2 = _run(c, d, ids=dev(np.ascontiguousarray(c.ids[:, perm])),
               weights=dev(np.ascontiguousarray(c.weights[:, perm])))
     assert np.max(np.abs(y1 - y2)) <= 2e-3 * max(1.0, np.abs(y1).max())
+
+
+@pytest.mark.parametrize("E,topk,T,hidden,inter,K", [(8, 2, 2, 1024, 256, 4), (16, 4, 3, 2048, 128, 3),
+                                                     (4, 4, 1, 512, 384, 5)])
+def test_moe_gateup_split_over_k(E, topk, T, hidden, inter, K):
+    """Few tokens: the gate+up projection is split over k across CTAs and the
+    last CTA of each tile adds the partial sums in split order.  Same result on
+    a second call (fixed order) and the arrival counters are back at zero."""
+    c = synth.moe_case(56, E * 100 + T, T, E=E, topk=topk, hidden=hidden, inter=inter, K=K)
+    d = _dev_case(c)
+    ws = torch.zeros(tq.exl3_moe_workspace_size(c.T, c.topk, c.E, d["w13"], d["w2"]), dtype=torch.uint8,
+                     device="cuda")
+    y1 = tq.exl3_moe_grouped(d["x"], d["ids"], d["w"], d["w13"], d["w2"], c.E, workspace_buf=ws).clone()
+    y2 = tq.exl3_moe_grouped(d["x"], d["ids"], d["w"], d["w13"], d["w2"], c.E, workspace_buf=ws).clone()
+    assert torch.equal(y1, y2)
+    assert tq.exl3_check_device_error(ws) == 0
+    assert int(ws[256:256 + 4 * 8192].view(torch.int32).abs().sum()) == 0
+    assert_close(host(y1).astype(np.float64), _oracle(c), f"moe split E{E} T{T}")

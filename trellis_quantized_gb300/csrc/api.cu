@@ -43,8 +43,8 @@ cudaError_t exl3_launch_moe_combine(const float *d, const int *pos, int T, int t
                                     bool f32out, cudaStream_t s);
 int exl3_launch_moe_fused_gateup(const uint16_t *xg, const uint16_t *xu, int U, int hidden, int inter, int K, int E,
                                  const uint16_t *w13_trellis, const int *mtiles, const int *n_mtiles, int max_mtiles,
-                                 const uint16_t *svh13, const uint16_t *suh2, uint16_t *hout, int *err,
-                                 cudaStream_t s);
+                                 const uint16_t *svh13, const uint16_t *suh2, uint16_t *hout, int splits,
+                                 float *partials, int *counters, int *err, cudaStream_t s);
 int exl3_launch_moe_fused_down(const uint16_t *hin, int U, int hidden, int inter, int K, int E,
                                const uint16_t *w2_trellis,
                                const int *mtiles, const int *n_mtiles, int max_mtiles, const uint16_t *svh2,
@@ -184,8 +184,8 @@ LinearInt8Ws linear_int8_ws(int M, int k, int n) {
 
 // ---- exl3_moe_grouped workspace layout
 struct MoeWs {
-  size_t counts, offsets, pos, perm, mtiles, n_mtiles, chunk, xg, xu, h, d, total;
-  int max_mtiles;
+  size_t counts, offsets, pos, perm, mtiles, n_mtiles, chunk, xg, xu, h, d, partials, total;
+  int max_mtiles, grid_mtiles, splits;
 };
 
 MoeWs moe_ws(int T, int topk, int E, int hidden, int inter) {
@@ -206,6 +206,17 @@ MoeWs moe_ws(int T, int topk, int E, int hidden, int inter) {
   w.xu = take(sizeof(uint16_t) * U * hidden);
   w.h = take(sizeof(uint16_t) * U * inter);
   w.d = take(sizeof(float) * U * hidden);
+  // Every 128-row tile holds at least one unit, so the grouped kernels need
+  // at most min(U, max_mtiles) tiles per output column block.  When those
+  // tiles cannot fill half the SMs (few tokens), the gate+up projection is
+  // split over k into an even number of k steps (at least 4) per CTA.
+  w.grid_mtiles = (int)(U < (size_t)w.max_mtiles ? U : (size_t)w.max_mtiles);
+  const long tiles1 = (long)w.grid_mtiles * (inter / 128);
+  const int kb = hidden / 64, sms = sm_count();
+  w.splits = 1;
+  for (int sp = 2; sp <= 8; ++sp)
+    if (kb % sp == 0 && (kb / sp) % 2 == 0 && kb / sp >= 4 && tiles1 * sp <= sms) w.splits = sp;
+  if (w.splits > 1) w.partials = take(sizeof(float) * (size_t)tiles1 * w.splits * 2 * 128 * 128);
   w.total = off;
   return w;
 }
@@ -415,9 +426,12 @@ int exl3_moe_grouped(const uint16_t *x, int T, int hidden, const int32_t *topk_i
   EXL3_TRY(exl3_cuda_check(exl3_launch_moe_gather(x, U, hidden, topk, perm, offsets, E, topk_ids, w13->suh, xg, xu,
                                                   stream),
                            "moe gather launch"));
+  float *partials = L.splits > 1 ? at<float>(workspace, L.partials) : nullptr;
+  int *counters = at<int>(workspace, kCounterOff);   // the fixed counter region, zero between calls
   EXL3_TRY(exl3_launch_moe_fused_gateup(xg, xu, U, hidden, inter, w13->K, E, w13->trellis, mtiles, n_mtiles,
-                                        L.max_mtiles, w13->svh, w2->suh, h, err, stream));
-  EXL3_TRY(exl3_launch_moe_fused_down(h, U, hidden, inter, w2->K, E, w2->trellis, mtiles, n_mtiles, L.max_mtiles,
+                                        L.grid_mtiles, w13->svh, w2->suh, h, L.splits, partials, counters, err,
+                                        stream));
+  EXL3_TRY(exl3_launch_moe_fused_down(h, U, hidden, inter, w2->K, E, w2->trellis, mtiles, n_mtiles, L.grid_mtiles,
                                       w2->svh, topk_weights, perm, d, err, stream));
   return exl3_cuda_check(exl3_launch_moe_combine(d, pos, T, topk, hidden, y, out_dtype == EXL3_OUT_F32, stream),
                          "moe combine launch");

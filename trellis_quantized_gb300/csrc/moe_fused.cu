@@ -76,6 +76,12 @@ struct Args {
   float *dout;              // [U][hidden]
   int hidden;
   int *err;
+  // phase 1 split over k (small token counts): CTA blockIdx.x takes split
+  // blockIdx.x % splits of tile blockIdx.x / splits; the last CTA of a tile
+  // to arrive adds the partial sums in split order
+  int splits;
+  float *partials;          // [tiles][splits][2][128][128] fp32
+  int *counters;            // [tiles], zero between calls
 };
 
 template <int K, int PHASE>
@@ -85,13 +91,16 @@ __global__ void __launch_bounds__(kWarps * 32, 1) moe_fused_kernel(const __grid_
   using C = Cfg<K, PHASE>;
   using S = ftc::Shape<K, 32>;
   constexpr int NP = C::NP, XS = C::XS, TS = C::TS, NPS = C::NPS;
-  const int tile = blockIdx.x;
+  const int tile = blockIdx.x / a.splits, split = blockIdx.x % a.splits;
   if (tile >= *a.n_mtiles * a.NT) return;   // uniform per CTA: the tile list is device-side
   const int4 mt = a.mtiles[tile / a.NT];
   const int nt = tile % a.NT, e = mt.x, row0 = mt.y, rows = mt.z;
   const int tn0 = nt * (BN / 16);
   const int KB = a.KB;
-  const int npairs = PHASE == 1 ? KB : KB / 2;       // KB is even
+  // this CTA's pairs: absolute pair P0 + P for P < npairs (P0 even, so a
+  // trellis stage still holds pairs 2j, 2j + 1 of the range)
+  const int npairs = (PHASE == 1 ? KB : KB / 2) / a.splits;
+  const int P0 = split * npairs;
   const int ntst = (npairs + 1) / 2;                 // a trellis stage holds two pairs
 
   extern __shared__ uint8_t smem_raw[];
@@ -109,6 +118,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) moe_fused_kernel(const __grid_
   uint64_t *accum = wempty + NPS;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accum + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  volatile int *s_last = abort_flag + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -157,7 +167,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) moe_fused_kernel(const __grid_
 #pragma unroll
           for (int p = 0; p < 2; ++p)
             tc::tma_load_2d(sT + st * C::T_STAGE + p * 8 * C::ROWB, &tmT, &tfull[st], tn0 * (4 * K),
-                            (e * a.nslots + p) * a.tiles_k + 8 * j);
+                            (e * a.nslots + p) * a.tiles_k + 4 * P0 + 8 * j);
         } else {
           tc::tma_load_2d(sT + st * C::T_STAGE, &tmT, &tfull[st], tn0 * (4 * K), e * a.tiles_k + 16 * j);
         }
@@ -176,8 +186,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1) moe_fused_kernel(const __grid_
         }
         tc::mbar_arrive_expect_tx(&xfull[st], C::X_STAGE);
         if (PHASE == 1) {
-          tc::tma_load_2d(sX + st * C::X_STAGE, &tmX0, &xfull[st], P * BK, row0);
-          tc::tma_load_2d(sX + st * C::X_STAGE + X_STEP, &tmX1, &xfull[st], P * BK, row0);
+          tc::tma_load_2d(sX + st * C::X_STAGE, &tmX0, &xfull[st], (P0 + P) * BK, row0);
+          tc::tma_load_2d(sX + st * C::X_STAGE + X_STEP, &tmX1, &xfull[st], (P0 + P) * BK, row0);
         } else {
           tc::tma_load_3d(sX + st * C::X_STAGE, &tmX0, &xfull[st], 0, row0, 2 * P);
         }
@@ -319,8 +329,48 @@ __global__ void __launch_bounds__(kWarps * 32, 1) moe_fused_kernel(const __grid_
       tc::tc_fence_before();
     }
     asm volatile("bar.sync 1, %0;" ::"n"(NGRP * NDEC * 32) : "memory");
+    bool finish = true;
+    if (PHASE == 1 && a.splits > 1) {
+      // split over k: store this split's sums, count the arrival; the last CTA
+      // of the tile adds all splits in order (no CTA waits for another)
+      constexpr int TILE_F = 2 * XROWS * 128;
+      float *part = a.partials + ((long)tile * a.splits + split) * TILE_F;
+#pragma unroll
+      for (int p = 0; p < 2; ++p)
+        for (int m = dw; m < rows; m += NGRP * NDEC)
+          *reinterpret_cast<float4 *>(part + (p * XROWS + m) * 128 + 4 * lane) =
+              *reinterpret_cast<const float4 *>(scratch + (p * XROWS + m) * 128 + 4 * lane);
+      __threadfence();
+      asm volatile("bar.sync 1, %0;" ::"n"(NGRP * NDEC * 32) : "memory");
+      if (dw == 0 && lane == 0) {
+        const int old = atomicAdd(a.counters + tile, 1);
+        if (old >= a.splits) set_device_error(a.err, kErrDirtyCounter);
+        *s_last = (old == a.splits - 1);
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(NGRP * NDEC * 32) : "memory");
+      finish = *s_last != 0;
+      if (finish) {
+        __threadfence();
+        const float *base = a.partials + (long)tile * a.splits * TILE_F;
+#pragma unroll
+        for (int p = 0; p < 2; ++p)
+          for (int m = dw; m < rows; m += NGRP * NDEC) {   // the rows this warp transforms below
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int sp = 0; sp < a.splits; ++sp) {
+              const float4 t = __ldcg(reinterpret_cast<const float4 *>(base + sp * TILE_F + (p * XROWS + m) * 128 + 4 * lane));
+              acc.x += t.x;
+              acc.y += t.y;
+              acc.z += t.z;
+              acc.w += t.w;
+            }
+            *reinterpret_cast<float4 *>(scratch + (p * XROWS + m) * 128 + 4 * lane) = acc;
+          }
+        if (dw == 0 && lane == 0) a.counters[tile] = 0;   // leave the workspace clean
+        __syncwarp();
+      }
+    }
     // (2) one warp per row of the tile
-    for (int m = dw; m < rows; m += NGRP * NDEC) {
+    for (int m = dw; finish && m < rows; m += NGRP * NDEC) {
       const long row = (long)row0 + m;
       const float4 g4 = *reinterpret_cast<const float4 *>(scratch + m * 128 + 4 * lane);
       float v[4] = {g4.x, g4.y, g4.z, g4.w};
@@ -426,10 +476,12 @@ static int mf_launch(int K, const CUtensorMap &t0, const CUtensorMap &t1, const 
 }
 
 // Phase 1: xg, xu [U][hidden] fp16 sorted rows; w13 trellis [E][2][hidden/16][inter/16][16K].
+// splits > 1 (k split of the gate+up projection): partials [max_mtiles * inter/128][splits][2][128][128]
+// fp32 and counters [max_mtiles * inter/128], zero on entry and left zero.
 int exl3_launch_moe_fused_gateup(const uint16_t *xg, const uint16_t *xu, int U, int hidden, int inter, int K, int E,
                                  const uint16_t *w13_trellis, const int *mtiles, const int *n_mtiles, int max_mtiles,
-                                 const uint16_t *svh13, const uint16_t *suh2, uint16_t *hout, int *err,
-                                 cudaStream_t s) {
+                                 const uint16_t *svh13, const uint16_t *suh2, uint16_t *hout, int splits,
+                                 float *partials, int *counters, int *err, cudaStream_t s) {
   CUtensorMap t0, t1, tt;
   int rc = mf_xmap(&t0, xg, U, hidden);
   if (!rc) rc = mf_xmap(&t1, xu, U, hidden);
@@ -447,7 +499,10 @@ int exl3_launch_moe_fused_gateup(const uint16_t *xg, const uint16_t *xu, int U, 
   a.hout = reinterpret_cast<__half *>(hout);
   a.inter = inter;
   a.err = err;
-  return mf_launch<1>(K, t0, t1, tt, a, max_mtiles * a.NT, s);
+  a.splits = splits;
+  a.partials = partials;
+  a.counters = counters;
+  return mf_launch<1>(K, t0, t1, tt, a, max_mtiles * a.NT * splits, s);
 }
 
 // Phase 2: h' [U][inter] fp16 sorted rows; w2 trellis [E][1][inter/16][hidden/16][16K]; d [U][hidden] fp32.
@@ -477,5 +532,6 @@ int exl3_launch_moe_fused_down(const uint16_t *hin, int U, int hidden, int inter
   a.dout = dout;
   a.hidden = hidden;
   a.err = err;
+  a.splits = 1;
   return mf_launch<2>(K, t0, t0, tt, a, max_mtiles * a.NT, s);
 }
