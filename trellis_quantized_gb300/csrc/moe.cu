@@ -153,16 +153,19 @@ __global__ void __launch_bounds__(256) gather_rht_kernel(const __half *__restric
                                                          const __half *__restrict__ suh13,  // [E][2][hidden]
                                                          __half *__restrict__ xg, __half *__restrict__ xu) {
   const int lane = threadIdx.x & 31;
-  const int i = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (i >= offsets[E]) return;
+  const long wid = (long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int chunks = (hidden + 511) / 512;
+  const int i = (int)(wid / chunks);             // sorted row; one 512-element chunk per warp
+  if (i >= offsets[E]) return;                  // uniform per warp
   const int u = perm[i];
   const int t = u / topk, e = ids[u];
   const __half *xr = x + (long)t * hidden;
   const __half *sg = suh13 + (long)e * 2 * hidden, *su = sg + hidden;
   __half *dg = xg + (long)i * hidden, *du = xu + (long)i * hidden;
-  // a pass covers 512 elements (four 128-blocks): lane l holds 16 contiguous
-  // elements, col = 512 p + 16 l (fwht128_x8 layout)
-  for (int c0 = 0; c0 < hidden; c0 += 512) {
+  // the warp's chunk covers 512 elements (four 128-blocks): lane l holds 16
+  // contiguous elements, col = 512 c + 16 l (fwht128_x8 layout)
+  {
+    const int c0 = (int)(wid % chunks) * 512;
     const int col = c0 + 16 * lane;
     const bool in = col < hidden;      // whole 128-blocks are in or out (hidden % 128 == 0)
     uint4 xv[2] = {}, gv[2] = {}, uv[2] = {};
@@ -263,7 +266,8 @@ cudaError_t exl3_launch_moe_remap(const int32_t *ids, int U, int E, int *counts,
 cudaError_t exl3_launch_moe_gather(const uint16_t *x, int U, int hidden, int topk, const int *perm,
                                    const int *offsets, int E, const int32_t *ids, const uint16_t *suh13,
                                    uint16_t *xg, uint16_t *xu, cudaStream_t s) {
-  const unsigned grid = (unsigned)(((long)U + 7) / 8);   // one warp per row; rows <= U
+  const long warps = (long)U * ((hidden + 511) / 512);     // one warp per (row, 512 chunk); rows <= U
+  const unsigned grid = (unsigned)((warps + 7) / 8);
   if (grid == 0) return cudaSuccess;
   moe::gather_rht_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const __half *>(x), hidden, topk, perm, offsets, E,
                                                ids, reinterpret_cast<const __half *>(suh13),
