@@ -143,6 +143,62 @@ __global__ void remap_place_kernel(const int32_t *__restrict__ ids, int U, int E
   p.pos[u] = r;
 }
 
+// Few units (U <= 1024, E <= 256): the three steps above in one CTA of 1024
+// threads, thread u = unit u, with the per-warp counts [32][E] in shared
+// memory (the same stable order: expert, then unit).
+constexpr int kSmallU = 1024, kSmallE = 256;
+
+__global__ void __launch_bounds__(1024) remap_small_kernel(const int32_t *__restrict__ ids, int U, int E, Plan p,
+                                                           int max_mtiles, int *err) {
+  __shared__ int wc[32][kSmallE];
+  __shared__ int base[kSmallE];
+  __shared__ int warp_sums[32];
+  __shared__ int total;
+  const int t = threadIdx.x, w = t >> 5;
+  for (int i = t; i < 32 * kSmallE; i += 1024) (&wc[0][0])[i] = 0;
+  __syncthreads();
+  const int id = t < U ? ids[t] : -1;
+  const bool valid = id >= 0 && id < E;
+  if (t < U && !valid) {
+    set_device_error(err, kErrExpertId);
+    p.pos[t] = -1;
+  }
+  const unsigned peers = __match_any_sync(0xffffffffu, valid ? id : -1);
+  const unsigned lt = lanemask_lt();
+  if (valid && (peers & lt) == 0) wc[w][id] = __popc(peers);
+  __syncthreads();
+  // thread e: the expert's units per warp become the units of earlier warps
+  int c = 0;
+  if (t < E) {
+    for (int j = 0; j < 32; ++j) {
+      const int v = wc[j][t];
+      wc[j][t] = c;
+      c += v;
+    }
+    p.counts[t] = c;
+  }
+  const int off = block_exclusive_scan(c, warp_sums, &total);
+  if (t < E) {
+    p.offsets[t] = off;
+    base[t] = off;
+  }
+  if (t == 0) p.offsets[E] = total;
+  const int nt = (c + 127) >> 7;
+  const int tb = block_exclusive_scan(nt, warp_sums, &total);
+  for (int j = 0; j < nt; ++j)
+    if (tb + j < max_mtiles) p.mtiles[tb + j] = make_int4(t, off + 128 * j, min(128, c - 128 * j), 0);
+  if (t == 0) {
+    if (total > max_mtiles) set_device_error(err, kErrBounds);
+    *p.n_mtiles = min(total, max_mtiles);
+  }
+  __syncthreads();
+  if (valid) {
+    const int r = base[id] + wc[w][id] + __popc(peers & lt);
+    p.perm[r] = t;
+    p.pos[t] = r;
+  }
+}
+
 // Sorted rows of the transformed token inputs for gate and up:
 // xg[i] = RHT(x_t . suh_gate[e]), xu[i] = RHT(x_t . suh_up[e]), t = perm[i] / topk.
 // One warp per sorted row: both slots, every 128-block of the row.
@@ -249,6 +305,10 @@ cudaError_t exl3_launch_moe_remap(const int32_t *ids, int U, int E, int *counts,
                                   cudaStream_t s) {
   if (E < 1 || E > 1024) return cudaErrorInvalidValue;
   moe::Plan p{counts, offsets, perm, pos, reinterpret_cast<int4 *>(mtiles), n_mtiles, chunk_tab};
+  if (U <= moe::kSmallU && E <= moe::kSmallE) {
+    moe::remap_small_kernel<<<1, 1024, 0, s>>>(ids, U, E, p, max_mtiles, err);
+    return cudaGetLastError();
+  }
   const int CH = exl3_moe_remap_chunk(E);
   const int nchunks = (U + CH - 1) / CH;
   if (nchunks > 0) {
