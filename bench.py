@@ -40,8 +40,8 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # dram bytes (read + write) per launch from an ncu capture of gemv_m1_kernel<4>
 # at k=5120 n=17408, with the hash of gemv.cu at capture time; a changed
 # kernel source makes the recorded traffic stale (reported as null).
-TRAFFIC = {"file": "trellis_quantized_gb300/csrc/gemv.cu", "sha1": "aa65d5f8ec46714d67af09b8850fcb8ab5a7e158",
-           "bytes_per_launch": 65982720, "workload": "k5120 n25600 K4 M1"}
+TRAFFIC = {"file": "trellis_quantized_gb300/csrc/gemv.cu", "sha1": "5a8df5539408c058720a141b80be7574810d1ff2",
+           "bytes_per_launch": 65975552, "workload": "k5120 n25600 K4 M1"}
 
 
 def peaks():
