@@ -156,6 +156,10 @@ def run_ours(args):
 
     # One step = the three linears, captured as a CUDA graph per weight copy,
     # so the timed region measures the device and not Python launch overhead.
+    # With weight prefetch (the default) each linear is a programmatic
+    # dependent launch that streams its weights while the previous one ends.
+    prefetch = not args.no_prefetch
+    tq.exl3_set_weight_prefetch(prefetch)
     graphs = []
     for cp in range(copies):
         g = torch.cuda.CUDAGraph()
@@ -163,13 +167,16 @@ def run_ours(args):
             for d in dcases:
                 launch(d, cp)
         graphs.append(g)
-    # Per-kernel duration for the roofline: 30 launches of the largest linear in one graph.
+    # Per-kernel duration for the roofline: 30 launches of the largest linear
+    # in one graph, launched plainly (no overlap between launches).
+    tq.exl3_set_weight_prefetch(False)
     big = len(dcases) - 1
     reps_k = 30
     gk = torch.cuda.CUDAGraph()
     with torch.cuda.graph(gk):
         for i in range(reps_k):
             launch(dcases[big], i % copies)
+    tq.exl3_set_weight_prefetch(prefetch)
     for i in range(args.warmup):
         graphs[i % copies].replay()
     gk.replay()
@@ -208,7 +215,7 @@ def run_ours(args):
                 "peak": hbm, "peak_source": src, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                 "traffic": traffic, "kernel_us": round(kern_ms * 1e3, 2),
                 "algorithmic_bytes_per_launch": big_bytes,
-                "timing": "CUDA events around 20 replays of a graph of 30 launches (3 rotating weight copies)"}
+                "timing": "CUDA events around 20 replays of a graph of 30 plain launches (3 rotating weight copies)"}
 
     # e2e: host x (pinned) -> device, linear, y -> host, every linear of the step
     hx = [torch.from_numpy(d["case"].x).pin_memory() for d in dcases]
@@ -247,9 +254,11 @@ def run_ours(args):
         "data": "synthetic (seeded PCG64: uniform trellis, +-1 suh/svh, x ~ N(0,1) fp16)",
         "config": {"workload": WORKLOAD, "K": 4, "k": 5120, "n": list(synth.CONFIG2_N), "M": 1,
                    "l2": "3 rotating weight copies (369 MB > 2x L2), no flush",
+                   "weight_prefetch": prefetch,
                    "parallelism": "single GPU; replicas only"},
         "gpu_launches": int(args.steps * len(dcases)),
-        "step": "one CUDA graph replay of the three M=1 linears (one GEMV kernel each)",
+        "step": "one CUDA graph replay of the three M=1 linears (one GEMV kernel each; "
+                "programmatic dependent launches when weight_prefetch)",
         "roofline": roofline, "e2e": e2e, "clocks": clk.summary(), "prefill": prefill, "other": extras,
     }
     if not args.skip_cpu:
@@ -411,6 +420,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-prefill", action="store_true")
+    ap.add_argument("--no-prefetch", action="store_true",
+                    help="launch the step's linears plainly (no weight prefetch across launches)")
     ap.add_argument("--only", choices=["small", "moe", "prefill"], default=None,
                     help="run one extra section alone and print its JSON (for profiling)")
     ap.add_argument("--moe-tokens", type=int, nargs="*", default=None,

@@ -127,6 +127,23 @@ int exl3_linear(const uint16_t *x, int M, int k, int n,
                 void *workspace, size_t ws_bytes, exl3_stream_t stream);
 
 /*
+ * exl3_set_weight_prefetch -- let M = 1 calls of exl3_linear stream their
+ * weights before the kernel launched ahead of them on the stream has
+ * finished (CUDA programmatic dependent launch).  The source pages have no
+ * counterpart: this is an addition of this library for decode loops, where
+ * consecutive linears otherwise pay the start-up of each kernel in series.
+ *   enable = 0 (the default) or 1; returns the previous setting.  Applies to
+ *   calls made after it, from any host thread.
+ *   When on, an M = 1 call may read trellis while earlier kernels on the
+ *   stream are still running; it reads x, suh, svh and the workspace and
+ *   writes y only once those kernels have completed and their writes are
+ *   visible.  The caller must therefore not write a trellis buffer with
+ *   kernels that can still be in flight when a call reading it is launched
+ *   (write weights, then synchronise, then run the linears).
+ */
+int exl3_set_weight_prefetch(int enable);
+
+/*
  * exl3_linear_int8 -- the int8 prefill variant ("exl3xpu" README, "Prefill:
  * int8 linears and oneDNN fused attention").
  *   a_r  = max_j |x'_rj| / 127 (fp32), x' the fp32 input transform above;

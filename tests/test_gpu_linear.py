@@ -201,3 +201,52 @@ def test_linear_rejects_small_workspace():
     with pytest.raises(tq.Exl3Error) as e:
         tq.exl3_linear(dev(case.x), dev(case.trellis), dev(case.suh), dev(case.svh), 4, workspace_buf=ws)
     assert e.value.code == tq.EXL3_ERR_WORKSPACE
+
+
+def test_linear_m1_weight_prefetch_chain():
+    """With weight prefetch on, M = 1 linears launch as programmatic dependents:
+    each may stream weights while the kernel ahead of it runs, but must read
+    its input only after that kernel completes.  A chain in which each output
+    is the next input (a long linear feeding a short one, directly, through a
+    torch kernel, and captured in a CUDA graph) must give bit-for-bit the
+    results of the same chain run without prefetch."""
+    a = synth.linear_case(18, 0, 1, 5120, 17408, 4)
+    b = synth.linear_case(18, 1, 1, 17408, 5120, 3)
+    A = [dev(v) for v in (a.x, a.trellis, a.suh, a.svh)]
+    B = [dev(v) for v in (b.trellis, b.suh, b.svh)]
+    wsa = torch.zeros(tq.exl3_linear_workspace_size(1, a.k, a.n, 4), dtype=torch.uint8, device="cuda")
+    wsb = torch.zeros(tq.exl3_linear_workspace_size(1, b.k, b.n, 3), dtype=torch.uint8, device="cuda")
+    ya = torch.empty((1, a.n), dtype=torch.float16, device="cuda")
+    yb = torch.empty((1, b.n), dtype=torch.float16, device="cuda")
+
+    def chain(via_torch=False):
+        tq.exl3_linear(A[0], A[1], A[2], A[3], 4, y=ya, workspace_buf=wsa)
+        xb = ya * 1.0 if via_torch else ya
+        tq.exl3_linear(xb, B[0], B[1], B[2], 3, y=yb, workspace_buf=wsb)
+
+    prev = tq.exl3_set_weight_prefetch(False)
+    try:
+        chain()
+        ref_a, ref_b = ya.clone(), yb.clone()
+        assert_close(host(ref_a).astype(np.float64), oracle.linear(a.x, a.trellis, a.suh, a.svh, 4), "chain head")
+        tq.exl3_set_weight_prefetch(True)
+        for via_torch in (False, True):
+            for _ in range(5):
+                yb.fill_(0)
+                chain(via_torch)
+                assert torch.equal(ya, ref_a) and torch.equal(yb, ref_b)
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            chain()
+            with torch.cuda.graph(g, stream=s):
+                chain()
+        torch.cuda.current_stream().wait_stream(s)
+        for _ in range(5):
+            yb.fill_(0)
+            g.replay()
+            assert torch.equal(ya, ref_a) and torch.equal(yb, ref_b)
+        assert tq.exl3_check_device_error(wsa) == 0 and tq.exl3_check_device_error(wsb) == 0
+    finally:
+        tq.exl3_set_weight_prefetch(prev)

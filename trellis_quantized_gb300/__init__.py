@@ -81,6 +81,8 @@ def lib():
         L.exl3_moe_workspace_size.restype = Z
         L.exl3_moe_grouped.argtypes = [P, I, I, P, P, I, I, P, P, P, I, P, Z, P]
         L.exl3_linear_gemv_noalloc.argtypes = [P, I, I, P, P, P, I, I, P, I, P]
+        L.exl3_set_weight_prefetch.argtypes = [I]
+        L.exl3_set_weight_prefetch.restype = I
         _lib = L
         return L
 
@@ -189,6 +191,14 @@ def exl3_linear(x, trellis, suh, svh, K: int, codebook: int = EXL3_CB_MUL1, out_
                              _ptr(svh, "svh", 2), K, codebook, _ptr(y, "y"), out_dtype, _ptr(ws, "workspace"),
                              ws.numel() * ws.element_size(), _stream(stream)))
     return y
+
+
+def exl3_set_weight_prefetch(enable: bool) -> bool:
+    """Let M = 1 linears stream their weights while the kernel ahead of them
+    on the stream finishes (CUDA programmatic dependent launch); returns the
+    previous setting.  Weight buffers must not be written by kernels still in
+    flight when a linear reading them is launched."""
+    return bool(lib().exl3_set_weight_prefetch(1 if enable else 0))
 
 
 def exl3_linear_int8_workspace_size(M: int, k: int, n: int, K: int) -> int:

@@ -2,6 +2,7 @@
 // validation, workspace layout and kernel dispatch.  No entry point
 // allocates device memory or synchronises the caller's stream (except the
 // test helper exl3_check_device_error).
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -18,7 +19,8 @@ cudaError_t exl3_launch_input_rht(const uint16_t *x, int M, int k, const uint16_
                                   bool f32out, cudaStream_t s);
 cudaError_t exl3_launch_gemv_m1(const uint16_t *x, const uint16_t *trellis, const uint16_t *suh,
                                 const uint16_t *svh, int k, int n, int K, void *y, bool f32out,
-                                float *partials, int *counters, int *err, int grid, cudaStream_t s);
+                                float *partials, int *counters, int *err, int grid, cudaStream_t s,
+                                bool prefetch = false);
 void exl3_gemv_plan(int k, int n, int K, int *grid, size_t *partial_floats);
 int exl3_launch_gemm_tc(const uint16_t *xh, const uint16_t *wt, int M, int n, int k, const uint16_t *svh,
                         void *y, bool f32out, const float *row_scale, float pre, int *err, cudaStream_t s,
@@ -53,6 +55,7 @@ int exl3_launch_moe_fused_down(const uint16_t *hin, int U, int hidden, int inter
 // ---------------------------------------------------------------- errors --
 
 static thread_local std::string g_last_error;
+static std::atomic<int> g_weight_prefetch{0};
 
 int exl3_fail(int code, const char *fmt, ...) {
   char buf[512];
@@ -268,6 +271,8 @@ const char *exl3_last_error(void) { return g_last_error.c_str(); }
 
 int exl3_version(void) { return 100; }
 
+int exl3_set_weight_prefetch(int enable) { return g_weight_prefetch.exchange(enable ? 1 : 0); }
+
 int exl3_workspace_clear(void *workspace, size_t ws_bytes, exl3_stream_t stream) {
   g_last_error.clear();
   if (!workspace || ws_bytes == 0) return EXL3_OK;
@@ -344,7 +349,8 @@ int exl3_linear(const uint16_t *x, int M, int k, int n, const uint16_t *trellis,
   int *err = at<int>(workspace, L.ctrl);
   if (M == 1) {
     return exl3_cuda_check(exl3_launch_gemv_m1(x, trellis, suh, svh, k, n, K, y, f32, at<float>(workspace, L.partials),
-                                               at<int>(workspace, L.counters), err, L.grid, stream),
+                                               at<int>(workspace, L.counters), err, L.grid, stream,
+                                               g_weight_prefetch.load() != 0),
                            "gemv launch");
   }
   uint16_t *xh = at<uint16_t>(workspace, L.xh);

@@ -12,34 +12,46 @@
 // the fp16 x' into an fp32 accumulator: sum x' (1024 + B).  The offset is
 // removed once per lane, 1534 * sum x' (1024 + 510 = 1534), at the end.
 //
-// Lane work.  A lane owns G = 8 / gcd(K, 8) consecutive rows of one tile:
-// 16 G weights whose states come from CPL = K / gcd(K, 8) contiguous 16-byte
-// chunks (128 CPL bits) plus the first 32 bits of the next row group (one
-// warp shuffle; the last group of a tile wraps to the first).  LPT = 16 / G
-// lanes cover a tile and a warp covers 2 G consecutive tiles along n.  Each
-// window is cut out of byte-aligned (possibly pre-shifted) words with one
-// LOP/SHR/PRMT where it can, hashed (IMAD), byte-summed by DP4A and
-// accumulated by one mixed-precision FMA.
-//
-// Staging.  One producer warp streams the CTA's rows (the tiles of one
-// column block at one tile row, 0.5-3.5 KB of contiguous trellis each) into
-// a ring of shared-memory stages with bulk asynchronous copies completing on
-// mbarriers; eight consumer warps decode out of shared memory.  Every wait is
-// bounded; a wait that runs out sets the device error word.
+// Lane work.  A lane owns G >= 4 consecutive rows of one tile: 16 G weights
+// whose states come from CPL contiguous 16-byte chunks (128 CPL bits) plus
+// the first 32 bits of the next row group (the last group of a tile wraps to
+// the first).  LPT = 16 / G lanes cover a tile and a warp covers one tile row
+// of the CTA's column block (128 or 256 columns).  Each window is cut out of
+// byte-aligned (possibly pre-shifted) words with one LOP/SHR/PRMT where it
+// can, hashed (IMAD), byte-summed by DP4A and accumulated by one
+// mixed-precision FMA.
 //
 // Work split.  The work is the list of "rows" (column block c, tile row tk),
-// c-major; a column block is 128 (or 256) output columns.  A persistent grid
-// sized to the resident CTA slots takes equal contiguous ranges of that list,
-// so every SM gets the same amount of trellis.  A CTA's range crosses column
-// blocks; at each crossing it reduces its accumulators and either finishes
-// the block itself (it owned all of it) or stores a partial sum in a slot
-// fixed by (block, CTA).  The last CTA to arrive at a block (atomic counter,
-// no waiting) adds the partials in CTA order, applies the output transform
-// and writes y: the result does not depend on timing.
+// c-major.  One CTA per SM takes an equal contiguous range of that list, so
+// every SM gets the same amount of trellis.  Inside the CTA one thread loads
+// the rows with 3-D tensor copies (8 tile rows of the column block each) into
+// a ring of shared-memory stages, and NCW consumer warps decode every stage
+// together (warp w takes rows w, w + NCW, ...).  Because all consumer warps
+// share one ring, none can run more than the ring's depth ahead of the
+// others, so they finish together; separate CTAs per SM did not (the warp
+// schedulers favour the first-resident CTA, which left the SM's last CTA
+// running alone at low issue rate).  Every wait is bounded; a wait that runs
+// out sets the device error word.
+//
+// Column blocks.  A CTA's range crosses column blocks.  At each crossing
+// the consumer warps leave their column sums in shared memory for a flusher
+// warp and go straight on with the next block; the flusher adds the warps'
+// sums in warp order and either finishes the block itself (its CTA owned all
+// of it) or stores a partial sum in a slot fixed by (block, CTA).  The last
+// CTA to arrive at a block (atomic counter, no waiting) adds the partials in
+// CTA order, applies the output transform and writes y: the result does not
+// depend on timing.
+#include <cudaTypedefs.h>
+
 #include "exl3_common.cuh"
+#include "tc_ptx.cuh"
 #include "trellis_window.cuh"
 
 namespace exl3 {
+
+constexpr int kGemvBoxRows = 8;                 // tile rows per tensor copy
+constexpr int kGemvSmemMax = 232448;            // opt-in shared memory per CTA (227 KB; no static smem)
+constexpr int kGemvMaxStages = 6;
 
 template <int K>
 struct GemvShape {
@@ -50,33 +62,31 @@ struct GemvShape {
   static constexpr int CPL = K * G / 8;          // 16-byte chunks per lane
   static constexpr int LPT = 16 / G;             // lanes per tile
   static constexpr int TPW = 32 / LPT;           // tiles per warp
-  static constexpr int COLW = TPW * 16;          // columns per warp
-  static constexpr int WC = COLW >= 128 ? 1 : 128 / COLW;  // column warps per CTA
-  static constexpr int WK = 8 / WC;              // k warps per CTA
-  static constexpr int CTA_COLS = WC * COLW;     // 128 or 256
+  static constexpr int CTA_COLS = TPW * 16;      // 128 or 256 columns per block
   static constexpr int NW = 4 * CPL;             // 32-bit stream words per lane
   static constexpr int ROWB = CTA_COLS * 2 * K;  // bytes of one row (CTA_COLS/16 tiles of 32K bytes)
-  // rows per stage: each k-warp takes RPW rows per wait, aiming at 16 KB
-  // stages (at least the one or two rows of a wide or narrow row, at most 4)
-  static constexpr int RPW_MIN = ROWB >= 2048 ? 1 : 2;
-  static constexpr int RPW_FIT = 16384 / (WK * ROWB);
-  static constexpr int RPW = RPW_FIT > 4 ? 4 : (RPW_FIT < RPW_MIN ? RPW_MIN : RPW_FIT);
-  static constexpr int R = RPW * WK;
+  // consumer warps, and rows per consumer warp per stage: stages of 16-48 KB
+  // so that two stages and x' for the largest k fit in shared memory
+  static constexpr int NCW = ROWB >= 2560 ? 16 : 24;
+  static constexpr int RPW = ROWB >= 1536 ? 1 : 2;
+  static constexpr int R = RPW * NCW;            // rows per stage
   static constexpr int STAGE_B = R * ROWB;
-  static constexpr int STAGES = (48 * 1024) / STAGE_B < 2 ? 2 : (48 * 1024) / STAGE_B;
-  static constexpr int RING_B = STAGES * STAGE_B;
+  static constexpr int NG = CTA_COLS / 128;      // 128-column groups per block
+  static constexpr int THREADS = (NCW + 2) * 32; // + the producer and the flusher warp
+  static constexpr int FIXED_B = 4 * NCW * CTA_COLS + 256;   // red, flags, barriers
+  static_assert(R % kGemvBoxRows == 0, "stages hold whole tensor copies");
+  static_assert(ROWB % 128 == 0, "tensor copies land on 128-byte boundaries");
 };
 
 struct GemvArgs {
   const __half *x;          // [k]
-  const uint16_t *trellis;  // [k/16][n/16][16K]
   const __half *suh;        // [k]
   const __half *svh;        // [n]
   void *y;                  // [n] fp16 or fp32
   float *partials;          // [colblocks + grid][CTA_COLS]
   int *counters;            // [colblocks]
   int *err;                 // device error word
-  int k, n, tiles_k, colblocks;
+  int k, n, tiles_k, colblocks, stages;
   long long total;          // colblocks * tiles_k
 };
 
@@ -89,40 +99,9 @@ __device__ __forceinline__ float fma_f16_f32(unsigned short x, uint32_t r, float
   return acc;
 }
 
-__device__ __forceinline__ uint32_t smem_addr(const void *p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+__device__ __forceinline__ void consumer_sync(int nthreads) {
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
-__device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t n) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(b)), "r"(n));
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *b, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(b)), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive1(uint64_t *b) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(b)) : "memory");
-}
-// Bounded wait for the phase of the given parity; false if it ran out.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *b, uint32_t parity) {
-  const long long t0 = clock64();
-  while (true) {
-    uint32_t ok;
-    // the suspend-time hint (ns) lets the thread sleep until the phase
-    // completes instead of spinning through issue slots
-    asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 10000;\nselp.u32 %0, 1, 0, p;\n}\n"
-                 : "=r"(ok)
-                 : "r"(smem_addr(b)), "r"(parity)
-                 : "memory");
-    if (ok) return true;
-    if (clock64() - t0 > 2000000000LL) return false;
-  }
-}
-__device__ __forceinline__ void bulk_copy(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   smem_addr(dst)),
-               "l"(src), "r"(bytes), "r"(smem_addr(bar))
-               : "memory");
-}
-__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 // Decode the lane's 16 G weights and accumulate x'_row * (1024 + B) into the
 // 16 column accumulators.
@@ -151,60 +130,70 @@ __device__ __forceinline__ int range_owner(long long r, long long total, int gri
 }
 
 template <int K, bool F32OUT>
-__global__ void __launch_bounds__(288) gemv_m1_kernel(GemvArgs a) {
+__global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
+    gemv_m1_kernel(const __grid_constant__ CUtensorMap tmT, GemvArgs a) {
   using S = GemvShape<K>;
+  constexpr int NCW = S::NCW, NCT = NCW * 32;
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  uint8_t *ring = smem_raw;                                         // [STAGES][R][ROWB]
-  float *red = reinterpret_cast<float *>(smem_raw + S::RING_B);    // [WK][CTA_COLS]
-  float *ys = red + S::WK * S::CTA_COLS;                           // [CTA_COLS]
-  uint64_t *full = reinterpret_cast<uint64_t *>(ys + S::CTA_COLS); // [STAGES]
-  uint64_t *empty = full + S::STAGES;                              // [STAGES]
-  __half *xs = reinterpret_cast<__half *>(empty + S::STAGES);      // [k] fp16 x' (touched blocks)
-  __shared__ int s_last;
-  __shared__ volatile int s_abort;
+  const int STAGES = a.stages;
+  uint8_t *ring = smem_raw;                                            // [STAGES][R][ROWB]
+  float *red = reinterpret_cast<float *>(smem_raw + (size_t)STAGES * S::STAGE_B);   // [NCW][CTA_COLS]
+  volatile int *s_abort = reinterpret_cast<volatile int *>(red + NCW * S::CTA_COLS);   // a wait ran out
+  uint64_t *full = reinterpret_cast<uint64_t *>(red + NCW * S::CTA_COLS + 2);    // [STAGES]
+  uint64_t *empty = full + STAGES;                                     // [STAGES]
+  uint64_t *seg_full = empty + STAGES;                                 // red holds a finished segment
+  uint64_t *red_free = seg_full + 1;                                   // the flusher has read red
+  __half *xs = reinterpret_cast<__half *>(red_free + 1);               // [k] fp16 x' (touched blocks)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int grid = gridDim.x, me = blockIdx.x;
-  const int TK = a.tiles_k, tiles_n = a.n >> 4;
+  const int TK = a.tiles_k;
+  // the kernel launched after this one on the stream may start as soon as
+  // every CTA has begun (it only streams weights until this grid completes)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const long long t0 = range_start(me, a.total, grid), t1 = range_start(me + 1, a.total, grid);
   if (t0 >= t1) return;
 
   if (tid == 0) {
-    for (int st = 0; st < S::STAGES; ++st) {
-      mbar_init(&full[st], 1);
-      mbar_init(&empty[st], 8);
+    for (int st = 0; st < STAGES; ++st) {
+      tc::mbar_init(&full[st], 1);
+      tc::mbar_init(&empty[st], NCW);
     }
-    s_abort = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    tc::mbar_init(seg_full, NCW);
+    tc::mbar_init(red_free, 1);
+    *s_abort = 0;
+    tc::fence_mbar_init();
   }
   __syncthreads();
 
-  if (warp == 8) {
-    // ---------------- producer: one thread streams the rows into the ring
+  if (warp == NCW) {
+    // ---------------- producer: one thread loads the rows into the ring
     if (lane == 0) {
+      tc::prefetch_tmap(&tmT);
       int stage = 0;
       uint32_t phase = 0;
-      for (long long t = t0; t < t1 && !s_abort;) {
+      for (long long t = t0; t < t1 && !*s_abort;) {
         const int c = (int)(t / TK);
         const long long seg_end = min(t1, (long long)(c + 1) * TK);
         const int tk_first = (int)(t - (long long)c * TK), nrows = (int)(seg_end - t);
         const int tn0 = c * (S::CTA_COLS / 16);
-        const int tiles_valid = min(S::CTA_COLS / 16, tiles_n - tn0);
-        const uint32_t bytes = (uint32_t)tiles_valid * 32u * K;
-        for (int r0 = 0; r0 < nrows && !s_abort; r0 += S::R) {
+        for (int r0 = 0; r0 < nrows && !*s_abort; r0 += S::R) {
           const int cnt = min(S::R, nrows - r0);
-          if (!mbar_wait_bounded(&empty[stage], phase ^ 1)) {
+          if (!tc::mbar_wait(&empty[stage], phase ^ 1)) {
             set_device_error(a.err, kErrBounds);
-            s_abort = 1;
+            *s_abort = 1;
             break;
           }
-          mbar_expect_tx(&full[stage], bytes * cnt);
-          for (int j = 0; j < cnt; ++j) {
-            const long tk = tk_first + r0 + j;
-            const uint16_t *src = a.trellis + ((long)tk * tiles_n + tn0) * 16 * K;
-            bulk_copy(ring + (size_t)stage * S::STAGE_B + (size_t)j * S::ROWB, src, bytes, &full[stage]);
-          }
-          if (++stage == S::STAGES) { stage = 0; phase ^= 1; }
+          // whole 8-row copies: rows past the block's end are outside the
+          // tensor (zero-filled, not read); rows past the range's end are
+          // loaded and ignored
+          const int nb = (cnt + kGemvBoxRows - 1) / kGemvBoxRows;
+          tc::mbar_arrive_expect_tx(&full[stage], (uint32_t)(nb * kGemvBoxRows * S::ROWB));
+          uint8_t *dst = ring + (size_t)stage * S::STAGE_B;
+          for (int b = 0; b < nb; ++b)
+            tc::tma_load_3d(dst + (size_t)b * kGemvBoxRows * S::ROWB, &tmT, &full[stage], 0, tn0,
+                            tk_first + r0 + b * kGemvBoxRows);
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
         t = seg_end;
       }
@@ -212,7 +201,110 @@ __global__ void __launch_bounds__(288) gemv_m1_kernel(GemvArgs a) {
     return;
   }
 
-  // ---------------- consumers (warps 0..7)
+  // Under a programmatic dependent launch the producer above is already
+  // streaming weights; everything below (x, the workspace, y) waits until
+  // the preceding kernel on the stream has completed and its writes are
+  // visible.  Without one the wait returns at once.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  if (warp == NCW + 1) {
+    // ---------------- flusher: finishes each column block the consumers hand
+    // over while they go on decoding the next one.  Lane l holds columns
+    // 128 g + 4 l .. +3 of every 128-column group g.
+    uint32_t sp = 0;
+    for (long long t = t0; t < t1;) {
+      const int c = (int)(t / TK);
+      const long long seg_end = min(t1, (long long)(c + 1) * TK);
+      if (!*s_abort && !tc::mbar_wait(seg_full, sp)) {
+        if (lane == 0) set_device_error(a.err, kErrBounds);
+        *s_abort = 1;
+      }
+      float v[S::NG][4];
+#pragma unroll
+      for (int g = 0; g < S::NG; ++g) {
+        v[g][0] = v[g][1] = v[g][2] = v[g][3] = 0.f;
+        for (int w = 0; w < NCW; ++w) {   // fixed order: the result does not depend on timing
+          const float4 r = *reinterpret_cast<const float4 *>(red + w * S::CTA_COLS + g * 128 + lane * 4);
+          v[g][0] += r.x;
+          v[g][1] += r.y;
+          v[g][2] += r.z;
+          v[g][3] += r.w;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(red_free);
+#pragma unroll
+      for (int g = 0; g < S::NG; ++g)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[g][e] *= kSigma;
+
+      const int col0 = c * S::CTA_COLS;
+      const long long blk_first = (long long)c * TK, blk_last = min((long long)(c + 1) * TK, a.total) - 1;
+      const int i_first = range_owner(blk_first, a.total, grid), i_last = range_owner(blk_last, a.total, grid);
+      bool finish = true;
+      if (i_first != i_last) {
+        // partial sum in the (block, CTA) slot; the last CTA to arrive adds them
+#pragma unroll
+        for (int g = 0; g < S::NG; ++g)
+          *reinterpret_cast<float4 *>(a.partials + (long)(c + me) * S::CTA_COLS + g * 128 + lane * 4) =
+              make_float4(v[g][0], v[g][1], v[g][2], v[g][3]);
+        __threadfence();
+        __syncwarp();
+        int old = 0;
+        const int expected = i_last - i_first + 1;
+        if (lane == 0) {
+          old = atomicAdd(a.counters + c, 1);
+          if (old >= expected) set_device_error(a.err, kErrDirtyCounter);
+        }
+        old = __shfl_sync(0xffffffffu, old, 0);
+        finish = old == expected - 1;
+        if (finish) {
+          __threadfence();
+#pragma unroll
+          for (int g = 0; g < S::NG; ++g) v[g][0] = v[g][1] = v[g][2] = v[g][3] = 0.f;
+          for (int i = i_first; i <= i_last; ++i) {
+#pragma unroll
+            for (int g = 0; g < S::NG; ++g) {
+              const float4 r = __ldcg(reinterpret_cast<const float4 *>(a.partials + (long)(c + i) * S::CTA_COLS +
+                                                                       g * 128 + lane * 4));
+              v[g][0] += r.x;
+              v[g][1] += r.y;
+              v[g][2] += r.z;
+              v[g][3] += r.w;
+            }
+          }
+          if (lane == 0) a.counters[c] = 0;   // leave the workspace clean
+        }
+      }
+      if (finish) {
+        // ---- output transform of the block's 128-column groups
+#pragma unroll
+        for (int g = 0; g < S::NG; ++g) {
+          const int gc = col0 + g * 128 + lane * 4;
+          if (col0 + g * 128 < a.n) {
+            fwht128_warp(v[g], lane);
+            const uint2 sv = *reinterpret_cast<const uint2 *>(a.svh + gc);
+            const __half2 *sh = reinterpret_cast<const __half2 *>(&sv);
+            const float o0 = v[g][0] * kRhtScale * __low2float(sh[0]);
+            const float o1 = v[g][1] * kRhtScale * __high2float(sh[0]);
+            const float o2 = v[g][2] * kRhtScale * __low2float(sh[1]);
+            const float o3 = v[g][3] * kRhtScale * __high2float(sh[1]);
+            if (F32OUT) {
+              *reinterpret_cast<float4 *>(static_cast<float *>(a.y) + gc) = make_float4(o0, o1, o2, o3);
+            } else {
+              __half2 o[2] = {__floats2half2_rn(o0, o1), __floats2half2_rn(o2, o3)};
+              *reinterpret_cast<uint2 *>(static_cast<__half *>(a.y) + gc) = *reinterpret_cast<uint2 *>(o);
+            }
+          }
+        }
+      }
+      sp ^= 1;
+      t = seg_end;
+    }
+    return;
+  }
+
+  // ---------------- consumers (warps 0..NCW-1)
   // prologue: x' = 2^-3.5 H (x . suh) for the 128-blocks this range touches
   {
     const int KB = a.k >> 7;
@@ -223,36 +315,48 @@ __global__ void __launch_bounds__(288) gemv_m1_kernel(GemvArgs a) {
       const bool wrap = (t0 / TK) != ((t1 - 1) / TK);
       nb = !wrap ? b1 - b0 + 1 : (b1 >= b0 ? KB : KB - b0 + b1 + 1);
     }
-    for (int i = warp; i < nb; i += 8) {
-      const int b = (b0 + i) % KB;
-      const int col = b * 128 + lane * 4;
-      const uint2 xv = *reinterpret_cast<const uint2 *>(a.x + col);
-      const uint2 sv = *reinterpret_cast<const uint2 *>(a.suh + col);
-      const __half2 *xh = reinterpret_cast<const __half2 *>(&xv);
-      const __half2 *sh = reinterpret_cast<const __half2 *>(&sv);
-      float v[4] = {__low2float(xh[0]) * __low2float(sh[0]), __high2float(xh[0]) * __high2float(sh[0]),
-                    __low2float(xh[1]) * __low2float(sh[1]), __high2float(xh[1]) * __high2float(sh[1])};
-      fwht128_warp(v, lane);
-      __half2 o[2] = {__floats2half2_rn(v[0] * kRhtScale, v[1] * kRhtScale),
-                      __floats2half2_rn(v[2] * kRhtScale, v[3] * kRhtScale)};
-      *reinterpret_cast<uint2 *>(xs + col) = *reinterpret_cast<uint2 *>(o);
+    // four blocks per warp per round, all loads issued before any arithmetic
+    for (int i0 = warp; i0 < nb; i0 += 4 * NCW) {
+      uint2 xv[4], sv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * NCW;
+        if (i < nb) {
+          const int col = ((b0 + i) % KB) * 128 + lane * 4;
+          xv[u] = *reinterpret_cast<const uint2 *>(a.x + col);
+          sv[u] = *reinterpret_cast<const uint2 *>(a.suh + col);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * NCW;
+        if (i < nb) {
+          const int col = ((b0 + i) % KB) * 128 + lane * 4;
+          const __half2 *xh = reinterpret_cast<const __half2 *>(&xv[u]);
+          const __half2 *sh = reinterpret_cast<const __half2 *>(&sv[u]);
+          float v[4] = {__low2float(xh[0]) * __low2float(sh[0]), __high2float(xh[0]) * __high2float(sh[0]),
+                        __low2float(xh[1]) * __low2float(sh[1]), __high2float(xh[1]) * __high2float(sh[1])};
+          fwht128_warp(v, lane);
+          __half2 o[2] = {__floats2half2_rn(v[0] * kRhtScale, v[1] * kRhtScale),
+                          __floats2half2_rn(v[2] * kRhtScale, v[3] * kRhtScale)};
+          *reinterpret_cast<uint2 *>(xs + col) = *reinterpret_cast<uint2 *>(o);
+        }
+      }
     }
   }
-  consumer_sync();
+  consumer_sync(NCT);
 
-  const int wc = warp % S::WC, wk = warp / S::WC;
+  const int wk = warp;
   const int tile_in_warp = lane / S::LPT, q = lane % S::LPT;
-  const int tile_local = wc * S::TPW + tile_in_warp;                 // tile within the row
-  const int my_off = tile_local * 32 * K + q * 16 * S::CPL;          // byte offset in a row
-  const int next_off = tile_local * 32 * K + ((q + 1) % S::LPT) * 16 * S::CPL;  // next row group (wraps)
+  const int my_off = tile_in_warp * 32 * K + q * 16 * S::CPL;                  // byte offset in a row
+  const int next_off = tile_in_warp * 32 * K + ((q + 1) % S::LPT) * 16 * S::CPL;  // next row group (wraps)
   int stage = 0;
-  uint32_t phase = 0;
+  uint32_t phase = 0, sp = 0;
 
   for (long long t = t0; t < t1;) {
     const int c = (int)(t / TK);
     const long long seg_end = min(t1, (long long)(c + 1) * TK);
     const int tk_first = (int)(t - (long long)c * TK), nrows = (int)(seg_end - t);
-    const bool valid = c * (S::CTA_COLS / 16) + tile_local < tiles_n;
 
     float acc[16];
 #pragma unroll
@@ -261,31 +365,26 @@ __global__ void __launch_bounds__(288) gemv_m1_kernel(GemvArgs a) {
 
     for (int r0 = 0; r0 < nrows; r0 += S::R) {
       const int cnt = min(S::R, nrows - r0);
-      if (!s_abort && !mbar_wait_bounded(&full[stage], phase)) {
+      if (!*s_abort && !tc::mbar_wait(&full[stage], phase)) {
         if (lane == 0) set_device_error(a.err, kErrBounds);
-        s_abort = 1;
+        *s_abort = 1;
       }
       const uint8_t *sbase = ring + (size_t)stage * S::STAGE_B;
 #pragma unroll
-      for (int jj = 0; jj < S::R / S::WK; ++jj) {
-        const int j = wk + jj * S::WK;
+      for (int jj = 0; jj < S::RPW; ++jj) {
+        const int j = wk + jj * NCW;
         if (j < cnt) {
           uint32_t w[S::NW + 1];
           const uint8_t *rowp = sbase + (size_t)j * S::ROWB;
-          if (valid) {
 #pragma unroll
-            for (int cc = 0; cc < S::CPL; ++cc) {
-              const uint4 v4 = *reinterpret_cast<const uint4 *>(rowp + my_off + 16 * cc);
-              w[4 * cc + 0] = v4.x;
-              w[4 * cc + 1] = v4.y;
-              w[4 * cc + 2] = v4.z;
-              w[4 * cc + 3] = v4.w;
-            }
-            w[S::NW] = *reinterpret_cast<const uint32_t *>(rowp + next_off);
-          } else {
-#pragma unroll
-            for (int i = 0; i <= S::NW; ++i) w[i] = 0u;
+          for (int cc = 0; cc < S::CPL; ++cc) {
+            const uint4 v4 = *reinterpret_cast<const uint4 *>(rowp + my_off + 16 * cc);
+            w[4 * cc + 0] = v4.x;
+            w[4 * cc + 1] = v4.y;
+            w[4 * cc + 2] = v4.z;
+            w[4 * cc + 3] = v4.w;
           }
+          w[S::NW] = *reinterpret_cast<const uint32_t *>(rowp + next_off);
           const int tk = tk_first + r0 + j;
           unsigned short xr[S::G];
 #pragma unroll
@@ -298,11 +397,12 @@ __global__ void __launch_bounds__(288) gemv_m1_kernel(GemvArgs a) {
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive1(&empty[stage]);
-      if (++stage == S::STAGES) { stage = 0; phase ^= 1; }
+      if (lane == 0) tc::mbar_arrive(&empty[stage]);
+      if (++stage == STAGES) { stage = 0; phase ^= 1; }
     }
 
-    // ---- reduce: LPT lanes of a tile, then the k-warps of the CTA
+    // ---- hand the block over: reduce over the LPT lanes of a tile, then
+    // leave this warp's column sums in red for the flusher
     float accf[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) accf[i] = fmaf(-1534.0f, sx, acc[i]);
@@ -310,110 +410,82 @@ __global__ void __launch_bounds__(288) gemv_m1_kernel(GemvArgs a) {
     for (int m = 1; m < S::LPT; m <<= 1)
 #pragma unroll
       for (int i = 0; i < 16; ++i) accf[i] += __shfl_xor_sync(0xffffffffu, accf[i], m);
+    if (!*s_abort && !tc::mbar_wait(red_free, sp ^ 1)) {
+      if (lane == 0) set_device_error(a.err, kErrBounds);
+      *s_abort = 1;
+    }
     if (q == 0) {
+      float4 *dst = reinterpret_cast<float4 *>(red + wk * S::CTA_COLS + tile_in_warp * 16);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) red[wk * S::CTA_COLS + wc * S::COLW + tile_in_warp * 16 + i] = accf[i];
+      for (int i = 0; i < 4; ++i) dst[i] = make_float4(accf[4 * i], accf[4 * i + 1], accf[4 * i + 2], accf[4 * i + 3]);
     }
-    consumer_sync();
-    const int col0 = c * S::CTA_COLS;
-    float part = 0.f;
-    if (tid < S::CTA_COLS) {
-#pragma unroll
-      for (int w = 0; w < S::WK; ++w) part += red[w * S::CTA_COLS + tid];
-      part *= kSigma;
-    }
-    const long long blk_first = (long long)c * TK, blk_last = min((long long)(c + 1) * TK, a.total) - 1;
-    const int i_first = range_owner(blk_first, a.total, grid), i_last = range_owner(blk_last, a.total, grid);
-    bool finish;
-    if (i_first == i_last) {
-      if (tid < S::CTA_COLS) ys[tid] = part;
-      finish = true;
-    } else {
-      if (tid < S::CTA_COLS) {
-        a.partials[(long)(c + me) * S::CTA_COLS + tid] = part;
-        __threadfence();
-      }
-      consumer_sync();
-      if (tid == 0) {
-        const int expected = i_last - i_first + 1;
-        const int old = atomicAdd(a.counters + c, 1);
-        if (old >= expected) set_device_error(a.err, kErrDirtyCounter);
-        s_last = (old == expected - 1);
-      }
-      consumer_sync();
-      finish = s_last != 0;
-      if (finish) {
-        __threadfence();
-        if (tid < S::CTA_COLS) {
-          float sum = 0.f;
-          for (int i = i_first; i <= i_last; ++i) sum += __ldcg(a.partials + (long)(c + i) * S::CTA_COLS + tid);
-          ys[tid] = sum;
-        }
-        if (tid == 0) a.counters[c] = 0;   // leave the workspace clean
-      }
-    }
-    consumer_sync();
-
-    // ---- output transform of the block's 128-column groups
-    if (finish && warp < S::CTA_COLS / 128 && col0 + warp * 128 < a.n) {
-      const int cc = warp * 128 + lane * 4;
-      float v[4] = {ys[cc], ys[cc + 1], ys[cc + 2], ys[cc + 3]};
-      fwht128_warp(v, lane);
-      const int gc = col0 + cc;
-      const uint2 sv = *reinterpret_cast<const uint2 *>(a.svh + gc);
-      const __half2 *sh = reinterpret_cast<const __half2 *>(&sv);
-      v[0] = v[0] * kRhtScale * __low2float(sh[0]);
-      v[1] = v[1] * kRhtScale * __high2float(sh[0]);
-      v[2] = v[2] * kRhtScale * __low2float(sh[1]);
-      v[3] = v[3] * kRhtScale * __high2float(sh[1]);
-      if (F32OUT) {
-        *reinterpret_cast<float4 *>(static_cast<float *>(a.y) + gc) = make_float4(v[0], v[1], v[2], v[3]);
-      } else {
-        __half2 o[2] = {__floats2half2_rn(v[0], v[1]), __floats2half2_rn(v[2], v[3])};
-        *reinterpret_cast<uint2 *>(static_cast<__half *>(a.y) + gc) = *reinterpret_cast<uint2 *>(o);
-      }
-    }
-    consumer_sync();   // red / ys are reused by the next segment
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(seg_full);
+    sp ^= 1;
     t = seg_end;
   }
 }
 
+static int gemv_sm_count() {
+  static int cached = 0;
+  if (cached) return cached;
+  int dev = 0, v = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) ==
+                                                cudaSuccess && v > 0)
+    cached = v;
+  else {
+    cudaGetLastError();
+    return 152;
+  }
+  return cached;
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 gemv_tmap_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
 template <int K, bool F32>
 struct Launcher {
-  static size_t smem(int k) {
-    using S = GemvShape<K>;
-    return (size_t)S::RING_B + sizeof(float) * ((size_t)S::WK * S::CTA_COLS + S::CTA_COLS) +
-           sizeof(uint64_t) * 2 * S::STAGES + sizeof(__half) * (size_t)k;
+  using S = GemvShape<K>;
+  // ring stages that fit beside x' (2 bytes per k) and the reduction buffers
+  static int stages(int k) {
+    const long avail = (long)kGemvSmemMax - S::FIXED_B - 2L * k;
+    long st = avail / S::STAGE_B;
+    if (st > kGemvMaxStages) st = kGemvMaxStages;
+    return (int)st;
   }
-  static int grid(int k) {
-    static int cached_k = -1, cached = 0;
-    if (cached_k == k) return cached;
-    int dev = 0, sms = 0, occ = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const size_t sm = smem(k);
-    cudaFuncSetAttribute(gemv_m1_kernel<K, F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gemv_m1_kernel<K, F32>, 288, sm);
-    cudaGetLastError();
-    if (sms <= 0) sms = 152;
-    if (occ <= 0) occ = 1;
-    // three resident CTAs per SM: more rows per CTA between column-block
-    // flushes, still enough warps to hide the decode latencies (measured
-    // faster than four at k = 5120, n = 5120 ... 25600)
-    if (occ > 3) occ = 3;
-    cached_k = k;
-    cached = sms * occ;
-    return cached;
-  }
-  static cudaError_t launch(const GemvArgs &a, int grid, cudaStream_t s) {
-    static int attr_k = -1;
-    const size_t sm = smem(a.k);
-    if (attr_k != a.k) {
-      cudaFuncSetAttribute(gemv_m1_kernel<K, F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-      attr_k = a.k;
+  static size_t smem(int k, int st) { return (size_t)st * S::STAGE_B + S::FIXED_B + 2 * (size_t)k; }
+  static cudaError_t launch(const CUtensorMap &tm, const GemvArgs &a, int grid, cudaStream_t s, bool prefetch) {
+    const size_t sm = smem(a.k, a.stages);
+    static size_t attr = 0;
+    if (attr < sm) {
+      cudaError_t e = cudaFuncSetAttribute(gemv_m1_kernel<K, F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)sm);
+      if (e != cudaSuccess) return e;
+      attr = sm;
     }
-    gemv_m1_kernel<K, F32><<<grid, 288, sm, s>>>(a);
-    return cudaGetLastError();
+    cudaLaunchAttribute attrs[1];
+    attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(S::THREADS);
+    cfg.dynamicSmemBytes = sm;
+    cfg.stream = s;
+    // programmatic dependent launch: CTAs may become resident (and stream
+    // weights) while the preceding kernel on the stream finishes
+    cfg.attrs = prefetch ? attrs : nullptr;
+    cfg.numAttrs = prefetch ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, gemv_m1_kernel<K, F32>, tm, a);
   }
 };
 
@@ -440,12 +512,13 @@ int exl3_gemv_cta_cols(int K) {
   return r;
 }
 
-// Persistent grid size and the partial-sum slots (floats) the GEMV needs.
+// Grid size (one CTA per SM, at most one per row) and the partial-sum slots
+// (floats) the GEMV needs.
 void exl3_gemv_plan(int k, int n, int K, int *grid, size_t *partial_floats) {
-  int g = 0, cc = 128;
-  EXL3_K_SWITCH(K, (g = Launcher<KK, false>::grid(k), cc = GemvShape<KK>::CTA_COLS));
+  const int cc = exl3_gemv_cta_cols(K);
   const long long colblocks = (n + cc - 1) / cc;
   const long long total = colblocks * (k / 16);
+  int g = gemv_sm_count();
   if (g > total) g = (int)total;
   *grid = g;
   *partial_floats = (size_t)(colblocks + g) * (size_t)cc;
@@ -453,10 +526,26 @@ void exl3_gemv_plan(int k, int n, int K, int *grid, size_t *partial_floats) {
 
 cudaError_t exl3_launch_gemv_m1(const uint16_t *x, const uint16_t *trellis, const uint16_t *suh,
                                 const uint16_t *svh, int k, int n, int K, void *y, bool f32out,
-                                float *partials, int *counters, int *err, int grid, cudaStream_t s) {
+                                float *partials, int *counters, int *err, int grid, cudaStream_t s,
+                                bool prefetch) {
+  auto fn = gemv_tmap_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const int cc = exl3_gemv_cta_cols(K);
+  // trellis [k/16][n/16][32K bytes] as u64 (4K per tile): one copy brings 8
+  // tile rows of the CTA_COLS / 16 tiles of a column block
+  CUtensorMap tm;
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)4 * K, (cuuint64_t)(n / 16), (cuuint64_t)(k / 16)};
+    cuuint64_t strides[2] = {(cuuint64_t)32 * K, (cuuint64_t)(n / 16) * 32 * K};
+    cuuint32_t box[3] = {(cuuint32_t)(4 * K), (cuuint32_t)(cc / 16), (cuuint32_t)kGemvBoxRows};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<uint16_t *>(trellis), dims, strides, box,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
   GemvArgs a;
   a.x = reinterpret_cast<const __half *>(x);
-  a.trellis = trellis;
   a.suh = reinterpret_cast<const __half *>(suh);
   a.svh = reinterpret_cast<const __half *>(svh);
   a.y = y;
@@ -466,14 +555,16 @@ cudaError_t exl3_launch_gemv_m1(const uint16_t *x, const uint16_t *trellis, cons
   a.k = k;
   a.n = n;
   a.tiles_k = k / 16;
-  const int cc = exl3_gemv_cta_cols(K);
   a.colblocks = (n + cc - 1) / cc;
   a.total = (long long)a.colblocks * a.tiles_k;
+  a.stages = 0;
+  EXL3_K_SWITCH(K, a.stages = Launcher<KK, false>::stages(k));
+  if (a.stages < 2) return cudaErrorInvalidValue;
   cudaError_t e = cudaSuccess;
   if (f32out) {
-    EXL3_K_SWITCH(K, e = Launcher<KK, true>::launch(a, grid, s));
+    EXL3_K_SWITCH(K, e = Launcher<KK, true>::launch(tm, a, grid, s, prefetch));
   } else {
-    EXL3_K_SWITCH(K, e = Launcher<KK, false>::launch(a, grid, s));
+    EXL3_K_SWITCH(K, e = Launcher<KK, false>::launch(tm, a, grid, s, prefetch));
   }
   return e;
 }

@@ -25,7 +25,8 @@
 
 cudaError_t exl3_launch_gemv_m1(const uint16_t *x, const uint16_t *trellis, const uint16_t *suh,
                                 const uint16_t *svh, int k, int n, int K, void *y, bool f32out,
-                                float *partials, int *counters, int *err, int grid, cudaStream_t s);
+                                float *partials, int *counters, int *err, int grid, cudaStream_t s,
+                                bool prefetch = false);
 int exl3_gemv_cta_cols(int K);
 void exl3_gemv_plan(int k, int n, int K, int *grid, size_t *partial_floats);
 
