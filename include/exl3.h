@@ -118,7 +118,9 @@ int exl3_input_rht(const uint16_t *x, int M, int k, const uint16_t *suh,
  *   suh [k], svh [n] fp16         K in 1..8, codebook = EXL3_CB_MUL1
  *   y        [M][n], fp16 (EXL3_OUT_F16) or fp32 (EXL3_OUT_F32)
  *   workspace of exl3_linear_workspace_size(M, k, n, K) bytes.
- *   M = 1 runs the fused CUDA-core GEMV; larger M runs the tensor-core paths.
+ *   M = 1 runs the fused CUDA-core GEMV (or, for a k whose x' does not fit
+ *   in its shared memory, about k > 44000 at K = 7, the small-M tensor-core
+ *   path); larger M runs the tensor-core paths.
  */
 size_t exl3_linear_workspace_size(int M, int k, int n, int K);
 int exl3_linear(const uint16_t *x, int M, int k, int n,
@@ -205,8 +207,9 @@ int exl3_moe_grouped(const uint16_t *x, int T, int hidden,
  *   y [n] fp16 (EXL3_OUT_F16) or fp32 (EXL3_OUT_F32); K, codebook as above.
  *   Scratch: one fixed 2 MiB array of library device memory per GPU that
  *   loads the library, held until the process exits.  A shape whose k-split
- *   partial sums do not fit is rejected with EXL3_ERR_SHAPE (use exl3_linear
- *   with a workspace instead).  The first call on a device looks up the
+ *   partial sums do not fit, or whose k is too large for the GEMV (see
+ *   exl3_linear), is rejected with EXL3_ERR_SHAPE (use exl3_linear with a
+ *   workspace instead).  The first call on a device looks up the
  *   array's device address (cudaGetSymbolAddress) with that device current;
  *   make that first call before any stream capture.  Each call clears the
  *   parts of the array that must start at zero.  All calls share the array:

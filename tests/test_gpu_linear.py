@@ -250,3 +250,14 @@ def test_linear_m1_weight_prefetch_chain():
         assert tq.exl3_check_device_error(wsa) == 0 and tq.exl3_check_device_error(wsb) == 0
     finally:
         tq.exl3_set_weight_prefetch(prev)
+
+
+def test_linear_m1_k_too_large_for_gemv_takes_tensor_core_path():
+    """At K = 7 and k = 49152, x' and two 56 KB ring stages do not fit in the
+    GEMV's shared memory: M = 1 then runs the small-M tensor-core path, with
+    the same results; the workspace-free GEMV entry rejects the shape."""
+    case = synth.linear_case(19, 0, 1, 49152, 256, 7)
+    _check_case(case)
+    with pytest.raises(tq.Exl3Error) as e:
+        tq.exl3_linear_gemv_noalloc(dev(case.x), dev(case.trellis), dev(case.suh), dev(case.svh), 7)
+    assert e.value.code == tq.EXL3_ERR_SHAPE

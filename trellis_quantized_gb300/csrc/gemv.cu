@@ -9,8 +9,9 @@
 // paths do); both differences (< 2^-11 relative per term) stay inside the
 // output tolerance.  DP4A seeded with 0x6400 yields the fp16 value 1024 + B
 // in the low half of its result, which a mixed-precision FMA multiplies by
-// the fp16 x' into an fp32 accumulator: sum x' (1024 + B).  The offset is
-// removed once per lane, 1534 * sum x' (1024 + 510 = 1534), at the end.
+// the fp16 x' into an fp32 accumulator: sum x' (1024 + B).  The offset,
+// 1534 * sum x' (1024 + 510 = 1534), is removed once per column block from
+// per-tile-row sums of x' kept beside x'.
 //
 // Lane work.  A lane owns G >= 4 consecutive rows of one tile: 16 G weights
 // whose states come from CPL contiguous 16-byte chunks (128 CPL bits) plus
@@ -51,7 +52,7 @@ namespace exl3 {
 
 constexpr int kGemvBoxRows = 8;                 // tile rows per tensor copy
 constexpr int kGemvSmemMax = 232448;            // opt-in shared memory per CTA (227 KB; no static smem)
-constexpr int kGemvMaxStages = 6;
+constexpr int kGemvMaxStages = 8;
 
 template <int K>
 struct GemvShape {
@@ -65,9 +66,10 @@ struct GemvShape {
   static constexpr int CTA_COLS = TPW * 16;      // 128 or 256 columns per block
   static constexpr int NW = 4 * CPL;             // 32-bit stream words per lane
   static constexpr int ROWB = CTA_COLS * 2 * K;  // bytes of one row (CTA_COLS/16 tiles of 32K bytes)
-  // consumer warps, and rows per consumer warp per stage: stages of 16-48 KB
-  // so that two stages and x' for the largest k fit in shared memory
-  static constexpr int NCW = ROWB >= 2560 ? 16 : 24;
+  // consumer warps (16 measured faster than 8, 12, 20 or 24: more
+  // registers per thread and a shorter spread of warp finishing times), and
+  // rows per consumer warp per stage (stages of 16-56 KB)
+  static constexpr int NCW = 16;
   static constexpr int RPW = ROWB >= 1536 ? 1 : 2;
   static constexpr int R = RPW * NCW;            // rows per stage
   static constexpr int STAGE_B = R * ROWB;
@@ -139,11 +141,12 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
   uint8_t *ring = smem_raw;                                            // [STAGES][R][ROWB]
   float *red = reinterpret_cast<float *>(smem_raw + (size_t)STAGES * S::STAGE_B);   // [NCW][CTA_COLS]
   volatile int *s_abort = reinterpret_cast<volatile int *>(red + NCW * S::CTA_COLS);   // a wait ran out
-  uint64_t *full = reinterpret_cast<uint64_t *>(red + NCW * S::CTA_COLS + 2);    // [STAGES]
+  uint64_t *full = reinterpret_cast<uint64_t *>(red + NCW * S::CTA_COLS + 4);    // [STAGES]
   uint64_t *empty = full + STAGES;                                     // [STAGES]
   uint64_t *seg_full = empty + STAGES;                                 // red holds a finished segment
   uint64_t *red_free = seg_full + 1;                                   // the flusher has read red
   __half *xs = reinterpret_cast<__half *>(red_free + 1);               // [k] fp16 x' (touched blocks)
+  float *rsum = reinterpret_cast<float *>(xs + a.k);                   // [k/16] sum of x' per tile row
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int grid = gridDim.x, me = blockIdx.x;
@@ -233,10 +236,18 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
       }
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(red_free);
+      // every column's sum is sum x' (1024 + B): remove 1534 * (the segment's sum of x')
+      float sg = 0.f;
+      {
+        const int tk_first = (int)(t - (long long)c * TK), nrows = (int)(seg_end - t);
+        for (int r = lane; r < nrows; r += 32) sg += rsum[tk_first + r];
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) sg += __shfl_xor_sync(0xffffffffu, sg, m);
+      }
 #pragma unroll
       for (int g = 0; g < S::NG; ++g)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) v[g][e] *= kSigma;
+        for (int e = 0; e < 4; ++e) v[g][e] = fmaf(-1534.0f, sg, v[g][e]) * kSigma;
 
       const int col0 = c * S::CTA_COLS;
       const long long blk_first = (long long)c * TK, blk_last = min((long long)(c + 1) * TK, a.total) - 1;
@@ -248,18 +259,18 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
         for (int g = 0; g < S::NG; ++g)
           *reinterpret_cast<float4 *>(a.partials + (long)(c + me) * S::CTA_COLS + g * 128 + lane * 4) =
               make_float4(v[g][0], v[g][1], v[g][2], v[g][3]);
-        __threadfence();
+        // the warp barrier orders every lane's stores before lane 0's
+        // release; its acquire orders the reads of the last arriver
         __syncwarp();
         int old = 0;
         const int expected = i_last - i_first + 1;
         if (lane == 0) {
-          old = atomicAdd(a.counters + c, 1);
+          asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(old) : "l"(a.counters + c) : "memory");
           if (old >= expected) set_device_error(a.err, kErrDirtyCounter);
         }
         old = __shfl_sync(0xffffffffu, old, 0);
         finish = old == expected - 1;
         if (finish) {
-          __threadfence();
 #pragma unroll
           for (int g = 0; g < S::NG; ++g) v[g][0] = v[g][1] = v[g][2] = v[g][3] = 0.f;
           for (int i = i_first; i <= i_last; ++i) {
@@ -305,42 +316,52 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
   }
 
   // ---------------- consumers (warps 0..NCW-1)
-  // prologue: x' = 2^-3.5 H (x . suh) for the 128-blocks this range touches
+  // prologue: x' = 2^-3.5 H (x . suh) for the 512-element chunks (32 tile
+  // rows) this range touches; a warp transforms four 128-blocks at once,
+  // eight lanes per block and 16 contiguous elements per lane
   {
-    const int KB = a.k >> 7;
-    int b0 = 0, nb = KB;
+    const int KC = (a.k + 511) >> 9;
+    int c0 = 0, nc = KC;
     if (t1 - t0 < TK) {   // fewer rows than one block: at most two column blocks
-      b0 = (int)(t0 % TK) >> 3;
-      const int b1 = (int)((t1 - 1) % TK) >> 3;
+      c0 = (int)(t0 % TK) >> 5;
+      const int c1 = (int)((t1 - 1) % TK) >> 5;
       const bool wrap = (t0 / TK) != ((t1 - 1) / TK);
-      nb = !wrap ? b1 - b0 + 1 : (b1 >= b0 ? KB : KB - b0 + b1 + 1);
+      nc = !wrap ? c1 - c0 + 1 : (c1 >= c0 ? KC : KC - c0 + c1 + 1);
     }
-    // four blocks per warp per round, all loads issued before any arithmetic
-    for (int i0 = warp; i0 < nb; i0 += 4 * NCW) {
-      uint2 xv[4], sv[4];
+    for (int i = warp; i < nc; i += NCW) {
+      const int e0 = ((c0 + i) % KC) * 512 + lane * 16;
+      const bool live = e0 < a.k;   // k is a multiple of 128: whole 8-lane groups
+      float v[16];
+      if (live) {
+        uint4 xv[2], sv[2];
+        xv[0] = *reinterpret_cast<const uint4 *>(a.x + e0);
+        xv[1] = *reinterpret_cast<const uint4 *>(a.x + e0 + 8);
+        sv[0] = *reinterpret_cast<const uint4 *>(a.suh + e0);
+        sv[1] = *reinterpret_cast<const uint4 *>(a.suh + e0 + 8);
+        const __half2 *xh = reinterpret_cast<const __half2 *>(xv);
+        const __half2 *sh = reinterpret_cast<const __half2 *>(sv);
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = i0 + u * NCW;
-        if (i < nb) {
-          const int col = ((b0 + i) % KB) * 128 + lane * 4;
-          xv[u] = *reinterpret_cast<const uint2 *>(a.x + col);
-          sv[u] = *reinterpret_cast<const uint2 *>(a.suh + col);
+        for (int j = 0; j < 8; ++j) {
+          v[2 * j] = __low2float(xh[j]) * __low2float(sh[j]);
+          v[2 * j + 1] = __high2float(xh[j]) * __high2float(sh[j]);
         }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = 0.f;
       }
+      fwht128_x8(v, lane);
+      if (live) {
+        uint4 o[2];
+        __half2 *oh = reinterpret_cast<__half2 *>(o);
+        float rs = 0.f;   // the 16 elements are one tile row
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = i0 + u * NCW;
-        if (i < nb) {
-          const int col = ((b0 + i) % KB) * 128 + lane * 4;
-          const __half2 *xh = reinterpret_cast<const __half2 *>(&xv[u]);
-          const __half2 *sh = reinterpret_cast<const __half2 *>(&sv[u]);
-          float v[4] = {__low2float(xh[0]) * __low2float(sh[0]), __high2float(xh[0]) * __high2float(sh[0]),
-                        __low2float(xh[1]) * __low2float(sh[1]), __high2float(xh[1]) * __high2float(sh[1])};
-          fwht128_warp(v, lane);
-          __half2 o[2] = {__floats2half2_rn(v[0] * kRhtScale, v[1] * kRhtScale),
-                          __floats2half2_rn(v[2] * kRhtScale, v[3] * kRhtScale)};
-          *reinterpret_cast<uint2 *>(xs + col) = *reinterpret_cast<uint2 *>(o);
+        for (int j = 0; j < 8; ++j) {
+          oh[j] = __floats2half2_rn(v[2 * j] * kRhtScale, v[2 * j + 1] * kRhtScale);
+          rs += __low2float(oh[j]) + __high2float(oh[j]);
         }
+        *reinterpret_cast<uint4 *>(xs + e0) = o[0];
+        *reinterpret_cast<uint4 *>(xs + e0 + 8) = o[1];
+        rsum[e0 >> 4] = rs;
       }
     }
   }
@@ -361,7 +382,6 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
     float acc[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-    float sx = 0.f;   // sum of the x' this lane used (for the 1024 + 510 offset)
 
     for (int r0 = 0; r0 < nrows; r0 += S::R) {
       const int cnt = min(S::R, nrows - r0);
@@ -388,11 +408,7 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
           const int tk = tk_first + r0 + j;
           unsigned short xr[S::G];
 #pragma unroll
-          for (int i = 0; i < S::G; ++i) {
-            const __half xv = xs[tk * 16 + S::G * q + i];
-            xr[i] = __half_as_ushort(xv);
-            sx += __half2float(xv);
-          }
+          for (int i = 0; i < S::G; ++i) xr[i] = __half_as_ushort(xs[tk * 16 + S::G * q + i]);
           decode_accumulate<K, 0>(w, xr, acc);
         }
       }
@@ -405,7 +421,7 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
     // leave this warp's column sums in red for the flusher
     float accf[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) accf[i] = fmaf(-1534.0f, sx, acc[i]);
+    for (int i = 0; i < 16; ++i) accf[i] = acc[i];
 #pragma unroll
     for (int m = 1; m < S::LPT; m <<= 1)
 #pragma unroll
@@ -457,13 +473,15 @@ template <int K, bool F32>
 struct Launcher {
   using S = GemvShape<K>;
   // ring stages that fit beside x' (2 bytes per k) and the reduction buffers
+  // x' (2 bytes per k) and its per-tile-row sums (4 bytes per 16 k)
+  static size_t xbytes(int k) { return 2 * (size_t)k + (size_t)k / 4; }
   static int stages(int k) {
-    const long avail = (long)kGemvSmemMax - S::FIXED_B - 2L * k;
+    const long avail = (long)kGemvSmemMax - S::FIXED_B - (long)xbytes(k);
     long st = avail / S::STAGE_B;
     if (st > kGemvMaxStages) st = kGemvMaxStages;
     return (int)st;
   }
-  static size_t smem(int k, int st) { return (size_t)st * S::STAGE_B + S::FIXED_B + 2 * (size_t)k; }
+  static size_t smem(int k, int st) { return (size_t)st * S::STAGE_B + S::FIXED_B + xbytes(k); }
   static cudaError_t launch(const CUtensorMap &tm, const GemvArgs &a, int grid, cudaStream_t s, bool prefetch) {
     const size_t sm = smem(a.k, a.stages);
     static size_t attr = 0;
@@ -510,6 +528,14 @@ int exl3_gemv_cta_cols(int K) {
   int r = 128;
   EXL3_K_SWITCH(K, r = GemvShape<KK>::CTA_COLS);
   return r;
+}
+
+// Whether the GEMV holds x' for this k beside two ring stages (otherwise
+// the caller takes the tensor-core path).
+bool exl3_gemv_fits(int k, int K) {
+  int st = 0;
+  EXL3_K_SWITCH(K, st = Launcher<KK, false>::stages(k));
+  return st >= 2;
 }
 
 // Grid size (one CTA per SM, at most one per row) and the partial-sum slots
