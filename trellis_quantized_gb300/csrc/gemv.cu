@@ -38,9 +38,10 @@
 // the consumer warps leave their column sums in shared memory for a flusher
 // warp and go straight on with the next block; the flusher adds the warps'
 // sums in warp order and either finishes the block itself (its CTA owned all
-// of it) or stores a partial sum in a slot fixed by (block, CTA).  The last
-// CTA to arrive at a block (atomic counter, no waiting) adds the partials in
-// CTA order, applies the output transform and writes y: the result does not
+// of it) or shares it with the neighbouring CTAs: the block's first CTA, for
+// which it is the last segment, waits (bounded) until the others have
+// published partial sums in slots fixed by (block, CTA), adds them in CTA
+// order, applies the output transform and writes y.  The result does not
 // depend on timing.
 #include <cudaTypedefs.h>
 
@@ -254,26 +255,39 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
       const int i_first = range_owner(blk_first, a.total, grid), i_last = range_owner(blk_last, a.total, grid);
       bool finish = true;
       if (i_first != i_last) {
-        // partial sum in the (block, CTA) slot; the last CTA to arrive adds them
+        // A shared block is finished by its first CTA, whose range ends in it
+        // (for the others it is the first or only segment, so their partials
+        // are usually stored long before).  The others store a partial in
+        // their (block, CTA) slot and make one release increment; the
+        // finisher waits (bounded) for all of them with acquire loads and
+        // adds the partials in CTA order.
+        const int others = i_last - i_first;
+        if (me != i_first) {
 #pragma unroll
-        for (int g = 0; g < S::NG; ++g)
-          *reinterpret_cast<float4 *>(a.partials + (long)(c + me) * S::CTA_COLS + g * 128 + lane * 4) =
-              make_float4(v[g][0], v[g][1], v[g][2], v[g][3]);
-        // the warp barrier orders every lane's stores before lane 0's
-        // release; its acquire orders the reads of the last arriver
-        __syncwarp();
-        int old = 0;
-        const int expected = i_last - i_first + 1;
-        if (lane == 0) {
-          asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(old) : "l"(a.counters + c) : "memory");
-          if (old >= expected) set_device_error(a.err, kErrDirtyCounter);
-        }
-        old = __shfl_sync(0xffffffffu, old, 0);
-        finish = old == expected - 1;
-        if (finish) {
-#pragma unroll
-          for (int g = 0; g < S::NG; ++g) v[g][0] = v[g][1] = v[g][2] = v[g][3] = 0.f;
-          for (int i = i_first; i <= i_last; ++i) {
+          for (int g = 0; g < S::NG; ++g)
+            *reinterpret_cast<float4 *>(a.partials + (long)(c + me) * S::CTA_COLS + g * 128 + lane * 4) =
+                make_float4(v[g][0], v[g][1], v[g][2], v[g][3]);
+          // the warp barrier orders every lane's stores before lane 0's release
+          __syncwarp();
+          if (lane == 0) asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(a.counters + c) : "memory");
+          finish = false;
+        } else {
+          if (lane == 0) {
+            const long long w0 = clock64();
+            int got = 0;
+            while (true) {
+              asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(got) : "l"(a.counters + c) : "memory");
+              if (got >= others) break;
+              if (clock64() - w0 > tc::kWaitLimit) {
+                set_device_error(a.err, kErrBounds);
+                break;
+              }
+              __nanosleep(64);
+            }
+            if (got > others) set_device_error(a.err, kErrDirtyCounter);
+          }
+          __syncwarp();
+          for (int i = i_first + 1; i <= i_last; ++i) {
 #pragma unroll
             for (int g = 0; g < S::NG; ++g) {
               const float4 r = __ldcg(reinterpret_cast<const float4 *>(a.partials + (long)(c + i) * S::CTA_COLS +
