@@ -27,18 +27,20 @@ constexpr int NWARPS = 3 + NGRP * NDEC;
 
 template <int K, int NMAX>
 struct Shape {
-  // Items.  K = 4 and 8: an item is G = 8 / gcd(K, 8) rows of a tile, read as
-  // CPL 16-byte chunks.  Other widths (RP): an item is one row pair of a tile,
-  // the K + 1 stream words starting at word K * rp, so every width gives 256
-  // or more items per k step (all decoder threads busy).
+  // Items.  K = 4 and 8: an item is G = 4 rows of a tile (64 weights, so the
+  // per-item costs are shared by 64 weights), read as CPL 16-byte chunks;
+  // a pair of k steps has 256 of them.  Other widths (RP): an item is one row
+  // pair of a tile, the K + 1 stream words starting at word K * rp, 256 per
+  // k step.  Either way all decoder threads are busy.
   static constexpr bool RP = (K != 4 && K != 8);
-  static constexpr int G = RP ? 2 : 8 / gcd_c(K, 8);    // rows per lane item
-  static constexpr int CPL = RP ? 0 : K / gcd_c(K, 8);  // 16-byte chunks per item
+  static constexpr int G = RP ? 2 : 4;               // rows per lane item
+  static constexpr int CPL = RP ? 0 : K * G / 8;     // 16-byte chunks per item
   static constexpr int LPT = 16 / G;             // items per tile
   static constexpr int ROWB = (BN / 16) * 32 * K;   // one tile row of the CTA: 8 tiles
   static constexpr int T_BYTES = 4 * ROWB;          // 4 tile rows per 64-deep k step
   static constexpr int X_BYTES = NMAX * BK * 2;     // x' operand of one step (up to NMAX tokens)
-  static constexpr int ITEMS = 32 * LPT;         // (tile, group) items per stage
+  static constexpr int ITEMS = 32 * LPT;         // (tile, group) items per k step
+  static_assert(2 * ITEMS % 256 == 0, "a pair of k steps keeps all 256 decoder threads busy");
   static constexpr int NW = RP ? K : 4 * CPL;    // stream words per item (one more is read)
   // Streaming: a trellis stage is TSTEPS k steps (16 tile rows) fetched by one
   // tensor load; an x' stage is XSTEPS k steps, also one tensor load.  Few,
@@ -165,24 +167,16 @@ __device__ __forceinline__ void item_map(int it, int &ti, int &q, int &swap) {
     ti = 4 * w + (l >> 3);
     q = l & 7;
     swap = q >> 2;
-  } else if constexpr (LPT == 8) {
-    // two tiles per phase pair: lanes 0-3 of a phase take groups 0-3 of one
-    // tile, lanes 4-7 groups 4-7 of the other; the halves store opposite
-    // chunk parities first
-    const int w = it >> 5, l = it & 31, p = l >> 3, i = l & 7;
-    ti = w * 4 + 2 * (p >> 1) + ((i >> 2) ^ (p & 1));
-    q = i;
-    swap = i >> 2;
-  } else if constexpr (LPT == 2) {
-    // tiles fastest (8 per phase), the second half of the phase stores the odd chunk first
-    const int w = it >> 5, l = it & 31, p = l >> 3, i = l & 7;
-    ti = (w * 16) + ((p & 1) << 3) + i;
-    q = p >> 1;
-    swap = i >> 2;
   } else {
-    ti = it / LPT;
-    q = it % LPT;
-    swap = 0;
+    // G = 4: one tile row of 8 tiles per warp; each 8-lane phase takes four
+    // tiles of one 64-column atom for two row groups, the odd group storing
+    // its odd chunk first, so a phase's stores fall in 8 distinct 16-byte
+    // bank groups
+    static_assert(LPT == 4, "item map");
+    const int w = it >> 5, l = it & 31, p = l >> 3, i = l & 7;
+    ti = 8 * w + 4 * (p & 1) + (i & 3);
+    q = 2 * (p >> 1) + (i >> 2);
+    swap = i >> 2;
   }
 }
 

@@ -205,20 +205,20 @@ __global__ void __launch_bounds__(kFtcWarps * 32, 1) fused_tc_kernel(const __gri
         if (lane == 0) set_device_error(a.err, kErrBounds);
         *abort_flag = 1;
       }
+      // the pair's items: k step 2P + h, item it (h = it2 / ITEMS)
 #pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
+      for (int it2 = dt; it2 < 2 * S::ITEMS; it2 += NDEC * 32) {
+        const int h = it2 / S::ITEMS, it = it2 - h * S::ITEMS;
         const int i = 2 * P + h;
         const uint8_t *tst = sT + ts * S::T_STAGE + (i % S::TSTEPS) * S::T_BYTES;
         uint8_t *bst = sW + (2 * ps + h) * W_BYTES;
-        for (int it = dt; it < S::ITEMS; it += NDEC * 32) {
-          int ti, q, swp;
-          item_map<K>(it, ti, q, swp);
-          const int tkl = ti >> 3, tnl = ti & 7;
-          const uint8_t *tile = tst + tkl * S::ROWB + tnl * 32 * K;
-          uint32_t w[S::NW + 1];
-          ftc::load_item<K>(tile, q, w);
-          decode_rows<K, 0>(w, bst, tkl * 16 + S::G * q, tnl * 16, swp);
-        }
+        int ti, q, swp;
+        item_map<K>(it, ti, q, swp);
+        const int tkl = ti >> 3, tnl = ti & 7;
+        const uint8_t *tile = tst + tkl * S::ROWB + tnl * 32 * K;
+        uint32_t w[S::NW + 1];
+        ftc::load_item<K>(tile, q, w);
+        decode_rows<K, 0>(w, bst, tkl * 16 + S::G * q, tnl * 16, swp);
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic stores -> tensor-core reads
       __syncwarp();

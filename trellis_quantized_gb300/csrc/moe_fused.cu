@@ -264,22 +264,22 @@ __global__ void __launch_bounds__(kWarps * 32, 1) moe_fused_kernel(const __grid_
         if (lane == 0) set_device_error(a.err, kErrBounds);
         *abort_flag = 1;
       }
+      // the pair's items: half h = it2 / ITEMS, item it
 #pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
+      for (int it2 = dt; it2 < 2 * C::ITEMS; it2 += NDEC * 32) {
+        const int h = it2 / C::ITEMS, it = it2 - h * C::ITEMS;
         // phase 1: projection h of k step P (stage rows h * 8 + (P % 2) * 4);
         // phase 2: k step 2P + h (stage rows ((2P + h) % 4) * 4)
         const int r0 = PHASE == 1 ? h * 8 + (P % 2) * 4 : ((2 * P + h) % 4) * 4;
         const uint8_t *tst = sT + ts * C::T_STAGE + r0 * C::ROWB;
         uint8_t *bst = sW + (2 * ps + h) * W_BYTES;
-        for (int it = dt; it < C::ITEMS; it += NDEC * 32) {
-          int ti, q, swp;
-          ftc::item_map<K>(it, ti, q, swp);
-          const int tkl = ti >> 3, tnl = ti & 7;
-          const uint8_t *tilep = tst + tkl * C::ROWB + tnl * 32 * K;
-          uint32_t w[S::NW + 1];
-          ftc::load_item<K>(tilep, q, w);
-          ftc::decode_rows<K, 0>(w, bst, tkl * 16 + S::G * q, tnl * 16, swp);
-        }
+        int ti, q, swp;
+        ftc::item_map<K>(it, ti, q, swp);
+        const int tkl = ti >> 3, tnl = ti & 7;
+        const uint8_t *tilep = tst + tkl * C::ROWB + tnl * 32 * K;
+        uint32_t w[S::NW + 1];
+        ftc::load_item<K>(tilep, q, w);
+        ftc::decode_rows<K, 0>(w, bst, tkl * 16 + S::G * q, tnl * 16, swp);
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic stores -> tensor-core reads
       __syncwarp();
