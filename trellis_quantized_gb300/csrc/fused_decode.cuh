@@ -95,29 +95,37 @@ __device__ __forceinline__ uint32_t decode_pair(const uint32_t (&w)[Shape<K, 32>
   return *reinterpret_cast<const uint32_t *>(&d);
 }
 
-// Decode one (tile, row group) item: rows G q .. G q + G - 1 of the tile,
-// 16 columns each, into the operand stage.
+// Decode rows R.. of one (tile, row group) item into the operand stage.  The
+// item's G rows (G = 2 or 4) start at a multiple of G within the 64-deep k
+// step, so they share one 8-row k group and row R sits at kr = kr0 + R =
+// kr0 ^ R: the 16-byte slot of its even chunk is (ch ^ kr0 ^ R), that of its
+// odd chunk the same ^ 1.  base is the item's k group, n atom and row kr0;
+// slot0 = (ch ^ kr0) << 4.
 template <int K, int R>
-__device__ __forceinline__ void decode_rows(const uint32_t (&w)[Shape<K, 32>::NW + 1], uint8_t *bstage, int k0,
-                                            int nn0, int swap) {
+__device__ __forceinline__ void decode_rows(const uint32_t (&w)[Shape<K, 32>::NW + 1], uint8_t *base,
+                                            uint32_t slot0) {
   if constexpr (R < Shape<K, 32>::G) {
     const uint4 lo = make_uint4(decode_pair<K, R, 0>(w), decode_pair<K, R, 2>(w), decode_pair<K, R, 4>(w),
                                 decode_pair<K, R, 6>(w));
     const uint4 hi = make_uint4(decode_pair<K, R, 8>(w), decode_pair<K, R, 10>(w), decode_pair<K, R, 12>(w),
                                 decode_pair<K, R, 14>(w));
-    const int kk = k0 + R;                         // k within the 64-deep step
-    const int kg = kk >> 3, kr = kk & 7;
-    const int na = nn0 >> 6, ch = (nn0 & 63) >> 3;  // 16 columns = chunks ch, ch + 1 of a 64-wide atom
-    uint8_t *row = bstage + kg * 2048 + na * 1024 + kr * 128;
-    if (swap) {
-      *reinterpret_cast<uint4 *>(row + (((ch + 1) ^ kr) << 4)) = hi;
-      *reinterpret_cast<uint4 *>(row + ((ch ^ kr) << 4)) = lo;
-    } else {
-      *reinterpret_cast<uint4 *>(row + ((ch ^ kr) << 4)) = lo;
-      *reinterpret_cast<uint4 *>(row + (((ch + 1) ^ kr) << 4)) = hi;
-    }
-    decode_rows<K, R + 1>(w, bstage, k0, nn0, swap);
+    uint8_t *row = base + R * 128;
+    *reinterpret_cast<uint4 *>(row + (slot0 ^ (uint32_t)(R << 4))) = lo;
+    *reinterpret_cast<uint4 *>(row + (slot0 ^ (uint32_t)((R ^ 1) << 4))) = hi;
+    decode_rows<K, R + 1>(w, base, slot0);
   }
+}
+
+// Decode the item of tile (tkl, tnl) of a k step (tkl: tile row 0..3, tnl:
+// tile column 0..7) and row group q into the k step's operand stage.
+template <int K>
+__device__ __forceinline__ void decode_item(const uint32_t (&w)[Shape<K, 32>::NW + 1], uint8_t *bstage, int tkl,
+                                            int tnl, int q) {
+  constexpr int G = Shape<K, 32>::G;
+  static_assert(8 % G == 0, "an item stays inside one 8-row k group");
+  const int k0 = tkl * 16 + G * q, kr0 = k0 & 7;
+  uint8_t *base = bstage + (k0 >> 3) * 2048 + (tnl >> 2) * 1024 + kr0 * 128;
+  decode_rows<K, 0>(w, base, (uint32_t)((((tnl & 3) * 2) ^ kr0) << 4));
 }
 
 // The item's stream words w[0..NW] (w[NW] is the first word of the next item
@@ -153,30 +161,23 @@ __device__ __forceinline__ void load_item(const uint8_t *tile, int q, uint32_t (
   }
 }
 
-// Item -> (tile 0..31 of the step, row group q, which chunk is stored first).
-// 32 consecutive items form one warp instruction; each 8-lane phase should
-// touch 8 distinct 16-byte bank groups for the chunk loads and the stores.
+// Item -> (tile 0..31 of the step, row group q).  32 consecutive items form
+// one warp instruction.
 template <int K>
-__device__ __forceinline__ void item_map(int it, int &ti, int &q, int &swap) {
+__device__ __forceinline__ void item_map(int it, int &ti, int &q) {
   constexpr int LPT = Shape<K, 32>::LPT;
   if constexpr (Shape<K, 32>::RP) {
     // four tiles per warp, lane = 8 tile + row pair: the words K (8 tile + rp)
     // + j of one load fall in 32 distinct banks (odd K) or 16 distinct 8-byte
-    // units per half warp (K = 2, 6); row pairs 4..7 store the odd chunk first
+    // units per half warp (K = 2, 6)
     const int w = it >> 5, l = it & 31;
     ti = 4 * w + (l >> 3);
     q = l & 7;
-    swap = q >> 2;
   } else {
-    // G = 4: one tile row of 8 tiles per warp; each 8-lane phase takes four
-    // tiles of one 64-column atom for two row groups, the odd group storing
-    // its odd chunk first, so a phase's stores fall in 8 distinct 16-byte
-    // bank groups
+    // G = 4: one tile row of 8 tiles per warp, four row groups per tile
     static_assert(LPT == 4, "item map");
-    const int w = it >> 5, l = it & 31, p = l >> 3, i = l & 7;
-    ti = 8 * w + 4 * (p & 1) + (i & 3);
-    q = 2 * (p >> 1) + (i >> 2);
-    swap = i >> 2;
+    ti = it >> 2;
+    q = it & 3;
   }
 }
 

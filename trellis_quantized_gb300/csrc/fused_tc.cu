@@ -26,9 +26,8 @@
 //                1024 + B), subtracts 1534 in half2 (exact) and stores the
 //                integers B - 510 as the MN-major, 128-byte-swizzled fp16
 //                operand (row k, 64 n per 128-byte row; 8-row k groups 2 KB
-//                apart, 64-wide n atoms 1 KB apart).  The lane-to-chunk
-//                mapping keeps both the 16-byte chunk loads and the swizzled
-//                stores free of bank conflicts where the width allows.  The
+//                apart, 64-wide n atoms 1 KB apart); an item's rows share
+//                one 8-row k group, so its store slots are one XOR each.  The
 //                decoders then run the epilogue: the TMEM accumulator
 //                (lane = output column, column = token) transposed into a
 //                shared scratch, the fixed-order split-k combine (last CTA to
@@ -212,13 +211,13 @@ __global__ void __launch_bounds__(kFtcWarps * 32, 1) fused_tc_kernel(const __gri
         const int i = 2 * P + h;
         const uint8_t *tst = sT + ts * S::T_STAGE + (i % S::TSTEPS) * S::T_BYTES;
         uint8_t *bst = sW + (2 * ps + h) * W_BYTES;
-        int ti, q, swp;
-        item_map<K>(it, ti, q, swp);
+        int ti, q;
+        item_map<K>(it, ti, q);
         const int tkl = ti >> 3, tnl = ti & 7;
         const uint8_t *tile = tst + tkl * S::ROWB + tnl * 32 * K;
         uint32_t w[S::NW + 1];
         ftc::load_item<K>(tile, q, w);
-        decode_rows<K, 0>(w, bst, tkl * 16 + S::G * q, tnl * 16, swp);
+        decode_item<K>(w, bst, tkl, tnl, q);
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic stores -> tensor-core reads
       __syncwarp();

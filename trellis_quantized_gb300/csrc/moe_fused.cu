@@ -273,13 +273,13 @@ __global__ void __launch_bounds__(kWarps * 32, 1) moe_fused_kernel(const __grid_
         const int r0 = PHASE == 1 ? h * 8 + (P % 2) * 4 : ((2 * P + h) % 4) * 4;
         const uint8_t *tst = sT + ts * C::T_STAGE + r0 * C::ROWB;
         uint8_t *bst = sW + (2 * ps + h) * W_BYTES;
-        int ti, q, swp;
-        ftc::item_map<K>(it, ti, q, swp);
+        int ti, q;
+        ftc::item_map<K>(it, ti, q);
         const int tkl = ti >> 3, tnl = ti & 7;
         const uint8_t *tilep = tst + tkl * C::ROWB + tnl * 32 * K;
         uint32_t w[S::NW + 1];
         ftc::load_item<K>(tilep, q, w);
-        ftc::decode_rows<K, 0>(w, bst, tkl * 16 + S::G * q, tnl * 16, swp);
+        ftc::decode_item<K>(w, bst, tkl, tnl, q);
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic stores -> tensor-core reads
       __syncwarp();
