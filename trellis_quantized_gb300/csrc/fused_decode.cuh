@@ -49,9 +49,10 @@ struct Shape {
   static constexpr int T_STAGE = TSTEPS * T_BYTES;
   static constexpr int XSTEPS = NMAX <= 32 ? 4 : 2;
   static constexpr int X_STAGE = XSTEPS * X_BYTES;
-  // decoded-weight ring depth (steps; even, so each decoder group owns WS / 2
-  // slots and reuses one only after its MMA of WS steps earlier)
-  static constexpr int WS = NMAX <= 32 ? 8 : 6;
+  // decoded-weight ring depth in k steps: WS / 2 pair slots, a multiple of
+  // the decoder groups (2) and of the small-M kernel's MMA issuers (4 or 2),
+  // so that each slot has one decoder group and one issuer
+  static constexpr int WS = NMAX <= 32 ? 8 : 4;
   static constexpr int XS = 2;                      // x' ring depth (stages)
   static constexpr int TS_FIT = (227 * 1024 - 2048 - WS * W_BYTES - XS * X_STAGE) / T_STAGE;
   static constexpr int TS = TS_FIT > 8 ? 8 : TS_FIT;   // trellis ring depth (stages)

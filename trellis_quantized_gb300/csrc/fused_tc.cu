@@ -13,13 +13,14 @@
 // Per CTA: one 128-column tile of y and one k-range (k splits over CTAs).
 //   warp 0       trellis producer: one tensor load per stage of 16 tile rows
 //                (8 tiles each, four 64-deep k steps) into a ring
-//   warps 1, 2   MMA issuers, one per decoder group: 4 x tcgen05.mma M128
-//                N(M) K16 per step into the group's own TMEM accumulator (a
-//                single issuer, with its barrier waits, could not keep up
-//                with the decoders)
-//   warp 19      operand producer: one tensor load of the x' tiles of 2-4 k
+//   warps 1-4    MMA issuers, one per SM sub-partition, taking every fourth
+//                pair of k steps: 4 x tcgen05.mma M128 N(M) K16 per step
+//                into the issuer's own TMEM accumulator (an issuer thread
+//                shares its sub-partition's issue slots with four decoder
+//                warps; fewer issuers could not keep up with the decoders)
+//   warp 21      operand producer: one tensor load of the x' tiles of 2-4 k
 //                steps (M rows x 64 k each, 128-byte swizzled)
-//   warps 3-18   decoders, two groups of eight taking alternate pairs of k
+//   warps 5-20   decoders, two groups of eight taking alternate pairs of k
 //                steps (one fence and one signal per pair): each
 //                lane cuts 16 G trellis states out of its chunk, hashes them
 //                (IMAD + DP4A seeded with 0x6400 gives the fp16 value
@@ -42,8 +43,16 @@
 namespace exl3 {
 namespace ftc {
 
-constexpr int kXWarp = NWARPS;            // the x' producer follows the decoder warps
-constexpr int kFtcWarps = NWARPS + 1;
+// Warp roles.  Every weight slot pair and x' slot is used by one issuer only
+// (NPS and the x' stage-to-slot map are multiples of NISS), so an issuer's
+// waits on a slot's barrier are for consecutive phases.
+template <int NMAX>
+struct Roles {
+  static constexpr int NISS = NMAX <= 32 ? 4 : 2;   // MMA issuer warps
+  static constexpr int DEC0 = 1 + NISS;              // first decoder warp
+  static constexpr int XWARP = DEC0 + NGRP * NDEC;   // the x' producer follows the decoder warps
+  static constexpr int WARPS = XWARP + 1;
+};
 
 struct Args {
   const uint16_t *trellis;
@@ -56,10 +65,13 @@ struct Args {
 };
 
 template <int K, bool F32OUT, int NMAX>
-__global__ void __launch_bounds__(kFtcWarps * 32, 1) fused_tc_kernel(const __grid_constant__ CUtensorMap tmX,
+__global__ void __launch_bounds__(Roles<NMAX>::WARPS * 32, 1) fused_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                                                                   const __grid_constant__ CUtensorMap tmT, Args a) {
   using S = Shape<K, NMAX>;
   constexpr int WS = S::WS, XS = S::XS, TS = S::TS;
+  constexpr int NISS = Roles<NMAX>::NISS, kDec0 = Roles<NMAX>::DEC0, kXWarp = Roles<NMAX>::XWARP;
+  static_assert((WS / 2) % NISS == 0 && (WS / 2) % NGRP == 0, "one issuer and one decoder group per weight slot");
+  static_assert((XS * (S::XSTEPS / 2)) % NISS == 0, "the same issuers on every use of an x' slot");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = tc::smem_u32(smem_raw);
   uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -107,14 +119,14 @@ __global__ void __launch_bounds__(kFtcWarps * 32, 1) fused_tc_kernel(const __gri
       tc::mbar_init(&wfull[s], NDEC);            // one group's warps, once per pair
       tc::mbar_init(&wempty[s], 1);
     }
-    tc::mbar_init(accum, NGRP);
+    tc::mbar_init(accum, NISS);
     *abort_flag = 0;
     tc::fence_mbar_init();
     tc::prefetch_tmap(&tmX);
     tc::prefetch_tmap(&tmT);
   }
   if (warp == 1) {
-    tc::tmem_alloc(tmem_slot, NGRP * NMAX);   // one accumulator per decoder group
+    tc::tmem_alloc(tmem_slot, NISS * NMAX);   // one accumulator per issuer
     tc::tmem_relinquish();
   }
   tc::tc_fence_before();
@@ -152,17 +164,19 @@ __global__ void __launch_bounds__(kFtcWarps * 32, 1) fused_tc_kernel(const __gri
         tc::tma_load_3d(sX + st * S::X_STAGE, &tmX, &xfull[st], 0, 0, kb0 + j * S::XSTEPS);
       }
     }
-  } else if (warp <= NGRP) {
-    // ---------------- MMA issuers: warp 1 + g takes the pairs P = g, g + 2,
+  } else if (warp <= NISS) {
+    // ---------------- MMA issuers: warp 1 + g takes the pairs P = g, g + 4,
     // ... (8 MMAs after one wait) into its own accumulator (TMEM columns
-    // g * NMAX ...), so neither issuer limits the decode rate
+    // g * NMAX ...).  One issuer per SM sub-partition: an issuer shares its
+    // sub-partition's issue slots with four decoder warps, and two issuers
+    // could not keep up with the decoders
     if (lane == 0) {
       const int g = warp - 1;
       const uint32_t dcol = tmem_base + (uint32_t)(g * NMAX);
       const uint32_t idesc = idesc_f16_amn(BN, npad);
       int xwaited = -1;
       bool stop = false;
-      for (int P = g; P < npairs; P += NGRP) {
+      for (int P = g; P < npairs; P += NISS) {
         const int xj = (2 * P) / S::XSTEPS, xs = xj % XS, ps = P % NPS;
         bool ok = true;
         if (xj != xwaited) {            // once per x' stage
@@ -194,7 +208,7 @@ __global__ void __launch_bounds__(kFtcWarps * 32, 1) fused_tc_kernel(const __gri
     }
   } else {
     // ---------------- decoders: group g takes k steps i = g, g + 2, ...
-    const int dw = warp - 3;                 // 0..15
+    const int dw = warp - kDec0;             // 0..15
     const int grp = dw / NDEC, dt = (dw % NDEC) * 32 + lane;
     for (int P = grp; P < npairs; P += NGRP) {
       const int tj = P / 2, ts = tj % TS, ps = P % NPS;   // a trellis stage holds two pairs
@@ -228,12 +242,12 @@ __global__ void __launch_bounds__(kFtcWarps * 32, 1) fused_tc_kernel(const __gri
     }
 
     // ---------------- epilogue
-    // (1) warps 3..6 (TMEM lanes 96-127, 0-31, 32-63, 64-95 = output columns)
-    // write the sum of the two groups' accumulators (group 0 + group 1, in
-    // that order), times sigma, transposed into a scratch [M][128] fp32 that
-    // reuses the operand ring (free once every MMA has completed).
+    // (1) the first four decoder warps (one per TMEM lane quarter = output
+    // columns) write the sum of the issuers' accumulators (issuer 0 + 1 + 2 +
+    // 3, in that order), times sigma, transposed into a scratch [M][128] fp32
+    // that reuses the operand ring (free once every MMA has completed).
     float *scratch = reinterpret_cast<float *>(smem);
-    if (warp < 7) {
+    if (dw < 4) {
       bool ok = tc::mbar_wait(accum, 0);
       ok = __all_sync(0xffffffffu, ok) && !*abort_flag;
       if (!ok && lane == 0) set_device_error(a.err, kErrBounds);
@@ -241,23 +255,23 @@ __global__ void __launch_bounds__(kFtcWarps * 32, 1) fused_tc_kernel(const __gri
       const int lane_base = 32 * (warp & 3);
       const int ncol = lane_base + lane;
       for (int m0 = 0; m0 < a.M; m0 += 8) {
-        uint32_t r[8], u[8];
-        const uint32_t taddr = tmem_base + ((uint32_t)lane_base << 16) + (uint32_t)m0;
-        asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
-                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-                     : "r"(taddr));
-        asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
-                     : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7])
-                     : "r"(taddr + (uint32_t)NMAX));
-        tc::tmem_ld_wait();
-        if (npairs < 2) {                // group 1 had no pair: its accumulator was never written
+        float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int j = 0; j < 8; ++j) u[j] = 0u;
+        for (int g = 0; g < NISS; ++g) {
+          if (g >= npairs) break;        // issuer g had no pair: its accumulator was never written
+          uint32_t r[8];
+          const uint32_t taddr = tmem_base + ((uint32_t)lane_base << 16) + (uint32_t)(g * NMAX + m0);
+          asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+                       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                         "=r"(r[7])
+                       : "r"(taddr));
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 8; ++j) sum[j] += __uint_as_float(r[j]);
         }
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          if (m0 + j < a.M)
-            scratch[(m0 + j) * 128 + ncol] = (__uint_as_float(r[j]) + __uint_as_float(u[j])) * kSigma;
+          if (m0 + j < a.M) scratch[(m0 + j) * 128 + ncol] = sum[j] * kSigma;
       }
       tc::tc_fence_before();
     }
@@ -326,7 +340,7 @@ __global__ void __launch_bounds__(kFtcWarps * 32, 1) fused_tc_kernel(const __gri
   __syncthreads();
   if (warp == 1) {
     tc::tc_fence_after();
-    tc::tmem_dealloc(tmem_base, NGRP * NMAX);
+    tc::tmem_dealloc(tmem_base, NISS * NMAX);
   }
 }
 
@@ -415,7 +429,7 @@ int exl3_launch_fused_tc(const uint16_t *xh, const uint16_t *trellis, const uint
   do {                                                                                                      \
     auto kfn = ftc::fused_tc_kernel<KK, F32, NM>;                                                           \
     cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, ftc::Shape<KK, NM>::SMEM_BYTES);  \
-    kfn<<<grid, ftc::kFtcWarps * 32, ftc::Shape<KK, NM>::SMEM_BYTES, s>>>(ta, tt, a);                              \
+    kfn<<<grid, ftc::Roles<NM>::WARPS * 32, ftc::Shape<KK, NM>::SMEM_BYTES, s>>>(ta, tt, a);                              \
     e = cudaGetLastError();                                                                                 \
   } while (0)
 #define EXL3_FTC_K(KK)                                          \

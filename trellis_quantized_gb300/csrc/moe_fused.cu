@@ -45,7 +45,12 @@ struct Cfg {
   static constexpr int NP = PHASE == 1 ? 2 : 1;         // projections (accumulators per issuer)
   static constexpr int ROWB = (BN / 16) * 32 * K;       // one tile row of the CTA's 8 tiles
   static constexpr int T_STAGE = 16 * ROWB;             // two pairs
-  static constexpr int NPS = 3;                         // pair slots of the weight ring
+  // pair slots of the weight ring: a multiple of the issuers and of the
+  // decoder groups (2), so that every slot has one issuer and one group and
+  // their waits on the slot's barriers are for consecutive phases; four
+  // where they fit beside two x' and two trellis stages
+  static constexpr int NPS_FIT4 = (227 * 1024 - 2048 - 8 * W_BYTES - 2 * 2 * XROWS * BK * 2 - 2 * 16 * ROWB) >= 0;
+  static constexpr int NPS = NPS_FIT4 ? 4 : 2;
   static constexpr int W_RING = 2 * NPS * W_BYTES;
   static constexpr int X_STAGE = 2 * X_STEP;            // one pair
   // x' ring: as deep as the budget allows after two trellis stages (the
@@ -58,6 +63,7 @@ struct Cfg {
   static constexpr int ITEMS = 32 * ftc::Shape<K, 32>::LPT;  // items per (k step, projection)
   static constexpr uint32_t TMEM_COLS = NGRP * NP * XROWS;
   static_assert(TS >= 2 && XS >= 2, "operand rings too shallow");
+  static_assert(NPS % NGRP == 0, "one issuer and one decoder group per weight slot");
   static_assert(NP * XROWS * 128 * 4 <= XS * X_STAGE + W_RING, "epilogue scratch exceeds the operand rings");
 };
 
