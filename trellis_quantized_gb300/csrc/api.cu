@@ -16,7 +16,7 @@ cudaError_t exl3_launch_decode_tile(const uint16_t *trellis, int n, int K, int t
 cudaError_t exl3_launch_reconstruct_t(const uint16_t *trellis, int k, int n, int K, uint16_t *wt,
                                       cudaStream_t s);
 cudaError_t exl3_launch_input_rht(const uint16_t *x, int M, int k, const uint16_t *suh, void *out,
-                                  bool f32out, cudaStream_t s);
+                                  bool f32out, cudaStream_t s, float *xsum = nullptr);
 cudaError_t exl3_launch_gemv_m1(const uint16_t *x, const uint16_t *trellis, const uint16_t *suh,
                                 const uint16_t *svh, int k, int n, int K, void *y, bool f32out,
                                 float *partials, int *counters, int *err, int grid, cudaStream_t s,
@@ -31,9 +31,9 @@ cudaError_t exl3_launch_quant_act(const uint16_t *x, int M, int k, const uint16_
 cudaError_t exl3_launch_reconstruct_q8_t(const uint16_t *trellis, int k, int n, int K, uint16_t *wq,
                                          cudaStream_t s);
 int exl3_fused_tc_splits(int k, int n);
-int exl3_launch_fused_tc(const uint16_t *xh, const uint16_t *trellis, const uint16_t *svh, int M, int k, int n,
-                         int K, void *y, bool f32out, float *partials, int *counters, int *err, int splits,
-                         cudaStream_t s);
+int exl3_launch_fused_tc(const uint16_t *xh, const float *xsum, const uint16_t *trellis, const uint16_t *svh, int M,
+                         int k, int n, int K, void *y, bool f32out, float *partials, int *counters, int *err,
+                         int splits, cudaStream_t s);
 
 cudaError_t exl3_launch_moe_remap(const int32_t *ids, int U, int E, int *counts, int *offsets, int *perm, int *pos,
                                   int *mtiles, int *n_mtiles, int max_mtiles, int *chunk_tab, int *err,
@@ -139,7 +139,7 @@ int check_linear_shape(int M, int k, int n) {
 
 // ---- exl3_linear workspace layout
 struct LinearWs {
-  size_t ctrl = 0, counters = 0, partials = 0, xh = 0, wt = 0, total = 0;
+  size_t ctrl = 0, counters = 0, partials = 0, xh = 0, xsum = 0, wt = 0, total = 0;
   int grid = 1, splits = 1;
 };
 
@@ -155,6 +155,8 @@ LinearWs linear_ws(int M, int k, int n, int K) {
   } else if (M <= kFusedMaxM) {
     w.xh = off;
     off = align_up(off + sizeof(uint16_t) * (size_t)M * k);
+    w.xsum = off;   // per-token sums of x' over 256-element units
+    off = align_up(off + sizeof(float) * (size_t)M * ((k + 255) / 256));
     w.splits = exl3_fused_tc_splits(k, n);
     w.partials = off;
     off = align_up(off + (w.splits > 1 ? sizeof(float) * (size_t)w.splits * M * n : 0));
@@ -356,10 +358,13 @@ int exl3_linear(const uint16_t *x, int M, int k, int n, const uint16_t *trellis,
                            "gemv launch");
   }
   uint16_t *xh = at<uint16_t>(workspace, L.xh);
-  EXL3_TRY(exl3_cuda_check(exl3_launch_input_rht(x, M, k, suh, xh, false, stream), "input_rht launch"));
-  if (M <= kFusedMaxM)
-    return exl3_launch_fused_tc(xh, trellis, svh, M, k, n, K, y, f32, at<float>(workspace, L.partials),
+  if (M <= kFusedMaxM) {
+    float *xsum = at<float>(workspace, L.xsum);
+    EXL3_TRY(exl3_cuda_check(exl3_launch_input_rht(x, M, k, suh, xh, false, stream, xsum), "input_rht launch"));
+    return exl3_launch_fused_tc(xh, xsum, trellis, svh, M, k, n, K, y, f32, at<float>(workspace, L.partials),
                                 at<int>(workspace, L.counters), err, L.splits, stream);
+  }
+  EXL3_TRY(exl3_cuda_check(exl3_launch_input_rht(x, M, k, suh, xh, false, stream), "input_rht launch"));
   uint16_t *wt = at<uint16_t>(workspace, L.wt);
   EXL3_TRY(exl3_cuda_check(exl3_launch_reconstruct_t(trellis, k, n, K, wt, stream), "reconstruct launch"));
   return exl3_launch_gemm_tc(xh, wt, M, n, k, svh, y, f32, nullptr, 1.0f, err, stream);

@@ -5,8 +5,9 @@
 // decoder item is (tile, row group q): G = 8 / gcd(K, 8) rows of 16 weights
 // from CPL = K / gcd(K, 8) 16-byte chunks.  Each weight's 16-bit state is
 // hashed (IMAD), byte-summed by DP4A seeded with 0x6400 (the fp16 value
-// 1024 + B), and 1534 is subtracted in half2, which leaves the exact integer
-// B - 510 as fp16; sigma is applied by the caller's epilogue.  The values go
+// 1024 + B), and either 1534 is subtracted in half2, which leaves the exact
+// integer B - 510 as fp16, or 1024 + B is kept and the caller removes
+// 1534 * sum x' per token; sigma is applied by the caller's epilogue.  The values go
 // to an MN-major, 128-byte-swizzled operand: row k holds 64 n values, 8-row k
 // groups are 2 KB apart and 64-wide n atoms 1 KB apart (descriptor LBO =
 // 1024, SBO = 2048).
@@ -84,14 +85,17 @@ __device__ __forceinline__ void bulk_copy(void *dst, const void *src, uint32_t b
                : "memory");
 }
 
-// Two adjacent weights (columns C, C + 1 of row R) as the half2 (B0 - 510, B1 - 510):
-// DP4A seeded with 0x6400 gives the fp16 bits of 1024 + B; 1024 + B - 1534 is exact.
-template <int K, int R, int C>
+// Two adjacent weights (columns C, C + 1 of row R) as a half2: DP4A seeded
+// with 0x6400 gives the fp16 bits of 1024 + B.  OFS = false subtracts 1534
+// (exact) for (B0 - 510, B1 - 510); OFS = true keeps (1024 + B0, 1024 + B1)
+// and the caller removes 1534 * sum x' per token after the contraction.
+template <int K, int R, int C, bool OFS>
 __device__ __forceinline__ uint32_t decode_pair(const uint32_t (&w)[Shape<K, 32>::NW + 1]) {
   const uint32_t s0 = window_at<(16 * R + C) * K>(w), s1 = window_at<(16 * R + C + 1) * K>(w);
   const uint32_t h0 = __dp4a(s0 * kMul1, 0x01010101u, 0x6400u);
   const uint32_t h1 = __dp4a(s1 * kMul1, 0x01010101u, 0x6400u);
   const uint32_t pr = __byte_perm(h0, h1, 0x5410);
+  if constexpr (OFS) return pr;
   const __half2 d = __hsub2(*reinterpret_cast<const __half2 *>(&pr), __half2half2(__ushort_as_half(0x65FE)));
   return *reinterpret_cast<const uint32_t *>(&d);
 }
@@ -102,31 +106,31 @@ __device__ __forceinline__ uint32_t decode_pair(const uint32_t (&w)[Shape<K, 32>
 // kr0 ^ R: the 16-byte slot of its even chunk is (ch ^ kr0 ^ R), that of its
 // odd chunk the same ^ 1.  base is the item's k group, n atom and row kr0;
 // slot0 = (ch ^ kr0) << 4.
-template <int K, int R>
+template <int K, int R, bool OFS>
 __device__ __forceinline__ void decode_rows(const uint32_t (&w)[Shape<K, 32>::NW + 1], uint8_t *base,
                                             uint32_t slot0) {
   if constexpr (R < Shape<K, 32>::G) {
-    const uint4 lo = make_uint4(decode_pair<K, R, 0>(w), decode_pair<K, R, 2>(w), decode_pair<K, R, 4>(w),
-                                decode_pair<K, R, 6>(w));
-    const uint4 hi = make_uint4(decode_pair<K, R, 8>(w), decode_pair<K, R, 10>(w), decode_pair<K, R, 12>(w),
-                                decode_pair<K, R, 14>(w));
+    const uint4 lo = make_uint4(decode_pair<K, R, 0, OFS>(w), decode_pair<K, R, 2, OFS>(w),
+                                decode_pair<K, R, 4, OFS>(w), decode_pair<K, R, 6, OFS>(w));
+    const uint4 hi = make_uint4(decode_pair<K, R, 8, OFS>(w), decode_pair<K, R, 10, OFS>(w),
+                                decode_pair<K, R, 12, OFS>(w), decode_pair<K, R, 14, OFS>(w));
     uint8_t *row = base + R * 128;
     *reinterpret_cast<uint4 *>(row + (slot0 ^ (uint32_t)(R << 4))) = lo;
     *reinterpret_cast<uint4 *>(row + (slot0 ^ (uint32_t)((R ^ 1) << 4))) = hi;
-    decode_rows<K, R + 1>(w, base, slot0);
+    decode_rows<K, R + 1, OFS>(w, base, slot0);
   }
 }
 
 // Decode the item of tile (tkl, tnl) of a k step (tkl: tile row 0..3, tnl:
 // tile column 0..7) and row group q into the k step's operand stage.
-template <int K>
+template <int K, bool OFS = false>
 __device__ __forceinline__ void decode_item(const uint32_t (&w)[Shape<K, 32>::NW + 1], uint8_t *bstage, int tkl,
                                             int tnl, int q) {
   constexpr int G = Shape<K, 32>::G;
   static_assert(8 % G == 0, "an item stays inside one 8-row k group");
   const int k0 = tkl * 16 + G * q, kr0 = k0 & 7;
   uint8_t *base = bstage + (k0 >> 3) * 2048 + (tnl >> 2) * 1024 + kr0 * 128;
-  decode_rows<K, 0>(w, base, (uint32_t)((((tnl & 3) * 2) ^ kr0) << 4));
+  decode_rows<K, 0, OFS>(w, base, (uint32_t)((((tnl & 3) * 2) ^ kr0) << 4));
 }
 
 // The item's stream words w[0..NW] (w[NW] is the first word of the next item

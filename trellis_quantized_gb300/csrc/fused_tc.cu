@@ -24,9 +24,11 @@
 //                steps (one fence and one signal per pair): each
 //                lane cuts 16 G trellis states out of its chunk, hashes them
 //                (IMAD + DP4A seeded with 0x6400 gives the fp16 value
-//                1024 + B), subtracts 1534 in half2 (exact) and stores the
-//                integers B - 510 as the MN-major, 128-byte-swizzled fp16
-//                operand (row k, 64 n per 128-byte row; 8-row k groups 2 KB
+//                1024 + B) and stores these integers (exact in fp16) as the
+//                MN-major, 128-byte-swizzled fp16 operand; the epilogue
+//                removes 1534 sum x' per token, from per-256 sums of x'
+//                that the input transform writes (row k, 64 n per 128-byte
+//                row of the operand; 8-row k groups 2 KB
 //                apart, 64-wide n atoms 1 KB apart); an item's rows share
 //                one 8-row k group, so its store slots are one XOR each.  The
 //                decoders then run the epilogue: the TMEM accumulator
@@ -56,12 +58,13 @@ struct Roles {
 
 struct Args {
   const uint16_t *trellis;
+  const float *xsum;   // [M][xunits] sums of x' over 256-element units of k
   const __half *svh;
   void *y;
   float *partials;     // [splits][M][n]
   int *counters;       // [n / 128]
   int *err;
-  int M, k, n, tiles_n, kb_per_split, splits;
+  int M, k, n, tiles_n, kb_per_split, splits, xunits;
 };
 
 template <int K, bool F32OUT, int NMAX>
@@ -88,6 +91,7 @@ __global__ void __launch_bounds__(Roles<NMAX>::WARPS * 32, 1) fused_tc_kernel(co
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accum + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   int *s_last = const_cast<int *>(abort_flag + 1);
+  float *s_sx = reinterpret_cast<float *>(s_last + 1);   // [M] sum of x' over this split's k
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nt = blockIdx.x, split = blockIdx.y;
@@ -231,7 +235,7 @@ __global__ void __launch_bounds__(Roles<NMAX>::WARPS * 32, 1) fused_tc_kernel(co
         const uint8_t *tile = tst + tkl * S::ROWB + tnl * 32 * K;
         uint32_t w[S::NW + 1];
         ftc::load_item<K>(tile, q, w);
-        decode_item<K>(w, bst, tkl, tnl, q);
+        decode_item<K, true>(w, bst, tkl, tnl, q);   // the operand keeps 1024 + B
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic stores -> tensor-core reads
       __syncwarp();
@@ -247,6 +251,19 @@ __global__ void __launch_bounds__(Roles<NMAX>::WARPS * 32, 1) fused_tc_kernel(co
     // 3, in that order), times sigma, transposed into a scratch [M][128] fp32
     // that reuses the operand ring (free once every MMA has completed).
     float *scratch = reinterpret_cast<float *>(smem);
+    // (0) each token's sum of x' over this split's k (256-element units of
+    // four k steps; the last stage may hold two): the accumulators hold
+    // sum x' (1024 + B), and 1534 sum x' is removed below
+    {
+      const int dtid = dw * 32 + lane;
+      if (dtid < a.M) {
+        const int u0 = kb0 / S::TSTEPS, u1 = (kb0 + nkb + S::TSTEPS - 1) / S::TSTEPS;
+        float sx = 0.f;
+        for (int u = u0; u < u1; ++u) sx += a.xsum[(long)dtid * a.xunits + u];
+        s_sx[dtid] = sx;
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(NGRP * NDEC * 32) : "memory");   // all decoder warps
+    }
     if (dw < 4) {
       bool ok = tc::mbar_wait(accum, 0);
       ok = __all_sync(0xffffffffu, ok) && !*abort_flag;
@@ -271,7 +288,7 @@ __global__ void __launch_bounds__(Roles<NMAX>::WARPS * 32, 1) fused_tc_kernel(co
         }
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          if (m0 + j < a.M) scratch[(m0 + j) * 128 + ncol] = sum[j] * kSigma;
+          if (m0 + j < a.M) scratch[(m0 + j) * 128 + ncol] = fmaf(-1534.0f, s_sx[m0 + j], sum[j]) * kSigma;
       }
       tc::tc_fence_before();
     }
@@ -389,9 +406,9 @@ int exl3_fused_tc_splits(int k, int n) {
 }
 
 // xh: x' fp16 [M][k] (M <= 128); partials: [splits][M][n] fp32 (unused when splits == 1).
-int exl3_launch_fused_tc(const uint16_t *xh, const uint16_t *trellis, const uint16_t *svh, int M, int k, int n,
-                         int K, void *y, bool f32out, float *partials, int *counters, int *err, int splits,
-                         cudaStream_t s) {
+int exl3_launch_fused_tc(const uint16_t *xh, const float *xsum, const uint16_t *trellis, const uint16_t *svh, int M,
+                         int k, int n, int K, void *y, bool f32out, float *partials, int *counters, int *err,
+                         int splits, cudaStream_t s) {
   auto fn = ftc_tmap_fn();
   if (!fn) return exl3_fail(EXL3_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   // x' [M][k] as (64 k, M rows, k/64 blocks): one load brings XSTEPS k blocks
@@ -421,8 +438,8 @@ int exl3_launch_fused_tc(const uint16_t *xh, const uint16_t *trellis, const uint
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return exl3_fail(EXL3_ERR_CUDA, "cuTensorMapEncodeTiled (trellis) failed (%d)", (int)r);
   }
-  ftc::Args a{trellis, reinterpret_cast<const __half *>(svh), y, partials, counters, err, M, k, n, n / 16,
-              0, splits};
+  ftc::Args a{trellis, xsum, reinterpret_cast<const __half *>(svh), y, partials, counters, err, M, k, n, n / 16,
+              0, splits, (k + 255) / 256};
   dim3 grid(n / 128, splits);
   cudaError_t e = cudaSuccess;
 #define EXL3_FTC(KK, F32, NM)                                                                                \

@@ -12,12 +12,14 @@ namespace exl3 {
 
 // x [M][k] fp16 -> out [M][k] fp32 (OUT_F32) or fp16.  One warp per group of
 // four 128-blocks of a row (512 elements, 16 contiguous per lane: the
-// fwht128_x8 layout).
+// fwht128_x8 layout).  With fp16 output, xsum (optional) receives the sum of
+// each 256-element unit of the fp16 x' row, [M][ceil(k / 256)] fp32: 16
+// values per lane in order, then lanes 0-15 (or 16-31) by halving.
 
 template <bool F32OUT>
 __global__ void __launch_bounds__(256) input_rht_kernel(const __half *__restrict__ x,
                                                         const __half *__restrict__ suh, int M, int k,
-                                                        void *__restrict__ out) {
+                                                        void *__restrict__ out, float *__restrict__ xsum) {
   const int lane = threadIdx.x & 31;
   const long wid = (long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int groups = (k + 511) / 512;
@@ -41,8 +43,8 @@ __global__ void __launch_bounds__(256) input_rht_kernel(const __half *__restrict
   fwht128_x8(v, lane);
 #pragma unroll
   for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], kRhtScale);
-  if (!in) return;
   if (F32OUT) {
+    if (!in) return;
     float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(out) + row * k + col);
 #pragma unroll
     for (int q = 0; q < 4; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
@@ -50,9 +52,19 @@ __global__ void __launch_bounds__(256) input_rht_kernel(const __half *__restrict
     __align__(16) __half2 o[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) o[j] = __floats2half2_rn(v[2 * j], v[2 * j + 1]);
-    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__half *>(out) + row * k + col);
-    dst[0] = reinterpret_cast<const uint4 *>(o)[0];
-    dst[1] = reinterpret_cast<const uint4 *>(o)[1];
+    if (in) {
+      uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__half *>(out) + row * k + col);
+      dst[0] = reinterpret_cast<const uint4 *>(o)[0];
+      dst[1] = reinterpret_cast<const uint4 *>(o)[1];
+    }
+    if (xsum) {   // uniform per launch; lanes outside k hold zeros
+      float t = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) t += __low2float(o[j]) + __high2float(o[j]);
+#pragma unroll
+      for (int m = 8; m >= 1; m >>= 1) t += __shfl_xor_sync(0xffffffffu, t, m);
+      if ((lane & 15) == 0 && in) xsum[row * ((k + 255) / 256) + col / 256] = t;
+    }
   }
 }
 
@@ -61,14 +73,14 @@ __global__ void __launch_bounds__(256) input_rht_kernel(const __half *__restrict
 using namespace exl3;
 
 cudaError_t exl3_launch_input_rht(const uint16_t *x, int M, int k, const uint16_t *suh, void *out,
-                                  bool f32out, cudaStream_t s) {
+                                  bool f32out, cudaStream_t s, float *xsum) {
   const long warps = (long)M * ((k + 511) / 512);
   const unsigned grid = (unsigned)((warps + 7) / 8);
   if (grid == 0) return cudaSuccess;
   const __half *xh = reinterpret_cast<const __half *>(x);
   const __half *sh = reinterpret_cast<const __half *>(suh);
-  if (f32out) input_rht_kernel<true><<<grid, 256, 0, s>>>(xh, sh, M, k, out);
-  else input_rht_kernel<false><<<grid, 256, 0, s>>>(xh, sh, M, k, out);
+  if (f32out) input_rht_kernel<true><<<grid, 256, 0, s>>>(xh, sh, M, k, out, nullptr);
+  else input_rht_kernel<false><<<grid, 256, 0, s>>>(xh, sh, M, k, out, xsum);
   return cudaGetLastError();
 }
 
