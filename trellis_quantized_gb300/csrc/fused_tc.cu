@@ -155,6 +155,11 @@ __global__ void __launch_bounds__(Roles<NMAX>::WARPS * 32, 1) fused_tc_kernel(co
     }
   } else if (warp == kXWarp) {
     // ---------------- x' producer: XSTEPS k blocks of every token per tensor load
+    // This kernel is a programmatic dependent of the input transform that
+    // writes x' and its sums: everything before this wait (set-up, trellis
+    // loads, decoding) overlaps that kernel; x' and the workspace are read
+    // after it.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (lane == 0) {
       const uint32_t xbytes = (uint32_t)S::XSTEPS * npad * BK * 2;
       for (int j = 0; j < nxst && !*abort_flag; ++j) {
@@ -251,6 +256,7 @@ __global__ void __launch_bounds__(Roles<NMAX>::WARPS * 32, 1) fused_tc_kernel(co
     // 3, in that order), times sigma, transposed into a scratch [M][128] fp32
     // that reuses the operand ring (free once every MMA has completed).
     float *scratch = reinterpret_cast<float *>(smem);
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // x' sums, workspace and y (see the x' producer)
     // (0) each token's sum of x' over this split's k (256-element units of
     // four k steps; the last stage may hold two): the accumulators hold
     // sum x' (1024 + B), and 1534 sum x' is removed below
@@ -379,6 +385,25 @@ static PFN_cuTensorMapEncodeTiled_v12000 ftc_tmap_fn() {
   return fn;
 }
 
+// Launch as a programmatic dependent of the kernel before it on the stream
+// (the input transform): CTAs become resident, load trellis and decode while
+// that kernel finishes; they read its output after griddepcontrol.wait.
+template <typename... Params, typename... Args>
+static cudaError_t launch_dependent(void (*kfn)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                    const Args &...args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kfn, args...);
+}
+
 // Number of k splits (one CTA per SM): the split count whose CTAs fill whole
 // waves best, keeping at least 4 trellis stages (16 k steps of 64) per CTA
 // (fewer splits on ties).  Splits fall on stage boundaries.
@@ -446,8 +471,7 @@ int exl3_launch_fused_tc(const uint16_t *xh, const float *xsum, const uint16_t *
   do {                                                                                                      \
     auto kfn = ftc::fused_tc_kernel<KK, F32, NM>;                                                           \
     cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, ftc::Shape<KK, NM>::SMEM_BYTES);  \
-    kfn<<<grid, ftc::Roles<NM>::WARPS * 32, ftc::Shape<KK, NM>::SMEM_BYTES, s>>>(ta, tt, a);                              \
-    e = cudaGetLastError();                                                                                 \
+    e = launch_dependent(kfn, grid, dim3(ftc::Roles<NM>::WARPS * 32), ftc::Shape<KK, NM>::SMEM_BYTES, s, ta, tt, a); \
   } while (0)
 #define EXL3_FTC_K(KK)                                          \
   case KK:                                                      \

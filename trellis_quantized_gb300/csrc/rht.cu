@@ -20,6 +20,9 @@ template <bool F32OUT>
 __global__ void __launch_bounds__(256) input_rht_kernel(const __half *__restrict__ x,
                                                         const __half *__restrict__ suh, int M, int k,
                                                         void *__restrict__ out, float *__restrict__ xsum) {
+  // a dependent kernel (the small-M linear) may start its set-up and
+  // weight loads now; it reads x' only after this grid completes
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const long wid = (long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int groups = (k + 511) / 512;
