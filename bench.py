@@ -40,8 +40,8 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # dram bytes (read + write) per launch from an ncu capture of gemv_m1_kernel<4>
 # at k=5120 n=17408, with the hash of gemv.cu at capture time; a changed
 # kernel source makes the recorded traffic stale (reported as null).
-TRAFFIC = {"file": "trellis_quantized_gb300/csrc/gemv.cu", "sha1": "aedad46169873d751f69e7bdc49b210d74a8e180",
-           "bytes_per_launch": 66052608, "workload": "k5120 n25600 K4 M1"}
+TRAFFIC = {"file": "trellis_quantized_gb300/csrc/gemv.cu", "sha1": "d7fe6e3afcd4e0b9e4180fb958c2d608d76aa517",
+           "bytes_per_launch": 65675264, "workload": "k5120 n25600 K4 M1"}
 
 
 def peaks():
