@@ -103,21 +103,22 @@ __device__ __forceinline__ uint32_t decode_pair(const uint32_t (&w)[Shape<K, 32>
 // Decode rows R.. of one (tile, row group) item into the operand stage.  The
 // item's G rows (G = 2 or 4) start at a multiple of G within the 64-deep k
 // step, so they share one 8-row k group and row R sits at kr = kr0 + R =
-// kr0 ^ R: the 16-byte slot of its even chunk is (ch ^ kr0 ^ R), that of its
-// odd chunk the same ^ 1.  base is the item's k group, n atom and row kr0;
-// slot0 = (ch ^ kr0) << 4.
+// kr0 ^ R.  With c = ch ^ kr0 (even), the 16-byte slot of row R's even chunk
+// is c ^ R and of its odd chunk c ^ R ^ 1: for R = 0, 1 these are c + R and
+// c + 1 - R, for R = 2, 3 the same from c ^ 2.  So with pA = row 0 + 16 c and
+// pB = row 0 + 16 (c ^ 2), every store address is one of them plus a
+// constant.
 template <int K, int R, bool OFS>
-__device__ __forceinline__ void decode_rows(const uint32_t (&w)[Shape<K, 32>::NW + 1], uint8_t *base,
-                                            uint32_t slot0) {
+__device__ __forceinline__ void decode_rows(const uint32_t (&w)[Shape<K, 32>::NW + 1], uint8_t *pA, uint8_t *pB) {
   if constexpr (R < Shape<K, 32>::G) {
     const uint4 lo = make_uint4(decode_pair<K, R, 0, OFS>(w), decode_pair<K, R, 2, OFS>(w),
                                 decode_pair<K, R, 4, OFS>(w), decode_pair<K, R, 6, OFS>(w));
     const uint4 hi = make_uint4(decode_pair<K, R, 8, OFS>(w), decode_pair<K, R, 10, OFS>(w),
                                 decode_pair<K, R, 12, OFS>(w), decode_pair<K, R, 14, OFS>(w));
-    uint8_t *row = base + R * 128;
-    *reinterpret_cast<uint4 *>(row + (slot0 ^ (uint32_t)(R << 4))) = lo;
-    *reinterpret_cast<uint4 *>(row + (slot0 ^ (uint32_t)((R ^ 1) << 4))) = hi;
-    decode_rows<K, R + 1, OFS>(w, base, slot0);
+    uint8_t *row = (R < 2 ? pA : pB) + R * 128;
+    *reinterpret_cast<uint4 *>(row + ((R & 1) ? 16 : 0)) = lo;
+    *reinterpret_cast<uint4 *>(row + ((R & 1) ? 0 : 16)) = hi;
+    decode_rows<K, R + 1, OFS>(w, pA, pB);
   }
 }
 
@@ -127,10 +128,11 @@ template <int K, bool OFS = false>
 __device__ __forceinline__ void decode_item(const uint32_t (&w)[Shape<K, 32>::NW + 1], uint8_t *bstage, int tkl,
                                             int tnl, int q) {
   constexpr int G = Shape<K, 32>::G;
-  static_assert(8 % G == 0, "an item stays inside one 8-row k group");
+  static_assert(G == 2 || G == 4, "an item stays inside one 8-row k group");
   const int k0 = tkl * 16 + G * q, kr0 = k0 & 7;
   uint8_t *base = bstage + (k0 >> 3) * 2048 + (tnl >> 2) * 1024 + kr0 * 128;
-  decode_rows<K, 0, OFS>(w, base, (uint32_t)((((tnl & 3) * 2) ^ kr0) << 4));
+  const int c = ((tnl & 3) * 2) ^ kr0;
+  decode_rows<K, 0, OFS>(w, base + 16 * c, base + 16 * (c ^ 2));
 }
 
 // The item's stream words w[0..NW] (w[NW] is the first word of the next item
