@@ -61,10 +61,13 @@ struct Cfg {
   static constexpr int TS = TS_FIT > 8 ? 8 : TS_FIT;
   static constexpr int SMEM_BYTES = XS * X_STAGE + W_RING + TS * T_STAGE + 2048;
   static constexpr int ITEMS = 32 * ftc::Shape<K, 32>::LPT;  // items per (k step, projection)
-  static constexpr uint32_t TMEM_COLS = NGRP * NP * XROWS;
+  // phase 2 may take two output tiles per CTA (one accumulator set each)
+  static constexpr int NTC = PHASE == 2 ? 2 : 1;
+  static constexpr uint32_t TMEM_COLS = NGRP * NP * XROWS * NTC;
   static_assert(TS >= 2 && XS >= 2, "operand rings too shallow");
   static_assert(NPS % NGRP == 0, "one issuer and one decoder group per weight slot");
-  static_assert(NP * XROWS * 128 * 4 <= XS * X_STAGE + W_RING, "epilogue scratch exceeds the operand rings");
+  static_assert(NTC * NP * XROWS * 128 * 4 <= XS * X_STAGE + W_RING, "epilogue scratch exceeds the operand rings");
+  static_assert(TMEM_COLS <= 512, "TMEM");
 };
 
 struct Args {
@@ -86,6 +89,7 @@ struct Args {
   // blockIdx.x % splits of tile blockIdx.x / splits; the last CTA of a tile
   // to arrive adds the partial sums in split order
   int splits;
+  int ntc;                  // output tiles per CTA (phase 2: 1 or 2)
   float *partials;          // [tiles][splits][2][128][128] fp32
   int *counters;            // [tiles], zero between calls
 };
@@ -98,14 +102,18 @@ __global__ void __launch_bounds__(kWarps * 32, 1) moe_fused_kernel(const __grid_
   using S = ftc::Shape<K, 32>;
   constexpr int NP = C::NP, XS = C::XS, TS = C::TS, NPS = C::NPS;
   const int tile = blockIdx.x / a.splits, split = blockIdx.x % a.splits;
-  if (tile >= *a.n_mtiles * a.NT) return;   // uniform per CTA: the tile list is device-side
-  const int4 mt = a.mtiles[tile / a.NT];
-  const int nt = tile % a.NT, e = mt.x, row0 = mt.y, rows = mt.z;
-  const int tn0 = nt * (BN / 16);
+  // output tiles nt0 .. nt0 + nts - 1 (phase 2 may take two: their pairs
+  // follow one another, tile j's pair Pt being pair j * nptile + Pt)
+  const int ntc = PHASE == 2 ? a.ntc : 1, NTG = (a.NT + ntc - 1) / ntc;
+  if (tile >= *a.n_mtiles * NTG) return;   // uniform per CTA: the tile list is device-side
+  const int4 mt = a.mtiles[tile / NTG];
+  const int nt0 = (tile % NTG) * ntc, nts = min(ntc, a.NT - nt0), e = mt.x, row0 = mt.y, rows = mt.z;
   const int KB = a.KB;
   // this CTA's pairs: absolute pair P0 + P for P < npairs (P0 even, so a
-  // trellis stage still holds pairs 2j, 2j + 1 of the range)
-  const int npairs = (PHASE == 1 ? KB : KB / 2) / a.splits;
+  // trellis stage still holds pairs 2j, 2j + 1 of the range; with two tiles
+  // nptile is even, so no stage spans them)
+  const int nptile = (PHASE == 1 ? KB : KB / 2) / a.splits;
+  const int npairs = nptile * nts;
   const int P0 = split * npairs;
   const int ntst = (npairs + 1) / 2;                 // a trellis stage holds two pairs
 
@@ -172,10 +180,12 @@ __global__ void __launch_bounds__(kWarps * 32, 1) moe_fused_kernel(const __grid_
         if (PHASE == 1) {
 #pragma unroll
           for (int p = 0; p < 2; ++p)
-            tc::tma_load_2d(sT + st * C::T_STAGE + p * 8 * C::ROWB, &tmT, &tfull[st], tn0 * (4 * K),
+            tc::tma_load_2d(sT + st * C::T_STAGE + p * 8 * C::ROWB, &tmT, &tfull[st], nt0 * (BN / 16) * (4 * K),
                             (e * a.nslots + p) * a.tiles_k + 4 * P0 + 8 * j);
         } else {
-          tc::tma_load_2d(sT + st * C::T_STAGE, &tmT, &tfull[st], tn0 * (4 * K), e * a.tiles_k + 16 * j);
+          const int jt = (2 * j) / nptile, js = j - jt * (nptile / 2);   // tile, stage within its k
+          tc::tma_load_2d(sT + st * C::T_STAGE, &tmT, &tfull[st], (nt0 + jt) * (BN / 16) * (4 * K),
+                          e * a.tiles_k + 16 * js);
         }
       }
     }
@@ -195,13 +205,14 @@ __global__ void __launch_bounds__(kWarps * 32, 1) moe_fused_kernel(const __grid_
           tc::tma_load_2d(sX + st * C::X_STAGE, &tmX0, &xfull[st], (P0 + P) * BK, row0);
           tc::tma_load_2d(sX + st * C::X_STAGE + X_STEP, &tmX1, &xfull[st], (P0 + P) * BK, row0);
         } else {
-          tc::tma_load_3d(sX + st * C::X_STAGE, &tmX0, &xfull[st], 0, row0, 2 * P);
+          tc::tma_load_3d(sX + st * C::X_STAGE, &tmX0, &xfull[st], 0, row0, 2 * (P % nptile));
         }
       }
     }
   } else if (warp <= NGRP) {
     // ---------------- MMA issuers: warp 1 + g takes the pairs P = g, g + 2, ...
-    // into accumulators (g NP + p) * 128 (phase 1: p = gate, up)
+    // into accumulators (j NGRP NP + g NP + p) * 128 (phase 1: p = gate, up;
+    // j: the CTA's output tile)
     if (lane == 0) {
       const int g = warp - 1;
       const uint32_t idesc = ftc::idesc_f16_amn(BN, XROWS);
@@ -219,10 +230,11 @@ __global__ void __launch_bounds__(kWarps * 32, 1) moe_fused_kernel(const __grid_
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int p = PHASE == 1 ? h : 0;
-          const uint32_t dcol = tmem_base + (uint32_t)((g * NP + p) * XROWS);
+          const int jt = P / nptile, Pt = P - jt * nptile;
+          const uint32_t dcol = tmem_base + (uint32_t)(((jt * NGRP + g) * NP + p) * XROWS);
           const uint64_t ad = ftc::sdesc_mn_sw128(sW + (2 * ps + h) * W_BYTES, 1024, 2048);
           const uint64_t bd = tc::sdesc_k_sw128(sX + xs * C::X_STAGE + h * X_STEP);
-          const bool first = (P == g) && (PHASE == 1 || h == 0);
+          const bool first = (Pt == g) && (PHASE == 1 || h == 0);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
             tc::mma_f16(dcol, ad + (uint64_t)((2 * 2048 * kk) >> 4), bd + 2 * kk, idesc,
@@ -239,9 +251,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1) moe_fused_kernel(const __grid_
     const int grp = dw / NDEC, dt = (dw % NDEC) * 32 + lane;
     // Epilogue operands, loaded now so that their latency hides behind the
     // decode: this lane's 4 columns of svh (gate, up) and suh (down), or of
-    // svh (down) and the routing weights of the warp's rows (lane q holds
-    // row dw + 16 q).
-    const int col0 = nt * BN;
+    // svh (down, both output tiles) and the routing weights of the warp's
+    // rows (lane q holds row dw + 16 q).
+    const int col0 = nt0 * BN;
     float ep_a[4], ep_b[4], ep_c[4], row_w = 0.f;
     {
       auto ld4 = [&](const __half *src, float (&o)[4]) {
@@ -258,6 +270,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) moe_fused_kernel(const __grid_
         ld4(a.suh2 + (long)e * a.inter, ep_c);
       } else {
         ld4(a.svh2 + (long)e * a.hidden, ep_a);
+        if (nts > 1) ld4(a.svh2 + (long)e * a.hidden + BN, ep_b);
         const int m = dw + NGRP * NDEC * lane;
         if (lane < XROWS / (NGRP * NDEC) && m < rows) row_w = a.weights[a.perm[row0 + m]];
       }
@@ -297,9 +310,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1) moe_fused_kernel(const __grid_
 
     // ---------------- epilogue
     // (1) warps 3..6 (TMEM lanes 96-127, 0-31, 32-63, 64-95 = output columns)
-    // write issuer 0's plus issuer 1's accumulator of each projection, times
-    // sigma, transposed into a scratch [NP][rows][128] over the x' and weight
-    // rings (idle once every MMA has completed).
+    // write issuer 0's plus issuer 1's accumulator of each projection (and
+    // output tile), times sigma, transposed into a scratch [tile][NP][rows][128]
+    // over the x' and weight rings (idle once every MMA has completed).
     float *scratch = reinterpret_cast<float *>(smem);
     if (warp < 7) {
       bool okw = tc::mbar_wait(accum, 0);
@@ -308,11 +321,12 @@ __global__ void __launch_bounds__(kWarps * 32, 1) moe_fused_kernel(const __grid_
       tc::tc_fence_after();
       const int lane_base = 32 * (warp & 3);
       const int ncol = lane_base + lane;
-#pragma unroll
-      for (int p = 0; p < NP; ++p) {
+      for (int jp = 0; jp < nts * NP; ++jp) {   // (tile, projection) jt NP + p
+        const int jt = jp / NP, p = jp - jt * NP;
         for (int m0 = 0; m0 < rows; m0 += 8) {
           uint32_t r[8], u[8];
-          const uint32_t taddr = tmem_base + ((uint32_t)lane_base << 16) + (uint32_t)(p * XROWS + m0);
+          const uint32_t taddr =
+              tmem_base + ((uint32_t)lane_base << 16) + (uint32_t)(((jt * NGRP) * NP + p) * XROWS + m0);
           asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
                        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
                          "=r"(r[7])
@@ -322,14 +336,14 @@ __global__ void __launch_bounds__(kWarps * 32, 1) moe_fused_kernel(const __grid_
                          "=r"(u[7])
                        : "r"(taddr + (uint32_t)(NP * XROWS)));
           tc::tmem_ld_wait();
-          if (npairs < 2) {            // issuer 1 had no pair: its accumulators were never written
+          if (nptile < 2) {            // issuer 1 had no pair: its accumulators were never written
 #pragma unroll
             for (int q = 0; q < 8; ++q) u[q] = 0u;
           }
 #pragma unroll
           for (int q = 0; q < 8; ++q)
             if (m0 + q < rows)
-              scratch[(p * XROWS + m0 + q) * 128 + ncol] = (__uint_as_float(r[q]) + __uint_as_float(u[q])) * kSigma;
+              scratch[(jp * XROWS + m0 + q) * 128 + ncol] = (__uint_as_float(r[q]) + __uint_as_float(u[q])) * kSigma;
         }
       }
       tc::tc_fence_before();
@@ -403,6 +417,16 @@ __global__ void __launch_bounds__(kWarps * 32, 1) moe_fused_kernel(const __grid_
         o.z = v[2] * kRhtScale * ep_a[2] * w;
         o.w = v[3] * kRhtScale * ep_a[3] * w;
         *reinterpret_cast<float4 *>(a.dout + row * a.hidden + col0 + 4 * lane) = o;
+        if (nts > 1) {   // the second output tile
+          const float4 h4 = *reinterpret_cast<const float4 *>(scratch + (XROWS + m) * 128 + 4 * lane);
+          float t[4] = {h4.x, h4.y, h4.z, h4.w};
+          fwht128_warp(t, lane);
+          o.x = t[0] * kRhtScale * ep_b[0] * w;
+          o.y = t[1] * kRhtScale * ep_b[1] * w;
+          o.z = t[2] * kRhtScale * ep_b[2] * w;
+          o.w = t[3] * kRhtScale * ep_b[3] * w;
+          *reinterpret_cast<float4 *>(a.dout + row * a.hidden + col0 + BN + 4 * lane) = o;
+        }
       }
     }
   }
@@ -506,6 +530,7 @@ int exl3_launch_moe_fused_gateup(const uint16_t *xg, const uint16_t *xu, int U, 
   a.inter = inter;
   a.err = err;
   a.splits = splits;
+  a.ntc = 1;
   a.partials = partials;
   a.counters = counters;
   return mf_launch<1>(K, t0, t1, tt, a, max_mtiles * a.NT * splits, s);
@@ -539,5 +564,17 @@ int exl3_launch_moe_fused_down(const uint16_t *hin, int U, int hidden, int inter
   a.hidden = hidden;
   a.err = err;
   a.splits = 1;
-  return mf_launch<2>(K, t0, t0, tt, a, max_mtiles * a.NT, s);
+  // two output tiles per CTA (one fill and one epilogue for both) when each
+  // tile's pairs fill whole trellis stages and the grid still covers the SMs
+  // twice over; few routed rows keep one tile per CTA for parallelism
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess || sms <= 0)
+      sms = 152;
+    cudaGetLastError();
+  }
+  a.ntc = ((a.KB / 2) % 2 == 0 && (long)max_mtiles * (a.NT / 2) >= 2L * sms) ? 2 : 1;
+  return mf_launch<2>(K, t0, t0, tt, a, max_mtiles * ((a.NT + a.ntc - 1) / a.ntc), s);
 }
