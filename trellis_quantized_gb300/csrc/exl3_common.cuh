@@ -116,6 +116,30 @@ __device__ __forceinline__ void set_device_error(int *err, int bit) {
   if (err) atomicOr(err, bit);
 }
 
+// Programmatic dependent launch.  pdl_trigger lets the kernel launched after
+// this one on the stream start its CTAs; pdl_wait blocks until the kernel
+// launched before it has completed and its writes are visible (both return at
+// once when the launch had no programmatic dependency).
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launch kfn as a programmatic dependent of the preceding kernel on s.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kfn)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       const Args &...args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kfn, args...);
+}
+
 __host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 __host__ __device__ constexpr int gcd_c(int a, int b) { return b == 0 ? a : gcd_c(b, a % b); }

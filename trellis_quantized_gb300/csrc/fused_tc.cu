@@ -385,25 +385,6 @@ static PFN_cuTensorMapEncodeTiled_v12000 ftc_tmap_fn() {
   return fn;
 }
 
-// Launch as a programmatic dependent of the kernel before it on the stream
-// (the input transform): CTAs become resident, load trellis and decode while
-// that kernel finishes; they read its output after griddepcontrol.wait.
-template <typename... Params, typename... Args>
-static cudaError_t launch_dependent(void (*kfn)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                                    const Args &...args) {
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kfn, args...);
-}
-
 // Number of k splits (one CTA per SM): the split count whose CTAs fill whole
 // waves best, keeping at least 4 trellis stages (16 k steps of 64) per CTA
 // (fewer splits on ties).  Splits fall on stage boundaries.
@@ -471,7 +452,8 @@ int exl3_launch_fused_tc(const uint16_t *xh, const float *xsum, const uint16_t *
   do {                                                                                                      \
     auto kfn = ftc::fused_tc_kernel<KK, F32, NM>;                                                           \
     cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, ftc::Shape<KK, NM>::SMEM_BYTES);  \
-    e = launch_dependent(kfn, grid, dim3(ftc::Roles<NM>::WARPS * 32), ftc::Shape<KK, NM>::SMEM_BYTES, s, ta, tt, a); \
+    /* a programmatic dependent of the input transform: CTAs start while it finishes */                  \
+    e = launch_pdl(kfn, grid, dim3(ftc::Roles<NM>::WARPS * 32), ftc::Shape<KK, NM>::SMEM_BYTES, s, ta, tt, a); \
   } while (0)
 #define EXL3_FTC_K(KK)                                          \
   case KK:                                                      \

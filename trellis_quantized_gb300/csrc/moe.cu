@@ -35,6 +35,8 @@ __device__ __forceinline__ unsigned lanemask_lt() {
 // leader, which adds the group size: one shared atomic per distinct id per
 // warp.  Invalid ids are reported, their unit gets pos = -1.
 __global__ void remap_hist_kernel(const int32_t *__restrict__ ids, int U, int E, Plan p, int *err) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ int hist[];   // [E]
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
@@ -84,6 +86,8 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *warp_sums, int *
 // counts become the expert's rows before each chunk; counts, offsets and the
 // 128-row tile list follow from two block scans.
 __global__ void __launch_bounds__(1024) remap_scan_kernel(int E, int nchunks, Plan p, int max_mtiles, int *err) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ int warp_sums[32];
   __shared__ int total;
   const int e = threadIdx.x;
@@ -125,6 +129,8 @@ __global__ void __launch_bounds__(1024) remap_scan_kernel(int E, int nchunks, Pl
 // chunk) + (units of e in earlier warps of the chunk) + (earlier lanes of
 // the same warp with e), so rows of an expert follow unit order.
 __global__ void remap_place_kernel(const int32_t *__restrict__ ids, int U, int E, Plan p) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ int wc[];   // [W][E]
   const int W = blockDim.x >> 5, w = threadIdx.x >> 5;
   for (int i = threadIdx.x; i < W * E; i += blockDim.x) wc[i] = 0;
@@ -154,6 +160,8 @@ __global__ void __launch_bounds__(1024) remap_small_kernel(const int32_t *__rest
   __shared__ int base[kSmallE];
   __shared__ int warp_sums[32];
   __shared__ int total;
+  pdl_trigger();
+  pdl_wait();
   const int t = threadIdx.x, w = t >> 5;
   for (int i = t; i < 32 * kSmallE; i += 1024) (&wc[0][0])[i] = 0;
   __syncthreads();
@@ -208,6 +216,8 @@ __global__ void __launch_bounds__(256) gather_rht_kernel(const __half *__restric
                                                          const int32_t *__restrict__ ids,
                                                          const __half *__restrict__ suh13,  // [E][2][hidden]
                                                          __half *__restrict__ xg, __half *__restrict__ xu) {
+  pdl_trigger();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const long wid = (long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int chunks = (hidden + 511) / 512;
@@ -266,6 +276,8 @@ __global__ void __launch_bounds__(256) gather_rht_kernel(const __half *__restric
 template <bool F32OUT>
 __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ d, const int *__restrict__ pos,
                                                       int T, int topk, int hidden, void *__restrict__ y) {
+  pdl_trigger();
+  pdl_wait();
   const long idx = ((long)blockIdx.x * 256 + threadIdx.x) * 4;
   if (idx >= (long)T * hidden) return;
   const int t = (int)(idx / hidden), c = (int)(idx % hidden);
@@ -306,21 +318,17 @@ cudaError_t exl3_launch_moe_remap(const int32_t *ids, int U, int E, int *counts,
   if (E < 1 || E > 1024) return cudaErrorInvalidValue;
   moe::Plan p{counts, offsets, perm, pos, reinterpret_cast<int4 *>(mtiles), n_mtiles, chunk_tab};
   if (U <= moe::kSmallU && E <= moe::kSmallE) {
-    moe::remap_small_kernel<<<1, 1024, 0, s>>>(ids, U, E, p, max_mtiles, err);
-    return cudaGetLastError();
+    return launch_pdl(moe::remap_small_kernel, dim3(1), dim3(1024), 0, s, ids, U, E, p, max_mtiles, err);
   }
   const int CH = exl3_moe_remap_chunk(E);
   const int nchunks = (U + CH - 1) / CH;
   if (nchunks > 0) {
-    moe::remap_hist_kernel<<<nchunks, CH, sizeof(int) * E, s>>>(ids, U, E, p, err);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(moe::remap_hist_kernel, dim3(nchunks), dim3(CH), sizeof(int) * E, s, ids, U, E, p, err);
     if (e != cudaSuccess) return e;
   }
-  moe::remap_scan_kernel<<<1, 1024, 0, s>>>(E, nchunks, p, max_mtiles, err);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(moe::remap_scan_kernel, dim3(1), dim3(1024), 0, s, E, nchunks, p, max_mtiles, err);
   if (e != cudaSuccess || nchunks == 0) return e;
-  moe::remap_place_kernel<<<nchunks, CH, sizeof(int) * (CH / 32) * E, s>>>(ids, U, E, p);
-  return cudaGetLastError();
+  return launch_pdl(moe::remap_place_kernel, dim3(nchunks), dim3(CH), sizeof(int) * (CH / 32) * E, s, ids, U, E, p);
 }
 
 cudaError_t exl3_launch_moe_gather(const uint16_t *x, int U, int hidden, int topk, const int *perm,
@@ -329,10 +337,9 @@ cudaError_t exl3_launch_moe_gather(const uint16_t *x, int U, int hidden, int top
   const long warps = (long)U * ((hidden + 511) / 512);     // one warp per (row, 512 chunk); rows <= U
   const unsigned grid = (unsigned)((warps + 7) / 8);
   if (grid == 0) return cudaSuccess;
-  moe::gather_rht_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const __half *>(x), hidden, topk, perm, offsets, E,
-                                               ids, reinterpret_cast<const __half *>(suh13),
-                                               reinterpret_cast<__half *>(xg), reinterpret_cast<__half *>(xu));
-  return cudaGetLastError();
+  return launch_pdl(moe::gather_rht_kernel, dim3(grid), dim3(256), 0, s, reinterpret_cast<const __half *>(x), hidden,
+                    topk, perm, offsets, E, ids, reinterpret_cast<const __half *>(suh13),
+                    reinterpret_cast<__half *>(xg), reinterpret_cast<__half *>(xu));
 }
 
 cudaError_t exl3_launch_moe_combine(const float *d, const int *pos, int T, int topk, int hidden, void *y,
@@ -340,7 +347,6 @@ cudaError_t exl3_launch_moe_combine(const float *d, const int *pos, int T, int t
   const long quads = (long)T * hidden / 4;
   const unsigned grid = (unsigned)((quads + 255) / 256);
   if (grid == 0) return cudaSuccess;
-  if (f32out) moe::combine_kernel<true><<<grid, 256, 0, s>>>(d, pos, T, topk, hidden, y);
-  else moe::combine_kernel<false><<<grid, 256, 0, s>>>(d, pos, T, topk, hidden, y);
-  return cudaGetLastError();
+  if (f32out) return launch_pdl(moe::combine_kernel<true>, dim3(grid), dim3(256), 0, s, d, pos, T, topk, hidden, y);
+  return launch_pdl(moe::combine_kernel<false>, dim3(grid), dim3(256), 0, s, d, pos, T, topk, hidden, y);
 }

@@ -104,6 +104,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1) moe_fused_kernel(const __grid_
   const int tile = blockIdx.x / a.splits, split = blockIdx.x % a.splits;
   // output tiles nt0 .. nt0 + nts - 1 (phase 2 may take two: their pairs
   // follow one another, tile j's pair Pt being pair j * nptile + Pt)
+  pdl_trigger();   // the chain's kernels are programmatic dependents of one another
+  pdl_wait();      // the tile list and x' come from the kernels before
   const int ntc = PHASE == 2 ? a.ntc : 1, NTG = (a.NT + ntc - 1) / ntc;
   if (tile >= *a.n_mtiles * NTG) return;   // uniform per CTA: the tile list is device-side
   const int4 mt = a.mtiles[tile / NTG];
@@ -494,8 +496,7 @@ static int mf_launch(int K, const CUtensorMap &t0, const CUtensorMap &t1, const 
   case KK: {                                                                                                \
     auto kfn = mf::moe_fused_kernel<KK, PHASE>;                                                             \
     cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, mf::Cfg<KK, PHASE>::SMEM_BYTES); \
-    kfn<<<grid, mf::kWarps * 32, mf::Cfg<KK, PHASE>::SMEM_BYTES, s>>>(t0, t1, tt, a);                       \
-    e = cudaGetLastError();                                                                                 \
+    e = launch_pdl(kfn, dim3(grid), dim3(mf::kWarps * 32), mf::Cfg<KK, PHASE>::SMEM_BYTES, s, t0, t1, tt, a);     \
   } break;
   switch (K) {
     EXL3_MF(1) EXL3_MF(2) EXL3_MF(3) EXL3_MF(4) EXL3_MF(5) EXL3_MF(6) EXL3_MF(7) EXL3_MF(8)
