@@ -66,6 +66,10 @@ template <int K>
 __global__ void __launch_bounds__(256) reconstruct_t_kernel(const uint16_t *__restrict__ trellis,
                                                             int tiles_k, int tiles_n,
                                                             uint16_t *__restrict__ wt, int k) {
+  // A programmatic dependent of the input transform: it reads only the
+  // trellis, so it runs beside that kernel, and it waits for it at the end so
+  // that its own completion (which the GEMM waits for) implies both.
+  pdl_trigger();
   __shared__ __align__(16) __half sm[32][128 + 8];
   const int t = threadIdx.x;
   const int tile_local = t >> 4, r = t & 15;       // 16 tiles per block
@@ -87,6 +91,7 @@ __global__ void __launch_bounds__(256) reconstruct_t_kernel(const uint16_t *__re
     if (ng < tiles_n * 16 && kg < k)
       *reinterpret_cast<uint4 *>(wt + (long)ng * k + kg) = *reinterpret_cast<const uint4 *>(&sm[nrow][kc]);
   }
+  pdl_wait();
 }
 
 // int8 weights ("exl3xpu" README, "Prefill: int8 linears and oneDNN fused
@@ -106,6 +111,7 @@ template <int K>
 __global__ void __launch_bounds__(256) reconstruct_q8_t_kernel(const uint16_t *__restrict__ trellis,
                                                                int tiles_k, int tiles_n,
                                                                uint16_t *__restrict__ wq, int k) {
+  pdl_trigger();   // beside the activation quantiser, as reconstruct_t_kernel
   __shared__ __align__(16) __half sm[32][128 + 8];
   const int t = threadIdx.x;
   const int tile_local = t >> 4, r = t & 15;
@@ -129,6 +135,7 @@ __global__ void __launch_bounds__(256) reconstruct_q8_t_kernel(const uint16_t *_
     if (ng < tiles_n * 16 && kg < k)
       *reinterpret_cast<uint4 *>(wq + (long)ng * k + kg) = *reinterpret_cast<const uint4 *>(&sm[nrow][kc]);
   }
+  pdl_wait();
 }
 
 }  // namespace exl3
@@ -140,7 +147,7 @@ cudaError_t exl3_launch_reconstruct_q8_t(const uint16_t *trellis, int k, int n, 
   dim3 grid(ceil_div(n / 16, 2), ceil_div(k / 16, 8));
   switch (K) {
 #define EXL3_CASE(KK) \
-  case KK: reconstruct_q8_t_kernel<KK><<<grid, 256, 0, s>>>(trellis, k / 16, n / 16, wq, k); break;
+  case KK: return launch_pdl(reconstruct_q8_t_kernel<KK>, grid, dim3(256), 0, s, trellis, k / 16, n / 16, wq, k);
     EXL3_CASE(1) EXL3_CASE(2) EXL3_CASE(3) EXL3_CASE(4) EXL3_CASE(5) EXL3_CASE(6) EXL3_CASE(7)
     EXL3_CASE(8)
 #undef EXL3_CASE
@@ -174,7 +181,7 @@ cudaError_t exl3_launch_reconstruct_t(const uint16_t *trellis, int k, int n, int
   dim3 grid(ceil_div(n / 16, 2), ceil_div(k / 16, 8));
   switch (K) {
 #define EXL3_CASE(KK) \
-  case KK: reconstruct_t_kernel<KK><<<grid, 256, 0, s>>>(trellis, k / 16, n / 16, wt, k); break;
+  case KK: return launch_pdl(reconstruct_t_kernel<KK>, grid, dim3(256), 0, s, trellis, k / 16, n / 16, wt, k);
     EXL3_CASE(1) EXL3_CASE(2) EXL3_CASE(3) EXL3_CASE(4) EXL3_CASE(5) EXL3_CASE(6) EXL3_CASE(7)
     EXL3_CASE(8)
 #undef EXL3_CASE

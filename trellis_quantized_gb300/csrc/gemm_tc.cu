@@ -153,6 +153,9 @@ __global__ void __launch_bounds__((2 + epi_warps<BN, Q8>()) * 32, 1) gemm_tc_ker
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // a programmatic dependent of the reconstruct, whose completion implies
+  // the activation transform's: operands, y and the error word after this
+  pdl_wait();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -361,11 +364,13 @@ int exl3_launch_gemm_tc(const uint16_t *xh, const uint16_t *wt, int M, int n, in
   gtc::Args a{M, n, k, reinterpret_cast<const __half *>(svh), y, row_scale, pre, err, acc_out};
   const int tiles = ((M + gtc::BM - 1) / gtc::BM) * (n / (wide ? 256 : 128));
   const int grid = tiles < sms ? tiles : sms;
+  cudaError_t e = cudaSuccess;
 #define EXL3_GTC(BNV, F32, Q)                                                                           \
   do {                                                                                                \
     auto kfn = gtc::gemm_tc_kernel<BNV, F32, Q>;                                                      \
     cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, gtc::Cfg<BNV>::SMEM_BYTES); \
-    kfn<<<grid, (2 + gtc::epi_warps<BNV, Q>()) * 32, gtc::Cfg<BNV>::SMEM_BYTES, s>>>(ta, tb, a);       \
+    e = launch_pdl(kfn, dim3(grid), dim3((2 + gtc::epi_warps<BNV, Q>()) * 32), gtc::Cfg<BNV>::SMEM_BYTES, s, ta, \
+                   tb, a);                                                                            \
   } while (0)
   if (q8 && wide) {
     if (f32out) EXL3_GTC(256, true, true); else EXL3_GTC(256, false, true);
@@ -377,6 +382,5 @@ int exl3_launch_gemm_tc(const uint16_t *xh, const uint16_t *wt, int M, int n, in
     if (f32out) EXL3_GTC(128, true, false); else EXL3_GTC(128, false, false);
   }
 #undef EXL3_GTC
-  cudaError_t e = cudaGetLastError();
   return exl3_cuda_check(e, "gemm_tc launch");
 }
