@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(Roles<NMAX>::WARPS * 32, 1) fused_tc_kernel(co
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accum + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   int *s_last = const_cast<int *>(abort_flag + 1);
-  float *s_sx = reinterpret_cast<float *>(s_last + 1);   // [M] sum of x' over this split's k
+  float *s_sx = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(s_last + 1) + 15) & ~(uintptr_t)15);   // [128] sum of x' over this split's k, 16-byte aligned
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nt = blockIdx.x, split = blockIdx.y;
@@ -265,6 +265,7 @@ __global__ void __launch_bounds__(Roles<NMAX>::WARPS * 32, 1) fused_tc_kernel(co
       if (dtid < a.M) {
         const int u0 = kb0 / S::TSTEPS, u1 = (kb0 + nkb + S::TSTEPS - 1) / S::TSTEPS;
         float sx = 0.f;
+#pragma unroll 8
         for (int u = u0; u < u1; ++u) sx += a.xsum[(long)dtid * a.xunits + u];
         s_sx[dtid] = sx;
       }
@@ -278,6 +279,11 @@ __global__ void __launch_bounds__(Roles<NMAX>::WARPS * 32, 1) fused_tc_kernel(co
       const int lane_base = 32 * (warp & 3);
       const int ncol = lane_base + lane;
       for (int m0 = 0; m0 < a.M; m0 += 8) {
+        // the tokens' x' sums, read before the TMEM loads so that their
+        // latency overlaps them
+        const float4 sa = *reinterpret_cast<const float4 *>(s_sx + m0);
+        const float4 sb = *reinterpret_cast<const float4 *>(s_sx + m0 + 4);
+        const float sxv[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
         float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int g = 0; g < NISS; ++g) {
@@ -294,7 +300,7 @@ __global__ void __launch_bounds__(Roles<NMAX>::WARPS * 32, 1) fused_tc_kernel(co
         }
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          if (m0 + j < a.M) scratch[(m0 + j) * 128 + ncol] = fmaf(-1534.0f, s_sx[m0 + j], sum[j]) * kSigma;
+          if (m0 + j < a.M) scratch[(m0 + j) * 128 + ncol] = fmaf(-1534.0f, sxv[j], sum[j]) * kSigma;
       }
       tc::tc_fence_before();
     }
