@@ -114,12 +114,13 @@ def test_moe_slot_order_does_not_matter():
     assert np.max(np.abs(y1 - y2)) <= 2e-3 * max(1.0, np.abs(y1).max())
 
 
-@pytest.mark.parametrize("E,topk,T,hidden,inter,K", [(8, 2, 2, 1024, 256, 4), (16, 4, 3, 2048, 128, 3),
-                                                     (4, 4, 1, 512, 384, 5)])
+@pytest.mark.parametrize("E,topk,T,hidden,inter,K", [(8, 2, 17, 1024, 256, 4), (16, 4, 10, 2048, 128, 3),
+                                                     (4, 4, 9, 512, 384, 5)])
 def test_moe_gateup_split_over_k(E, topk, T, hidden, inter, K):
-    """Few tokens: the gate+up projection is split over k across CTAs and the
-    last CTA of each tile adds the partial sums in split order.  Same result on
-    a second call (fixed order) and the arrival counters are back at zero."""
+    """Few tokens (but more than 32 routed rows, so the tile kernels run): the
+    gate+up projection is split over k across CTAs and the last CTA of each
+    tile adds the partial sums in split order.  Same result on a second call
+    (fixed order) and the arrival counters are back at zero."""
     c = synth.moe_case(56, E * 100 + T, T, E=E, topk=topk, hidden=hidden, inter=inter, K=K)
     d = _dev_case(c)
     ws = torch.zeros(tq.exl3_moe_workspace_size(c.T, c.topk, c.E, d["w13"], d["w2"]), dtype=torch.uint8,
@@ -130,3 +131,24 @@ def test_moe_gateup_split_over_k(E, topk, T, hidden, inter, K):
     assert tq.exl3_check_device_error(ws) == 0
     assert int(ws[256:256 + 4 * 8192].view(torch.int32).abs().sum()) == 0
     assert_close(host(y1).astype(np.float64), _oracle(c), f"moe split E{E} T{T}")
+
+
+@pytest.mark.parametrize("T,E,topk,hidden,inter,K,K2", [(4, 256, 8, 2048, 512, 3, 3), (2, 16, 8, 512, 256, 8, 2),
+                                                        (3, 6, 3, 256, 384, 1, 7), (1, 4, 2, 768, 128, 6, 5)])
+def test_moe_few_tokens_grouped_gemv(T, E, topk, hidden, inter, K, K2):
+    """Up to 32 routed rows take the few-token path: gate and up as grouped
+    M = 1 GEMVs over (unit, slot), SiLU, down as grouped GEMVs times the
+    routing weight, and the combine.  32 rows at the pages' shape is the
+    boundary; also mixed widths and odd tile counts.  Deterministic, with the
+    arrival counters back at zero."""
+    c = synth.moe_case(57, T * 100 + K, T, E=E, topk=topk, hidden=hidden, inter=inter, K=K, K2=K2)
+    d = _dev_case(c)
+    ws = torch.zeros(tq.exl3_moe_workspace_size(c.T, c.topk, c.E, d["w13"], d["w2"]), dtype=torch.uint8,
+                     device="cuda")
+    y1 = tq.exl3_moe_grouped(d["x"], d["ids"], d["w"], d["w13"], d["w2"], c.E, workspace_buf=ws).clone()
+    y2 = tq.exl3_moe_grouped(d["x"], d["ids"], d["w"], d["w13"], d["w2"], c.E, workspace_buf=ws).clone()
+    assert torch.equal(y1, y2)
+    assert tq.exl3_check_device_error(ws) == 0
+    counters = host(ws[256:256 + 4 * 1024]).view(np.int32)
+    assert np.all(counters == 0)
+    assert_close(host(y1).astype(np.float64), _oracle(c), f"moe few tokens T{T} E{E} K{K}/{K2}")

@@ -44,6 +44,11 @@ cudaError_t exl3_launch_moe_gather(const uint16_t *x, int U, int hidden, int top
                                    cudaStream_t s);
 cudaError_t exl3_launch_moe_combine(const float *d, const int *pos, int T, int topk, int hidden, void *y,
                                     bool f32out, cudaStream_t s);
+bool exl3_moe_gemv_plan(int U, int nslots, int k, int n, int K, int *grid, size_t *partial_floats, int *blocks);
+cudaError_t exl3_launch_moe_gemv(const uint16_t *x, const float *act_in, int *pos_out, const int32_t *ids,
+                                 const float *weights, int U, int topk, int E, int nslots, int k, int n, int K,
+                                 const uint16_t *trellis, const uint16_t *suh, const uint16_t *svh, float *y,
+                                 float *partials, int *counters, int *err, cudaStream_t s);
 int exl3_launch_moe_fused_gateup(const uint16_t *xg, const uint16_t *xu, int U, int hidden, int inter, int K, int E,
                                  const uint16_t *w13_trellis, const int *mtiles, const int *n_mtiles, int max_mtiles,
                                  const uint16_t *svh13, const uint16_t *suh2, uint16_t *hout, int splits,
@@ -192,11 +197,34 @@ LinearInt8Ws linear_int8_ws(int M, int k, int n) {
 struct MoeWs {
   size_t counts, offsets, pos, perm, mtiles, n_mtiles, chunk, xg, xu, h, d, partials, total;
   int max_mtiles, grid_mtiles, splits;
+  bool gemv;          // few routed rows: grouped M = 1 GEMVs instead of the tile kernels
+  size_t y13;         // gemv: gate/up outputs [U][2][inter] fp32 (d, pos, partials as above)
 };
 
-MoeWs moe_ws(int T, int topk, int E, int hidden, int inter) {
+// Routed rows up to which the few-token path (one grouped CUDA-core GEMV
+// launch per projection, no sort) runs instead of the tensor-core tiles.
+constexpr int kMoeGemvMaxU = 32;
+
+MoeWs moe_ws(int T, int topk, int E, int hidden, int inter, int K13, int K2) {
   MoeWs w{};
   const size_t U = (size_t)T * topk;
+  {
+    int g1 = 0, g2 = 0, b1 = 0, b2 = 0;
+    size_t p1 = 0, p2 = 0;
+    if (U <= (size_t)kMoeGemvMaxU && exl3_moe_gemv_plan((int)U, 2, hidden, inter, K13, &g1, &p1, &b1) &&
+        exl3_moe_gemv_plan((int)U, 1, inter, hidden, K2, &g2, &p2, &b2) && (size_t)b1 <= kMaxCounters &&
+        (size_t)b2 <= kMaxCounters) {
+      w.gemv = true;
+      size_t off = kDataOff;
+      auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes); return o; };
+      w.y13 = take(sizeof(float) * U * 2 * inter);
+      w.d = take(sizeof(float) * U * hidden);
+      w.pos = take(sizeof(int) * U);
+      w.partials = take(sizeof(float) * (p1 > p2 ? p1 : p2));
+      w.total = off;
+      return w;
+    }
+  }
   w.max_mtiles = (int)(U / 128 + E + 1);
   size_t off = kDataOff;
   auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes); return o; };
@@ -407,7 +435,7 @@ int exl3_linear_int8(const uint16_t *x, int M, int k, int n, const uint16_t *tre
 size_t exl3_moe_workspace_size(int T, int topk, int E, const exl3_expert_proj *w13,
                                const exl3_expert_proj *w2) {
   if (!w13 || !w2 || T < 1 || topk < 1 || E < 1 || E > 1024) return 0;
-  return moe_ws(T, topk, E, w13->k, w13->n).total;
+  return moe_ws(T, topk, E, w13->k, w13->n, w13->K, w2->K).total;
 }
 
 int exl3_moe_grouped(const uint16_t *x, int T, int hidden, const int32_t *topk_ids, const float *topk_weights,
@@ -423,9 +451,28 @@ int exl3_moe_grouped(const uint16_t *x, int T, int hidden, const int32_t *topk_i
     return exl3_fail(EXL3_ERR_ARG, "out_dtype %d invalid", out_dtype);
   const int inter = w13->n;
   const int U = T * topk;
-  const MoeWs L = moe_ws(T, topk, E, hidden, inter);
+  const MoeWs L = moe_ws(T, topk, E, hidden, inter, w13->K, w2->K);
   EXL3_TRY(check_workspace(workspace, ws_bytes, L.total));
   int *err = at<int>(workspace, 0);
+  if (L.gemv) {
+    // few routed rows: gate and up as U x 2 GEMVs, down as U GEMVs whose
+    // input transform applies SiLU(gate) up (output times the routing
+    // weight), combine; no sort, expert ids read in place
+    float *y13 = at<float>(workspace, L.y13), *d = at<float>(workspace, L.d);
+    int *pos = at<int>(workspace, L.pos);
+    float *partials = at<float>(workspace, L.partials);
+    int *counters = at<int>(workspace, kCounterOff);   // the fixed counter region, zero between calls
+    EXL3_TRY(exl3_cuda_check(exl3_launch_moe_gemv(x, nullptr, nullptr, topk_ids, nullptr, U, topk, E, 2, hidden,
+                                                  inter, w13->K, w13->trellis, w13->suh, w13->svh, y13, partials,
+                                                  counters, err, stream),
+                             "moe gate/up gemv launch"));
+    EXL3_TRY(exl3_cuda_check(exl3_launch_moe_gemv(nullptr, y13, pos, topk_ids, topk_weights, U, topk, E, 1, inter,
+                                                  hidden, w2->K, w2->trellis, w2->suh, w2->svh, d, partials,
+                                                  counters, err, stream),
+                             "moe down gemv launch"));
+    return exl3_cuda_check(exl3_launch_moe_combine(d, pos, T, topk, hidden, y, out_dtype == EXL3_OUT_F32, stream),
+                           "moe combine launch");
+  }
   int *counts = at<int>(workspace, L.counts), *offsets = at<int>(workspace, L.offsets);
   int *pos = at<int>(workspace, L.pos), *perm = at<int>(workspace, L.perm);
   int *mtiles = at<int>(workspace, L.mtiles), *chunk_tab = at<int>(workspace, L.chunk);

@@ -46,40 +46,10 @@
 #include <cudaTypedefs.h>
 
 #include "exl3_common.cuh"
+#include "gemv_core.cuh"
 #include "tc_ptx.cuh"
-#include "trellis_window.cuh"
 
 namespace exl3 {
-
-constexpr int kGemvBoxRows = 8;                 // tile rows per tensor copy
-constexpr int kGemvSmemMax = 232448;            // opt-in shared memory per CTA (227 KB; no static smem)
-constexpr int kGemvMaxStages = 8;
-
-template <int K>
-struct GemvShape {
-  // rows per lane item: a whole number of 16-byte chunks, and at least four
-  // rows so that per-item costs (loads, x', loop) are shared by 64+ weights
-  static constexpr int G0 = 8 / gcd_c(K, 8);
-  static constexpr int G = G0 < 4 ? 4 : G0;
-  static constexpr int CPL = K * G / 8;          // 16-byte chunks per lane
-  static constexpr int LPT = 16 / G;             // lanes per tile
-  static constexpr int TPW = 32 / LPT;           // tiles per warp
-  static constexpr int CTA_COLS = TPW * 16;      // 128 or 256 columns per block
-  static constexpr int NW = 4 * CPL;             // 32-bit stream words per lane
-  static constexpr int ROWB = CTA_COLS * 2 * K;  // bytes of one row (CTA_COLS/16 tiles of 32K bytes)
-  // consumer warps (16 measured faster than 8, 12, 20 or 24: more
-  // registers per thread and a shorter spread of warp finishing times), and
-  // rows per consumer warp per stage (stages of 16-56 KB)
-  static constexpr int NCW = 16;
-  static constexpr int RPW = ROWB >= 1536 ? 1 : 2;
-  static constexpr int R = RPW * NCW;            // rows per stage
-  static constexpr int STAGE_B = R * ROWB;
-  static constexpr int NG = CTA_COLS / 128;      // 128-column groups per block
-  static constexpr int THREADS = (NCW + 2) * 32; // + the producer and the flusher warp
-  static constexpr int FIXED_B = 4 * NCW * CTA_COLS + 256;   // red, flags, barriers
-  static_assert(R % kGemvBoxRows == 0, "stages hold whole tensor copies");
-  static_assert(ROWB % 128 == 0, "tensor copies land on 128-byte boundaries");
-};
 
 struct GemvArgs {
   const __half *x;          // [k]
@@ -87,52 +57,59 @@ struct GemvArgs {
   const __half *svh;        // [n]
   void *y;                  // [n] fp16 or fp32
   float *partials;          // [colblocks + grid][CTA_COLS]
-  int *counters;            // [colblocks]
+  int *counters;            // [nops * colblocks]
   int *err;                 // device error word
   int k, n, tiles_k, colblocks, stages;
-  long long total;          // colblocks * tiles_k
+  long long total;          // nops * colblocks * tiles_k
+  // Routed-expert mode (GROUPED): the rows of op o = unit u * nslots + slot
+  // follow those of op o - 1; op o multiplies x row (x_per_unit ? u : u / topk)
+  // by expert e = ids[u]'s slot `slot` (trellis rows (e nslots + slot) k/16 of
+  // one tensor over all experts, suh/svh [E][nslots][k or n]) into y[o][n]
+  // fp32, times weights[u] when weights is set.  An id outside [0, E) sets the
+  // error word and makes the op's output zero.
+  const int32_t *ids;
+  const float *weights;
+  int topk, nslots, E, x_per_unit, nops;
+  long long op_rows;        // colblocks * tiles_k
+  // act_in set (down projection): unit u's input is SiLU(g) u of the gate and
+  // up outputs act_in[u][0][k], act_in[u][1][k] (fp32) instead of x; pos_out
+  // (if set) receives u, or -1 for an invalid expert id, for the combine
+  const float *act_in;
+  int *pos_out;
 };
 
-// acc += x * h, x and h binary16 (h = low half of r), acc binary32.
-__device__ __forceinline__ float fma_f16_f32(unsigned short x, uint32_t r, float acc) {
-  asm("{\n.reg .f16 hx, hh;\n.reg .b16 lo, hi;\nmov.b32 {lo, hi}, %1;\nmov.b16 hh, lo;\nmov.b16 hx, %2;\n"
-      "fma.rn.f32.f16 %0, hx, hh, %0;\n}\n"
-      : "+f"(acc)
-      : "r"(r), "h"(x));
-  return acc;
-}
+constexpr int kGemvMaxOps = 4;   // ops one CTA's range may touch in GROUPED mode
 
-__device__ __forceinline__ void consumer_sync(int nthreads) {
-  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
-}
+// The pointers of op o (one op, the linear itself, when not GROUPED).
+struct GemvOp {
+  const __half *x, *suh, *svh;
+  void *y;
+  float scale;
+  int trow;                 // first trellis row of the op's weights
+  bool bad;                 // invalid expert id
+};
 
-// Decode the lane's 16 G weights and accumulate x'_row * (1024 + B) into the
-// 16 column accumulators.
-template <int K, int J>
-__device__ __forceinline__ void decode_accumulate(const uint32_t (&w)[GemvShape<K>::NW + 1],
-                                                  const unsigned short (&xr)[GemvShape<K>::G],
-                                                  float (&acc)[16]) {
-  if constexpr (J < 16 * GemvShape<K>::G) {
-    const uint32_t s = window_at<J * K>(w);
-    const uint32_t h = __dp4a(s * kMul1, 0x01010101u, 0x6400u);   // fp16 bits of 1024 + B
-    acc[J & 15] = fma_f16_f32(xr[J >> 4], h, acc[J & 15]);
-    decode_accumulate<K, J + 1>(w, xr, acc);
+template <bool GROUPED>
+__device__ __forceinline__ GemvOp gemv_op(const GemvArgs &a, int o) {
+  if constexpr (!GROUPED) {
+    return GemvOp{a.x, a.suh, a.svh, a.y, 1.0f, 0, false};
+  } else {
+    const int u = o / a.nslots, slot = o - u * a.nslots;
+    int e = a.ids[u];
+    const bool bad = e < 0 || e >= a.E;
+    float scale = a.weights ? a.weights[u] : 1.0f;
+    if (bad) {
+      e = 0;
+      scale = 0.0f;
+    }
+    const long es = (long)e * a.nslots + slot;
+    const long xr = a.x_per_unit ? u : u / a.topk;
+    return GemvOp{a.x + xr * a.k, a.suh + es * a.k, a.svh + es * a.n,
+                  static_cast<float *>(a.y) + (long)o * a.n, scale, (int)(es * a.tiles_k), bad};
   }
 }
 
-__device__ __forceinline__ long long range_start(int i, long long total, int grid) {
-  return (long long)i * total / grid;
-}
-
-// Index of the CTA whose range holds row r.
-__device__ __forceinline__ int range_owner(long long r, long long total, int grid) {
-  int i = (int)((r * grid) / total);
-  while (i + 1 < grid && range_start(i + 1, total, grid) <= r) ++i;
-  while (i > 0 && range_start(i, total, grid) > r) --i;
-  return i;
-}
-
-template <int K, bool F32OUT>
+template <int K, bool F32OUT, bool GROUPED>
 __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
     gemv_m1_kernel(const __grid_constant__ CUtensorMap tmT, GemvArgs a) {
   using S = GemvShape<K>;
@@ -146,8 +123,9 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
   uint64_t *empty = full + STAGES;                                     // [STAGES]
   uint64_t *seg_full = empty + STAGES;                                 // red holds a finished segment
   uint64_t *red_free = seg_full + 1;                                   // the flusher has read red
-  __half *xs = reinterpret_cast<__half *>(red_free + 1);               // [k] fp16 x' (touched blocks)
-  float *rsum = reinterpret_cast<float *>(xs + a.k);                   // [k/16] sum of x' per tile row
+  constexpr int NOPS = GROUPED ? kGemvMaxOps : 1;
+  __half *xs = reinterpret_cast<__half *>(red_free + 1);               // [NOPS][k] fp16 x' (touched blocks)
+  float *rsum = reinterpret_cast<float *>(xs + NOPS * a.k);            // [NOPS][k/16] sum of x' per tile row
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int grid = gridDim.x, me = blockIdx.x;
@@ -177,10 +155,12 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       for (long long t = t0; t < t1 && !*s_abort;) {
-        const int c = (int)(t / TK);
+        const int c = (int)(t / TK);   // block: op c / colblocks, column block c % colblocks
         const long long seg_end = min(t1, (long long)(c + 1) * TK);
         const int tk_first = (int)(t - (long long)c * TK), nrows = (int)(seg_end - t);
-        const int tn0 = c * (S::CTA_COLS / 16);
+        const int op = GROUPED ? c / a.colblocks : 0;
+        const int tn0 = (c - op * a.colblocks) * (S::CTA_COLS / 16);
+        const int trow = gemv_op<GROUPED>(a, op).trow + tk_first;
         for (int r0 = 0; r0 < nrows && !*s_abort; r0 += S::R) {
           const int cnt = min(S::R, nrows - r0);
           if (!tc::mbar_wait(&empty[stage], phase ^ 1)) {
@@ -196,7 +176,7 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
           uint8_t *dst = ring + (size_t)stage * S::STAGE_B;
           for (int b = 0; b < nb; ++b)
             tc::tma_load_3d(dst + (size_t)b * kGemvBoxRows * S::ROWB, &tmT, &full[stage], 0, tn0,
-                            tk_first + r0 + b * kGemvBoxRows);
+                            trow + r0 + b * kGemvBoxRows);
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
         t = seg_end;
@@ -216,9 +196,13 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
     // over while they go on decoding the next one.  Lane l holds columns
     // 128 g + 4 l .. +3 of every 128-column group g.
     uint32_t sp = 0;
+    const int op0 = GROUPED ? (int)(t0 / a.op_rows) : 0;
     for (long long t = t0; t < t1;) {
-      const int c = (int)(t / TK);
+      const int c = (int)(t / TK);   // block: op c / colblocks, column block c % colblocks
       const long long seg_end = min(t1, (long long)(c + 1) * TK);
+      const int op = GROUPED ? c / a.colblocks : 0;
+      const GemvOp P = gemv_op<GROUPED>(a, op);
+      const float *rs = rsum + (op - op0) * (a.k / 16);
       if (!*s_abort && !tc::mbar_wait(seg_full, sp)) {
         if (lane == 0) set_device_error(a.err, kErrBounds);
         *s_abort = 1;
@@ -241,7 +225,7 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
       float sg = 0.f;
       {
         const int tk_first = (int)(t - (long long)c * TK), nrows = (int)(seg_end - t);
-        for (int r = lane; r < nrows; r += 32) sg += rsum[tk_first + r];
+        for (int r = lane; r < nrows; r += 32) sg += rs[tk_first + r];
 #pragma unroll
         for (int m = 16; m >= 1; m >>= 1) sg += __shfl_xor_sync(0xffffffffu, sg, m);
       }
@@ -250,7 +234,7 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e) v[g][e] = fmaf(-1534.0f, sg, v[g][e]) * kSigma;
 
-      const int col0 = c * S::CTA_COLS;
+      const int col0 = (c - op * a.colblocks) * S::CTA_COLS;
       const long long blk_first = (long long)c * TK, blk_last = min((long long)(c + 1) * TK, a.total) - 1;
       const int i_first = range_owner(blk_first, a.total, grid), i_last = range_owner(blk_last, a.total, grid);
       bool finish = true;
@@ -308,17 +292,23 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
           const int gc = col0 + g * 128 + lane * 4;
           if (col0 + g * 128 < a.n) {
             fwht128_warp(v[g], lane);
-            const uint2 sv = *reinterpret_cast<const uint2 *>(a.svh + gc);
+            const uint2 sv = *reinterpret_cast<const uint2 *>(P.svh + gc);
             const __half2 *sh = reinterpret_cast<const __half2 *>(&sv);
-            const float o0 = v[g][0] * kRhtScale * __low2float(sh[0]);
-            const float o1 = v[g][1] * kRhtScale * __high2float(sh[0]);
-            const float o2 = v[g][2] * kRhtScale * __low2float(sh[1]);
-            const float o3 = v[g][3] * kRhtScale * __high2float(sh[1]);
+            float o0 = v[g][0] * kRhtScale * __low2float(sh[0]);
+            float o1 = v[g][1] * kRhtScale * __high2float(sh[0]);
+            float o2 = v[g][2] * kRhtScale * __low2float(sh[1]);
+            float o3 = v[g][3] * kRhtScale * __high2float(sh[1]);
+            if (GROUPED) {   // the routing weight (or zero for an invalid expert id)
+              o0 *= P.scale;
+              o1 *= P.scale;
+              o2 *= P.scale;
+              o3 *= P.scale;
+            }
             if (F32OUT) {
-              *reinterpret_cast<float4 *>(static_cast<float *>(a.y) + gc) = make_float4(o0, o1, o2, o3);
+              *reinterpret_cast<float4 *>(static_cast<float *>(P.y) + gc) = make_float4(o0, o1, o2, o3);
             } else {
               __half2 o[2] = {__floats2half2_rn(o0, o1), __floats2half2_rn(o2, o3)};
-              *reinterpret_cast<uint2 *>(static_cast<__half *>(a.y) + gc) = *reinterpret_cast<uint2 *>(o);
+              *reinterpret_cast<uint2 *>(static_cast<__half *>(P.y) + gc) = *reinterpret_cast<uint2 *>(o);
             }
           }
         }
@@ -333,25 +323,55 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
   // prologue: x' = 2^-3.5 H (x . suh) for the 512-element chunks (32 tile
   // rows) this range touches; a warp transforms four 128-blocks at once,
   // eight lanes per block and 16 contiguous elements per lane
+  const int op0 = GROUPED ? (int)(t0 / a.op_rows) : 0;
+  if (GROUPED && a.pos_out && me == 0) {   // the combine's row of each unit
+    for (int u = tid; u < a.nops / a.nslots; u += NCT) {
+      const int e = a.ids[u];
+      a.pos_out[u] = (e >= 0 && e < a.E) ? u : -1;
+    }
+  }
   {
     const int KC = (a.k + 511) >> 9;
     int c0 = 0, nc = KC;
-    if (t1 - t0 < TK) {   // fewer rows than one block: at most two column blocks
+    if (GROUPED) {          // every chunk of each op the range touches (ops op0 ..)
+      nc = ((int)((t1 - 1) / a.op_rows) - op0 + 1) * KC;
+    } else if (t1 - t0 < TK) {   // fewer rows than one block: at most two column blocks
       c0 = (int)(t0 % TK) >> 5;
       const int c1 = (int)((t1 - 1) % TK) >> 5;
       const bool wrap = (t0 / TK) != ((t1 - 1) / TK);
       nc = !wrap ? c1 - c0 + 1 : (c1 >= c0 ? KC : KC - c0 + c1 + 1);
     }
     for (int i = warp; i < nc; i += NCW) {
-      const int e0 = ((c0 + i) % KC) * 512 + lane * 16;
+      const int jop = GROUPED ? i / KC : 0;               // op op0 + jop
+      const GemvOp P = gemv_op<GROUPED>(a, op0 + jop);
+      if (GROUPED && P.bad && lane == 0 && i % KC == 0) set_device_error(a.err, kErrExpertId);
+      const int e0 = ((c0 + i - jop * KC) % KC) * 512 + lane * 16;
       const bool live = e0 < a.k;   // k is a multiple of 128: whole 8-lane groups
+      __half *xso = xs + jop * a.k;
+      float *rso = rsum + jop * (a.k / 16);
       float v[16];
-      if (live) {
+      if (live && GROUPED && a.act_in) {
+        // h = SiLU(g) u of this unit (fp32, the gate and up outputs), times suh
+        const int u = (op0 + jop) / a.nslots;
+        const float *g = a.act_in + (long)(2 * u) * a.k + e0, *up = g + a.k;
+        uint4 sv[2];
+        sv[0] = *reinterpret_cast<const uint4 *>(P.suh + e0);
+        sv[1] = *reinterpret_cast<const uint4 *>(P.suh + e0 + 8);
+        const __half *sh = reinterpret_cast<const __half *>(sv);
+#pragma unroll
+        for (int j = 0; j < 16; j += 4) {
+          const float4 gg = *reinterpret_cast<const float4 *>(g + j), uu = *reinterpret_cast<const float4 *>(up + j);
+          v[j] = gg.x / (1.0f + expf(-gg.x)) * uu.x * __half2float(sh[j]);
+          v[j + 1] = gg.y / (1.0f + expf(-gg.y)) * uu.y * __half2float(sh[j + 1]);
+          v[j + 2] = gg.z / (1.0f + expf(-gg.z)) * uu.z * __half2float(sh[j + 2]);
+          v[j + 3] = gg.w / (1.0f + expf(-gg.w)) * uu.w * __half2float(sh[j + 3]);
+        }
+      } else if (live) {
         uint4 xv[2], sv[2];
-        xv[0] = *reinterpret_cast<const uint4 *>(a.x + e0);
-        xv[1] = *reinterpret_cast<const uint4 *>(a.x + e0 + 8);
-        sv[0] = *reinterpret_cast<const uint4 *>(a.suh + e0);
-        sv[1] = *reinterpret_cast<const uint4 *>(a.suh + e0 + 8);
+        xv[0] = *reinterpret_cast<const uint4 *>(P.x + e0);
+        xv[1] = *reinterpret_cast<const uint4 *>(P.x + e0 + 8);
+        sv[0] = *reinterpret_cast<const uint4 *>(P.suh + e0);
+        sv[1] = *reinterpret_cast<const uint4 *>(P.suh + e0 + 8);
         const __half2 *xh = reinterpret_cast<const __half2 *>(xv);
         const __half2 *sh = reinterpret_cast<const __half2 *>(sv);
 #pragma unroll
@@ -373,9 +393,9 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
           oh[j] = __floats2half2_rn(v[2 * j] * kRhtScale, v[2 * j + 1] * kRhtScale);
           rs += __low2float(oh[j]) + __high2float(oh[j]);
         }
-        *reinterpret_cast<uint4 *>(xs + e0) = o[0];
-        *reinterpret_cast<uint4 *>(xs + e0 + 8) = o[1];
-        rsum[e0 >> 4] = rs;
+        *reinterpret_cast<uint4 *>(xso + e0) = o[0];
+        *reinterpret_cast<uint4 *>(xso + e0 + 8) = o[1];
+        rso[e0 >> 4] = rs;
       }
     }
   }
@@ -392,6 +412,7 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
     const int c = (int)(t / TK);
     const long long seg_end = min(t1, (long long)(c + 1) * TK);
     const int tk_first = (int)(t - (long long)c * TK), nrows = (int)(seg_end - t);
+    const __half *xso = xs + (GROUPED ? c / a.colblocks - op0 : 0) * a.k;   // this op's x'
 
     float acc[16];
 #pragma unroll
@@ -422,7 +443,7 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
           const int tk = tk_first + r0 + j;
           unsigned short xr[S::G];
 #pragma unroll
-          for (int i = 0; i < S::G; ++i) xr[i] = __half_as_ushort(xs[tk * 16 + S::G * q + i]);
+          for (int i = 0; i < S::G; ++i) xr[i] = __half_as_ushort(xso[tk * 16 + S::G * q + i]);
           decode_accumulate<K, 0>(w, xr, acc);
         }
       }
@@ -483,12 +504,13 @@ static PFN_cuTensorMapEncodeTiled_v12000 gemv_tmap_fn() {
   return fn;
 }
 
-template <int K, bool F32>
+template <int K, bool F32, bool GROUPED = false>
 struct Launcher {
   using S = GemvShape<K>;
-  // ring stages that fit beside x' (2 bytes per k) and the reduction buffers
-  // x' (2 bytes per k) and its per-tile-row sums (4 bytes per 16 k)
-  static size_t xbytes(int k) { return 2 * (size_t)k + (size_t)k / 4; }
+  // ring stages that fit beside the reduction buffers, x' (2 bytes per k)
+  // and its per-tile-row sums (4 bytes per 16 k), for up to kGemvMaxOps ops
+  // in GROUPED mode
+  static size_t xbytes(int k) { return (GROUPED ? kGemvMaxOps : 1) * (2 * (size_t)k + (size_t)k / 4); }
   static int stages(int k) {
     const long avail = (long)kGemvSmemMax - S::FIXED_B - (long)xbytes(k);
     long st = avail / S::STAGE_B;
@@ -500,8 +522,8 @@ struct Launcher {
     const size_t sm = smem(a.k, a.stages);
     static size_t attr = 0;
     if (attr < sm) {
-      cudaError_t e = cudaFuncSetAttribute(gemv_m1_kernel<K, F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)sm);
+      cudaError_t e = cudaFuncSetAttribute(gemv_m1_kernel<K, F32, GROUPED>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
       if (e != cudaSuccess) return e;
       attr = sm;
     }
@@ -517,7 +539,7 @@ struct Launcher {
     // weights) while the preceding kernel on the stream finishes
     cfg.attrs = prefetch ? attrs : nullptr;
     cfg.numAttrs = prefetch ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, gemv_m1_kernel<K, F32>, tm, a);
+    return cudaLaunchKernelEx(&cfg, gemv_m1_kernel<K, F32, GROUPED>, tm, a);
   }
 };
 
@@ -597,6 +619,13 @@ cudaError_t exl3_launch_gemv_m1(const uint16_t *x, const uint16_t *trellis, cons
   a.tiles_k = k / 16;
   a.colblocks = (n + cc - 1) / cc;
   a.total = (long long)a.colblocks * a.tiles_k;
+  a.ids = nullptr;
+  a.weights = nullptr;
+  a.topk = a.nslots = a.nops = 1;
+  a.E = a.x_per_unit = 0;
+  a.op_rows = a.total;
+  a.act_in = nullptr;
+  a.pos_out = nullptr;
   a.stages = 0;
   EXL3_K_SWITCH(K, a.stages = Launcher<KK, false>::stages(k));
   if (a.stages < 2) return cudaErrorInvalidValue;
@@ -606,5 +635,89 @@ cudaError_t exl3_launch_gemv_m1(const uint16_t *x, const uint16_t *trellis, cons
   } else {
     EXL3_K_SWITCH(K, e = Launcher<KK, false>::launch(tm, a, grid, s, prefetch));
   }
+  return e;
+}
+
+// ---- routed experts for a few tokens: U * nslots M = 1 GEMVs in one launch
+
+// Grid, partial-sum floats and arrival counters for nops = U * nslots ops of
+// [k] x [k][n]; false when a CTA's range would touch more than kGemvMaxOps
+// ops or x' for them does not fit beside two ring stages.
+bool exl3_moe_gemv_plan(int U, int nslots, int k, int n, int K, int *grid, size_t *partial_floats, int *blocks) {
+  const int cc = exl3_gemv_cta_cols(K);
+  const long long colblocks = (n + cc - 1) / cc, op_rows = colblocks * (k / 16);
+  const long long total = (long long)U * nslots * op_rows;
+  long long g = gemv_sm_count();
+  if (g > total) g = total;
+  if (g < 1) return false;
+  const long long range = (total + g - 1) / g;
+  if ((range + op_rows - 1) / op_rows + 1 > kGemvMaxOps) return false;
+  int st = 0;
+  EXL3_K_SWITCH(K, st = Launcher<KK, true, true>::stages(k));
+  if (st < 2) return false;
+  *grid = (int)g;
+  *blocks = (int)(U * nslots * colblocks);
+  *partial_floats = (size_t)(*blocks + g) * (size_t)cc;
+  return true;
+}
+
+// Input: x [T][k] fp16, row u / topk for unit u (gate and up), or act_in
+// [U][2][k] fp32, SiLU(gate) up of unit u (down); trellis: all experts'
+// slots [E][nslots][k/16][n/16][16K];
+// suh [E][nslots][k], svh [E][nslots][n]; y: [U * nslots][n] fp32, times
+// weights[u] when weights is not NULL.
+cudaError_t exl3_launch_moe_gemv(const uint16_t *x, const float *act_in, int *pos_out, const int32_t *ids,
+                                 const float *weights, int U, int topk, int E, int nslots, int k, int n, int K,
+                                 const uint16_t *trellis, const uint16_t *suh, const uint16_t *svh, float *y,
+                                 float *partials, int *counters, int *err, cudaStream_t s) {
+  auto fn = gemv_tmap_fn();
+  if (!fn) return cudaErrorNotSupported;
+  int grid = 0, blocks = 0;
+  size_t pf = 0;
+  if (!exl3_moe_gemv_plan(U, nslots, k, n, K, &grid, &pf, &blocks)) return cudaErrorInvalidValue;
+  const int cc = exl3_gemv_cta_cols(K);
+  // all experts' trellis as u64 rows: row (e nslots + slot) k/16 + tk
+  CUtensorMap tm;
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)4 * K, (cuuint64_t)(n / 16), (cuuint64_t)E * nslots * (k / 16)};
+    cuuint64_t strides[2] = {(cuuint64_t)32 * K, (cuuint64_t)(n / 16) * 32 * K};
+    cuuint32_t box[3] = {(cuuint32_t)(4 * K), (cuuint32_t)(cc / 16), (cuuint32_t)kGemvBoxRows};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<uint16_t *>(trellis), dims, strides, box,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  GemvArgs a;
+  a.x = reinterpret_cast<const __half *>(x);
+  a.suh = reinterpret_cast<const __half *>(suh);
+  a.svh = reinterpret_cast<const __half *>(svh);
+  a.y = y;
+  a.partials = partials;
+  a.counters = counters;
+  a.err = err;
+  a.k = k;
+  a.n = n;
+  a.tiles_k = k / 16;
+  a.colblocks = (n + cc - 1) / cc;
+  a.ids = ids;
+  a.weights = weights;
+  a.topk = topk;
+  a.nslots = nslots;
+  a.E = E;
+  a.x_per_unit = 0;
+  a.act_in = act_in;
+  a.pos_out = pos_out;
+  a.nops = U * nslots;
+  a.op_rows = (long long)a.colblocks * a.tiles_k;
+  a.total = (long long)a.nops * a.op_rows;
+  a.stages = 0;
+  EXL3_K_SWITCH(K, a.stages = Launcher<KK, true, true>::stages(k));
+  cudaError_t e = cudaSuccess;
+  // The down projection (act_in set) is a programmatic dependent of the gate
+  // and up launch: it streams its experts' weights (the expert ids are final
+  // before that launch began) while gate and up finish, and reads their
+  // outputs after griddepcontrol.wait.
+  EXL3_K_SWITCH(K, e = Launcher<KK, true, true>::launch(tm, a, grid, s, act_in != nullptr));
   return e;
 }
