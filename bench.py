@@ -38,10 +38,11 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
 # dram bytes (read + write) per launch from an ncu capture of gemv_m1_kernel<4>
-# at k=5120 n=17408, with the hash of gemv.cu at capture time; a changed
-# kernel source makes the recorded traffic stale (reported as null).
-TRAFFIC = {"file": "trellis_quantized_gb300/csrc/gemv.cu", "sha1": "d7fe6e3afcd4e0b9e4180fb958c2d608d76aa517",
-           "bytes_per_launch": 65675264, "workload": "k5120 n25600 K4 M1"}
+# at k=5120 n=25600, with the hash of the kernel's sources at capture time; a
+# changed kernel source makes the recorded traffic stale (reported as null).
+TRAFFIC = {"files": ["trellis_quantized_gb300/csrc/gemv.cu", "trellis_quantized_gb300/csrc/gemv_core.cuh"],
+           "sha1": "81bb96e0921b7c9f3a069546bee8d74e856eed22", "bytes_per_launch": 65673472,
+           "workload": "k5120 n25600 K4 M1"}
 
 
 def peaks():
@@ -59,9 +60,12 @@ def linear_bytes(case) -> int:
     return case.trellis.nbytes + case.x.nbytes + case.suh.nbytes + case.svh.nbytes + case.M * case.n * 2
 
 
-def file_sha1(rel):
-    with open(os.path.join(ROOT, rel), "rb") as f:
-        return hashlib.sha1(f.read()).hexdigest()
+def files_sha1(rels):
+    h = hashlib.sha1()
+    for rel in rels:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 class ClockSampler:
@@ -226,7 +230,7 @@ def run_ours(args):
     kern_ms = k0.elapsed_time(k1) / (kreps * reps_k)
     achieved = big_bytes / (kern_ms * 1e-3) / 1e9
     traffic = None
-    if TRAFFIC["sha1"] and TRAFFIC["sha1"] == file_sha1(TRAFFIC["file"]):
+    if TRAFFIC["sha1"] and TRAFFIC["sha1"] == files_sha1(TRAFFIC["files"]):
         traffic = TRAFFIC["bytes_per_launch"]
     roofline = {"bound": "hbm", "kernel": "gemv_m1_kernel<K=4> (k=5120 n=25600)", "achieved": round(achieved, 1),
                 "peak": hbm, "peak_source": src, "unit": "GB/s", "frac": round(achieved / hbm, 4),
