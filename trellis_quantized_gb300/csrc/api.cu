@@ -22,7 +22,7 @@ cudaError_t exl3_launch_gemv_m1(const uint16_t *x, const uint16_t *trellis, cons
                                 float *partials, int *counters, int *err, int grid, cudaStream_t s,
                                 bool prefetch = false);
 void exl3_gemv_plan(int k, int n, int K, int *grid, size_t *partial_floats);
-bool exl3_gemv_fits(int k, int K);
+bool exl3_gemv_fits(int k, int n, int K);
 int exl3_launch_gemm_tc(const uint16_t *xh, const uint16_t *wt, int M, int n, int k, const uint16_t *svh,
                         void *y, bool f32out, const float *row_scale, float pre, int *err, cudaStream_t s,
                         bool q8 = false, int32_t *acc_out = nullptr);
@@ -152,7 +152,7 @@ LinearWs linear_ws(int M, int k, int n, int K) {
   LinearWs w;
   size_t off = kDataOff;
   w.counters = kCounterOff;
-  if (M == 1 && exl3_gemv_fits(k, K)) {
+  if (M == 1 && exl3_gemv_fits(k, n, K)) {
     size_t floats = 0;
     exl3_gemv_plan(k, n, K, &w.grid, &floats);
     w.partials = off;
@@ -379,7 +379,7 @@ int exl3_linear(const uint16_t *x, int M, int k, int n, const uint16_t *trellis,
   const bool f32 = out_dtype == EXL3_OUT_F32;
   int *err = at<int>(workspace, L.ctrl);
   // M = 1 runs the GEMV unless x' for this k does not fit beside its ring
-  if (M == 1 && exl3_gemv_fits(k, K)) {
+  if (M == 1 && exl3_gemv_fits(k, n, K)) {
     return exl3_cuda_check(exl3_launch_gemv_m1(x, trellis, suh, svh, k, n, K, y, f32, at<float>(workspace, L.partials),
                                                at<int>(workspace, L.counters), err, L.grid, stream,
                                                g_weight_prefetch.load() != 0),

@@ -60,7 +60,8 @@ struct GemvArgs {
   int *counters;            // [nops * colblocks]
   int *err;                 // device error word
   int k, n, tiles_k, colblocks, stages;
-  long long total;          // nops * colblocks * tiles_k
+  int pre_stages;           // stages the producer loads before x' is ready
+  uint32_t total;           // nops * colblocks * tiles_k (grid * total < 2^32)
   // Routed-expert mode (GROUPED): the rows of op o = unit u * nslots + slot
   // follow those of op o - 1; op o multiplies x row (x_per_unit ? u : u / topk)
   // by expert e = ids[u]'s slot `slot` (trellis rows (e nslots + slot) k/16 of
@@ -70,7 +71,7 @@ struct GemvArgs {
   const int32_t *ids;
   const float *weights;
   int topk, nslots, E, x_per_unit, nops;
-  long long op_rows;        // colblocks * tiles_k
+  uint32_t op_rows;         // colblocks * tiles_k
   // act_in set (down projection): unit u's input is SiLU(g) u of the gate and
   // up outputs act_in[u][0][k], act_in[u][1][k] (fp32) instead of x; pos_out
   // (if set) receives u, or -1 for an invalid expert id, for the combine
@@ -78,7 +79,9 @@ struct GemvArgs {
   int *pos_out;
 };
 
-constexpr int kGemvMaxOps = 4;   // ops one CTA's range may touch in GROUPED mode
+constexpr int kGemvMaxOps = 4;        // ops one CTA's range may touch in GROUPED mode
+constexpr int kGemvPrePartials = 2;   // partials a finisher loads before its segment ends
+constexpr int kGemvPreStages = 2;     // stages the producer loads before x' is ready
 
 // The pointers of op o (one op, the linear itself, when not GROUPED).
 struct GemvOp {
@@ -123,8 +126,9 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
   uint64_t *empty = full + STAGES;                                     // [STAGES]
   uint64_t *seg_full = empty + STAGES;                                 // red holds a finished segment
   uint64_t *red_free = seg_full + 1;                                   // the flusher has read red
+  uint64_t *xready = red_free + 1;                                     // the consumers' x' is ready
   constexpr int NOPS = GROUPED ? kGemvMaxOps : 1;
-  __half *xs = reinterpret_cast<__half *>(red_free + 1);               // [NOPS][k] fp16 x' (touched blocks)
+  __half *xs = reinterpret_cast<__half *>(xready + 2);                 // [NOPS][k] fp16 x' (touched blocks)
   float *rsum = reinterpret_cast<float *>(xs + NOPS * a.k);            // [NOPS][k/16] sum of x' per tile row
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -133,7 +137,10 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
   // the kernel launched after this one on the stream may start as soon as
   // every CTA has begun (it only streams weights until this grid completes)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const long long t0 = range_start(me, a.total, grid), t1 = range_start(me + 1, a.total, grid);
+  // Row arithmetic is 32-bit (the host keeps grid * total below 2^32): a
+  // 64-bit division is a long software sequence on every path's start.
+  const uint32_t TKU = (uint32_t)TK;
+  const uint32_t t0 = range_start(me, a.total, grid), t1 = range_start(me + 1, a.total, grid);
   if (t0 >= t1) return;
 
   if (tid == 0) {
@@ -143,6 +150,7 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
     }
     tc::mbar_init(seg_full, NCW);
     tc::mbar_init(red_free, 1);
+    tc::mbar_init(xready, 1);
     *s_abort = 0;
     tc::fence_mbar_init();
   }
@@ -152,17 +160,30 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
     // ---------------- producer: one thread loads the rows into the ring
     if (lane == 0) {
       tc::prefetch_tmap(&tmT);
-      int stage = 0;
+      int stage = 0, issued = 0;
       uint32_t phase = 0;
-      for (long long t = t0; t < t1 && !*s_abort;) {
-        const int c = (int)(t / TK);   // block: op c / colblocks, column block c % colblocks
-        const long long seg_end = min(t1, (long long)(c + 1) * TK);
-        const int tk_first = (int)(t - (long long)c * TK), nrows = (int)(seg_end - t);
-        const int op = GROUPED ? c / a.colblocks : 0;
-        const int tn0 = (c - op * a.colblocks) * (S::CTA_COLS / 16);
+      for (uint32_t t = t0; t < t1 && !*s_abort;) {
+        const uint32_t c = t / TKU;   // block: op c / colblocks, column block c % colblocks
+        const uint32_t seg_end = min(t1, (c + 1) * TKU);
+        const int tk_first = (int)(t - c * TKU), nrows = (int)(seg_end - t);
+        const int op = GROUPED ? (int)(c / (uint32_t)a.colblocks) : 0;
+        const int tn0 = ((int)c - op * a.colblocks) * (S::CTA_COLS / 16);
         const int trow = gemv_op<GROUPED>(a, op).trow + tk_first;
         for (int r0 = 0; r0 < nrows && !*s_abort; r0 += S::R) {
           const int cnt = min(S::R, nrows - r0);
+          if (issued++ == a.pre_stages) {
+            // The first stages are in flight.  Hold the rest until the
+            // consumers have made x': with every SM's whole ring queued the
+            // x loads (and the first stages) wait behind those copies.  The
+            // hardware wait covers the preceding kernel, so the bounded wait
+            // only spans the x' prologue.
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            if (!tc::mbar_wait(xready, 0)) {
+              set_device_error(a.err, kErrBounds);
+              *s_abort = 1;
+              break;
+            }
+          }
           if (!tc::mbar_wait(&empty[stage], phase ^ 1)) {
             set_device_error(a.err, kErrBounds);
             *s_abort = 1;
@@ -185,6 +206,17 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
     return;
   }
 
+  // Bring x and suh into L2 (one 128-byte line per thread) while the
+  // preceding kernel finishes.  L2 is the point of coherence, so a line that
+  // kernel writes later is still read current after the wait below.
+  if (!GROUPED && warp < NCW) {
+    const int lines = a.k >> 6;   // 64 fp16 per line
+    for (int i = tid; i < 2 * lines; i += NCT) {
+      const __half *p = i < lines ? a.x + (i << 6) : a.suh + ((i - lines) << 6);
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+    }
+  }
+
   // Under a programmatic dependent launch the producer above is already
   // streaming weights; everything below (x, the workspace, y) waits until
   // the preceding kernel on the stream has completed and its writes are
@@ -197,12 +229,62 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
     // 128 g + 4 l .. +3 of every 128-column group g.
     uint32_t sp = 0;
     const int op0 = GROUPED ? (int)(t0 / a.op_rows) : 0;
-    for (long long t = t0; t < t1;) {
-      const int c = (int)(t / TK);   // block: op c / colblocks, column block c % colblocks
-      const long long seg_end = min(t1, (long long)(c + 1) * TK);
+    for (uint32_t t = t0; t < t1;) {
+      const int c = (int)(t / TKU);   // block: op c / colblocks, column block c % colblocks
+      const uint32_t seg_end = min(t1, (uint32_t)(c + 1) * TKU);
       const int op = GROUPED ? c / a.colblocks : 0;
       const GemvOp P = gemv_op<GROUPED>(a, op);
       const float *rs = rsum + (op - op0) * (a.k / 16);
+      const int col0 = (c - op * a.colblocks) * S::CTA_COLS;
+      const uint32_t blk_first = (uint32_t)c * TKU, blk_last = min((uint32_t)(c + 1) * TKU, a.total) - 1;
+      const int i_first = range_owner(blk_first, a.total, grid), i_last = range_owner(blk_last, a.total, grid);
+      // A block shared by several CTAs is finished by its first CTA, whose
+      // range ends in it (for the others it is the first or only segment,
+      // so their partials are usually stored long before).  The others
+      // store a partial in their (block, CTA) slot and make one release
+      // increment; the finisher waits (bounded) for all of them with
+      // acquire loads and adds the partials in CTA order.  It does the wait
+      // and loads the first kGemvPrePartials partials while its own
+      // consumers still decode the segment, off the launch's critical path.
+      const bool shared = i_first != i_last, finisher = shared && me == i_first;
+      const int others = i_last - i_first;
+      float pre[kGemvPrePartials][S::NG][4];
+      if (finisher) {
+        if (lane == 0) {
+          const long long w0 = clock64();
+          int got = 0;
+          while (true) {
+            asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(got) : "l"(a.counters + c) : "memory");
+            if (got >= others) break;
+            if (clock64() - w0 > tc::kWaitLimit) {
+              set_device_error(a.err, kErrBounds);
+              break;
+            }
+            __nanosleep(64);
+          }
+          if (got > others) set_device_error(a.err, kErrDirtyCounter);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < kGemvPrePartials; ++j)
+#pragma unroll
+          for (int g = 0; g < S::NG; ++g) {
+            float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (j < others)
+              r = __ldcg(reinterpret_cast<const float4 *>(a.partials + (long)(c + i_first + 1 + j) * S::CTA_COLS +
+                                                          g * 128 + lane * 4));
+            pre[j][g][0] = r.x;
+            pre[j][g][1] = r.y;
+            pre[j][g][2] = r.z;
+            pre[j][g][3] = r.w;
+          }
+      }
+      uint2 svv[S::NG];   // the block's svh, loaded ahead as well
+#pragma unroll
+      for (int g = 0; g < S::NG; ++g)
+        svv[g] = (!shared || finisher) && col0 + g * 128 < a.n
+                     ? *reinterpret_cast<const uint2 *>(P.svh + col0 + g * 128 + lane * 4)
+                     : make_uint2(0u, 0u);
       if (!*s_abort && !tc::mbar_wait(seg_full, sp)) {
         if (lane == 0) set_device_error(a.err, kErrBounds);
         *s_abort = 1;
@@ -224,7 +306,7 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
       // every column's sum is sum x' (1024 + B): remove 1534 * (the segment's sum of x')
       float sg = 0.f;
       {
-        const int tk_first = (int)(t - (long long)c * TK), nrows = (int)(seg_end - t);
+        const int tk_first = (int)(t - (uint32_t)c * TKU), nrows = (int)(seg_end - t);
         for (int r = lane; r < nrows; r += 32) sg += rs[tk_first + r];
 #pragma unroll
         for (int m = 16; m >= 1; m >>= 1) sg += __shfl_xor_sync(0xffffffffu, sg, m);
@@ -234,19 +316,9 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e) v[g][e] = fmaf(-1534.0f, sg, v[g][e]) * kSigma;
 
-      const int col0 = (c - op * a.colblocks) * S::CTA_COLS;
-      const long long blk_first = (long long)c * TK, blk_last = min((long long)(c + 1) * TK, a.total) - 1;
-      const int i_first = range_owner(blk_first, a.total, grid), i_last = range_owner(blk_last, a.total, grid);
       bool finish = true;
-      if (i_first != i_last) {
-        // A shared block is finished by its first CTA, whose range ends in it
-        // (for the others it is the first or only segment, so their partials
-        // are usually stored long before).  The others store a partial in
-        // their (block, CTA) slot and make one release increment; the
-        // finisher waits (bounded) for all of them with acquire loads and
-        // adds the partials in CTA order.
-        const int others = i_last - i_first;
-        if (me != i_first) {
+      if (shared) {
+        if (!finisher) {
 #pragma unroll
           for (int g = 0; g < S::NG; ++g)
             *reinterpret_cast<float4 *>(a.partials + (long)(c + me) * S::CTA_COLS + g * 128 + lane * 4) =
@@ -256,22 +328,14 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
           if (lane == 0) asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(a.counters + c) : "memory");
           finish = false;
         } else {
-          if (lane == 0) {
-            const long long w0 = clock64();
-            int got = 0;
-            while (true) {
-              asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(got) : "l"(a.counters + c) : "memory");
-              if (got >= others) break;
-              if (clock64() - w0 > tc::kWaitLimit) {
-                set_device_error(a.err, kErrBounds);
-                break;
-              }
-              __nanosleep(64);
-            }
-            if (got > others) set_device_error(a.err, kErrDirtyCounter);
-          }
-          __syncwarp();
-          for (int i = i_first + 1; i <= i_last; ++i) {
+#pragma unroll
+          for (int j = 0; j < kGemvPrePartials; ++j)
+            if (j < others)
+#pragma unroll
+              for (int g = 0; g < S::NG; ++g)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) v[g][e] += pre[j][g][e];
+          for (int i = i_first + 1 + kGemvPrePartials; i <= i_last; ++i) {
 #pragma unroll
             for (int g = 0; g < S::NG; ++g) {
               const float4 r = __ldcg(reinterpret_cast<const float4 *>(a.partials + (long)(c + i) * S::CTA_COLS +
@@ -292,8 +356,7 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
           const int gc = col0 + g * 128 + lane * 4;
           if (col0 + g * 128 < a.n) {
             fwht128_warp(v[g], lane);
-            const uint2 sv = *reinterpret_cast<const uint2 *>(P.svh + gc);
-            const __half2 *sh = reinterpret_cast<const __half2 *>(&sv);
+            const __half2 *sh = reinterpret_cast<const __half2 *>(&svv[g]);
             float o0 = v[g][0] * kRhtScale * __low2float(sh[0]);
             float o1 = v[g][1] * kRhtScale * __high2float(sh[0]);
             float o2 = v[g][2] * kRhtScale * __low2float(sh[1]);
@@ -336,9 +399,9 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
     if (GROUPED) {          // every chunk of each op the range touches (ops op0 ..)
       nc = ((int)((t1 - 1) / a.op_rows) - op0 + 1) * KC;
     } else if (t1 - t0 < TK) {   // fewer rows than one block: at most two column blocks
-      c0 = (int)(t0 % TK) >> 5;
-      const int c1 = (int)((t1 - 1) % TK) >> 5;
-      const bool wrap = (t0 / TK) != ((t1 - 1) / TK);
+      c0 = (int)(t0 % TKU) >> 5;
+      const int c1 = (int)((t1 - 1) % TKU) >> 5;
+      const bool wrap = (t0 / TKU) != ((t1 - 1) / TKU);
       nc = !wrap ? c1 - c0 + 1 : (c1 >= c0 ? KC : KC - c0 + c1 + 1);
     }
     for (int i = warp; i < nc; i += NCW) {
@@ -400,6 +463,7 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
     }
   }
   consumer_sync(NCT);
+  if (tid == 0) tc::mbar_arrive(xready);
 
   const int wk = warp;
   const int tile_in_warp = lane / S::LPT, q = lane % S::LPT;
@@ -407,11 +471,16 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
   const int next_off = tile_in_warp * 32 * K + ((q + 1) % S::LPT) * 16 * S::CPL;  // next row group (wraps)
   int stage = 0;
   uint32_t phase = 0, sp = 0;
+  // Row g of the range (counted across its segments) belongs to warp
+  // g mod NCW, so the partial stages at segment ends do not always give
+  // their rows to the same warps: every warp has the same number of rows,
+  // to within one, and the assignment stays fixed.
+  uint32_t gbase = 0;
 
-  for (long long t = t0; t < t1;) {
-    const int c = (int)(t / TK);
-    const long long seg_end = min(t1, (long long)(c + 1) * TK);
-    const int tk_first = (int)(t - (long long)c * TK), nrows = (int)(seg_end - t);
+  for (uint32_t t = t0; t < t1;) {
+    const int c = (int)(t / TKU);
+    const uint32_t seg_end = min(t1, (uint32_t)(c + 1) * TKU);
+    const int tk_first = (int)(t - (uint32_t)c * TKU), nrows = (int)(seg_end - t);
     const __half *xso = xs + (GROUPED ? c / a.colblocks - op0 : 0) * a.k;   // this op's x'
 
     float acc[16];
@@ -425,9 +494,11 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
         *s_abort = 1;
       }
       const uint8_t *sbase = ring + (size_t)stage * S::STAGE_B;
+      const int j0 = (wk - (int)(gbase % NCW) + NCW) % NCW;
+      gbase += cnt;
 #pragma unroll
       for (int jj = 0; jj < S::RPW; ++jj) {
-        const int j = wk + jj * NCW;
+        const int j = j0 + jj * NCW;
         if (j < cnt) {
           uint32_t w[S::NW + 1];
           const uint8_t *rowp = sbase + (size_t)j * S::ROWB;
@@ -568,10 +639,12 @@ int exl3_gemv_cta_cols(int K) {
 
 // Whether the GEMV holds x' for this k beside two ring stages (otherwise
 // the caller takes the tensor-core path).
-bool exl3_gemv_fits(int k, int K) {
+bool exl3_gemv_fits(int k, int n, int K) {
   int st = 0;
   EXL3_K_SWITCH(K, st = Launcher<KK, false>::stages(k));
-  return st >= 2;
+  const int cc = exl3_gemv_cta_cols(K);
+  const unsigned long long total = (unsigned long long)((n + cc - 1) / cc) * (unsigned long long)(k / 16);
+  return st >= 2 && total * (unsigned long long)gemv_sm_count() < (1ull << 32);
 }
 
 // Grid size (one CTA per SM, at most one per row) and the partial-sum slots
@@ -618,7 +691,9 @@ cudaError_t exl3_launch_gemv_m1(const uint16_t *x, const uint16_t *trellis, cons
   a.n = n;
   a.tiles_k = k / 16;
   a.colblocks = (n + cc - 1) / cc;
-  a.total = (long long)a.colblocks * a.tiles_k;
+  if ((unsigned long long)a.colblocks * a.tiles_k * (unsigned long long)grid >= (1ull << 32))
+    return cudaErrorInvalidValue;
+  a.total = (uint32_t)a.colblocks * (uint32_t)a.tiles_k;
   a.ids = nullptr;
   a.weights = nullptr;
   a.topk = a.nslots = a.nops = 1;
@@ -626,6 +701,7 @@ cudaError_t exl3_launch_gemv_m1(const uint16_t *x, const uint16_t *trellis, cons
   a.op_rows = a.total;
   a.act_in = nullptr;
   a.pos_out = nullptr;
+  a.pre_stages = kGemvPreStages;
   a.stages = 0;
   EXL3_K_SWITCH(K, a.stages = Launcher<KK, false>::stages(k));
   if (a.stages < 2) return cudaErrorInvalidValue;
@@ -650,6 +726,7 @@ bool exl3_moe_gemv_plan(int U, int nslots, int k, int n, int K, int *grid, size_
   long long g = gemv_sm_count();
   if (g > total) g = total;
   if (g < 1) return false;
+  if ((unsigned long long)total * (unsigned long long)g >= (1ull << 32)) return false;
   const long long range = (total + g - 1) / g;
   if ((range + op_rows - 1) / op_rows + 1 > kGemvMaxOps) return false;
   int st = 0;
@@ -708,9 +785,12 @@ cudaError_t exl3_launch_moe_gemv(const uint16_t *x, const float *act_in, int *po
   a.x_per_unit = 0;
   a.act_in = act_in;
   a.pos_out = pos_out;
+  a.pre_stages = kGemvPreStages;
   a.nops = U * nslots;
-  a.op_rows = (long long)a.colblocks * a.tiles_k;
-  a.total = (long long)a.nops * a.op_rows;
+  if ((unsigned long long)a.colblocks * a.tiles_k * a.nops * (unsigned long long)grid >= (1ull << 32))
+    return cudaErrorInvalidValue;
+  a.op_rows = (uint32_t)a.colblocks * (uint32_t)a.tiles_k;
+  a.total = (uint32_t)a.nops * a.op_rows;
   a.stages = 0;
   EXL3_K_SWITCH(K, a.stages = Launcher<KK, true, true>::stages(k));
   cudaError_t e = cudaSuccess;

@@ -67,13 +67,14 @@ __device__ __forceinline__ void decode_accumulate(const uint32_t (&w)[GemvShape<
   }
 }
 
-__device__ __forceinline__ long long range_start(int i, long long total, int grid) {
-  return (long long)i * total / grid;
+// Start of CTA i's rows (grid * total < 2^32).
+__device__ __forceinline__ uint32_t range_start(int i, uint32_t total, int grid) {
+  return (uint32_t)i * total / (uint32_t)grid;
 }
 
 // Index of the CTA whose range holds row r.
-__device__ __forceinline__ int range_owner(long long r, long long total, int grid) {
-  int i = (int)((r * grid) / total);
+__device__ __forceinline__ int range_owner(uint32_t r, uint32_t total, int grid) {
+  int i = (int)((r * (uint32_t)grid) / total);
   while (i + 1 < grid && range_start(i + 1, total, grid) <= r) ++i;
   while (i > 0 && range_start(i, total, grid) > r) --i;
   return i;

@@ -29,7 +29,7 @@ cudaError_t exl3_launch_gemv_m1(const uint16_t *x, const uint16_t *trellis, cons
                                 bool prefetch = false);
 int exl3_gemv_cta_cols(int K);
 void exl3_gemv_plan(int k, int n, int K, int *grid, size_t *partial_floats);
-bool exl3_gemv_fits(int k, int K);
+bool exl3_gemv_fits(int k, int n, int K);
 
 namespace {
 
@@ -82,8 +82,8 @@ extern "C" int exl3_linear_gemv_noalloc(const uint16_t *x, int k, int n, const u
   if (out_dtype != EXL3_OUT_F16 && out_dtype != EXL3_OUT_F32)
     return exl3_fail(EXL3_ERR_ARG, "out_dtype %d invalid", out_dtype);
 
-  if (k > 49152 || !exl3_gemv_fits(k, K))
-    return exl3_fail(EXL3_ERR_SHAPE, "k = %d too large for the M = 1 GEMV at K = %d", k, K);
+  if (k > 49152 || !exl3_gemv_fits(k, n, K))
+    return exl3_fail(EXL3_ERR_SHAPE, "k = %d, n = %d too large for the M = 1 GEMV at K = %d", k, n, K);
   void *scratch = nullptr;
   int rc = scratch_for_current_device(&scratch);
   if (rc) return rc;
