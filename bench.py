@@ -389,6 +389,22 @@ def bench_extras(only=None, moe_tokens=None):
         ms = _timed(lambda: tq.exl3_linear(x, t, suh, svh, 4, y=y, workspace_buf=ws))
         small[f"M{M}"] = {"ms": round(ms, 4), "GBs": round(linear_bytes(c) / (ms * 1e-3) / 1e9, 1),
                           "tflops": round(2.0 * M * c.k * c.n / (ms * 1e-3) / 1e12, 2)}
+    # the row-invariant mode (every M through the 32-token-wide fused
+    # kernel, 32 rows at a time): its cost against the default paths
+    inv = {}
+    if only in (None, "small"):
+        prev = tq.exl3_set_row_invariant(True)
+        try:
+            for i, M in enumerate((1, 16, 4096)):
+                c = synth.linear_case(2, 90 + i, M, 5120, 17408, 4)
+                x, t, suh, svh = dev(c.x), dev(c.trellis), dev(c.suh), dev(c.svh)
+                ws = tq.workspace(tq.exl3_linear_workspace_size(M, c.k, c.n, c.K))
+                y = torch.empty((M, c.n), dtype=torch.float16, device="cuda")
+                ms = _timed(lambda: tq.exl3_linear(x, t, suh, svh, 4, y=y, workspace_buf=ws), reps=3 if M > 128 else 10)
+                inv[f"M{M}"] = {"ms": round(ms, 4), "tflops": round(2.0 * M * c.k * c.n / (ms * 1e-3) / 1e12, 2)}
+                del x, ws, y
+        finally:
+            tq.exl3_set_row_invariant(prev)
     moe = {}
     for T in ((moe_tokens or synth.CONFIG5_T) if only in (None, "moe") else ()):
         c = synth.config5(T)
@@ -407,7 +423,7 @@ def bench_extras(only=None, moe_tokens=None):
                         "unique_weight_GBs": round(used * per_expert / (ms * 1e-3) / 1e9, 1),
                         "tflops": round(flops / (ms * 1e-3) / 1e12, 2)}
         del d
-    return {"small_m_k5120_n17408": small, "moe_E256_top8_h2048_i512_K3": moe,
+    return {"small_m_k5120_n17408": small, "row_invariant_k5120_n17408": inv, "moe_E256_top8_h2048_i512_K3": moe,
             "note": "small M: trellis decoded into tcgen05 operands (one fused kernel after the input RHT); "
                     "MoE: device remap + gather/RHT + two grouped tcgen05 kernels decoding the experts' trellis "
                     "on the fly + fixed-order combine"}

@@ -146,6 +146,27 @@ int exl3_linear(const uint16_t *x, int M, int k, int n,
 int exl3_set_weight_prefetch(int enable);
 
 /*
+ * exl3_set_row_invariant -- make every row of an exl3_linear result
+ * independent of the other rows in the call: y[m] has the same bits for any
+ * M and any neighbouring rows ("EXL3 checkpoints on the native engine
+ * (tracker) #832", opening paragraph: a row-invariant linear; "The gate":
+ * rows keep one arithmetic at every row count).
+ *   enable = 0 (the default) or 1; returns the previous setting.  Applies to
+ *   calls made after it, from any host thread.
+ *   When on, exl3_linear runs the input transform for all M rows and then the
+ *   small-M tensor-core kernel with a 32-token MMA width over chunks of 32
+ *   rows, for every M, so the k splits and the per-token reduction order
+ *   depend on k and n only.  Up to 32 rows cost what the small-M path costs
+ *   (M = 1 a little more than the GEMV); larger M costs one small-M call per
+ *   32 rows, far more than the reconstruct + GEMM path at prefill sizes.
+ *   exl3_linear_workspace_size covers both modes.
+ *   exl3_linear_int8 is row-invariant in either mode (per-row activation
+ *   scales and exact integer accumulation); exl3_linear_gemv_noalloc is not
+ *   affected by this setting.
+ */
+int exl3_set_row_invariant(int enable);
+
+/*
  * exl3_linear_int8 -- the int8 prefill variant ("exl3xpu" README, "Prefill:
  * int8 linears and oneDNN fused attention").
  *   a_r  = max_j |x'_rj| / 127 (fp32), x' the fp32 input transform above;

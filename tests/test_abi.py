@@ -93,3 +93,18 @@ def test_workspace_sizes(M, k, n, K):
     assert size >= 256 and size % 256 == 0
     assert tq.exl3_linear_workspace_size(M, k + 1, n, K) == 0
     assert tq.exl3_linear_workspace_size(M, k, n, 0) == 0
+
+
+def test_host_settings_round_trip():
+    """The row-invariant and weight-prefetch switches return the previous
+    setting, and the workspace size does not depend on the row-invariant one
+    (it covers both layouts)."""
+    sizes = {}
+    for inv in (False, True):
+        prev = tq.exl3_set_row_invariant(inv)
+        assert tq.exl3_set_row_invariant(inv) == inv
+        sizes[inv] = [tq.exl3_linear_workspace_size(M, 5120, 512, 4) for M in (1, 16, 300)]
+        tq.exl3_set_row_invariant(prev)
+    assert sizes[False] == sizes[True]
+    prev = tq.exl3_set_weight_prefetch(True)
+    assert tq.exl3_set_weight_prefetch(prev) is True

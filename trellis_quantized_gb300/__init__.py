@@ -83,6 +83,8 @@ def lib():
         L.exl3_linear_gemv_noalloc.argtypes = [P, I, I, P, P, P, I, I, P, I, P]
         L.exl3_set_weight_prefetch.argtypes = [I]
         L.exl3_set_weight_prefetch.restype = I
+        L.exl3_set_row_invariant.argtypes = [I]
+        L.exl3_set_row_invariant.restype = I
         _lib = L
         return L
 
@@ -191,6 +193,12 @@ def exl3_linear(x, trellis, suh, svh, K: int, codebook: int = EXL3_CB_MUL1, out_
                              _ptr(svh, "svh", 2), K, codebook, _ptr(y, "y"), out_dtype, _ptr(ws, "workspace"),
                              ws.numel() * ws.element_size(), _stream(stream)))
     return y
+
+
+def exl3_set_row_invariant(enable: bool) -> bool:
+    """Make each row of an exl3_linear result independent of the row count and
+    of the other rows (same bits at every M); returns the previous setting."""
+    return bool(lib().exl3_set_row_invariant(1 if enable else 0))
 
 
 def exl3_set_weight_prefetch(enable: bool) -> bool:

@@ -33,7 +33,7 @@ cudaError_t exl3_launch_reconstruct_q8_t(const uint16_t *trellis, int k, int n, 
 int exl3_fused_tc_splits(int k, int n);
 int exl3_launch_fused_tc(const uint16_t *xh, const float *xsum, const uint16_t *trellis, const uint16_t *svh, int M,
                          int k, int n, int K, void *y, bool f32out, float *partials, int *counters, int *err,
-                         int splits, cudaStream_t s);
+                         int splits, cudaStream_t s, int npad_fixed);
 
 cudaError_t exl3_launch_moe_remap(const int32_t *ids, int U, int E, int *counts, int *offsets, int *perm, int *pos,
                                   int *mtiles, int *n_mtiles, int max_mtiles, int *chunk_tab, int *err,
@@ -62,6 +62,7 @@ int exl3_launch_moe_fused_down(const uint16_t *hin, int U, int hidden, int inter
 
 static thread_local std::string g_last_error;
 static std::atomic<int> g_weight_prefetch{0};
+static std::atomic<int> g_row_invariant{0};
 
 int exl3_fail(int code, const char *fmt, ...) {
   char buf[512];
@@ -95,6 +96,7 @@ constexpr size_t kMaxCounters = 8192;
 constexpr size_t kCounterOff = kCtrlBytes;
 constexpr size_t kDataOff = kCounterOff + kMaxCounters * sizeof(int);
 constexpr int kFusedMaxM = 128;      // 2 <= M <= this: fused decode + tcgen05; above: reconstruct + tcgen05
+constexpr int kRowInvChunk = 32;     // row-invariant mode: MMA width and rows per fused launch
 constexpr int kMaxGemvK = 49152;     // the M = 1 GEMV keeps x' for all of k in shared memory
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
@@ -148,11 +150,22 @@ struct LinearWs {
   int grid = 1, splits = 1;
 };
 
-LinearWs linear_ws(int M, int k, int n, int K) {
+// row_invariant: every M takes the 128-token-wide fused kernel, 128 rows at
+// a time (x' and its sums for all M rows, partials for one chunk).
+LinearWs linear_ws(int M, int k, int n, int K, bool row_invariant) {
   LinearWs w;
   size_t off = kDataOff;
   w.counters = kCounterOff;
-  if (M == 1 && exl3_gemv_fits(k, n, K)) {
+  if (row_invariant) {
+    const int Mc = M < kRowInvChunk ? M : kRowInvChunk;
+    w.xh = off;
+    off = align_up(off + sizeof(uint16_t) * (size_t)M * k);
+    w.xsum = off;
+    off = align_up(off + sizeof(float) * (size_t)M * ((k + 255) / 256));
+    w.splits = exl3_fused_tc_splits(k, n);
+    w.partials = off;
+    off = align_up(off + (w.splits > 1 ? sizeof(float) * (size_t)w.splits * Mc * n : 0));
+  } else if (M == 1 && exl3_gemv_fits(k, n, K)) {
     size_t floats = 0;
     exl3_gemv_plan(k, n, K, &w.grid, &floats);
     w.partials = off;
@@ -304,6 +317,8 @@ int exl3_version(void) { return 100; }
 
 int exl3_set_weight_prefetch(int enable) { return g_weight_prefetch.exchange(enable ? 1 : 0); }
 
+int exl3_set_row_invariant(int enable) { return g_row_invariant.exchange(enable ? 1 : 0); }
+
 int exl3_workspace_clear(void *workspace, size_t ws_bytes, exl3_stream_t stream) {
   g_last_error.clear();
   if (!workspace || ws_bytes == 0) return EXL3_OK;
@@ -358,7 +373,10 @@ int exl3_input_rht(const uint16_t *x, int M, int k, const uint16_t *suh, void *o
 size_t exl3_linear_workspace_size(int M, int k, int n, int K) {
   if (M < 1 || k <= 0 || n <= 0 || k % 128 || n % 128 || K < 1 || K > 8) return 0;
   if ((size_t)(n / 128) > kMaxCounters || (M == 1 && k > kMaxGemvK)) return 0;
-  return linear_ws(M, k, n, K).total;
+  // large enough in either mode, so the mode may change between the query
+  // and the call
+  const size_t a = linear_ws(M, k, n, K, false).total, b = linear_ws(M, k, n, K, true).total;
+  return a > b ? a : b;
 }
 
 int exl3_linear(const uint16_t *x, int M, int k, int n, const uint16_t *trellis, const uint16_t *suh,
@@ -374,10 +392,30 @@ int exl3_linear(const uint16_t *x, int M, int k, int n, const uint16_t *trellis,
   EXL3_TRY(check_linear_shape(M, k, n));
   if (out_dtype != EXL3_OUT_F16 && out_dtype != EXL3_OUT_F32)
     return exl3_fail(EXL3_ERR_ARG, "out_dtype %d invalid", out_dtype);
-  const LinearWs L = linear_ws(M, k, n, K);
+  const bool inv = g_row_invariant.load() != 0;
+  const LinearWs L = linear_ws(M, k, n, K, inv);
   EXL3_TRY(check_workspace(workspace, ws_bytes, L.total));
   const bool f32 = out_dtype == EXL3_OUT_F32;
   int *err = at<int>(workspace, L.ctrl);
+  if (inv) {
+    // Row-invariant mode: x' for every row, then the fused kernel at one
+    // fixed MMA width over chunks of that many rows.  A row's x' depends on that row only,
+    // the MMA width and the k splits (a function of k and n) are the same
+    // for every chunk, and rows past the chunk's end read as zero, so y[m]
+    // has the same bits whatever M is.
+    uint16_t *xh = at<uint16_t>(workspace, L.xh);
+    float *xsum = at<float>(workspace, L.xsum);
+    const int xunits = (k + 255) / 256;
+    EXL3_TRY(exl3_cuda_check(exl3_launch_input_rht(x, M, k, suh, xh, false, stream, xsum), "input_rht launch"));
+    for (int m0 = 0; m0 < M; m0 += kRowInvChunk) {
+      const int Mc = M - m0 < kRowInvChunk ? M - m0 : kRowInvChunk;
+      void *yc = static_cast<uint8_t *>(y) + (size_t)m0 * n * (f32 ? 4 : 2);
+      EXL3_TRY(exl3_launch_fused_tc(xh + (size_t)m0 * k, xsum + (size_t)m0 * xunits, trellis, svh, Mc, k, n, K, yc,
+                                    f32, at<float>(workspace, L.partials), at<int>(workspace, L.counters), err,
+                                    L.splits, stream, kRowInvChunk));
+    }
+    return EXL3_OK;
+  }
   // M = 1 runs the GEMV unless x' for this k does not fit beside its ring
   if (M == 1 && exl3_gemv_fits(k, n, K)) {
     return exl3_cuda_check(exl3_launch_gemv_m1(x, trellis, suh, svh, k, n, K, y, f32, at<float>(workspace, L.partials),
@@ -390,7 +428,7 @@ int exl3_linear(const uint16_t *x, int M, int k, int n, const uint16_t *trellis,
     float *xsum = at<float>(workspace, L.xsum);
     EXL3_TRY(exl3_cuda_check(exl3_launch_input_rht(x, M, k, suh, xh, false, stream, xsum), "input_rht launch"));
     return exl3_launch_fused_tc(xh, xsum, trellis, svh, M, k, n, K, y, f32, at<float>(workspace, L.partials),
-                                at<int>(workspace, L.counters), err, L.splits, stream);
+                                at<int>(workspace, L.counters), err, L.splits, stream, 0);
   }
   EXL3_TRY(exl3_cuda_check(exl3_launch_input_rht(x, M, k, suh, xh, false, stream), "input_rht launch"));
   uint16_t *wt = at<uint16_t>(workspace, L.wt);

@@ -65,6 +65,7 @@ struct Args {
   int *counters;       // [n / 128]
   int *err;
   int M, k, n, tiles_n, kb_per_split, splits, xunits;
+  int npad;            // MMA N: tokens rounded up to 16, or 128 for every M (row-invariant mode)
 };
 
 template <int K, bool F32OUT, int NMAX>
@@ -108,7 +109,7 @@ __global__ void __launch_bounds__(Roles<NMAX>::WARPS * 32, 1) fused_tc_kernel(co
   constexpr int NPS = WS / 2;
   const int npairs = nkb / 2;
   const int tn0 = nt * (BN / 16);
-  const int npad = (a.M + 15) & ~15;                    // MMA N: tokens rounded up to 16
+  const int npad = a.npad;                              // MMA N (x' rows past M read as zero)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < TS; ++s) {
@@ -418,14 +419,19 @@ int exl3_fused_tc_splits(int k, int n) {
 }
 
 // xh: x' fp16 [M][k] (M <= 128); partials: [splits][M][n] fp32 (unused when splits == 1).
+// npad_fixed (32 or 128, at least M): the MMA is that many tokens wide
+// whatever M is, so that a token's result does not depend on how many tokens
+// share the call; 0: M rounded up to 16.
 int exl3_launch_fused_tc(const uint16_t *xh, const float *xsum, const uint16_t *trellis, const uint16_t *svh, int M,
                          int k, int n, int K, void *y, bool f32out, float *partials, int *counters, int *err,
-                         int splits, cudaStream_t s) {
+                         int splits, cudaStream_t s, int npad_fixed) {
   auto fn = ftc_tmap_fn();
   if (!fn) return exl3_fail(EXL3_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   // x' [M][k] as (64 k, M rows, k/64 blocks): one load brings XSTEPS k blocks
   // of every token, each block a 128-byte-swizzled K-major operand.
-  const int npad = (M + 15) & ~15;
+  const int npad = npad_fixed ? npad_fixed : (M + 15) & ~15;
+  if (npad < M || (npad_fixed && npad_fixed != 32 && npad_fixed != 128))
+    return exl3_fail(EXL3_ERR_ARG, "MMA width %d for M = %d", npad, M);
   const int xsteps = npad <= 32 ? ftc::Shape<1, 32>::XSTEPS : ftc::Shape<1, 128>::XSTEPS;
   CUtensorMap ta, tt;
   {
@@ -451,7 +457,7 @@ int exl3_launch_fused_tc(const uint16_t *xh, const float *xsum, const uint16_t *
     if (r != CUDA_SUCCESS) return exl3_fail(EXL3_ERR_CUDA, "cuTensorMapEncodeTiled (trellis) failed (%d)", (int)r);
   }
   ftc::Args a{trellis, xsum, reinterpret_cast<const __half *>(svh), y, partials, counters, err, M, k, n, n / 16,
-              0, splits, (k + 255) / 256};
+              0, splits, (k + 255) / 256, npad};
   dim3 grid(n / 128, splits);
   cudaError_t e = cudaSuccess;
 #define EXL3_FTC(KK, F32, NM)                                                                                \
