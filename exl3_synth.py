@@ -14,6 +14,8 @@ Recipe (all numpy PCG64, seed = 20260000 + 100 * config + sub_case):
 * suh / svh: +1 or -1 with equal probability, stored as IEEE binary16.
 * x: N(0, 1) drawn in float64 and rounded to binary16, with the outlier rule
   of the workload (rows scaled x20 or channels scaled x30).
+* bias (linears with an output bias): N(0, 4^2) rounded to binary16, from
+  its own seed stream (config 6).
 * MoE routing: logits N(0, 1) [T, E]; the top-k logits by value (ties toward
   the lower expert id) and the softmax of those k logits as routing weights.
 """
@@ -67,6 +69,19 @@ def activations(rng: np.random.Generator, M: int, k: int, *, outlier_rows: float
         cols = rng.permutation(k)[:cnt]
         x[:, cols] *= channel_scale
     return x.astype(np.float16)
+
+
+def bias(rng: np.random.Generator, n: int, scale: float = 4.0) -> np.ndarray:
+    """Output bias, N(0, scale^2) in float64 rounded to float16 [n]."""
+    return (rng.standard_normal(n) * scale).astype(np.float16)
+
+
+BIAS_CONFIG = 6   # seed stream of the bias vectors (kept apart from the five workloads)
+
+
+def bias_for(sub: int, n: int) -> np.ndarray:
+    """The bias vector of sub-case ``sub`` (seed 20260000 + 600 + sub)."""
+    return bias(rng_for(BIAS_CONFIG, sub), n)
 
 
 def routing(rng: np.random.Generator, T: int, E: int, topk: int):

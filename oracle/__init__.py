@@ -72,6 +72,7 @@ def _load():
         lib.or_rht_out_f64.argtypes = [P, P, I, I]
         lib.or_linear.argtypes = [P, I, I, I, P, P, P, I, P]
         lib.or_linear_w.argtypes = [P, I, I, I, P, P, P, P]
+        lib.or_add_bias.argtypes = [P, P, I, I]
         lib.or_quant_act.argtypes = [P, P, I, I, P, P]
         lib.or_quant_weight.argtypes = [ctypes.c_uint16]
         lib.or_quant_weight.restype = ctypes.c_int
@@ -191,8 +192,18 @@ def rht_out_f64(yp, svh) -> np.ndarray:
     return y
 
 
-def linear(x, trellis, suh, svh, K: int) -> np.ndarray:
-    """y [M, n] float64 = RHT_out(RHT_in(x . suh) @ W) . svh."""
+def add_bias(y, bias) -> np.ndarray:
+    """y + bias (fp16 [n], one value per output feature) in float64, in place."""
+    M, n = y.shape
+    b = _u16(bias)
+    if b.shape != (n,):
+        raise ValueError(f"bias must have shape ({n},), got {b.shape}")
+    _check(_load().or_add_bias(_ptr(y), _ptr(b), M, n), "add_bias")
+    return y
+
+
+def linear(x, trellis, suh, svh, K: int, bias=None) -> np.ndarray:
+    """y [M, n] float64 = RHT_out(RHT_in(x . suh) @ W) . svh (+ bias)."""
     x = _u16(x)
     M, k = x.shape
     t = _u16(trellis)
@@ -200,11 +211,11 @@ def linear(x, trellis, suh, svh, K: int) -> np.ndarray:
     y = np.zeros((M, n), dtype=np.float64)
     _check(_load().or_linear(_ptr(x), M, k, n, _ptr(t), _ptr(_u16(suh)), _ptr(_u16(svh)), K,
                              _ptr(y)), "linear")
-    return y
+    return y if bias is None else add_bias(y, bias)
 
 
-def linear_w(x, W, suh, svh) -> np.ndarray:
-    """Linear from dequantised fp16 weights W [k, n]."""
+def linear_w(x, W, suh, svh, bias=None) -> np.ndarray:
+    """Linear from dequantised fp16 weights W [k, n] (+ bias)."""
     x = _u16(x)
     M, k = x.shape
     Wb = _u16(W)
@@ -212,7 +223,7 @@ def linear_w(x, W, suh, svh) -> np.ndarray:
     y = np.zeros((M, n), dtype=np.float64)
     _check(_load().or_linear_w(_ptr(x), M, k, n, _ptr(Wb), _ptr(_u16(suh)), _ptr(_u16(svh)),
                                _ptr(y)), "linear_w")
-    return y
+    return y if bias is None else add_bias(y, bias)
 
 
 def quant_act(x, suh):
@@ -246,8 +257,8 @@ def int8_acc(qx, qw) -> np.ndarray:
     return acc
 
 
-def linear_int8(x, trellis, suh, svh, K: int):
-    """Returns dict(qx, row_scale, qw, acc (int64), y (float64))."""
+def linear_int8(x, trellis, suh, svh, K: int, bias=None):
+    """Returns dict(qx, row_scale, qw, acc (int64), y (float64, + bias if given))."""
     x = _u16(x)
     M, k = x.shape
     t = _u16(trellis)
@@ -259,6 +270,8 @@ def linear_int8(x, trellis, suh, svh, K: int):
     y = np.zeros((M, n), dtype=np.float64)
     _check(_load().or_linear_int8(_ptr(x), M, k, n, _ptr(t), _ptr(_u16(suh)), _ptr(_u16(svh)), K,
                                   _ptr(qx), _ptr(a), _ptr(qw), _ptr(acc), _ptr(y)), "linear_int8")
+    if bias is not None:
+        add_bias(y, bias)
     return dict(qx=qx, row_scale=a, qw=qw, acc=acc, y=y)
 
 

@@ -305,6 +305,20 @@ int or_linear(const uint16_t *x, int M, int k, int n, const uint16_t *trellis,
   return rc;
 }
 
+/*
+ * Output bias ([TF-832], "What is left": a checkpoint's EXL3 group holds a
+ * bias beside trellis, suh and svh).  The pages do not place it; this file
+ * reads it as the bias of the original linear, one fp16 value per output
+ * feature added after the output transform and svh:
+ *   y[r][j] += bias[j]   (float64, in place on y [M][n]).
+ */
+int or_add_bias(double *y, const uint16_t *bias, int M, int n) {
+  if (M < 0 || n <= 0) return OR_ERR_SHAPE;
+  for (long r = 0; r < M; ++r)
+    for (int j = 0; j < n; ++j) y[r * n + j] += or_f16_to_f64(bias[j]);
+  return OR_OK;
+}
+
 /* ------------------------------------------------------------------------- */
 /* int8 variant ([README-int8]; rounding details are this library's reading)   */
 /* ------------------------------------------------------------------------- */

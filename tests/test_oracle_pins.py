@@ -209,6 +209,27 @@ def test_transform_form_bruteforce(K, k, n):
     assert np.max(np.abs(got - ref)) <= 1e-10 * max(1.0, np.max(np.abs(ref)))
 
 
+@pytest.mark.parametrize("K,k,n", [(2, 128, 256), (4, 256, 128), (7, 256, 256)])
+def test_bias_is_the_offset_of_the_affine_map(K, k, n):
+    """With a bias, y == x @ W_eff + b (the textbook affine map, explicit scipy
+    matrices): the bias is added per output feature after svh, outside the
+    Hadamard domain.  Adding it before the output transform would spread it
+    over each 128-block and fail this."""
+    case = synth.linear_case(91, 100 + K, 3, k, n, K)
+    b = synth.bias_for(K, n)
+    W = oracle.reconstruct(case.trellis, k, n, K).astype(np.float64)
+    Weff = (np.diag(case.suh.astype(np.float64)) @ block_hadamard(k) @ W
+            @ block_hadamard(n) @ np.diag(case.svh.astype(np.float64)))
+    ref = case.x.astype(np.float64) @ Weff + b.astype(np.float64)[None, :]
+    got = oracle.linear(case.x, case.trellis, case.suh, case.svh, K, bias=b)
+    assert np.max(np.abs(got - ref)) <= 1e-10 * max(1.0, np.max(np.abs(ref)))
+    # the dequantised-weight form takes the same bias
+    got_w = oracle.linear_w(case.x, oracle.reconstruct(case.trellis, k, n, K), case.suh, case.svh, bias=b)
+    assert np.max(np.abs(got_w - ref)) <= 1e-10 * max(1.0, np.max(np.abs(ref)))
+    with pytest.raises(ValueError):
+        oracle.linear(case.x, case.trellis, case.suh, case.svh, K, bias=b[:-1])
+
+
 def test_one_hot_probe_recovers_a_weight_row():
     """x = suh * (H e_j) gives x' = sqrt(128) e_j, so Hn y = sqrt(128) W[j, :] (svh = 1)."""
     K, k, n = 3, 256, 256
@@ -290,6 +311,12 @@ def test_int8_accumulators_and_output():
     yp = acc * a[:, None].astype(np.float64) * (BOUND / 127.0)
     ref = yp @ block_hadamard(256) * case.svh.astype(np.float64)
     assert np.max(np.abs(res["y"] - ref)) <= 1e-9 * np.abs(ref).max()
+    # an output bias is added to the dequantised result, per output feature
+    b = synth.bias_for(95, 256)
+    resb = oracle.linear_int8(case.x, case.trellis, case.suh, case.svh, 4, bias=b)
+    assert np.array_equal(resb["acc"], res["acc"])
+    refb = ref + b.astype(np.float64)[None, :]
+    assert np.max(np.abs(resb["y"] - refb)) <= 1e-9 * np.abs(refb).max()
 
 
 # ---------------------------------------------------------------------- MoE --
