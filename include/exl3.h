@@ -129,6 +129,24 @@ int exl3_linear(const uint16_t *x, int M, int k, int n,
                 void *workspace, size_t ws_bytes, exl3_stream_t stream);
 
 /*
+ * exl3_linear_bias -- exl3_linear plus an output bias:
+ *   y = RHT_out( RHT_in(x . suh) @ W ) . svh + bias
+ * ("EXL3 checkpoints on the native engine (tracker) #832", "What is left": a
+ * checkpoint's EXL3 group holds a bias beside trellis, suh and svh).  The
+ * pages do not say where it enters; this library adds it as the bias of the
+ * original linear: one fp16 value per output feature, added in fp32 after
+ * svh, in the epilogue of every path (M = 1 GEMV, small-M and prefill
+ * tensor-core kernels, row-invariant mode), before the output is rounded.
+ *   bias [n] fp16 (device, 16-byte aligned; NULL is rejected with
+ *   EXL3_ERR_ARG: use exl3_linear).  Everything else as exl3_linear, with the
+ *   same workspace size.
+ */
+int exl3_linear_bias(const uint16_t *x, int M, int k, int n,
+                     const uint16_t *trellis, const uint16_t *suh, const uint16_t *svh,
+                     const uint16_t *bias, int K, int codebook, void *y, int out_dtype,
+                     void *workspace, size_t ws_bytes, exl3_stream_t stream);
+
+/*
  * exl3_set_weight_prefetch -- let M = 1 calls of exl3_linear stream their
  * weights before the kernel launched ahead of them on the stream has
  * finished (CUDA programmatic dependent launch).  The source pages have no
@@ -184,6 +202,20 @@ int exl3_linear_int8(const uint16_t *x, int M, int k, int n,
                      int K, int codebook, float weight_scale, uint16_t *y,
                      int8_t *xq_out, float *row_scale_out, int32_t *acc_out,
                      void *workspace, size_t ws_bytes, exl3_stream_t stream);
+
+/*
+ * exl3_linear_int8_bias -- exl3_linear_int8 plus an output bias (the same
+ * reading as exl3_linear_bias):
+ *   y = fp16( RHT_out(acc * a_r * weight_scale) . svh + bias )
+ *   bias [n] fp16 (device, 16-byte aligned; NULL is rejected with
+ *   EXL3_ERR_ARG).  The intermediate results (xq_out, row_scale_out,
+ *   acc_out) do not depend on the bias.
+ */
+int exl3_linear_int8_bias(const uint16_t *x, int M, int k, int n,
+                          const uint16_t *trellis, const uint16_t *suh, const uint16_t *svh,
+                          const uint16_t *bias, int K, int codebook, float weight_scale, uint16_t *y,
+                          int8_t *xq_out, float *row_scale_out, int32_t *acc_out,
+                          void *workspace, size_t ws_bytes, exl3_stream_t stream);
 
 /*
  * Routed experts ("exl3xpu" README, "MoE (routed experts)"; Arc 140V MoE

@@ -78,6 +78,30 @@ def test_linear_argument_errors():
     assert "workspace" in _err(L)
 
 
+def test_linear_bias_argument_errors():
+    """The bias entry points check the bias pointer (required, 16-byte aligned)
+    and otherwise share exl3_linear's checks; nothing is launched."""
+    L = tq.lib()
+    ws = 1 << 20
+    args = lambda **kw: [kw.get("x", FAKE), kw.get("M", 1), kw.get("k", 256), kw.get("n", 256),
+                         kw.get("t", FAKE), kw.get("suh", FAKE), kw.get("svh", FAKE), kw.get("b", FAKE),
+                         kw.get("K", 4), kw.get("cb", 2), kw.get("y", FAKE), kw.get("od", 0), kw.get("ws", FAKE),
+                         kw.get("wsb", ws), None]
+    assert L.exl3_linear_bias(*args(b=None)) == tq.EXL3_ERR_ARG
+    assert "bias" in _err(L)
+    assert L.exl3_linear_bias(*args(b=FAKE_MIS)) == tq.EXL3_ERR_ARG
+    assert "bias" in _err(L)
+    assert L.exl3_linear_bias(*args(K=0)) == tq.EXL3_ERR_BITS
+    assert L.exl3_linear_bias(*args(n=200)) == tq.EXL3_ERR_SHAPE
+    assert L.exl3_linear_bias(*args(wsb=16)) == tq.EXL3_ERR_WORKSPACE
+    i8 = lambda **kw: [FAKE, 4, 256, 256, FAKE, FAKE, FAKE, kw.get("b", FAKE), kw.get("K", 4), 2,
+                       kw.get("sw", 3.453125 / 127), FAKE, None, None, None, FAKE, ws, None]
+    assert L.exl3_linear_int8_bias(*i8(b=None)) == tq.EXL3_ERR_ARG
+    assert L.exl3_linear_int8_bias(*i8(b=FAKE_MIS)) == tq.EXL3_ERR_ARG
+    assert L.exl3_linear_int8_bias(*i8(sw=-1.0)) == tq.EXL3_ERR_ARG
+    assert L.exl3_linear_int8_bias(*i8(K=9)) == tq.EXL3_ERR_BITS
+
+
 def test_input_rht_argument_errors():
     L = tq.lib()
     assert L.exl3_input_rht(FAKE, 1, 100, FAKE, FAKE, 1, None) == tq.EXL3_ERR_SHAPE

@@ -74,9 +74,11 @@ def lib():
         L.exl3_linear_workspace_size.argtypes = [I, I, I, I]
         L.exl3_linear_workspace_size.restype = Z
         L.exl3_linear.argtypes = [P, I, I, I, P, P, P, I, I, P, I, P, Z, P]
+        L.exl3_linear_bias.argtypes = [P, I, I, I, P, P, P, P, I, I, P, I, P, Z, P]
         L.exl3_linear_int8_workspace_size.argtypes = [I, I, I, I]
         L.exl3_linear_int8_workspace_size.restype = Z
         L.exl3_linear_int8.argtypes = [P, I, I, I, P, P, P, I, I, ctypes.c_float, P, P, P, P, P, Z, P]
+        L.exl3_linear_int8_bias.argtypes = [P, I, I, I, P, P, P, P, I, I, ctypes.c_float, P, P, P, P, P, Z, P]
         L.exl3_moe_workspace_size.argtypes = [I, I, I, P, P]
         L.exl3_moe_workspace_size.restype = Z
         L.exl3_moe_grouped.argtypes = [P, I, I, P, P, I, I, P, P, P, I, P, Z, P]
@@ -195,6 +197,22 @@ def exl3_linear(x, trellis, suh, svh, K: int, codebook: int = EXL3_CB_MUL1, out_
     return y
 
 
+def exl3_linear_bias(x, trellis, suh, svh, bias, K: int, codebook: int = EXL3_CB_MUL1,
+                     out_dtype: int = EXL3_OUT_F16, y=None, workspace_buf=None, stream=None) -> torch.Tensor:
+    """y = RHT_out(RHT_in(x . suh) @ W) . svh + bias for x [M, k] fp16, bias [n] fp16."""
+    M, k = x.shape
+    n = trellis.shape[1] * 16
+    if y is None:
+        y = torch.empty((M, n), dtype=torch.float32 if out_dtype == EXL3_OUT_F32 else torch.float16,
+                        device=x.device)
+    need = exl3_linear_workspace_size(M, k, n, K)
+    ws = workspace_buf if workspace_buf is not None else workspace(need, x.device, stream)
+    _check(lib().exl3_linear_bias(_ptr(x, "x", 2), M, k, n, _ptr(trellis, "trellis", 2), _ptr(suh, "suh", 2),
+                                  _ptr(svh, "svh", 2), _ptr(bias, "bias", 2), K, codebook, _ptr(y, "y"), out_dtype,
+                                  _ptr(ws, "workspace"), ws.numel() * ws.element_size(), _stream(stream)))
+    return y
+
+
 def exl3_set_row_invariant(enable: bool) -> bool:
     """Make each row of an exl3_linear result independent of the row count and
     of the other rows (same bits at every M); returns the previous setting."""
@@ -232,6 +250,24 @@ def exl3_linear_int8(x, trellis, suh, svh, K: int, codebook: int = EXL3_CB_MUL1,
                                   _ptr(xq_out, "xq_out", 1), _ptr(row_scale_out, "row_scale_out", 4),
                                   _ptr(acc_out, "acc_out", 4), _ptr(ws, "workspace"),
                                   ws.numel() * ws.element_size(), _stream(stream)))
+    return y
+
+
+def exl3_linear_int8_bias(x, trellis, suh, svh, bias, K: int, codebook: int = EXL3_CB_MUL1,
+                          weight_scale: float = WEIGHT_SCALE, y=None, xq_out=None, row_scale_out=None,
+                          acc_out=None, workspace_buf=None, stream=None) -> torch.Tensor:
+    """int8 prefill linear plus an output bias [n] fp16: y fp16 [M, n]."""
+    M, k = x.shape
+    n = trellis.shape[1] * 16
+    if y is None:
+        y = torch.empty((M, n), dtype=torch.float16, device=x.device)
+    need = exl3_linear_int8_workspace_size(M, k, n, K)
+    ws = workspace_buf if workspace_buf is not None else workspace(need, x.device, stream)
+    _check(lib().exl3_linear_int8_bias(_ptr(x, "x", 2), M, k, n, _ptr(trellis, "trellis", 2),
+                                       _ptr(suh, "suh", 2), _ptr(svh, "svh", 2), _ptr(bias, "bias", 2), K,
+                                       codebook, weight_scale, _ptr(y, "y", 2), _ptr(xq_out, "xq_out", 1),
+                                       _ptr(row_scale_out, "row_scale_out", 4), _ptr(acc_out, "acc_out", 4),
+                                       _ptr(ws, "workspace"), ws.numel() * ws.element_size(), _stream(stream)))
     return y
 
 

@@ -21,11 +21,15 @@ cudaError_t exl3_launch_gemv_m1(const uint16_t *x, const uint16_t *trellis, cons
                                 const uint16_t *svh, int k, int n, int K, void *y, bool f32out,
                                 float *partials, int *counters, int *err, int grid, cudaStream_t s,
                                 bool prefetch = false);
+cudaError_t exl3_launch_gemv_m1_bias(const uint16_t *x, const uint16_t *trellis, const uint16_t *suh,
+                                     const uint16_t *svh, const uint16_t *bias, int k, int n, int K, void *y,
+                                     bool f32out, float *partials, int *counters, int *err, int grid,
+                                     cudaStream_t s, bool prefetch);
 void exl3_gemv_plan(int k, int n, int K, int *grid, size_t *partial_floats);
 bool exl3_gemv_fits(int k, int n, int K);
 int exl3_launch_gemm_tc(const uint16_t *xh, const uint16_t *wt, int M, int n, int k, const uint16_t *svh,
                         void *y, bool f32out, const float *row_scale, float pre, int *err, cudaStream_t s,
-                        bool q8 = false, int32_t *acc_out = nullptr);
+                        bool q8 = false, int32_t *acc_out = nullptr, const uint16_t *bias = nullptr);
 cudaError_t exl3_launch_quant_act(const uint16_t *x, int M, int k, const uint16_t *suh, uint16_t *qh,
                                   int8_t *q8, float *row_scale, cudaStream_t s);
 cudaError_t exl3_launch_reconstruct_q8_t(const uint16_t *trellis, int k, int n, int K, uint16_t *wq,
@@ -33,7 +37,7 @@ cudaError_t exl3_launch_reconstruct_q8_t(const uint16_t *trellis, int k, int n, 
 int exl3_fused_tc_splits(int k, int n);
 int exl3_launch_fused_tc(const uint16_t *xh, const float *xsum, const uint16_t *trellis, const uint16_t *svh, int M,
                          int k, int n, int K, void *y, bool f32out, float *partials, int *counters, int *err,
-                         int splits, cudaStream_t s, int npad_fixed);
+                         int splits, cudaStream_t s, int npad_fixed, const uint16_t *bias = nullptr);
 
 cudaError_t exl3_launch_moe_remap(const int32_t *ids, int U, int E, int *counts, int *offsets, int *perm, int *pos,
                                   int *mtiles, int *n_mtiles, int max_mtiles, int *chunk_tab, int *err,
@@ -379,14 +383,20 @@ size_t exl3_linear_workspace_size(int M, int k, int n, int K) {
   return a > b ? a : b;
 }
 
-int exl3_linear(const uint16_t *x, int M, int k, int n, const uint16_t *trellis, const uint16_t *suh,
-                const uint16_t *svh, int K, int codebook, void *y, int out_dtype, void *workspace,
-                size_t ws_bytes, exl3_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// exl3_linear with an optional output bias (NULL: none).
+int linear_impl(const uint16_t *x, int M, int k, int n, const uint16_t *trellis, const uint16_t *suh,
+                const uint16_t *svh, const uint16_t *bias, int K, int codebook, void *y, int out_dtype,
+                void *workspace, size_t ws_bytes, exl3_stream_t stream) {
   g_last_error.clear();
   EXL3_TRY(check_ptr(x, "x"));
   EXL3_TRY(check_ptr(trellis, "trellis"));
   EXL3_TRY(check_ptr(suh, "suh"));
   EXL3_TRY(check_ptr(svh, "svh"));
+  EXL3_TRY(check_ptr(bias, "bias", false));
   EXL3_TRY(check_ptr(y, "y"));
   EXL3_TRY(check_bits_codebook(K, codebook));
   EXL3_TRY(check_linear_shape(M, k, n));
@@ -412,15 +422,15 @@ int exl3_linear(const uint16_t *x, int M, int k, int n, const uint16_t *trellis,
       void *yc = static_cast<uint8_t *>(y) + (size_t)m0 * n * (f32 ? 4 : 2);
       EXL3_TRY(exl3_launch_fused_tc(xh + (size_t)m0 * k, xsum + (size_t)m0 * xunits, trellis, svh, Mc, k, n, K, yc,
                                     f32, at<float>(workspace, L.partials), at<int>(workspace, L.counters), err,
-                                    L.splits, stream, kRowInvChunk));
+                                    L.splits, stream, kRowInvChunk, bias));
     }
     return EXL3_OK;
   }
   // M = 1 runs the GEMV unless x' for this k does not fit beside its ring
   if (M == 1 && exl3_gemv_fits(k, n, K)) {
-    return exl3_cuda_check(exl3_launch_gemv_m1(x, trellis, suh, svh, k, n, K, y, f32, at<float>(workspace, L.partials),
-                                               at<int>(workspace, L.counters), err, L.grid, stream,
-                                               g_weight_prefetch.load() != 0),
+    return exl3_cuda_check(exl3_launch_gemv_m1_bias(x, trellis, suh, svh, bias, k, n, K, y, f32,
+                                                    at<float>(workspace, L.partials), at<int>(workspace, L.counters),
+                                                    err, L.grid, stream, g_weight_prefetch.load() != 0),
                            "gemv launch");
   }
   uint16_t *xh = at<uint16_t>(workspace, L.xh);
@@ -428,28 +438,25 @@ int exl3_linear(const uint16_t *x, int M, int k, int n, const uint16_t *trellis,
     float *xsum = at<float>(workspace, L.xsum);
     EXL3_TRY(exl3_cuda_check(exl3_launch_input_rht(x, M, k, suh, xh, false, stream, xsum), "input_rht launch"));
     return exl3_launch_fused_tc(xh, xsum, trellis, svh, M, k, n, K, y, f32, at<float>(workspace, L.partials),
-                                at<int>(workspace, L.counters), err, L.splits, stream, 0);
+                                at<int>(workspace, L.counters), err, L.splits, stream, 0, bias);
   }
   EXL3_TRY(exl3_cuda_check(exl3_launch_input_rht(x, M, k, suh, xh, false, stream), "input_rht launch"));
   uint16_t *wt = at<uint16_t>(workspace, L.wt);
   EXL3_TRY(exl3_cuda_check(exl3_launch_reconstruct_t(trellis, k, n, K, wt, stream), "reconstruct launch"));
-  return exl3_launch_gemm_tc(xh, wt, M, n, k, svh, y, f32, nullptr, 1.0f, err, stream);
+  return exl3_launch_gemm_tc(xh, wt, M, n, k, svh, y, f32, nullptr, 1.0f, err, stream, false, nullptr, bias);
 }
 
-size_t exl3_linear_int8_workspace_size(int M, int k, int n, int K) {
-  if (M < 1 || k <= 0 || n <= 0 || k % 128 || n % 128 || K < 1 || K > 8) return 0;
-  return linear_int8_ws(M, k, n).total;
-}
-
-int exl3_linear_int8(const uint16_t *x, int M, int k, int n, const uint16_t *trellis, const uint16_t *suh,
-                     const uint16_t *svh, int K, int codebook, float weight_scale, uint16_t *y, int8_t *xq_out,
-                     float *row_scale_out, int32_t *acc_out, void *workspace, size_t ws_bytes,
-                     exl3_stream_t stream) {
+// exl3_linear_int8 with an optional output bias (NULL: none).
+int linear_int8_impl(const uint16_t *x, int M, int k, int n, const uint16_t *trellis, const uint16_t *suh,
+                     const uint16_t *svh, const uint16_t *bias, int K, int codebook, float weight_scale,
+                     uint16_t *y, int8_t *xq_out, float *row_scale_out, int32_t *acc_out, void *workspace,
+                     size_t ws_bytes, exl3_stream_t stream) {
   g_last_error.clear();
   EXL3_TRY(check_ptr(x, "x"));
   EXL3_TRY(check_ptr(trellis, "trellis"));
   EXL3_TRY(check_ptr(suh, "suh"));
   EXL3_TRY(check_ptr(svh, "svh"));
+  EXL3_TRY(check_ptr(bias, "bias", false));
   EXL3_TRY(check_ptr(y, "y"));
   EXL3_TRY(check_ptr(xq_out, "xq_out", false));
   EXL3_TRY(check_ptr(row_scale_out, "row_scale_out", false));
@@ -467,7 +474,53 @@ int exl3_linear_int8(const uint16_t *x, int M, int k, int n, const uint16_t *tre
   int *err = at<int>(workspace, 0);
   EXL3_TRY(exl3_cuda_check(exl3_launch_quant_act(x, M, k, suh, qh, xq_out, rs, stream), "quant_act launch"));
   EXL3_TRY(exl3_cuda_check(exl3_launch_reconstruct_q8_t(trellis, k, n, K, wq, stream), "reconstruct_q8 launch"));
-  return exl3_launch_gemm_tc(qh, wq, M, n, k, svh, y, false, rs, weight_scale, err, stream, true, acc_out);
+  return exl3_launch_gemm_tc(qh, wq, M, n, k, svh, y, false, rs, weight_scale, err, stream, true, acc_out, bias);
+}
+
+}  // namespace
+
+extern "C" {
+
+int exl3_linear(const uint16_t *x, int M, int k, int n, const uint16_t *trellis, const uint16_t *suh,
+                const uint16_t *svh, int K, int codebook, void *y, int out_dtype, void *workspace,
+                size_t ws_bytes, exl3_stream_t stream) {
+  return linear_impl(x, M, k, n, trellis, suh, svh, nullptr, K, codebook, y, out_dtype, workspace, ws_bytes,
+                     stream);
+}
+
+int exl3_linear_bias(const uint16_t *x, int M, int k, int n, const uint16_t *trellis, const uint16_t *suh,
+                     const uint16_t *svh, const uint16_t *bias, int K, int codebook, void *y, int out_dtype,
+                     void *workspace, size_t ws_bytes, exl3_stream_t stream) {
+  if (!bias) {
+    g_last_error.clear();
+    return exl3_fail(EXL3_ERR_ARG, "bias is NULL (use exl3_linear for a linear without bias)");
+  }
+  return linear_impl(x, M, k, n, trellis, suh, svh, bias, K, codebook, y, out_dtype, workspace, ws_bytes, stream);
+}
+
+size_t exl3_linear_int8_workspace_size(int M, int k, int n, int K) {
+  if (M < 1 || k <= 0 || n <= 0 || k % 128 || n % 128 || K < 1 || K > 8) return 0;
+  return linear_int8_ws(M, k, n).total;
+}
+
+int exl3_linear_int8(const uint16_t *x, int M, int k, int n, const uint16_t *trellis, const uint16_t *suh,
+                     const uint16_t *svh, int K, int codebook, float weight_scale, uint16_t *y, int8_t *xq_out,
+                     float *row_scale_out, int32_t *acc_out, void *workspace, size_t ws_bytes,
+                     exl3_stream_t stream) {
+  return linear_int8_impl(x, M, k, n, trellis, suh, svh, nullptr, K, codebook, weight_scale, y, xq_out,
+                          row_scale_out, acc_out, workspace, ws_bytes, stream);
+}
+
+int exl3_linear_int8_bias(const uint16_t *x, int M, int k, int n, const uint16_t *trellis, const uint16_t *suh,
+                          const uint16_t *svh, const uint16_t *bias, int K, int codebook, float weight_scale,
+                          uint16_t *y, int8_t *xq_out, float *row_scale_out, int32_t *acc_out, void *workspace,
+                          size_t ws_bytes, exl3_stream_t stream) {
+  if (!bias) {
+    g_last_error.clear();
+    return exl3_fail(EXL3_ERR_ARG, "bias is NULL (use exl3_linear_int8 for a linear without bias)");
+  }
+  return linear_int8_impl(x, M, k, n, trellis, suh, svh, bias, K, codebook, weight_scale, y, xq_out, row_scale_out,
+                          acc_out, workspace, ws_bytes, stream);
 }
 
 size_t exl3_moe_workspace_size(int T, int topk, int E, const exl3_expert_proj *w13,

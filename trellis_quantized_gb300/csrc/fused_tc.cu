@@ -66,6 +66,7 @@ struct Args {
   int *err;
   int M, k, n, tiles_n, kb_per_split, splits, xunits;
   int npad;            // MMA N: tokens rounded up to 16, or 128 for every M (row-invariant mode)
+  const __half *bias;  // [n] fp16 added after svh, or NULL
 };
 
 template <int K, bool F32OUT, int NMAX>
@@ -355,6 +356,14 @@ __global__ void __launch_bounds__(Roles<NMAX>::WARPS * 32, 1) fused_tc_kernel(co
         v[1] = v[1] * kRhtScale * __high2float(sh[0]);
         v[2] = v[2] * kRhtScale * __low2float(sh[1]);
         v[3] = v[3] * kRhtScale * __high2float(sh[1]);
+        if (a.bias) {   // the output bias, per output feature
+          const uint2 bv = *reinterpret_cast<const uint2 *>(a.bias + gc);
+          const __half2 *bh = reinterpret_cast<const __half2 *>(&bv);
+          v[0] = __fadd_rn(v[0], __low2float(bh[0]));   // one rounding, never contracted
+          v[1] = __fadd_rn(v[1], __high2float(bh[0]));
+          v[2] = __fadd_rn(v[2], __low2float(bh[1]));
+          v[3] = __fadd_rn(v[3], __high2float(bh[1]));
+        }
         if (F32OUT) {
           *reinterpret_cast<float4 *>(static_cast<float *>(a.y) + (long)m * a.n + gc) = make_float4(v[0], v[1], v[2], v[3]);
         } else {
@@ -419,12 +428,13 @@ int exl3_fused_tc_splits(int k, int n) {
 }
 
 // xh: x' fp16 [M][k] (M <= 128); partials: [splits][M][n] fp32 (unused when splits == 1).
+// bias: [n] fp16 added to the output, or NULL.
 // npad_fixed (32 or 128, at least M): the MMA is that many tokens wide
 // whatever M is, so that a token's result does not depend on how many tokens
 // share the call; 0: M rounded up to 16.
 int exl3_launch_fused_tc(const uint16_t *xh, const float *xsum, const uint16_t *trellis, const uint16_t *svh, int M,
                          int k, int n, int K, void *y, bool f32out, float *partials, int *counters, int *err,
-                         int splits, cudaStream_t s, int npad_fixed) {
+                         int splits, cudaStream_t s, int npad_fixed, const uint16_t *bias) {
   auto fn = ftc_tmap_fn();
   if (!fn) return exl3_fail(EXL3_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   // x' [M][k] as (64 k, M rows, k/64 blocks): one load brings XSTEPS k blocks
@@ -457,7 +467,7 @@ int exl3_launch_fused_tc(const uint16_t *xh, const float *xsum, const uint16_t *
     if (r != CUDA_SUCCESS) return exl3_fail(EXL3_ERR_CUDA, "cuTensorMapEncodeTiled (trellis) failed (%d)", (int)r);
   }
   ftc::Args a{trellis, xsum, reinterpret_cast<const __half *>(svh), y, partials, counters, err, M, k, n, n / 16,
-              0, splits, (k + 255) / 256, npad};
+              0, splits, (k + 255) / 256, npad, reinterpret_cast<const __half *>(bias)};
   dim3 grid(n / 128, splits);
   cudaError_t e = cudaSuccess;
 #define EXL3_FTC(KK, F32, NM)                                                                                \

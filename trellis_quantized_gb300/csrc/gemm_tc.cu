@@ -67,6 +67,7 @@ struct Args {
   float pre;
   int *err;
   int32_t *acc_out;      // integer mode: optional [M][n] copy of the accumulators
+  const __half *bias;    // [n] fp16 added after svh, or null
 };
 
 __device__ __forceinline__ void fwht128_regs(float (&v)[128]) {
@@ -82,7 +83,7 @@ __device__ __forceinline__ void fwht128_regs(float (&v)[128]) {
       }
 }
 
-// y[row][col0 .. col0+127] = v * 2^-3.5 * svh (v already transformed).
+// y[row][col0 .. col0+127] = v * 2^-3.5 * svh (+ bias) (v already transformed).
 template <bool F32OUT>
 __device__ __forceinline__ void store_row(const float (&v)[128], const Args &a, int row, int col0) {
   if (row >= a.M) return;
@@ -95,6 +96,15 @@ __device__ __forceinline__ void store_row(const float (&v)[128], const Args &a, 
     for (int j = 0; j < 4; ++j) {
       o[2 * j] = v[8 * c8 + 2 * j] * kRhtScale * __low2float(sh[j]);
       o[2 * j + 1] = v[8 * c8 + 2 * j + 1] * kRhtScale * __high2float(sh[j]);
+    }
+    if (a.bias) {   // the output bias, per output feature
+      const uint4 bv = __ldg(reinterpret_cast<const uint4 *>(a.bias + col0 + 8 * c8));
+      const __half2 *bh = reinterpret_cast<const __half2 *>(&bv);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        o[2 * j] = __fadd_rn(o[2 * j], __low2float(bh[j]));   // one rounding, never contracted
+        o[2 * j + 1] = __fadd_rn(o[2 * j + 1], __high2float(bh[j]));
+      }
     }
     if (F32OUT) {
       float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(a.y) + (long)row * a.n + col0 + 8 * c8);
@@ -345,9 +355,10 @@ static int make_tmap_f16(CUtensorMap *m, const void *base, int rows, int cols, i
 
 // n must be a multiple of 128 and k of 64; rows of x' beyond M read as zero.
 // q8: integer mode (operands integer-valued fp16, exact int32 accumulation).
+// bias: [n] fp16 added to the output, or null.
 int exl3_launch_gemm_tc(const uint16_t *xh, const uint16_t *wt, int M, int n, int k, const uint16_t *svh,
                         void *y, bool f32out, const float *row_scale, float pre, int *err, cudaStream_t s,
-                        bool q8 = false, int32_t *acc_out = nullptr) {
+                        bool q8 = false, int32_t *acc_out = nullptr, const uint16_t *bias = nullptr) {
   CUtensorMap ta, tb;
   int rc = make_tmap_f16(&ta, xh, M, k, gtc::BM);
   if (rc) return rc;
@@ -361,7 +372,8 @@ int exl3_launch_gemm_tc(const uint16_t *xh, const uint16_t *wt, int M, int n, in
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (sms <= 0) sms = 148;
   }
-  gtc::Args a{M, n, k, reinterpret_cast<const __half *>(svh), y, row_scale, pre, err, acc_out};
+  gtc::Args a{M, n, k, reinterpret_cast<const __half *>(svh), y, row_scale, pre, err, acc_out,
+              reinterpret_cast<const __half *>(bias)};
   const int tiles = ((M + gtc::BM - 1) / gtc::BM) * (n / (wide ? 256 : 128));
   const int grid = tiles < sms ? tiles : sms;
   cudaError_t e = cudaSuccess;

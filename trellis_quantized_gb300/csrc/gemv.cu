@@ -77,6 +77,8 @@ struct GemvArgs {
   // (if set) receives u, or -1 for an invalid expert id, for the combine
   const float *act_in;
   int *pos_out;
+  // Output bias [n] fp16 added after svh (NULL: none; not GROUPED)
+  const __half *bias;
 };
 
 constexpr int kGemvMaxOps = 4;        // ops one CTA's range may touch in GROUPED mode
@@ -279,12 +281,16 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
             pre[j][g][3] = r.w;
           }
       }
-      uint2 svv[S::NG];   // the block's svh, loaded ahead as well
+      uint2 svv[S::NG];   // the block's svh (and bias), loaded ahead as well
+      uint2 bvv[S::NG];
+      const bool has_bias = !GROUPED && a.bias != nullptr;
 #pragma unroll
-      for (int g = 0; g < S::NG; ++g)
-        svv[g] = (!shared || finisher) && col0 + g * 128 < a.n
-                     ? *reinterpret_cast<const uint2 *>(P.svh + col0 + g * 128 + lane * 4)
-                     : make_uint2(0u, 0u);
+      for (int g = 0; g < S::NG; ++g) {
+        const bool mine = (!shared || finisher) && col0 + g * 128 < a.n;
+        svv[g] = mine ? *reinterpret_cast<const uint2 *>(P.svh + col0 + g * 128 + lane * 4) : make_uint2(0u, 0u);
+        bvv[g] = mine && has_bias ? *reinterpret_cast<const uint2 *>(a.bias + col0 + g * 128 + lane * 4)
+                                  : make_uint2(0u, 0u);
+      }
       if (!*s_abort && !tc::mbar_wait(seg_full, sp)) {
         if (lane == 0) set_device_error(a.err, kErrBounds);
         *s_abort = 1;
@@ -366,6 +372,13 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
               o1 *= P.scale;
               o2 *= P.scale;
               o3 *= P.scale;
+            }
+            if (has_bias) {   // the output bias, per output feature
+              const __half2 *bh = reinterpret_cast<const __half2 *>(&bvv[g]);
+              o0 = __fadd_rn(o0, __low2float(bh[0]));   // one rounding, never contracted
+              o1 = __fadd_rn(o1, __high2float(bh[0]));
+              o2 = __fadd_rn(o2, __low2float(bh[1]));
+              o3 = __fadd_rn(o3, __high2float(bh[1]));
             }
             if (F32OUT) {
               *reinterpret_cast<float4 *>(static_cast<float *>(P.y) + gc) = make_float4(o0, o1, o2, o3);
@@ -659,10 +672,11 @@ void exl3_gemv_plan(int k, int n, int K, int *grid, size_t *partial_floats) {
   *partial_floats = (size_t)(colblocks + g) * (size_t)cc;
 }
 
-cudaError_t exl3_launch_gemv_m1(const uint16_t *x, const uint16_t *trellis, const uint16_t *suh,
-                                const uint16_t *svh, int k, int n, int K, void *y, bool f32out,
-                                float *partials, int *counters, int *err, int grid, cudaStream_t s,
-                                bool prefetch) {
+// bias: [n] fp16 added to the output (NULL: none).
+cudaError_t exl3_launch_gemv_m1_bias(const uint16_t *x, const uint16_t *trellis, const uint16_t *suh,
+                                     const uint16_t *svh, const uint16_t *bias, int k, int n, int K, void *y,
+                                     bool f32out, float *partials, int *counters, int *err, int grid,
+                                     cudaStream_t s, bool prefetch) {
   auto fn = gemv_tmap_fn();
   if (!fn) return cudaErrorNotSupported;
   const int cc = exl3_gemv_cta_cols(K);
@@ -701,6 +715,7 @@ cudaError_t exl3_launch_gemv_m1(const uint16_t *x, const uint16_t *trellis, cons
   a.op_rows = a.total;
   a.act_in = nullptr;
   a.pos_out = nullptr;
+  a.bias = reinterpret_cast<const __half *>(bias);
   a.pre_stages = kGemvPreStages;
   a.stages = 0;
   EXL3_K_SWITCH(K, a.stages = Launcher<KK, false>::stages(k));
@@ -712,6 +727,14 @@ cudaError_t exl3_launch_gemv_m1(const uint16_t *x, const uint16_t *trellis, cons
     EXL3_K_SWITCH(K, e = Launcher<KK, false>::launch(tm, a, grid, s, prefetch));
   }
   return e;
+}
+
+cudaError_t exl3_launch_gemv_m1(const uint16_t *x, const uint16_t *trellis, const uint16_t *suh,
+                                const uint16_t *svh, int k, int n, int K, void *y, bool f32out,
+                                float *partials, int *counters, int *err, int grid, cudaStream_t s,
+                                bool prefetch) {
+  return exl3_launch_gemv_m1_bias(x, trellis, suh, svh, nullptr, k, n, K, y, f32out, partials, counters, err, grid,
+                                  s, prefetch);
 }
 
 // ---- routed experts for a few tokens: U * nslots M = 1 GEMVs in one launch
@@ -785,6 +808,7 @@ cudaError_t exl3_launch_moe_gemv(const uint16_t *x, const float *act_in, int *po
   a.x_per_unit = 0;
   a.act_in = act_in;
   a.pos_out = pos_out;
+  a.bias = nullptr;
   a.pre_stages = kGemvPreStages;
   a.nops = U * nslots;
   if ((unsigned long long)a.colblocks * a.tiles_k * a.nops * (unsigned long long)grid >= (1ull << 32))
