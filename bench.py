@@ -41,7 +41,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # at k=5120 n=25600, with the hash of the kernel's sources at capture time; a
 # changed kernel source makes the recorded traffic stale (reported as null).
 TRAFFIC = {"files": ["trellis_quantized_gb300/csrc/gemv.cu", "trellis_quantized_gb300/csrc/gemv_core.cuh"],
-           "sha1": "39eccf8edf26aee4abb8358e8a12c43c7a601c35", "bytes_per_launch": 65664000,
+           "sha1": "ed62b54024519b95b1a8eae7b69bf698bc9e5116", "bytes_per_launch": 65665280,
            "workload": "k5120 n25600 K4 M1"}
 
 
