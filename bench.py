@@ -431,21 +431,31 @@ def bench_extras(only=None, moe_tokens=None):
 
 # ------------------------------------------------------------------------- oracle
 
+CPU_SAMPLE_S = 10.0   # seconds of oracle work in the bench's cpu_baseline
+
+
 def cpu_baseline(args):
-    """The CPU oracle, as it stands, on a bounded sample: the n = 5120 linear of
-    the sweep (decode + float64 contraction + transforms), timed in full."""
+    """The CPU oracle, as it stands, on a bounded sample of the workload: the
+    sweep's three M = 1 linears (decode + float64 contraction + transforms),
+    repeated whole until at least CPU_SAMPLE_S seconds have passed."""
     import oracle
     oracle.build()
-    c = synth.config2(5120, 1)
-    oracle.linear(c.x[:1, :128], c.trellis[:8, :8], c.suh[:128], c.svh[:128], 4)   # load
-    reps = 1
+    cases = [synth.config2(n, 1) for n in synth.CONFIG2_N]
+    oracle.linear(cases[0].x[:1, :128], cases[0].trellis[:8, :8], cases[0].suh[:128], cases[0].svh[:128], 4)  # load
+    step_bytes = sum(linear_bytes(c) for c in cases)
+    reps = 0
     t0 = time.perf_counter()
-    for _ in range(reps):
-        oracle.linear(c.x, c.trellis, c.suh, c.svh, 4)
-    dt = (time.perf_counter() - t0) / reps
+    while True:
+        for c in cases:
+            oracle.linear(c.x, c.trellis, c.suh, c.svh, 4)
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= CPU_SAMPLE_S:
+            break
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    return {"value": round(linear_bytes(c) / dt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"one k=5120 n=5120 K=4 M=1 linear ({linear_bytes(c)} algorithmic bytes) in {dt:.2f} s"}
+    return {"value": round(step_bytes * reps / dt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{reps} repetitions of the step's three k=5120 K=4 M=1 linears (n = 5120, 17408, 25600; "
+                      f"{step_bytes} algorithmic bytes each) in {dt:.1f} s"}
 
 
 def run_reference(args):
