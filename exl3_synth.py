@@ -212,6 +212,58 @@ def moe_case(config: int, sub: int, T: int, *, E: int = 256, topk: int = 8, hidd
     return MoECase(name or f"moe{config}.{sub}", T, hidden, inter, E, topk, K, x, ids, w, w13, w2)
 
 
+@dataclass
+class MixedExpertProj:
+    """One projection kind with a width per expert: the trellis arena packs
+    expert e's nslots tensors ([k/16, n/16, 16*K[e]] each) right after expert
+    e-1's, as one flat uint16 array."""
+    trellis: np.ndarray  # flat uint16, sum over e of nslots * k * n * K[e] / 16 words
+    suh: np.ndarray      # [E, nslots, k] fp16
+    svh: np.ndarray      # [E, nslots, n] fp16
+    K: np.ndarray        # [E] int32 widths
+    k: int
+    n: int
+    nslots: int
+
+
+@dataclass
+class MixedMoECase:
+    name: str
+    T: int
+    hidden: int
+    inter: int
+    E: int
+    topk: int
+    x: np.ndarray
+    ids: np.ndarray
+    weights: np.ndarray
+    w13: MixedExpertProj
+    w2: MixedExpertProj
+
+
+def mixed_expert_proj(rng: np.random.Generator, K: np.ndarray, nslots: int, k: int, n: int) -> MixedExpertProj:
+    K = np.asarray(K, dtype=np.int32)
+    E = len(K)
+    words = int(sum(nslots * (k // 16) * (n // 16) * 16 * int(w) for w in K))
+    tr = rng.integers(0, 1 << 16, size=words, dtype=np.uint16)
+    suh = np.where(rng.integers(0, 2, size=(E, nslots, k)) == 1, 1.0, -1.0).astype(np.float16)
+    svh = np.where(rng.integers(0, 2, size=(E, nslots, n)) == 1, 1.0, -1.0).astype(np.float16)
+    return MixedExpertProj(tr, suh, svh, K, k, n, nslots)
+
+
+def mixed_moe_case(config: int, sub: int, T: int, K13, K2, *, topk: int = 8, hidden: int = 2048,
+                   inter: int = 512, name: str = "") -> MixedMoECase:
+    """Routed experts with a width per expert: K13[e] for gate+up, K2[e] for
+    down (E = len(K13)); otherwise the recipe of moe_case."""
+    rng = rng_for(config, sub)
+    E = len(K13)
+    w13 = mixed_expert_proj(rng, K13, 2, hidden, inter)
+    w2 = mixed_expert_proj(rng, K2, 1, inter, hidden)
+    ids, w = routing(rng, T, E, topk)
+    x = activations(rng, T, hidden)
+    return MixedMoECase(name or f"moe-mixed{config}.{sub}", T, hidden, inter, E, topk, x, ids, w, w13, w2)
+
+
 def config5(T: int) -> MoECase:
     """Grouped MoE: E=256, top-8, hidden 2048, inter 512, K=3."""
     return moe_case(5, CONFIG5_T.index(T), T, name=f"cfg5 E256 top8 h2048 i512 K3 T{T}")

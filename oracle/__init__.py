@@ -79,6 +79,7 @@ def _load():
         lib.or_int8_acc.argtypes = [P, P, I, I, I, P]
         lib.or_linear_int8.argtypes = [P, I, I, I, P, P, P, I, P, P, P, P, P]
         lib.or_moe.argtypes = [P, I, I, P, P, I, I, P, P, P, I, I, P, P, P, I, P, I, P]
+        lib.or_moe_k.argtypes = [P, I, I, P, P, I, I, P, P, P, I, P, P, P, P, P, P, I, P]
         _lib = lib
         return lib
 
@@ -293,4 +294,33 @@ def moe(x, ids, weights, w13_trellis, w13_suh, w13_svh, K13, w2_trellis, w2_suh,
                           _ptr(t13), _ptr(_u16(w13_suh)), _ptr(_u16(w13_svh)), inter, K13,
                           _ptr(t2), _ptr(_u16(w2_suh)), _ptr(_u16(w2_svh)), K2,
                           _ptr(tok), len(tok), _ptr(y)), "moe")
+    return y
+
+
+def moe_k(x, ids, weights, w13_trellis, w13_suh, w13_svh, K13, w2_trellis, w2_suh, w2_svh, K2, inter: int,
+          tokens=None) -> np.ndarray:
+    """Routed-expert output with a width per expert (K13[e], K2[e]); the trellis
+    arenas are flat, expert e packed right after expert e-1."""
+    x = _u16(x)
+    T, hidden = x.shape
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    weights = np.ascontiguousarray(weights, dtype=np.float32)
+    topk = ids.shape[1]
+    k13 = np.ascontiguousarray(K13, dtype=np.int32)
+    k2 = np.ascontiguousarray(K2, dtype=np.int32)
+    E = len(k13)
+    if len(k2) != E:
+        raise ValueError("K13 and K2 must have one width per expert")
+    t13 = _u16(w13_trellis).reshape(-1)
+    t2 = _u16(w2_trellis).reshape(-1)
+    need13 = int(sum(2 * (hidden // 16) * (inter // 16) * 16 * int(w) for w in k13))
+    need2 = int(sum((inter // 16) * (hidden // 16) * 16 * int(w) for w in k2))
+    if t13.size != need13 or t2.size != need2:
+        raise ValueError(f"arena sizes {t13.size}/{t2.size} words, widths need {need13}/{need2}")
+    tok = np.arange(T, dtype=np.int32) if tokens is None else np.ascontiguousarray(tokens, dtype=np.int32)
+    y = np.zeros((len(tok), hidden), dtype=np.float64)
+    _check(_load().or_moe_k(_ptr(x), T, hidden, _ptr(ids), _ptr(weights), topk, E,
+                            _ptr(t13), _ptr(_u16(w13_suh)), _ptr(_u16(w13_svh)), inter, _ptr(k13),
+                            _ptr(t2), _ptr(_u16(w2_suh)), _ptr(_u16(w2_svh)), _ptr(k2),
+                            _ptr(tok), len(tok), _ptr(y)), "moe_k")
     return y

@@ -452,23 +452,39 @@ static void lin_f64_in(const double *xin, int k, int n, const uint16_t *W,
  * linear of this file, its own input and output transforms.  Experts' weights
  * are dequantised once per expert used.  Only the tokens listed in `tok`
  * (n_tok of them) are evaluated, so callers can sample a large batch.
+ *
+ * Per-expert widths ("EXL3 checkpoints on the native engine (tracker) #832":
+ * per-expert widths stay in the representation): expert e of w13 has width
+ * K13[e] and of w2 K2[e].  Each arena packs the experts in id order, expert
+ * e's slots right after expert e-1's, so expert e starts at the sum of the
+ * earlier experts' sizes (nslots * (k/16) * (n/16) * 16 * K words each).
  */
-int or_moe(const uint16_t *x, int T, int hidden, const int32_t *ids, const float *weights,
-           int topk, int E,
-           const uint16_t *w13_trellis, const uint16_t *w13_suh, const uint16_t *w13_svh,
-           int inter, int K13,
-           const uint16_t *w2_trellis, const uint16_t *w2_suh, const uint16_t *w2_svh, int K2,
-           const int32_t *tok, int n_tok, double *y /* [n_tok][hidden] */) {
-  if (K13 < 1 || K13 > 8 || K2 < 1 || K2 > 8) return OR_ERR_BITS;
+int or_moe_k(const uint16_t *x, int T, int hidden, const int32_t *ids, const float *weights,
+             int topk, int E,
+             const uint16_t *w13_trellis, const uint16_t *w13_suh, const uint16_t *w13_svh,
+             int inter, const int32_t *K13,
+             const uint16_t *w2_trellis, const uint16_t *w2_suh, const uint16_t *w2_svh,
+             const int32_t *K2,
+             const int32_t *tok, int n_tok, double *y /* [n_tok][hidden] */) {
   if (hidden % 128 || inter % 128 || T < 0 || topk < 1 || E < 1) return OR_ERR_SHAPE;
-  long w13_slot = (long)(hidden / 16) * (inter / 16) * 16 * K13;  /* words per slot */
-  long w2_slot = (long)(inter / 16) * (hidden / 16) * 16 * K2;
+  for (int e = 0; e < E; ++e)
+    if (K13[e] < 1 || K13[e] > 8 || K2[e] < 1 || K2[e] > 8) return OR_ERR_BITS;
+  /* word offset of each expert in the two arenas */
+  long *off13 = (long *)malloc(sizeof(long) * (size_t)E);
+  long *off2 = (long *)malloc(sizeof(long) * (size_t)E);
+  long a13 = 0, a2 = 0;
+  for (int e = 0; e < E; ++e) {
+    off13[e] = a13;
+    off2[e] = a2;
+    a13 += 2L * (hidden / 16) * (inter / 16) * 16 * K13[e];
+    a2 += (long)(inter / 16) * (hidden / 16) * 16 * K2[e];
+  }
   char *need = (char *)calloc((size_t)E, 1);
   for (int i = 0; i < n_tok; ++i) {
-    if (tok[i] < 0 || tok[i] >= T) { free(need); return OR_ERR_SHAPE; }
+    if (tok[i] < 0 || tok[i] >= T) { free(need); free(off13); free(off2); return OR_ERR_SHAPE; }
     for (int s = 0; s < topk; ++s) {
       int e = ids[(long)tok[i] * topk + s];
-      if (e < 0 || e >= E) { free(need); return OR_ERR_SHAPE; }
+      if (e < 0 || e >= E) { free(need); free(off13); free(off2); return OR_ERR_SHAPE; }
       need[e] = 1;
     }
   }
@@ -477,12 +493,13 @@ int or_moe(const uint16_t *x, int T, int hidden, const int32_t *ids, const float
   uint16_t **Wd = (uint16_t **)calloc((size_t)E, sizeof(uint16_t *));
   for (int e = 0; e < E; ++e) {
     if (!need[e]) continue;
+    long slot13 = (long)(hidden / 16) * (inter / 16) * 16 * K13[e];
     Wg[e] = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)hidden * inter);
     Wu[e] = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)hidden * inter);
     Wd[e] = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)inter * hidden);
-    or_reconstruct(w13_trellis + (2L * e + 0) * w13_slot, hidden, inter, K13, Wg[e]);
-    or_reconstruct(w13_trellis + (2L * e + 1) * w13_slot, hidden, inter, K13, Wu[e]);
-    or_reconstruct(w2_trellis + (long)e * w2_slot, inter, hidden, K2, Wd[e]);
+    or_reconstruct(w13_trellis + off13[e], hidden, inter, K13[e], Wg[e]);
+    or_reconstruct(w13_trellis + off13[e] + slot13, hidden, inter, K13[e], Wu[e]);
+    or_reconstruct(w2_trellis + off2[e], inter, hidden, K2[e], Wd[e]);
   }
 #pragma omp parallel for schedule(dynamic)
   for (int i = 0; i < n_tok; ++i) {
@@ -508,6 +525,25 @@ int or_moe(const uint16_t *x, int T, int hidden, const int32_t *ids, const float
     free(g); free(u); free(h); free(d);
   }
   for (int e = 0; e < E; ++e) { free(Wg[e]); free(Wu[e]); free(Wd[e]); }
-  free(Wg); free(Wu); free(Wd); free(need);
+  free(Wg); free(Wu); free(Wd); free(need); free(off13); free(off2);
   return OR_OK;
+}
+
+/* One width for all experts of each projection kind: the arenas are
+ * [E][nslots][k/16][n/16][16K], the packed layout above with equal sizes. */
+int or_moe(const uint16_t *x, int T, int hidden, const int32_t *ids, const float *weights,
+           int topk, int E,
+           const uint16_t *w13_trellis, const uint16_t *w13_suh, const uint16_t *w13_svh,
+           int inter, int K13,
+           const uint16_t *w2_trellis, const uint16_t *w2_suh, const uint16_t *w2_svh, int K2,
+           const int32_t *tok, int n_tok, double *y /* [n_tok][hidden] */) {
+  if (K13 < 1 || K13 > 8 || K2 < 1 || K2 > 8) return OR_ERR_BITS;
+  if (E < 1) return OR_ERR_SHAPE;
+  int32_t *k13 = (int32_t *)malloc(sizeof(int32_t) * (size_t)E);
+  int32_t *k2 = (int32_t *)malloc(sizeof(int32_t) * (size_t)E);
+  for (int e = 0; e < E; ++e) { k13[e] = K13; k2[e] = K2; }
+  int rc = or_moe_k(x, T, hidden, ids, weights, topk, E, w13_trellis, w13_suh, w13_svh, inter, k13,
+                    w2_trellis, w2_suh, w2_svh, k2, tok, n_tok, y);
+  free(k13); free(k2);
+  return rc;
 }

@@ -375,3 +375,53 @@ def test_moe_token_sampling_matches_full():
     full = oracle.moe(c.x, c.ids, c.weights, *args)
     part = oracle.moe(c.x, c.ids, c.weights, *args, tokens=[4, 1])
     assert np.array_equal(part, full[[4, 1]])
+
+
+# ------------------------------------------------ MoE with per-expert widths --
+
+def _mixed_dense_expert(c, e):
+    """Dense effective (gate, up, down) of expert e of a mixed-width case: the
+    expert's tensors are cut out of the flat arenas at offsets summed here
+    from the widths, then dequantised and wrapped in scipy Hadamards."""
+    h, i = c.hidden, c.inter
+    mats = []
+    for proj, slot, k, n in ((c.w13, 0, h, i), (c.w13, 1, h, i), (c.w2, 0, i, h)):
+        sizes = [proj.nslots * (k // 16) * (n // 16) * 16 * int(w) for w in proj.K]
+        start = int(np.sum(sizes[:e])) + slot * sizes[e] // proj.nslots
+        K = int(proj.K[e])
+        words = proj.trellis[start:start + (k // 16) * (n // 16) * 16 * K].reshape(k // 16, n // 16, 16 * K)
+        W = oracle.reconstruct(words, k, n, K).astype(np.float64)
+        mats.append(np.diag(proj.suh[e, slot].astype(np.float64)) @ block_hadamard(k) @ W
+                    @ block_hadamard(n) @ np.diag(proj.svh[e, slot].astype(np.float64)))
+    return mats
+
+
+def test_moe_mixed_widths_match_dense_composition():
+    """Per-expert widths: every expert decoded at its own K from its own place
+    in the packed arena, composed with scipy's logistic function."""
+    c = synth.mixed_moe_case(97, 0, 3, [1, 3, 8, 3], [2, 5, 4, 7], topk=2, hidden=256, inter=128)
+    got = oracle.moe_k(c.x, c.ids, c.weights, c.w13.trellis, c.w13.suh, c.w13.svh, c.w13.K,
+                       c.w2.trellis, c.w2.suh, c.w2.svh, c.w2.K, c.inter)
+    ref = np.zeros((c.T, c.hidden))
+    for t in range(c.T):
+        xt = c.x[t].astype(np.float64)
+        for s_ in range(c.topk):
+            G, U, D = _mixed_dense_expert(c, int(c.ids[t, s_]))
+            g, u = xt @ G, xt @ U
+            ref[t] += float(c.weights[t, s_]) * ((g * scipy.special.expit(g) * u) @ D)
+    assert np.max(np.abs(got - ref)) <= 1e-9 * np.abs(ref).max()
+
+
+def test_moe_mixed_with_equal_widths_is_the_uniform_definition():
+    """Equal widths in the packed arena are the [E][nslots][k/16][n/16][16K]
+    layout, so the two entry points must agree exactly."""
+    c = _moe_small(5, T=4, E=5, topk=3, K=4)
+    base = oracle.moe(c.x, c.ids, c.weights, c.w13.trellis, c.w13.suh, c.w13.svh, 4,
+                      c.w2.trellis, c.w2.suh, c.w2.svh, 4)
+    K = np.full(c.E, 4, dtype=np.int32)
+    mixed = oracle.moe_k(c.x, c.ids, c.weights, c.w13.trellis.reshape(-1), c.w13.suh, c.w13.svh, K,
+                         c.w2.trellis.reshape(-1), c.w2.suh, c.w2.svh, K, c.inter)
+    assert np.array_equal(base, mixed)
+    with pytest.raises(ValueError):
+        oracle.moe_k(c.x, c.ids, c.weights, c.w13.trellis.reshape(-1)[:-16], c.w13.suh, c.w13.svh, K,
+                     c.w2.trellis.reshape(-1), c.w2.suh, c.w2.svh, K, c.inter)
