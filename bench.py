@@ -423,10 +423,33 @@ def bench_extras(only=None, moe_tokens=None):
                         "unique_weight_GBs": round(used * per_expert / (ms * 1e-3) / 1e9, 1),
                         "tflops": round(flops / (ms * 1e-3) / 1e12, 2)}
         del d
+    # per-expert widths: the same shape with experts 0-127 at K = 3 and
+    # 128-255 at K = 4 (down the other way round), two runs per projection
+    mixed = {}
+    for T in ((moe_tokens or (1, 128)) if only in (None, "moe") else ()):
+        K13, K2 = [3] * 128 + [4] * 128, [4] * 128 + [3] * 128
+        c = synth.mixed_moe_case(59, 10 + T, T, K13, K2)
+        d = dict(x=dev(c.x), ids=dev(c.ids), w=dev(c.weights), t13=dev(c.w13.trellis), s13=dev(c.w13.suh),
+                 v13=dev(c.w13.svh), t2=dev(c.w2.trellis), s2=dev(c.w2.suh), v2=dev(c.w2.svh))
+        w13 = tq.expert_proj_mixed(d["t13"], d["s13"], d["v13"], K13, c.hidden, c.inter)
+        w2 = tq.expert_proj_mixed(d["t2"], d["s2"], d["v2"], K2, c.inter, c.hidden)
+        ws = tq.workspace(tq.exl3_moe_mixed_workspace_size(T, c.topk, c.E, w13, w2))
+        y = torch.empty((T, c.hidden), dtype=torch.float16, device="cuda")
+        ms = _timed(lambda: tq.exl3_moe_grouped_mixed(d["x"], d["ids"], d["w"], w13, w2, c.E, y=y,
+                                                      workspace_buf=ws), reps=3)
+        used = np.unique(c.ids)
+        words13 = [2 * (c.hidden // 16) * (c.inter // 16) * 16 * K for K in K13]
+        words2 = [(c.inter // 16) * (c.hidden // 16) * 16 * K for K in K2]
+        ubytes = 2 * sum(words13[e] + words2[e] for e in used)
+        mixed[f"T{T}"] = {"ms": round(ms, 4), "experts_hit": len(used),
+                          "unique_weight_GBs": round(ubytes / (ms * 1e-3) / 1e9, 1)}
+        del d
     return {"small_m_k5120_n17408": small, "row_invariant_k5120_n17408": inv, "moe_E256_top8_h2048_i512_K3": moe,
+            "moe_mixed_E256_top8_h2048_i512_K3K4": mixed,
             "note": "small M: trellis decoded into tcgen05 operands (one fused kernel after the input RHT); "
                     "MoE: device remap + gather/RHT + two grouped tcgen05 kernels decoding the experts' trellis "
-                    "on the fly + fixed-order combine"}
+                    "on the fly + fixed-order combine; mixed widths: the tile kernels once per run of equal "
+                    "width (two runs here), for every token count"}
 
 
 # ------------------------------------------------------------------------- oracle

@@ -248,6 +248,43 @@ int exl3_moe_grouped(const uint16_t *x, int T, int hidden,
                      void *workspace, size_t ws_bytes, exl3_stream_t stream);
 
 /*
+ * Routed experts with a width per expert ("EXL3 checkpoints on the native
+ * engine (tracker) #832": widths 1..8 per tensor, and per-expert widths stay
+ * in the representation).  Same computation as exl3_moe_grouped; each
+ * projection kind has one width per expert instead of one for all.
+ *   trellis  one packed arena per projection kind: expert e's nslots tensors
+ *            ([k/16][n/16][16*K[e]] uint16 each) follow expert e-1's, so
+ *            expert e starts sum_{e' < e} nslots*(k/16)*(n/16)*16*K[e'] words
+ *            in (always a multiple of 16 bytes);
+ *   suh, svh [E][nslots][k], [E][nslots][n] fp16 as for exl3_moe_grouped;
+ *   K        HOST array of E widths (1..8), read during the call only.
+ * Each maximal run of consecutive experts with one width gets its own
+ * grouped launch per projection (over that run's experts; tiles of other
+ * experts are skipped), so the call costs about one launch per run on top of
+ * the work: number the experts so that equal widths are consecutive (the
+ * arena order is the caller's; router ids index it).  Every token count runs
+ * the tile kernels (the few-token GEMV path of exl3_moe_grouped is not used).
+ * Routing, invalid ids, workspace rules and the output are as for
+ * exl3_moe_grouped; the workspace size comes from
+ * exl3_moe_mixed_workspace_size.
+ */
+typedef struct {
+  const uint16_t *trellis;  /* packed arena, expert e right after expert e-1 */
+  const uint16_t *suh;      /* [E][nslots][k] fp16 */
+  const uint16_t *svh;      /* [E][nslots][n] fp16 */
+  const int32_t *K;         /* HOST [E] widths */
+  int k, n, codebook, nslots;
+} exl3_expert_proj_mixed;
+
+size_t exl3_moe_mixed_workspace_size(int T, int topk, int E, const exl3_expert_proj_mixed *w13,
+                                     const exl3_expert_proj_mixed *w2);
+int exl3_moe_grouped_mixed(const uint16_t *x, int T, int hidden,
+                           const int32_t *topk_ids, const float *topk_weights, int topk, int E,
+                           const exl3_expert_proj_mixed *w13, const exl3_expert_proj_mixed *w2,
+                           void *y, int out_dtype,
+                           void *workspace, size_t ws_bytes, exl3_stream_t stream);
+
+/*
  * exl3_linear_gemv_noalloc -- the M = 1 linear (the same fused GEMV, with
  * the same result, as exl3_linear with M = 1) for callers that cannot
  * allocate device memory.  The source pages have no counterpart: this is an

@@ -102,6 +102,35 @@ def test_linear_bias_argument_errors():
     assert L.exl3_linear_int8_bias(*i8(K=9)) == tq.EXL3_ERR_BITS
 
 
+def test_moe_mixed_argument_errors():
+    """Per-expert widths are checked on the host before anything is launched."""
+    L = tq.lib()
+    E = 4
+    Pi = ctypes.POINTER(ctypes.c_int32)
+    K13 = (ctypes.c_int32 * E)(3, 3, 4, 4)
+    K2 = (ctypes.c_int32 * E)(2, 2, 2, 9)        # expert 3: width 9
+    w13 = tq.ExpertProjMixed(FAKE.value, FAKE.value, FAKE.value, ctypes.cast(K13, Pi), 256, 128, 2, 2)
+    w2 = tq.ExpertProjMixed(FAKE.value, FAKE.value, FAKE.value, ctypes.cast(K2, Pi), 128, 256, 2, 1)
+    call = lambda wsb=1 << 26: L.exl3_moe_grouped_mixed(FAKE, 3, 256, FAKE, FAKE, 2, E, ctypes.byref(w13),
+                                                       ctypes.byref(w2), FAKE, 0, FAKE, wsb, None)
+    assert call() == tq.EXL3_ERR_BITS and "w2.K[3]" in _err(L)
+    K2[3] = 2
+    need = L.exl3_moe_mixed_workspace_size(3, 2, E, ctypes.byref(w13), ctypes.byref(w2))
+    assert need > 0
+    assert call(wsb=need - 1) == tq.EXL3_ERR_WORKSPACE
+    w13.codebook = 1
+    assert call() == tq.EXL3_ERR_CODEBOOK
+    w13.codebook = 2
+    w13.nslots = 1
+    assert call() == tq.EXL3_ERR_SHAPE
+    w13.nslots = 2
+    w13.K = None
+    assert call() == tq.EXL3_ERR_ARG
+    w13.K = ctypes.cast(K13, Pi)
+    w2.trellis = FAKE_MIS.value
+    assert call() == tq.EXL3_ERR_ARG
+
+
 def test_input_rht_argument_errors():
     L = tq.lib()
     assert L.exl3_input_rht(FAKE, 1, 100, FAKE, FAKE, 1, None) == tq.EXL3_ERR_SHAPE

@@ -46,6 +46,14 @@ class ExpertProj(ctypes.Structure):
                 ("nslots", ctypes.c_int)]
 
 
+class ExpertProjMixed(ctypes.Structure):
+    """exl3_expert_proj_mixed: one projection kind with a width per expert
+    (device trellis/suh/svh, host widths K[E])."""
+    _fields_ = [("trellis", ctypes.c_void_p), ("suh", ctypes.c_void_p), ("svh", ctypes.c_void_p),
+                ("K", ctypes.POINTER(ctypes.c_int32)), ("k", ctypes.c_int), ("n", ctypes.c_int),
+                ("codebook", ctypes.c_int), ("nslots", ctypes.c_int)]
+
+
 class Exl3Error(RuntimeError):
     def __init__(self, code: int, msg: str):
         super().__init__(f"libexl3 error {code}: {msg}")
@@ -83,6 +91,9 @@ def lib():
         L.exl3_moe_workspace_size.restype = Z
         L.exl3_moe_grouped.argtypes = [P, I, I, P, P, I, I, P, P, P, I, P, Z, P]
         L.exl3_linear_gemv_noalloc.argtypes = [P, I, I, P, P, P, I, I, P, I, P]
+        L.exl3_moe_mixed_workspace_size.argtypes = [I, I, I, P, P]
+        L.exl3_moe_mixed_workspace_size.restype = Z
+        L.exl3_moe_grouped_mixed.argtypes = [P, I, I, P, P, I, I, P, P, P, I, P, Z, P]
         L.exl3_set_weight_prefetch.argtypes = [I]
         L.exl3_set_weight_prefetch.restype = I
         L.exl3_set_row_invariant.argtypes = [I]
@@ -297,6 +308,39 @@ def exl3_moe_grouped(x, topk_ids, topk_weights, w13: ExpertProj, w2: ExpertProj,
                                   _ptr(topk_weights, "topk_weights", 4), topk, E, ctypes.byref(w13),
                                   ctypes.byref(w2), _ptr(y, "y"), out_dtype, _ptr(ws, "workspace"),
                                   ws.numel() * ws.element_size(), _stream(stream)))
+    return y
+
+
+def expert_proj_mixed(trellis, suh, svh, K, k: int, n: int, codebook: int = EXL3_CB_MUL1) -> ExpertProjMixed:
+    """Descriptor of a mixed-width projection arena: trellis flat (expert e's
+    slots right after expert e-1's), suh [E, nslots, k], svh [E, nslots, n]
+    (CUDA tensors kept alive by the caller), K the E widths (host)."""
+    E, nslots, _ = suh.shape
+    widths = (ctypes.c_int32 * E)(*[int(w) for w in K])
+    d = ExpertProjMixed(_ptr(trellis, "trellis", 2).value, _ptr(suh, "suh", 2).value, _ptr(svh, "svh", 2).value,
+                        ctypes.cast(widths, ctypes.POINTER(ctypes.c_int32)), k, n, codebook, nslots)
+    d._widths = widths   # keep the host array alive with the descriptor
+    return d
+
+
+def exl3_moe_mixed_workspace_size(T: int, topk: int, E: int, w13: ExpertProjMixed, w2: ExpertProjMixed) -> int:
+    return lib().exl3_moe_mixed_workspace_size(T, topk, E, ctypes.byref(w13), ctypes.byref(w2))
+
+
+def exl3_moe_grouped_mixed(x, topk_ids, topk_weights, w13: ExpertProjMixed, w2: ExpertProjMixed, E: int,
+                           out_dtype: int = EXL3_OUT_F16, y=None, workspace_buf=None, stream=None) -> torch.Tensor:
+    """Routed-expert contribution y [T, hidden] with a width per expert."""
+    T, hidden = x.shape
+    topk = topk_ids.shape[1]
+    if y is None:
+        y = torch.empty((T, hidden), dtype=torch.float32 if out_dtype == EXL3_OUT_F32 else torch.float16,
+                        device=x.device)
+    need = exl3_moe_mixed_workspace_size(T, topk, E, w13, w2)
+    ws = workspace_buf if workspace_buf is not None else workspace(need, x.device, stream)
+    _check(lib().exl3_moe_grouped_mixed(_ptr(x, "x", 2), T, hidden, _ptr(topk_ids, "topk_ids", 4),
+                                        _ptr(topk_weights, "topk_weights", 4), topk, E, ctypes.byref(w13),
+                                        ctypes.byref(w2), _ptr(y, "y"), out_dtype, _ptr(ws, "workspace"),
+                                        ws.numel() * ws.element_size(), _stream(stream)))
     return y
 
 

@@ -7,6 +7,7 @@
 #include <cstdio>
 #include <cstring>
 #include <string>
+#include <vector>
 
 #include "exl3_common.cuh"
 
@@ -56,11 +57,13 @@ cudaError_t exl3_launch_moe_gemv(const uint16_t *x, const float *act_in, int *po
 int exl3_launch_moe_fused_gateup(const uint16_t *xg, const uint16_t *xu, int U, int hidden, int inter, int K, int E,
                                  const uint16_t *w13_trellis, const int *mtiles, const int *n_mtiles, int max_mtiles,
                                  const uint16_t *svh13, const uint16_t *suh2, uint16_t *hout, int splits,
-                                 float *partials, int *counters, int *err, cudaStream_t s);
+                                 float *partials, int *counters, int *err, cudaStream_t s, int e_lo = 0,
+                                 int e_cnt = -1);
 int exl3_launch_moe_fused_down(const uint16_t *hin, int U, int hidden, int inter, int K, int E,
                                const uint16_t *w2_trellis,
                                const int *mtiles, const int *n_mtiles, int max_mtiles, const uint16_t *svh2,
-                               const float *weights, const int *perm, float *dout, int *err, cudaStream_t s);
+                               const float *weights, const int *perm, float *dout, int *err, cudaStream_t s,
+                               int e_lo = 0, int e_cnt = -1);
 
 // ---------------------------------------------------------------- errors --
 
@@ -222,10 +225,12 @@ struct MoeWs {
 // launch per projection, no sort) runs instead of the tensor-core tiles.
 constexpr int kMoeGemvMaxU = 32;
 
-MoeWs moe_ws(int T, int topk, int E, int hidden, int inter, int K13, int K2) {
+// allow_gemv = false keeps every token count on the tile kernels (the
+// mixed-width call, whose runs of equal width each need their own launch).
+MoeWs moe_ws(int T, int topk, int E, int hidden, int inter, int K13, int K2, bool allow_gemv = true) {
   MoeWs w{};
   const size_t U = (size_t)T * topk;
-  {
+  if (allow_gemv) {
     int g1 = 0, g2 = 0, b1 = 0, b2 = 0;
     size_t p1 = 0, p2 = 0;
     if (U <= (size_t)kMoeGemvMaxU && exl3_moe_gemv_plan((int)U, 2, hidden, inter, K13, &g1, &p1, &b1) &&
@@ -293,6 +298,41 @@ int check_moe(int T, int hidden, int topk, int E, const exl3_expert_proj *w13, c
   if (hidden <= 0 || inter <= 0 || hidden % 256 || inter % 128)
     return exl3_fail(EXL3_ERR_SHAPE, "hidden = %d must be a multiple of 256 and inter = %d of 128", hidden, inter);
   return EXL3_OK;
+}
+
+// Runs of equal width in expert order: [e_lo, e_lo + cnt) of width K, whose
+// trellis starts `words` uint16 words into the arena.
+struct WidthRun {
+  int e_lo, cnt, K;
+  size_t words;
+};
+
+int check_mixed_proj(const exl3_expert_proj_mixed *p, const char *name, int E, int nslots, int k, int n) {
+  if (!p) return exl3_fail(EXL3_ERR_ARG, "%s descriptor is NULL", name);
+  EXL3_TRY(check_ptr(p->trellis, "trellis"));
+  EXL3_TRY(check_ptr(p->suh, "suh"));
+  EXL3_TRY(check_ptr(p->svh, "svh"));
+  if (!p->K) return exl3_fail(EXL3_ERR_ARG, "%s.K (host array of %d widths) is NULL", name, E);
+  EXL3_TRY(check_bits_codebook(1, p->codebook));
+  for (int e = 0; e < E; ++e)
+    if (p->K[e] < 1 || p->K[e] > 8)
+      return exl3_fail(EXL3_ERR_BITS, "%s.K[%d] = %d outside 1..8", name, e, p->K[e]);
+  if (p->nslots != nslots || p->k != k || p->n != n)
+    return exl3_fail(EXL3_ERR_SHAPE, "%s is %d slots of %d -> %d, expected %d slots of %d -> %d", name, p->nslots,
+                     p->k, p->n, nslots, k, n);
+  return EXL3_OK;
+}
+
+std::vector<WidthRun> width_runs(const exl3_expert_proj_mixed *p, int E) {
+  std::vector<WidthRun> runs;
+  const size_t per_bit = (size_t)p->nslots * (p->k / 16) * (p->n / 16) * 16;   // words per expert per bit of width
+  size_t off = 0;
+  for (int e = 0; e < E; ++e) {
+    if (runs.empty() || runs.back().K != p->K[e]) runs.push_back(WidthRun{e, 0, p->K[e], off});
+    ++runs.back().cnt;
+    off += per_bit * (size_t)p->K[e];
+  }
+  return runs;
 }
 
 int check_workspace(const void *ws, size_t have, size_t need) {
@@ -584,6 +624,63 @@ int exl3_moe_grouped(const uint16_t *x, int T, int hidden, const int32_t *topk_i
                                         stream));
   EXL3_TRY(exl3_launch_moe_fused_down(h, U, hidden, inter, w2->K, E, w2->trellis, mtiles, n_mtiles, L.grid_mtiles,
                                       w2->svh, topk_weights, perm, d, err, stream));
+  return exl3_cuda_check(exl3_launch_moe_combine(d, pos, T, topk, hidden, y, out_dtype == EXL3_OUT_F32, stream),
+                         "moe combine launch");
+}
+
+size_t exl3_moe_mixed_workspace_size(int T, int topk, int E, const exl3_expert_proj_mixed *w13,
+                                     const exl3_expert_proj_mixed *w2) {
+  if (!w13 || !w2 || T < 1 || topk < 1 || E < 1 || E > 1024) return 0;
+  return moe_ws(T, topk, E, w13->k, w13->n, 1, 1, false).total;
+}
+
+int exl3_moe_grouped_mixed(const uint16_t *x, int T, int hidden, const int32_t *topk_ids,
+                           const float *topk_weights, int topk, int E, const exl3_expert_proj_mixed *w13,
+                           const exl3_expert_proj_mixed *w2, void *y, int out_dtype, void *workspace,
+                           size_t ws_bytes, exl3_stream_t stream) {
+  g_last_error.clear();
+  EXL3_TRY(check_ptr(x, "x"));
+  EXL3_TRY(check_ptr(topk_ids, "topk_ids"));
+  EXL3_TRY(check_ptr(topk_weights, "topk_weights"));
+  EXL3_TRY(check_ptr(y, "y"));
+  if (!w13 || !w2) return exl3_fail(EXL3_ERR_ARG, "w13 / w2 descriptor is NULL");
+  if (T < 1 || topk < 1 || E < 1 || E > 1024 || (int64_t)T * topk > (1 << 24))
+    return exl3_fail(EXL3_ERR_SHAPE, "T = %d, topk = %d, E = %d out of range (E <= 1024)", T, topk, E);
+  const int inter = w13->n;
+  if (hidden <= 0 || inter <= 0 || hidden % 256 || inter % 128)
+    return exl3_fail(EXL3_ERR_SHAPE, "hidden = %d must be a multiple of 256 and inter = %d of 128", hidden, inter);
+  EXL3_TRY(check_mixed_proj(w13, "w13", E, 2, hidden, inter));
+  EXL3_TRY(check_mixed_proj(w2, "w2", E, 1, inter, hidden));
+  if (out_dtype != EXL3_OUT_F16 && out_dtype != EXL3_OUT_F32)
+    return exl3_fail(EXL3_ERR_ARG, "out_dtype %d invalid", out_dtype);
+  const int U = T * topk;
+  const MoeWs L = moe_ws(T, topk, E, hidden, inter, 1, 1, false);
+  EXL3_TRY(check_workspace(workspace, ws_bytes, L.total));
+  int *err = at<int>(workspace, 0);
+  int *counts = at<int>(workspace, L.counts), *offsets = at<int>(workspace, L.offsets);
+  int *pos = at<int>(workspace, L.pos), *perm = at<int>(workspace, L.perm);
+  int *mtiles = at<int>(workspace, L.mtiles), *chunk_tab = at<int>(workspace, L.chunk);
+  int *n_mtiles = at<int>(workspace, L.n_mtiles);
+  uint16_t *xg = at<uint16_t>(workspace, L.xg), *xu = at<uint16_t>(workspace, L.xu);
+  uint16_t *h = at<uint16_t>(workspace, L.h);
+  float *d = at<float>(workspace, L.d);
+  // routing, gather and combine as in exl3_moe_grouped; each projection runs
+  // one grouped launch per run of equal width, over that run's experts only
+  EXL3_TRY(exl3_cuda_check(exl3_launch_moe_remap(topk_ids, U, E, counts, offsets, perm, pos, mtiles,
+                                                 n_mtiles, L.max_mtiles, chunk_tab, err, stream),
+                           "moe remap launch"));
+  EXL3_TRY(exl3_cuda_check(exl3_launch_moe_gather(x, U, hidden, topk, perm, offsets, E, topk_ids, w13->suh, xg, xu,
+                                                  stream),
+                           "moe gather launch"));
+  float *partials = L.splits > 1 ? at<float>(workspace, L.partials) : nullptr;
+  int *counters = at<int>(workspace, kCounterOff);
+  for (const WidthRun &r : width_runs(w13, E))
+    EXL3_TRY(exl3_launch_moe_fused_gateup(xg, xu, U, hidden, inter, r.K, E, w13->trellis + r.words, mtiles, n_mtiles,
+                                          L.grid_mtiles, w13->svh, w2->suh, h, L.splits, partials, counters, err,
+                                          stream, r.e_lo, r.cnt));
+  for (const WidthRun &r : width_runs(w2, E))
+    EXL3_TRY(exl3_launch_moe_fused_down(h, U, hidden, inter, r.K, E, w2->trellis + r.words, mtiles, n_mtiles,
+                                        L.grid_mtiles, w2->svh, topk_weights, perm, d, err, stream, r.e_lo, r.cnt));
   return exl3_cuda_check(exl3_launch_moe_combine(d, pos, T, topk, hidden, y, out_dtype == EXL3_OUT_F32, stream),
                          "moe combine launch");
 }

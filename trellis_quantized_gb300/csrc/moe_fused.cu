@@ -92,6 +92,9 @@ struct Args {
   int ntc;                  // output tiles per CTA (phase 2: 1 or 2)
   float *partials;          // [tiles][splits][2][128][128] fp32
   int *counters;            // [tiles], zero between calls
+  // experts [e_lo, e_hi) only: the trellis map covers just their arena
+  // (row 0 = expert e_lo) and tiles of other experts are left to other launches
+  int e_lo, e_hi;
 };
 
 template <int K, int PHASE>
@@ -110,6 +113,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1) moe_fused_kernel(const __grid_
   if (tile >= *a.n_mtiles * NTG) return;   // uniform per CTA: the tile list is device-side
   const int4 mt = a.mtiles[tile / NTG];
   const int nt0 = (tile % NTG) * ntc, nts = min(ntc, a.NT - nt0), e = mt.x, row0 = mt.y, rows = mt.z;
+  if (e < a.e_lo || e >= a.e_hi) return;   // uniform per CTA: another launch's expert
+  const int et = e - a.e_lo;                // the expert's place in this launch's trellis map
   const int KB = a.KB;
   // this CTA's pairs: absolute pair P0 + P for P < npairs (P0 even, so a
   // trellis stage still holds pairs 2j, 2j + 1 of the range; with two tiles
@@ -183,11 +188,11 @@ __global__ void __launch_bounds__(kWarps * 32, 1) moe_fused_kernel(const __grid_
 #pragma unroll
           for (int p = 0; p < 2; ++p)
             tc::tma_load_2d(sT + st * C::T_STAGE + p * 8 * C::ROWB, &tmT, &tfull[st], nt0 * (BN / 16) * (4 * K),
-                            (e * a.nslots + p) * a.tiles_k + 4 * P0 + 8 * j);
+                            (et * a.nslots + p) * a.tiles_k + 4 * P0 + 8 * j);
         } else {
           const int jt = (2 * j) / nptile, js = j - jt * (nptile / 2);   // tile, stage within its k
           tc::tma_load_2d(sT + st * C::T_STAGE, &tmT, &tfull[st], (nt0 + jt) * (BN / 16) * (4 * K),
-                          e * a.tiles_k + 16 * js);
+                          et * a.tiles_k + 16 * js);
         }
       }
     }
@@ -509,16 +514,24 @@ static int mf_launch(int K, const CUtensorMap &t0, const CUtensorMap &t1, const 
 // Phase 1: xg, xu [U][hidden] fp16 sorted rows; w13 trellis [E][2][hidden/16][inter/16][16K].
 // splits > 1 (k split of the gate+up projection): partials [max_mtiles * inter/128][splits][2][128][128]
 // fp32 and counters [max_mtiles * inter/128], zero on entry and left zero.
+// e_lo, e_cnt: only experts [e_lo, e_lo + e_cnt), whose trellis starts at
+// w13_trellis (e_cnt < 0: all E experts from 0).
 int exl3_launch_moe_fused_gateup(const uint16_t *xg, const uint16_t *xu, int U, int hidden, int inter, int K, int E,
                                  const uint16_t *w13_trellis, const int *mtiles, const int *n_mtiles, int max_mtiles,
                                  const uint16_t *svh13, const uint16_t *suh2, uint16_t *hout, int splits,
-                                 float *partials, int *counters, int *err, cudaStream_t s) {
+                                 float *partials, int *counters, int *err, cudaStream_t s, int e_lo, int e_cnt) {
+  if (e_cnt < 0) {
+    e_lo = 0;
+    e_cnt = E;
+  }
   CUtensorMap t0, t1, tt;
   int rc = mf_xmap(&t0, xg, U, hidden);
   if (!rc) rc = mf_xmap(&t1, xu, U, hidden);
-  if (!rc) rc = mf_tmap(&tt, w13_trellis, (long)E * 2 * (hidden / 16), inter, K, 8);
+  if (!rc) rc = mf_tmap(&tt, w13_trellis, (long)e_cnt * 2 * (hidden / 16), inter, K, 8);
   if (rc) return rc;
   mf::Args a{};
+  a.e_lo = e_lo;
+  a.e_hi = e_lo + e_cnt;
   a.mtiles = reinterpret_cast<const int4 *>(mtiles);
   a.n_mtiles = n_mtiles;
   a.NT = inter / 128;
@@ -538,10 +551,15 @@ int exl3_launch_moe_fused_gateup(const uint16_t *xg, const uint16_t *xu, int U, 
 }
 
 // Phase 2: h' [U][inter] fp16 sorted rows; w2 trellis [E][1][inter/16][hidden/16][16K]; d [U][hidden] fp32.
+// e_lo, e_cnt as for the gate+up launch.
 int exl3_launch_moe_fused_down(const uint16_t *hin, int U, int hidden, int inter, int K, int E,
                                const uint16_t *w2_trellis, const int *mtiles, const int *n_mtiles, int max_mtiles,
                                const uint16_t *svh2, const float *weights, const int *perm, float *dout, int *err,
-                               cudaStream_t s) {
+                               cudaStream_t s, int e_lo, int e_cnt) {
+  if (e_cnt < 0) {
+    e_lo = 0;
+    e_cnt = E;
+  }
   CUtensorMap t0, tt;
   // h' as (64 k, U rows, inter/64 blocks): one load brings two k steps of the tile's rows
   cuuint64_t dims[3] = {64, (cuuint64_t)U, (cuuint64_t)(inter / 64)};
@@ -549,9 +567,11 @@ int exl3_launch_moe_fused_down(const uint16_t *hin, int U, int hidden, int inter
   cuuint32_t box[3] = {64, (cuuint32_t)mf::XROWS, 2};
   int rc = mf_encode(&t0, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, hin, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
                      "h'");
-  if (!rc) rc = mf_tmap(&tt, w2_trellis, (long)E * (inter / 16), hidden, K, 16);
+  if (!rc) rc = mf_tmap(&tt, w2_trellis, (long)e_cnt * (inter / 16), hidden, K, 16);
   if (rc) return rc;
   mf::Args a{};
+  a.e_lo = e_lo;
+  a.e_hi = e_lo + e_cnt;
   a.mtiles = reinterpret_cast<const int4 *>(mtiles);
   a.n_mtiles = n_mtiles;
   a.NT = hidden / 128;
