@@ -249,8 +249,8 @@ int exl3_moe_grouped(const uint16_t *x, int T, int hidden,
 
 /*
  * Routed experts with a width per expert ("EXL3 checkpoints on the native
- * engine (tracker) #832": widths 1..8 per tensor, and per-expert widths stay
- * in the representation).  Same computation as exl3_moe_grouped; each
+ * engine (tracker) #832": widths 1..8 per tensor, and the Oct 17 comment keeps
+ * each expert's own width in the format).  Same computation as exl3_moe_grouped; each
  * projection kind has one width per expert instead of one for all.
  *   trellis  one packed arena per projection kind: expert e's nslots tensors
  *            ([k/16][n/16][16*K[e]] uint16 each) follow expert e-1's, so

@@ -453,8 +453,8 @@ static void lin_f64_in(const double *xin, int k, int n, const uint16_t *W,
  * are dequantised once per expert used.  Only the tokens listed in `tok`
  * (n_tok of them) are evaluated, so callers can sample a large batch.
  *
- * Per-expert widths ("EXL3 checkpoints on the native engine (tracker) #832":
- * per-expert widths stay in the representation): expert e of w13 has width
+ * Per-expert widths ("EXL3 checkpoints on the native engine (tracker) #832",
+ * comment of Oct 17: the format keeps each expert's own width): expert e of w13 has width
  * K13[e] and of w2 K2[e].  Each arena packs the experts in id order, expert
  * e's slots right after expert e-1's, so expert e starts at the sum of the
  * earlier experts' sizes (nslots * (k/16) * (n/16) * 16 * K words each).

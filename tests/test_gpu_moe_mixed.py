@@ -1,7 +1,7 @@
 """GPU parity of the routed experts with a width per expert
 (exl3_moe_grouped_mixed) against the CPU oracle ("EXL3 checkpoints on the
-native engine (tracker) #832": widths 1..8 per tensor; per-expert widths stay
-in the representation).
+native engine (tracker) #832": widths 1..8 per tensor, and the Oct 17 comment
+keeps each expert's own width in the format).
 
 Each projection's arena packs expert e right after expert e-1 at its own
 width; every run of consecutive equal widths is one grouped launch.  Outputs
