@@ -389,6 +389,44 @@ def bench_extras(only=None, moe_tokens=None):
         ms = _timed(lambda: tq.exl3_linear(x, t, suh, svh, 4, y=y, workspace_buf=ws))
         small[f"M{M}"] = {"ms": round(ms, 4), "GBs": round(linear_bytes(c) / (ms * 1e-3) / 1e9, 1),
                           "tflops": round(2.0 * M * c.k * c.n / (ms * 1e-3) / 1e12, 2)}
+    # fused shards: gate and up of the dense family (2 x k=5120 -> n=17408,
+    # K=4) at M = 1, as one grouped-GEMV launch and as two linears; two
+    # copies of the weights (178 MB, more than L2) alternate; weight
+    # prefetch on, as in a decode loop
+    shards = {}
+    if only in (None, "small"):
+        cs = [synth.linear_case(2, 80 + i, 1, 5120, 17408, 4) for i in range(4)]
+        x = dev(cs[0].x)
+        copies = []
+        for j in (0, 2):
+            copies.append((dev(np.stack([cs[j].trellis, cs[j + 1].trellis])), dev(np.stack([cs[j].suh, cs[j + 1].suh])),
+                           dev(np.stack([cs[j].svh, cs[j + 1].svh]))))
+        ys = torch.empty((2, 1, 17408), dtype=torch.float16, device="cuda")
+        ws = tq.workspace(max(tq.exl3_linear_shards_workspace_size(1, 5120, 17408, 4, 2),
+                              tq.exl3_linear_workspace_size(1, 5120, 17408, 4)))
+        prev = tq.exl3_set_weight_prefetch(True)
+        try:
+            turn = [0]
+
+            def fused():
+                t, su, sv = copies[turn[0] % 2]
+                turn[0] += 1
+                tq.exl3_linear_shards(x, t, su, sv, 4, y=ys, workspace_buf=ws)
+
+            def separate():
+                t, su, sv = copies[turn[0] % 2]
+                turn[0] += 1
+                for i in range(2):
+                    tq.exl3_linear(x, t[i], su[i], sv[i], 4, y=ys[i], workspace_buf=ws)
+
+            one = _timed(fused)
+            two = _timed(separate)
+        finally:
+            tq.exl3_set_weight_prefetch(prev)
+        gb = 2 * linear_bytes(cs[0]) / 1e9
+        shards = {"one_launch": {"ms": round(one, 4), "GBs": round(gb / (one * 1e-3), 1)},
+                  "two_linears": {"ms": round(two, 4), "GBs": round(gb / (two * 1e-3), 1)}}
+        del copies, x, ys
     # the row-invariant mode (every M through the 32-token-wide fused
     # kernel, 32 rows at a time): its cost against the default paths
     inv = {}
@@ -444,7 +482,8 @@ def bench_extras(only=None, moe_tokens=None):
         mixed[f"T{T}"] = {"ms": round(ms, 4), "experts_hit": len(used),
                           "unique_weight_GBs": round(ubytes / (ms * 1e-3) / 1e9, 1)}
         del d
-    return {"small_m_k5120_n17408": small, "row_invariant_k5120_n17408": inv, "moe_E256_top8_h2048_i512_K3": moe,
+    return {"small_m_k5120_n17408": small, "shards_gate_up_k5120_n17408x2_M1": shards,
+            "row_invariant_k5120_n17408": inv, "moe_E256_top8_h2048_i512_K3": moe,
             "moe_mixed_E256_top8_h2048_i512_K3K4": mixed,
             "note": "small M: trellis decoded into tcgen05 operands (one fused kernel after the input RHT); "
                     "MoE: device remap + gather/RHT + two grouped tcgen05 kernels decoding the experts' trellis "

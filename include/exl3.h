@@ -147,6 +147,33 @@ int exl3_linear_bias(const uint16_t *x, int M, int k, int n,
                      void *workspace, size_t ws_bytes, exl3_stream_t stream);
 
 /*
+ * exl3_linear_shards -- several linears over one input in one call: the
+ * fused shards of a layer ("exl3xpu" README, "Layout": the vLLM linear
+ * method handles fused shards), such as gate and up, or q, k and v when they
+ * have one width and shape.  The pages do not describe the fusion; here the
+ * shards keep their own suh and svh:
+ *   y[s] = RHT_out( RHT_in(x . suh[s]) @ W[s] ) . svh[s]   for s < nshards
+ *   x        [M][k] fp16
+ *   trellis  [nshards][k/16][n/16][16K] uint16 (the shards stacked)
+ *   suh      [nshards][k] fp16, svh [nshards][n] fp16
+ *   y        [nshards][M][n], fp16 (EXL3_OUT_F16) or fp32 (EXL3_OUT_F32):
+ *            shard-major, so at M = 1 the shards' outputs lie side by side
+ *   nshards  1..64; K, codebook as for exl3_linear
+ *   workspace of exl3_linear_shards_workspace_size(M, k, n, K, nshards) bytes.
+ * At M = 1 all shards run in one launch of the CUDA-core GEMV (each CTA
+ * takes an equal share of all shards' tile rows), unless a CTA's share would
+ * span more than four shards or the row-invariant mode is on; otherwise, and
+ * for M > 1, each shard runs as exl3_linear into its block of y.  Results
+ * are within the library's tolerance of exl3_linear on each shard; the
+ * one-launch GEMV splits the sums differently, so bits may differ.
+ */
+size_t exl3_linear_shards_workspace_size(int M, int k, int n, int K, int nshards);
+int exl3_linear_shards(const uint16_t *x, int M, int k, int n, int nshards,
+                       const uint16_t *trellis, const uint16_t *suh, const uint16_t *svh,
+                       int K, int codebook, void *y, int out_dtype,
+                       void *workspace, size_t ws_bytes, exl3_stream_t stream);
+
+/*
  * exl3_set_weight_prefetch -- let M = 1 calls of exl3_linear stream their
  * weights before the kernel launched ahead of them on the stream has
  * finished (CUDA programmatic dependent launch).  The source pages have no

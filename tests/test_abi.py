@@ -131,6 +131,26 @@ def test_moe_mixed_argument_errors():
     assert call() == tq.EXL3_ERR_ARG
 
 
+def test_linear_shards_argument_errors():
+    L = tq.lib()
+    args = lambda **kw: [FAKE, kw.get("M", 1), 256, kw.get("n", 256), kw.get("S", 2), FAKE, FAKE,
+                         kw.get("svh", FAKE), kw.get("K", 4), kw.get("cb", 2), FAKE, kw.get("od", 0), FAKE,
+                         kw.get("wsb", 1 << 24), None]
+    assert L.exl3_linear_shards(*args(S=0)) == tq.EXL3_ERR_SHAPE
+    assert L.exl3_linear_shards(*args(S=65)) == tq.EXL3_ERR_SHAPE
+    assert L.exl3_linear_shards(*args(n=100)) == tq.EXL3_ERR_SHAPE
+    assert L.exl3_linear_shards(*args(K=0)) == tq.EXL3_ERR_BITS
+    assert L.exl3_linear_shards(*args(cb=3)) == tq.EXL3_ERR_CODEBOOK
+    assert L.exl3_linear_shards(*args(od=2)) == tq.EXL3_ERR_ARG
+    assert L.exl3_linear_shards(*args(svh=FAKE_MIS)) == tq.EXL3_ERR_ARG
+    assert L.exl3_linear_shards(*args(wsb=64)) == tq.EXL3_ERR_WORKSPACE
+    # the workspace covers one shard's exl3_linear at every M
+    for M in (1, 7, 300):
+        assert L.exl3_linear_shards_workspace_size(M, 5120, 17408, 4, 2) >= L.exl3_linear_workspace_size(
+            M, 5120, 17408, 4)
+    assert L.exl3_linear_shards_workspace_size(1, 5120, 17408, 4, 0) == 0
+
+
 def test_input_rht_argument_errors():
     L = tq.lib()
     assert L.exl3_input_rht(FAKE, 1, 100, FAKE, FAKE, 1, None) == tq.EXL3_ERR_SHAPE

@@ -91,6 +91,9 @@ def lib():
         L.exl3_moe_workspace_size.restype = Z
         L.exl3_moe_grouped.argtypes = [P, I, I, P, P, I, I, P, P, P, I, P, Z, P]
         L.exl3_linear_gemv_noalloc.argtypes = [P, I, I, P, P, P, I, I, P, I, P]
+        L.exl3_linear_shards_workspace_size.argtypes = [I, I, I, I, I]
+        L.exl3_linear_shards_workspace_size.restype = Z
+        L.exl3_linear_shards.argtypes = [P, I, I, I, I, P, P, P, I, I, P, I, P, Z, P]
         L.exl3_moe_mixed_workspace_size.argtypes = [I, I, I, P, P]
         L.exl3_moe_mixed_workspace_size.restype = Z
         L.exl3_moe_grouped_mixed.argtypes = [P, I, I, P, P, I, I, P, P, P, I, P, Z, P]
@@ -221,6 +224,28 @@ def exl3_linear_bias(x, trellis, suh, svh, bias, K: int, codebook: int = EXL3_CB
     _check(lib().exl3_linear_bias(_ptr(x, "x", 2), M, k, n, _ptr(trellis, "trellis", 2), _ptr(suh, "suh", 2),
                                   _ptr(svh, "svh", 2), _ptr(bias, "bias", 2), K, codebook, _ptr(y, "y"), out_dtype,
                                   _ptr(ws, "workspace"), ws.numel() * ws.element_size(), _stream(stream)))
+    return y
+
+
+def exl3_linear_shards_workspace_size(M: int, k: int, n: int, K: int, nshards: int) -> int:
+    return lib().exl3_linear_shards_workspace_size(M, k, n, K, nshards)
+
+
+def exl3_linear_shards(x, trellis, suh, svh, K: int, codebook: int = EXL3_CB_MUL1, out_dtype: int = EXL3_OUT_F16,
+                       y=None, workspace_buf=None, stream=None) -> torch.Tensor:
+    """Fused shards over one input: trellis [S, k/16, n/16, 16K], suh [S, k], svh [S, n];
+    returns y [S, M, n]."""
+    M, k = x.shape
+    S = trellis.shape[0]
+    n = trellis.shape[2] * 16
+    if y is None:
+        y = torch.empty((S, M, n), dtype=torch.float32 if out_dtype == EXL3_OUT_F32 else torch.float16,
+                        device=x.device)
+    need = exl3_linear_shards_workspace_size(M, k, n, K, S)
+    ws = workspace_buf if workspace_buf is not None else workspace(need, x.device, stream)
+    _check(lib().exl3_linear_shards(_ptr(x, "x", 2), M, k, n, S, _ptr(trellis, "trellis", 2), _ptr(suh, "suh", 2),
+                                    _ptr(svh, "svh", 2), K, codebook, _ptr(y, "y"), out_dtype, _ptr(ws, "workspace"),
+                                    ws.numel() * ws.element_size(), _stream(stream)))
     return y
 
 

@@ -50,6 +50,10 @@ cudaError_t exl3_launch_moe_gather(const uint16_t *x, int U, int hidden, int top
 cudaError_t exl3_launch_moe_combine(const float *d, const int *pos, int T, int topk, int hidden, void *y,
                                     bool f32out, cudaStream_t s);
 bool exl3_moe_gemv_plan(int U, int nslots, int k, int n, int K, int *grid, size_t *partial_floats, int *blocks);
+bool exl3_gemv_shards_plan(int S, int k, int n, int K, int *grid, size_t *partial_floats, int *blocks);
+cudaError_t exl3_launch_gemv_shards(const uint16_t *x, int S, int k, int n, int K, const uint16_t *trellis,
+                                    const uint16_t *suh, const uint16_t *svh, void *y, bool f32out,
+                                    float *partials, int *counters, int *err, cudaStream_t s, bool prefetch);
 cudaError_t exl3_launch_moe_gemv(const uint16_t *x, const float *act_in, int *pos_out, const int32_t *ids,
                                  const float *weights, int U, int topk, int E, int nslots, int k, int n, int K,
                                  const uint16_t *trellis, const uint16_t *suh, const uint16_t *svh, float *y,
@@ -683,6 +687,63 @@ int exl3_moe_grouped_mixed(const uint16_t *x, int T, int hidden, const int32_t *
                                         L.grid_mtiles, w2->svh, topk_weights, perm, d, err, stream, r.e_lo, r.cnt));
   return exl3_cuda_check(exl3_launch_moe_combine(d, pos, T, topk, hidden, y, out_dtype == EXL3_OUT_F32, stream),
                          "moe combine launch");
+}
+
+// Fused shards: the one-launch plan at M = 1 (grid, partial floats), or
+// false when the shards take one exl3_linear each.
+static bool shards_one_launch(int M, int k, int n, int K, int S, size_t *floats) {
+  int grid = 0, blocks = 0;
+  size_t pf = 0;
+  if (M != 1 || g_row_invariant.load() != 0) return false;
+  if (!exl3_gemv_shards_plan(S, k, n, K, &grid, &pf, &blocks) || (size_t)blocks > kMaxCounters) return false;
+  if (floats) *floats = pf;
+  return true;
+}
+
+size_t exl3_linear_shards_workspace_size(int M, int k, int n, int K, int nshards) {
+  if (nshards < 1 || nshards > 64) return 0;
+  const size_t per = exl3_linear_workspace_size(M, k, n, K);
+  if (per == 0) return 0;
+  size_t pf = 0;
+  int grid = 0, blocks = 0;
+  size_t one = 0;
+  if (M == 1 && exl3_gemv_shards_plan(nshards, k, n, K, &grid, &pf, &blocks))
+    one = align_up(kDataOff + sizeof(float) * pf);
+  return per > one ? per : one;
+}
+
+int exl3_linear_shards(const uint16_t *x, int M, int k, int n, int nshards, const uint16_t *trellis,
+                       const uint16_t *suh, const uint16_t *svh, int K, int codebook, void *y, int out_dtype,
+                       void *workspace, size_t ws_bytes, exl3_stream_t stream) {
+  g_last_error.clear();
+  EXL3_TRY(check_ptr(x, "x"));
+  EXL3_TRY(check_ptr(trellis, "trellis"));
+  EXL3_TRY(check_ptr(suh, "suh"));
+  EXL3_TRY(check_ptr(svh, "svh"));
+  EXL3_TRY(check_ptr(y, "y"));
+  EXL3_TRY(check_bits_codebook(K, codebook));
+  EXL3_TRY(check_linear_shape(M, k, n));
+  if (nshards < 1 || nshards > 64) return exl3_fail(EXL3_ERR_SHAPE, "nshards = %d outside 1..64", nshards);
+  if (out_dtype != EXL3_OUT_F16 && out_dtype != EXL3_OUT_F32)
+    return exl3_fail(EXL3_ERR_ARG, "out_dtype %d invalid", out_dtype);
+  const size_t need = exl3_linear_shards_workspace_size(M, k, n, K, nshards);
+  EXL3_TRY(check_workspace(workspace, ws_bytes, need));
+  const bool f32 = out_dtype == EXL3_OUT_F32;
+  size_t pf = 0;
+  if (shards_one_launch(M, k, n, K, nshards, &pf)) {
+    return exl3_cuda_check(exl3_launch_gemv_shards(x, nshards, k, n, K, trellis, suh, svh, y, f32,
+                                                   at<float>(workspace, kDataOff), at<int>(workspace, kCounterOff),
+                                                   at<int>(workspace, 0), stream, g_weight_prefetch.load() != 0),
+                           "gemv shards launch");
+  }
+  // one linear per shard, each into its own [M][n] block of y
+  const size_t words = (size_t)(k / 16) * (n / 16) * 16 * K;
+  const size_t ybytes = (size_t)M * n * (f32 ? 4 : 2);
+  for (int sh = 0; sh < nshards; ++sh)
+    EXL3_TRY(linear_impl(x, M, k, n, trellis + sh * words, suh + (size_t)sh * k, svh + (size_t)sh * n, nullptr, K,
+                         codebook, static_cast<uint8_t *>(y) + sh * ybytes, out_dtype, workspace, ws_bytes,
+                         stream));
+  return EXL3_OK;
 }
 
 }  // extern "C"

@@ -66,8 +66,10 @@ struct GemvArgs {
   // follow those of op o - 1; op o multiplies x row (x_per_unit ? u : u / topk)
   // by expert e = ids[u]'s slot `slot` (trellis rows (e nslots + slot) k/16 of
   // one tensor over all experts, suh/svh [E][nslots][k or n]) into y[o][n]
-  // fp32, times weights[u] when weights is set.  An id outside [0, E) sets the
-  // error word and makes the op's output zero.
+  // (fp32, or fp16 when F32OUT is false), times weights[u] when weights is
+  // set.  An id outside [0, E) sets the error word and makes the op's output
+  // zero.  ids NULL: every unit uses expert 0 (the fused shards of one
+  // input, op o = shard o).
   const int32_t *ids;
   const float *weights;
   int topk, nslots, E, x_per_unit, nops;
@@ -94,13 +96,13 @@ struct GemvOp {
   bool bad;                 // invalid expert id
 };
 
-template <bool GROUPED>
+template <bool GROUPED, bool F32OUT>
 __device__ __forceinline__ GemvOp gemv_op(const GemvArgs &a, int o) {
   if constexpr (!GROUPED) {
     return GemvOp{a.x, a.suh, a.svh, a.y, 1.0f, 0, false};
   } else {
     const int u = o / a.nslots, slot = o - u * a.nslots;
-    int e = a.ids[u];
+    int e = a.ids ? a.ids[u] : 0;   // no id list: every unit uses expert 0 (fused shards)
     const bool bad = e < 0 || e >= a.E;
     float scale = a.weights ? a.weights[u] : 1.0f;
     if (bad) {
@@ -110,7 +112,7 @@ __device__ __forceinline__ GemvOp gemv_op(const GemvArgs &a, int o) {
     const long es = (long)e * a.nslots + slot;
     const long xr = a.x_per_unit ? u : u / a.topk;
     return GemvOp{a.x + xr * a.k, a.suh + es * a.k, a.svh + es * a.n,
-                  static_cast<float *>(a.y) + (long)o * a.n, scale, (int)(es * a.tiles_k), bad};
+                  static_cast<char *>(a.y) + (long)o * a.n * (F32OUT ? 4 : 2), scale, (int)(es * a.tiles_k), bad};
   }
 }
 
@@ -170,7 +172,7 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
         const int tk_first = (int)(t - c * TKU), nrows = (int)(seg_end - t);
         const int op = GROUPED ? (int)(c / (uint32_t)a.colblocks) : 0;
         const int tn0 = ((int)c - op * a.colblocks) * (S::CTA_COLS / 16);
-        const int trow = gemv_op<GROUPED>(a, op).trow + tk_first;
+        const int trow = gemv_op<GROUPED, F32OUT>(a, op).trow + tk_first;
         for (int r0 = 0; r0 < nrows && !*s_abort; r0 += S::R) {
           const int cnt = min(S::R, nrows - r0);
           if (issued++ == a.pre_stages) {
@@ -235,7 +237,7 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
       const int c = (int)(t / TKU);   // block: op c / colblocks, column block c % colblocks
       const uint32_t seg_end = min(t1, (uint32_t)(c + 1) * TKU);
       const int op = GROUPED ? c / a.colblocks : 0;
-      const GemvOp P = gemv_op<GROUPED>(a, op);
+      const GemvOp P = gemv_op<GROUPED, F32OUT>(a, op);
       const float *rs = rsum + (op - op0) * (a.k / 16);
       const int col0 = (c - op * a.colblocks) * S::CTA_COLS;
       const uint32_t blk_first = (uint32_t)c * TKU, blk_last = min((uint32_t)(c + 1) * TKU, a.total) - 1;
@@ -419,7 +421,7 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
     }
     for (int i = warp; i < nc; i += NCW) {
       const int jop = GROUPED ? i / KC : 0;               // op op0 + jop
-      const GemvOp P = gemv_op<GROUPED>(a, op0 + jop);
+      const GemvOp P = gemv_op<GROUPED, F32OUT>(a, op0 + jop);
       if (GROUPED && P.bad && lane == 0 && i % KC == 0) set_device_error(a.err, kErrExpertId);
       const int e0 = ((c0 + i - jop * KC) % KC) * 512 + lane * 16;
       const bool live = e0 < a.k;   // k is a multiple of 128: whole 8-lane groups
@@ -823,5 +825,72 @@ cudaError_t exl3_launch_moe_gemv(const uint16_t *x, const float *act_in, int *po
   // before that launch began) while gate and up finish, and reads their
   // outputs after griddepcontrol.wait.
   EXL3_K_SWITCH(K, e = Launcher<KK, true, true>::launch(tm, a, grid, s, act_in != nullptr));
+  return e;
+}
+
+// ---- fused shards: S linears of one input row, [S][k/16][n/16][16K]
+// trellis, suh [S][k], svh [S][n], y [S][n], in one launch of the grouped
+// GEMV (one unit, S slots, no expert ids).  False when a CTA's range would
+// touch more than kGemvMaxOps shards or x' for them does not fit.
+bool exl3_gemv_shards_plan(int S, int k, int n, int K, int *grid, size_t *partial_floats, int *blocks) {
+  return exl3_moe_gemv_plan(1, S, k, n, K, grid, partial_floats, blocks);
+}
+
+cudaError_t exl3_launch_gemv_shards(const uint16_t *x, int S, int k, int n, int K, const uint16_t *trellis,
+                                    const uint16_t *suh, const uint16_t *svh, void *y, bool f32out,
+                                    float *partials, int *counters, int *err, cudaStream_t s, bool prefetch) {
+  auto fn = gemv_tmap_fn();
+  if (!fn) return cudaErrorNotSupported;
+  int grid = 0, blocks = 0;
+  size_t pf = 0;
+  if (!exl3_gemv_shards_plan(S, k, n, K, &grid, &pf, &blocks)) return cudaErrorInvalidValue;
+  const int cc = exl3_gemv_cta_cols(K);
+  // the shards' trellis as u64 rows: row s k/16 + tk
+  CUtensorMap tm;
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)4 * K, (cuuint64_t)(n / 16), (cuuint64_t)S * (k / 16)};
+    cuuint64_t strides[2] = {(cuuint64_t)32 * K, (cuuint64_t)(n / 16) * 32 * K};
+    cuuint32_t box[3] = {(cuuint32_t)(4 * K), (cuuint32_t)(cc / 16), (cuuint32_t)kGemvBoxRows};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<uint16_t *>(trellis), dims, strides, box,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  GemvArgs a;
+  a.x = reinterpret_cast<const __half *>(x);
+  a.suh = reinterpret_cast<const __half *>(suh);
+  a.svh = reinterpret_cast<const __half *>(svh);
+  a.y = y;
+  a.partials = partials;
+  a.counters = counters;
+  a.err = err;
+  a.k = k;
+  a.n = n;
+  a.tiles_k = k / 16;
+  a.colblocks = (n + cc - 1) / cc;
+  a.ids = nullptr;
+  a.weights = nullptr;
+  a.topk = 1;
+  a.nslots = S;
+  a.E = 1;
+  a.x_per_unit = 0;
+  a.act_in = nullptr;
+  a.pos_out = nullptr;
+  a.bias = nullptr;
+  a.pre_stages = kGemvPreStages;
+  a.nops = S;
+  if ((unsigned long long)a.colblocks * a.tiles_k * a.nops * (unsigned long long)grid >= (1ull << 32))
+    return cudaErrorInvalidValue;
+  a.op_rows = (uint32_t)a.colblocks * (uint32_t)a.tiles_k;
+  a.total = (uint32_t)a.nops * a.op_rows;
+  a.stages = 0;
+  EXL3_K_SWITCH(K, a.stages = Launcher<KK, true, true>::stages(k));
+  cudaError_t e = cudaSuccess;
+  if (f32out) {
+    EXL3_K_SWITCH(K, e = Launcher<KK, true, true>::launch(tm, a, grid, s, prefetch));
+  } else {
+    EXL3_K_SWITCH(K, e = Launcher<KK, false, true>::launch(tm, a, grid, s, prefetch));
+  }
   return e;
 }
