@@ -41,7 +41,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # at k=5120 n=25600, with the hash of the kernel's sources at capture time; a
 # changed kernel source makes the recorded traffic stale (reported as null).
 TRAFFIC = {"files": ["trellis_quantized_gb300/csrc/gemv.cu", "trellis_quantized_gb300/csrc/gemv_core.cuh"],
-           "sha1": "ed62b54024519b95b1a8eae7b69bf698bc9e5116", "bytes_per_launch": 65665280,
+           "sha1": "bb3a15e36287a2ed3ce23e691e19c42da8558144", "bytes_per_launch": 65666560,
            "workload": "k5120 n25600 K4 M1"}
 
 
@@ -427,6 +427,48 @@ def bench_extras(only=None, moe_tokens=None):
         shards = {"one_launch": {"ms": round(one, 4), "GBs": round(gb / (one * 1e-3), 1)},
                   "two_linears": {"ms": round(two, 4), "GBs": round(gb / (two * 1e-3), 1)}}
         del copies, x, ys
+    # shards of different widths at M = 1, one launch against one linear
+    # each, weight prefetch on: q, k, v of grouped-query attention (k=5120,
+    # n = 5120 + 1024 + 1024, 8 weight copies = 147 MB) and the three
+    # linears of the decode sweep (n = 5120 + 17408 + 25600, 3 copies =
+    # 369 MB), both more than L2
+    var = {}
+    if only in (None, "small"):
+        for name, widths, ncopy in (("qkv_gqa_k5120_n5120+1024+1024", (5120, 1024, 1024), 8),
+                                    ("sweep_k5120_n5120+17408+25600", (5120, 17408, 25600), 3)):
+            cs = [[synth.linear_case(2, 60 + 10 * j + i, 1, 5120, n, 4) for i, n in enumerate(widths)]
+                  for j in range(ncopy)]
+            x = dev(cs[0][0].x)
+            copies = [(dev(np.concatenate([c.trellis.reshape(-1) for c in cc])), dev(np.stack([c.suh for c in cc])),
+                       dev(np.concatenate([c.svh for c in cc])), [dev(c.trellis) for c in cc]) for cc in cs]
+            yv = torch.empty(sum(widths), dtype=torch.float16, device="cuda")
+            ws = tq.workspace(tq.exl3_linear_shards_var_workspace_size(1, 5120, widths, 4))
+            prev = tq.exl3_set_weight_prefetch(True)
+            try:
+                turn = [0]
+
+                def fused():
+                    t, su, sv, _ = copies[turn[0] % ncopy]
+                    turn[0] += 1
+                    tq.exl3_linear_shards_var(x, t, su, sv, widths, 4, y=yv, workspace_buf=ws)
+
+                def separate():
+                    _, su, sv, ts = copies[turn[0] % ncopy]
+                    turn[0] += 1
+                    off = 0
+                    for i, n in enumerate(widths):
+                        tq.exl3_linear(x, ts[i], su[i], sv[off:off + n], 4, y=yv[off:off + n].view(1, n),
+                                       workspace_buf=ws)
+                        off += n
+
+                one = _timed(fused, reps=ncopy * 2)
+                sep = _timed(separate, reps=ncopy * 2)
+            finally:
+                tq.exl3_set_weight_prefetch(prev)
+            gb = sum(linear_bytes(c) for c in cs[0]) / 1e9
+            var[name] = {"one_launch": {"ms": round(one, 4), "GBs": round(gb / (one * 1e-3), 1)},
+                         "one_linear_each": {"ms": round(sep, 4), "GBs": round(gb / (sep * 1e-3), 1)}}
+            del copies, x, yv
     # the row-invariant mode (every M through the 32-token-wide fused
     # kernel, 32 rows at a time): its cost against the default paths
     inv = {}
@@ -482,7 +524,7 @@ def bench_extras(only=None, moe_tokens=None):
         mixed[f"T{T}"] = {"ms": round(ms, 4), "experts_hit": len(used),
                           "unique_weight_GBs": round(ubytes / (ms * 1e-3) / 1e9, 1)}
         del d
-    return {"small_m_k5120_n17408": small, "shards_gate_up_k5120_n17408x2_M1": shards,
+    return {"small_m_k5120_n17408": small, "shards_gate_up_k5120_n17408x2_M1": shards, "shards_var_M1": var,
             "row_invariant_k5120_n17408": inv, "moe_E256_top8_h2048_i512_K3": moe,
             "moe_mixed_E256_top8_h2048_i512_K3K4": mixed,
             "note": "small M: trellis decoded into tcgen05 operands (one fused kernel after the input RHT); "

@@ -174,6 +174,28 @@ int exl3_linear_shards(const uint16_t *x, int M, int k, int n, int nshards,
                        void *workspace, size_t ws_bytes, exl3_stream_t stream);
 
 /*
+ * exl3_linear_shards_var -- fused shards of different widths over one input,
+ * such as q, k and v under grouped-query attention.  Same computation as
+ * exl3_linear_shards, with shard s of width n[s]:
+ *   n        HOST array of nshards widths (multiples of 128), read during
+ *            the call only; nshards 1..64
+ *   trellis  shard s as its own [k/16][n[s]/16][16K] tensor, right after
+ *            shard s-1's (every shard starts on a 16-byte boundary)
+ *   suh      [nshards][k] fp16; svh the shards' svh side by side [sum n]
+ *   y        shard-major: shard s is an [M][n[s]] block starting at element
+ *            M * (n[0] + ... + n[s-1]); at M = 1 the outputs side by side
+ *   workspace of exl3_linear_shards_var_workspace_size(M, k, nshards, n, K).
+ * At M = 1, for up to 8 shards whose CTA shares each span at most four
+ * shards, one launch of the CUDA-core GEMV with a trellis map per shard;
+ * otherwise (and in row-invariant mode) one exl3_linear per shard.
+ */
+size_t exl3_linear_shards_var_workspace_size(int M, int k, int nshards, const int *n, int K);
+int exl3_linear_shards_var(const uint16_t *x, int M, int k, int nshards, const int *n,
+                           const uint16_t *trellis, const uint16_t *suh, const uint16_t *svh,
+                           int K, int codebook, void *y, int out_dtype,
+                           void *workspace, size_t ws_bytes, exl3_stream_t stream);
+
+/*
  * exl3_set_weight_prefetch -- let M = 1 calls of exl3_linear stream their
  * weights before the kernel launched ahead of them on the stream has
  * finished (CUDA programmatic dependent launch).  The source pages have no

@@ -151,6 +151,21 @@ def test_linear_shards_argument_errors():
     assert L.exl3_linear_shards_workspace_size(1, 5120, 17408, 4, 0) == 0
 
 
+def test_linear_shards_var_argument_errors():
+    L = tq.lib()
+    n = (ctypes.c_int * 3)(5120, 1024, 1024)
+    bad = (ctypes.c_int * 3)(5120, 1000, 1024)
+    args = lambda **kw: [FAKE, 1, 5120, kw.get("S", 3), kw.get("n", n), FAKE, FAKE, FAKE, kw.get("K", 4), 2, FAKE,
+                         0, FAKE, kw.get("wsb", 1 << 26), None]
+    assert L.exl3_linear_shards_var(*args(n=None)) == tq.EXL3_ERR_ARG
+    assert L.exl3_linear_shards_var(*args(n=bad)) == tq.EXL3_ERR_SHAPE
+    assert L.exl3_linear_shards_var(*args(S=0)) == tq.EXL3_ERR_SHAPE
+    assert L.exl3_linear_shards_var(*args(K=9)) == tq.EXL3_ERR_BITS
+    assert L.exl3_linear_shards_var(*args(wsb=64)) == tq.EXL3_ERR_WORKSPACE
+    assert L.exl3_linear_shards_var_workspace_size(1, 5120, 3, n, 4) >= L.exl3_linear_workspace_size(1, 5120, 5120, 4)
+    assert L.exl3_linear_shards_var_workspace_size(1, 5120, 3, None, 4) == 0
+
+
 def test_input_rht_argument_errors():
     L = tq.lib()
     assert L.exl3_input_rht(FAKE, 1, 100, FAKE, FAKE, 1, None) == tq.EXL3_ERR_SHAPE

@@ -94,6 +94,9 @@ def lib():
         L.exl3_linear_shards_workspace_size.argtypes = [I, I, I, I, I]
         L.exl3_linear_shards_workspace_size.restype = Z
         L.exl3_linear_shards.argtypes = [P, I, I, I, I, P, P, P, I, I, P, I, P, Z, P]
+        L.exl3_linear_shards_var_workspace_size.argtypes = [I, I, I, P, I]
+        L.exl3_linear_shards_var_workspace_size.restype = Z
+        L.exl3_linear_shards_var.argtypes = [P, I, I, I, P, P, P, P, I, I, P, I, P, Z, P]
         L.exl3_moe_mixed_workspace_size.argtypes = [I, I, I, P, P]
         L.exl3_moe_mixed_workspace_size.restype = Z
         L.exl3_moe_grouped_mixed.argtypes = [P, I, I, P, P, I, I, P, P, P, I, P, Z, P]
@@ -246,6 +249,30 @@ def exl3_linear_shards(x, trellis, suh, svh, K: int, codebook: int = EXL3_CB_MUL
     _check(lib().exl3_linear_shards(_ptr(x, "x", 2), M, k, n, S, _ptr(trellis, "trellis", 2), _ptr(suh, "suh", 2),
                                     _ptr(svh, "svh", 2), K, codebook, _ptr(y, "y"), out_dtype, _ptr(ws, "workspace"),
                                     ws.numel() * ws.element_size(), _stream(stream)))
+    return y
+
+
+def exl3_linear_shards_var_workspace_size(M: int, k: int, widths, K: int) -> int:
+    n = (ctypes.c_int * len(widths))(*[int(w) for w in widths])
+    return lib().exl3_linear_shards_var_workspace_size(M, k, len(widths), n, K)
+
+
+def exl3_linear_shards_var(x, trellis, suh, svh, widths, K: int, codebook: int = EXL3_CB_MUL1,
+                           out_dtype: int = EXL3_OUT_F16, y=None, workspace_buf=None, stream=None) -> torch.Tensor:
+    """Fused shards of different widths over one input: trellis flat (shard s's
+    [k/16, n_s/16, 16K] tensor right after shard s-1's), suh [S, k], svh [sum n];
+    returns y flat, shard-major (shard s an [M, n_s] block)."""
+    M, k = x.shape
+    S = len(widths)
+    n = (ctypes.c_int * S)(*[int(w) for w in widths])
+    total = M * sum(int(w) for w in widths)
+    if y is None:
+        y = torch.empty(total, dtype=torch.float32 if out_dtype == EXL3_OUT_F32 else torch.float16, device=x.device)
+    need = lib().exl3_linear_shards_var_workspace_size(M, k, S, n, K)
+    ws = workspace_buf if workspace_buf is not None else workspace(need, x.device, stream)
+    _check(lib().exl3_linear_shards_var(_ptr(x, "x", 2), M, k, S, n, _ptr(trellis, "trellis", 2), _ptr(suh, "suh", 2),
+                                        _ptr(svh, "svh", 2), K, codebook, _ptr(y, "y"), out_dtype,
+                                        _ptr(ws, "workspace"), ws.numel() * ws.element_size(), _stream(stream)))
     return y
 
 

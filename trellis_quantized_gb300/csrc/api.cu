@@ -51,6 +51,10 @@ cudaError_t exl3_launch_moe_combine(const float *d, const int *pos, int T, int t
                                     bool f32out, cudaStream_t s);
 bool exl3_moe_gemv_plan(int U, int nslots, int k, int n, int K, int *grid, size_t *partial_floats, int *blocks);
 bool exl3_gemv_shards_plan(int S, int k, int n, int K, int *grid, size_t *partial_floats, int *blocks);
+bool exl3_gemv_shards_var_plan(int S, int k, const int *n, int K, int *grid, size_t *partial_floats, int *blocks);
+cudaError_t exl3_launch_gemv_shards_var(const uint16_t *x, int S, int k, const int *n, int K, const uint16_t *trellis,
+                                        const uint16_t *suh, const uint16_t *svh, void *y, bool f32out,
+                                        float *partials, int *counters, int *err, cudaStream_t s, bool prefetch);
 cudaError_t exl3_launch_gemv_shards(const uint16_t *x, int S, int k, int n, int K, const uint16_t *trellis,
                                     const uint16_t *suh, const uint16_t *svh, void *y, bool f32out,
                                     float *partials, int *counters, int *err, cudaStream_t s, bool prefetch);
@@ -743,6 +747,68 @@ int exl3_linear_shards(const uint16_t *x, int M, int k, int n, int nshards, cons
     EXL3_TRY(linear_impl(x, M, k, n, trellis + sh * words, suh + (size_t)sh * k, svh + (size_t)sh * n, nullptr, K,
                          codebook, static_cast<uint8_t *>(y) + sh * ybytes, out_dtype, workspace, ws_bytes,
                          stream));
+  return EXL3_OK;
+}
+
+size_t exl3_linear_shards_var_workspace_size(int M, int k, int nshards, const int *n, int K) {
+  if (nshards < 1 || nshards > 64 || !n) return 0;
+  size_t need = 0;
+  for (int i = 0; i < nshards; ++i) {
+    const size_t w = exl3_linear_workspace_size(M, k, n[i], K);
+    if (w == 0) return 0;
+    if (w > need) need = w;
+  }
+  int grid = 0, blocks = 0;
+  size_t pf = 0;
+  if (M == 1 && exl3_gemv_shards_var_plan(nshards, k, n, K, &grid, &pf, &blocks)) {
+    const size_t one = align_up(kDataOff + sizeof(float) * pf);
+    if (one > need) need = one;
+  }
+  return need;
+}
+
+int exl3_linear_shards_var(const uint16_t *x, int M, int k, int nshards, const int *n, const uint16_t *trellis,
+                           const uint16_t *suh, const uint16_t *svh, int K, int codebook, void *y, int out_dtype,
+                           void *workspace, size_t ws_bytes, exl3_stream_t stream) {
+  g_last_error.clear();
+  EXL3_TRY(check_ptr(x, "x"));
+  EXL3_TRY(check_ptr(trellis, "trellis"));
+  EXL3_TRY(check_ptr(suh, "suh"));
+  EXL3_TRY(check_ptr(svh, "svh"));
+  EXL3_TRY(check_ptr(y, "y"));
+  if (!n) return exl3_fail(EXL3_ERR_ARG, "n (host array of shard widths) is NULL");
+  EXL3_TRY(check_bits_codebook(K, codebook));
+  if (nshards < 1 || nshards > 64) return exl3_fail(EXL3_ERR_SHAPE, "nshards = %d outside 1..64", nshards);
+  long long ntot = 0;
+  for (int i = 0; i < nshards; ++i) {
+    EXL3_TRY(check_linear_shape(M, k, n[i]));
+    ntot += n[i];
+  }
+  if ((long long)M * ntot > INT32_MAX) return exl3_fail(EXL3_ERR_SHAPE, "M * sum of widths too large");
+  if (out_dtype != EXL3_OUT_F16 && out_dtype != EXL3_OUT_F32)
+    return exl3_fail(EXL3_ERR_ARG, "out_dtype %d invalid", out_dtype);
+  const size_t need = exl3_linear_shards_var_workspace_size(M, k, nshards, n, K);
+  EXL3_TRY(check_workspace(workspace, ws_bytes, need));
+  const bool f32 = out_dtype == EXL3_OUT_F32;
+  int grid = 0, blocks = 0;
+  size_t pf = 0;
+  if (M == 1 && g_row_invariant.load() == 0 && exl3_gemv_shards_var_plan(nshards, k, n, K, &grid, &pf, &blocks) &&
+      (size_t)blocks <= kMaxCounters) {
+    return exl3_cuda_check(exl3_launch_gemv_shards_var(x, nshards, k, n, K, trellis, suh, svh, y, f32,
+                                                       at<float>(workspace, kDataOff),
+                                                       at<int>(workspace, kCounterOff), at<int>(workspace, 0),
+                                                       stream, g_weight_prefetch.load() != 0),
+                           "gemv shards launch");
+  }
+  // one linear per shard, into its [M][n] block of the shard-major output
+  size_t words = 0, col = 0;
+  for (int i = 0; i < nshards; ++i) {
+    EXL3_TRY(linear_impl(x, M, k, n[i], trellis + words, suh + (size_t)i * k, svh + col, nullptr, K, codebook,
+                         static_cast<uint8_t *>(y) + (size_t)M * col * (f32 ? 4 : 2), out_dtype, workspace,
+                         ws_bytes, stream));
+    words += (size_t)(k / 16) * (n[i] / 16) * 16 * K;
+    col += n[i];
+  }
   return EXL3_OK;
 }
 

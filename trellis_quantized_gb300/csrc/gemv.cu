@@ -81,9 +81,17 @@ struct GemvArgs {
   int *pos_out;
   // Output bias [n] fp16 added after svh (NULL: none; not GROUPED)
   const __half *bias;
+  // Shards of different widths (GROUPED, var > 0 shards, no expert ids):
+  // shard s has width vn[s], its column blocks are global blocks
+  // vb[s] .. vb[s + 1] - 1, its svh and y start at column vo[s] of the
+  // concatenated [sum of widths] vectors, suh at s k, and its trellis is
+  // tensor map s.
+  int var;
+  int vn[8], vo[8], vb[9];
 };
 
 constexpr int kGemvMaxOps = 4;        // ops one CTA's range may touch in GROUPED mode
+constexpr int kGemvMaxShards = 8;     // shards of different widths in one launch
 constexpr int kGemvPrePartials = 2;   // partials a finisher loads before its segment ends
 constexpr int kGemvPreStages = 2;     // stages the producer loads before x' is ready
 
@@ -94,13 +102,17 @@ struct GemvOp {
   float scale;
   int trow;                 // first trellis row of the op's weights
   bool bad;                 // invalid expert id
+  int map;                  // tensor map of the op's trellis
 };
 
 template <bool GROUPED, bool F32OUT>
 __device__ __forceinline__ GemvOp gemv_op(const GemvArgs &a, int o) {
   if constexpr (!GROUPED) {
-    return GemvOp{a.x, a.suh, a.svh, a.y, 1.0f, 0, false};
+    return GemvOp{a.x, a.suh, a.svh, a.y, 1.0f, 0, false, 0};
   } else {
+    if (a.var)   // shard o of different widths: its own map, column offset vo[o]
+      return GemvOp{a.x, a.suh + (long)o * a.k, a.svh + a.vo[o],
+                    static_cast<char *>(a.y) + (long)a.vo[o] * (F32OUT ? 4 : 2), 1.0f, 0, false, o};
     const int u = o / a.nslots, slot = o - u * a.nslots;
     int e = a.ids ? a.ids[u] : 0;   // no id list: every unit uses expert 0 (fused shards)
     const bool bad = e < 0 || e >= a.E;
@@ -112,13 +124,29 @@ __device__ __forceinline__ GemvOp gemv_op(const GemvArgs &a, int o) {
     const long es = (long)e * a.nslots + slot;
     const long xr = a.x_per_unit ? u : u / a.topk;
     return GemvOp{a.x + xr * a.k, a.suh + es * a.k, a.svh + es * a.n,
-                  static_cast<char *>(a.y) + (long)o * a.n * (F32OUT ? 4 : 2), scale, (int)(es * a.tiles_k), bad};
+                  static_cast<char *>(a.y) + (long)o * a.n * (F32OUT ? 4 : 2), scale, (int)(es * a.tiles_k), bad, 0};
   }
 }
 
+// GROUPED mode: the op of global column block c, c's index inside that op,
+// and the op's width.
+__device__ __forceinline__ int op_of_block(const GemvArgs &a, int c) {
+  if (!a.var) return c / a.colblocks;
+  int o = 0;
+#pragma unroll
+  for (int s = 1; s < kGemvMaxShards; ++s)
+    if (s < a.var && c >= a.vb[s]) o = s;
+  return o;
+}
+__device__ __forceinline__ int block_in_op(const GemvArgs &a, int c, int op) {
+  return a.var ? c - a.vb[op] : c - op * a.colblocks;
+}
+__device__ __forceinline__ int op_width(const GemvArgs &a, int op) { return a.var ? a.vn[op] : a.n; }
+
+// The kernel body; maps holds the trellis tensor map (one per shard for
+// shards of different widths).
 template <int K, bool F32OUT, bool GROUPED>
-__global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
-    gemv_m1_kernel(const __grid_constant__ CUtensorMap tmT, GemvArgs a) {
+__device__ __forceinline__ void gemv_body(const CUtensorMap *maps, const GemvArgs &a) {
   using S = GemvShape<K>;
   constexpr int NCW = S::NCW, NCT = NCW * 32;
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -163,16 +191,18 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
   if (warp == NCW) {
     // ---------------- producer: one thread loads the rows into the ring
     if (lane == 0) {
-      tc::prefetch_tmap(&tmT);
+      for (int m = 0; m < (GROUPED && a.var ? a.var : 1); ++m) tc::prefetch_tmap(maps + m);
       int stage = 0, issued = 0;
       uint32_t phase = 0;
       for (uint32_t t = t0; t < t1 && !*s_abort;) {
         const uint32_t c = t / TKU;   // block: op c / colblocks, column block c % colblocks
         const uint32_t seg_end = min(t1, (c + 1) * TKU);
         const int tk_first = (int)(t - c * TKU), nrows = (int)(seg_end - t);
-        const int op = GROUPED ? (int)(c / (uint32_t)a.colblocks) : 0;
-        const int tn0 = ((int)c - op * a.colblocks) * (S::CTA_COLS / 16);
-        const int trow = gemv_op<GROUPED, F32OUT>(a, op).trow + tk_first;
+        const int op = GROUPED ? op_of_block(a, (int)c) : 0;
+        const int tn0 = (GROUPED ? block_in_op(a, (int)c, op) : (int)c) * (S::CTA_COLS / 16);
+        const GemvOp Pp = gemv_op<GROUPED, F32OUT>(a, op);
+        const int trow = Pp.trow + tk_first;
+        const CUtensorMap *tmT = maps + Pp.map;
         for (int r0 = 0; r0 < nrows && !*s_abort; r0 += S::R) {
           const int cnt = min(S::R, nrows - r0);
           if (issued++ == a.pre_stages) {
@@ -200,7 +230,7 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
           tc::mbar_arrive_expect_tx(&full[stage], (uint32_t)(nb * kGemvBoxRows * S::ROWB));
           uint8_t *dst = ring + (size_t)stage * S::STAGE_B;
           for (int b = 0; b < nb; ++b)
-            tc::tma_load_3d(dst + (size_t)b * kGemvBoxRows * S::ROWB, &tmT, &full[stage], 0, tn0,
+            tc::tma_load_3d(dst + (size_t)b * kGemvBoxRows * S::ROWB, tmT, &full[stage], 0, tn0,
                             trow + r0 + b * kGemvBoxRows);
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
@@ -232,14 +262,15 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
     // over while they go on decoding the next one.  Lane l holds columns
     // 128 g + 4 l .. +3 of every 128-column group g.
     uint32_t sp = 0;
-    const int op0 = GROUPED ? (int)(t0 / a.op_rows) : 0;
+    const int op0 = GROUPED ? op_of_block(a, (int)(t0 / TKU)) : 0;
     for (uint32_t t = t0; t < t1;) {
       const int c = (int)(t / TKU);   // block: op c / colblocks, column block c % colblocks
       const uint32_t seg_end = min(t1, (uint32_t)(c + 1) * TKU);
-      const int op = GROUPED ? c / a.colblocks : 0;
+      const int op = GROUPED ? op_of_block(a, c) : 0;
       const GemvOp P = gemv_op<GROUPED, F32OUT>(a, op);
+      const int nop = GROUPED ? op_width(a, op) : a.n;
       const float *rs = rsum + (op - op0) * (a.k / 16);
-      const int col0 = (c - op * a.colblocks) * S::CTA_COLS;
+      const int col0 = (GROUPED ? block_in_op(a, c, op) : c) * S::CTA_COLS;
       const uint32_t blk_first = (uint32_t)c * TKU, blk_last = min((uint32_t)(c + 1) * TKU, a.total) - 1;
       const int i_first = range_owner(blk_first, a.total, grid), i_last = range_owner(blk_last, a.total, grid);
       // A block shared by several CTAs is finished by its first CTA, whose
@@ -288,7 +319,7 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
       const bool has_bias = !GROUPED && a.bias != nullptr;
 #pragma unroll
       for (int g = 0; g < S::NG; ++g) {
-        const bool mine = (!shared || finisher) && col0 + g * 128 < a.n;
+        const bool mine = (!shared || finisher) && col0 + g * 128 < nop;
         svv[g] = mine ? *reinterpret_cast<const uint2 *>(P.svh + col0 + g * 128 + lane * 4) : make_uint2(0u, 0u);
         bvv[g] = mine && has_bias ? *reinterpret_cast<const uint2 *>(a.bias + col0 + g * 128 + lane * 4)
                                   : make_uint2(0u, 0u);
@@ -362,7 +393,7 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
 #pragma unroll
         for (int g = 0; g < S::NG; ++g) {
           const int gc = col0 + g * 128 + lane * 4;
-          if (col0 + g * 128 < a.n) {
+          if (col0 + g * 128 < nop) {
             fwht128_warp(v[g], lane);
             const __half2 *sh = reinterpret_cast<const __half2 *>(&svv[g]);
             float o0 = v[g][0] * kRhtScale * __low2float(sh[0]);
@@ -401,7 +432,7 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
   // prologue: x' = 2^-3.5 H (x . suh) for the 512-element chunks (32 tile
   // rows) this range touches; a warp transforms four 128-blocks at once,
   // eight lanes per block and 16 contiguous elements per lane
-  const int op0 = GROUPED ? (int)(t0 / a.op_rows) : 0;
+  const int op0 = GROUPED ? op_of_block(a, (int)(t0 / TKU)) : 0;
   if (GROUPED && a.pos_out && me == 0) {   // the combine's row of each unit
     for (int u = tid; u < a.nops / a.nslots; u += NCT) {
       const int e = a.ids[u];
@@ -412,7 +443,7 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
     const int KC = (a.k + 511) >> 9;
     int c0 = 0, nc = KC;
     if (GROUPED) {          // every chunk of each op the range touches (ops op0 ..)
-      nc = ((int)((t1 - 1) / a.op_rows) - op0 + 1) * KC;
+      nc = (op_of_block(a, (int)((t1 - 1) / TKU)) - op0 + 1) * KC;
     } else if (t1 - t0 < TK) {   // fewer rows than one block: at most two column blocks
       c0 = (int)(t0 % TKU) >> 5;
       const int c1 = (int)((t1 - 1) % TKU) >> 5;
@@ -496,7 +527,7 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
     const int c = (int)(t / TKU);
     const uint32_t seg_end = min(t1, (uint32_t)(c + 1) * TKU);
     const int tk_first = (int)(t - (uint32_t)c * TKU), nrows = (int)(seg_end - t);
-    const __half *xso = xs + (GROUPED ? c / a.colblocks - op0 : 0) * a.k;   // this op's x'
+    const __half *xso = xs + (GROUPED ? op_of_block(a, c) - op0 : 0) * a.k;   // this op's x'
 
     float acc[16];
 #pragma unroll
@@ -561,6 +592,23 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
     sp ^= 1;
     t = seg_end;
   }
+}
+
+template <int K, bool F32OUT, bool GROUPED>
+__global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
+    gemv_m1_kernel(const __grid_constant__ CUtensorMap tmT, GemvArgs a) {
+  gemv_body<K, F32OUT, GROUPED>(&tmT, a);
+}
+
+// Shards of different widths: one trellis map per shard.
+struct GemvShardMaps {
+  CUtensorMap m[kGemvMaxShards];
+};
+
+template <int K, bool F32OUT>
+__global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
+    gemv_shards_kernel(const __grid_constant__ GemvShardMaps maps, GemvArgs a) {
+  gemv_body<K, F32OUT, true>(maps.m, a);
 }
 
 static int gemv_sm_count() {
@@ -717,6 +765,7 @@ cudaError_t exl3_launch_gemv_m1_bias(const uint16_t *x, const uint16_t *trellis,
   a.op_rows = a.total;
   a.act_in = nullptr;
   a.pos_out = nullptr;
+  a.var = 0;
   a.bias = reinterpret_cast<const __half *>(bias);
   a.pre_stages = kGemvPreStages;
   a.stages = 0;
@@ -810,6 +859,7 @@ cudaError_t exl3_launch_moe_gemv(const uint16_t *x, const float *act_in, int *po
   a.x_per_unit = 0;
   a.act_in = act_in;
   a.pos_out = pos_out;
+  a.var = 0;
   a.bias = nullptr;
   a.pre_stages = kGemvPreStages;
   a.nops = U * nslots;
@@ -877,6 +927,7 @@ cudaError_t exl3_launch_gemv_shards(const uint16_t *x, int S, int k, int n, int 
   a.x_per_unit = 0;
   a.act_in = nullptr;
   a.pos_out = nullptr;
+  a.var = 0;
   a.bias = nullptr;
   a.pre_stages = kGemvPreStages;
   a.nops = S;
@@ -892,5 +943,126 @@ cudaError_t exl3_launch_gemv_shards(const uint16_t *x, int S, int k, int n, int 
   } else {
     EXL3_K_SWITCH(K, e = Launcher<KK, false, true>::launch(tm, a, grid, s, prefetch));
   }
+  return e;
+}
+
+// ---- shards of different widths: shard s has n[s] (host) output columns, its
+// trellis [k/16][n[s]/16][16K] right after shard s-1's, suh [S][k], svh and y
+// the concatenated [sum n] vectors; one launch with a tensor map per shard.
+// False when S is outside 1..kGemvMaxShards, a CTA's range would touch more
+// than kGemvMaxOps shards, or x' for them does not fit.
+bool exl3_gemv_shards_var_plan(int S, int k, const int *n, int K, int *grid, size_t *partial_floats, int *blocks) {
+  if (S < 1 || S > kGemvMaxShards) return false;
+  const int cc = exl3_gemv_cta_cols(K);
+  long long vb[kGemvMaxShards + 1];
+  vb[0] = 0;
+  for (int i = 0; i < S; ++i) vb[i + 1] = vb[i] + (n[i] + cc - 1) / cc;
+  const long long TK = k / 16, total = vb[S] * TK;
+  long long g = gemv_sm_count();
+  if (g > total) g = total;
+  if (g < 1 || (unsigned long long)total * (unsigned long long)g >= (1ull << 32)) return false;
+  auto op_of = [&](long long c) {
+    int o = 0;
+    for (int i = 1; i < S; ++i)
+      if (c >= vb[i]) o = i;
+    return o;
+  };
+  for (long long i = 0; i < g; ++i) {   // the kernel's split: CTA i takes rows [i total / g, (i + 1) total / g)
+    const long long r0 = i * total / g, r1 = (i + 1) * total / g;
+    if (r1 > r0 && op_of((r1 - 1) / TK) - op_of(r0 / TK) + 1 > kGemvMaxOps) return false;
+  }
+  int st = 0;
+  EXL3_K_SWITCH(K, st = Launcher<KK, true, true>::stages(k));
+  if (st < 2) return false;
+  *grid = (int)g;
+  *blocks = (int)vb[S];
+  *partial_floats = (size_t)(vb[S] + g) * (size_t)cc;
+  return true;
+}
+
+cudaError_t exl3_launch_gemv_shards_var(const uint16_t *x, int S, int k, const int *n, int K, const uint16_t *trellis,
+                                        const uint16_t *suh, const uint16_t *svh, void *y, bool f32out,
+                                        float *partials, int *counters, int *err, cudaStream_t s, bool prefetch) {
+  auto fn = gemv_tmap_fn();
+  if (!fn) return cudaErrorNotSupported;
+  int grid = 0, blocks = 0;
+  size_t pf = 0;
+  if (!exl3_gemv_shards_var_plan(S, k, n, K, &grid, &pf, &blocks)) return cudaErrorInvalidValue;
+  const int cc = exl3_gemv_cta_cols(K);
+  GemvShardMaps maps;
+  memset(&maps, 0, sizeof maps);
+  GemvArgs a;
+  memset(&a, 0, sizeof a);
+  size_t words = 0;
+  int vo = 0, vb = 0;
+  for (int i = 0; i < S; ++i) {
+    cuuint64_t dims[3] = {(cuuint64_t)4 * K, (cuuint64_t)(n[i] / 16), (cuuint64_t)(k / 16)};
+    cuuint64_t strides[2] = {(cuuint64_t)32 * K, (cuuint64_t)(n[i] / 16) * 32 * K};
+    cuuint32_t box[3] = {(cuuint32_t)(4 * K), (cuuint32_t)(cc / 16), (cuuint32_t)kGemvBoxRows};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(&maps.m[i], CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<uint16_t *>(trellis) + words, dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    words += (size_t)(k / 16) * (n[i] / 16) * 16 * K;
+    a.vn[i] = n[i];
+    a.vo[i] = vo;
+    a.vb[i] = vb;
+    vo += n[i];
+    vb += (n[i] + cc - 1) / cc;
+  }
+  a.vb[S] = vb;
+  a.var = S;
+  a.x = reinterpret_cast<const __half *>(x);
+  a.suh = reinterpret_cast<const __half *>(suh);
+  a.svh = reinterpret_cast<const __half *>(svh);
+  a.y = y;
+  a.partials = partials;
+  a.counters = counters;
+  a.err = err;
+  a.k = k;
+  a.n = vo;
+  a.tiles_k = k / 16;
+  a.colblocks = vb;
+  a.ids = nullptr;
+  a.weights = nullptr;
+  a.topk = 1;
+  a.nslots = S;
+  a.E = 1;
+  a.nops = S;
+  a.bias = nullptr;
+  a.pre_stages = kGemvPreStages;
+  a.total = (uint32_t)vb * (uint32_t)a.tiles_k;
+  a.op_rows = a.total;
+  EXL3_K_SWITCH(K, a.stages = Launcher<KK, true, true>::stages(k));
+  cudaLaunchAttribute attrs[1];
+  attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.stream = s;
+  cfg.attrs = prefetch ? attrs : nullptr;
+  cfg.numAttrs = prefetch ? 1 : 0;
+  cudaError_t e = cudaSuccess;
+#define EXL3_GSV(KK, F32)                                                                                    \
+  do {                                                                                                     \
+    const size_t sm = Launcher<KK, F32, true>::smem(k, a.stages);                                          \
+    static size_t attr = 0;                                                                                \
+    if (attr < sm) {                                                                                       \
+      e = cudaFuncSetAttribute(gemv_shards_kernel<KK, F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,   \
+                               (int)sm);                                                                   \
+      if (e != cudaSuccess) break;                                                                         \
+      attr = sm;                                                                                           \
+    }                                                                                                      \
+    cfg.blockDim = dim3(GemvShape<KK>::THREADS);                                                           \
+    cfg.dynamicSmemBytes = sm;                                                                             \
+    e = cudaLaunchKernelEx(&cfg, gemv_shards_kernel<KK, F32>, maps, a);                                    \
+  } while (0)
+  if (f32out) {
+    EXL3_K_SWITCH(K, EXL3_GSV(KK, true));
+  } else {
+    EXL3_K_SWITCH(K, EXL3_GSV(KK, false));
+  }
+#undef EXL3_GSV
   return e;
 }
