@@ -365,7 +365,7 @@ extern "C" {
 
 const char *exl3_last_error(void) { return g_last_error.c_str(); }
 
-int exl3_version(void) { return 100; }
+int exl3_version(void) { return 200; }
 
 int exl3_set_weight_prefetch(int enable) { return g_weight_prefetch.exchange(enable ? 1 : 0); }
 
