@@ -33,6 +33,33 @@ sys.path.insert(0, ROOT)
 import exl3_synth as synth  # noqa: E402
 
 METRIC = "EXL3 trellis GEMV HBM GB/s (M=1) & GEMM TFLOPS (M=4096), % of roofline"
+
+
+def _world() -> int:
+    """Ranks of the job (torchrun sets WORLD_SIZE; 1 without it)."""
+    return int(os.environ.get("WORLD_SIZE", "1"))
+
+
+def _barrier():
+    """All ranks meet here when the job runs replicas under torchrun."""
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def aggregate_replicas(out: dict, dist, device) -> dict:
+    """The whole-job line of N replicas: every rank's algorithmic bytes over
+    the slowest rank's step time (max over ranks); n_gpus = world size."""
+    import torch
+    t = torch.tensor([out["ms_per_step"]], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ws = dist.get_world_size()
+    step_bytes = out["value"] * 1e9 * out["ms_per_step"] * 1e-3      # this rank's bytes per step
+    res = dict(out)
+    res["ms_per_step"] = float(t.item())
+    res["value"] = round(step_bytes * ws / (res["ms_per_step"] * 1e-3) / 1e9, 1)
+    res["n_gpus"] = ws
+    return res
 WORKLOAD = "dense decode GEMV sweep k=5120 n={5120,17408,25600} K=4 M=1 mul1, fp16 out"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -203,6 +230,7 @@ def run_ours(args):
     with ClockSampler(torch.cuda.current_device()) as clk:
         time.sleep(0.3)
         torch.cuda.synchronize()
+        _barrier()
         t_start.record(stream)
         done = 0
         while done + chunk <= args.steps:
@@ -213,6 +241,7 @@ def run_ours(args):
             done += 1
         t_end.record(stream)
         torch.cuda.synchronize()
+        _barrier()
         k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         kreps = 20
         k0.record(stream)
@@ -305,7 +334,7 @@ def run_ours(args):
                 "weight_prefetch), captured 10 steps per CUDA graph",
         "roofline": roofline, "e2e": e2e, "clocks": clk.summary(), "prefill": prefill, "other": extras,
     }
-    if not args.skip_cpu:
+    if not args.skip_cpu and _world() == 1:   # the oracle baseline: rank 0 of a one-GPU run only
         out["cpu_baseline"] = cpu_baseline(args)
     return out
 
@@ -623,14 +652,7 @@ def main():
         local = int(os.environ.get("LOCAL_RANK", "0"))
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
-        out = run_ours(args)
-        t = torch.tensor([out["ms_per_step"]], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ws = dist.get_world_size()
-        step_bytes = out["value"] * 1e9 * out["ms_per_step"] * 1e-3      # this rank's bytes per step
-        out["ms_per_step"] = float(t.item())                             # slowest rank
-        out["value"] = round(step_bytes * ws / (out["ms_per_step"] * 1e-3) / 1e9, 1)
-        out["n_gpus"] = ws
+        out = aggregate_replicas(run_ours(args), dist, "cuda")
         if rank == 0:
             print(json.dumps(out))
         dist.destroy_process_group()
