@@ -41,6 +41,13 @@ def _err(L):
     return L.exl3_last_error().decode()
 
 
+def test_every_declared_symbol_has_a_binding_of_the_same_name():
+    """The Python layer wraps every C entry point under its own name (the
+    error message is read by the wrappers themselves)."""
+    missing = [n for n in header_functions() if n != "exl3_last_error" and not hasattr(tq, n)]
+    assert not missing, missing
+
+
 def test_decode_tile_argument_errors():
     L = tq.lib()
     assert L.exl3_decode_tile(None, 128, 128, 4, 2, 0, 8, 0, 8, FAKE, 128, None) == tq.EXL3_ERR_ARG
