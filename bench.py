@@ -562,6 +562,57 @@ def bench_extras(only=None, moe_tokens=None):
                     "width (two runs here), for every token count"}
 
 
+# ---------------------------------------------------------------- pipe ceilings
+
+# (mix id, name, chains per thread, lane-instructions per chain-iteration by
+# class (an ffma2 is one instruction of two FMAs), weights per chain-iteration)
+PIPE_MIXES = [
+    (0, "imad", 8, {"imad": 1}, 0), (1, "dp4a", 8, {"dp4a": 1}, 0),
+    (2, "imad+dp4a", 8, {"imad": 1, "dp4a": 1}, 0),
+    (3, "fhfma", 8, {"fhfma": 1}, 0), (4, "ffma2", 8, {"ffma2": 1}, 0), (5, "ffma", 8, {"ffma": 1}, 0),
+    (6, "decode_fhfma", 8, {"imad": 1, "dp4a": 1, "fhfma": 1}, 1),
+    (7, "decode_ffma2", 8, {"imad": 1, "dp4a": 1, "ffma2": 0.5}, 1),
+    (8, "alu", 8, {"alu": 1}, 0),
+    (9, "decode_k4_ffma2", 1, {"alu": 13, "imad": 8, "dp4a": 8, "ffma2": 4}, 8),
+    (10, "decode_k4_fhfma", 1, {"alu": 13, "imad": 8, "dp4a": 8, "fhfma": 8}, 8),
+    (11, "hmma_m16n8k16", 1, {"hmma_warp_inst": 8 / 32}, 0),
+    (12, "decode_k4_hmma", 1, {"alu": 26, "imad": 16, "dp4a": 16, "hmma_warp_inst": 4 / 32}, 16),
+    (13, "decode_ffma", 8, {"imad": 1, "dp4a": 1, "ffma": 1}, 1),
+    (14, "decode_k4_ffma", 1, {"alu": 13, "imad": 8, "dp4a": 8, "ffma": 8}, 8),
+]
+
+
+def bench_pipes(iters=20000):
+    """Instruction throughput per SM clock (lane-operations, or decoded
+    weights, per clock per SM) of the decode's instruction classes, measured
+    with clock64 in one 1024-thread CTA per SM; see ubench/pipes.cu."""
+    import ctypes
+
+    import torch
+    from trellis_quantized_gb300 import _build
+    L = ctypes.CDLL(_build.build_ubench())
+    L.exl3_ubench_pipes.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                    ctypes.c_void_p]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    cyc = torch.zeros(sms, dtype=torch.int64, device="cuda")
+    sink = torch.zeros(1024, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    res = {}
+    for mix, name, chains, ops, wpc in PIPE_MIXES:
+        for rep in range(2):   # the first run warms up
+            rc = L.exl3_ubench_pipes(mix, sms, iters, cyc.data_ptr(), sink.data_ptr(), ctypes.c_void_p(stream))
+            assert rc == 0, f"ubench mix {mix}: cuda error {rc}"
+            torch.cuda.synchronize()
+        cycles = float(cyc.double().median().item())
+        units = 1024.0 * iters * chains / cycles   # chain-iterations per clock per SM
+        r = {k: round(v * units, 2) for k, v in ops.items()}
+        if wpc:
+            r["weights_per_clk"] = round(wpc * units, 2)
+        res[name] = r
+    return {"sms": sms, "per_sm_per_clock": res,
+            "method": "one 1024-thread CTA per SM, 8 independent chains per thread, clock64 cycles (median CTA)"}
+
+
 # ------------------------------------------------------------------------- oracle
 
 CPU_SAMPLE_S = 10.0   # seconds of oracle work in the bench's cpu_baseline
@@ -625,7 +676,7 @@ def main():
     ap.add_argument("--skip-prefill", action="store_true")
     ap.add_argument("--no-prefetch", action="store_true",
                     help="launch the step's linears plainly (no weight prefetch across launches)")
-    ap.add_argument("--only", choices=["small", "moe", "prefill"], default=None,
+    ap.add_argument("--only", choices=["small", "moe", "prefill", "pipes"], default=None,
                     help="run one extra section alone and print its JSON (for profiling)")
     ap.add_argument("--moe-tokens", type=int, nargs="*", default=None,
                     help="token counts of the MoE section (default: all of the MoE workload's)")
@@ -634,6 +685,8 @@ def main():
         import torch
         if args.only == "prefill":
             print(json.dumps(bench_prefill(args, *peaks()[1:])))
+        elif args.only == "pipes":
+            print(json.dumps(bench_pipes()))
         else:
             print(json.dumps(bench_extras(args.only, args.moe_tokens)))
         return
