@@ -359,6 +359,19 @@ int exl3_linear_gemv_noalloc(const uint16_t *x, int k, int n, const uint16_t *tr
                              const uint16_t *suh, const uint16_t *svh, int K, int codebook,
                              void *y, int out_dtype, exl3_stream_t stream);
 
+/*
+ * exl3_noalloc_device_error -- the device error word of the fixed scratch
+ * array that exl3_linear_gemv_noalloc uses on the current device (no
+ * counterpart on the source pages; a companion of that entry point).
+ *   Waits for `stream` (cudaStreamSynchronize), copies the word to
+ *   *err_out with a plain cudaMemcpy and clears it; allocates nothing.
+ *   Nonzero means a call since the last read hit a device-side check (a
+ *   bounded wait that ran out, an index out of range): that call's y is
+ *   incomplete.  The bits are those of exl3_check_device_error.  Returns
+ *   EXL3_ERR_ARG for a NULL err_out, EXL3_ERR_CUDA if a CUDA call fails.
+ */
+int exl3_noalloc_device_error(exl3_stream_t stream, int *err_out);
+
 #ifdef __cplusplus
 }
 #endif

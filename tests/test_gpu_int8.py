@@ -45,8 +45,11 @@ def test_int8_small_all_widths(K):
     _check(synth.linear_case(20, K, 37, 640, 384, K, outlier_rows=0.1))
 
 
-@pytest.mark.parametrize("K,M", [(2, 64), (6, 8), (7, 1)])
-def test_int8_config3(K, M):
+@pytest.mark.parametrize("M", synth.CONFIG3_M)
+@pytest.mark.parametrize("K", synth.CONFIG3_K)
+def test_int8_config3_all_widths_and_rows(K, M):
+    """Every (K, M) pair of the mixed-width layer through the int8 variant:
+    q_x, row scales and accumulators bit-exact on every row."""
     _check(synth.config3(K, M))
 
 

@@ -120,9 +120,13 @@ def test_linear_config2_m1(n):
     _check_case(synth.config2(n, 1))
 
 
+@pytest.mark.parametrize("M", synth.CONFIG3_M)
 @pytest.mark.parametrize("K", synth.CONFIG3_K)
-def test_linear_config3_m1(K):
-    _check_case(synth.config3(K, 1))
+def test_linear_config3_all_widths_and_rows(K, M):
+    """Every (K, M) pair of the mixed-width layer (k = n = 4096, 5% outlier
+    rows x20): M = 1 on the GEMV, M = 8 and 64 on the fused tensor-core
+    kernel; fp16 and fp32 outputs."""
+    _check_case(synth.config3(K, M))
 
 
 @pytest.mark.parametrize("K", range(1, 9))
@@ -134,8 +138,11 @@ def test_linear_m1_ragged_shapes(K, k, n):
 
 
 @pytest.mark.parametrize("M", [4, 16])
-def test_linear_config2_small_m(M):
-    _check_case(synth.config2(5120, M))
+@pytest.mark.parametrize("n", synth.CONFIG2_N)
+def test_linear_config2_small_m(n, M):
+    """The decode sweep's small-M rows at every width (k = 5120, K = 4, n up to
+    25600: 1600 tiles along n), fp16 and fp32 outputs."""
+    _check_case(synth.config2(n, M))
 
 
 @pytest.mark.parametrize("M", [2, 3, 31, 127, 128, 129, 200])
@@ -157,11 +164,6 @@ def test_linear_fused_small_m_short_k(K, k, M):
     accumulator stay idle); k = 256 and 384 give one and a half trellis stages;
     M = 33 and 100 use the wide x' layout."""
     _check_case(synth.linear_case(17, K * 1000 + k, M, k, 256, K, outlier_rows=0.1))
-
-
-@pytest.mark.parametrize("K,M", [(2, 8), (5, 8), (8, 64), (3, 64)])
-def test_linear_config3_small_m(K, M):
-    _check_case(synth.config3(K, M))
 
 
 def test_linear_prefill_config4_sampled_rows():
@@ -261,3 +263,37 @@ def test_linear_m1_k_too_large_for_gemv_takes_tensor_core_path():
     with pytest.raises(tq.Exl3Error) as e:
         tq.exl3_linear_gemv_noalloc(dev(case.x), dev(case.trellis), dev(case.suh), dev(case.svh), 7)
     assert e.value.code == tq.EXL3_ERR_SHAPE
+
+
+def test_linear_m1_concurrent_streams_share_the_gpu():
+    """The GEMV finishes a column block shared by several CTAs in whichever
+    CTA arrives last, with no CTA waiting for another, so it does not need
+    all its CTAs resident at once.  Four GEMVs on four streams (each with its
+    own workspace) run beside a stream of large matmuls that holds SMs; every
+    result must be bit-identical to the same linear run alone, with clean
+    device error words."""
+    case = synth.config2(25600, 1)
+    x, t, suh, svh = dev(case.x), dev(case.trellis), dev(case.suh), dev(case.svh)
+    need = tq.exl3_linear_workspace_size(1, case.k, case.n, case.K)
+    ref = tq.exl3_linear(x, t, suh, svh, 4, out_dtype=tq.EXL3_OUT_F32).clone()
+    assert_close(host(ref).astype(np.float64), oracle.linear(case.x, case.trellis, case.suh, case.svh, 4),
+                 "alone")
+    a = torch.randn(4096, 4096, device="cuda", dtype=torch.float16)
+    hog = torch.cuda.Stream()
+    streams = [torch.cuda.Stream() for _ in range(4)]
+    wss = [torch.zeros(need, dtype=torch.uint8, device="cuda") for _ in streams]
+    ys = [torch.empty((1, case.n), dtype=torch.float32, device="cuda") for _ in streams]
+    torch.cuda.synchronize()
+    for rep in range(3):
+        with torch.cuda.stream(hog):
+            b = a
+            for _ in range(20):
+                b = b @ a * 1e-3
+        for s, ws, y in zip(streams, wss, ys):
+            with torch.cuda.stream(s):
+                for _ in range(5):
+                    tq.exl3_linear(x, t, suh, svh, 4, out_dtype=tq.EXL3_OUT_F32, y=y, workspace_buf=ws, stream=s)
+        torch.cuda.synchronize()
+        for ws, y in zip(wss, ys):
+            assert torch.equal(y, ref)
+            assert tq.exl3_check_device_error(ws) == 0

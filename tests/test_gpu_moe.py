@@ -50,13 +50,16 @@ def test_moe_config5_full(T):
 
 
 def test_moe_config5_t4096_sampled_tokens():
+    """T = 4096 in full on the GPU (fp16 and fp32 outputs); the oracle
+    evaluates a seeded sample of tokens."""
     c = synth.config5(4096)
     d = _dev_case(c)
-    y = _run(c, d)
     rng = np.random.default_rng(50)
     tokens = np.unique(np.concatenate([[0, 4095], rng.choice(4096, 14, replace=False)])).astype(np.int32)
     ref = _oracle(c, tokens=tokens)
-    assert_close(y[tokens], ref, c.name + " sampled")
+    for od in (tq.EXL3_OUT_F16, tq.EXL3_OUT_F32):
+        y = _run(c, d, od)
+        assert_close(y[tokens], ref, f"{c.name} sampled out={od}")
 
 
 @pytest.mark.parametrize("E,topk,T", [(4, 2, 3), (1, 1, 5), (8, 8, 37), (1000, 4, 300)])

@@ -91,6 +91,7 @@ def lib():
         L.exl3_moe_workspace_size.restype = Z
         L.exl3_moe_grouped.argtypes = [P, I, I, P, P, I, I, P, P, P, I, P, Z, P]
         L.exl3_linear_gemv_noalloc.argtypes = [P, I, I, P, P, P, I, I, P, I, P]
+        L.exl3_noalloc_device_error.argtypes = [P, ctypes.POINTER(I)]
         L.exl3_linear_shards_workspace_size.argtypes = [I, I, I, I, I]
         L.exl3_linear_shards_workspace_size.restype = Z
         L.exl3_linear_shards.argtypes = [P, I, I, I, I, P, P, P, I, I, P, I, P, Z, P]
@@ -409,3 +410,12 @@ def exl3_linear_gemv_noalloc(x, trellis, suh, svh, K: int, codebook: int = EXL3_
                                           _ptr(suh, "suh", 2), _ptr(svh, "svh", 2), K, codebook,
                                           _ptr(y, "y"), out_dtype, _stream(stream)))
     return y
+
+
+def exl3_noalloc_device_error(stream=None) -> int:
+    """Device error word of the fixed scratch array used by
+    exl3_linear_gemv_noalloc on the current device (waits for the stream,
+    then reads and clears it; 0 = no device-side check failed)."""
+    v = ctypes.c_int(0)
+    _check(lib().exl3_noalloc_device_error(_stream(stream), ctypes.byref(v)))
+    return v.value

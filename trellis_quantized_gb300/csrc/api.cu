@@ -94,6 +94,53 @@ int exl3_cuda_check(cudaError_t e, const char *what) {
   return exl3_fail(EXL3_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
+int exl3_sm_count() {
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0, v = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 152;
+  }
+  const bool cached = dev >= 0 && dev < kMaxDevices;
+  if (cached && (v = cache[dev].load(std::memory_order_relaxed)) > 0) return v;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) {
+    cudaGetLastError();
+    return 152;
+  }
+  if (cached) cache[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 exl3_tmap_encode_fn() {
+  // a function-local static is initialised once, even with concurrent callers
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+cudaError_t exl3_ensure_smem(const void *kfn, size_t bytes, std::atomic<size_t> *per_dev) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool cached = dev >= 0 && dev < kMaxDevices;
+  if (cached && per_dev[dev].load(std::memory_order_acquire) >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e != cudaSuccess || !cached) return e;
+  size_t cur = per_dev[dev].load(std::memory_order_relaxed);
+  while (cur < bytes && !per_dev[dev].compare_exchange_weak(cur, bytes, std::memory_order_release)) {
+  }
+  return cudaSuccess;
+}
+
 #define EXL3_TRY(expr)            \
   do {                            \
     int _rc = (expr);             \
@@ -118,19 +165,6 @@ size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int sm_count() {
-  static int cached = 0;
-  if (cached) return cached;
-  int dev = 0, v = 0;
-  if (cudaGetDevice(&dev) == cudaSuccess &&
-      cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
-    cached = v;
-  else {
-    cudaGetLastError();
-    return 152;
-  }
-  return cached;
-}
 
 int check_ptr(const void *p, const char *name, bool required = true) {
   if (!p) return required ? exl3_fail(EXL3_ERR_ARG, "%s is NULL", name) : EXL3_OK;
@@ -276,7 +310,7 @@ MoeWs moe_ws(int T, int topk, int E, int hidden, int inter, int K13, int K2, boo
   // split over k into an even number of k steps (at least 4) per CTA.
   w.grid_mtiles = (int)(U < (size_t)w.max_mtiles ? U : (size_t)w.max_mtiles);
   const long tiles1 = (long)w.grid_mtiles * (inter / 128);
-  const int kb = hidden / 64, sms = sm_count();
+  const int kb = hidden / 64, sms = exl3_sm_count();
   w.splits = 1;
   for (int sp = 2; sp <= 8; ++sp)
     if (kb % sp == 0 && (kb / sp) % 2 == 0 && kb / sp >= 4 && tiles1 * sp <= sms) w.splits = sp;

@@ -14,9 +14,12 @@
 //    scale 2^-3.5 per side, butterfly stages 1, 2, ..., 64 of (a+b, a-b).
 #pragma once
 
+#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <atomic>
 
 #include "../../include/exl3.h"
 
@@ -150,3 +153,16 @@ __host__ __device__ constexpr int gcd_c(int a, int b) { return b == 0 ? a : gcd_
 // Defined in api.cu: thread-local error message and CUDA error capture.
 int exl3_fail(int code, const char *fmt, ...);
 int exl3_cuda_check(cudaError_t e, const char *what);
+
+// Device-dependent host state (SM counts, kernel attributes) is cached per
+// device ordinal, for ordinals below kMaxDevices (larger ones query each
+// time); the caches are safe to use from several host threads.
+constexpr int kMaxDevices = 64;
+// SM count of the current device (152 if the query fails).
+int exl3_sm_count();
+// Raise kfn's dynamic shared-memory limit on the current device to at least
+// `bytes` (cudaFuncSetAttribute applies per device); `per_dev` caches what
+// each device was given, one array per kernel.
+cudaError_t exl3_ensure_smem(const void *kfn, size_t bytes, std::atomic<size_t> *per_dev);
+// The driver's cuTensorMapEncodeTiled (NULL if unavailable), looked up once.
+PFN_cuTensorMapEncodeTiled_v12000 exl3_tmap_encode_fn();

@@ -388,30 +388,13 @@ __global__ void __launch_bounds__(Roles<NMAX>::WARPS * 32, 1) fused_tc_kernel(co
 
 using namespace exl3;
 
-static PFN_cuTensorMapEncodeTiled_v12000 ftc_tmap_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
+static PFN_cuTensorMapEncodeTiled_v12000 ftc_tmap_fn() { return exl3_tmap_encode_fn(); }
 
 // Number of k splits (one CTA per SM): the split count whose CTAs fill whole
 // waves best, keeping at least 4 trellis stages (16 k steps of 64) per CTA
 // (fewer splits on ties).  Splits fall on stage boundaries.
 int exl3_fused_tc_splits(int k, int n) {
-  static int sms = 0;
-  if (!sms) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 152;
-    cudaGetLastError();
-  }
+  const int sms = exl3_sm_count();
   const int kst = (k / 64 + 3) / 4, tiles = n / 128;
   int best = 1;
   double best_eff = 0.0;

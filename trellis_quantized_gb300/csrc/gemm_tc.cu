@@ -325,18 +325,7 @@ __global__ void __launch_bounds__((2 + epi_warps<BN, Q8>()) * 32, 1) gemm_tc_ker
 
 using namespace exl3;
 
-static PFN_cuTensorMapEncodeTiled_v12000 tmap_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
+static PFN_cuTensorMapEncodeTiled_v12000 tmap_encode_fn() { return exl3_tmap_encode_fn(); }
 
 // 2-D fp16 tensor [rows][cols] (cols contiguous), box [box_rows][64], 128-byte swizzle.
 static int make_tmap_f16(CUtensorMap *m, const void *base, int rows, int cols, int box_rows) {
@@ -365,13 +354,7 @@ int exl3_launch_gemm_tc(const uint16_t *xh, const uint16_t *wt, int M, int n, in
   const bool wide = (n % 256) == 0;
   rc = make_tmap_f16(&tb, wt, n, k, wide ? 256 : 128);
   if (rc) return rc;
-  static int sms = 0;
-  if (!sms) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) sms = 148;
-  }
+  const int sms = exl3_sm_count();
   gtc::Args a{M, n, k, reinterpret_cast<const __half *>(svh), y, row_scale, pre, err, acc_out,
               reinterpret_cast<const __half *>(bias)};
   const int tiles = ((M + gtc::BM - 1) / gtc::BM) * (n / (wide ? 256 : 128));

@@ -5,13 +5,12 @@
 //   y = RHT_out( sigma * sum_k x'_k (B_kn - 510) ) . svh,  x' = RHT_in(x . suh)
 //
 // The contraction uses the exact codebook value (B - 510) * sigma, of which
-// the fp16 weight is the rounding, and x' rounded to fp16 (as the tensor-core
-// paths do); both differences (< 2^-11 relative per term) stay inside the
-// output tolerance.  DP4A seeded with 0x6400 yields the fp16 value 1024 + B
-// in the low half of its result, which a mixed-precision FMA multiplies by
-// the fp16 x' into an fp32 accumulator: sum x' (1024 + B).  The offset,
-// 1534 * sum x' (1024 + 510 = 1534), is removed once per column block from
-// per-tile-row sums of x' kept beside x'.
+// the fp16 weight is the rounding (a difference below 2^-11 relative per
+// term, inside the output tolerance), and x' in fp32.  DP4A yields the
+// integer byte sum B, read as the bit pattern of the subnormal fp32 B 2^-149;
+// with x' held as x' 2^100 the product is exact, and one fp32 FMA adds it to
+// the column's accumulator: sum x' B.  The offset 510 * sum x' is removed once per column
+// block from per-tile-row sums of x' kept beside x'.
 //
 // Lane work.  A lane owns G >= 4 consecutive rows of one tile: 16 G weights
 // whose states come from CPL contiguous 16-byte chunks (128 CPL bits) plus
@@ -19,8 +18,7 @@
 // the first).  LPT = 16 / G lanes cover a tile and a warp covers one tile row
 // of the CTA's column block (128 or 256 columns).  Each window is cut out of
 // byte-aligned (possibly pre-shifted) words with one LOP/SHR/PRMT where it
-// can, hashed (IMAD), byte-summed by DP4A and accumulated by one
-// mixed-precision FMA.
+// can, hashed (IMAD), byte-summed by DP4A and accumulated by one fp32 FMA.
 //
 // Work split.  The work is the list of "rows" (column block c, tile row tk),
 // c-major.  One CTA per SM takes an equal contiguous range of that list, so
@@ -92,7 +90,7 @@ struct GemvArgs {
 
 constexpr int kGemvMaxOps = 4;        // ops one CTA's range may touch in GROUPED mode
 constexpr int kGemvMaxShards = 8;     // shards of different widths in one launch
-constexpr int kGemvPrePartials = 2;   // partials a finisher loads before its segment ends
+constexpr int kGemvPrePartials = 2;   // partials a block's first CTA loads before its segment ends
 constexpr int kGemvPreStages = 2;     // stages the producer loads before x' is ready
 
 // The pointers of op o (one op, the linear itself, when not GROUPED).
@@ -143,6 +141,77 @@ __device__ __forceinline__ int block_in_op(const GemvArgs &a, int c, int op) {
 }
 __device__ __forceinline__ int op_width(const GemvArgs &a, int op) { return a.var ? a.vn[op] : a.n; }
 
+// Whether all `others` CTAs sharing column block c besides its first have
+// published their partials (one acquire load, no waiting).
+__device__ __forceinline__ bool gemv_all_arrived(const GemvArgs &a, int c, int others, int lane) {
+  int got = 0;
+  if (lane == 0) {
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(got) : "l"(a.counters + c) : "memory");
+    if (got > others) set_device_error(a.err, kErrDirtyCounter);
+  }
+  got = __shfl_sync(0xffffffffu, got, 0);
+  __threadfence();
+  return got >= others;
+}
+
+// pre[j] = the partial of CTA i0 + 1 + j of column block c, for j below
+// min(cnt, kGemvPrePartials) (lane l: columns 128 g + 4 l .. +3).
+template <int NG>
+__device__ __forceinline__ void gemv_load_partials(const GemvArgs &a, int c, int i0, int cnt, int lane,
+                                                   float (&pre)[kGemvPrePartials][NG][4]) {
+#pragma unroll
+  for (int j = 0; j < kGemvPrePartials; ++j)
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+      float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (j < cnt)
+        r = __ldcg(reinterpret_cast<const float4 *>(a.partials + (long)(c + i0 + 1 + j) * (NG * 128) + g * 128 +
+                                                    lane * 4));
+      pre[j][g][0] = r.x;
+      pre[j][g][1] = r.y;
+      pre[j][g][2] = r.z;
+      pre[j][g][3] = r.w;
+    }
+}
+
+// p = the partial of CTA i of column block c.
+template <int NG>
+__device__ __forceinline__ void gemv_load_partial(const GemvArgs &a, int c, int i, int lane, float (&p)[NG][4]) {
+#pragma unroll
+  for (int g = 0; g < NG; ++g) {
+    const float4 r = __ldcg(reinterpret_cast<const float4 *>(a.partials + (long)(c + i) * (NG * 128) + g * 128 +
+                                                             lane * 4));
+    p[g][0] = r.x;
+    p[g][1] = r.y;
+    p[g][2] = r.z;
+    p[g][3] = r.w;
+  }
+}
+
+// v += the partial of CTA i of column block c.
+template <int NG>
+__device__ __forceinline__ void gemv_add_partial(const GemvArgs &a, int c, int i, int lane, float (&v)[NG][4]) {
+  float p[NG][4];
+  gemv_load_partial<NG>(a, c, i, lane, p);
+#pragma unroll
+  for (int g = 0; g < NG; ++g)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) v[g][e] += p[g][e];
+}
+
+// The block's svh and output bias for lane l's columns (zero when not
+// `load` or past the op's width).
+template <int NG>
+__device__ __forceinline__ void gemv_load_out_vectors(const __half *svh, const __half *bias, int col0, int nop,
+                                                      int lane, bool load, uint2 (&svv)[NG], uint2 (&bvv)[NG]) {
+#pragma unroll
+  for (int g = 0; g < NG; ++g) {
+    const bool mine = load && col0 + g * 128 < nop;
+    svv[g] = mine ? *reinterpret_cast<const uint2 *>(svh + col0 + g * 128 + lane * 4) : make_uint2(0u, 0u);
+    bvv[g] = mine && bias ? *reinterpret_cast<const uint2 *>(bias + col0 + g * 128 + lane * 4) : make_uint2(0u, 0u);
+  }
+}
+
 // The kernel body; maps holds the trellis tensor map (one per shard for
 // shards of different widths).
 template <int K, bool F32OUT, bool GROUPED>
@@ -160,8 +229,8 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap *maps, const GemvArg
   uint64_t *red_free = seg_full + 1;                                   // the flusher has read red
   uint64_t *xready = red_free + 1;                                     // the consumers' x' is ready
   constexpr int NOPS = GROUPED ? kGemvMaxOps : 1;
-  __half *xs = reinterpret_cast<__half *>(xready + 2);                 // [NOPS][k] fp16 x' (touched blocks)
-  float *rsum = reinterpret_cast<float *>(xs + NOPS * a.k);            // [NOPS][k/16] sum of x' per tile row
+  float *xs = reinterpret_cast<float *>(xready + 2);                   // [NOPS][k] x' 2^100 (touched blocks)
+  float *rsum = xs + NOPS * a.k;                                       // [NOPS][k/16] sum of x' per tile row
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int grid = gridDim.x, me = blockIdx.x;
@@ -273,57 +342,29 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap *maps, const GemvArg
       const int col0 = (GROUPED ? block_in_op(a, c, op) : c) * S::CTA_COLS;
       const uint32_t blk_first = (uint32_t)c * TKU, blk_last = min((uint32_t)(c + 1) * TKU, a.total) - 1;
       const int i_first = range_owner(blk_first, a.total, grid), i_last = range_owner(blk_last, a.total, grid);
-      // A block shared by several CTAs is finished by its first CTA, whose
-      // range ends in it (for the others it is the first or only segment,
-      // so their partials are usually stored long before).  The others
-      // store a partial in their (block, CTA) slot and make one release
-      // increment; the finisher waits (bounded) for all of them with
-      // acquire loads and adds the partials in CTA order.  It does the wait
-      // and loads the first kGemvPrePartials partials while its own
-      // consumers still decode the segment, off the launch's critical path.
-      const bool shared = i_first != i_last, finisher = shared && me == i_first;
+      // A block shared by several CTAs is finished by whichever of them
+      // publishes its partial sum last: each stores its partial in the slot
+      // of (block, CTA) and makes one acquire-release increment of the
+      // block's counter, and the one that sees every other arrival adds all
+      // partials in CTA order (its own from registers, the same bits as the
+      // stored one), so the result does not depend on timing and no CTA ever
+      // waits for another.  The block's first CTA, whose range ends in it
+      // (for the others it is the first segment, done long before), looks at
+      // the counter without waiting, before and after its own segment; when
+      // every other CTA is in it adds their partials straight away (loaded
+      // while its consumers still decode) and publishes nothing.
+      const bool shared = i_first != i_last, first = shared && me == i_first;
       const int others = i_last - i_first;
       float pre[kGemvPrePartials][S::NG][4];
-      if (finisher) {
-        if (lane == 0) {
-          const long long w0 = clock64();
-          int got = 0;
-          while (true) {
-            asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(got) : "l"(a.counters + c) : "memory");
-            if (got >= others) break;
-            if (clock64() - w0 > tc::kWaitLimit) {
-              set_device_error(a.err, kErrBounds);
-              break;
-            }
-            __nanosleep(64);
-          }
-          if (got > others) set_device_error(a.err, kErrDirtyCounter);
-        }
-        __syncwarp();
-#pragma unroll
-        for (int j = 0; j < kGemvPrePartials; ++j)
-#pragma unroll
-          for (int g = 0; g < S::NG; ++g) {
-            float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (j < others)
-              r = __ldcg(reinterpret_cast<const float4 *>(a.partials + (long)(c + i_first + 1 + j) * S::CTA_COLS +
-                                                          g * 128 + lane * 4));
-            pre[j][g][0] = r.x;
-            pre[j][g][1] = r.y;
-            pre[j][g][2] = r.z;
-            pre[j][g][3] = r.w;
-          }
+      bool all_in = false;
+      if (first) {
+        all_in = gemv_all_arrived(a, c, others, lane);
+        if (all_in) gemv_load_partials<S::NG>(a, c, i_first, others, lane, pre);
       }
-      uint2 svv[S::NG];   // the block's svh (and bias), loaded ahead as well
+      uint2 svv[S::NG];   // the block's svh (and bias), loaded ahead where this CTA usually finishes
       uint2 bvv[S::NG];
       const bool has_bias = !GROUPED && a.bias != nullptr;
-#pragma unroll
-      for (int g = 0; g < S::NG; ++g) {
-        const bool mine = (!shared || finisher) && col0 + g * 128 < nop;
-        svv[g] = mine ? *reinterpret_cast<const uint2 *>(P.svh + col0 + g * 128 + lane * 4) : make_uint2(0u, 0u);
-        bvv[g] = mine && has_bias ? *reinterpret_cast<const uint2 *>(a.bias + col0 + g * 128 + lane * 4)
-                                  : make_uint2(0u, 0u);
-      }
+      gemv_load_out_vectors<S::NG>(P.svh, has_bias ? a.bias : nullptr, col0, nop, lane, !shared || first, svv, bvv);
       if (!*s_abort && !tc::mbar_wait(seg_full, sp)) {
         if (lane == 0) set_device_error(a.err, kErrBounds);
         *s_abort = 1;
@@ -342,7 +383,7 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap *maps, const GemvArg
       }
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(red_free);
-      // every column's sum is sum x' (1024 + B): remove 1534 * (the segment's sum of x')
+      // every column's sum is 2^-49 sum x' B: remove 510 * (the segment's sum of x')
       float sg = 0.f;
       {
         const int tk_first = (int)(t - (uint32_t)c * TKU), nrows = (int)(seg_end - t);
@@ -353,20 +394,16 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap *maps, const GemvArg
 #pragma unroll
       for (int g = 0; g < S::NG; ++g)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) v[g][e] = fmaf(-1534.0f, sg, v[g][e]) * kSigma;
+        for (int e = 0; e < 4; ++e) v[g][e] = fmaf(-510.0f, sg, v[g][e] * kAccUnscale) * kSigma;
 
       bool finish = true;
       if (shared) {
-        if (!finisher) {
-#pragma unroll
-          for (int g = 0; g < S::NG; ++g)
-            *reinterpret_cast<float4 *>(a.partials + (long)(c + me) * S::CTA_COLS + g * 128 + lane * 4) =
-                make_float4(v[g][0], v[g][1], v[g][2], v[g][3]);
-          // the warp barrier orders every lane's stores before lane 0's release
-          __syncwarp();
-          if (lane == 0) asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(a.counters + c) : "memory");
-          finish = false;
-        } else {
+        if (first && !all_in) {   // a second look, now that the own segment is done
+          all_in = gemv_all_arrived(a, c, others, lane);
+          if (all_in) gemv_load_partials<S::NG>(a, c, i_first, others, lane, pre);
+        }
+        if (first && all_in) {
+          // every other CTA is in: add their partials in CTA order
 #pragma unroll
           for (int j = 0; j < kGemvPrePartials; ++j)
             if (j < others)
@@ -374,19 +411,47 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap *maps, const GemvArg
               for (int g = 0; g < S::NG; ++g)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) v[g][e] += pre[j][g][e];
-          for (int i = i_first + 1 + kGemvPrePartials; i <= i_last; ++i) {
+          for (int i = i_first + 1 + kGemvPrePartials; i <= i_last; ++i) gemv_add_partial<S::NG>(a, c, i, lane, v);
+        } else {
+          // publish this CTA's partial and arrive; the last to arrive finishes
 #pragma unroll
-            for (int g = 0; g < S::NG; ++g) {
-              const float4 r = __ldcg(reinterpret_cast<const float4 *>(a.partials + (long)(c + i) * S::CTA_COLS +
-                                                                       g * 128 + lane * 4));
-              v[g][0] += r.x;
-              v[g][1] += r.y;
-              v[g][2] += r.z;
-              v[g][3] += r.w;
+          for (int g = 0; g < S::NG; ++g)
+            __stcg(reinterpret_cast<float4 *>(a.partials + (long)(c + me) * S::CTA_COLS + g * 128 + lane * 4),
+                   make_float4(v[g][0], v[g][1], v[g][2], v[g][3]));
+          __threadfence();
+          __syncwarp();
+          int old = 0;
+          if (lane == 0)
+            asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(a.counters + c) : "memory");
+          old = __shfl_sync(0xffffffffu, old, 0);
+          if (old > others && lane == 0) set_device_error(a.err, kErrDirtyCounter);
+          finish = old >= others;
+          if (finish) {
+            __threadfence();
+            float own[S::NG][4];
+#pragma unroll
+            for (int g = 0; g < S::NG; ++g)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) own[g][e] = v[g][e];
+            for (int i = i_first; i <= i_last; ++i) {   // CTA order: p[i_first] + p[i_first + 1] + ...
+              float p[S::NG][4];
+              if (i == me) {
+#pragma unroll
+                for (int g = 0; g < S::NG; ++g)
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) p[g][e] = own[g][e];
+              } else {
+                gemv_load_partial<S::NG>(a, c, i, lane, p);
+              }
+#pragma unroll
+              for (int g = 0; g < S::NG; ++g)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) v[g][e] = i == i_first ? p[g][e] : v[g][e] + p[g][e];
             }
+            if (!first) gemv_load_out_vectors<S::NG>(P.svh, has_bias ? a.bias : nullptr, col0, nop, lane, true, svv, bvv);
           }
-          if (lane == 0) a.counters[c] = 0;   // leave the workspace clean
         }
+        if (finish && lane == 0) a.counters[c] = 0;   // leave the workspace clean
       }
       if (finish) {
         // ---- output transform of the block's 128-column groups
@@ -456,7 +521,7 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap *maps, const GemvArg
       if (GROUPED && P.bad && lane == 0 && i % KC == 0) set_device_error(a.err, kErrExpertId);
       const int e0 = ((c0 + i - jop * KC) % KC) * 512 + lane * 16;
       const bool live = e0 < a.k;   // k is a multiple of 128: whole 8-lane groups
-      __half *xso = xs + jop * a.k;
+      float *xso = xs + jop * a.k;
       float *rso = rsum + jop * (a.k / 16);
       float v[16];
       if (live && GROUPED && a.act_in) {
@@ -494,17 +559,16 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap *maps, const GemvArg
       }
       fwht128_x8(v, lane);
       if (live) {
-        uint4 o[2];
-        __half2 *oh = reinterpret_cast<__half2 *>(o);
         float rs = 0.f;   // the 16 elements are one tile row
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          oh[j] = __floats2half2_rn(v[2 * j] * kRhtScale, v[2 * j + 1] * kRhtScale);
-          rs += __low2float(oh[j]) + __high2float(oh[j]);
+        for (int j = 0; j < 16; ++j) {
+          v[j] *= kRhtScale * kXScale;   // x' 2^100: the same rounding as x', then an exact scale
+          rs += v[j];
         }
-        *reinterpret_cast<uint4 *>(xso + e0) = o[0];
-        *reinterpret_cast<uint4 *>(xso + e0 + 8) = o[1];
-        rso[e0 >> 4] = rs;
+#pragma unroll
+        for (int j = 0; j < 16; j += 4)
+          *reinterpret_cast<float4 *>(xso + e0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+        rso[e0 >> 4] = rs * (1.0f / kXScale);
       }
     }
   }
@@ -527,7 +591,7 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap *maps, const GemvArg
     const int c = (int)(t / TKU);
     const uint32_t seg_end = min(t1, (uint32_t)(c + 1) * TKU);
     const int tk_first = (int)(t - (uint32_t)c * TKU), nrows = (int)(seg_end - t);
-    const __half *xso = xs + (GROUPED ? op_of_block(a, c) - op0 : 0) * a.k;   // this op's x'
+    const float *xso = xs + (GROUPED ? op_of_block(a, c) - op0 : 0) * a.k;   // this op's x' 2^100
 
     float acc[16];
 #pragma unroll
@@ -558,9 +622,15 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap *maps, const GemvArg
           }
           w[S::NW] = *reinterpret_cast<const uint32_t *>(rowp + next_off);
           const int tk = tk_first + r0 + j;
-          unsigned short xr[S::G];
+          float xr[S::G];
 #pragma unroll
-          for (int i = 0; i < S::G; ++i) xr[i] = __half_as_ushort(xso[tk * 16 + S::G * q + i]);
+          for (int i = 0; i < S::G; i += 4) {
+            const float4 x4 = *reinterpret_cast<const float4 *>(xso + tk * 16 + S::G * q + i);
+            xr[i] = x4.x;
+            xr[i + 1] = x4.y;
+            xr[i + 2] = x4.z;
+            xr[i + 3] = x4.w;
+          }
           decode_accumulate<K, 0>(w, xr, acc);
         }
       }
@@ -611,40 +681,17 @@ __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
   gemv_body<K, F32OUT, true>(maps.m, a);
 }
 
-static int gemv_sm_count() {
-  static int cached = 0;
-  if (cached) return cached;
-  int dev = 0, v = 0;
-  if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) ==
-                                                cudaSuccess && v > 0)
-    cached = v;
-  else {
-    cudaGetLastError();
-    return 152;
-  }
-  return cached;
-}
+static int gemv_sm_count() { return exl3_sm_count(); }
 
-static PFN_cuTensorMapEncodeTiled_v12000 gemv_tmap_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
+static PFN_cuTensorMapEncodeTiled_v12000 gemv_tmap_fn() { return exl3_tmap_encode_fn(); }
 
 template <int K, bool F32, bool GROUPED = false>
 struct Launcher {
   using S = GemvShape<K>;
-  // ring stages that fit beside the reduction buffers, x' (2 bytes per k)
+  // ring stages that fit beside the reduction buffers, x' (4 bytes per k)
   // and its per-tile-row sums (4 bytes per 16 k), for up to kGemvMaxOps ops
   // in GROUPED mode
-  static size_t xbytes(int k) { return (GROUPED ? kGemvMaxOps : 1) * (2 * (size_t)k + (size_t)k / 4); }
+  static size_t xbytes(int k) { return (GROUPED ? kGemvMaxOps : 1) * (4 * (size_t)k + (size_t)k / 4); }
   static int stages(int k) {
     const long avail = (long)kGemvSmemMax - S::FIXED_B - (long)xbytes(k);
     long st = avail / S::STAGE_B;
@@ -654,13 +701,9 @@ struct Launcher {
   static size_t smem(int k, int st) { return (size_t)st * S::STAGE_B + S::FIXED_B + xbytes(k); }
   static cudaError_t launch(const CUtensorMap &tm, const GemvArgs &a, int grid, cudaStream_t s, bool prefetch) {
     const size_t sm = smem(a.k, a.stages);
-    static size_t attr = 0;
-    if (attr < sm) {
-      cudaError_t e = cudaFuncSetAttribute(gemv_m1_kernel<K, F32, GROUPED>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-      if (e != cudaSuccess) return e;
-      attr = sm;
-    }
+    static std::atomic<size_t> attr[kMaxDevices];   // per device: the attribute is per device
+    cudaError_t e = exl3_ensure_smem(reinterpret_cast<const void *>(gemv_m1_kernel<K, F32, GROUPED>), sm, attr);
+    if (e != cudaSuccess) return e;
     cudaLaunchAttribute attrs[1];
     attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attrs[0].val.programmaticStreamSerializationAllowed = 1;
@@ -1047,13 +1090,9 @@ cudaError_t exl3_launch_gemv_shards_var(const uint16_t *x, int S, int k, const i
 #define EXL3_GSV(KK, F32)                                                                                    \
   do {                                                                                                     \
     const size_t sm = Launcher<KK, F32, true>::smem(k, a.stages);                                          \
-    static size_t attr = 0;                                                                                \
-    if (attr < sm) {                                                                                       \
-      e = cudaFuncSetAttribute(gemv_shards_kernel<KK, F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,   \
-                               (int)sm);                                                                   \
-      if (e != cudaSuccess) break;                                                                         \
-      attr = sm;                                                                                           \
-    }                                                                                                      \
+    static std::atomic<size_t> attr[kMaxDevices];                                                          \
+    e = exl3_ensure_smem(reinterpret_cast<const void *>(gemv_shards_kernel<KK, F32>), sm, attr);           \
+    if (e != cudaSuccess) break;                                                                           \
     cfg.blockDim = dim3(GemvShape<KK>::THREADS);                                                           \
     cfg.dynamicSmemBytes = sm;                                                                             \
     e = cudaLaunchKernelEx(&cfg, gemv_shards_kernel<KK, F32>, maps, a);                                    \

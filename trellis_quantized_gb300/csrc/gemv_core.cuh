@@ -40,29 +40,27 @@ struct GemvShape {
 };
 
 
-// acc += x * h, x and h binary16 (h = low half of r), acc binary32.
-__device__ __forceinline__ float fma_f16_f32(unsigned short x, uint32_t r, float acc) {
-  asm("{\n.reg .f16 hx, hh;\n.reg .b16 lo, hi;\nmov.b32 {lo, hi}, %1;\nmov.b16 hh, lo;\nmov.b16 hx, %2;\n"
-      "fma.rn.f32.f16 %0, hx, hh, %0;\n}\n"
-      : "+f"(acc)
-      : "r"(r), "h"(x));
-  return acc;
-}
-
 __device__ __forceinline__ void consumer_sync(int nthreads) {
   asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
 
-// Decode the lane's 16 G weights and accumulate x'_row * (1024 + B) into the
-// 16 column accumulators.
+// x' is held scaled by 2^100 (kXScale) and the byte sum B of a weight, an
+// integer below 2^10, is read as the bit pattern of the fp32 value B * 2^-149
+// (a subnormal, exact): their product is x' B 2^-49, exact in fp32, so one
+// fp32 FMA accumulates a weight with fp32 rounding of the sums only.  The
+// column sums carry 510 * sum x', removed once per column block from
+// per-tile-row sums of x'.
+constexpr float kXScale = 0x1p100f;      // x' scale in shared memory
+constexpr float kAccUnscale = 0x1p49f;   // accumulator scale back to x' B
+
+// Decode the lane's 16 G weights and accumulate x'_row * B into the 16
+// column accumulators.
 template <int K, int J>
 __device__ __forceinline__ void decode_accumulate(const uint32_t (&w)[GemvShape<K>::NW + 1],
-                                                  const unsigned short (&xr)[GemvShape<K>::G],
-                                                  float (&acc)[16]) {
+                                                  const float (&xr)[GemvShape<K>::G], float (&acc)[16]) {
   if constexpr (J < 16 * GemvShape<K>::G) {
-    const uint32_t s = window_at<J * K>(w);
-    const uint32_t h = __dp4a(s * kMul1, 0x01010101u, 0x6400u);   // fp16 bits of 1024 + B
-    acc[J & 15] = fma_f16_f32(xr[J >> 4], h, acc[J & 15]);
+    const uint32_t b = __dp4a(window_at<J * K>(w) * kMul1, 0x01010101u, 0u);
+    acc[J & 15] = fmaf(xr[J >> 4], __uint_as_float(b), acc[J & 15]);
     decode_accumulate<K, J + 1>(w, xr, acc);
   }
 }

@@ -451,18 +451,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) moe_fused_kernel(const __grid_
 
 using namespace exl3;
 
-static PFN_cuTensorMapEncodeTiled_v12000 mf_tmap_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
+static PFN_cuTensorMapEncodeTiled_v12000 mf_tmap_fn() { return exl3_tmap_encode_fn(); }
 
 static int mf_encode(CUtensorMap *m, CUtensorMapDataType dt, int rank, const void *base, const cuuint64_t *dims,
                      const cuuint64_t *strides, const cuuint32_t *box, CUtensorMapSwizzle sw, const char *what) {
@@ -588,14 +577,7 @@ int exl3_launch_moe_fused_down(const uint16_t *hin, int U, int hidden, int inter
   // two output tiles per CTA (one fill and one epilogue for both) when each
   // tile's pairs fill whole trellis stages and the grid still covers the SMs
   // twice over; few routed rows keep one tile per CTA for parallelism
-  static int sms = 0;
-  if (!sms) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
-                                                  cudaSuccess || sms <= 0)
-      sms = 152;
-    cudaGetLastError();
-  }
+  const int sms = exl3_sm_count();
   a.ntc = ((a.KB / 2) % 2 == 0 && (long)max_mtiles * (a.NT / 2) >= 2L * sms) ? 2 : 1;
   return mf_launch<2>(K, t0, t0, tt, a, max_mtiles * ((a.NT + a.ntc - 1) / a.ntc), s);
 }

@@ -18,7 +18,9 @@
 // stream capture.  All calls share the array and it keeps the last call's
 // contents: each call clears the error word and the counters it uses, and
 // calls that overlap on the GPU (different streams, or several host threads)
-// race on it.
+// race on it.  exl3_noalloc_device_error reads (and clears) the error word,
+// which a call sets when one of its bounded waits runs out or an index check
+// fails; such a call's y is incomplete.
 #include <mutex>
 
 #include "exl3_common.cuh"
@@ -37,7 +39,6 @@ constexpr size_t kNoAllocScratchBytes = 2u << 20;   // the stated maximum
 constexpr size_t kCtrl = 256;                        // error word
 constexpr size_t kCounterBytes = 8192 * sizeof(int); // up to n / 128 = 8192 column blocks
 constexpr size_t kPartialsOff = kCtrl + kCounterBytes;
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
@@ -110,4 +111,20 @@ extern "C" int exl3_linear_gemv_noalloc(const uint16_t *x, int k, int n, const u
   return exl3_cuda_check(exl3_launch_gemv_m1(x, trellis, suh, svh, k, n, K, y, out_dtype == EXL3_OUT_F32,
                                              partials, counters, err, grid, stream),
                          "gemv launch");
+}
+
+extern "C" int exl3_noalloc_device_error(exl3_stream_t stream, int *err_out) {
+  if (!err_out) return exl3_fail(EXL3_ERR_ARG, "err_out is NULL");
+  void *scratch = nullptr;
+  int rc = scratch_for_current_device(&scratch);
+  if (rc) return rc;
+  rc = exl3_cuda_check(cudaStreamSynchronize(stream), "cudaStreamSynchronize");
+  if (rc) return rc;
+  int v = 0;
+  rc = exl3_cuda_check(cudaMemcpy(&v, scratch, sizeof v, cudaMemcpyDeviceToHost), "read the error word");
+  if (rc) return rc;
+  rc = exl3_cuda_check(cudaMemset(scratch, 0, sizeof v), "clear the error word");
+  if (rc) return rc;
+  *err_out = v;
+  return EXL3_OK;
 }
