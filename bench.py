@@ -62,6 +62,11 @@ def aggregate_replicas(out: dict, dist, device) -> dict:
     return res
 WORKLOAD = "dense decode GEMV sweep k=5120 n={5120,17408,25600} K=4 M=1 mul1, fp16 out"
 FALLBACK_HBM_GBS = 6800.0
+# The mul1 decode's ceiling at K = 4 on this chip (ubench/pipes.cu, bench.py
+# --only pipes): hash + byte sum + accumulate share one 64-lane pipe, ~26
+# weights per clock per SM = 26 * 152 * 2.07 GHz * 0.5 B = 4.09 TB/s, 0.60 of
+# the measured 6767 GB/s copy rate.
+DECODE_CEILING_FRAC_K4 = 0.60
 FALLBACK_BF16_TFLOPS = 1900.0
 
 # dram bytes (read + write) per launch from an ncu capture of gemv_m1_kernel<4>
@@ -210,12 +215,17 @@ def run_ours(args):
                 launch(d, cp)
         single.append(g)
     # Per-kernel duration for the roofline: 30 launches of the largest linear
-    # in one graph, launched plainly (no overlap between launches).
-    tq.exl3_set_weight_prefetch(False)
+    # in one graph, launched as in the step (programmatic dependent launches
+    # when weight_prefetch), and the same 30 launched plainly for reference.
     big = len(dcases) - 1
     reps_k = 30
     gk = torch.cuda.CUDAGraph()
     with torch.cuda.graph(gk):
+        for i in range(reps_k):
+            launch(dcases[big], i % copies)
+    tq.exl3_set_weight_prefetch(False)
+    gkp = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gkp):
         for i in range(reps_k):
             launch(dcases[big], i % copies)
     tq.exl3_set_weight_prefetch(prefetch)
@@ -223,6 +233,7 @@ def run_ours(args):
         single[i % copies].replay()
     graphs[0].replay()
     gk.replay()
+    gkp.replay()
     torch.cuda.synchronize()
 
     stream = torch.cuda.current_stream()
@@ -249,6 +260,12 @@ def run_ours(args):
             gk.replay()
         k1.record(stream)
         torch.cuda.synchronize()
+        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        p0.record(stream)
+        for _ in range(kreps):
+            gkp.replay()
+        p1.record(stream)
+        torch.cuda.synchronize()
         time.sleep(0.2)
     total_ms = t_start.elapsed_time(t_end)
     ms_per_step = total_ms / args.steps
@@ -257,6 +274,7 @@ def run_ours(args):
     hbm, bf16, src = peaks()
     big_bytes = linear_bytes(dcases[big]["case"])
     kern_ms = k0.elapsed_time(k1) / (kreps * reps_k)
+    plain_ms = p0.elapsed_time(p1) / (kreps * reps_k)
     achieved = big_bytes / (kern_ms * 1e-3) / 1e9
     traffic = None
     if TRAFFIC["sha1"] and TRAFFIC["sha1"] == files_sha1(TRAFFIC["files"]):
@@ -265,12 +283,17 @@ def run_ours(args):
                 "peak": hbm, "peak_source": src, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                 "traffic": traffic, "kernel_us": round(kern_ms * 1e3, 2),
                 "algorithmic_bytes_per_launch": big_bytes,
-                "timing": "CUDA events around 20 replays of a graph of 30 plain launches (3 rotating weight copies)"}
+                "kernel_us_plain_launches": round(plain_ms * 1e3, 2),
+                "frac_plain_launches": round(big_bytes / (plain_ms * 1e-3) / 1e9 / hbm, 4),
+                "decode_ceiling_frac": DECODE_CEILING_FRAC_K4,
+                "timing": "CUDA events around 20 replays of a graph of 30 launches (3 rotating weight copies), "
+                          "launched as in the step (programmatic dependent launches when weight_prefetch); "
+                          "kernel_us_plain_launches: the same without overlap between launches"}
 
     # e2e: the step's inputs (the three linears' x, packed in one pinned host
     # buffer) go host -> device in one copy, the linears run through the C ABI
-    # on views of the device copy, and their outputs (packed) come back in one
-    # copy; both copies are inside the timed region
+    # on views of the device copy, and their outputs (packed) come back to
+    # pinned host memory in one copy; both copies are inside the timed region
     kx = [d["case"].k for d in dcases]
     ny = [d["case"].n for d in dcases]
     hx = torch.from_numpy(np.concatenate([d["case"].x.reshape(-1) for d in dcases])).pin_memory()
@@ -295,28 +318,57 @@ def run_ours(args):
         hy.copy_(dy, non_blocking=True)
 
     e2e_steps = max(10, args.steps // 4)
+    e2e_steps -= e2e_steps % chunk
     stream = torch.cuda.current_stream()
     for i in range(3):
         e2e_step(i)
     torch.cuda.synchronize()
+    # eager: one C-ABI call per linear from Python each step
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(e2e_steps):
         e2e_step(i)
     e1.record(stream)
     torch.cuda.synchronize()
+    eager_ms = e0.elapsed_time(e1) / e2e_steps
+    # as a decode loop runs it: the same calls and copies captured in CUDA
+    # graphs (`chunk` steps per graph, one graph per starting weight copy)
+    egraphs = []
+    for cp in range(copies):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for jj in range(chunk):
+                e2e_step(cp + jj)
+        egraphs.append(g)
+    for g in egraphs:
+        g.replay()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    done = 0
+    while done < e2e_steps:
+        egraphs[(done // chunk) % copies].replay()
+        done += chunk
+    e1.record(stream)
+    torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     ref_y = [dcases[j]["y"] for j in range(len(dcases))]
     for j in range(len(dcases)):   # the packed path computes what the per-linear path did
         assert torch.equal(dy[int(yo[j]):int(yo[j + 1])].view(1, -1), ref_y[j]), "e2e output differs"
+        assert torch.equal(hy[int(yo[j]):int(yo[j + 1])].view(1, -1), ref_y[j].cpu()), "e2e host copy differs"
+    hy_bytes = hy.numel() * hy.element_size()
     e2e = {"value": round(step_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
            "h2d_bytes_per_step": int(hx.numel() * hx.element_size()),
-           "d2h_bytes_per_step": int(hy.numel() * hy.element_size()),
-           "timing": "eager C-ABI calls; one packed host->device copy of the step's x and one packed "
-                     "device->host copy of its y per step, inside the timed region"}
+           "d2h_bytes_per_step": int(hy_bytes),
+           "ms_per_step": round(e2e_ms, 5),
+           "eager": {"value": round(step_bytes / (eager_ms * 1e-3) / 1e9, 1), "ms_per_step": round(eager_ms, 5)},
+           "timing": "per step: one packed host->device copy of the step's x (pinned), the three linears "
+                     "through the C ABI, one packed device->host copy of their y (pinned), all inside the timed "
+                     "region, in stream order; captured in CUDA graphs of 10 steps as a decode loop runs them "
+                     "(eager: the same calls issued from Python every step)"}
 
     prefill = bench_prefill(args, bf16, src) if not args.skip_prefill else None
     extras = bench_extras() if not args.skip_prefill else None
+    configs = bench_configs() if not args.skip_prefill else None
     for d in dcases:
         assert tq.exl3_check_device_error(d["ws"]) == 0
 
@@ -332,7 +384,8 @@ def run_ours(args):
         "gpu_launches": int(args.steps * len(dcases)),
         "step": "the three M=1 linears (one GEMV kernel each; programmatic dependent launches when "
                 "weight_prefetch), captured 10 steps per CUDA graph",
-        "roofline": roofline, "e2e": e2e, "clocks": clk.summary(), "prefill": prefill, "other": extras,
+        "roofline": roofline, "e2e": e2e, "clocks": clk.summary(), "prefill": prefill, "configs": configs,
+        "other": extras,
     }
     if not args.skip_cpu and _world() == 1:   # the oracle baseline: rank 0 of a one-GPU run only
         out["cpu_baseline"] = cpu_baseline(args)
@@ -403,21 +456,115 @@ def _timed(fn, reps=10, warm=3):
     return a.elapsed_time(b) / (3 * reps)
 
 
+L2_BYTES = 129 * 2 ** 20       # GB300 L2; rotated weight copies exceed 2x this
+ROTATE_BYTES = 2 * L2_BYTES + 8 * 2 ** 20
+
+
+def _copies_for(nbytes: int, minimum: int = 3) -> int:
+    """Weight copies to rotate so that together they exceed twice the L2."""
+    return max(minimum, -(-ROTATE_BYTES // max(nbytes, 1)))
+
+
+def _timed_rotating(calls, rounds=4, warm=2):
+    """Device time per call of a list of closures (one per weight copy, so
+    that consecutive calls read different copies): `rounds` passes over the
+    list captured in one CUDA graph, replayed and timed with CUDA events."""
+    import torch
+    for _ in range(warm):
+        for f in calls:
+            f()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(rounds):
+            for f in calls:
+                f()
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(2):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / (2 * rounds * len(calls))
+
+
+def _linear_line(case, ms, hbm):
+    gb = linear_bytes(case) / (ms * 1e-3) / 1e9
+    return {"us": round(ms * 1e3, 2), "GBs": round(gb, 1), "frac": round(gb / hbm, 4),
+            "tflops": round(2.0 * case.M * case.k * case.n / (ms * 1e-3) / 1e12, 2)}
+
+
+def bench_configs(which=("1", "2", "3")):
+    """Every linear workload, each call timed on weight copies that rotate
+    through more than twice the L2 (so the weights come from HBM), M = 1
+    with weight prefetch on as in a decode loop:
+      config1  k=2048 n=512 K=4 M=1 (a latency figure: 0.5 MB of weights)
+      config2  k=5120, n in {5120, 17408, 25600}, K=4, M in {1, 4, 16}, fp16 and fp32 out
+      config3  k=n=4096, K=2..8, M in {1, 8, 64} (fp16 out; int8 variant at M=64)"""
+    import torch
+    import trellis_quantized_gb300 as tq
+    hbm = peaks()[0]
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16
+                                     else np.ascontiguousarray(a)).cuda()
+    prev = tq.exl3_set_weight_prefetch(True)
+    out = {}
+
+    def run(case, out_dtype=tq.EXL3_OUT_F16, int8=False):
+        x, suh, svh = dev(case.x), dev(case.suh), dev(case.svh)
+        base = dev(case.trellis)
+        ts = [base] + [base.clone() for _ in range(_copies_for(base.numel() * 2) - 1)]
+        if int8:
+            ws = tq.workspace(tq.exl3_linear_int8_workspace_size(case.M, case.k, case.n, case.K))
+        else:
+            ws = tq.workspace(tq.exl3_linear_workspace_size(case.M, case.k, case.n, case.K))
+        y = torch.empty((case.M, case.n), dtype=torch.float32 if out_dtype == tq.EXL3_OUT_F32 else torch.float16,
+                        device="cuda")
+        if int8:
+            calls = [lambda t=t: tq.exl3_linear_int8(x, t, suh, svh, case.K, y=y, workspace_buf=ws) for t in ts]
+        else:
+            calls = [lambda t=t: tq.exl3_linear(x, t, suh, svh, case.K, out_dtype=out_dtype, y=y, workspace_buf=ws)
+                     for t in ts]
+        ms = _timed_rotating(calls, rounds=2 if case.M > 16 else 4)
+        assert tq.exl3_check_device_error(ws) == 0
+        del ts, ws, y
+        return ms
+
+    try:
+        if "1" in which:
+            c = synth.config1()
+            out["config1_k2048_n512_K4_M1"] = dict(_linear_line(c, run(c), hbm),
+                                                   note="0.5 MB of weights: a latency figure (launch-bound)")
+        if "2" in which:
+            for n in synth.CONFIG2_N:
+                for M in synth.CONFIG2_M:
+                    c = synth.config2(n, M)
+                    for od, tag in ((tq.EXL3_OUT_F16, "f16"), (tq.EXL3_OUT_F32, "f32")):
+                        out[f"config2_k5120_n{n}_K4_M{M}_{tag}"] = _linear_line(c, run(c, od), hbm)
+        if "3" in which:
+            for K in synth.CONFIG3_K:
+                for M in synth.CONFIG3_M:
+                    c = synth.config3(K, M)
+                    out[f"config3_k4096_n4096_K{K}_M{M}"] = _linear_line(c, run(c), hbm)
+                c = synth.config3(K, 64)
+                out[f"config3_k4096_n4096_K{K}_M64_int8"] = _linear_line(c, run(c, int8=True), hbm)
+    finally:
+        tq.exl3_set_weight_prefetch(prev)
+    return {"per_call": out, "peak_GBs": hbm,
+            "timing": "CUDA graph of back-to-back calls over weight copies rotating through > 2x L2; "
+                      "GB/s = packed trellis + x + suh + svh + y bytes per call"}
+
+
+MOE_T = (1, 16, 32, 64, 128, 4096)
+
+
 def bench_extras(only=None, moe_tokens=None):
     """Small-M linears (config 2 shapes) and the grouped MoE (config 5) per call."""
     import torch
     import trellis_quantized_gb300 as tq
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16
                                      else np.ascontiguousarray(a)).cuda()
-    small = {}
-    for M in ((4, 16) if only in (None, "small") else ()):
-        c = synth.config2(17408, M)
-        x, t, suh, svh = dev(c.x), dev(c.trellis), dev(c.suh), dev(c.svh)
-        ws = tq.workspace(tq.exl3_linear_workspace_size(M, c.k, c.n, c.K))
-        y = torch.empty((M, c.n), dtype=torch.float16, device="cuda")
-        ms = _timed(lambda: tq.exl3_linear(x, t, suh, svh, 4, y=y, workspace_buf=ws))
-        small[f"M{M}"] = {"ms": round(ms, 4), "GBs": round(linear_bytes(c) / (ms * 1e-3) / 1e9, 1),
-                          "tflops": round(2.0 * M * c.k * c.n / (ms * 1e-3) / 1e12, 2)}
     # fused shards: gate and up of the dense family (2 x k=5120 -> n=17408,
     # K=4) at M = 1, as one grouped-GEMV launch and as two linears; two
     # copies of the weights (178 MB, more than L2) alternate; weight
@@ -514,24 +661,36 @@ def bench_extras(only=None, moe_tokens=None):
                 del x, ws, y
         finally:
             tq.exl3_set_row_invariant(prev)
+    # grouped experts over the whole 302 MB arena; few-token calls rotate
+    # through several routing draws so that consecutive calls hit different
+    # experts (the weights they read come from HBM, not from the L2)
     moe = {}
-    for T in ((moe_tokens or synth.CONFIG5_T) if only in (None, "moe") else ()):
-        c = synth.config5(T)
-        d = dict(x=dev(c.x), ids=dev(c.ids), w=dev(c.weights), t13=dev(c.w13.trellis), s13=dev(c.w13.suh),
+    for T in ((moe_tokens or MOE_T) if only in (None, "moe") else ()):
+        c = synth.config5(T) if T in synth.CONFIG5_T else synth.moe_case(5, 10 + T, T,
+                                                                           name=f"E256 top8 h2048 i512 K3 T{T}")
+        d = dict(x=dev(c.x), t13=dev(c.w13.trellis), s13=dev(c.w13.suh),
                  v13=dev(c.w13.svh), t2=dev(c.w2.trellis), s2=dev(c.w2.suh), v2=dev(c.w2.svh))
         w13 = tq.expert_proj(d["t13"], d["s13"], d["v13"], c.K)
         w2 = tq.expert_proj(d["t2"], d["s2"], d["v2"], c.K)
+        nr = 16 if T <= 64 else (4 if T <= 128 else 1)
+        routes = [(c.ids, c.weights)] + [synth.routing(synth.rng_for(5, 1000 + 10 * T + r), T, c.E, c.topk)
+                                         for r in range(nr - 1)]
+        rd = [(dev(i), dev(w)) for i, w in routes]
         ws = tq.workspace(tq.exl3_moe_workspace_size(T, c.topk, c.E, w13, w2))
         y = torch.empty((T, c.hidden), dtype=torch.float16, device="cuda")
-        ms = _timed(lambda: tq.exl3_moe_grouped(d["x"], d["ids"], d["w"], w13, w2, c.E, y=y, workspace_buf=ws),
-                    reps=3)
-        used = len(np.unique(c.ids))
+        calls = [lambda i=i, w=w: tq.exl3_moe_grouped(d["x"], i, w, w13, w2, c.E, y=y, workspace_buf=ws)
+                 for i, w in rd]
+        ms = _timed_rotating(calls, rounds=max(1, 6 // nr)) if nr > 1 else _timed(calls[0], reps=3)
+        assert tq.exl3_check_device_error(ws) == 0
+        used = np.mean([len(np.unique(i)) for i, _ in routes])
         per_expert = (c.w13.trellis.nbytes + c.w2.trellis.nbytes) // c.E
         flops = 2.0 * T * c.topk * (2 * c.hidden * c.inter + c.inter * c.hidden)
-        moe[f"T{T}"] = {"ms": round(ms, 4), "experts_hit": used,
-                        "unique_weight_GBs": round(used * per_expert / (ms * 1e-3) / 1e9, 1),
-                        "tflops": round(flops / (ms * 1e-3) / 1e12, 2)}
-        del d
+        hbm = peaks()[0]
+        gbs = used * per_expert / (ms * 1e-3) / 1e9
+        moe[f"T{T}"] = {"ms": round(ms, 4), "experts_hit": round(float(used), 1),
+                        "unique_weight_GBs": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4),
+                        "tflops": round(flops / (ms * 1e-3) / 1e12, 2), "routings_rotated": nr}
+        del d, rd, ws
     # per-expert widths: the same shape with experts 0-127 at K = 3 and
     # 128-255 at K = 4 (down the other way round), two runs per projection
     mixed = {}
@@ -553,11 +712,10 @@ def bench_extras(only=None, moe_tokens=None):
         mixed[f"T{T}"] = {"ms": round(ms, 4), "experts_hit": len(used),
                           "unique_weight_GBs": round(ubytes / (ms * 1e-3) / 1e9, 1)}
         del d
-    return {"small_m_k5120_n17408": small, "shards_gate_up_k5120_n17408x2_M1": shards, "shards_var_M1": var,
+    return {"shards_gate_up_k5120_n17408x2_M1": shards, "shards_var_M1": var,
             "row_invariant_k5120_n17408": inv, "moe_E256_top8_h2048_i512_K3": moe,
             "moe_mixed_E256_top8_h2048_i512_K3K4": mixed,
-            "note": "small M: trellis decoded into tcgen05 operands (one fused kernel after the input RHT); "
-                    "MoE: device remap + gather/RHT + two grouped tcgen05 kernels decoding the experts' trellis "
+            "note": "MoE: device remap + gather/RHT + two grouped tcgen05 kernels decoding the experts' trellis "
                     "on the fly + fixed-order combine; mixed widths: the tile kernels once per run of equal "
                     "width (two runs here), for every token count"}
 
@@ -611,6 +769,58 @@ def bench_pipes(iters=20000):
         res[name] = r
     return {"sms": sms, "per_sm_per_clock": res,
             "method": "one 1024-thread CTA per SM, 8 independent chains per thread, clock64 cycles (median CTA)"}
+
+
+# ---------------------------------------------------------------- dense peaks
+
+def bench_peaks():
+    """Dense tensor-core peaks for the prefill fractions, measured the way
+    the driver measures bf16: torch.matmul of 8192^3 (2 N^3 flop), best of
+    10 (burst) and back to back for about 4 s (sustained); fp16 and bf16 on
+    cuBLAS, and int8 through torch._int_mm (s8 x s8 -> s32) for context."""
+    import torch
+    N = 8192
+    out = {}
+    for name, dt in (("fp16", torch.float16), ("bf16", torch.bfloat16), ("int8", torch.int8)):
+        if dt == torch.int8:
+            a = torch.randint(-127, 128, (N, N), dtype=dt, device="cuda")
+            b = torch.randint(-127, 128, (N, N), dtype=dt, device="cuda").t().contiguous().t()
+            mm = lambda: torch._int_mm(a, b)
+        else:
+            a = torch.randn(N, N, dtype=dt, device="cuda")
+            b = torch.randn(N, N, dtype=dt, device="cuda")
+            mm = lambda: torch.matmul(a, b)
+        try:
+            for _ in range(3):
+                mm()
+            torch.cuda.synchronize()
+        except Exception as e:   # an unsupported int8 layout or kernel: report, do not guess
+            out[name] = {"error": str(e).splitlines()[0][:200]}
+            continue
+        best = float("inf")
+        for _ in range(10):
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            mm()
+            e.record()
+            torch.cuda.synchronize()
+            best = min(best, s.elapsed_time(e))
+        reps = max(1, int(4000.0 / best))
+        with ClockSampler(torch.cuda.current_device()) as clk:
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            for _ in range(reps):
+                mm()
+            e.record()
+            torch.cuda.synchronize()
+        sus = s.elapsed_time(e) / reps
+        flop = 2.0 * N ** 3
+        unit = "TOP/s" if dt == torch.int8 else "TFLOP/s"
+        out[name] = {"burst": round(flop / (best * 1e-3) / 1e12, 1), "sustained": round(flop / (sus * 1e-3) / 1e12, 1),
+                     "unit": unit, "clocks": clk.summary()}
+        del a, b
+    return {"N": N, "peaks": out, "method": "torch.matmul / torch._int_mm of N^3, CUDA events; burst = best of 10, "
+                                            "sustained = mean of back-to-back calls over ~4 s"}
 
 
 # ------------------------------------------------------------------------- oracle
@@ -676,8 +886,9 @@ def main():
     ap.add_argument("--skip-prefill", action="store_true")
     ap.add_argument("--no-prefetch", action="store_true",
                     help="launch the step's linears plainly (no weight prefetch across launches)")
-    ap.add_argument("--only", choices=["small", "moe", "prefill", "pipes"], default=None,
+    ap.add_argument("--only", choices=["small", "moe", "prefill", "pipes", "peaks", "configs"], default=None,
                     help="run one extra section alone and print its JSON (for profiling)")
+    ap.add_argument("--configs", nargs="*", default=["1", "2", "3"], help="workloads of --only configs")
     ap.add_argument("--moe-tokens", type=int, nargs="*", default=None,
                     help="token counts of the MoE section (default: all of the MoE workload's)")
     args = ap.parse_args()
@@ -687,6 +898,10 @@ def main():
             print(json.dumps(bench_prefill(args, *peaks()[1:])))
         elif args.only == "pipes":
             print(json.dumps(bench_pipes()))
+        elif args.only == "peaks":
+            print(json.dumps(bench_peaks()))
+        elif args.only == "configs":
+            print(json.dumps(bench_configs(tuple(args.configs))))
         else:
             print(json.dumps(bench_extras(args.only, args.moe_tokens)))
         return

@@ -41,7 +41,7 @@ int exl3_launch_fused_tc(const uint16_t *xh, const float *xsum, const uint16_t *
                          int splits, cudaStream_t s, int npad_fixed, const uint16_t *bias = nullptr);
 
 cudaError_t exl3_launch_moe_remap(const int32_t *ids, int U, int E, int *counts, int *offsets, int *perm, int *pos,
-                                  int *mtiles, int *n_mtiles, int max_mtiles, int *chunk_tab, int *err,
+                                  int *mtiles, int *n_mtiles, int max_mtiles, int cap, int *chunk_tab, int *err,
                                   cudaStream_t s);
 int exl3_moe_remap_chunk(int E);
 cudaError_t exl3_launch_moe_gather(const uint16_t *x, int U, int hidden, int topk, const int *perm, const int *offsets,
@@ -64,14 +64,13 @@ cudaError_t exl3_launch_moe_gemv(const uint16_t *x, const float *act_in, int *po
                                  float *partials, int *counters, int *err, cudaStream_t s);
 int exl3_launch_moe_fused_gateup(const uint16_t *xg, const uint16_t *xu, int U, int hidden, int inter, int K, int E,
                                  const uint16_t *w13_trellis, const int *mtiles, const int *n_mtiles, int max_mtiles,
-                                 const uint16_t *svh13, const uint16_t *suh2, uint16_t *hout, int splits,
+                                 int cap, const uint16_t *svh13, const uint16_t *suh2, uint16_t *hout, int splits,
                                  float *partials, int *counters, int *err, cudaStream_t s, int e_lo = 0,
                                  int e_cnt = -1);
 int exl3_launch_moe_fused_down(const uint16_t *hin, int U, int hidden, int inter, int K, int E,
-                               const uint16_t *w2_trellis,
-                               const int *mtiles, const int *n_mtiles, int max_mtiles, const uint16_t *svh2,
-                               const float *weights, const int *perm, float *dout, int *err, cudaStream_t s,
-                               int e_lo = 0, int e_cnt = -1);
+                               const uint16_t *w2_trellis, const int *mtiles, const int *n_mtiles, int max_mtiles,
+                               int cap, const uint16_t *svh2, const float *weights, const int *perm, float *dout,
+                               int *err, cudaStream_t s, int e_lo = 0, int e_cnt = -1);
 
 // ---------------------------------------------------------------- errors --
 
@@ -259,6 +258,7 @@ LinearInt8Ws linear_int8_ws(int M, int k, int n) {
 struct MoeWs {
   size_t counts, offsets, pos, perm, mtiles, n_mtiles, chunk, xg, xu, h, d, partials, total;
   int max_mtiles, grid_mtiles, splits;
+  int cap;            // rows per expert tile: 32 when few rows per expert are routed, else 128
   bool gemv;          // few routed rows: grouped M = 1 GEMVs instead of the tile kernels
   size_t y13;         // gemv: gate/up outputs [U][2][inter] fp32 (d, pos, partials as above)
 };
@@ -289,7 +289,11 @@ MoeWs moe_ws(int T, int topk, int E, int hidden, int inter, int K13, int K2, boo
       return w;
     }
   }
-  w.max_mtiles = (int)(U / 128 + E + 1);
+  // Tiles of 32 rows (the grouped kernels then run MMAs 16 or 32 rows wide,
+  // with four issuers) when the call routes at most 16 rows per expert on
+  // average; 128 rows otherwise.
+  w.cap = U <= (size_t)16 * E ? 32 : 128;
+  w.max_mtiles = (int)(U / w.cap + E + 1);
   size_t off = kDataOff;
   auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes); return o; };
   w.counts = take(sizeof(int) * E);
@@ -304,7 +308,7 @@ MoeWs moe_ws(int T, int topk, int E, int hidden, int inter, int K13, int K2, boo
   w.xu = take(sizeof(uint16_t) * U * hidden);
   w.h = take(sizeof(uint16_t) * U * inter);
   w.d = take(sizeof(float) * U * hidden);
-  // Every 128-row tile holds at least one unit, so the grouped kernels need
+  // Every tile holds at least one unit, so the grouped kernels need
   // at most min(U, max_mtiles) tiles per output column block.  When those
   // tiles cannot fill half the SMs (few tokens), the gate+up projection is
   // split over k into an even number of k steps (at least 4) per CTA.
@@ -314,7 +318,7 @@ MoeWs moe_ws(int T, int topk, int E, int hidden, int inter, int K13, int K2, boo
   w.splits = 1;
   for (int sp = 2; sp <= 8; ++sp)
     if (kb % sp == 0 && (kb / sp) % 2 == 0 && kb / sp >= 4 && tiles1 * sp <= sms) w.splits = sp;
-  if (w.splits > 1) w.partials = take(sizeof(float) * (size_t)tiles1 * w.splits * 2 * 128 * 128);
+  if (w.splits > 1) w.partials = take(sizeof(float) * (size_t)tiles1 * w.splits * 2 * w.cap * 128);
   w.total = off;
   return w;
 }
@@ -654,7 +658,7 @@ int exl3_moe_grouped(const uint16_t *x, int T, int hidden, const int32_t *topk_i
   uint16_t *h = at<uint16_t>(workspace, L.h);
   float *d = at<float>(workspace, L.d);
   EXL3_TRY(exl3_cuda_check(exl3_launch_moe_remap(topk_ids, U, E, counts, offsets, perm, pos, mtiles,
-                                                 n_mtiles, L.max_mtiles, chunk_tab, err, stream),
+                                                 n_mtiles, L.max_mtiles, L.cap, chunk_tab, err, stream),
                            "moe remap launch"));
   EXL3_TRY(exl3_cuda_check(exl3_launch_moe_gather(x, U, hidden, topk, perm, offsets, E, topk_ids, w13->suh, xg, xu,
                                                   stream),
@@ -662,9 +666,9 @@ int exl3_moe_grouped(const uint16_t *x, int T, int hidden, const int32_t *topk_i
   float *partials = L.splits > 1 ? at<float>(workspace, L.partials) : nullptr;
   int *counters = at<int>(workspace, kCounterOff);   // the fixed counter region, zero between calls
   EXL3_TRY(exl3_launch_moe_fused_gateup(xg, xu, U, hidden, inter, w13->K, E, w13->trellis, mtiles, n_mtiles,
-                                        L.grid_mtiles, w13->svh, w2->suh, h, L.splits, partials, counters, err,
+                                        L.grid_mtiles, L.cap, w13->svh, w2->suh, h, L.splits, partials, counters, err,
                                         stream));
-  EXL3_TRY(exl3_launch_moe_fused_down(h, U, hidden, inter, w2->K, E, w2->trellis, mtiles, n_mtiles, L.grid_mtiles,
+  EXL3_TRY(exl3_launch_moe_fused_down(h, U, hidden, inter, w2->K, E, w2->trellis, mtiles, n_mtiles, L.grid_mtiles, L.cap,
                                       w2->svh, topk_weights, perm, d, err, stream));
   return exl3_cuda_check(exl3_launch_moe_combine(d, pos, T, topk, hidden, y, out_dtype == EXL3_OUT_F32, stream),
                          "moe combine launch");
@@ -709,7 +713,7 @@ int exl3_moe_grouped_mixed(const uint16_t *x, int T, int hidden, const int32_t *
   // routing, gather and combine as in exl3_moe_grouped; each projection runs
   // one grouped launch per run of equal width, over that run's experts only
   EXL3_TRY(exl3_cuda_check(exl3_launch_moe_remap(topk_ids, U, E, counts, offsets, perm, pos, mtiles,
-                                                 n_mtiles, L.max_mtiles, chunk_tab, err, stream),
+                                                 n_mtiles, L.max_mtiles, L.cap, chunk_tab, err, stream),
                            "moe remap launch"));
   EXL3_TRY(exl3_cuda_check(exl3_launch_moe_gather(x, U, hidden, topk, perm, offsets, E, topk_ids, w13->suh, xg, xu,
                                                   stream),
@@ -718,11 +722,11 @@ int exl3_moe_grouped_mixed(const uint16_t *x, int T, int hidden, const int32_t *
   int *counters = at<int>(workspace, kCounterOff);
   for (const WidthRun &r : width_runs(w13, E))
     EXL3_TRY(exl3_launch_moe_fused_gateup(xg, xu, U, hidden, inter, r.K, E, w13->trellis + r.words, mtiles, n_mtiles,
-                                          L.grid_mtiles, w13->svh, w2->suh, h, L.splits, partials, counters, err,
+                                          L.grid_mtiles, L.cap, w13->svh, w2->suh, h, L.splits, partials, counters, err,
                                           stream, r.e_lo, r.cnt));
   for (const WidthRun &r : width_runs(w2, E))
     EXL3_TRY(exl3_launch_moe_fused_down(h, U, hidden, inter, r.K, E, w2->trellis + r.words, mtiles, n_mtiles,
-                                        L.grid_mtiles, w2->svh, topk_weights, perm, d, err, stream, r.e_lo, r.cnt));
+                                        L.grid_mtiles, L.cap, w2->svh, topk_weights, perm, d, err, stream, r.e_lo, r.cnt));
   return exl3_cuda_check(exl3_launch_moe_combine(d, pos, T, topk, hidden, y, out_dtype == EXL3_OUT_F32, stream),
                          "moe combine launch");
 }

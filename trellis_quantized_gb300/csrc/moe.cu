@@ -17,7 +17,7 @@ struct Plan {       // device-side routing results (workspace)
   int *offsets;     // [E + 1] exclusive scan of counts (rows in sorted order)
   int *perm;        // [U] sorted row -> unit
   int *pos;         // [U] unit -> sorted row (-1 for an invalid expert id)
-  int4 *mtiles;     // [max_mtiles]: (expert, first row, rows, 0) per 128-row tile
+  int4 *mtiles;     // [max_mtiles]: (expert, first row, rows, 0) per tile of at most `cap` rows
   int *n_mtiles;    // [1]
   int *chunk;       // [nchunks][E]: units of each expert per chunk, then the
                     // expert's rows before the chunk (exclusive scan over chunks)
@@ -84,8 +84,10 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *warp_sums, int *
 
 // (2) one CTA of 1024 threads, thread e = expert e (E <= 1024): per-chunk
 // counts become the expert's rows before each chunk; counts, offsets and the
-// 128-row tile list follow from two block scans.
-__global__ void __launch_bounds__(1024) remap_scan_kernel(int E, int nchunks, Plan p, int max_mtiles, int *err) {
+// tile list (tiles of at most cap rows, cap a power of two) follow from two
+// block scans.
+__global__ void __launch_bounds__(1024) remap_scan_kernel(int E, int nchunks, Plan p, int max_mtiles, int cap,
+                                                          int *err) {
   pdl_trigger();
   pdl_wait();
   __shared__ int warp_sums[32];
@@ -115,10 +117,10 @@ __global__ void __launch_bounds__(1024) remap_scan_kernel(int E, int nchunks, Pl
   const int off = block_exclusive_scan(c, warp_sums, &total);
   if (e < E) p.offsets[e] = off;
   if (e == 0) p.offsets[E] = total;
-  const int nt = (c + 127) >> 7;
+  const int nt = (c + cap - 1) / cap;
   const int tb = block_exclusive_scan(nt, warp_sums, &total);
   for (int j = 0; j < nt; ++j)
-    if (tb + j < max_mtiles) p.mtiles[tb + j] = make_int4(e, off + 128 * j, min(128, c - 128 * j), 0);
+    if (tb + j < max_mtiles) p.mtiles[tb + j] = make_int4(e, off + cap * j, min(cap, c - cap * j), 0);
   if (e == 0) {
     if (total > max_mtiles) set_device_error(err, kErrBounds);
     *p.n_mtiles = min(total, max_mtiles);
@@ -155,7 +157,7 @@ __global__ void remap_place_kernel(const int32_t *__restrict__ ids, int U, int E
 constexpr int kSmallU = 1024, kSmallE = 256;
 
 __global__ void __launch_bounds__(1024) remap_small_kernel(const int32_t *__restrict__ ids, int U, int E, Plan p,
-                                                           int max_mtiles, int *err) {
+                                                           int max_mtiles, int cap, int *err) {
   __shared__ int wc[32][kSmallE];
   __shared__ int base[kSmallE];
   __shared__ int warp_sums[32];
@@ -191,10 +193,10 @@ __global__ void __launch_bounds__(1024) remap_small_kernel(const int32_t *__rest
     base[t] = off;
   }
   if (t == 0) p.offsets[E] = total;
-  const int nt = (c + 127) >> 7;
+  const int nt = (c + cap - 1) / cap;
   const int tb = block_exclusive_scan(nt, warp_sums, &total);
   for (int j = 0; j < nt; ++j)
-    if (tb + j < max_mtiles) p.mtiles[tb + j] = make_int4(t, off + 128 * j, min(128, c - 128 * j), 0);
+    if (tb + j < max_mtiles) p.mtiles[tb + j] = make_int4(t, off + cap * j, min(cap, c - cap * j), 0);
   if (t == 0) {
     if (total > max_mtiles) set_device_error(err, kErrBounds);
     *p.n_mtiles = min(total, max_mtiles);
@@ -312,13 +314,14 @@ int exl3_moe_remap_chunk(int E) {
 }
 
 // chunk_tab: [ceil(U / exl3_moe_remap_chunk(E))][E] ints of workspace.
+// cap: rows per tile (32 or 128) of the tile list the grouped kernels read.
 cudaError_t exl3_launch_moe_remap(const int32_t *ids, int U, int E, int *counts, int *offsets, int *perm, int *pos,
-                                  int *mtiles, int *n_mtiles, int max_mtiles, int *chunk_tab, int *err,
+                                  int *mtiles, int *n_mtiles, int max_mtiles, int cap, int *chunk_tab, int *err,
                                   cudaStream_t s) {
-  if (E < 1 || E > 1024) return cudaErrorInvalidValue;
+  if (E < 1 || E > 1024 || (cap != 32 && cap != 128)) return cudaErrorInvalidValue;
   moe::Plan p{counts, offsets, perm, pos, reinterpret_cast<int4 *>(mtiles), n_mtiles, chunk_tab};
   if (U <= moe::kSmallU && E <= moe::kSmallE) {
-    return launch_pdl(moe::remap_small_kernel, dim3(1), dim3(1024), 0, s, ids, U, E, p, max_mtiles, err);
+    return launch_pdl(moe::remap_small_kernel, dim3(1), dim3(1024), 0, s, ids, U, E, p, max_mtiles, cap, err);
   }
   const int CH = exl3_moe_remap_chunk(E);
   const int nchunks = (U + CH - 1) / CH;
@@ -326,7 +329,7 @@ cudaError_t exl3_launch_moe_remap(const int32_t *ids, int U, int E, int *counts,
     cudaError_t e = launch_pdl(moe::remap_hist_kernel, dim3(nchunks), dim3(CH), sizeof(int) * E, s, ids, U, E, p, err);
     if (e != cudaSuccess) return e;
   }
-  cudaError_t e = launch_pdl(moe::remap_scan_kernel, dim3(1), dim3(1024), 0, s, E, nchunks, p, max_mtiles, err);
+  cudaError_t e = launch_pdl(moe::remap_scan_kernel, dim3(1), dim3(1024), 0, s, E, nchunks, p, max_mtiles, cap, err);
   if (e != cudaSuccess || nchunks == 0) return e;
   return launch_pdl(moe::remap_place_kernel, dim3(nchunks), dim3(CH), sizeof(int) * (CH / 32) * E, s, ids, U, E, p);
 }

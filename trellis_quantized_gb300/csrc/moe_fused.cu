@@ -5,18 +5,27 @@
 // routing weight on the down output, in fp32, and no fp16 expert weights
 // anywhere).
 //
-// A CTA handles one (128-row expert tile, 128-column output tile) pair of the
-// device-side tile list.  The MMA computes the transposed product (decoded
-// weights as the MN-major A operand, M = 128 output columns; the tile's x'
-// rows as the K-major B operand, N = 128).  Roles (20 warps):
-//   warp 0       trellis producer: one tensor load per projection and stage
-//                over all experts' trellis (16 tile rows per stage)
-//   warps 1, 2   MMA issuers, one per decoder group, each with its own
-//                accumulators (summed in a fixed order by the epilogue)
-//   warps 3-18   decoders in two groups of eight, taking alternate "pairs":
-//                phase 1 a pair is the gate and up weights of one k step,
-//                phase 2 two k steps of down; one fence and one signal per pair
-//   warp 19      x' producer: one 32 KB stage (the pair's B operands) per load
+// A CTA handles one (expert tile, 128-column output tile) pair of the
+// device-side tile list.  A tile holds up to NMAX routed rows of one expert
+// (NMAX = 32 when the call routes few rows per expert, else 128); the MMA
+// computes the transposed product (decoded weights as the MN-major A operand,
+// M = 128 output columns; the tile's x' rows as the K-major B operand, N =
+// the tile's rows rounded up to 16).  Roles (2 + NISS + 16 warps):
+//   warp 0         trellis producer: one tensor load per projection and stage
+//                  over all experts' trellis (16 tile rows per stage)
+//   warps 1..NISS  MMA issuers: pair P goes to issuer P mod NISS, into that
+//                  issuer's own accumulators (summed in a fixed order by the
+//                  epilogue); four issuers for 32-row tiles, two for 128
+//                  (TMEM holds 512 columns)
+//   next 16 warps  decoders in two groups of eight, taking alternate "pairs":
+//                  phase 1 a pair is the gate and up weights of one k step,
+//                  phase 2 two k steps of down; one fence and one signal per pair
+//   last warp      x' producer: the pair's B operands in one or two loads
+//
+// Pair P uses weight slot P mod NPS and x' slot P mod XS; both ring sizes
+// are multiples of NISS (and NPS of the two decoder groups), so every slot
+// has one issuer and its waits on the slot's barriers are for consecutive
+// phases (a waiter never sees an older phase of the same parity).
 //
 // Phase 1 (gate + up): per token row the epilogue forms
 //   g = RHT_out(gate) . svh_gate, u = RHT_out(up) . svh_up, h = SiLU(g) u and
@@ -35,39 +44,47 @@ using ftc::NDEC;
 using ftc::NGRP;
 using ftc::W_BYTES;
 
-constexpr int XROWS = 128;                  // rows of a tile (MMA N)
-constexpr int X_STEP = XROWS * BK * 2;      // B operand of one k step (16 KB)
-constexpr int kWarps = 3 + NGRP * NDEC + 1;
-constexpr int kXWarp = kWarps - 1;
+template <int NMAX>
+struct Roles {
+  static constexpr int NISS = NMAX <= 32 ? 4 : 2;      // MMA issuer warps
+  static constexpr int DEC0 = 1 + NISS;                  // first decoder warp
+  static constexpr int XWARP = DEC0 + NGRP * NDEC;       // the x' producer
+  static constexpr int WARPS = XWARP + 1;
+};
 
-template <int K, int PHASE>
+template <int K, int PHASE, int NMAX>
 struct Cfg {
+  static constexpr int NISS = Roles<NMAX>::NISS;
+  static constexpr int XROWS = NMAX;                    // rows of a tile (largest MMA N)
+  static constexpr int X_STEP = XROWS * BK * 2;         // B operand of one k step
   static constexpr int NP = PHASE == 1 ? 2 : 1;         // projections (accumulators per issuer)
   static constexpr int ROWB = (BN / 16) * 32 * K;       // one tile row of the CTA's 8 tiles
   static constexpr int T_STAGE = 16 * ROWB;             // two pairs
-  // pair slots of the weight ring: a multiple of the issuers and of the
-  // decoder groups (2), so that every slot has one issuer and one group and
-  // their waits on the slot's barriers are for consecutive phases; four
-  // where they fit beside two x' and two trellis stages
-  static constexpr int NPS_FIT4 = (227 * 1024 - 2048 - 8 * W_BYTES - 2 * 2 * XROWS * BK * 2 - 2 * 16 * ROWB) >= 0;
-  static constexpr int NPS = NPS_FIT4 ? 4 : 2;
-  static constexpr int W_RING = 2 * NPS * W_BYTES;
   static constexpr int X_STAGE = 2 * X_STEP;            // one pair
+  static constexpr int BUDGET = 227 * 1024 - 2048;
+  // pair slots of the weight ring: 4 where they fit beside two x' and two
+  // trellis stages, else 2 (a multiple of the issuers and of the groups)
+  static constexpr int NPS_FIT4 = (BUDGET - 8 * W_BYTES - 2 * X_STAGE - 2 * T_STAGE) >= 0;
+  static constexpr int NPS = (NPS_FIT4 || NISS > 2) ? 4 : 2;
+  static constexpr int W_RING = 2 * NPS * W_BYTES;
   // x' ring: as deep as the budget allows after two trellis stages (the
-  // loads come from L2 or HBM and must run several pairs ahead)
-  static constexpr int XS_FIT = (227 * 1024 - 2048 - W_RING - 2 * T_STAGE) / X_STAGE;
-  static constexpr int XS = XS_FIT > 4 ? 4 : XS_FIT;
-  static constexpr int TS_FIT = (227 * 1024 - 2048 - W_RING - XS * X_STAGE) / T_STAGE;
+  // loads come from L2 or HBM and must run several pairs ahead), a multiple
+  // of the issuers
+  static constexpr int XS_FIT = (BUDGET - W_RING - 2 * T_STAGE) / X_STAGE;
+  static constexpr int XS = (XS_FIT >= 4 ? 4 : XS_FIT) / NISS * NISS;
+  static constexpr int TS_FIT = (BUDGET - W_RING - XS * X_STAGE) / T_STAGE;
   static constexpr int TS = TS_FIT > 8 ? 8 : TS_FIT;
   static constexpr int SMEM_BYTES = XS * X_STAGE + W_RING + TS * T_STAGE + 2048;
   static constexpr int ITEMS = 32 * ftc::Shape<K, 32>::LPT;  // items per (k step, projection)
   // phase 2 may take two output tiles per CTA (one accumulator set each)
   static constexpr int NTC = PHASE == 2 ? 2 : 1;
-  static constexpr uint32_t TMEM_COLS = NGRP * NP * XROWS * NTC;
-  static_assert(TS >= 2 && XS >= 2, "operand rings too shallow");
-  static_assert(NPS % NGRP == 0, "one issuer and one decoder group per weight slot");
+  static constexpr uint32_t TMEM_COLS = NISS * NP * XROWS * NTC;
+  static_assert(TS >= 2 && XS >= NISS, "operand rings too shallow");
+  static_assert(NPS % NISS == 0 && NPS % NGRP == 0, "one issuer and one decoder group per weight slot");
+  static_assert(XS % NISS == 0, "one issuer per x' slot");
   static_assert(NTC * NP * XROWS * 128 * 4 <= XS * X_STAGE + W_RING, "epilogue scratch exceeds the operand rings");
-  static_assert(TMEM_COLS <= 512, "TMEM");
+  static_assert(TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
 
 struct Args {
@@ -90,20 +107,21 @@ struct Args {
   // to arrive adds the partial sums in split order
   int splits;
   int ntc;                  // output tiles per CTA (phase 2: 1 or 2)
-  float *partials;          // [tiles][splits][2][128][128] fp32
+  float *partials;          // [tiles][splits][2][NMAX][128] fp32
   int *counters;            // [tiles], zero between calls
   // experts [e_lo, e_hi) only: the trellis map covers just their arena
   // (row 0 = expert e_lo) and tiles of other experts are left to other launches
   int e_lo, e_hi;
 };
 
-template <int K, int PHASE>
-__global__ void __launch_bounds__(kWarps * 32, 1) moe_fused_kernel(const __grid_constant__ CUtensorMap tmX0,
-                                                                   const __grid_constant__ CUtensorMap tmX1,
-                                                                   const __grid_constant__ CUtensorMap tmT, Args a) {
-  using C = Cfg<K, PHASE>;
+template <int K, int PHASE, int NMAX>
+__global__ void __launch_bounds__(Roles<NMAX>::WARPS * 32, 1)
+    moe_fused_kernel(const __grid_constant__ CUtensorMap tmX0, const __grid_constant__ CUtensorMap tmX1,
+                     const __grid_constant__ CUtensorMap tmT, Args a) {
+  using C = Cfg<K, PHASE, NMAX>;
   using S = ftc::Shape<K, 32>;
-  constexpr int NP = C::NP, XS = C::XS, TS = C::TS, NPS = C::NPS;
+  constexpr int NP = C::NP, XS = C::XS, TS = C::TS, NPS = C::NPS, NISS = C::NISS, XROWS = C::XROWS;
+  constexpr int kDec0 = Roles<NMAX>::DEC0, kXWarp = Roles<NMAX>::XWARP;
   const int tile = blockIdx.x / a.splits, split = blockIdx.x % a.splits;
   // output tiles nt0 .. nt0 + nts - 1 (phase 2 may take two: their pairs
   // follow one another, tile j's pair Pt being pair j * nptile + Pt)
@@ -115,6 +133,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) moe_fused_kernel(const __grid_
   const int nt0 = (tile % NTG) * ntc, nts = min(ntc, a.NT - nt0), e = mt.x, row0 = mt.y, rows = mt.z;
   if (e < a.e_lo || e >= a.e_hi) return;   // uniform per CTA: another launch's expert
   const int et = e - a.e_lo;                // the expert's place in this launch's trellis map
+  const int npad = (rows + 15) & ~15;       // MMA N: the tile's rows rounded up to 16
   const int KB = a.KB;
   // this CTA's pairs: absolute pair P0 + P for P < npairs (P0 even, so a
   // trellis stage still holds pairs 2j, 2j + 1 of the range; with two tiles
@@ -144,19 +163,19 @@ __global__ void __launch_bounds__(kWarps * 32, 1) moe_fused_kernel(const __grid_
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < TS; ++s) {
-      tc::mbar_init(&tfull[s], 1);
-      tc::mbar_init(&tempty[s], NGRP * NDEC);   // every decoder warp, once per stage
+    for (int st = 0; st < TS; ++st) {
+      tc::mbar_init(&tfull[st], 1);
+      tc::mbar_init(&tempty[st], NGRP * NDEC);   // every decoder warp, once per stage
     }
-    for (int s = 0; s < XS; ++s) {
-      tc::mbar_init(&xfull[s], 1);
-      tc::mbar_init(&xempty[s], 1);             // the issuer of the stage's pair
+    for (int st = 0; st < XS; ++st) {
+      tc::mbar_init(&xfull[st], 1);
+      tc::mbar_init(&xempty[st], 1);             // the issuer of the stage's pair
     }
-    for (int s = 0; s < NPS; ++s) {
-      tc::mbar_init(&wfull[s], NDEC);           // one group's warps, once per pair
-      tc::mbar_init(&wempty[s], 1);
+    for (int st = 0; st < NPS; ++st) {
+      tc::mbar_init(&wfull[st], NDEC);           // one group's warps, once per pair
+      tc::mbar_init(&wempty[st], 1);
     }
-    tc::mbar_init(accum, NGRP);
+    tc::mbar_init(accum, NISS);
     *abort_flag = 0;
     tc::fence_mbar_init();
     tc::prefetch_tmap(&tmX0);
@@ -198,7 +217,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) moe_fused_kernel(const __grid_
     }
   } else if (warp == kXWarp) {
     // ---------------- x' producer: the pair's two B operands (phase 1: x'g
-    // and x'u of k step P; phase 2: h' of k steps 2P, 2P + 1), 32 KB per load
+    // and x'u of k step P; phase 2: h' of k steps 2P, 2P + 1), XROWS rows each
     if (lane == 0) {
       for (int P = 0; P < npairs && !*abort_flag; ++P) {
         const int st = P % XS;
@@ -210,21 +229,22 @@ __global__ void __launch_bounds__(kWarps * 32, 1) moe_fused_kernel(const __grid_
         tc::mbar_arrive_expect_tx(&xfull[st], C::X_STAGE);
         if (PHASE == 1) {
           tc::tma_load_2d(sX + st * C::X_STAGE, &tmX0, &xfull[st], (P0 + P) * BK, row0);
-          tc::tma_load_2d(sX + st * C::X_STAGE + X_STEP, &tmX1, &xfull[st], (P0 + P) * BK, row0);
+          tc::tma_load_2d(sX + st * C::X_STAGE + C::X_STEP, &tmX1, &xfull[st], (P0 + P) * BK, row0);
         } else {
           tc::tma_load_3d(sX + st * C::X_STAGE, &tmX0, &xfull[st], 0, row0, 2 * (P % nptile));
         }
       }
     }
-  } else if (warp <= NGRP) {
-    // ---------------- MMA issuers: warp 1 + g takes the pairs P = g, g + 2, ...
-    // into accumulators (j NGRP NP + g NP + p) * 128 (phase 1: p = gate, up;
-    // j: the CTA's output tile)
+  } else if (warp <= NISS) {
+    // ---------------- MMA issuers: warp 1 + g takes the pairs P = g, g + NISS,
+    // ... into accumulators (jt NISS NP + g NP + p) * XROWS (phase 1: p =
+    // gate, up; jt: the CTA's output tile).  The first pair of a tile that
+    // an issuer sees is among the tile's first NISS pairs.
     if (lane == 0) {
       const int g = warp - 1;
-      const uint32_t idesc = ftc::idesc_f16_amn(BN, XROWS);
+      const uint32_t idesc = ftc::idesc_f16_amn(BN, npad);
       bool stop = false;
-      for (int P = g; P < npairs; P += NGRP) {
+      for (int P = g; P < npairs; P += NISS) {
         const int xs = P % XS, ps = P % NPS;
         const bool ok = tc::mbar_wait(&xfull[xs], (P / XS) & 1) && tc::mbar_wait(&wfull[ps], (P / NPS) & 1);
         if (!ok || *abort_flag) {
@@ -234,14 +254,14 @@ __global__ void __launch_bounds__(kWarps * 32, 1) moe_fused_kernel(const __grid_
           break;
         }
         tc::tc_fence_after();
+        const int jt = P / nptile, Pt = P - jt * nptile;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int p = PHASE == 1 ? h : 0;
-          const int jt = P / nptile, Pt = P - jt * nptile;
-          const uint32_t dcol = tmem_base + (uint32_t)(((jt * NGRP + g) * NP + p) * XROWS);
+          const uint32_t dcol = tmem_base + (uint32_t)(((jt * NISS + g) * NP + p) * XROWS);
           const uint64_t ad = ftc::sdesc_mn_sw128(sW + (2 * ps + h) * W_BYTES, 1024, 2048);
-          const uint64_t bd = tc::sdesc_k_sw128(sX + xs * C::X_STAGE + h * X_STEP);
-          const bool first = (Pt == g) && (PHASE == 1 || h == 0);
+          const uint64_t bd = tc::sdesc_k_sw128(sX + xs * C::X_STAGE + h * C::X_STEP);
+          const bool first = (Pt < NISS) && (PHASE == 1 || h == 0);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
             tc::mma_f16(dcol, ad + (uint64_t)((2 * 2048 * kk) >> 4), bd + 2 * kk, idesc,
@@ -254,7 +274,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1) moe_fused_kernel(const __grid_
     }
   } else {
     // ---------------- decoders: group g takes the pairs P = g, g + 2, ...
-    const int dw = warp - 3;
+    const int dw = warp - kDec0;
     const int grp = dw / NDEC, dt = (dw % NDEC) * 32 + lane;
     // Epilogue operands, loaded now so that their latency hides behind the
     // decode: this lane's 4 columns of svh (gate, up) and suh (down), or of
@@ -316,12 +336,13 @@ __global__ void __launch_bounds__(kWarps * 32, 1) moe_fused_kernel(const __grid_
     }
 
     // ---------------- epilogue
-    // (1) warps 3..6 (TMEM lanes 96-127, 0-31, 32-63, 64-95 = output columns)
-    // write issuer 0's plus issuer 1's accumulator of each projection (and
-    // output tile), times sigma, transposed into a scratch [tile][NP][rows][128]
-    // over the x' and weight rings (idle once every MMA has completed).
+    // (1) four decoder warps (one per TMEM lane quarter = output columns)
+    // write the sum of the issuers' accumulators of each projection (and
+    // output tile), in issuer order, times sigma, transposed into a scratch
+    // [tile][NP][rows][128] over the x' and weight rings (idle once every MMA
+    // has completed).
     float *scratch = reinterpret_cast<float *>(smem);
-    if (warp < 7) {
+    if (dw < 4) {
       bool okw = tc::mbar_wait(accum, 0);
       okw = __all_sync(0xffffffffu, okw) && !*abort_flag;
       if (!okw && lane == 0) set_device_error(a.err, kErrBounds);
@@ -331,26 +352,26 @@ __global__ void __launch_bounds__(kWarps * 32, 1) moe_fused_kernel(const __grid_
       for (int jp = 0; jp < nts * NP; ++jp) {   // (tile, projection) jt NP + p
         const int jt = jp / NP, p = jp - jt * NP;
         for (int m0 = 0; m0 < rows; m0 += 8) {
-          uint32_t r[8], u[8];
-          const uint32_t taddr =
-              tmem_base + ((uint32_t)lane_base << 16) + (uint32_t)(((jt * NGRP) * NP + p) * XROWS + m0);
-          asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
-                       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-                         "=r"(r[7])
-                       : "r"(taddr));
-          asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
-                       : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]),
-                         "=r"(u[7])
-                       : "r"(taddr + (uint32_t)(NP * XROWS)));
-          tc::tmem_ld_wait();
-          if (nptile < 2) {            // issuer 1 had no pair: its accumulators were never written
+          float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int q = 0; q < 8; ++q) u[q] = 0u;
+          for (int g = 0; g < NISS; ++g) {
+            // issuer g's first pair of tile jt is Pt = (g - jt nptile) mod NISS;
+            // without one its accumulator was never written
+            if (((g - jt * nptile) % NISS + NISS) % NISS >= nptile) continue;
+            uint32_t r[8];
+            const uint32_t taddr = tmem_base + ((uint32_t)lane_base << 16) +
+                                   (uint32_t)(((jt * NISS + g) * NP + p) * XROWS + m0);
+            asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+                         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                           "=r"(r[7])
+                         : "r"(taddr));
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int q = 0; q < 8; ++q) sum[q] += __uint_as_float(r[q]);
           }
 #pragma unroll
           for (int q = 0; q < 8; ++q)
-            if (m0 + q < rows)
-              scratch[(jp * XROWS + m0 + q) * 128 + ncol] = (__uint_as_float(r[q]) + __uint_as_float(u[q])) * kSigma;
+            if (m0 + q < rows) scratch[(jp * XROWS + m0 + q) * 128 + ncol] = sum[q] * kSigma;
         }
       }
       tc::tc_fence_before();
@@ -464,11 +485,11 @@ static int mf_encode(CUtensorMap *m, CUtensorMapDataType dt, int rank, const voi
   return EXL3_OK;
 }
 
-// rows x cols fp16 (cols contiguous), box 128 rows x 64, 128-byte swizzle.
-static int mf_xmap(CUtensorMap *m, const void *base, int rows, int cols) {
+// rows x cols fp16 (cols contiguous), box `box_rows` rows x 64, 128-byte swizzle.
+static int mf_xmap(CUtensorMap *m, const void *base, int rows, int cols, int box_rows) {
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)mf::XROWS};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   return mf_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, "x'");
 }
 
@@ -482,15 +503,16 @@ static int mf_tmap(CUtensorMap *m, const uint16_t *trellis, long rows, int n, in
                    "trellis");
 }
 
-template <int PHASE>
+template <int PHASE, int NMAX>
 static int mf_launch(int K, const CUtensorMap &t0, const CUtensorMap &t1, const CUtensorMap &tt, const mf::Args &a,
                      int grid, cudaStream_t s) {
   cudaError_t e = cudaSuccess;
-#define EXL3_MF(KK)                                                                                         \
-  case KK: {                                                                                                \
-    auto kfn = mf::moe_fused_kernel<KK, PHASE>;                                                             \
-    cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, mf::Cfg<KK, PHASE>::SMEM_BYTES); \
-    e = launch_pdl(kfn, dim3(grid), dim3(mf::kWarps * 32), mf::Cfg<KK, PHASE>::SMEM_BYTES, s, t0, t1, tt, a);     \
+#define EXL3_MF(KK)                                                                                              \
+  case KK: {                                                                                                     \
+    using CF = mf::Cfg<KK, PHASE, NMAX>;                                                                         \
+    auto kfn = mf::moe_fused_kernel<KK, PHASE, NMAX>;                                                            \
+    cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM_BYTES);                      \
+    e = launch_pdl(kfn, dim3(grid), dim3(mf::Roles<NMAX>::WARPS * 32), CF::SMEM_BYTES, s, t0, t1, tt, a);         \
   } break;
   switch (K) {
     EXL3_MF(1) EXL3_MF(2) EXL3_MF(3) EXL3_MF(4) EXL3_MF(5) EXL3_MF(6) EXL3_MF(7) EXL3_MF(8)
@@ -500,22 +522,24 @@ static int mf_launch(int K, const CUtensorMap &t0, const CUtensorMap &t1, const 
   return exl3_cuda_check(e, "moe fused launch");
 }
 
-// Phase 1: xg, xu [U][hidden] fp16 sorted rows; w13 trellis [E][2][hidden/16][inter/16][16K].
-// splits > 1 (k split of the gate+up projection): partials [max_mtiles * inter/128][splits][2][128][128]
+// Phase 1: xg, xu [U][hidden] fp16 sorted rows; w13 trellis [E][2][hidden/16][inter/16][16K];
+// the tile list holds tiles of at most cap (32 or 128) rows.
+// splits > 1 (k split of the gate+up projection): partials [max_mtiles * inter/128][splits][2][cap][128]
 // fp32 and counters [max_mtiles * inter/128], zero on entry and left zero.
 // e_lo, e_cnt: only experts [e_lo, e_lo + e_cnt), whose trellis starts at
 // w13_trellis (e_cnt < 0: all E experts from 0).
 int exl3_launch_moe_fused_gateup(const uint16_t *xg, const uint16_t *xu, int U, int hidden, int inter, int K, int E,
                                  const uint16_t *w13_trellis, const int *mtiles, const int *n_mtiles, int max_mtiles,
-                                 const uint16_t *svh13, const uint16_t *suh2, uint16_t *hout, int splits,
+                                 int cap, const uint16_t *svh13, const uint16_t *suh2, uint16_t *hout, int splits,
                                  float *partials, int *counters, int *err, cudaStream_t s, int e_lo, int e_cnt) {
   if (e_cnt < 0) {
     e_lo = 0;
     e_cnt = E;
   }
   CUtensorMap t0, t1, tt;
-  int rc = mf_xmap(&t0, xg, U, hidden);
-  if (!rc) rc = mf_xmap(&t1, xu, U, hidden);
+  if (cap != 32 && cap != 128) return exl3_fail(EXL3_ERR_ARG, "tile capacity %d", cap);
+  int rc = mf_xmap(&t0, xg, U, hidden, cap);
+  if (!rc) rc = mf_xmap(&t1, xu, U, hidden, cap);
   if (!rc) rc = mf_tmap(&tt, w13_trellis, (long)e_cnt * 2 * (hidden / 16), inter, K, 8);
   if (rc) return rc;
   mf::Args a{};
@@ -536,15 +560,17 @@ int exl3_launch_moe_fused_gateup(const uint16_t *xg, const uint16_t *xu, int U, 
   a.ntc = 1;
   a.partials = partials;
   a.counters = counters;
-  return mf_launch<1>(K, t0, t1, tt, a, max_mtiles * a.NT * splits, s);
+  const int grid = max_mtiles * a.NT * splits;
+  return cap == 32 ? mf_launch<1, 32>(K, t0, t1, tt, a, grid, s) : mf_launch<1, 128>(K, t0, t1, tt, a, grid, s);
 }
 
 // Phase 2: h' [U][inter] fp16 sorted rows; w2 trellis [E][1][inter/16][hidden/16][16K]; d [U][hidden] fp32.
 // e_lo, e_cnt as for the gate+up launch.
 int exl3_launch_moe_fused_down(const uint16_t *hin, int U, int hidden, int inter, int K, int E,
                                const uint16_t *w2_trellis, const int *mtiles, const int *n_mtiles, int max_mtiles,
-                               const uint16_t *svh2, const float *weights, const int *perm, float *dout, int *err,
-                               cudaStream_t s, int e_lo, int e_cnt) {
+                               int cap, const uint16_t *svh2, const float *weights, const int *perm, float *dout,
+                               int *err, cudaStream_t s, int e_lo, int e_cnt) {
+  if (cap != 32 && cap != 128) return exl3_fail(EXL3_ERR_ARG, "tile capacity %d", cap);
   if (e_cnt < 0) {
     e_lo = 0;
     e_cnt = E;
@@ -553,7 +579,7 @@ int exl3_launch_moe_fused_down(const uint16_t *hin, int U, int hidden, int inter
   // h' as (64 k, U rows, inter/64 blocks): one load brings two k steps of the tile's rows
   cuuint64_t dims[3] = {64, (cuuint64_t)U, (cuuint64_t)(inter / 64)};
   cuuint64_t strides[2] = {(cuuint64_t)inter * 2, 128};
-  cuuint32_t box[3] = {64, (cuuint32_t)mf::XROWS, 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)cap, 2};
   int rc = mf_encode(&t0, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, hin, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
                      "h'");
   if (!rc) rc = mf_tmap(&tt, w2_trellis, (long)e_cnt * (inter / 16), hidden, K, 16);
@@ -579,5 +605,6 @@ int exl3_launch_moe_fused_down(const uint16_t *hin, int U, int hidden, int inter
   // twice over; few routed rows keep one tile per CTA for parallelism
   const int sms = exl3_sm_count();
   a.ntc = ((a.KB / 2) % 2 == 0 && (long)max_mtiles * (a.NT / 2) >= 2L * sms) ? 2 : 1;
-  return mf_launch<2>(K, t0, t0, tt, a, max_mtiles * ((a.NT + a.ntc - 1) / a.ntc), s);
+  const int grid = max_mtiles * ((a.NT + a.ntc - 1) / a.ntc);
+  return cap == 32 ? mf_launch<2, 32>(K, t0, t0, tt, a, grid, s) : mf_launch<2, 128>(K, t0, t0, tt, a, grid, s);
 }
