@@ -189,5 +189,35 @@ __device__ __forceinline__ void item_map(int it, int &ti, int &q) {
 }
 
 
+
+// The loop-invariant part of a decoder thread's item (the same item every
+// pair): the byte offset of its tile from the start of a k step's tile rows
+// in a trellis stage, its row group, and the two store bases of its rows in
+// an operand slot (see decode_item).
+struct ItemPlan {
+  int tile_off, q, opA, opB;
+};
+
+template <int K>
+__device__ __forceinline__ ItemPlan item_plan(int it) {
+  constexpr int G = Shape<K, 32>::G;
+  int ti, q;
+  item_map<K>(it, ti, q);
+  const int tkl = ti >> 3, tnl = ti & 7;
+  const int k0 = tkl * 16 + G * q, kr0 = k0 & 7;
+  const int base = (k0 >> 3) * 2048 + (tnl >> 2) * 1024 + kr0 * 128;
+  const int c = ((tnl & 3) * 2) ^ kr0;
+  return ItemPlan{tkl * Shape<K, 32>::ROWB + tnl * 32 * K, q, base + 16 * c, base + 16 * (c ^ 2)};
+}
+
+// Load and decode the planned item of the k step whose tile rows start at
+// `rows` into the operand slot `slot`.
+template <int K, bool OFS>
+__device__ __forceinline__ void decode_planned(const uint8_t *rows, uint8_t *slot, const ItemPlan &ip) {
+  uint32_t w[Shape<K, 32>::NW + 1];
+  load_item<K>(rows + ip.tile_off, ip.q, w);
+  decode_rows<K, 0, OFS>(w, slot + ip.opA, slot + ip.opB);
+}
+
 }  // namespace ftc
 }  // namespace exl3

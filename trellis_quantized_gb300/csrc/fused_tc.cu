@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(Roles<NMAX>::WARPS * 32, 1) fused_tc_kernel(co
     if (lane == 0) {
       for (int j = 0; j < ntst && !*abort_flag; ++j) {
         const int st = j % TS;
-        if (!tc::mbar_wait(&tempty[st], ((j / TS) & 1) ^ 1)) {
+        if (!tc::mbar_wait_backoff(&tempty[st], ((j / TS) & 1) ^ 1)) {
           set_device_error(a.err, kErrBounds);
           *abort_flag = 1;
           break;
@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(Roles<NMAX>::WARPS * 32, 1) fused_tc_kernel(co
       const uint32_t xbytes = (uint32_t)S::XSTEPS * npad * BK * 2;
       for (int j = 0; j < nxst && !*abort_flag; ++j) {
         const int st = j % XS;
-        if (!tc::mbar_wait(&xempty[st], ((j / XS) & 1) ^ 1)) {
+        if (!tc::mbar_wait_backoff(&xempty[st], ((j / XS) & 1) ^ 1)) {
           set_device_error(a.err, kErrBounds);
           *abort_flag = 1;
           break;
@@ -221,6 +221,13 @@ __global__ void __launch_bounds__(Roles<NMAX>::WARPS * 32, 1) fused_tc_kernel(co
     // ---------------- decoders: group g takes k steps i = g, g + 2, ...
     const int dw = warp - kDec0;             // 0..15
     const int grp = dw / NDEC, dt = (dw % NDEC) * 32 + lane;
+    // this thread's items of a pair (the same every pair): k step 2P + h of
+    // item it, for it2 = dt + 256 j, h = it2 / ITEMS
+    constexpr int NI = 2 * S::ITEMS / (NDEC * 32);
+    static_assert(NI * NDEC * 32 == 2 * S::ITEMS, "whole items per decoder thread");
+    ItemPlan plan[NI];
+#pragma unroll
+    for (int j = 0; j < NI; ++j) plan[j] = item_plan<K>((dt + NDEC * 32 * j) % S::ITEMS);
     for (int P = grp; P < npairs; P += NGRP) {
       const int tj = P / 2, ts = tj % TS, ps = P % NPS;   // a trellis stage holds two pairs
       const bool ok = (*abort_flag) || (tc::mbar_wait(&tfull[ts], (tj / TS) & 1) &&
@@ -229,20 +236,13 @@ __global__ void __launch_bounds__(Roles<NMAX>::WARPS * 32, 1) fused_tc_kernel(co
         if (lane == 0) set_device_error(a.err, kErrBounds);
         *abort_flag = 1;
       }
-      // the pair's items: k step 2P + h, item it (h = it2 / ITEMS)
-#pragma unroll 1
-      for (int it2 = dt; it2 < 2 * S::ITEMS; it2 += NDEC * 32) {
-        const int h = it2 / S::ITEMS, it = it2 - h * S::ITEMS;
+      // the pair's items: k step 2P + h (the operand keeps 1024 + B)
+#pragma unroll
+      for (int j = 0; j < NI; ++j) {
+        const int h = (dt + NDEC * 32 * j) / S::ITEMS;
         const int i = 2 * P + h;
-        const uint8_t *tst = sT + ts * S::T_STAGE + (i % S::TSTEPS) * S::T_BYTES;
-        uint8_t *bst = sW + (2 * ps + h) * W_BYTES;
-        int ti, q;
-        item_map<K>(it, ti, q);
-        const int tkl = ti >> 3, tnl = ti & 7;
-        const uint8_t *tile = tst + tkl * S::ROWB + tnl * 32 * K;
-        uint32_t w[S::NW + 1];
-        ftc::load_item<K>(tile, q, w);
-        decode_item<K, true>(w, bst, tkl, tnl, q);   // the operand keeps 1024 + B
+        decode_planned<K, true>(sT + ts * S::T_STAGE + (i % S::TSTEPS) * S::T_BYTES, sW + (2 * ps + h) * W_BYTES,
+                                plan[j]);
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic stores -> tensor-core reads
       __syncwarp();

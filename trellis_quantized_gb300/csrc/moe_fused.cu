@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(Roles<NMAX>::WARPS * 32, 1)
     if (lane == 0) {
       for (int j = 0; j < ntst && !*abort_flag; ++j) {
         const int st = j % TS;
-        if (!tc::mbar_wait(&tempty[st], ((j / TS) & 1) ^ 1)) {
+        if (!tc::mbar_wait_backoff(&tempty[st], ((j / TS) & 1) ^ 1)) {
           set_device_error(a.err, kErrBounds);
           *abort_flag = 1;
           break;
@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(Roles<NMAX>::WARPS * 32, 1)
     if (lane == 0) {
       for (int P = 0; P < npairs && !*abort_flag; ++P) {
         const int st = P % XS;
-        if (!tc::mbar_wait(&xempty[st], ((P / XS) & 1) ^ 1)) {
+        if (!tc::mbar_wait_backoff(&xempty[st], ((P / XS) & 1) ^ 1)) {
           set_device_error(a.err, kErrBounds);
           *abort_flag = 1;
           break;
@@ -302,6 +302,13 @@ __global__ void __launch_bounds__(Roles<NMAX>::WARPS * 32, 1)
         if (lane < XROWS / (NGRP * NDEC) && m < rows) row_w = a.weights[a.perm[row0 + m]];
       }
     }
+    // this thread's items of a pair (the same every pair): half h = it2 /
+    // ITEMS of item it, for it2 = dt + 256 j
+    constexpr int NI = 2 * C::ITEMS / (NDEC * 32);
+    static_assert(NI * NDEC * 32 == 2 * C::ITEMS, "whole items per decoder thread");
+    ftc::ItemPlan plan[NI];
+#pragma unroll
+    for (int j = 0; j < NI; ++j) plan[j] = ftc::item_plan<K>((dt + NDEC * 32 * j) % C::ITEMS);
     for (int P = grp; P < npairs; P += NGRP) {
       const int tj = P / 2, ts = tj % TS, ps = P % NPS;
       const bool ok = (*abort_flag) || (tc::mbar_wait(&tfull[ts], (tj / TS) & 1) &&
@@ -310,22 +317,14 @@ __global__ void __launch_bounds__(Roles<NMAX>::WARPS * 32, 1)
         if (lane == 0) set_device_error(a.err, kErrBounds);
         *abort_flag = 1;
       }
-      // the pair's items: half h = it2 / ITEMS, item it
-#pragma unroll 1
-      for (int it2 = dt; it2 < 2 * C::ITEMS; it2 += NDEC * 32) {
-        const int h = it2 / C::ITEMS, it = it2 - h * C::ITEMS;
+      // the pair's items
+#pragma unroll
+      for (int j = 0; j < NI; ++j) {
+        const int h = (dt + NDEC * 32 * j) / C::ITEMS;
         // phase 1: projection h of k step P (stage rows h * 8 + (P % 2) * 4);
         // phase 2: k step 2P + h (stage rows ((2P + h) % 4) * 4)
         const int r0 = PHASE == 1 ? h * 8 + (P % 2) * 4 : ((2 * P + h) % 4) * 4;
-        const uint8_t *tst = sT + ts * C::T_STAGE + r0 * C::ROWB;
-        uint8_t *bst = sW + (2 * ps + h) * W_BYTES;
-        int ti, q;
-        ftc::item_map<K>(it, ti, q);
-        const int tkl = ti >> 3, tnl = ti & 7;
-        const uint8_t *tilep = tst + tkl * C::ROWB + tnl * 32 * K;
-        uint32_t w[S::NW + 1];
-        ftc::load_item<K>(tilep, q, w);
-        ftc::decode_item<K>(w, bst, tkl, tnl, q);
+        ftc::decode_planned<K, false>(sT + ts * C::T_STAGE + r0 * C::ROWB, sW + (2 * ps + h) * W_BYTES, plan[j]);
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic stores -> tensor-core reads
       __syncwarp();
