@@ -90,6 +90,19 @@ def test_moe_many_rows_one_expert_spans_tiles():
     assert_close(_run(c, d), _oracle(c), "moe one expert with 150+ rows")
 
 
+def test_moe_expert_beyond_one_256_row_tile():
+    """400 tokens, top-2 over 3 experts, every first slot on expert 1: 800
+    routed rows (at least 96 per expert) take 256-row tiles, expert 1's 400
+    rows span two of them (256 + 144) and its epilogue runs in 128-row
+    chunks; experts 0 and 2 hold 200 rows each in one tile."""
+    c = synth.moe_case(52, 1, 400, E=3, topk=2, hidden=512, inter=256, K=3)
+    c.ids[:, 0] = 1
+    c.ids[:, 1] = (np.arange(400) % 2) * 2
+    d = _dev_case(c)
+    for od in (tq.EXL3_OUT_F16, tq.EXL3_OUT_F32):
+        assert_close(_run(c, d, od), _oracle(c), f"moe 256-row tiles out={od}")
+
+
 def test_moe_invalid_expert_id_is_reported_and_skipped():
     c = synth.moe_case(53, 0, 4, E=4, topk=2, hidden=256, inter=128, K=3)
     d = _dev_case(c)

@@ -67,6 +67,7 @@ int exl3_launch_moe_fused_gateup(const uint16_t *xg, const uint16_t *xu, int U, 
                                  int cap, const uint16_t *svh13, const uint16_t *suh2, uint16_t *hout, int splits,
                                  float *partials, int *counters, int *err, cudaStream_t s, int e_lo = 0,
                                  int e_cnt = -1);
+bool exl3_moe_fused_cap_fits(int cap, int K);
 int exl3_launch_moe_fused_down(const uint16_t *hin, int U, int hidden, int inter, int K, int E,
                                const uint16_t *w2_trellis, const int *mtiles, const int *n_mtiles, int max_mtiles,
                                int cap, const uint16_t *svh2, const float *weights, const int *perm, float *dout,
@@ -291,8 +292,11 @@ MoeWs moe_ws(int T, int topk, int E, int hidden, int inter, int K13, int K2, boo
   }
   // Tiles of 32 rows (the grouped kernels then run MMAs 16 or 32 rows wide,
   // with four issuers) when the call routes at most 16 rows per expert on
-  // average; 128 rows otherwise.
+  // average; 256 rows when it routes at least 96 (so that an expert's rows
+  // stay in one tile and its weights are decoded once) and the widths fit;
+  // 128 rows otherwise.
   w.cap = U <= (size_t)16 * E ? 32 : 128;
+  if (U >= (size_t)96 * E && exl3_moe_fused_cap_fits(256, K13 > K2 ? K13 : K2)) w.cap = 256;
   w.max_mtiles = (int)(U / w.cap + E + 1);
   size_t off = kDataOff;
   auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes); return o; };
@@ -316,7 +320,7 @@ MoeWs moe_ws(int T, int topk, int E, int hidden, int inter, int K13, int K2, boo
   const long tiles1 = (long)w.grid_mtiles * (inter / 128);
   const int kb = hidden / 64, sms = exl3_sm_count();
   w.splits = 1;
-  for (int sp = 2; sp <= 8; ++sp)
+  for (int sp = 2; sp <= 8 && w.cap <= 128; ++sp)
     if (kb % sp == 0 && (kb / sp) % 2 == 0 && kb / sp >= 4 && tiles1 * sp <= sms) w.splits = sp;
   if (w.splits > 1) w.partials = take(sizeof(float) * (size_t)tiles1 * w.splits * 2 * w.cap * 128);
   w.total = off;
@@ -674,10 +678,17 @@ int exl3_moe_grouped(const uint16_t *x, int T, int hidden, const int32_t *topk_i
                          "moe combine launch");
 }
 
+// The largest width of a mixed projection's experts (host array K[E]).
+static int max_width(const exl3_expert_proj_mixed *p, int E) {
+  int m = 1;
+  for (int e = 0; p->K && e < E; ++e) m = p->K[e] > m ? p->K[e] : m;
+  return m;
+}
+
 size_t exl3_moe_mixed_workspace_size(int T, int topk, int E, const exl3_expert_proj_mixed *w13,
                                      const exl3_expert_proj_mixed *w2) {
-  if (!w13 || !w2 || T < 1 || topk < 1 || E < 1 || E > 1024) return 0;
-  return moe_ws(T, topk, E, w13->k, w13->n, 1, 1, false).total;
+  if (!w13 || !w2 || !w13->K || !w2->K || T < 1 || topk < 1 || E < 1 || E > 1024) return 0;
+  return moe_ws(T, topk, E, w13->k, w13->n, max_width(w13, E), max_width(w2, E), false).total;
 }
 
 int exl3_moe_grouped_mixed(const uint16_t *x, int T, int hidden, const int32_t *topk_ids,
@@ -700,7 +711,7 @@ int exl3_moe_grouped_mixed(const uint16_t *x, int T, int hidden, const int32_t *
   if (out_dtype != EXL3_OUT_F16 && out_dtype != EXL3_OUT_F32)
     return exl3_fail(EXL3_ERR_ARG, "out_dtype %d invalid", out_dtype);
   const int U = T * topk;
-  const MoeWs L = moe_ws(T, topk, E, hidden, inter, 1, 1, false);
+  const MoeWs L = moe_ws(T, topk, E, hidden, inter, max_width(w13, E), max_width(w2, E), false);
   EXL3_TRY(check_workspace(workspace, ws_bytes, L.total));
   int *err = at<int>(workspace, 0);
   int *counts = at<int>(workspace, L.counts), *offsets = at<int>(workspace, L.offsets);

@@ -211,7 +211,24 @@ __global__ void __launch_bounds__(1024) remap_small_kernel(const int32_t *__rest
 
 // Sorted rows of the transformed token inputs for gate and up:
 // xg[i] = RHT(x_t . suh_gate[e]), xu[i] = RHT(x_t . suh_up[e]), t = perm[i] / topk.
-// One warp per sorted row: both slots, every 128-block of the row.
+// One warp per sorted row: the row's unit and expert are looked up once, and
+// the row's 512-element chunks follow one another with the loads of chunk
+// c + 1 issued before chunk c is transformed (lane l holds 16 contiguous
+// elements of a chunk, the fwht128_x8 layout).
+struct GatherIn {
+  uint4 x[2], g[2], u[2];
+};
+
+__device__ __forceinline__ void gather_load(GatherIn &in, const __half *xr, const __half *sg, const __half *su,
+                                            int col, bool live) {
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    in.x[q] = live ? *reinterpret_cast<const uint4 *>(xr + col + 8 * q) : make_uint4(0u, 0u, 0u, 0u);
+    in.g[q] = live ? __ldg(reinterpret_cast<const uint4 *>(sg + col + 8 * q)) : make_uint4(0u, 0u, 0u, 0u);
+    in.u[q] = live ? __ldg(reinterpret_cast<const uint4 *>(su + col + 8 * q)) : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
 __global__ void __launch_bounds__(256) gather_rht_kernel(const __half *__restrict__ x, int hidden, int topk,
                                                          const int *__restrict__ perm,
                                                          const int *__restrict__ offsets, int E,
@@ -221,33 +238,24 @@ __global__ void __launch_bounds__(256) gather_rht_kernel(const __half *__restric
   pdl_trigger();
   pdl_wait();
   const int lane = threadIdx.x & 31;
-  const long wid = (long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int chunks = (hidden + 511) / 512;
-  const int i = (int)(wid / chunks);             // sorted row; one 512-element chunk per warp
-  if (i >= offsets[E]) return;                  // uniform per warp
+  const long i = (long)blockIdx.x * 8 + (threadIdx.x >> 5);   // sorted row
+  if (i >= offsets[E]) return;                                // uniform per warp
   const int u = perm[i];
   const int t = u / topk, e = ids[u];
   const __half *xr = x + (long)t * hidden;
   const __half *sg = suh13 + (long)e * 2 * hidden, *su = sg + hidden;
-  __half *dg = xg + (long)i * hidden, *du = xu + (long)i * hidden;
-  // the warp's chunk covers 512 elements (four 128-blocks): lane l holds 16
-  // contiguous elements, col = 512 c + 16 l (fwht128_x8 layout)
-  {
-    const int c0 = (int)(wid % chunks) * 512;
-    const int col = c0 + 16 * lane;
+  __half *dg = xg + i * hidden, *du = xu + i * hidden;
+  const int chunks = (hidden + 511) / 512;
+  GatherIn cur, nxt;
+  gather_load(cur, xr, sg, su, 16 * lane, 16 * lane < hidden);
+#pragma unroll 1
+  for (int c = 0; c < chunks; ++c) {
+    const int col = c * 512 + 16 * lane;
     const bool in = col < hidden;      // whole 128-blocks are in or out (hidden % 128 == 0)
-    uint4 xv[2] = {}, gv[2] = {}, uv[2] = {};
-    if (in) {
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        xv[q] = *reinterpret_cast<const uint4 *>(xr + col + 8 * q);
-        gv[q] = __ldg(reinterpret_cast<const uint4 *>(sg + col + 8 * q));
-        uv[q] = __ldg(reinterpret_cast<const uint4 *>(su + col + 8 * q));
-      }
-    }
-    const __half *xh = reinterpret_cast<const __half *>(xv);
-    const __half *gh = reinterpret_cast<const __half *>(gv);
-    const __half *uh = reinterpret_cast<const __half *>(uv);
+    if (c + 1 < chunks) gather_load(nxt, xr, sg, su, col + 512, col + 512 < hidden);
+    const __half *xh = reinterpret_cast<const __half *>(cur.x);
+    const __half *gh = reinterpret_cast<const __half *>(cur.g);
+    const __half *uh = reinterpret_cast<const __half *>(cur.u);
     float a[16], b[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
@@ -270,11 +278,10 @@ __global__ void __launch_bounds__(256) gather_rht_kernel(const __half *__restric
         *reinterpret_cast<uint4 *>(du + col + 8 * q) = reinterpret_cast<const uint4 *>(ou)[q];
       }
     }
+    cur = nxt;
   }
 }
 
-// y_t = sum over slots s (in order) of d[pos(t, s)]; d already carries the
-// routing weight.  Invalid units (pos = -1) contribute nothing.
 template <bool F32OUT>
 __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ d, const int *__restrict__ pos,
                                                       int T, int topk, int hidden, void *__restrict__ y) {
@@ -314,11 +321,11 @@ int exl3_moe_remap_chunk(int E) {
 }
 
 // chunk_tab: [ceil(U / exl3_moe_remap_chunk(E))][E] ints of workspace.
-// cap: rows per tile (32 or 128) of the tile list the grouped kernels read.
+// cap: rows per tile (32, 128 or 256) of the tile list the grouped kernels read.
 cudaError_t exl3_launch_moe_remap(const int32_t *ids, int U, int E, int *counts, int *offsets, int *perm, int *pos,
                                   int *mtiles, int *n_mtiles, int max_mtiles, int cap, int *chunk_tab, int *err,
                                   cudaStream_t s) {
-  if (E < 1 || E > 1024 || (cap != 32 && cap != 128)) return cudaErrorInvalidValue;
+  if (E < 1 || E > 1024 || (cap != 32 && cap != 128 && cap != 256)) return cudaErrorInvalidValue;
   moe::Plan p{counts, offsets, perm, pos, reinterpret_cast<int4 *>(mtiles), n_mtiles, chunk_tab};
   if (U <= moe::kSmallU && E <= moe::kSmallE) {
     return launch_pdl(moe::remap_small_kernel, dim3(1), dim3(1024), 0, s, ids, U, E, p, max_mtiles, cap, err);
@@ -337,8 +344,7 @@ cudaError_t exl3_launch_moe_remap(const int32_t *ids, int U, int E, int *counts,
 cudaError_t exl3_launch_moe_gather(const uint16_t *x, int U, int hidden, int topk, const int *perm,
                                    const int *offsets, int E, const int32_t *ids, const uint16_t *suh13,
                                    uint16_t *xg, uint16_t *xu, cudaStream_t s) {
-  const long warps = (long)U * ((hidden + 511) / 512);     // one warp per (row, 512 chunk); rows <= U
-  const unsigned grid = (unsigned)((warps + 7) / 8);
+  const unsigned grid = (unsigned)(((long)U + 7) / 8);       // one warp per sorted row; rows <= U
   if (grid == 0) return cudaSuccess;
   return launch_pdl(moe::gather_rht_kernel, dim3(grid), dim3(256), 0, s, reinterpret_cast<const __half *>(x), hidden,
                     topk, perm, offsets, E, ids, reinterpret_cast<const __half *>(suh13),

@@ -7,7 +7,8 @@
 //
 // A CTA handles one (expert tile, 128-column output tile) pair of the
 // device-side tile list.  A tile holds up to NMAX routed rows of one expert
-// (NMAX = 32 when the call routes few rows per expert, else 128); the MMA
+// (NMAX = 32 when the call routes few rows per expert, 256 when it routes
+// many and the widths leave room for 64 KB x' stages, else 128); the MMA
 // computes the transposed product (decoded weights as the MN-major A operand,
 // M = 128 output columns; the tile's x' rows as the K-major B operand, N =
 // the tile's rows rounded up to 16).  Roles (2 + NISS + 16 warps):
@@ -15,8 +16,8 @@
 //                  over all experts' trellis (16 tile rows per stage)
 //   warps 1..NISS  MMA issuers: pair P goes to issuer P mod NISS, into that
 //                  issuer's own accumulators (summed in a fixed order by the
-//                  epilogue); four issuers for 32-row tiles, two for 128
-//                  (TMEM holds 512 columns)
+//                  epilogue); four issuers for 32-row tiles, two for 128, one
+//                  for 256 (TMEM holds 512 columns)
 //   next 16 warps  decoders in two groups of eight, taking alternate "pairs":
 //                  phase 1 a pair is the gate and up weights of one k step,
 //                  phase 2 two k steps of down; one fence and one signal per pair
@@ -46,7 +47,7 @@ using ftc::W_BYTES;
 
 template <int NMAX>
 struct Roles {
-  static constexpr int NISS = NMAX <= 32 ? 4 : 2;      // MMA issuer warps
+  static constexpr int NISS = NMAX <= 32 ? 4 : (NMAX <= 128 ? 2 : 1);   // MMA issuer warps
   static constexpr int DEC0 = 1 + NISS;                  // first decoder warp
   static constexpr int XWARP = DEC0 + NGRP * NDEC;       // the x' producer
   static constexpr int WARPS = XWARP + 1;
@@ -66,6 +67,9 @@ struct Cfg {
   // trellis stages, else 2 (a multiple of the issuers and of the groups)
   static constexpr int NPS_FIT4 = (BUDGET - 8 * W_BYTES - 2 * X_STAGE - 2 * T_STAGE) >= 0;
   static constexpr int NPS = (NPS_FIT4 || NISS > 2) ? 4 : 2;
+  // the epilogue transposes the accumulators into a scratch over the rings,
+  // ECH rows at a time
+  static constexpr int ECH = NMAX < 128 ? NMAX : 128;
   static constexpr int W_RING = 2 * NPS * W_BYTES;
   // x' ring: as deep as the budget allows after two trellis stages (the
   // loads come from L2 or HBM and must run several pairs ahead), a multiple
@@ -79,12 +83,11 @@ struct Cfg {
   // phase 2 may take two output tiles per CTA (one accumulator set each)
   static constexpr int NTC = PHASE == 2 ? 2 : 1;
   static constexpr uint32_t TMEM_COLS = NISS * NP * XROWS * NTC;
-  static_assert(TS >= 2 && XS >= NISS, "operand rings too shallow");
-  static_assert(NPS % NISS == 0 && NPS % NGRP == 0, "one issuer and one decoder group per weight slot");
-  static_assert(XS % NISS == 0, "one issuer per x' slot");
-  static_assert(NTC * NP * XROWS * 128 * 4 <= XS * X_STAGE + W_RING, "epilogue scratch exceeds the operand rings");
-  static_assert(TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM");
-  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+  // whether this width and tile capacity fit (256-row tiles leave room for
+  // K <= 4 only); the host launches only configurations that do
+  static constexpr bool OK = TS >= 2 && XS >= NISS && NPS % NISS == 0 && NPS % NGRP == 0 && XS % NISS == 0 &&
+                             NTC * NP * ECH * 128 * 4 <= XS * X_STAGE + W_RING && TMEM_COLS <= 512 &&
+                             (TMEM_COLS & (TMEM_COLS - 1)) == 0 && SMEM_BYTES <= 227 * 1024;
 };
 
 struct Args {
@@ -107,7 +110,7 @@ struct Args {
   // to arrive adds the partial sums in split order
   int splits;
   int ntc;                  // output tiles per CTA (phase 2: 1 or 2)
-  float *partials;          // [tiles][splits][2][NMAX][128] fp32
+  float *partials;          // [tiles][splits][2][NMAX][128] fp32 (splits > 1 only with NMAX <= 128)
   int *counters;            // [tiles], zero between calls
   // experts [e_lo, e_hi) only: the trellis map covers just their arena
   // (row 0 = expert e_lo) and tiles of other experts are left to other launches
@@ -120,6 +123,7 @@ __global__ void __launch_bounds__(Roles<NMAX>::WARPS * 32, 1)
                      const __grid_constant__ CUtensorMap tmT, Args a) {
   using C = Cfg<K, PHASE, NMAX>;
   using S = ftc::Shape<K, 32>;
+  static_assert(C::OK, "rings, TMEM and shared memory fit this width and tile capacity");
   constexpr int NP = C::NP, XS = C::XS, TS = C::TS, NPS = C::NPS, NISS = C::NISS, XROWS = C::XROWS;
   constexpr int kDec0 = Roles<NMAX>::DEC0, kXWarp = Roles<NMAX>::XWARP;
   const int tile = blockIdx.x / a.splits, split = blockIdx.x % a.splits;
@@ -334,128 +338,138 @@ __global__ void __launch_bounds__(Roles<NMAX>::WARPS * 32, 1)
       }
     }
 
-    // ---------------- epilogue
+    // ---------------- epilogue, ECH rows of the tile at a time
     // (1) four decoder warps (one per TMEM lane quarter = output columns)
     // write the sum of the issuers' accumulators of each projection (and
     // output tile), in issuer order, times sigma, transposed into a scratch
-    // [tile][NP][rows][128] over the x' and weight rings (idle once every MMA
-    // has completed).
+    // [tile][NP][ECH rows][128] over the x' and weight rings (idle once every
+    // MMA has completed).
+    constexpr int ECH = C::ECH;
     float *scratch = reinterpret_cast<float *>(smem);
     if (dw < 4) {
       bool okw = tc::mbar_wait(accum, 0);
       okw = __all_sync(0xffffffffu, okw) && !*abort_flag;
       if (!okw && lane == 0) set_device_error(a.err, kErrBounds);
       tc::tc_fence_after();
-      const int lane_base = 32 * (warp & 3);
-      const int ncol = lane_base + lane;
-      for (int jp = 0; jp < nts * NP; ++jp) {   // (tile, projection) jt NP + p
-        const int jt = jp / NP, p = jp - jt * NP;
-        for (int m0 = 0; m0 < rows; m0 += 8) {
-          float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    }
+    for (int mc = 0; mc < rows; mc += ECH) {
+      const int mrows = min(ECH, rows - mc);
+      if (dw < 4) {
+        const int lane_base = 32 * (warp & 3);
+        const int ncol = lane_base + lane;
+        for (int jp = 0; jp < nts * NP; ++jp) {   // (tile, projection) jt NP + p
+          const int jt = jp / NP, p = jp - jt * NP;
+          for (int m0 = 0; m0 < mrows; m0 += 8) {
+            float sum[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int g = 0; g < NISS; ++g) {
-            // issuer g's first pair of tile jt is Pt = (g - jt nptile) mod NISS;
-            // without one its accumulator was never written
-            if (((g - jt * nptile) % NISS + NISS) % NISS >= nptile) continue;
-            uint32_t r[8];
-            const uint32_t taddr = tmem_base + ((uint32_t)lane_base << 16) +
-                                   (uint32_t)(((jt * NISS + g) * NP + p) * XROWS + m0);
-            asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
-                         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-                           "=r"(r[7])
-                         : "r"(taddr));
-            tc::tmem_ld_wait();
+            for (int g = 0; g < NISS; ++g) {
+              // issuer g's first pair of tile jt is Pt = (g - jt nptile) mod NISS;
+              // without one its accumulator was never written
+              if (((g - jt * nptile) % NISS + NISS) % NISS >= nptile) continue;
+              uint32_t r[8];
+              const uint32_t taddr = tmem_base + ((uint32_t)lane_base << 16) +
+                                     (uint32_t)(((jt * NISS + g) * NP + p) * XROWS + mc + m0);
+              asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+                           : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                             "=r"(r[7])
+                           : "r"(taddr));
+              tc::tmem_ld_wait();
 #pragma unroll
-            for (int q = 0; q < 8; ++q) sum[q] += __uint_as_float(r[q]);
+              for (int q = 0; q < 8; ++q) sum[q] += __uint_as_float(r[q]);
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              if (m0 + q < mrows) scratch[(jp * ECH + m0 + q) * 128 + ncol] = sum[q] * kSigma;
           }
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            if (m0 + q < rows) scratch[(jp * XROWS + m0 + q) * 128 + ncol] = sum[q] * kSigma;
         }
       }
-      tc::tc_fence_before();
-    }
-    asm volatile("bar.sync 1, %0;" ::"n"(NGRP * NDEC * 32) : "memory");
-    bool finish = true;
-    if (PHASE == 1 && a.splits > 1) {
-      // split over k: store this split's sums, count the arrival; the last CTA
-      // of the tile adds all splits in order (no CTA waits for another)
-      constexpr int TILE_F = 2 * XROWS * 128;
-      float *part = a.partials + ((long)tile * a.splits + split) * TILE_F;
-#pragma unroll
-      for (int p = 0; p < 2; ++p)
-        for (int m = dw; m < rows; m += NGRP * NDEC)
-          *reinterpret_cast<float4 *>(part + (p * XROWS + m) * 128 + 4 * lane) =
-              *reinterpret_cast<const float4 *>(scratch + (p * XROWS + m) * 128 + 4 * lane);
-      __threadfence();
       asm volatile("bar.sync 1, %0;" ::"n"(NGRP * NDEC * 32) : "memory");
-      if (dw == 0 && lane == 0) {
-        const int old = atomicAdd(a.counters + tile, 1);
-        if (old >= a.splits) set_device_error(a.err, kErrDirtyCounter);
-        *s_last = (old == a.splits - 1);
-      }
-      asm volatile("bar.sync 1, %0;" ::"n"(NGRP * NDEC * 32) : "memory");
-      finish = *s_last != 0;
-      if (finish) {
-        __threadfence();
-        const float *base = a.partials + (long)tile * a.splits * TILE_F;
+      bool finish = true;
+      if (PHASE == 1 && a.splits > 1) {
+        // split over k (the host uses it with one chunk only, NMAX <= 128):
+        // store this split's sums, count the arrival; the last CTA of the
+        // tile adds all splits in order (no CTA waits for another)
+        constexpr int TILE_F = 2 * XROWS * 128;
+        float *part = a.partials + ((long)tile * a.splits + split) * TILE_F;
 #pragma unroll
         for (int p = 0; p < 2; ++p)
-          for (int m = dw; m < rows; m += NGRP * NDEC) {   // the rows this warp transforms below
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int sp = 0; sp < a.splits; ++sp) {
-              const float4 t = __ldcg(reinterpret_cast<const float4 *>(base + sp * TILE_F + (p * XROWS + m) * 128 + 4 * lane));
-              acc.x += t.x;
-              acc.y += t.y;
-              acc.z += t.z;
-              acc.w += t.w;
-            }
-            *reinterpret_cast<float4 *>(scratch + (p * XROWS + m) * 128 + 4 * lane) = acc;
-          }
-        if (dw == 0 && lane == 0) a.counters[tile] = 0;   // leave the workspace clean
-        __syncwarp();
-      }
-    }
-    // (2) one warp per row of the tile
-    for (int m = dw; finish && m < rows; m += NGRP * NDEC) {
-      const long row = (long)row0 + m;
-      const float4 g4 = *reinterpret_cast<const float4 *>(scratch + m * 128 + 4 * lane);
-      float v[4] = {g4.x, g4.y, g4.z, g4.w};
-      fwht128_warp(v, lane);
-      if (PHASE == 1) {
-        const float4 u4 = *reinterpret_cast<const float4 *>(scratch + (XROWS + m) * 128 + 4 * lane);
-        float u[4] = {u4.x, u4.y, u4.z, u4.w};
-        fwht128_warp(u, lane);
+          for (int m = dw; m < mrows; m += NGRP * NDEC)
+            *reinterpret_cast<float4 *>(part + (p * XROWS + m) * 128 + 4 * lane) =
+                *reinterpret_cast<const float4 *>(scratch + (p * ECH + m) * 128 + 4 * lane);
+        __threadfence();
+        asm volatile("bar.sync 1, %0;" ::"n"(NGRP * NDEC * 32) : "memory");
+        if (dw == 0 && lane == 0) {
+          const int old = atomicAdd(a.counters + tile, 1);
+          if (old >= a.splits) set_device_error(a.err, kErrDirtyCounter);
+          *s_last = (old == a.splits - 1);
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(NGRP * NDEC * 32) : "memory");
+        finish = *s_last != 0;
+        if (finish) {
+          __threadfence();
+          const float *base = a.partials + (long)tile * a.splits * TILE_F;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float gg = v[q] * kRhtScale * ep_a[q];
-          const float uu = u[q] * kRhtScale * ep_b[q];
-          v[q] = gg / (1.0f + expf(-gg)) * uu * ep_c[q];   // h . suh_down
-        }
-        fwht128_warp(v, lane);
-        __half2 o[2] = {__floats2half2_rn(v[0] * kRhtScale, v[1] * kRhtScale),
-                        __floats2half2_rn(v[2] * kRhtScale, v[3] * kRhtScale)};
-        *reinterpret_cast<uint2 *>(a.hout + row * a.inter + col0 + 4 * lane) = *reinterpret_cast<uint2 *>(o);
-      } else {
-        const float w = __shfl_sync(0xffffffffu, row_w, m / (NGRP * NDEC));
-        float4 o;
-        o.x = v[0] * kRhtScale * ep_a[0] * w;
-        o.y = v[1] * kRhtScale * ep_a[1] * w;
-        o.z = v[2] * kRhtScale * ep_a[2] * w;
-        o.w = v[3] * kRhtScale * ep_a[3] * w;
-        *reinterpret_cast<float4 *>(a.dout + row * a.hidden + col0 + 4 * lane) = o;
-        if (nts > 1) {   // the second output tile
-          const float4 h4 = *reinterpret_cast<const float4 *>(scratch + (XROWS + m) * 128 + 4 * lane);
-          float t[4] = {h4.x, h4.y, h4.z, h4.w};
-          fwht128_warp(t, lane);
-          o.x = t[0] * kRhtScale * ep_b[0] * w;
-          o.y = t[1] * kRhtScale * ep_b[1] * w;
-          o.z = t[2] * kRhtScale * ep_b[2] * w;
-          o.w = t[3] * kRhtScale * ep_b[3] * w;
-          *reinterpret_cast<float4 *>(a.dout + row * a.hidden + col0 + BN + 4 * lane) = o;
+          for (int p = 0; p < 2; ++p)
+            for (int m = dw; m < mrows; m += NGRP * NDEC) {   // the rows this warp transforms below
+              float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+              for (int sp = 0; sp < a.splits; ++sp) {
+                const float4 t =
+                    __ldcg(reinterpret_cast<const float4 *>(base + sp * TILE_F + (p * XROWS + m) * 128 + 4 * lane));
+                acc.x += t.x;
+                acc.y += t.y;
+                acc.z += t.z;
+                acc.w += t.w;
+              }
+              *reinterpret_cast<float4 *>(scratch + (p * ECH + m) * 128 + 4 * lane) = acc;
+            }
+          if (dw == 0 && lane == 0) a.counters[tile] = 0;   // leave the workspace clean
+          __syncwarp();
         }
       }
+      // (2) one warp per row of the chunk
+      for (int ml = dw; finish && ml < mrows; ml += NGRP * NDEC) {
+        const int m = mc + ml;
+        const long row = (long)row0 + m;
+        const float4 g4 = *reinterpret_cast<const float4 *>(scratch + ml * 128 + 4 * lane);
+        float v[4] = {g4.x, g4.y, g4.z, g4.w};
+        fwht128_warp(v, lane);
+        if (PHASE == 1) {
+          const float4 u4 = *reinterpret_cast<const float4 *>(scratch + (ECH + ml) * 128 + 4 * lane);
+          float u[4] = {u4.x, u4.y, u4.z, u4.w};
+          fwht128_warp(u, lane);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float gg = v[q] * kRhtScale * ep_a[q];
+            const float uu = u[q] * kRhtScale * ep_b[q];
+            v[q] = gg / (1.0f + expf(-gg)) * uu * ep_c[q];   // h . suh_down
+          }
+          fwht128_warp(v, lane);
+          __half2 o[2] = {__floats2half2_rn(v[0] * kRhtScale, v[1] * kRhtScale),
+                          __floats2half2_rn(v[2] * kRhtScale, v[3] * kRhtScale)};
+          *reinterpret_cast<uint2 *>(a.hout + row * a.inter + col0 + 4 * lane) = *reinterpret_cast<uint2 *>(o);
+        } else {
+          const float w = __shfl_sync(0xffffffffu, row_w, m / (NGRP * NDEC));
+          float4 o;
+          o.x = v[0] * kRhtScale * ep_a[0] * w;
+          o.y = v[1] * kRhtScale * ep_a[1] * w;
+          o.z = v[2] * kRhtScale * ep_a[2] * w;
+          o.w = v[3] * kRhtScale * ep_a[3] * w;
+          *reinterpret_cast<float4 *>(a.dout + row * a.hidden + col0 + 4 * lane) = o;
+          if (nts > 1) {   // the second output tile
+            const float4 h4 = *reinterpret_cast<const float4 *>(scratch + (ECH + ml) * 128 + 4 * lane);
+            float t[4] = {h4.x, h4.y, h4.z, h4.w};
+            fwht128_warp(t, lane);
+            o.x = t[0] * kRhtScale * ep_b[0] * w;
+            o.y = t[1] * kRhtScale * ep_b[1] * w;
+            o.z = t[2] * kRhtScale * ep_b[2] * w;
+            o.w = t[3] * kRhtScale * ep_b[3] * w;
+            *reinterpret_cast<float4 *>(a.dout + row * a.hidden + col0 + BN + 4 * lane) = o;
+          }
+        }
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(NGRP * NDEC * 32) : "memory");   // the scratch is reused
     }
+    if (dw < 4) tc::tc_fence_before();
   }
 
   tc::tc_fence_before();
@@ -507,18 +521,41 @@ static int mf_launch(int K, const CUtensorMap &t0, const CUtensorMap &t1, const 
                      int grid, cudaStream_t s) {
   cudaError_t e = cudaSuccess;
 #define EXL3_MF(KK)                                                                                              \
-  case KK: {                                                                                                     \
-    using CF = mf::Cfg<KK, PHASE, NMAX>;                                                                         \
-    auto kfn = mf::moe_fused_kernel<KK, PHASE, NMAX>;                                                            \
-    cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM_BYTES);                      \
-    e = launch_pdl(kfn, dim3(grid), dim3(mf::Roles<NMAX>::WARPS * 32), CF::SMEM_BYTES, s, t0, t1, tt, a);         \
-  } break;
+  case KK:                                                                                                       \
+    if constexpr (mf::Cfg<KK, PHASE, NMAX>::OK) {                                                                \
+      using CF = mf::Cfg<KK, PHASE, NMAX>;                                                                       \
+      auto kfn = mf::moe_fused_kernel<KK, PHASE, NMAX>;                                                          \
+      cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM_BYTES);                    \
+      e = launch_pdl(kfn, dim3(grid), dim3(mf::Roles<NMAX>::WARPS * 32), CF::SMEM_BYTES, s, t0, t1, tt, a);       \
+    } else {                                                                                                     \
+      return exl3_fail(EXL3_ERR_ARG, "tile capacity %d does not fit K = %d", NMAX, KK);                          \
+    }                                                                                                            \
+    break;
   switch (K) {
     EXL3_MF(1) EXL3_MF(2) EXL3_MF(3) EXL3_MF(4) EXL3_MF(5) EXL3_MF(6) EXL3_MF(7) EXL3_MF(8)
     default: return exl3_fail(EXL3_ERR_BITS, "K = %d", K);
   }
 #undef EXL3_MF
   return exl3_cuda_check(e, "moe fused launch");
+}
+
+// Whether the grouped kernels have a configuration for tiles of `cap` rows
+// at width K.
+bool exl3_moe_fused_cap_fits(int cap, int K) {
+  bool ok = false;
+#define EXL3_MF_FIT(KK)                                                                                         \
+  case KK:                                                                                                      \
+    ok = cap == 32 ? (mf::Cfg<KK, 1, 32>::OK && mf::Cfg<KK, 2, 32>::OK)                                        \
+                   : cap == 128 ? (mf::Cfg<KK, 1, 128>::OK && mf::Cfg<KK, 2, 128>::OK)                           \
+                                : (mf::Cfg<KK, 1, 256>::OK && mf::Cfg<KK, 2, 256>::OK);                          \
+    break;
+  switch (K) {
+    EXL3_MF_FIT(1) EXL3_MF_FIT(2) EXL3_MF_FIT(3) EXL3_MF_FIT(4) EXL3_MF_FIT(5) EXL3_MF_FIT(6) EXL3_MF_FIT(7)
+    EXL3_MF_FIT(8)
+    default: break;
+  }
+#undef EXL3_MF_FIT
+  return ok;
 }
 
 // Phase 1: xg, xu [U][hidden] fp16 sorted rows; w13 trellis [E][2][hidden/16][inter/16][16K];
@@ -536,7 +573,7 @@ int exl3_launch_moe_fused_gateup(const uint16_t *xg, const uint16_t *xu, int U, 
     e_cnt = E;
   }
   CUtensorMap t0, t1, tt;
-  if (cap != 32 && cap != 128) return exl3_fail(EXL3_ERR_ARG, "tile capacity %d", cap);
+  if (cap != 32 && cap != 128 && cap != 256) return exl3_fail(EXL3_ERR_ARG, "tile capacity %d", cap);
   int rc = mf_xmap(&t0, xg, U, hidden, cap);
   if (!rc) rc = mf_xmap(&t1, xu, U, hidden, cap);
   if (!rc) rc = mf_tmap(&tt, w13_trellis, (long)e_cnt * 2 * (hidden / 16), inter, K, 8);
@@ -560,7 +597,10 @@ int exl3_launch_moe_fused_gateup(const uint16_t *xg, const uint16_t *xu, int U, 
   a.partials = partials;
   a.counters = counters;
   const int grid = max_mtiles * a.NT * splits;
-  return cap == 32 ? mf_launch<1, 32>(K, t0, t1, tt, a, grid, s) : mf_launch<1, 128>(K, t0, t1, tt, a, grid, s);
+  if (cap == 32) return mf_launch<1, 32>(K, t0, t1, tt, a, grid, s);
+  if (cap == 128) return mf_launch<1, 128>(K, t0, t1, tt, a, grid, s);
+  if (splits > 1) return exl3_fail(EXL3_ERR_ARG, "no k split with 256-row tiles");
+  return mf_launch<1, 256>(K, t0, t1, tt, a, grid, s);
 }
 
 // Phase 2: h' [U][inter] fp16 sorted rows; w2 trellis [E][1][inter/16][hidden/16][16K]; d [U][hidden] fp32.
@@ -569,7 +609,7 @@ int exl3_launch_moe_fused_down(const uint16_t *hin, int U, int hidden, int inter
                                const uint16_t *w2_trellis, const int *mtiles, const int *n_mtiles, int max_mtiles,
                                int cap, const uint16_t *svh2, const float *weights, const int *perm, float *dout,
                                int *err, cudaStream_t s, int e_lo, int e_cnt) {
-  if (cap != 32 && cap != 128) return exl3_fail(EXL3_ERR_ARG, "tile capacity %d", cap);
+  if (cap != 32 && cap != 128 && cap != 256) return exl3_fail(EXL3_ERR_ARG, "tile capacity %d", cap);
   if (e_cnt < 0) {
     e_lo = 0;
     e_cnt = E;
@@ -605,5 +645,7 @@ int exl3_launch_moe_fused_down(const uint16_t *hin, int U, int hidden, int inter
   const int sms = exl3_sm_count();
   a.ntc = ((a.KB / 2) % 2 == 0 && (long)max_mtiles * (a.NT / 2) >= 2L * sms) ? 2 : 1;
   const int grid = max_mtiles * ((a.NT + a.ntc - 1) / a.ntc);
-  return cap == 32 ? mf_launch<2, 32>(K, t0, t0, tt, a, grid, s) : mf_launch<2, 128>(K, t0, t0, tt, a, grid, s);
+  if (cap == 32) return mf_launch<2, 32>(K, t0, t0, tt, a, grid, s);
+  if (cap == 128) return mf_launch<2, 128>(K, t0, t0, tt, a, grid, s);
+  return mf_launch<2, 256>(K, t0, t0, tt, a, grid, s);
 }
