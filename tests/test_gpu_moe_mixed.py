@@ -4,7 +4,10 @@ native engine (tracker) #832": widths 1..8 per tensor, and the Oct 17 comment
 keeps each expert's own width in the format).
 
 Each projection's arena packs expert e right after expert e-1 at its own
-width; every run of consecutive equal widths is one grouped launch.  Outputs
+width.  With more than 32 routed rows every run of consecutive equal widths
+is one grouped tile launch; with at most 32 (and at most 8 runs), each
+projection is one grouped-GEMV launch over all its runs, whose CTAs split
+over the widths present.  Outputs
 must meet the tolerance of tests/gpu_util.py against the float64 oracle;
 with one width for all experts the call must give the bits of
 exl3_moe_grouped's tile path.
@@ -102,3 +105,63 @@ def test_moe_mixed_invalid_expert_id_is_reported_and_skipped():
     ref_w = c.weights.copy()
     ref_w[3, 0] = 0.0
     assert_close(host(y).astype(np.float64), _oracle(c, ids=ref_ids, weights=ref_w), "mixed invalid id")
+
+
+@pytest.mark.parametrize("T", [1, 4])
+def test_moe_mixed_few_tokens_grouped_gemv(T):
+    """At most 32 routed rows take the few-token path: per projection one
+    grouped M = 1 GEMV launch whose CTAs split over the widths of the routed
+    experts (found on the device).  The MoE workload's shape with two widths
+    per projection; deterministic, with the arrival counters back at zero."""
+    K13 = [3] * 128 + [4] * 128
+    K2 = [4] * 128 + [3] * 128
+    c = synth.mixed_moe_case(61, T, T, K13, K2)
+    d = _dev_mixed(c)
+    ws = torch.zeros(tq.exl3_moe_mixed_workspace_size(c.T, c.topk, c.E, d["w13"], d["w2"]), dtype=torch.uint8,
+                     device="cuda")
+    y1 = tq.exl3_moe_grouped_mixed(d["x"], d["ids"], d["w"], d["w13"], d["w2"], c.E, workspace_buf=ws,
+                                   out_dtype=tq.EXL3_OUT_F32).clone()
+    y2 = tq.exl3_moe_grouped_mixed(d["x"], d["ids"], d["w"], d["w13"], d["w2"], c.E, workspace_buf=ws,
+                                   out_dtype=tq.EXL3_OUT_F32).clone()
+    assert torch.equal(y1, y2)
+    assert tq.exl3_check_device_error(ws) == 0
+    assert np.all(host(ws[256:256 + 4 * 8192]).view(np.int32) == 0)
+    assert_close(host(y1).astype(np.float64), _oracle(c), f"mixed few tokens T={T}")
+
+
+def test_moe_mixed_few_tokens_width_without_units():
+    """Every routed expert has width 3, so no CTA of either launch takes the
+    width-5 experts' runs; the launches must still run only the routed
+    width and leave the chain ordered."""
+    c = synth.mixed_moe_case(62, 0, 3, [3, 3, 3, 3, 5, 5, 5, 5], [3, 3, 3, 3, 5, 5, 5, 5], topk=2, hidden=512,
+                             inter=256)
+    c.ids[:] = np.array([[0, 1], [2, 3], [1, 2]], dtype=np.int32)
+    d = _dev_mixed(c)
+    y = tq.exl3_moe_grouped_mixed(d["x"], d["ids"], d["w"], d["w13"], d["w2"], c.E, out_dtype=tq.EXL3_OUT_F32)
+    assert_close(host(y).astype(np.float64), _oracle(c), "mixed width without units")
+
+
+def test_moe_mixed_few_tokens_all_ids_invalid():
+    """No valid expert id: no CTA has a share, every unit's combine row is
+    -1, the output is zero and the error word is set."""
+    c = synth.mixed_moe_case(63, 0, 2, [3, 4], [4, 3], topk=2, hidden=256, inter=128)
+    d = _dev_mixed(c)
+    bad = np.full_like(c.ids, 5)
+    ws = torch.zeros(tq.exl3_moe_mixed_workspace_size(c.T, c.topk, c.E, d["w13"], d["w2"]), dtype=torch.uint8,
+                     device="cuda")
+    y = tq.exl3_moe_grouped_mixed(d["x"], dev(bad), d["w"], d["w13"], d["w2"], c.E, workspace_buf=ws)
+    assert tq.exl3_check_device_error(ws) != 0
+    assert np.all(host(y) == 0)
+
+
+@pytest.mark.parametrize("E", [8, 10])
+def test_moe_mixed_few_tokens_alternating_widths(E):
+    """Widths alternating per expert: 8 experts give 8 runs per projection
+    (one launch holds their 8 tensor maps); 10 give 10 runs, more than one
+    launch holds, so the call takes the tile kernels."""
+    K13 = [3 if e % 2 == 0 else 4 for e in range(E)]
+    K2 = [4 if e % 2 == 0 else 2 for e in range(E)]
+    c = synth.mixed_moe_case(64, E, 4, K13, K2, topk=6, hidden=256, inter=256)
+    d = _dev_mixed(c)
+    y = tq.exl3_moe_grouped_mixed(d["x"], d["ids"], d["w"], d["w13"], d["w2"], E, out_dtype=tq.EXL3_OUT_F32)
+    assert_close(host(y).astype(np.float64), _oracle(c), f"mixed alternating widths E={E}")

@@ -62,6 +62,13 @@ cudaError_t exl3_launch_moe_gemv(const uint16_t *x, const float *act_in, int *po
                                  const float *weights, int U, int topk, int E, int nslots, int k, int n, int K,
                                  const uint16_t *trellis, const uint16_t *suh, const uint16_t *svh, float *y,
                                  float *partials, int *counters, int *err, cudaStream_t s);
+bool exl3_moe_gemv_widths_plan(int U, int nslots, int k, int n, int runs, const int *K, int *grid,
+                               size_t *partial_floats, int *counters_needed);
+cudaError_t exl3_launch_moe_gemv_widths(const uint16_t *x, const float *act_in, int *pos_out, const int32_t *ids,
+                                        const float *weights, int U, int topk, int E, int nslots, int k, int n,
+                                        int runs, const int *K, const int *e_lo, const int *cnt, const size_t *words,
+                                        const uint16_t *trellis, const uint16_t *suh, const uint16_t *svh, float *y,
+                                        float *partials, int *counters, int *err, cudaStream_t s, bool prefetch);
 int exl3_launch_moe_fused_gateup(const uint16_t *xg, const uint16_t *xu, int U, int hidden, int inter, int K, int E,
                                  const uint16_t *w13_trellis, const int *mtiles, const int *n_mtiles, int max_mtiles,
                                  int cap, const uint16_t *svh13, const uint16_t *suh2, uint16_t *hout, int splits,
@@ -268,8 +275,23 @@ struct MoeWs {
 // launch per projection, no sort) runs instead of the tensor-core tiles.
 constexpr int kMoeGemvMaxU = 32;
 
+// Few routed rows (grouped M = 1 GEMVs): gate and up outputs [U][2][inter]
+// fp32, d [U][hidden] fp32, pos [U] and the GEMVs' split-k partials.
+MoeWs moe_gemv_layout(size_t U, int hidden, int inter, size_t partial_floats) {
+  MoeWs w{};
+  w.gemv = true;
+  size_t off = kDataOff;
+  auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes); return o; };
+  w.y13 = take(sizeof(float) * U * 2 * inter);
+  w.d = take(sizeof(float) * U * hidden);
+  w.pos = take(sizeof(int) * U);
+  w.partials = take(sizeof(float) * partial_floats);
+  w.total = off;
+  return w;
+}
+
 // allow_gemv = false keeps every token count on the tile kernels (the
-// mixed-width call, whose runs of equal width each need their own launch).
+// mixed-width call, which plans its few-token path itself).
 MoeWs moe_ws(int T, int topk, int E, int hidden, int inter, int K13, int K2, bool allow_gemv = true) {
   MoeWs w{};
   const size_t U = (size_t)T * topk;
@@ -279,15 +301,7 @@ MoeWs moe_ws(int T, int topk, int E, int hidden, int inter, int K13, int K2, boo
     if (U <= (size_t)kMoeGemvMaxU && exl3_moe_gemv_plan((int)U, 2, hidden, inter, K13, &g1, &p1, &b1) &&
         exl3_moe_gemv_plan((int)U, 1, inter, hidden, K2, &g2, &p2, &b2) && (size_t)b1 <= kMaxCounters &&
         (size_t)b2 <= kMaxCounters) {
-      w.gemv = true;
-      size_t off = kDataOff;
-      auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes); return o; };
-      w.y13 = take(sizeof(float) * U * 2 * inter);
-      w.d = take(sizeof(float) * U * hidden);
-      w.pos = take(sizeof(int) * U);
-      w.partials = take(sizeof(float) * (p1 > p2 ? p1 : p2));
-      w.total = off;
-      return w;
+      return moe_gemv_layout(U, hidden, inter, p1 > p2 ? p1 : p2);
     }
   }
   // Tiles of 32 rows (the grouped kernels then run MMAs 16 or 32 rows wide,
@@ -383,6 +397,31 @@ std::vector<WidthRun> width_runs(const exl3_expert_proj_mixed *p, int E) {
     off += per_bit * (size_t)p->K[e];
   }
   return runs;
+}
+
+// Few routed rows of experts with mixed widths: one grouped-GEMV launch per
+// projection over all its runs of equal width (at most 8 of them).  False
+// when the path does not apply; *partial_floats: the larger launch's
+// split-k partials.
+bool mixed_gemv_plan(size_t U, int E, int hidden, int inter, const exl3_expert_proj_mixed *w13,
+                     const exl3_expert_proj_mixed *w2, size_t *partial_floats) {
+  if (U > (size_t)kMoeGemvMaxU) return false;
+  size_t pmax = 0;
+  for (int proj = 0; proj < 2; ++proj) {
+    const std::vector<WidthRun> runs = width_runs(proj == 0 ? w13 : w2, E);
+    if (runs.size() > 8) return false;
+    int K[8];
+    for (size_t r = 0; r < runs.size(); ++r) K[r] = runs[r].K;
+    int grid = 0, counters = 0;
+    size_t pf = 0;
+    if (!exl3_moe_gemv_widths_plan((int)U, proj == 0 ? 2 : 1, proj == 0 ? hidden : inter,
+                                   proj == 0 ? inter : hidden, (int)runs.size(), K, &grid, &pf, &counters) ||
+        (size_t)counters > kMaxCounters)
+      return false;
+    pmax = pf > pmax ? pf : pmax;
+  }
+  *partial_floats = pmax;
+  return true;
 }
 
 int check_workspace(const void *ws, size_t have, size_t need) {
@@ -685,10 +724,22 @@ static int max_width(const exl3_expert_proj_mixed *p, int E) {
   return m;
 }
 
+// The mixed-width call's workspace: the few-token grouped GEMVs, or the
+// tile kernels.
+MoeWs moe_mixed_ws(int T, int topk, int E, int hidden, int inter, const exl3_expert_proj_mixed *w13,
+                   const exl3_expert_proj_mixed *w2) {
+  const size_t U = (size_t)T * topk;
+  size_t pf = 0;
+  if (mixed_gemv_plan(U, E, hidden, inter, w13, w2, &pf)) return moe_gemv_layout(U, hidden, inter, pf);
+  return moe_ws(T, topk, E, hidden, inter, max_width(w13, E), max_width(w2, E), false);
+}
+
 size_t exl3_moe_mixed_workspace_size(int T, int topk, int E, const exl3_expert_proj_mixed *w13,
                                      const exl3_expert_proj_mixed *w2) {
   if (!w13 || !w2 || !w13->K || !w2->K || T < 1 || topk < 1 || E < 1 || E > 1024) return 0;
-  return moe_ws(T, topk, E, w13->k, w13->n, max_width(w13, E), max_width(w2, E), false).total;
+  for (int e = 0; e < E; ++e)
+    if (w13->K[e] < 1 || w13->K[e] > 8 || w2->K[e] < 1 || w2->K[e] > 8) return 0;
+  return moe_mixed_ws(T, topk, E, w13->k, w13->n, w13, w2).total;
 }
 
 int exl3_moe_grouped_mixed(const uint16_t *x, int T, int hidden, const int32_t *topk_ids,
@@ -711,9 +762,43 @@ int exl3_moe_grouped_mixed(const uint16_t *x, int T, int hidden, const int32_t *
   if (out_dtype != EXL3_OUT_F16 && out_dtype != EXL3_OUT_F32)
     return exl3_fail(EXL3_ERR_ARG, "out_dtype %d invalid", out_dtype);
   const int U = T * topk;
-  const MoeWs L = moe_ws(T, topk, E, hidden, inter, max_width(w13, E), max_width(w2, E), false);
+  const MoeWs L = moe_mixed_ws(T, topk, E, hidden, inter, w13, w2);
   EXL3_TRY(check_workspace(workspace, ws_bytes, L.total));
   int *err = at<int>(workspace, 0);
+  if (L.gemv) {
+    // few routed rows: per projection, one grouped-GEMV launch over all its
+    // runs of equal width, which finds on the device the units of each
+    // width and splits its CTAs over the widths.  Gate and up write
+    // [U][2][inter] fp32, down reads SiLU(gate) up of them and writes d
+    // times the routing weight; the down launch streams its weights while
+    // gate and up finish.
+    float *y13 = at<float>(workspace, L.y13), *d = at<float>(workspace, L.d);
+    int *pos = at<int>(workspace, L.pos);
+    float *partials = at<float>(workspace, L.partials);
+    int *counters = at<int>(workspace, kCounterOff);
+    for (int proj = 0; proj < 2; ++proj) {
+      const std::vector<WidthRun> runs = width_runs(proj == 0 ? w13 : w2, E);
+      int K[8], lo[8], cnt[8];
+      size_t words[8];
+      const int nr = (int)runs.size();
+      for (int r = 0; r < nr; ++r) {
+        K[r] = runs[r].K;
+        lo[r] = runs[r].e_lo;
+        cnt[r] = runs[r].cnt;
+        words[r] = runs[r].words;
+      }
+      cudaError_t e =
+          proj == 0 ? exl3_launch_moe_gemv_widths(x, nullptr, nullptr, topk_ids, nullptr, U, topk, E, 2, hidden,
+                                                  inter, nr, K, lo, cnt, words, w13->trellis, w13->suh, w13->svh, y13,
+                                                  partials, counters, err, stream, false)
+                    : exl3_launch_moe_gemv_widths(nullptr, y13, pos, topk_ids, topk_weights, U, topk, E, 1, inter,
+                                                  hidden, nr, K, lo, cnt, words, w2->trellis, w2->suh, w2->svh, d,
+                                                  partials, counters, err, stream, true);
+      EXL3_TRY(exl3_cuda_check(e, proj == 0 ? "moe gate/up gemv launch" : "moe down gemv launch"));
+    }
+    return exl3_cuda_check(exl3_launch_moe_combine(d, pos, T, topk, hidden, y, out_dtype == EXL3_OUT_F32, stream),
+                           "moe combine launch");
+  }
   int *counts = at<int>(workspace, L.counts), *offsets = at<int>(workspace, L.offsets);
   int *pos = at<int>(workspace, L.pos), *perm = at<int>(workspace, L.perm);
   int *mtiles = at<int>(workspace, L.mtiles), *chunk_tab = at<int>(workspace, L.chunk);

@@ -43,6 +43,8 @@
 // depend on timing.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+
 #include "exl3_common.cuh"
 #include "gemv_core.cuh"
 #include "tc_ptx.cuh"
@@ -86,6 +88,31 @@ struct GemvArgs {
   // tensor map s.
   int var;
   int vn[8], vo[8], vb[9];
+  // Routed experts of mixed widths (GROUPED, runs > 0, at most 32 units):
+  // this launch serves the experts of runs [run_lo[r], run_hi[r]) of one
+  // width (tensor map r, over run r's part of the packed arena from expert
+  // run_lo[r]).  The units whose expert lies in one of them are the active
+  // ones: compacted in unit order (op o = active unit o / nslots, slot
+  // o % nslots) and counted on the device, so that the rows split evenly
+  // over the CTAs whatever the routing; `total` is then found on the device.
+  int runs, units;
+  int run_lo[8], run_hi[8], run_K[8];
+  // per width K (index 1..8) of a launch over runs of several widths: column
+  // blocks, ring stages, and the width's first arrival counter and partial
+  // slot in the launch's arrays
+  int wcolblocks[9], wstages[9], wcounter_base[9], wpartial_base[9];
+};
+
+// One CTA's share of a launch: its index and the number of CTAs sharing the
+// rows, the rows (total, op_rows per op, column blocks per op), the active
+// units (mixed widths), the ring depth, and the arrival counters and
+// partial slots of its column blocks.
+struct GemvPart {
+  int me, grid;
+  uint32_t total, op_rows, active;
+  int colblocks, stages;
+  int *counters;
+  float *partials;
 };
 
 constexpr int kGemvMaxOps = 4;        // ops one CTA's range may touch in GROUPED mode
@@ -101,17 +128,44 @@ struct GemvOp {
   int trow;                 // first trellis row of the op's weights
   bool bad;                 // invalid expert id
   int map;                  // tensor map of the op's trellis
+  int unit;                 // routed unit (GROUPED)
 };
 
+// Mixed widths: whether expert e belongs to one of the launch's runs, and
+// which (-1: none).
+__device__ __forceinline__ int gemv_run_of(const GemvArgs &a, int e) {
+  int r = -1;
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    if (i < a.runs && e >= a.run_lo[i] && e < a.run_hi[i]) r = i;
+  return r;
+}
+
+// The combine's row of each unit (-1 for an invalid expert id), when the
+// launch has pos_out; threads tid of nthreads.
+__device__ __forceinline__ void gemv_write_pos(const GemvArgs &a, int tid, int nthreads) {
+  if (!a.pos_out) return;
+  for (int u = tid; u < a.nops / a.nslots; u += nthreads) {
+    const int e = a.ids[u];
+    a.pos_out[u] = (e >= 0 && e < a.E) ? u : -1;
+  }
+}
+
 template <bool GROUPED, bool F32OUT>
-__device__ __forceinline__ GemvOp gemv_op(const GemvArgs &a, int o) {
+__device__ __forceinline__ GemvOp gemv_op(const GemvArgs &a, int o, uint32_t active = 0) {
   if constexpr (!GROUPED) {
-    return GemvOp{a.x, a.suh, a.svh, a.y, 1.0f, 0, false, 0};
+    return GemvOp{a.x, a.suh, a.svh, a.y, 1.0f, 0, false, 0, 0};
   } else {
     if (a.var)   // shard o of different widths: its own map, column offset vo[o]
       return GemvOp{a.x, a.suh + (long)o * a.k, a.svh + a.vo[o],
-                    static_cast<char *>(a.y) + (long)a.vo[o] * (F32OUT ? 4 : 2), 1.0f, 0, false, o};
-    const int u = o / a.nslots, slot = o - u * a.nslots;
+                    static_cast<char *>(a.y) + (long)a.vo[o] * (F32OUT ? 4 : 2), 1.0f, 0, false, o, 0};
+    int u = o / a.nslots;
+    const int slot = o - u * a.nslots;
+    if (a.runs) {   // the u-th active unit
+      uint32_t m = active;
+      for (int i = 0; i < u; ++i) m &= m - 1;
+      u = __ffs(m) - 1;
+    }
     int e = a.ids ? a.ids[u] : 0;   // no id list: every unit uses expert 0 (fused shards)
     const bool bad = e < 0 || e >= a.E;
     float scale = a.weights ? a.weights[u] : 1.0f;
@@ -121,32 +175,40 @@ __device__ __forceinline__ GemvOp gemv_op(const GemvArgs &a, int o) {
     }
     const long es = (long)e * a.nslots + slot;
     const long xr = a.x_per_unit ? u : u / a.topk;
+    int map = 0;
+    long trow = es * a.tiles_k;
+    if (a.runs) {   // the expert's run: its own map, experts counted from the run's first
+      map = gemv_run_of(a, e);
+      trow = ((long)(e - a.run_lo[map]) * a.nslots + slot) * a.tiles_k;
+    }
     return GemvOp{a.x + xr * a.k, a.suh + es * a.k, a.svh + es * a.n,
-                  static_cast<char *>(a.y) + (long)o * a.n * (F32OUT ? 4 : 2), scale, (int)(es * a.tiles_k), bad, 0};
+                  static_cast<char *>(a.y) + (long)(u * a.nslots + slot) * a.n * (F32OUT ? 4 : 2), scale,
+                  (int)trow, bad, map, u};
   }
 }
 
 // GROUPED mode: the op of global column block c, c's index inside that op,
 // and the op's width.
-__device__ __forceinline__ int op_of_block(const GemvArgs &a, int c) {
-  if (!a.var) return c / a.colblocks;
+__device__ __forceinline__ int op_of_block(const GemvArgs &a, const GemvPart &p, int c) {
+  if (!a.var) return c / p.colblocks;
   int o = 0;
 #pragma unroll
   for (int s = 1; s < kGemvMaxShards; ++s)
     if (s < a.var && c >= a.vb[s]) o = s;
   return o;
 }
-__device__ __forceinline__ int block_in_op(const GemvArgs &a, int c, int op) {
-  return a.var ? c - a.vb[op] : c - op * a.colblocks;
+__device__ __forceinline__ int block_in_op(const GemvArgs &a, const GemvPart &p, int c, int op) {
+  return a.var ? c - a.vb[op] : c - op * p.colblocks;
 }
 __device__ __forceinline__ int op_width(const GemvArgs &a, int op) { return a.var ? a.vn[op] : a.n; }
 
 // Whether all `others` CTAs sharing column block c besides its first have
 // published their partials (one acquire load, no waiting).
-__device__ __forceinline__ bool gemv_all_arrived(const GemvArgs &a, int c, int others, int lane) {
+__device__ __forceinline__ bool gemv_all_arrived(const GemvArgs &a, const GemvPart &p, int c, int others,
+                                                 int lane) {
   int got = 0;
   if (lane == 0) {
-    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(got) : "l"(a.counters + c) : "memory");
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(got) : "l"(p.counters + c) : "memory");
     if (got > others) set_device_error(a.err, kErrDirtyCounter);
   }
   got = __shfl_sync(0xffffffffu, got, 0);
@@ -157,7 +219,7 @@ __device__ __forceinline__ bool gemv_all_arrived(const GemvArgs &a, int c, int o
 // pre[j] = the partial of CTA i0 + 1 + j of column block c, for j below
 // min(cnt, kGemvPrePartials) (lane l: columns 128 g + 4 l .. +3).
 template <int NG>
-__device__ __forceinline__ void gemv_load_partials(const GemvArgs &a, int c, int i0, int cnt, int lane,
+__device__ __forceinline__ void gemv_load_partials(const GemvPart &p, int c, int i0, int cnt, int lane,
                                                    float (&pre)[kGemvPrePartials][NG][4]) {
 #pragma unroll
   for (int j = 0; j < kGemvPrePartials; ++j)
@@ -165,7 +227,7 @@ __device__ __forceinline__ void gemv_load_partials(const GemvArgs &a, int c, int
     for (int g = 0; g < NG; ++g) {
       float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
       if (j < cnt)
-        r = __ldcg(reinterpret_cast<const float4 *>(a.partials + (long)(c + i0 + 1 + j) * (NG * 128) + g * 128 +
+        r = __ldcg(reinterpret_cast<const float4 *>(p.partials + (long)(c + i0 + 1 + j) * (NG * 128) + g * 128 +
                                                     lane * 4));
       pre[j][g][0] = r.x;
       pre[j][g][1] = r.y;
@@ -176,10 +238,10 @@ __device__ __forceinline__ void gemv_load_partials(const GemvArgs &a, int c, int
 
 // p = the partial of CTA i of column block c.
 template <int NG>
-__device__ __forceinline__ void gemv_load_partial(const GemvArgs &a, int c, int i, int lane, float (&p)[NG][4]) {
+__device__ __forceinline__ void gemv_load_partial(const GemvPart &pt, int c, int i, int lane, float (&p)[NG][4]) {
 #pragma unroll
   for (int g = 0; g < NG; ++g) {
-    const float4 r = __ldcg(reinterpret_cast<const float4 *>(a.partials + (long)(c + i) * (NG * 128) + g * 128 +
+    const float4 r = __ldcg(reinterpret_cast<const float4 *>(pt.partials + (long)(c + i) * (NG * 128) + g * 128 +
                                                              lane * 4));
     p[g][0] = r.x;
     p[g][1] = r.y;
@@ -190,9 +252,9 @@ __device__ __forceinline__ void gemv_load_partial(const GemvArgs &a, int c, int 
 
 // v += the partial of CTA i of column block c.
 template <int NG>
-__device__ __forceinline__ void gemv_add_partial(const GemvArgs &a, int c, int i, int lane, float (&v)[NG][4]) {
+__device__ __forceinline__ void gemv_add_partial(const GemvPart &pt, int c, int i, int lane, float (&v)[NG][4]) {
   float p[NG][4];
-  gemv_load_partial<NG>(a, c, i, lane, p);
+  gemv_load_partial<NG>(pt, c, i, lane, p);
 #pragma unroll
   for (int g = 0; g < NG; ++g)
 #pragma unroll
@@ -215,11 +277,11 @@ __device__ __forceinline__ void gemv_load_out_vectors(const __half *svh, const _
 // The kernel body; maps holds the trellis tensor map (one per shard for
 // shards of different widths).
 template <int K, bool F32OUT, bool GROUPED>
-__device__ __forceinline__ void gemv_body(const CUtensorMap *maps, const GemvArgs &a) {
+__device__ __forceinline__ void gemv_body(const CUtensorMap *maps, const GemvArgs &a, const GemvPart &p) {
   using S = GemvShape<K>;
   constexpr int NCW = S::NCW, NCT = NCW * 32;
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  const int STAGES = a.stages;
+  const int STAGES = p.stages;
   uint8_t *ring = smem_raw;                                            // [STAGES][R][ROWB]
   float *red = reinterpret_cast<float *>(smem_raw + (size_t)STAGES * S::STAGE_B);   // [NCW][CTA_COLS]
   volatile int *s_abort = reinterpret_cast<volatile int *>(red + NCW * S::CTA_COLS);   // a wait ran out
@@ -233,7 +295,7 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap *maps, const GemvArg
   float *rsum = xs + NOPS * a.k;                                       // [NOPS][k/16] sum of x' per tile row
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int grid = gridDim.x, me = blockIdx.x;
+  const int me = p.me, grid = p.grid;
   const int TK = a.tiles_k;
   // the kernel launched after this one on the stream may start as soon as
   // every CTA has begun (it only streams weights until this grid completes)
@@ -241,8 +303,18 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap *maps, const GemvArg
   // Row arithmetic is 32-bit (the host keeps grid * total below 2^32): a
   // 64-bit division is a long software sequence on every path's start.
   const uint32_t TKU = (uint32_t)TK;
-  const uint32_t t0 = range_start(me, a.total, grid), t1 = range_start(me + 1, a.total, grid);
-  if (t0 >= t1) return;
+  const uint32_t total = p.total, active = p.active;
+  const uint32_t t0 = me < grid ? range_start(me, total, grid) : 0;
+  const uint32_t t1 = me < grid ? range_start(me + 1, total, grid) : 0;
+  if (t0 >= t1) {
+    // An empty share (mixed widths: fewer active rows than CTAs).  The
+    // launch must still complete only after the kernel before it, which the
+    // kernels after it rely on, so wait for it; the first CTA still writes
+    // the combine's row of every unit.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (GROUPED && me == 0) gemv_write_pos(a, tid, (S::NCW + 2) * 32);
+    return;
+  }
 
   if (tid == 0) {
     for (int st = 0; st < STAGES; ++st) {
@@ -267,9 +339,9 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap *maps, const GemvArg
         const uint32_t c = t / TKU;   // block: op c / colblocks, column block c % colblocks
         const uint32_t seg_end = min(t1, (c + 1) * TKU);
         const int tk_first = (int)(t - c * TKU), nrows = (int)(seg_end - t);
-        const int op = GROUPED ? op_of_block(a, (int)c) : 0;
-        const int tn0 = (GROUPED ? block_in_op(a, (int)c, op) : (int)c) * (S::CTA_COLS / 16);
-        const GemvOp Pp = gemv_op<GROUPED, F32OUT>(a, op);
+        const int op = GROUPED ? op_of_block(a, p, (int)c) : 0;
+        const int tn0 = (GROUPED ? block_in_op(a, p, (int)c, op) : (int)c) * (S::CTA_COLS / 16);
+        const GemvOp Pp = gemv_op<GROUPED, F32OUT>(a, op, active);
         const int trow = Pp.trow + tk_first;
         const CUtensorMap *tmT = maps + Pp.map;
         for (int r0 = 0; r0 < nrows && !*s_abort; r0 += S::R) {
@@ -331,17 +403,17 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap *maps, const GemvArg
     // over while they go on decoding the next one.  Lane l holds columns
     // 128 g + 4 l .. +3 of every 128-column group g.
     uint32_t sp = 0;
-    const int op0 = GROUPED ? op_of_block(a, (int)(t0 / TKU)) : 0;
+    const int op0 = GROUPED ? op_of_block(a, p, (int)(t0 / TKU)) : 0;
     for (uint32_t t = t0; t < t1;) {
       const int c = (int)(t / TKU);   // block: op c / colblocks, column block c % colblocks
       const uint32_t seg_end = min(t1, (uint32_t)(c + 1) * TKU);
-      const int op = GROUPED ? op_of_block(a, c) : 0;
-      const GemvOp P = gemv_op<GROUPED, F32OUT>(a, op);
+      const int op = GROUPED ? op_of_block(a, p, c) : 0;
+      const GemvOp P = gemv_op<GROUPED, F32OUT>(a, op, active);
       const int nop = GROUPED ? op_width(a, op) : a.n;
       const float *rs = rsum + (op - op0) * (a.k / 16);
-      const int col0 = (GROUPED ? block_in_op(a, c, op) : c) * S::CTA_COLS;
-      const uint32_t blk_first = (uint32_t)c * TKU, blk_last = min((uint32_t)(c + 1) * TKU, a.total) - 1;
-      const int i_first = range_owner(blk_first, a.total, grid), i_last = range_owner(blk_last, a.total, grid);
+      const int col0 = (GROUPED ? block_in_op(a, p, c, op) : c) * S::CTA_COLS;
+      const uint32_t blk_first = (uint32_t)c * TKU, blk_last = min((uint32_t)(c + 1) * TKU, total) - 1;
+      const int i_first = range_owner(blk_first, total, grid), i_last = range_owner(blk_last, total, grid);
       // A block shared by several CTAs is finished by whichever of them
       // publishes its partial sum last: each stores its partial in the slot
       // of (block, CTA) and makes one acquire-release increment of the
@@ -358,8 +430,8 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap *maps, const GemvArg
       float pre[kGemvPrePartials][S::NG][4];
       bool all_in = false;
       if (first) {
-        all_in = gemv_all_arrived(a, c, others, lane);
-        if (all_in) gemv_load_partials<S::NG>(a, c, i_first, others, lane, pre);
+        all_in = gemv_all_arrived(a, p, c, others, lane);
+        if (all_in) gemv_load_partials<S::NG>(p, c, i_first, others, lane, pre);
       }
       uint2 svv[S::NG];   // the block's svh (and bias), loaded ahead where this CTA usually finishes
       uint2 bvv[S::NG];
@@ -399,8 +471,8 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap *maps, const GemvArg
       bool finish = true;
       if (shared) {
         if (first && !all_in) {   // a second look, now that the own segment is done
-          all_in = gemv_all_arrived(a, c, others, lane);
-          if (all_in) gemv_load_partials<S::NG>(a, c, i_first, others, lane, pre);
+          all_in = gemv_all_arrived(a, p, c, others, lane);
+          if (all_in) gemv_load_partials<S::NG>(p, c, i_first, others, lane, pre);
         }
         if (first && all_in) {
           // every other CTA is in: add their partials in CTA order
@@ -411,18 +483,18 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap *maps, const GemvArg
               for (int g = 0; g < S::NG; ++g)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) v[g][e] += pre[j][g][e];
-          for (int i = i_first + 1 + kGemvPrePartials; i <= i_last; ++i) gemv_add_partial<S::NG>(a, c, i, lane, v);
+          for (int i = i_first + 1 + kGemvPrePartials; i <= i_last; ++i) gemv_add_partial<S::NG>(p, c, i, lane, v);
         } else {
           // publish this CTA's partial and arrive; the last to arrive finishes
 #pragma unroll
           for (int g = 0; g < S::NG; ++g)
-            __stcg(reinterpret_cast<float4 *>(a.partials + (long)(c + me) * S::CTA_COLS + g * 128 + lane * 4),
+            __stcg(reinterpret_cast<float4 *>(p.partials + (long)(c + me) * S::CTA_COLS + g * 128 + lane * 4),
                    make_float4(v[g][0], v[g][1], v[g][2], v[g][3]));
           __threadfence();
           __syncwarp();
           int old = 0;
           if (lane == 0)
-            asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(a.counters + c) : "memory");
+            asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(p.counters + c) : "memory");
           old = __shfl_sync(0xffffffffu, old, 0);
           if (old > others && lane == 0) set_device_error(a.err, kErrDirtyCounter);
           finish = old >= others;
@@ -434,24 +506,24 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap *maps, const GemvArg
 #pragma unroll
               for (int e = 0; e < 4; ++e) own[g][e] = v[g][e];
             for (int i = i_first; i <= i_last; ++i) {   // CTA order: p[i_first] + p[i_first + 1] + ...
-              float p[S::NG][4];
+              float pq[S::NG][4];
               if (i == me) {
 #pragma unroll
                 for (int g = 0; g < S::NG; ++g)
 #pragma unroll
-                  for (int e = 0; e < 4; ++e) p[g][e] = own[g][e];
+                  for (int e = 0; e < 4; ++e) pq[g][e] = own[g][e];
               } else {
-                gemv_load_partial<S::NG>(a, c, i, lane, p);
+                gemv_load_partial<S::NG>(p, c, i, lane, pq);
               }
 #pragma unroll
               for (int g = 0; g < S::NG; ++g)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) v[g][e] = i == i_first ? p[g][e] : v[g][e] + p[g][e];
+                for (int e = 0; e < 4; ++e) v[g][e] = i == i_first ? pq[g][e] : v[g][e] + pq[g][e];
             }
             if (!first) gemv_load_out_vectors<S::NG>(P.svh, has_bias ? a.bias : nullptr, col0, nop, lane, true, svv, bvv);
           }
         }
-        if (finish && lane == 0) a.counters[c] = 0;   // leave the workspace clean
+        if (finish && lane == 0) p.counters[c] = 0;   // leave the workspace clean
       }
       if (finish) {
         // ---- output transform of the block's 128-column groups
@@ -497,18 +569,13 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap *maps, const GemvArg
   // prologue: x' = 2^-3.5 H (x . suh) for the 512-element chunks (32 tile
   // rows) this range touches; a warp transforms four 128-blocks at once,
   // eight lanes per block and 16 contiguous elements per lane
-  const int op0 = GROUPED ? op_of_block(a, (int)(t0 / TKU)) : 0;
-  if (GROUPED && a.pos_out && me == 0) {   // the combine's row of each unit
-    for (int u = tid; u < a.nops / a.nslots; u += NCT) {
-      const int e = a.ids[u];
-      a.pos_out[u] = (e >= 0 && e < a.E) ? u : -1;
-    }
-  }
+  const int op0 = GROUPED ? op_of_block(a, p, (int)(t0 / TKU)) : 0;
+  if (GROUPED && me == 0) gemv_write_pos(a, tid, NCT);
   {
     const int KC = (a.k + 511) >> 9;
     int c0 = 0, nc = KC;
     if (GROUPED) {          // every chunk of each op the range touches (ops op0 ..)
-      nc = (op_of_block(a, (int)((t1 - 1) / TKU)) - op0 + 1) * KC;
+      nc = (op_of_block(a, p, (int)((t1 - 1) / TKU)) - op0 + 1) * KC;
     } else if (t1 - t0 < TK) {   // fewer rows than one block: at most two column blocks
       c0 = (int)(t0 % TKU) >> 5;
       const int c1 = (int)((t1 - 1) % TKU) >> 5;
@@ -517,7 +584,7 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap *maps, const GemvArg
     }
     for (int i = warp; i < nc; i += NCW) {
       const int jop = GROUPED ? i / KC : 0;               // op op0 + jop
-      const GemvOp P = gemv_op<GROUPED, F32OUT>(a, op0 + jop);
+      const GemvOp P = gemv_op<GROUPED, F32OUT>(a, op0 + jop, active);
       if (GROUPED && P.bad && lane == 0 && i % KC == 0) set_device_error(a.err, kErrExpertId);
       const int e0 = ((c0 + i - jop * KC) % KC) * 512 + lane * 16;
       const bool live = e0 < a.k;   // k is a multiple of 128: whole 8-lane groups
@@ -526,7 +593,7 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap *maps, const GemvArg
       float v[16];
       if (live && GROUPED && a.act_in) {
         // h = SiLU(g) u of this unit (fp32, the gate and up outputs), times suh
-        const int u = (op0 + jop) / a.nslots;
+        const int u = P.unit;
         const float *g = a.act_in + (long)(2 * u) * a.k + e0, *up = g + a.k;
         uint4 sv[2];
         sv[0] = *reinterpret_cast<const uint4 *>(P.suh + e0);
@@ -591,7 +658,7 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap *maps, const GemvArg
     const int c = (int)(t / TKU);
     const uint32_t seg_end = min(t1, (uint32_t)(c + 1) * TKU);
     const int tk_first = (int)(t - (uint32_t)c * TKU), nrows = (int)(seg_end - t);
-    const float *xso = xs + (GROUPED ? op_of_block(a, c) - op0 : 0) * a.k;   // this op's x' 2^100
+    const float *xso = xs + (GROUPED ? op_of_block(a, p, c) - op0 : 0) * a.k;   // this op's x' 2^100
 
     float acc[16];
 #pragma unroll
@@ -664,10 +731,16 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap *maps, const GemvArg
   }
 }
 
+// The partition of a launch over one width: every CTA of the grid.
+__device__ __forceinline__ GemvPart gemv_whole_grid(const GemvArgs &a) {
+  return GemvPart{(int)blockIdx.x, (int)gridDim.x, a.total, a.op_rows, 0u, a.colblocks, a.stages, a.counters,
+                  a.partials};
+}
+
 template <int K, bool F32OUT, bool GROUPED>
 __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
     gemv_m1_kernel(const __grid_constant__ CUtensorMap tmT, GemvArgs a) {
-  gemv_body<K, F32OUT, GROUPED>(&tmT, a);
+  gemv_body<K, F32OUT, GROUPED>(&tmT, a, gemv_whole_grid(a));
 }
 
 // Shards of different widths: one trellis map per shard.
@@ -678,7 +751,79 @@ struct GemvShardMaps {
 template <int K, bool F32OUT>
 __global__ void __launch_bounds__(GemvShape<K>::THREADS, 1)
     gemv_shards_kernel(const __grid_constant__ GemvShardMaps maps, GemvArgs a) {
-  gemv_body<K, F32OUT, true>(maps.m, a);
+  gemv_body<K, F32OUT, true>(maps.m, a, gemv_whole_grid(a));
+}
+
+constexpr int kGemvThreads = GemvShape<4>::THREADS;   // the same for every width
+static_assert(GemvShape<1>::THREADS == kGemvThreads && GemvShape<3>::THREADS == kGemvThreads &&
+                  GemvShape<8>::THREADS == kGemvThreads,
+              "one block size for every width");
+
+// Routed experts of mixed widths for a few tokens, one launch per
+// projection: the runs (at most 8, their tensor maps in `maps`) have widths
+// run_K[r].  Every CTA finds the active units of each width (lane u of a
+// warp holds unit u), splits the grid over the widths in proportion to
+// their rows (at least one CTA each, and no more CTAs than rows), and runs
+// the decode of its width on its share; the widths' column blocks have their
+// own arrival counters and partial slots.
+template <bool F32OUT>
+__global__ void __launch_bounds__(kGemvThreads, 1)
+    gemv_widths_kernel(const __grid_constant__ GemvShardMaps maps, GemvArgs a) {
+  const int lane = threadIdx.x & 31, me = blockIdx.x;
+  int ku = 0;   // width of unit `lane`'s expert (0: no run of this launch)
+  if (lane < a.units) {
+    const int e = a.ids[lane];
+    const int r = gemv_run_of(a, e);
+    if (r >= 0) ku = a.run_K[r];
+    if (me == 0 && threadIdx.x < 32 && (e < 0 || e >= a.E)) set_device_error(a.err, kErrExpertId);
+  }
+  uint32_t rows[9], mask[9], all = 0;
+  int nw = 0;
+#pragma unroll
+  for (int w = 1; w <= 8; ++w) {
+    mask[w] = __ballot_sync(0xffffffffu, ku == w);
+    rows[w] = (uint32_t)__popc(mask[w]) * (uint32_t)a.nslots * (uint32_t)a.wcolblocks[w] * (uint32_t)a.tiles_k;
+    all += rows[w];
+    nw += rows[w] > 0;
+  }
+  const int G = gridDim.x;
+  int wsel = 0, first = 0, cnt = 0;
+  for (int w = 1, start = 0; w <= 8; ++w) {   // width w takes CTAs [start, start + c)
+    if (rows[w] == 0) continue;
+    const int c = 1 + (int)((unsigned long long)(G - nw) * rows[w] / all);
+    if (me >= start && me < start + c) {
+      wsel = w;
+      first = start;
+      cnt = c;
+    }
+    start += c;
+  }
+  if (wsel == 0) {   // no share: still complete after the kernel before this one
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (me == 0) gemv_write_pos(a, threadIdx.x, kGemvThreads);
+    return;
+  }
+  GemvPart p;
+  p.me = me - first;
+  p.grid = (uint32_t)cnt < rows[wsel] ? cnt : (int)rows[wsel];   // every CTA taking part owns a row
+  p.total = rows[wsel];
+  p.active = mask[wsel];
+  p.colblocks = a.wcolblocks[wsel];
+  p.op_rows = (uint32_t)p.colblocks * (uint32_t)a.tiles_k;
+  p.stages = a.wstages[wsel];
+  p.counters = a.counters + a.wcounter_base[wsel];
+  p.partials = a.partials + a.wpartial_base[wsel];
+  switch (wsel) {
+    case 1: gemv_body<1, F32OUT, true>(maps.m, a, p); break;
+    case 2: gemv_body<2, F32OUT, true>(maps.m, a, p); break;
+    case 3: gemv_body<3, F32OUT, true>(maps.m, a, p); break;
+    case 4: gemv_body<4, F32OUT, true>(maps.m, a, p); break;
+    case 5: gemv_body<5, F32OUT, true>(maps.m, a, p); break;
+    case 6: gemv_body<6, F32OUT, true>(maps.m, a, p); break;
+    case 7: gemv_body<7, F32OUT, true>(maps.m, a, p); break;
+    default: gemv_body<8, F32OUT, true>(maps.m, a, p); break;
+  }
 }
 
 static int gemv_sm_count() { return exl3_sm_count(); }
@@ -786,7 +931,7 @@ cudaError_t exl3_launch_gemv_m1_bias(const uint16_t *x, const uint16_t *trellis,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
-  GemvArgs a;
+  GemvArgs a{};
   a.x = reinterpret_cast<const __half *>(x);
   a.suh = reinterpret_cast<const __half *>(suh);
   a.svh = reinterpret_cast<const __half *>(svh);
@@ -882,7 +1027,7 @@ cudaError_t exl3_launch_moe_gemv(const uint16_t *x, const float *act_in, int *po
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
-  GemvArgs a;
+  GemvArgs a{};
   a.x = reinterpret_cast<const __half *>(x);
   a.suh = reinterpret_cast<const __half *>(suh);
   a.svh = reinterpret_cast<const __half *>(svh);
@@ -921,6 +1066,136 @@ cudaError_t exl3_launch_moe_gemv(const uint16_t *x, const float *act_in, int *po
   return e;
 }
 
+// ---- routed experts of mixed widths for a few tokens: every routed unit
+// whose expert lies in one of `runs` runs (run r: experts e_lo[r] ..
+// e_lo[r] + cnt[r] - 1 of width K[r], their nslots tensors packed from
+// trellis + words[r]) as grouped M = 1 GEMVs, all widths in one launch.
+// Arguments otherwise as exl3_launch_moe_gemv (y [U * nslots][n] fp32).
+// partial_floats / counters_needed (optional): the sizes it uses.
+bool exl3_moe_gemv_widths_plan(int U, int nslots, int k, int n, int runs, const int *K, int *grid,
+                               size_t *partial_floats, int *counters_needed) {
+  if (runs < 1 || runs > kGemvMaxShards || U < 1 || U > 32) return false;
+  const long long g = gemv_sm_count();
+  bool seen[9] = {};
+  int nw = 0;
+  long long max_rows = 0;
+  for (int r = 0; r < runs; ++r) {
+    if (K[r] < 1 || K[r] > 8) return false;
+    if (!seen[K[r]]) ++nw;
+    seen[K[r]] = true;
+  }
+  if (g <= nw) return false;
+  size_t pf = 0;
+  int cnt = 0;
+  for (int w = 1; w <= 8; ++w) {
+    if (!seen[w]) continue;
+    const int cc = exl3_gemv_cta_cols(w);
+    const long long colblocks = (n + cc - 1) / cc, op_rows = colblocks * (k / 16);
+    const long long rows = (long long)U * nslots * op_rows;
+    max_rows += rows;
+    int st = 0;
+    EXL3_K_SWITCH(w, st = Launcher<KK, true, true>::stages(k));
+    if (st < 2) return false;
+    pf += (size_t)(U * nslots * colblocks + g) * (size_t)cc;
+    cnt += (int)(U * nslots * colblocks);
+  }
+  // a CTA's share is at most about max_rows / (g - nw) rows: it must touch
+  // no more than kGemvMaxOps ops of any width
+  for (int w = 1; w <= 8; ++w) {
+    if (!seen[w]) continue;
+    const int cc = exl3_gemv_cta_cols(w);
+    const long long op_rows = ((n + cc - 1) / cc) * (k / 16);
+    const long long range = (max_rows + (g - nw) - 1) / (g - nw) + 1;
+    if ((range + op_rows - 1) / op_rows + 1 > kGemvMaxOps) return false;
+    if ((unsigned long long)max_rows * (unsigned long long)g >= (1ull << 32)) return false;
+  }
+  *grid = (int)g;
+  if (partial_floats) *partial_floats = pf;
+  if (counters_needed) *counters_needed = cnt;
+  return true;
+}
+
+cudaError_t exl3_launch_moe_gemv_widths(const uint16_t *x, const float *act_in, int *pos_out, const int32_t *ids,
+                                        const float *weights, int U, int topk, int E, int nslots, int k, int n,
+                                        int runs, const int *K, const int *e_lo, const int *cnt, const size_t *words,
+                                        const uint16_t *trellis, const uint16_t *suh, const uint16_t *svh, float *y,
+                                        float *partials, int *counters, int *err, cudaStream_t s, bool prefetch) {
+  auto fn = gemv_tmap_fn();
+  if (!fn) return cudaErrorNotSupported;
+  int grid = 0;
+  if (!exl3_moe_gemv_widths_plan(U, nslots, k, n, runs, K, &grid, nullptr, nullptr)) return cudaErrorInvalidValue;
+  GemvShardMaps maps;
+  memset(&maps, 0, sizeof maps);
+  GemvArgs a{};
+  for (int r = 0; r < runs; ++r) {   // run r's experts' trellis as u64 rows: row (e' nslots + slot) k/16 + tk
+    const int cc = exl3_gemv_cta_cols(K[r]);
+    cuuint64_t dims[3] = {(cuuint64_t)4 * K[r], (cuuint64_t)(n / 16), (cuuint64_t)cnt[r] * nslots * (k / 16)};
+    cuuint64_t strides[2] = {(cuuint64_t)32 * K[r], (cuuint64_t)(n / 16) * 32 * K[r]};
+    cuuint32_t box[3] = {(cuuint32_t)(4 * K[r]), (cuuint32_t)(cc / 16), (cuuint32_t)kGemvBoxRows};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult rr = fn(&maps.m[r], CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<uint16_t *>(trellis) + words[r], dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (rr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    a.run_lo[r] = e_lo[r];
+    a.run_hi[r] = e_lo[r] + cnt[r];
+    a.run_K[r] = K[r];
+  }
+  // per width: column blocks, ring stages, and the first counter and
+  // partial slot of its blocks; the shared memory is the largest width's
+  size_t sm = 0;
+  int cbase = 0;
+  size_t pbase = 0;
+  bool seen[9] = {};
+  for (int r = 0; r < runs; ++r) seen[K[r]] = true;
+  for (int w = 1; w <= 8; ++w) {
+    if (!seen[w]) continue;
+    const int cc = exl3_gemv_cta_cols(w);
+    a.wcolblocks[w] = (n + cc - 1) / cc;
+    EXL3_K_SWITCH(w, a.wstages[w] = Launcher<KK, true, true>::stages(k);
+                  sm = std::max(sm, Launcher<KK, true, true>::smem(k, a.wstages[w])));
+    a.wcounter_base[w] = cbase;
+    a.wpartial_base[w] = (int)pbase;
+    cbase += U * nslots * a.wcolblocks[w];
+    pbase += (size_t)(U * nslots * a.wcolblocks[w] + grid) * (size_t)cc;
+  }
+  a.runs = runs;
+  a.units = U;
+  a.x = reinterpret_cast<const __half *>(x);
+  a.suh = reinterpret_cast<const __half *>(suh);
+  a.svh = reinterpret_cast<const __half *>(svh);
+  a.y = y;
+  a.partials = partials;
+  a.counters = counters;
+  a.err = err;
+  a.k = k;
+  a.n = n;
+  a.tiles_k = k / 16;
+  a.ids = ids;
+  a.weights = weights;
+  a.topk = topk;
+  a.nslots = nslots;
+  a.E = E;
+  a.act_in = act_in;
+  a.pos_out = pos_out;
+  a.pre_stages = kGemvPreStages;
+  a.nops = U * nslots;
+  cudaLaunchAttribute attrs[1];
+  attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kGemvThreads);
+  cfg.dynamicSmemBytes = sm;
+  cfg.stream = s;
+  cfg.attrs = prefetch ? attrs : nullptr;
+  cfg.numAttrs = prefetch ? 1 : 0;
+  static std::atomic<size_t> attr[kMaxDevices];
+  cudaError_t e = exl3_ensure_smem(reinterpret_cast<const void *>(gemv_widths_kernel<true>), sm, attr);
+  if (e != cudaSuccess) return e;
+  return cudaLaunchKernelEx(&cfg, gemv_widths_kernel<true>, maps, a);
+}
+
 // ---- fused shards: S linears of one input row, [S][k/16][n/16][16K]
 // trellis, suh [S][k], svh [S][n], y [S][n], in one launch of the grouped
 // GEMV (one unit, S slots, no expert ids).  False when a CTA's range would
@@ -950,7 +1225,7 @@ cudaError_t exl3_launch_gemv_shards(const uint16_t *x, int S, int k, int n, int 
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
-  GemvArgs a;
+  GemvArgs a{};
   a.x = reinterpret_cast<const __half *>(x);
   a.suh = reinterpret_cast<const __half *>(suh);
   a.svh = reinterpret_cast<const __half *>(svh);
@@ -1034,7 +1309,7 @@ cudaError_t exl3_launch_gemv_shards_var(const uint16_t *x, int S, int k, const i
   const int cc = exl3_gemv_cta_cols(K);
   GemvShardMaps maps;
   memset(&maps, 0, sizeof maps);
-  GemvArgs a;
+  GemvArgs a{};
   memset(&a, 0, sizeof a);
   size_t words = 0;
   int vo = 0, vb = 0;
