@@ -9,8 +9,11 @@ another's weights from L2.
 
 Extra objects on the same JSON line: `roofline` (the GEMV kernel against the
 measured HBM copy bandwidth), `cpu_baseline` (the CPU oracle on a bounded
-sample), `e2e` (the same metric through the C ABI with host buffers: x copied
-in and y copied out each step), `prefill` (M = 4096 TFLOP/s), and `clocks`.
+sample), `e2e` (the same metric through the C ABI with host buffers: each
+step copies x in from pinned host memory with exl3_copy_in and the linears
+write y straight into pinned host memory; copy-engine transfers beside it),
+`prefill` (M = 4096 TFLOP/s), `configs` (every decode and small-M shape),
+`other` (MoE, fused shards, row-invariant mode) and `clocks`.
 
     python bench.py [--gpus 1] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -73,7 +76,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # at k=5120 n=25600, with the hash of the kernel's sources at capture time; a
 # changed kernel source makes the recorded traffic stale (reported as null).
 TRAFFIC = {"files": ["trellis_quantized_gb300/csrc/gemv.cu", "trellis_quantized_gb300/csrc/gemv_core.cuh"],
-           "sha1": "bb3a15e36287a2ed3ce23e691e19c42da8558144", "bytes_per_launch": 65666560,
+           "sha1": "06c2c8c690957bb1d4fd2ce90dfa3835c525d33b", "bytes_per_launch": 65668864,
            "workload": "k5120 n25600 K4 M1"}
 
 
@@ -291,80 +294,107 @@ def run_ours(args):
                           "kernel_us_plain_launches: the same without overlap between launches"}
 
     # e2e: the step's inputs (the three linears' x, packed in one pinned host
-    # buffer) go host -> device in one copy, the linears run through the C ABI
-    # on views of the device copy, and their outputs (packed) come back to
-    # pinned host memory in one copy; both copies are inside the timed region
+    # buffer) go host -> device through exl3_copy_in (SM loads over
+    # NVLink-C2C, chained to the linears by programmatic dependent launch),
+    # the linears run through the C ABI on views of the device copy and write
+    # their y straight into one pinned host buffer; the transfers both ways
+    # are inside the timed region.  The same step with copy-engine transfers
+    # (one packed copy each way) is measured beside it.
     kx = [d["case"].k for d in dcases]
     ny = [d["case"].n for d in dcases]
-    hx = torch.from_numpy(np.concatenate([d["case"].x.reshape(-1) for d in dcases])).pin_memory()
+    hx = torch.from_numpy(np.concatenate([d["case"].x.reshape(-1) for d in dcases]).view(np.int16)).pin_memory()
     hy = torch.empty(sum(ny), dtype=torch.float16).pin_memory()
     dx = torch.empty(hx.shape, dtype=hx.dtype, device="cuda")
     dy = torch.empty(sum(ny), dtype=torch.float16, device="cuda")
-    xo = np.cumsum([0] + kx)
-    yo = np.cumsum([0] + ny)
+    xo = np.cumsum([0] + kx) * 2
+    yo = np.cumsum([0] + ny) * 2
+    hx_bytes = hx.numel() * hx.element_size()
+    hy_bytes = hy.numel() * hy.element_size()
 
-    def launch_e2e(j, copy):
+    def launch_e2e(j, copy, yp):
         d, c = dcases[j], dcases[j]["case"]
-        rc = L.exl3_linear(dx[int(xo[j]):].data_ptr(), 1, c.k, c.n, d["t"][copy].data_ptr(), d["suh"].data_ptr(),
-                           d["svh"].data_ptr(), c.K, tq.EXL3_CB_MUL1, dy[int(yo[j]):].data_ptr(), tq.EXL3_OUT_F16,
+        rc = L.exl3_linear(dx.data_ptr() + int(xo[j]), 1, c.k, c.n, d["t"][copy].data_ptr(), d["suh"].data_ptr(),
+                           d["svh"].data_ptr(), c.K, tq.EXL3_CB_MUL1, yp + int(yo[j]), tq.EXL3_OUT_F16,
                            d["ws"].data_ptr(), d["ws"].numel(), torch.cuda.current_stream().cuda_stream)
         if rc:
             raise tq.Exl3Error(rc, L.exl3_last_error().decode())
 
     def e2e_step(i):
+        rc = L.exl3_copy_in(hx.data_ptr(), dx.data_ptr(), hx_bytes, torch.cuda.current_stream().cuda_stream)
+        if rc:
+            raise tq.Exl3Error(rc, L.exl3_last_error().decode())
+        for j in range(len(dcases)):
+            launch_e2e(j, i % copies, hy.data_ptr())
+
+    def e2e_step_ce(i):
         dx.copy_(hx, non_blocking=True)
         for j in range(len(dcases)):
-            launch_e2e(j, i % copies)
+            launch_e2e(j, i % copies, dy.data_ptr())
         hy.copy_(dy, non_blocking=True)
 
     e2e_steps = max(10, args.steps // 4)
     e2e_steps -= e2e_steps % chunk
     stream = torch.cuda.current_stream()
-    for i in range(3):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    # eager: one C-ABI call per linear from Python each step
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(e2e_steps):
-        e2e_step(i)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    eager_ms = e0.elapsed_time(e1) / e2e_steps
-    # as a decode loop runs it: the same calls and copies captured in CUDA
-    # graphs (`chunk` steps per graph, one graph per starting weight copy)
-    egraphs = []
-    for cp in range(copies):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for jj in range(chunk):
-                e2e_step(cp + jj)
-        egraphs.append(g)
-    for g in egraphs:
-        g.replay()
-    torch.cuda.synchronize()
-    e0.record(stream)
-    done = 0
-    while done < e2e_steps:
-        egraphs[(done // chunk) % copies].replay()
-        done += chunk
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    ref_y = [dcases[j]["y"] for j in range(len(dcases))]
-    for j in range(len(dcases)):   # the packed path computes what the per-linear path did
-        assert torch.equal(dy[int(yo[j]):int(yo[j + 1])].view(1, -1), ref_y[j]), "e2e output differs"
-        assert torch.equal(hy[int(yo[j]):int(yo[j + 1])].view(1, -1), ref_y[j].cpu()), "e2e host copy differs"
-    hy_bytes = hy.numel() * hy.element_size()
-    e2e = {"value": round(step_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
-           "h2d_bytes_per_step": int(hx.numel() * hx.element_size()),
+    ref_y = [dcases[j]["y"].cpu() for j in range(len(dcases))]
+
+    def check_hy(what):
+        for j in range(len(dcases)):   # the packed path computes what the per-linear path did
+            got = hy[int(yo[j]) // 2:int(yo[j + 1]) // 2].view(1, -1)
+            assert torch.equal(got, ref_y[j]), f"e2e ({what}) output differs"
+
+    def timed_e2e(fn):
+        hy.zero_()
+        for i in range(3):
+            fn(i)
+        torch.cuda.synchronize()
+        check_hy("eager")
+        # eager: one C-ABI call per copy and linear from Python each step
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(e2e_steps):
+            fn(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        eager_ms = e0.elapsed_time(e1) / e2e_steps
+        # as a decode loop runs it: the same calls and copies captured in CUDA
+        # graphs (`chunk` steps per graph, one graph per starting weight copy)
+        egraphs = []
+        for cp in range(copies):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for jj in range(chunk):
+                    fn(cp + jj)
+            egraphs.append(g)
+        hy.zero_()
+        for g in egraphs:
+            g.replay()
+        torch.cuda.synchronize()
+        check_hy("graph")
+        e0.record(stream)
+        done = 0
+        while done < e2e_steps:
+            egraphs[(done // chunk) % copies].replay()
+            done += chunk
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / e2e_steps, eager_ms
+
+    e2e_ms, eager_ms = timed_e2e(e2e_step)
+    ce_ms, ce_eager_ms = timed_e2e(e2e_step_ce)
+    gbs = lambda ms: round(step_bytes / (ms * 1e-3) / 1e9, 1)
+    e2e = {"value": gbs(e2e_ms), "unit": "GB/s",
+           "h2d_bytes_per_step": int(hx_bytes),
            "d2h_bytes_per_step": int(hy_bytes),
            "ms_per_step": round(e2e_ms, 5),
-           "eager": {"value": round(step_bytes / (eager_ms * 1e-3) / 1e9, 1), "ms_per_step": round(eager_ms, 5)},
-           "timing": "per step: one packed host->device copy of the step's x (pinned), the three linears "
-                     "through the C ABI, one packed device->host copy of their y (pinned), all inside the timed "
-                     "region, in stream order; captured in CUDA graphs of 10 steps as a decode loop runs them "
-                     "(eager: the same calls issued from Python every step)"}
+           "eager": {"value": gbs(eager_ms), "ms_per_step": round(eager_ms, 5)},
+           "copy_engine": {"value": gbs(ce_ms), "ms_per_step": round(ce_ms, 5),
+                           "eager": {"value": gbs(ce_eager_ms), "ms_per_step": round(ce_eager_ms, 5)}},
+           "timing": "per step: the step's x (pinned host, packed) copied to the device by exl3_copy_in "
+                     "(SM loads over NVLink-C2C, a programmatic dependent launch), the three linears through "
+                     "the C ABI writing their y straight into pinned host memory; all inside the timed region, "
+                     "in stream order; captured in CUDA graphs of 10 steps as a decode loop runs them "
+                     "(eager: the same calls issued from Python every step; copy_engine: one packed "
+                     "cudaMemcpyAsync each way instead)"}
 
     prefill = bench_prefill(args, bf16, src) if not args.skip_prefill else None
     extras = bench_extras() if not args.skip_prefill else None
@@ -771,6 +801,42 @@ def bench_pipes(iters=20000):
             "method": "one 1024-thread CTA per SM, 8 independent chains per thread, clock64 cycles (median CTA)"}
 
 
+# ---------------------------------------------------------- single calls
+
+def one_linear(M, n, calls=5):
+    """exl3_linear on the dense decode family (k = 5120, K = 4, config-2
+    inputs at M rows and n columns), `calls` times: the case a profiler
+    captures one launch of (no timing)."""
+    import torch
+    import trellis_quantized_gb300 as tq
+    c = synth.linear_case(2, 900 + M, M, 5120, n, 4)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16
+                                     else np.ascontiguousarray(a)).cuda()
+    x, t, suh, svh = dev(c.x), dev(c.trellis), dev(c.suh), dev(c.svh)
+    for _ in range(calls):
+        y = tq.exl3_linear(x, t, suh, svh, 4)
+    torch.cuda.synchronize()
+    return {"case": f"k5120 n{n} K4 M{M}", "calls": calls, "y_shape": list(y.shape)}
+
+
+def one_moe(T, calls=3):
+    """exl3_moe_grouped on the MoE workload (256 experts, top-8, hidden
+    2048, inter 512, K = 3) at T tokens, `calls` times (no timing)."""
+    import torch
+    import trellis_quantized_gb300 as tq
+    c = synth.config5(T) if T in synth.CONFIG5_T else synth.moe_case(5, 10 + T, T)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16
+                                     else np.ascontiguousarray(a)).cuda()
+    d = {k: dev(v) for k, v in dict(x=c.x, ids=c.ids, w=c.weights, t13=c.w13.trellis, s13=c.w13.suh,
+                                     v13=c.w13.svh, t2=c.w2.trellis, s2=c.w2.suh, v2=c.w2.svh).items()}
+    w13 = tq.expert_proj(d["t13"], d["s13"], d["v13"], c.K)
+    w2 = tq.expert_proj(d["t2"], d["s2"], d["v2"], c.K)
+    for _ in range(calls):
+        y = tq.exl3_moe_grouped(d["x"], d["ids"], d["w"], w13, w2, c.E)
+    torch.cuda.synchronize()
+    return {"case": f"E256 top8 h2048 i512 K3 T{T}", "calls": calls, "y_shape": list(y.shape)}
+
+
 # ---------------------------------------------------------------- dense peaks
 
 def bench_peaks():
@@ -886,9 +952,13 @@ def main():
     ap.add_argument("--skip-prefill", action="store_true")
     ap.add_argument("--no-prefetch", action="store_true",
                     help="launch the step's linears plainly (no weight prefetch across launches)")
-    ap.add_argument("--only", choices=["small", "moe", "prefill", "pipes", "peaks", "configs"], default=None,
+    ap.add_argument("--only", choices=["small", "moe", "prefill", "pipes", "peaks", "configs", "linear", "moecall"],
+                    default=None,
                     help="run one extra section alone and print its JSON (for profiling)")
     ap.add_argument("--configs", nargs="*", default=["1", "2", "3"], help="workloads of --only configs")
+    ap.add_argument("--m", type=int, default=16, help="rows of --only linear")
+    ap.add_argument("--n", type=int, default=17408, help="columns of --only linear")
+    ap.add_argument("--t", type=int, default=128, help="tokens of --only moecall")
     ap.add_argument("--moe-tokens", type=int, nargs="*", default=None,
                     help="token counts of the MoE section (default: all of the MoE workload's)")
     args = ap.parse_args()
@@ -902,6 +972,10 @@ def main():
             print(json.dumps(bench_peaks()))
         elif args.only == "configs":
             print(json.dumps(bench_configs(tuple(args.configs))))
+        elif args.only == "linear":
+            print(json.dumps(one_linear(args.m, args.n)))
+        elif args.only == "moecall":
+            print(json.dumps(one_moe(args.t)))
         else:
             print(json.dumps(bench_extras(args.only, args.moe_tokens)))
         return

@@ -77,6 +77,25 @@ const char *exl3_last_error(void);
 /* Library version, major * 10000 + minor * 100 + patch. */
 int exl3_version(void);
 
+/*
+ * exl3_copy_in -- copy `bytes` from pinned host memory to device memory with
+ * a kernel on `stream` (no counterpart on the source pages; an addition of
+ * this library for decode loops that take their inputs from the host).
+ *   src   HOST memory the device can address: pinned (cudaHostAlloc,
+ *         cudaMallocHost, cudaHostRegister'ed or a pinned tensor), 16-byte
+ *         aligned.  dst: device memory, 16-byte aligned.  bytes: any size;
+ *         0 enqueues nothing.
+ *   The kernel reads src with 16-byte SM loads (over NVLink-C2C on GB300)
+ *   instead of a copy-engine transfer.  It is a programmatic dependent
+ *   launch: it reads src and writes dst only after the kernels ahead of it
+ *   on the stream have completed, and it lets the kernel after it launch at
+ *   once, so an M = 1 exl3_linear issued next with weight prefetch on
+ *   streams its weights while the copy runs.
+ *   Errors: EXL3_ERR_ARG for a NULL or misaligned pointer; a src the device
+ *   cannot address is a device fault, as for any bad pointer.
+ */
+int exl3_copy_in(const void *src, void *dst, size_t bytes, exl3_stream_t stream);
+
 /* Enqueue a zero fill of a workspace (cudaMemsetAsync; needed once before a
  * workspace is first used). */
 int exl3_workspace_clear(void *workspace, size_t ws_bytes, exl3_stream_t stream);
@@ -118,9 +137,16 @@ int exl3_input_rht(const uint16_t *x, int M, int k, const uint16_t *suh,
  *   suh [k], svh [n] fp16         K in 1..8, codebook = EXL3_CB_MUL1
  *   y        [M][n], fp16 (EXL3_OUT_F16) or fp32 (EXL3_OUT_F32)
  *   workspace of exl3_linear_workspace_size(M, k, n, K) bytes.
- *   M = 1 runs the fused CUDA-core GEMV (or, for a k whose x' does not fit
- *   in its shared memory, about k > 44000 at K = 7, the small-M tensor-core
- *   path); larger M runs the tensor-core paths.
+ *   M = 1 runs the fused CUDA-core GEMV (or, for a k whose fp32 x' does not
+ *   fit beside two stages of its ring, k > 23680 at K = 7 and k > 37248 at
+ *   K = 4, the small-M tensor-core path); larger M runs the tensor-core
+ *   paths.
+ *   At M = 1, y may instead be pinned HOST memory the device can address
+ *   (16-byte aligned): every M = 1 path writes y with plain stores, so the
+ *   result lands in host memory (over NVLink-C2C on GB300) when the call's
+ *   kernels complete, with no device-to-host copy.  x must stay in device
+ *   memory (every CTA of the GEMV reads all of it; exl3_copy_in brings it
+ *   over).
  */
 size_t exl3_linear_workspace_size(int M, int k, int n, int K);
 int exl3_linear(const uint16_t *x, int M, int k, int n,

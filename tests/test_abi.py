@@ -181,6 +181,17 @@ def test_input_rht_argument_errors():
     assert L.exl3_input_rht(FAKE, 1, 128, FAKE, FAKE, 3, None) == tq.EXL3_ERR_ARG
 
 
+def test_copy_in_argument_errors():
+    """NULL or misaligned pointers are rejected; zero bytes enqueue nothing."""
+    L = tq.lib()
+    assert L.exl3_copy_in(None, FAKE, 64, None) == tq.EXL3_ERR_ARG
+    assert "src" in _err(L)
+    assert L.exl3_copy_in(FAKE, None, 64, None) == tq.EXL3_ERR_ARG
+    assert L.exl3_copy_in(FAKE_MIS, FAKE, 64, None) == tq.EXL3_ERR_ARG
+    assert L.exl3_copy_in(FAKE, FAKE_MIS, 64, None) == tq.EXL3_ERR_ARG
+    assert L.exl3_copy_in(FAKE, FAKE, 0, None) == tq.EXL3_OK
+
+
 @pytest.mark.parametrize("M,k,n,K", [(1, 5120, 17408, 4), (4, 5120, 5120, 4), (4096, 5120, 17408, 4),
                                      (1, 128, 128, 1), (64, 4096, 4096, 7)])
 def test_workspace_sizes(M, k, n, K):

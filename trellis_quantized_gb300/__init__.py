@@ -76,6 +76,7 @@ def lib():
         L.exl3_last_error.restype = ctypes.c_char_p
         L.exl3_version.restype = I
         L.exl3_workspace_clear.argtypes = [P, Z, P]
+        L.exl3_copy_in.argtypes = [P, P, Z, P]
         L.exl3_check_device_error.argtypes = [P, Z, P, ctypes.POINTER(I)]
         L.exl3_decode_tile.argtypes = [P, I, I, I, I, I, I, I, I, P, L64, P]
         L.exl3_input_rht.argtypes = [P, I, I, P, P, I, P]
@@ -128,6 +129,19 @@ def _ptr(t, name: str, itemsize: int | None = None):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _ptr_pinned(t, name: str):
+    """A pinned host tensor's address (the device addresses pinned memory directly)."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    # (is_pinned asks the driver about the address; skipped while a CUDA
+    # graph is being captured)
+    if t.is_cuda or (not torch.cuda.is_current_stream_capturing() and not t.is_pinned()):
+        raise ValueError(f"{name} must be a pinned host tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
 def _stream(stream=None):
     s = stream if stream is not None else torch.cuda.current_stream()
     return ctypes.c_void_p(s.cuda_stream)
@@ -160,6 +174,16 @@ def exl3_version() -> int:
 
 def exl3_workspace_clear(ws: torch.Tensor, stream=None):
     _check(lib().exl3_workspace_clear(_ptr(ws, "workspace"), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def exl3_copy_in(src: torch.Tensor, dst: torch.Tensor, stream=None) -> torch.Tensor:
+    """Copy a pinned host tensor into a device tensor of the same byte size with
+    a kernel chained by programmatic dependent launch (see exl3_copy_in in exl3.h)."""
+    nbytes = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() != nbytes:
+        raise ValueError("src and dst must have the same size in bytes")
+    _check(lib().exl3_copy_in(_ptr_pinned(src, "src"), _ptr(dst, "dst"), nbytes, _stream(stream)))
+    return dst
 
 
 def exl3_check_device_error(ws: torch.Tensor, stream=None) -> int:
@@ -201,7 +225,8 @@ def exl3_linear_workspace_size(M: int, k: int, n: int, K: int) -> int:
 
 def exl3_linear(x, trellis, suh, svh, K: int, codebook: int = EXL3_CB_MUL1, out_dtype: int = EXL3_OUT_F16,
                 y=None, workspace_buf=None, stream=None) -> torch.Tensor:
-    """y = RHT_out(RHT_in(x . suh) @ W) . svh for x [M, k] fp16."""
+    """y = RHT_out(RHT_in(x . suh) @ W) . svh for x [M, k] fp16.  At M = 1, y may be
+    a pinned host tensor: the kernels write the result straight into it."""
     M, k = x.shape
     n = trellis.shape[1] * 16
     if y is None:
@@ -209,8 +234,9 @@ def exl3_linear(x, trellis, suh, svh, K: int, codebook: int = EXL3_CB_MUL1, out_
                         device=x.device)
     need = exl3_linear_workspace_size(M, k, n, K)
     ws = workspace_buf if workspace_buf is not None else workspace(need, x.device, stream)
+    yp = _ptr_pinned(y, "y") if (M == 1 and not y.is_cuda) else _ptr(y, "y")
     _check(lib().exl3_linear(_ptr(x, "x", 2), M, k, n, _ptr(trellis, "trellis", 2), _ptr(suh, "suh", 2),
-                             _ptr(svh, "svh", 2), K, codebook, _ptr(y, "y"), out_dtype, _ptr(ws, "workspace"),
+                             _ptr(svh, "svh", 2), K, codebook, yp, out_dtype, _ptr(ws, "workspace"),
                              ws.numel() * ws.element_size(), _stream(stream)))
     return y
 

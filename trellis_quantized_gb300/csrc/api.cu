@@ -28,6 +28,7 @@ cudaError_t exl3_launch_gemv_m1_bias(const uint16_t *x, const uint16_t *trellis,
                                      cudaStream_t s, bool prefetch);
 void exl3_gemv_plan(int k, int n, int K, int *grid, size_t *partial_floats);
 bool exl3_gemv_fits(int k, int n, int K);
+cudaError_t exl3_launch_copy_in(const void *src, void *dst, size_t bytes, cudaStream_t s, bool chained);
 int exl3_launch_gemm_tc(const uint16_t *xh, const uint16_t *wt, int M, int n, int k, const uint16_t *svh,
                         void *y, bool f32out, const float *row_scale, float pre, int *err, cudaStream_t s,
                         bool q8 = false, int32_t *acc_out = nullptr, const uint16_t *bias = nullptr);
@@ -266,7 +267,7 @@ LinearInt8Ws linear_int8_ws(int M, int k, int n) {
 struct MoeWs {
   size_t counts, offsets, pos, perm, mtiles, n_mtiles, chunk, xg, xu, h, d, partials, total;
   int max_mtiles, grid_mtiles, splits;
-  int cap;            // rows per expert tile: 32 when few rows per expert are routed, else 128
+  int cap;            // rows per expert tile: 32, 128 or 256 (chosen in moe_ws)
   bool gemv;          // few routed rows: grouped M = 1 GEMVs instead of the tile kernels
   size_t y13;         // gemv: gate/up outputs [U][2][inter] fp32 (d, pos, partials as above)
 };
@@ -451,6 +452,14 @@ int exl3_version(void) { return 200; }
 int exl3_set_weight_prefetch(int enable) { return g_weight_prefetch.exchange(enable ? 1 : 0); }
 
 int exl3_set_row_invariant(int enable) { return g_row_invariant.exchange(enable ? 1 : 0); }
+
+int exl3_copy_in(const void *src, void *dst, size_t bytes, exl3_stream_t stream) {
+  g_last_error.clear();
+  if (bytes == 0) return EXL3_OK;
+  EXL3_TRY(check_ptr(src, "src"));
+  EXL3_TRY(check_ptr(dst, "dst"));
+  return exl3_cuda_check(exl3_launch_copy_in(src, dst, bytes, stream, true), "copy_in launch");
+}
 
 int exl3_workspace_clear(void *workspace, size_t ws_bytes, exl3_stream_t stream) {
   g_last_error.clear();
