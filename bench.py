@@ -702,7 +702,9 @@ def bench_extras(only=None, moe_tokens=None):
                  v13=dev(c.w13.svh), t2=dev(c.w2.trellis), s2=dev(c.w2.suh), v2=dev(c.w2.svh))
         w13 = tq.expert_proj(d["t13"], d["s13"], d["v13"], c.K)
         w2 = tq.expert_proj(d["t2"], d["s2"], d["v2"], c.K)
-        nr = 16 if T <= 64 else (4 if T <= 128 else 1)
+        # between two calls with the same routing, more than 2x L2 of expert
+        # weights goes through (T <= 4: 32 draws of about 9.4 MB per token)
+        nr = 32 if T <= 4 else (16 if T <= 64 else (4 if T <= 128 else 1))
         routes = [(c.ids, c.weights)] + [synth.routing(synth.rng_for(5, 1000 + 10 * T + r), T, c.E, c.topk)
                                          for r in range(nr - 1)]
         rd = [(dev(i), dev(w)) for i, w in routes]
@@ -733,21 +735,29 @@ def bench_extras(only=None, moe_tokens=None):
         w2 = tq.expert_proj_mixed(d["t2"], d["s2"], d["v2"], K2, c.inter, c.hidden)
         ws = tq.workspace(tq.exl3_moe_mixed_workspace_size(T, c.topk, c.E, w13, w2))
         y = torch.empty((T, c.hidden), dtype=torch.float16, device="cuda")
-        ms = _timed(lambda: tq.exl3_moe_grouped_mixed(d["x"], d["ids"], d["w"], w13, w2, c.E, y=y,
-                                                      workspace_buf=ws), reps=3)
-        used = np.unique(c.ids)
+        nr = 32 if T <= 4 else (4 if T <= 128 else 1)   # routings rotated, as for one width
+        routes = [(c.ids, c.weights)] + [synth.routing(synth.rng_for(59, 1000 + 10 * T + r), T, c.E, c.topk)
+                                         for r in range(nr - 1)]
+        rd = [(dev(i), dev(w)) for i, w in routes]
+        calls = [lambda i=i, w=w: tq.exl3_moe_grouped_mixed(d["x"], i, w, w13, w2, c.E, y=y, workspace_buf=ws)
+                 for i, w in rd]
+        ms = _timed_rotating(calls, rounds=max(1, 6 // nr)) if nr > 1 else _timed(calls[0], reps=3)
+        assert tq.exl3_check_device_error(ws) == 0
         words13 = [2 * (c.hidden // 16) * (c.inter // 16) * 16 * K for K in K13]
         words2 = [(c.inter // 16) * (c.hidden // 16) * 16 * K for K in K2]
-        ubytes = 2 * sum(words13[e] + words2[e] for e in used)
-        mixed[f"T{T}"] = {"ms": round(ms, 4), "experts_hit": len(used),
-                          "unique_weight_GBs": round(ubytes / (ms * 1e-3) / 1e9, 1)}
+        ubytes = np.mean([2 * sum(words13[e] + words2[e] for e in np.unique(i)) for i, _ in routes])
+        used = np.mean([len(np.unique(i)) for i, _ in routes])
+        mixed[f"T{T}"] = {"ms": round(ms, 4), "experts_hit": round(float(used), 1),
+                          "unique_weight_GBs": round(ubytes / (ms * 1e-3) / 1e9, 1), "routings_rotated": nr}
         del d
     return {"shards_gate_up_k5120_n17408x2_M1": shards, "shards_var_M1": var,
             "row_invariant_k5120_n17408": inv, "moe_E256_top8_h2048_i512_K3": moe,
             "moe_mixed_E256_top8_h2048_i512_K3K4": mixed,
             "note": "MoE: device remap + gather/RHT + two grouped tcgen05 kernels decoding the experts' trellis "
-                    "on the fly + fixed-order combine; mixed widths: the tile kernels once per run of equal "
-                    "width (two runs here), for every token count"}
+                    "on the fly + fixed-order combine (expert tiles of 32/128/256 rows by routed rows per "
+                    "expert); up to 32 routed rows: one grouped M=1 GEMV launch per projection + combine. "
+                    "Mixed widths: the tile kernels once per run of equal width (two runs here); up to 32 "
+                    "routed rows one grouped GEMV launch per projection over all runs"}
 
 
 # ---------------------------------------------------------------- pipe ceilings
@@ -819,14 +829,27 @@ def one_linear(M, n, calls=5):
     return {"case": f"k5120 n{n} K4 M{M}", "calls": calls, "y_shape": list(y.shape)}
 
 
-def one_moe(T, calls=3):
+def one_moe(T, calls=3, mixed=False):
     """exl3_moe_grouped on the MoE workload (256 experts, top-8, hidden
-    2048, inter 512, K = 3) at T tokens, `calls` times (no timing)."""
+    2048, inter 512, K = 3) at T tokens, `calls` times (no timing); with
+    `mixed`, exl3_moe_grouped_mixed with experts 0-127 at K = 3 and 128-255 at
+    K = 4 for gate+up (down the other way round)."""
     import torch
     import trellis_quantized_gb300 as tq
-    c = synth.config5(T) if T in synth.CONFIG5_T else synth.moe_case(5, 10 + T, T)
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16
                                      else np.ascontiguousarray(a)).cuda()
+    if mixed:
+        K13, K2 = [3] * 128 + [4] * 128, [4] * 128 + [3] * 128
+        c = synth.mixed_moe_case(59, 10 + T, T, K13, K2)
+        d = {k: dev(v) for k, v in dict(x=c.x, ids=c.ids, w=c.weights, t13=c.w13.trellis, s13=c.w13.suh,
+                                         v13=c.w13.svh, t2=c.w2.trellis, s2=c.w2.suh, v2=c.w2.svh).items()}
+        w13 = tq.expert_proj_mixed(d["t13"], d["s13"], d["v13"], K13, c.hidden, c.inter)
+        w2 = tq.expert_proj_mixed(d["t2"], d["s2"], d["v2"], K2, c.inter, c.hidden)
+        for _ in range(calls):
+            y = tq.exl3_moe_grouped_mixed(d["x"], d["ids"], d["w"], w13, w2, c.E)
+        torch.cuda.synchronize()
+        return {"case": f"E256 top8 h2048 i512 K3/K4 T{T}", "calls": calls, "y_shape": list(y.shape)}
+    c = synth.config5(T) if T in synth.CONFIG5_T else synth.moe_case(5, 10 + T, T)
     d = {k: dev(v) for k, v in dict(x=c.x, ids=c.ids, w=c.weights, t13=c.w13.trellis, s13=c.w13.suh,
                                      v13=c.w13.svh, t2=c.w2.trellis, s2=c.w2.suh, v2=c.w2.svh).items()}
     w13 = tq.expert_proj(d["t13"], d["s13"], d["v13"], c.K)
@@ -959,6 +982,7 @@ def main():
     ap.add_argument("--m", type=int, default=16, help="rows of --only linear")
     ap.add_argument("--n", type=int, default=17408, help="columns of --only linear")
     ap.add_argument("--t", type=int, default=128, help="tokens of --only moecall")
+    ap.add_argument("--mixed", action="store_true", help="--only moecall with two expert widths")
     ap.add_argument("--moe-tokens", type=int, nargs="*", default=None,
                     help="token counts of the MoE section (default: all of the MoE workload's)")
     args = ap.parse_args()
@@ -975,7 +999,7 @@ def main():
         elif args.only == "linear":
             print(json.dumps(one_linear(args.m, args.n)))
         elif args.only == "moecall":
-            print(json.dumps(one_moe(args.t)))
+            print(json.dumps(one_moe(args.t, mixed=args.mixed)))
         else:
             print(json.dumps(bench_extras(args.only, args.moe_tokens)))
         return

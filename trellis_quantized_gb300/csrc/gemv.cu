@@ -777,20 +777,29 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     if (r >= 0) ku = a.run_K[r];
     if (me == 0 && threadIdx.x < 32 && (e < 0 || e >= a.E)) set_device_error(a.err, kErrExpertId);
   }
-  uint32_t rows[9], mask[9], all = 0;
+  // Rows of odd widths hold 256 columns, of even widths 128: the CTAs are
+  // split in proportion to each width's weights, so that every CTA decodes
+  // about as many weights whatever its width.
+  constexpr uint32_t cols_of[9] = {0,
+                                   GemvShape<1>::CTA_COLS, GemvShape<2>::CTA_COLS, GemvShape<3>::CTA_COLS,
+                                   GemvShape<4>::CTA_COLS, GemvShape<5>::CTA_COLS, GemvShape<6>::CTA_COLS,
+                                   GemvShape<7>::CTA_COLS, GemvShape<8>::CTA_COLS};
+  uint32_t rows[9], mask[9];
+  unsigned long long weights[9], all = 0;
   int nw = 0;
 #pragma unroll
   for (int w = 1; w <= 8; ++w) {
     mask[w] = __ballot_sync(0xffffffffu, ku == w);
     rows[w] = (uint32_t)__popc(mask[w]) * (uint32_t)a.nslots * (uint32_t)a.wcolblocks[w] * (uint32_t)a.tiles_k;
-    all += rows[w];
+    weights[w] = (unsigned long long)rows[w] * cols_of[w];
+    all += weights[w];
     nw += rows[w] > 0;
   }
   const int G = gridDim.x;
   int wsel = 0, first = 0, cnt = 0;
   for (int w = 1, start = 0; w <= 8; ++w) {   // width w takes CTAs [start, start + c)
     if (rows[w] == 0) continue;
-    const int c = 1 + (int)((unsigned long long)(G - nw) * rows[w] / all);
+    const int c = 1 + (int)((unsigned long long)(G - nw) * weights[w] / all);
     if (me >= start && me < start + c) {
       wsel = w;
       first = start;
@@ -1087,25 +1096,30 @@ bool exl3_moe_gemv_widths_plan(int U, int nslots, int k, int n, int runs, const 
   if (g <= nw) return false;
   size_t pf = 0;
   int cnt = 0;
+  long long max_weights = 0;   // of one width, had every unit that width
   for (int w = 1; w <= 8; ++w) {
     if (!seen[w]) continue;
     const int cc = exl3_gemv_cta_cols(w);
     const long long colblocks = (n + cc - 1) / cc, op_rows = colblocks * (k / 16);
     const long long rows = (long long)U * nslots * op_rows;
     max_rows += rows;
+    if (rows * cc > max_weights) max_weights = rows * cc;
     int st = 0;
     EXL3_K_SWITCH(w, st = Launcher<KK, true, true>::stages(k));
     if (st < 2) return false;
     pf += (size_t)(U * nslots * colblocks + g) * (size_t)cc;
     cnt += (int)(U * nslots * colblocks);
   }
-  // a CTA's share is at most about max_rows / (g - nw) rows: it must touch
-  // no more than kGemvMaxOps ops of any width
+  // The device splits the CTAs over the widths in proportion to their
+  // weights, so a CTA of width w gets at most about (all weights) / (cols(w)
+  // (g - nw)) rows; all weights are at most max_weights (units of one
+  // width's weights add up to at most what all U units would have at the
+  // width with the most).  The share must touch no more than kGemvMaxOps ops.
   for (int w = 1; w <= 8; ++w) {
     if (!seen[w]) continue;
     const int cc = exl3_gemv_cta_cols(w);
     const long long op_rows = ((n + cc - 1) / cc) * (k / 16);
-    const long long range = (max_rows + (g - nw) - 1) / (g - nw) + 1;
+    const long long range = (max_weights + (long long)cc * (g - nw) - 1) / ((long long)cc * (g - nw)) + 1;
     if ((range + op_rows - 1) / op_rows + 1 > kGemvMaxOps) return false;
     if ((unsigned long long)max_rows * (unsigned long long)g >= (1ull << 32)) return false;
   }
