@@ -80,8 +80,9 @@ struct Cfg {
   static constexpr int TS = TS_FIT > 8 ? 8 : TS_FIT;
   static constexpr int SMEM_BYTES = XS * X_STAGE + W_RING + TS * T_STAGE + 2048;
   static constexpr int ITEMS = 32 * ftc::Shape<K, 32>::LPT;  // items per (k step, projection)
-  // phase 2 may take two output tiles per CTA (one accumulator set each)
-  static constexpr int NTC = PHASE == 2 ? 2 : 1;
+  // phase 2 may take several output tiles per CTA (one accumulator set
+  // each): four with 32-row tiles, two otherwise (TMEM holds 512 columns)
+  static constexpr int NTC = PHASE == 2 ? (NMAX <= 32 ? 4 : 2) : 1;
   static constexpr uint32_t TMEM_COLS = NISS * NP * XROWS * NTC;
   // whether this width and tile capacity fit (256-row tiles leave room for
   // K <= 4 only); the host launches only configurations that do
@@ -109,7 +110,7 @@ struct Args {
   // blockIdx.x % splits of tile blockIdx.x / splits; the last CTA of a tile
   // to arrive adds the partial sums in split order
   int splits;
-  int ntc;                  // output tiles per CTA (phase 2: 1 or 2)
+  int ntc;                  // output tiles per CTA (phase 2: 1, 2 or 4, at most Cfg::NTC)
   float *partials;          // [tiles][splits][2][NMAX][128] fp32 (splits > 1 only with NMAX <= 128)
   int *counters;            // [tiles], zero between calls
   // experts [e_lo, e_hi) only: the trellis map covers just their arena
@@ -127,8 +128,8 @@ __global__ void __launch_bounds__(Roles<NMAX>::WARPS * 32, 1)
   constexpr int NP = C::NP, XS = C::XS, TS = C::TS, NPS = C::NPS, NISS = C::NISS, XROWS = C::XROWS;
   constexpr int kDec0 = Roles<NMAX>::DEC0, kXWarp = Roles<NMAX>::XWARP;
   const int tile = blockIdx.x / a.splits, split = blockIdx.x % a.splits;
-  // output tiles nt0 .. nt0 + nts - 1 (phase 2 may take two: their pairs
-  // follow one another, tile j's pair Pt being pair j * nptile + Pt)
+  // output tiles nt0 .. nt0 + nts - 1 (phase 2 may take several: their
+  // pairs follow one another, tile j's pair Pt being pair j * nptile + Pt)
   pdl_trigger();   // the chain's kernels are programmatic dependents of one another
   pdl_wait();      // the tile list and x' come from the kernels before
   const int ntc = PHASE == 2 ? a.ntc : 1, NTG = (a.NT + ntc - 1) / ntc;
@@ -282,10 +283,11 @@ __global__ void __launch_bounds__(Roles<NMAX>::WARPS * 32, 1)
     const int grp = dw / NDEC, dt = (dw % NDEC) * 32 + lane;
     // Epilogue operands, loaded now so that their latency hides behind the
     // decode: this lane's 4 columns of svh (gate, up) and suh (down), or of
-    // svh (down, both output tiles) and the routing weights of the warp's
-    // rows (lane q holds row dw + 16 q).
+    // svh (down, every output tile of the CTA) and the routing weights of
+    // the warp's rows (lane q holds row dw + 16 q).
     const int col0 = nt0 * BN;
     float ep_a[4], ep_b[4], ep_c[4], row_w = 0.f;
+    float ep_t[PHASE == 2 ? C::NTC : 1][4];
     {
       auto ld4 = [&](const __half *src, float (&o)[4]) {
         const uint2 r = __ldg(reinterpret_cast<const uint2 *>(src + col0 + 4 * lane));
@@ -300,8 +302,9 @@ __global__ void __launch_bounds__(Roles<NMAX>::WARPS * 32, 1)
         ld4(a.svh13 + ((long)e * 2 + 1) * a.inter, ep_b);
         ld4(a.suh2 + (long)e * a.inter, ep_c);
       } else {
-        ld4(a.svh2 + (long)e * a.hidden, ep_a);
-        if (nts > 1) ld4(a.svh2 + (long)e * a.hidden + BN, ep_b);
+#pragma unroll
+        for (int jt = 0; jt < (PHASE == 2 ? C::NTC : 1); ++jt)
+          if (jt < nts) ld4(a.svh2 + (long)e * a.hidden + jt * BN, ep_t[jt]);
         const int m = dw + NGRP * NDEC * lane;
         if (lane < XROWS / (NGRP * NDEC) && m < rows) row_w = a.weights[a.perm[row0 + m]];
       }
@@ -450,20 +453,22 @@ __global__ void __launch_bounds__(Roles<NMAX>::WARPS * 32, 1)
         } else {
           const float w = __shfl_sync(0xffffffffu, row_w, m / (NGRP * NDEC));
           float4 o;
-          o.x = v[0] * kRhtScale * ep_a[0] * w;
-          o.y = v[1] * kRhtScale * ep_a[1] * w;
-          o.z = v[2] * kRhtScale * ep_a[2] * w;
-          o.w = v[3] * kRhtScale * ep_a[3] * w;
+          o.x = v[0] * kRhtScale * ep_t[0][0] * w;
+          o.y = v[1] * kRhtScale * ep_t[0][1] * w;
+          o.z = v[2] * kRhtScale * ep_t[0][2] * w;
+          o.w = v[3] * kRhtScale * ep_t[0][3] * w;
           *reinterpret_cast<float4 *>(a.dout + row * a.hidden + col0 + 4 * lane) = o;
-          if (nts > 1) {   // the second output tile
-            const float4 h4 = *reinterpret_cast<const float4 *>(scratch + (ECH + ml) * 128 + 4 * lane);
+#pragma unroll
+          for (int jt = 1; jt < (PHASE == 2 ? C::NTC : 1); ++jt) {   // the CTA's further output tiles
+            if (jt >= nts) break;
+            const float4 h4 = *reinterpret_cast<const float4 *>(scratch + (jt * ECH + ml) * 128 + 4 * lane);
             float t[4] = {h4.x, h4.y, h4.z, h4.w};
             fwht128_warp(t, lane);
-            o.x = t[0] * kRhtScale * ep_b[0] * w;
-            o.y = t[1] * kRhtScale * ep_b[1] * w;
-            o.z = t[2] * kRhtScale * ep_b[2] * w;
-            o.w = t[3] * kRhtScale * ep_b[3] * w;
-            *reinterpret_cast<float4 *>(a.dout + row * a.hidden + col0 + BN + 4 * lane) = o;
+            o.x = t[0] * kRhtScale * ep_t[jt][0] * w;
+            o.y = t[1] * kRhtScale * ep_t[jt][1] * w;
+            o.z = t[2] * kRhtScale * ep_t[jt][2] * w;
+            o.w = t[3] * kRhtScale * ep_t[jt][3] * w;
+            *reinterpret_cast<float4 *>(a.dout + row * a.hidden + col0 + jt * BN + 4 * lane) = o;
           }
         }
       }
@@ -639,11 +644,18 @@ int exl3_launch_moe_fused_down(const uint16_t *hin, int U, int hidden, int inter
   a.hidden = hidden;
   a.err = err;
   a.splits = 1;
-  // two output tiles per CTA (one fill and one epilogue for both) when each
-  // tile's pairs fill whole trellis stages and the grid still covers the SMs
-  // twice over; few routed rows keep one tile per CTA for parallelism
+  // several output tiles per CTA (one fill and one epilogue for all: four
+  // with 32-row tiles, else two) when each tile's pairs fill whole trellis
+  // stages and the grid still covers the SMs twice over; few routed rows
+  // keep fewer tiles per CTA for parallelism
   const int sms = exl3_sm_count();
-  a.ntc = ((a.KB / 2) % 2 == 0 && (long)max_mtiles * (a.NT / 2) >= 2L * sms) ? 2 : 1;
+  a.ntc = 1;
+  if ((a.KB / 2) % 2 == 0)
+    for (int c = cap == 32 ? 4 : 2; c >= 2; c /= 2)
+      if ((long)max_mtiles * (a.NT / c) >= 2L * sms) {
+        a.ntc = c;
+        break;
+      }
   const int grid = max_mtiles * ((a.NT + a.ntc - 1) / a.ntc);
   if (cap == 32) return mf_launch<2, 32>(K, t0, t0, tt, a, grid, s);
   if (cap == 128) return mf_launch<2, 128>(K, t0, t0, tt, a, grid, s);
