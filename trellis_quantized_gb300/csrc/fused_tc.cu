@@ -180,28 +180,31 @@ __global__ void __launch_bounds__(Roles<NMAX>::WARPS * 32, 1) fused_tc_kernel(co
     // ... (8 MMAs after one wait) into its own accumulator (TMEM columns
     // g * NMAX ...).  One issuer per SM sub-partition: an issuer shares its
     // sub-partition's issue slots with four decoder warps, and two issuers
-    // could not keep up with the decoders
-    if (lane == 0) {
-      const int g = warp - 1;
-      const uint32_t dcol = tmem_base + (uint32_t)(g * NMAX);
-      const uint32_t idesc = idesc_f16_amn(BN, npad);
-      int xwaited = -1;
-      bool stop = false;
-      for (int P = g; P < npairs; P += NISS) {
-        const int xj = (2 * P) / S::XSTEPS, xs = xj % XS, ps = P % NPS;
-        bool ok = true;
-        if (xj != xwaited) {            // once per x' stage
-          ok = tc::mbar_wait(&xfull[xs], (xj / XS) & 1);
-          xwaited = xj;
-        }
-        ok = ok && tc::mbar_wait(&wfull[ps], (P / NPS) & 1);
-        if (!ok || *abort_flag) {
-          set_device_error(a.err, kErrBounds);
-          *abort_flag = 1;
-          stop = true;
-          break;
-        }
-        tc::tc_fence_after();
+    // could not keep up with the decoders.  The whole warp runs the loop
+    // (waits and descriptors stay warp-uniform); one elected lane issues
+    // the MMAs and their commits.
+    const int g = __shfl_sync(0xffffffffu, warp, 0) - 1;
+    const uint32_t dcol = tmem_base + (uint32_t)(g * NMAX);
+    const uint32_t idesc = idesc_f16_amn(BN, npad);
+    int xwaited = -1;
+    bool stop = false;
+    for (int P = g; P < npairs; P += NISS) {
+      const int xj = (2 * P) / S::XSTEPS, xs = xj % XS, ps = P % NPS;
+      bool ok = true;
+      if (xj != xwaited) {            // once per x' stage
+        ok = tc::mbar_wait(&xfull[xs], (xj / XS) & 1);
+        xwaited = xj;
+      }
+      ok = ok && tc::mbar_wait(&wfull[ps], (P / NPS) & 1);
+      ok = __all_sync(0xffffffffu, ok && !*abort_flag);
+      if (!ok) {
+        if (lane == 0) set_device_error(a.err, kErrBounds);
+        *abort_flag = 1;
+        stop = true;
+        break;
+      }
+      tc::tc_fence_after();
+      if (tc::elect_one()) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int i = 2 * P + h;
@@ -215,8 +218,9 @@ __global__ void __launch_bounds__(Roles<NMAX>::WARPS * 32, 1) fused_tc_kernel(co
         tc::mma_commit(&wempty[ps]);
         tc::mma_commit(&xempty[xs]);    // each issuer uses an x' stage for one pair
       }
-      if (!stop) tc::mma_commit(accum);
+      __syncwarp();
     }
+    if (!stop && tc::elect_one()) tc::mma_commit(accum);
   } else {
     // ---------------- decoders: group g takes k steps i = g, g + 2, ...
     const int dw = warp - kDec0;             // 0..15

@@ -187,38 +187,48 @@ __global__ void __launch_bounds__((2 + epi_warps<BN, Q8>()) * 32, 1) gemm_tc_ker
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      int stage = 0, acc = 0;
-      uint32_t phase = 0, acc_phase = 0;
-      const int CH = Q8 ? Q8_CHUNK_KB : KB;       // k-blocks per accumulator hand-off
-      for (int tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x) {
-        for (int kb0 = 0; kb0 < KB && !*abort_flag; kb0 += CH) {
-          if (!tc::mbar_wait(&tempty[acc], acc_phase ^ 1)) {
-            set_device_error(a.err, kErrBounds);
+    // MMA issuer: the whole warp runs the loop (waits and descriptors stay
+    // warp-uniform); one elected lane issues the MMAs and their commits.
+    int stage = 0, acc = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    const int CH = Q8 ? Q8_CHUNK_KB : KB;       // k-blocks per accumulator hand-off
+    bool stop = __any_sync(0xffffffffu, *abort_flag != 0);
+    for (int tile = blockIdx.x; tile < num_tiles && !stop; tile += gridDim.x) {
+      for (int kb0 = 0; kb0 < KB && !stop; kb0 += CH) {
+        const bool okt = __all_sync(0xffffffffu, tc::mbar_wait(&tempty[acc], acc_phase ^ 1));
+        if (!okt) {
+          if (lane == 0) set_device_error(a.err, kErrBounds);
+          *abort_flag = 1;
+          stop = true;
+          break;
+        }
+        tc::tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(acc * BN);
+        const int kb1 = min(KB, kb0 + CH);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          const bool okf = __all_sync(0xffffffffu, tc::mbar_wait(&full[stage], phase));
+          if (!okf) {
+            if (lane == 0) set_device_error(a.err, kErrBounds);
             *abort_flag = 1;
+            stop = true;
             break;
           }
           tc::tc_fence_after();
-          const uint32_t d = tmem_base + (uint32_t)(acc * BN);
-          const int kb1 = min(KB, kb0 + CH);
-          for (int kb = kb0; kb < kb1; ++kb) {
-            if (!tc::mbar_wait(&full[stage], phase)) {
-              set_device_error(a.err, kErrBounds);
-              *abort_flag = 1;
-              break;
-            }
-            tc::tc_fence_after();
-            const uint64_t ad = tc::sdesc_k_sw128(sA + stage * A_BYTES);
-            const uint64_t bd = tc::sdesc_k_sw128(sB + stage * B_BYTES);
+          const uint64_t ad = tc::sdesc_k_sw128(sA + stage * A_BYTES);
+          const uint64_t bd = tc::sdesc_k_sw128(sB + stage * B_BYTES);
+          if (tc::elect_one()) {
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk)
               tc::mma_f16(d, ad + 2 * kk, bd + 2 * kk, C::IDESC, (kb != kb0 || kk != 0) ? 1u : 0u);
             tc::mma_commit(&empty[stage]);
-            if (++stage == STAGES) { stage = 0; phase ^= 1; }
           }
-          tc::mma_commit(&tfull[acc]);
-          if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+          __syncwarp();
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
+        if (tc::elect_one()) tc::mma_commit(&tfull[acc]);
+        __syncwarp();
+        if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+        stop = stop || __any_sync(0xffffffffu, *abort_flag != 0);
       }
     }
   } else {

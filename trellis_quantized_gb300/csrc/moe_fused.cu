@@ -244,22 +244,25 @@ __global__ void __launch_bounds__(Roles<NMAX>::WARPS * 32, 1)
     // ---------------- MMA issuers: warp 1 + g takes the pairs P = g, g + NISS,
     // ... into accumulators (jt NISS NP + g NP + p) * XROWS (phase 1: p =
     // gate, up; jt: the CTA's output tile).  The first pair of a tile that
-    // an issuer sees is among the tile's first NISS pairs.
-    if (lane == 0) {
-      const int g = warp - 1;
-      const uint32_t idesc = ftc::idesc_f16_amn(BN, npad);
-      bool stop = false;
-      for (int P = g; P < npairs; P += NISS) {
-        const int xs = P % XS, ps = P % NPS;
-        const bool ok = tc::mbar_wait(&xfull[xs], (P / XS) & 1) && tc::mbar_wait(&wfull[ps], (P / NPS) & 1);
-        if (!ok || *abort_flag) {
-          set_device_error(a.err, kErrBounds);
-          *abort_flag = 1;
-          stop = true;
-          break;
-        }
-        tc::tc_fence_after();
-        const int jt = P / nptile, Pt = P - jt * nptile;
+    // an issuer sees is among the tile's first NISS pairs.  The whole warp
+    // runs the loop (waits and descriptors stay warp-uniform); one elected
+    // lane issues the MMAs and their commits.
+    const int g = __shfl_sync(0xffffffffu, warp, 0) - 1;
+    const uint32_t idesc = ftc::idesc_f16_amn(BN, npad);
+    bool stop = false;
+    for (int P = g; P < npairs; P += NISS) {
+      const int xs = P % XS, ps = P % NPS;
+      bool ok = tc::mbar_wait(&xfull[xs], (P / XS) & 1) && tc::mbar_wait(&wfull[ps], (P / NPS) & 1);
+      ok = __all_sync(0xffffffffu, ok && !*abort_flag);
+      if (!ok) {
+        if (lane == 0) set_device_error(a.err, kErrBounds);
+        *abort_flag = 1;
+        stop = true;
+        break;
+      }
+      tc::tc_fence_after();
+      const int jt = P / nptile, Pt = P - jt * nptile;
+      if (tc::elect_one()) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int p = PHASE == 1 ? h : 0;
@@ -275,8 +278,9 @@ __global__ void __launch_bounds__(Roles<NMAX>::WARPS * 32, 1)
         tc::mma_commit(&wempty[ps]);
         tc::mma_commit(&xempty[xs]);
       }
-      if (!stop) tc::mma_commit(accum);
+      __syncwarp();
     }
+    if (!stop && tc::elect_one()) tc::mma_commit(accum);
   } else {
     // ---------------- decoders: group g takes the pairs P = g, g + 2, ...
     const int dw = warp - kDec0;
