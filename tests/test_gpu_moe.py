@@ -103,6 +103,19 @@ def test_moe_expert_beyond_one_256_row_tile():
         assert_close(_run(c, d, od), _oracle(c), f"moe 256-row tiles out={od}")
 
 
+def test_moe_expert_beyond_one_160_row_tile():
+    """240 tokens, top-2 over 4 experts: 480 routed rows (120 per expert on
+    average, between 96 and 136) take 160-row tiles; every first slot on
+    expert 1 gives it 240 rows over two tiles (160 + 80), whose epilogue runs
+    in a 128-row and a 32-row chunk; experts 0 and 2 hold 120 rows each."""
+    c = synth.moe_case(52, 2, 240, E=4, topk=2, hidden=512, inter=256, K=3)
+    c.ids[:, 0] = 1
+    c.ids[:, 1] = (np.arange(240) % 2) * 2
+    d = _dev_case(c)
+    for od in (tq.EXL3_OUT_F16, tq.EXL3_OUT_F32):
+        assert_close(_run(c, d, od), _oracle(c), f"moe 160-row tiles out={od}")
+
+
 def test_moe_invalid_expert_id_is_reported_and_skipped():
     c = synth.moe_case(53, 0, 4, E=4, topk=2, hidden=256, inter=128, K=3)
     d = _dev_case(c)

@@ -267,7 +267,7 @@ LinearInt8Ws linear_int8_ws(int M, int k, int n) {
 struct MoeWs {
   size_t counts, offsets, pos, perm, mtiles, n_mtiles, chunk, xg, xu, h, d, partials, total;
   int max_mtiles, grid_mtiles, splits;
-  int cap;            // rows per expert tile: 32, 128 or 256 (chosen in moe_ws)
+  int cap;            // rows per expert tile: 32, 128, 160 or 256 (chosen in moe_ws)
   bool gemv;          // few routed rows: grouped M = 1 GEMVs instead of the tile kernels
   size_t y13;         // gemv: gate/up outputs [U][2][inter] fp32 (d, pos, partials as above)
 };
@@ -307,11 +307,17 @@ MoeWs moe_ws(int T, int topk, int E, int hidden, int inter, int K13, int K2, boo
   }
   // Tiles of 32 rows (the grouped kernels then run MMAs 16 or 32 rows wide,
   // with four issuers) when the call routes at most 16 rows per expert on
-  // average; 256 rows when it routes at least 96 (so that an expert's rows
-  // stay in one tile and its weights are decoded once) and the widths fit;
-  // 128 rows otherwise.
+  // average; when it routes at least 96, tiles that keep an expert's rows
+  // together (its weights are then decoded once): 160 rows up to 136 rows
+  // per expert on average (room for three x' stages), 256 above; 128 rows
+  // otherwise.  The larger tiles need widths that fit their rings.
   w.cap = U <= (size_t)16 * E ? 32 : 128;
-  if (U >= (size_t)96 * E && exl3_moe_fused_cap_fits(256, K13 > K2 ? K13 : K2)) w.cap = 256;
+  const int kmax = K13 > K2 ? K13 : K2;
+  if (U >= (size_t)96 * E) {
+    const int big = U < (size_t)136 * E ? 160 : 256;
+    if (exl3_moe_fused_cap_fits(big, kmax)) w.cap = big;
+    else if (big == 160 && exl3_moe_fused_cap_fits(256, kmax)) w.cap = 256;
+  }
   w.max_mtiles = (int)(U / w.cap + E + 1);
   size_t off = kDataOff;
   auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes); return o; };

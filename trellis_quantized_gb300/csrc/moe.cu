@@ -84,7 +84,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *warp_sums, int *
 
 // (2) one CTA of 1024 threads, thread e = expert e (E <= 1024): per-chunk
 // counts become the expert's rows before each chunk; counts, offsets and the
-// tile list (tiles of at most cap rows, cap a power of two) follow from two
+// tile list (tiles of at most cap rows) follow from two
 // block scans.
 __global__ void __launch_bounds__(1024) remap_scan_kernel(int E, int nchunks, Plan p, int max_mtiles, int cap,
                                                           int *err) {
@@ -321,11 +321,11 @@ int exl3_moe_remap_chunk(int E) {
 }
 
 // chunk_tab: [ceil(U / exl3_moe_remap_chunk(E))][E] ints of workspace.
-// cap: rows per tile (32, 128 or 256) of the tile list the grouped kernels read.
+// cap: rows per tile (32, 128, 160 or 256) of the tile list the grouped kernels read.
 cudaError_t exl3_launch_moe_remap(const int32_t *ids, int U, int E, int *counts, int *offsets, int *perm, int *pos,
                                   int *mtiles, int *n_mtiles, int max_mtiles, int cap, int *chunk_tab, int *err,
                                   cudaStream_t s) {
-  if (E < 1 || E > 1024 || (cap != 32 && cap != 128 && cap != 256)) return cudaErrorInvalidValue;
+  if (E < 1 || E > 1024 || (cap != 32 && cap != 128 && cap != 160 && cap != 256)) return cudaErrorInvalidValue;
   moe::Plan p{counts, offsets, perm, pos, reinterpret_cast<int4 *>(mtiles), n_mtiles, chunk_tab};
   if (U <= moe::kSmallU && E <= moe::kSmallE) {
     return launch_pdl(moe::remap_small_kernel, dim3(1), dim3(1024), 0, s, ids, U, E, p, max_mtiles, cap, err);

@@ -7,8 +7,9 @@
 //
 // A CTA handles one (expert tile, 128-column output tile) pair of the
 // device-side tile list.  A tile holds up to NMAX routed rows of one expert
-// (NMAX = 32 when the call routes few rows per expert, 256 when it routes
-// many and the widths leave room for 64 KB x' stages, else 128); the MMA
+// (NMAX = 32 when the call routes few rows per expert; 160 or 256 when it
+// routes many (160 keeps three x' stages in shared memory, 256 holds more
+// rows per expert) and the widths fit; else 128); the MMA
 // computes the transposed product (decoded weights as the MN-major A operand,
 // M = 128 output columns; the tile's x' rows as the K-major B operand, N =
 // the tile's rows rounded up to 16).  Roles (2 + NISS + 16 warps):
@@ -84,11 +85,14 @@ struct Cfg {
   // each): four with 32-row tiles, two otherwise (TMEM holds 512 columns)
   static constexpr int NTC = PHASE == 2 ? (NMAX <= 32 ? 4 : 2) : 1;
   static constexpr uint32_t TMEM_COLS = NISS * NP * XROWS * NTC;
+  // the allocation: the next power of two (160-row tiles use 320 columns)
+  static constexpr uint32_t TMEM_ALLOC = TMEM_COLS <= 32 ? 32 : TMEM_COLS <= 64 ? 64 : TMEM_COLS <= 128 ? 128
+                                         : TMEM_COLS <= 256 ? 256 : 512;
   // whether this width and tile capacity fit (256-row tiles leave room for
   // K <= 4 only); the host launches only configurations that do
   static constexpr bool OK = TS >= 2 && XS >= NISS && NPS % NISS == 0 && NPS % NGRP == 0 && XS % NISS == 0 &&
                              NTC * NP * ECH * 128 * 4 <= XS * X_STAGE + W_RING && TMEM_COLS <= 512 &&
-                             (TMEM_COLS & (TMEM_COLS - 1)) == 0 && SMEM_BYTES <= 227 * 1024;
+                             SMEM_BYTES <= 227 * 1024;
 };
 
 struct Args {
@@ -188,7 +192,7 @@ __global__ void __launch_bounds__(Roles<NMAX>::WARPS * 32, 1)
     tc::prefetch_tmap(&tmT);
   }
   if (warp == 1) {
-    tc::tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tc::tmem_alloc(tmem_slot, C::TMEM_ALLOC);
     tc::tmem_relinquish();
   }
   tc::tc_fence_before();
@@ -485,7 +489,7 @@ __global__ void __launch_bounds__(Roles<NMAX>::WARPS * 32, 1)
   __syncthreads();
   if (warp == 1) {
     tc::tc_fence_after();
-    tc::tmem_dealloc(tmem_base, C::TMEM_COLS);
+    tc::tmem_dealloc(tmem_base, C::TMEM_ALLOC);
   }
 }
 
@@ -556,6 +560,7 @@ bool exl3_moe_fused_cap_fits(int cap, int K) {
   case KK:                                                                                                      \
     ok = cap == 32 ? (mf::Cfg<KK, 1, 32>::OK && mf::Cfg<KK, 2, 32>::OK)                                        \
                    : cap == 128 ? (mf::Cfg<KK, 1, 128>::OK && mf::Cfg<KK, 2, 128>::OK)                           \
+                   : cap == 160 ? (mf::Cfg<KK, 1, 160>::OK && mf::Cfg<KK, 2, 160>::OK)                           \
                                 : (mf::Cfg<KK, 1, 256>::OK && mf::Cfg<KK, 2, 256>::OK);                          \
     break;
   switch (K) {
@@ -568,7 +573,7 @@ bool exl3_moe_fused_cap_fits(int cap, int K) {
 }
 
 // Phase 1: xg, xu [U][hidden] fp16 sorted rows; w13 trellis [E][2][hidden/16][inter/16][16K];
-// the tile list holds tiles of at most cap (32 or 128) rows.
+// the tile list holds tiles of at most cap (32, 128, 160 or 256) rows.
 // splits > 1 (k split of the gate+up projection): partials [max_mtiles * inter/128][splits][2][cap][128]
 // fp32 and counters [max_mtiles * inter/128], zero on entry and left zero.
 // e_lo, e_cnt: only experts [e_lo, e_lo + e_cnt), whose trellis starts at
@@ -582,7 +587,7 @@ int exl3_launch_moe_fused_gateup(const uint16_t *xg, const uint16_t *xu, int U, 
     e_cnt = E;
   }
   CUtensorMap t0, t1, tt;
-  if (cap != 32 && cap != 128 && cap != 256) return exl3_fail(EXL3_ERR_ARG, "tile capacity %d", cap);
+  if (cap != 32 && cap != 128 && cap != 160 && cap != 256) return exl3_fail(EXL3_ERR_ARG, "tile capacity %d", cap);
   int rc = mf_xmap(&t0, xg, U, hidden, cap);
   if (!rc) rc = mf_xmap(&t1, xu, U, hidden, cap);
   if (!rc) rc = mf_tmap(&tt, w13_trellis, (long)e_cnt * 2 * (hidden / 16), inter, K, 8);
@@ -608,7 +613,8 @@ int exl3_launch_moe_fused_gateup(const uint16_t *xg, const uint16_t *xu, int U, 
   const int grid = max_mtiles * a.NT * splits;
   if (cap == 32) return mf_launch<1, 32>(K, t0, t1, tt, a, grid, s);
   if (cap == 128) return mf_launch<1, 128>(K, t0, t1, tt, a, grid, s);
-  if (splits > 1) return exl3_fail(EXL3_ERR_ARG, "no k split with 256-row tiles");
+  if (splits > 1) return exl3_fail(EXL3_ERR_ARG, "no k split with tiles of more than 128 rows");
+  if (cap == 160) return mf_launch<1, 160>(K, t0, t1, tt, a, grid, s);
   return mf_launch<1, 256>(K, t0, t1, tt, a, grid, s);
 }
 
@@ -618,7 +624,7 @@ int exl3_launch_moe_fused_down(const uint16_t *hin, int U, int hidden, int inter
                                const uint16_t *w2_trellis, const int *mtiles, const int *n_mtiles, int max_mtiles,
                                int cap, const uint16_t *svh2, const float *weights, const int *perm, float *dout,
                                int *err, cudaStream_t s, int e_lo, int e_cnt) {
-  if (cap != 32 && cap != 128 && cap != 256) return exl3_fail(EXL3_ERR_ARG, "tile capacity %d", cap);
+  if (cap != 32 && cap != 128 && cap != 160 && cap != 256) return exl3_fail(EXL3_ERR_ARG, "tile capacity %d", cap);
   if (e_cnt < 0) {
     e_lo = 0;
     e_cnt = E;
@@ -663,5 +669,6 @@ int exl3_launch_moe_fused_down(const uint16_t *hin, int U, int hidden, int inter
   const int grid = max_mtiles * ((a.NT + a.ntc - 1) / a.ntc);
   if (cap == 32) return mf_launch<2, 32>(K, t0, t0, tt, a, grid, s);
   if (cap == 128) return mf_launch<2, 128>(K, t0, t0, tt, a, grid, s);
+  if (cap == 160) return mf_launch<2, 160>(K, t0, t0, tt, a, grid, s);
   return mf_launch<2, 256>(K, t0, t0, tt, a, grid, s);
 }
