@@ -376,8 +376,11 @@ int exl3_moe_grouped_mixed(const uint16_t *x, int T, int hidden,
  *   exl3_linear), is rejected with EXL3_ERR_SHAPE (use exl3_linear with a
  *   workspace instead).  The first call on a device looks up the
  *   array's device address (cudaGetSymbolAddress) with that device current;
- *   make that first call before any stream capture.  Each call clears the
- *   parts of the array that must start at zero.  All calls share the array:
+ *   make that first call before any stream capture.  Each call enqueues two
+ *   kernels: a one-CTA kernel that clears the parts of the array that must
+ *   start at zero, and the GEMV as its programmatic dependent (it streams
+ *   its weights while the clear runs; the clear waits for all earlier work
+ *   on the stream).  All calls share the array:
  *   calls that can overlap on the GPU (other streams, other host threads)
  *   race with each other.  No cudaMalloc or cudaFree is ever called.
  */
@@ -391,9 +394,9 @@ int exl3_linear_gemv_noalloc(const uint16_t *x, int k, int n, const uint16_t *tr
  * counterpart on the source pages; a companion of that entry point).
  *   Waits for `stream` (cudaStreamSynchronize), copies the word to
  *   *err_out with a plain cudaMemcpy and clears it; allocates nothing.
- *   Nonzero means a call since the last read hit a device-side check (a
- *   bounded wait that ran out, an index out of range): that call's y is
- *   incomplete.  The bits are those of exl3_check_device_error.  Returns
+ *   Each call clears the word first, so nonzero means the most recent call
+ *   on this device hit a device-side check (a bounded wait that ran out, an
+ *   index out of range): that call's y is incomplete.  The bits are those of exl3_check_device_error.  Returns
  *   EXL3_ERR_ARG for a NULL err_out, EXL3_ERR_CUDA if a CUDA call fails.
  */
 int exl3_noalloc_device_error(exl3_stream_t stream, int *err_out);

@@ -11,7 +11,12 @@
 // only inputs and outputs.
 //
 // The array is kNoAllocScratchBytes (2 MiB) of device memory on every GPU
-// that loads the library, held until the process exits.  In host code its
+// that loads the library, held until the process exits.  A call first
+// clears the error word and the arrival counters it uses with a one-CTA
+// kernel and launches the GEMV as its programmatic dependent, so the GEMV
+// streams its weights while the clear runs (the clear itself waits for all
+// earlier work on the stream) and touches the scratch only after the clear
+// has completed.  In host code its
 // name is only a host-side stand-in, not a device address, so the first call
 // on each device (with that device current) looks the address up with
 // cudaGetSymbolAddress and caches it; that first call should come before any
@@ -63,6 +68,11 @@ int scratch_for_current_device(void **ptr) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+__global__ void __launch_bounds__(256) clear_words_kernel(int *words, int n) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  for (int i = threadIdx.x; i < n; i += blockDim.x) words[i] = 0;
+}
+
 }  // namespace
 
 extern "C" int exl3_linear_gemv_noalloc(const uint16_t *x, int k, int n, const uint16_t *trellis,
@@ -106,10 +116,12 @@ extern "C" int exl3_linear_gemv_noalloc(const uint16_t *x, int k, int n, const u
   float *partials = reinterpret_cast<float *>(base + kPartialsOff);
   // The error word and the counters must start at zero; a previous call that
   // did not finish cleanly could have left them set.
-  rc = exl3_cuda_check(cudaMemsetAsync(base, 0, kCtrl + colblocks * sizeof(int), stream), "clear scratch");
+  clear_words_kernel<<<1, 256, 0, stream>>>(reinterpret_cast<int *>(base),
+                                            (int)((kCtrl + colblocks * sizeof(int)) / sizeof(int)));
+  rc = exl3_cuda_check(cudaGetLastError(), "clear scratch");
   if (rc) return rc;
   return exl3_cuda_check(exl3_launch_gemv_m1(x, trellis, suh, svh, k, n, K, y, out_dtype == EXL3_OUT_F32,
-                                             partials, counters, err, grid, stream),
+                                             partials, counters, err, grid, stream, /*prefetch=*/true),
                          "gemv launch");
 }
 
