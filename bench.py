@@ -76,7 +76,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # at k=5120 n=25600, with the hash of the kernel's sources at capture time; a
 # changed kernel source makes the recorded traffic stale (reported as null).
 TRAFFIC = {"files": ["trellis_quantized_gb300/csrc/gemv.cu", "trellis_quantized_gb300/csrc/gemv_core.cuh"],
-           "sha1": "c62721dd7bfb7ddb2595af5372a60ffbb441f264", "bytes_per_launch": 65677824,
+           "sha1": "b3e1108fb96292e5a394240e807a00c560c2bffe", "bytes_per_launch": 65719552,
            "workload": "k5120 n25600 K4 M1"}
 
 

@@ -115,6 +115,7 @@ struct GemvPart {
   float *partials;
 };
 
+constexpr int kGemvMinRows = 32;       // rows per CTA below which the M = 1 GEMV uses fewer CTAs
 constexpr int kGemvMaxOps = 4;        // ops one CTA's range may touch in GROUPED mode
 constexpr int kGemvMaxShards = 8;     // shards of different widths in one launch
 constexpr int kGemvPrePartials = 2;   // partials a block's first CTA loads before its segment ends
@@ -913,7 +914,22 @@ void exl3_gemv_plan(int k, int n, int K, int *grid, size_t *partial_floats) {
   const int cc = exl3_gemv_cta_cols(K);
   const long long colblocks = (n + cc - 1) / cc;
   const long long total = colblocks * (k / 16);
-  int g = gemv_sm_count();
+  // One CTA per SM, or, with fewer column blocks than SMs, the same number
+  // of CTAs for every block so that block boundaries fall on CTA boundaries
+  // (no block is then shared, or each is shared evenly): taken when it
+  // keeps at least 80% of the SMs busy (n = 17408 at k = 5120: 136 CTAs of
+  // one block each ran 7% faster than 152 sharing blocks), or when one CTA
+  // per SM would get fewer than kGemvMinRows rows (a small matrix on every
+  // SM leaves each block split over dozens of CTAs, whose partials the
+  // block's finisher then adds one after another).
+  const int sms = gemv_sm_count();
+  int g = sms;
+  if (colblocks < sms) {
+    long long per = sms / colblocks;   // CTAs per block
+    while (per > 1 && (k / 16) / per < kGemvMinRows) --per;
+    const long long aligned = colblocks * per;
+    if (5 * aligned >= 4LL * sms || total / sms < kGemvMinRows) g = (int)aligned;
+  }
   if (g > total) g = (int)total;
   *grid = g;
   *partial_floats = (size_t)(colblocks + g) * (size_t)cc;
