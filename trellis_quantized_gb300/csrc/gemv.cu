@@ -800,7 +800,15 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
   int wsel = 0, first = 0, cnt = 0;
   for (int w = 1, start = 0; w <= 8; ++w) {   // width w takes CTAs [start, start + c)
     if (rows[w] == 0) continue;
-    const int c = 1 + (int)((unsigned long long)(G - nw) * weights[w] / all);
+    int c = 1 + (int)((unsigned long long)(G - nw) * weights[w] / all);
+    // as many CTAs for every column block of the width (block boundaries
+    // then fall on CTA boundaries), at least kGemvMinRows rows each
+    const int wblocks = (int)(rows[w] / (uint32_t)a.tiles_k);
+    if (c >= wblocks) {
+      int per = c / wblocks;
+      while (per > 1 && a.tiles_k / per < kGemvMinRows) --per;
+      c = per * wblocks;
+    }
     if (me >= start && me < start + c) {
       wsel = w;
       first = start;
@@ -910,27 +918,32 @@ bool exl3_gemv_fits(int k, int n, int K) {
 
 // Grid size (one CTA per SM, at most one per row) and the partial-sum slots
 // (floats) the GEMV needs.
+// One CTA per SM, or, with fewer column blocks than SMs, the same number of
+// CTAs for every block so that block boundaries fall on CTA boundaries (no
+// block is then shared, or each is shared evenly): taken when it keeps at
+// least 80% of the SMs busy (n = 17408 at k = 5120: 136 CTAs of one block
+// each ran 7% faster than 152 sharing blocks), or when one CTA per SM would
+// get fewer than kGemvMinRows rows (a small matrix on every SM leaves each
+// block split over dozens of CTAs, whose partials the block's finisher then
+// adds one after another).  The equal ranges of the partition put block
+// boundaries on CTA boundaries: CTA b per + j of g = blocks per starts at
+// b rows_per_block + floor(j rows_per_block / per).
+static long long gemv_grid_for(long long blocks, long long rows_per_block, long long sms) {
+  const long long total = blocks * rows_per_block;
+  long long g = sms;
+  if (blocks < sms) {
+    long long per = sms / blocks;   // CTAs per block
+    while (per > 1 && rows_per_block / per < kGemvMinRows) --per;
+    const long long aligned = blocks * per;
+    if (5 * aligned >= 4 * sms || total / sms < kGemvMinRows) g = aligned;
+  }
+  return g > total ? total : g;
+}
+
 void exl3_gemv_plan(int k, int n, int K, int *grid, size_t *partial_floats) {
   const int cc = exl3_gemv_cta_cols(K);
   const long long colblocks = (n + cc - 1) / cc;
-  const long long total = colblocks * (k / 16);
-  // One CTA per SM, or, with fewer column blocks than SMs, the same number
-  // of CTAs for every block so that block boundaries fall on CTA boundaries
-  // (no block is then shared, or each is shared evenly): taken when it
-  // keeps at least 80% of the SMs busy (n = 17408 at k = 5120: 136 CTAs of
-  // one block each ran 7% faster than 152 sharing blocks), or when one CTA
-  // per SM would get fewer than kGemvMinRows rows (a small matrix on every
-  // SM leaves each block split over dozens of CTAs, whose partials the
-  // block's finisher then adds one after another).
-  const int sms = gemv_sm_count();
-  int g = sms;
-  if (colblocks < sms) {
-    long long per = sms / colblocks;   // CTAs per block
-    while (per > 1 && (k / 16) / per < kGemvMinRows) --per;
-    const long long aligned = colblocks * per;
-    if (5 * aligned >= 4LL * sms || total / sms < kGemvMinRows) g = (int)aligned;
-  }
-  if (g > total) g = (int)total;
+  const int g = (int)gemv_grid_for(colblocks, k / 16, gemv_sm_count());
   *grid = g;
   *partial_floats = (size_t)(colblocks + g) * (size_t)cc;
 }
@@ -1010,8 +1023,7 @@ bool exl3_moe_gemv_plan(int U, int nslots, int k, int n, int K, int *grid, size_
   const int cc = exl3_gemv_cta_cols(K);
   const long long colblocks = (n + cc - 1) / cc, op_rows = colblocks * (k / 16);
   const long long total = (long long)U * nslots * op_rows;
-  long long g = gemv_sm_count();
-  if (g > total) g = total;
+  const long long g = gemv_grid_for((long long)U * nslots * colblocks, k / 16, gemv_sm_count());
   if (g < 1) return false;
   if ((unsigned long long)total * (unsigned long long)g >= (1ull << 32)) return false;
   const long long range = (total + g - 1) / g;
