@@ -272,9 +272,16 @@ struct MoeWs {
   size_t y13;         // gemv: gate/up outputs [U][2][inter] fp32 (d, pos, partials as above)
 };
 
-// Routed rows up to which the few-token path (one grouped CUDA-core GEMV
-// launch per projection, no sort) runs instead of the tensor-core tiles.
+// The few-token path (one grouped CUDA-core GEMV launch per projection, no
+// sort) runs instead of the tensor-core tiles for up to 32 routed rows, and
+// for up to one routed row per expert (at most 512 rows, and as long as no
+// CTA's share spans more ops than the GEMV keeps x' for): it decodes every
+// routed row's expert weights separately, at about twice the rate per
+// weight of the tile kernels' decoders, which pays while few rows share an
+// expert (E = 256, top-8, T = 16: 0.090 ms against 0.124 ms).
 constexpr int kMoeGemvMaxU = 32;
+constexpr int kMoeGemvMaxUPerExpert = 512;
+constexpr int kMoeMixedGemvMaxU = 32;   // the mixed-width kernel counts units with one warp ballot
 
 // Few routed rows (grouped M = 1 GEMVs): gate and up outputs [U][2][inter]
 // fp32, d [U][hidden] fp32, pos [U] and the GEMVs' split-k partials.
@@ -299,7 +306,8 @@ MoeWs moe_ws(int T, int topk, int E, int hidden, int inter, int K13, int K2, boo
   if (allow_gemv) {
     int g1 = 0, g2 = 0, b1 = 0, b2 = 0;
     size_t p1 = 0, p2 = 0;
-    if (U <= (size_t)kMoeGemvMaxU && exl3_moe_gemv_plan((int)U, 2, hidden, inter, K13, &g1, &p1, &b1) &&
+    const bool few = U <= (size_t)kMoeGemvMaxU || (U <= (size_t)E && U <= (size_t)kMoeGemvMaxUPerExpert);
+    if (few && exl3_moe_gemv_plan((int)U, 2, hidden, inter, K13, &g1, &p1, &b1) &&
         exl3_moe_gemv_plan((int)U, 1, inter, hidden, K2, &g2, &p2, &b2) && (size_t)b1 <= kMaxCounters &&
         (size_t)b2 <= kMaxCounters) {
       return moe_gemv_layout(U, hidden, inter, p1 > p2 ? p1 : p2);
@@ -412,7 +420,7 @@ std::vector<WidthRun> width_runs(const exl3_expert_proj_mixed *p, int E) {
 // split-k partials.
 bool mixed_gemv_plan(size_t U, int E, int hidden, int inter, const exl3_expert_proj_mixed *w13,
                      const exl3_expert_proj_mixed *w2, size_t *partial_floats) {
-  if (U > (size_t)kMoeGemvMaxU) return false;
+  if (U > (size_t)kMoeMixedGemvMaxU) return false;
   size_t pmax = 0;
   for (int proj = 0; proj < 2; ++proj) {
     const std::vector<WidthRun> runs = width_runs(proj == 0 ? w13 : w2, E);
