@@ -164,14 +164,15 @@ def test_moe_gateup_split_over_k(E, topk, T, hidden, inter, K):
 
 @pytest.mark.parametrize("T,E,topk,hidden,inter,K,K2", [(4, 256, 8, 2048, 512, 3, 3), (2, 16, 8, 512, 256, 8, 2),
                                                         (3, 6, 3, 256, 384, 1, 7), (1, 4, 2, 768, 128, 6, 5),
-                                                        (16, 256, 8, 2048, 512, 3, 3), (9, 96, 8, 512, 256, 4, 6)])
+                                                        (16, 256, 8, 2048, 512, 3, 3), (32, 256, 8, 2048, 512, 3, 3),
+                                                        (9, 96, 8, 512, 256, 4, 6)])
 def test_moe_few_tokens_grouped_gemv(T, E, topk, hidden, inter, K, K2):
     """Up to 32 routed rows, or up to one per expert, take the few-token
     path: gate and up as grouped M = 1 GEMVs over (unit, slot), SiLU, down as
     grouped GEMVs times the routing weight, and the combine.  32 rows at the
-    pages' shape is the first boundary, 128 rows over 256 experts (T = 16)
-    and 72 over 96 lie under the second; also mixed widths and odd tile
-    counts.  Deterministic, with the arrival counters back at zero."""
+    pages' shape is the first boundary, 128 and 256 rows over 256 experts
+    (T = 16, and T = 32, whose CTAs' shares span five gate/up ops) and 72
+    over 96 lie under the second; also mixed widths and odd tile counts.  Deterministic, with the arrival counters back at zero."""
     c = synth.moe_case(57, T * 100 + K, T, E=E, topk=topk, hidden=hidden, inter=inter, K=K, K2=K2)
     d = _dev_case(c)
     ws = torch.zeros(tq.exl3_moe_workspace_size(c.T, c.topk, c.E, d["w13"], d["w2"]), dtype=torch.uint8,

@@ -50,7 +50,8 @@ cudaError_t exl3_launch_moe_gather(const uint16_t *x, int U, int hidden, int top
                                    cudaStream_t s);
 cudaError_t exl3_launch_moe_combine(const float *d, const int *pos, int T, int topk, int hidden, void *y,
                                     bool f32out, cudaStream_t s);
-bool exl3_moe_gemv_plan(int U, int nslots, int k, int n, int K, int *grid, size_t *partial_floats, int *blocks);
+bool exl3_moe_gemv_plan(int U, int nslots, int k, int n, int K, int *grid, size_t *partial_floats, int *blocks,
+                        int *xops = nullptr);
 bool exl3_gemv_shards_plan(int S, int k, int n, int K, int *grid, size_t *partial_floats, int *blocks);
 bool exl3_gemv_shards_var_plan(int S, int k, const int *n, int K, int *grid, size_t *partial_floats, int *blocks);
 cudaError_t exl3_launch_gemv_shards_var(const uint16_t *x, int S, int k, const int *n, int K, const uint16_t *trellis,

@@ -60,6 +60,7 @@ struct GemvArgs {
   int *counters;            // [nops * colblocks]
   int *err;                 // device error word
   int k, n, tiles_k, colblocks, stages;
+  int xops;                 // GROUPED: x' slots in shared memory (ops a CTA's range may touch)
   int pre_stages;           // stages the producer loads before x' is ready
   uint32_t total;           // nops * colblocks * tiles_k (grid * total < 2^32)
   // Routed-expert mode (GROUPED): the rows of op o = unit u * nslots + slot
@@ -116,7 +117,8 @@ struct GemvPart {
 };
 
 constexpr int kGemvMinRows = 32;       // rows per CTA below which the M = 1 GEMV uses fewer CTAs
-constexpr int kGemvMaxOps = 4;        // ops one CTA's range may touch in GROUPED mode
+constexpr int kGemvMaxOps = 4;        // ops one CTA's range may touch in GROUPED mode (x' slots)
+constexpr int kGemvMaxOpsMoe = 8;     // the routed-expert plan's limit, when x' for them fits
 constexpr int kGemvMaxShards = 8;     // shards of different widths in one launch
 constexpr int kGemvPrePartials = 2;   // partials a block's first CTA loads before its segment ends
 constexpr int kGemvPreStages = 2;     // stages the producer loads before x' is ready
@@ -291,7 +293,7 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap *maps, const GemvArg
   uint64_t *seg_full = empty + STAGES;                                 // red holds a finished segment
   uint64_t *red_free = seg_full + 1;                                   // the flusher has read red
   uint64_t *xready = red_free + 1;                                     // the consumers' x' is ready
-  constexpr int NOPS = GROUPED ? kGemvMaxOps : 1;
+  const int NOPS = GROUPED ? a.xops : 1;
   float *xs = reinterpret_cast<float *>(xready + 2);                   // [NOPS][k] x' 2^100 (touched blocks)
   float *rsum = xs + NOPS * a.k;                                       // [NOPS][k/16] sum of x' per tile row
 
@@ -852,18 +854,22 @@ template <int K, bool F32, bool GROUPED = false>
 struct Launcher {
   using S = GemvShape<K>;
   // ring stages that fit beside the reduction buffers, x' (4 bytes per k)
-  // and its per-tile-row sums (4 bytes per 16 k), for up to kGemvMaxOps ops
-  // in GROUPED mode
-  static size_t xbytes(int k) { return (GROUPED ? kGemvMaxOps : 1) * (4 * (size_t)k + (size_t)k / 4); }
-  static int stages(int k) {
-    const long avail = (long)kGemvSmemMax - S::FIXED_B - (long)xbytes(k);
+  // and its per-tile-row sums (4 bytes per 16 k), for xops ops in GROUPED
+  // mode
+  static size_t xbytes(int k, int xops = kGemvMaxOps) {
+    return (GROUPED ? xops : 1) * (4 * (size_t)k + (size_t)k / 4);
+  }
+  static int stages(int k, int xops = kGemvMaxOps) {
+    const long avail = (long)kGemvSmemMax - S::FIXED_B - (long)xbytes(k, xops);
     long st = avail / S::STAGE_B;
     if (st > kGemvMaxStages) st = kGemvMaxStages;
     return (int)st;
   }
-  static size_t smem(int k, int st) { return (size_t)st * S::STAGE_B + S::FIXED_B + xbytes(k); }
+  static size_t smem(int k, int st, int xops = kGemvMaxOps) {
+    return (size_t)st * S::STAGE_B + S::FIXED_B + xbytes(k, xops);
+  }
   static cudaError_t launch(const CUtensorMap &tm, const GemvArgs &a, int grid, cudaStream_t s, bool prefetch) {
-    const size_t sm = smem(a.k, a.stages);
+    const size_t sm = smem(a.k, a.stages, GROUPED ? a.xops : 1);
     static std::atomic<size_t> attr[kMaxDevices];   // per device: the attribute is per device
     cudaError_t e = exl3_ensure_smem(reinterpret_cast<const void *>(gemv_m1_kernel<K, F32, GROUPED>), sm, attr);
     if (e != cudaSuccess) return e;
@@ -970,6 +976,7 @@ cudaError_t exl3_launch_gemv_m1_bias(const uint16_t *x, const uint16_t *trellis,
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
   GemvArgs a{};
+  a.xops = kGemvMaxOps;
   a.x = reinterpret_cast<const __half *>(x);
   a.suh = reinterpret_cast<const __half *>(suh);
   a.svh = reinterpret_cast<const __half *>(svh);
@@ -1019,7 +1026,8 @@ cudaError_t exl3_launch_gemv_m1(const uint16_t *x, const uint16_t *trellis, cons
 // Grid, partial-sum floats and arrival counters for nops = U * nslots ops of
 // [k] x [k][n]; false when a CTA's range would touch more than kGemvMaxOps
 // ops or x' for them does not fit beside two ring stages.
-bool exl3_moe_gemv_plan(int U, int nslots, int k, int n, int K, int *grid, size_t *partial_floats, int *blocks) {
+bool exl3_moe_gemv_plan(int U, int nslots, int k, int n, int K, int *grid, size_t *partial_floats, int *blocks,
+                        int *xops) {
   const int cc = exl3_gemv_cta_cols(K);
   const long long colblocks = (n + cc - 1) / cc, op_rows = colblocks * (k / 16);
   const long long total = (long long)U * nslots * op_rows;
@@ -1027,13 +1035,18 @@ bool exl3_moe_gemv_plan(int U, int nslots, int k, int n, int K, int *grid, size_
   if (g < 1) return false;
   if ((unsigned long long)total * (unsigned long long)g >= (1ull << 32)) return false;
   const long long range = (total + g - 1) / g;
-  if ((range + op_rows - 1) / op_rows + 1 > kGemvMaxOps) return false;
+  // x' slots for the ops a CTA's range may touch (at least kGemvMaxOps, at
+  // most kGemvMaxOpsMoe), with two ring stages beside them
+  const long long need = (range + op_rows - 1) / op_rows + 1;
+  if (need > kGemvMaxOpsMoe) return false;
+  const int xo = need > kGemvMaxOps ? (int)need : kGemvMaxOps;
   int st = 0;
-  EXL3_K_SWITCH(K, st = Launcher<KK, true, true>::stages(k));
+  EXL3_K_SWITCH(K, st = Launcher<KK, true, true>::stages(k, xo));
   if (st < 2) return false;
   *grid = (int)g;
   *blocks = (int)(U * nslots * colblocks);
   *partial_floats = (size_t)(*blocks + g) * (size_t)cc;
+  if (xops) *xops = xo;
   return true;
 }
 
@@ -1050,7 +1063,8 @@ cudaError_t exl3_launch_moe_gemv(const uint16_t *x, const float *act_in, int *po
   if (!fn) return cudaErrorNotSupported;
   int grid = 0, blocks = 0;
   size_t pf = 0;
-  if (!exl3_moe_gemv_plan(U, nslots, k, n, K, &grid, &pf, &blocks)) return cudaErrorInvalidValue;
+  int xo = kGemvMaxOps;
+  if (!exl3_moe_gemv_plan(U, nslots, k, n, K, &grid, &pf, &blocks, &xo)) return cudaErrorInvalidValue;
   const int cc = exl3_gemv_cta_cols(K);
   // all experts' trellis as u64 rows: row (e nslots + slot) k/16 + tk
   CUtensorMap tm;
@@ -1065,6 +1079,7 @@ cudaError_t exl3_launch_moe_gemv(const uint16_t *x, const float *act_in, int *po
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
   GemvArgs a{};
+  a.xops = kGemvMaxOps;
   a.x = reinterpret_cast<const __half *>(x);
   a.suh = reinterpret_cast<const __half *>(suh);
   a.svh = reinterpret_cast<const __half *>(svh);
@@ -1093,7 +1108,8 @@ cudaError_t exl3_launch_moe_gemv(const uint16_t *x, const float *act_in, int *po
   a.op_rows = (uint32_t)a.colblocks * (uint32_t)a.tiles_k;
   a.total = (uint32_t)a.nops * a.op_rows;
   a.stages = 0;
-  EXL3_K_SWITCH(K, a.stages = Launcher<KK, true, true>::stages(k));
+  a.xops = xo;
+  EXL3_K_SWITCH(K, a.stages = Launcher<KK, true, true>::stages(k, xo));
   cudaError_t e = cudaSuccess;
   // The down projection (act_in set) is a programmatic dependent of the gate
   // and up launch: it streams its experts' weights (the expert ids are final
@@ -1169,6 +1185,7 @@ cudaError_t exl3_launch_moe_gemv_widths(const uint16_t *x, const float *act_in, 
   GemvShardMaps maps;
   memset(&maps, 0, sizeof maps);
   GemvArgs a{};
+  a.xops = kGemvMaxOps;
   for (int r = 0; r < runs; ++r) {   // run r's experts' trellis as u64 rows: row (e' nslots + slot) k/16 + tk
     const int cc = exl3_gemv_cta_cols(K[r]);
     cuuint64_t dims[3] = {(cuuint64_t)4 * K[r], (cuuint64_t)(n / 16), (cuuint64_t)cnt[r] * nslots * (k / 16)};
@@ -1243,7 +1260,9 @@ cudaError_t exl3_launch_moe_gemv_widths(const uint16_t *x, const float *act_in, 
 // GEMV (one unit, S slots, no expert ids).  False when a CTA's range would
 // touch more than kGemvMaxOps shards or x' for them does not fit.
 bool exl3_gemv_shards_plan(int S, int k, int n, int K, int *grid, size_t *partial_floats, int *blocks) {
-  return exl3_moe_gemv_plan(1, S, k, n, K, grid, partial_floats, blocks);
+  int xo = kGemvMaxOps;
+  if (!exl3_moe_gemv_plan(1, S, k, n, K, grid, partial_floats, blocks, &xo)) return false;
+  return xo <= kGemvMaxOps;   // the shards' launch keeps kGemvMaxOps x' slots
 }
 
 cudaError_t exl3_launch_gemv_shards(const uint16_t *x, int S, int k, int n, int K, const uint16_t *trellis,
@@ -1268,6 +1287,7 @@ cudaError_t exl3_launch_gemv_shards(const uint16_t *x, int S, int k, int n, int 
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
   GemvArgs a{};
+  a.xops = kGemvMaxOps;
   a.x = reinterpret_cast<const __half *>(x);
   a.suh = reinterpret_cast<const __half *>(suh);
   a.svh = reinterpret_cast<const __half *>(svh);
@@ -1353,6 +1373,7 @@ cudaError_t exl3_launch_gemv_shards_var(const uint16_t *x, int S, int k, const i
   memset(&maps, 0, sizeof maps);
   GemvArgs a{};
   memset(&a, 0, sizeof a);
+  a.xops = kGemvMaxOps;
   size_t words = 0;
   int vo = 0, vb = 0;
   for (int i = 0; i < S; ++i) {
