@@ -167,7 +167,7 @@ def test_moe_gateup_split_over_k(E, topk, T, hidden, inter, K):
                                                         (16, 256, 8, 2048, 512, 3, 3), (32, 256, 8, 2048, 512, 3, 3),
                                                         (9, 96, 8, 512, 256, 4, 6)])
 def test_moe_few_tokens_grouped_gemv(T, E, topk, hidden, inter, K, K2):
-    """Up to 32 routed rows, or up to one per expert, take the few-token
+    """Up to 32 routed rows, or up to 1.25 per expert, take the few-token
     path: gate and up as grouped M = 1 GEMVs over (unit, slot), SiLU, down as
     grouped GEMVs times the routing weight, and the combine.  32 rows at the
     pages' shape is the first boundary, 128 and 256 rows over 256 experts

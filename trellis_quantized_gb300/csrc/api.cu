@@ -275,11 +275,12 @@ struct MoeWs {
 
 // The few-token path (one grouped CUDA-core GEMV launch per projection, no
 // sort) runs instead of the tensor-core tiles for up to 32 routed rows, and
-// for up to one routed row per expert (at most 512 rows, and as long as no
-// CTA's share spans more ops than the GEMV keeps x' for): it decodes every
-// routed row's expert weights separately, at about twice the rate per
+// for up to 1.25 routed rows per expert (at most 512 rows, and as long as
+// no CTA's share spans more ops than the GEMV keeps x' for): it decodes
+// every routed row's expert weights separately, at about twice the rate per
 // weight of the tile kernels' decoders, which pays while few rows share an
-// expert (E = 256, top-8, T = 16: 0.090 ms against 0.124 ms).
+// expert (E = 256, top-8: T = 16 0.090 against 0.124 ms, T = 40 0.196
+// against about 0.205 ms; at T = 48 the tiles are faster).
 constexpr int kMoeGemvMaxU = 32;
 constexpr int kMoeGemvMaxUPerExpert = 512;
 constexpr int kMoeMixedGemvMaxU = 32;   // the mixed-width kernel counts units with one warp ballot
@@ -307,7 +308,8 @@ MoeWs moe_ws(int T, int topk, int E, int hidden, int inter, int K13, int K2, boo
   if (allow_gemv) {
     int g1 = 0, g2 = 0, b1 = 0, b2 = 0;
     size_t p1 = 0, p2 = 0;
-    const bool few = U <= (size_t)kMoeGemvMaxU || (U <= (size_t)E && U <= (size_t)kMoeGemvMaxUPerExpert);
+    const bool few =
+        U <= (size_t)kMoeGemvMaxU || (4 * U <= (size_t)5 * E && U <= (size_t)kMoeGemvMaxUPerExpert);
     if (few && exl3_moe_gemv_plan((int)U, 2, hidden, inter, K13, &g1, &p1, &b1) &&
         exl3_moe_gemv_plan((int)U, 1, inter, hidden, K2, &g2, &p2, &b2) && (size_t)b1 <= kMaxCounters &&
         (size_t)b2 <= kMaxCounters) {
