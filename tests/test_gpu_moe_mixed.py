@@ -107,12 +107,14 @@ def test_moe_mixed_invalid_expert_id_is_reported_and_skipped():
     assert_close(host(y).astype(np.float64), _oracle(c, ids=ref_ids, weights=ref_w), "mixed invalid id")
 
 
-@pytest.mark.parametrize("T", [1, 4])
+@pytest.mark.parametrize("T", [1, 4, 16, 32])
 def test_moe_mixed_few_tokens_grouped_gemv(T):
-    """At most 32 routed rows take the few-token path: per projection one
-    grouped M = 1 GEMV launch whose CTAs split over the widths of the routed
-    experts (found on the device).  The MoE workload's shape with two widths
-    per projection; deterministic, with the arrival counters back at zero."""
+    """Up to 32 routed rows, or up to 1.25 per expert, take the few-token
+    path: per projection one grouped M = 1 GEMV launch whose CTAs split over
+    the widths of the routed experts (found on the device, each CTA keeping
+    its width's unit list in shared memory: 8 to 256 units here).  The MoE
+    workload's shape with two widths per projection; deterministic, with the
+    arrival counters back at zero."""
     K13 = [3] * 128 + [4] * 128
     K2 = [4] * 128 + [3] * 128
     c = synth.mixed_moe_case(61, T, T, K13, K2)

@@ -89,7 +89,7 @@ struct GemvArgs {
   // tensor map s.
   int var;
   int vn[8], vo[8], vb[9];
-  // Routed experts of mixed widths (GROUPED, runs > 0, at most 32 units):
+  // Routed experts of mixed widths (GROUPED, runs > 0, at most 512 units):
   // this launch serves the experts of runs [run_lo[r], run_hi[r]) of one
   // width (tensor map r, over run r's part of the packed arena from expert
   // run_lo[r]).  The units whose expert lies in one of them are the active
@@ -97,6 +97,7 @@ struct GemvArgs {
   // o % nslots) and counted on the device, so that the rows split evenly
   // over the CTAs whatever the routing; `total` is then found on the device.
   int runs, units;
+  int wlist_off;            // byte offset of the unit list in dynamic shared memory (past every width's layout)
   int run_lo[8], run_hi[8], run_K[8];
   // per width K (index 1..8) of a launch over runs of several widths: column
   // blocks, ring stages, and the width's first arrival counter and partial
@@ -110,7 +111,8 @@ struct GemvArgs {
 // partial slots of its column blocks.
 struct GemvPart {
   int me, grid;
-  uint32_t total, op_rows, active;
+  uint32_t total, op_rows;
+  const int *ulist;         // mixed widths: this width's units in unit order (shared memory), else NULL
   int colblocks, stages;
   int *counters;
   float *partials;
@@ -155,7 +157,7 @@ __device__ __forceinline__ void gemv_write_pos(const GemvArgs &a, int tid, int n
 }
 
 template <bool GROUPED, bool F32OUT>
-__device__ __forceinline__ GemvOp gemv_op(const GemvArgs &a, int o, uint32_t active = 0) {
+__device__ __forceinline__ GemvOp gemv_op(const GemvArgs &a, int o, const int *ulist = nullptr) {
   if constexpr (!GROUPED) {
     return GemvOp{a.x, a.suh, a.svh, a.y, 1.0f, 0, false, 0, 0};
   } else {
@@ -164,11 +166,7 @@ __device__ __forceinline__ GemvOp gemv_op(const GemvArgs &a, int o, uint32_t act
                     static_cast<char *>(a.y) + (long)a.vo[o] * (F32OUT ? 4 : 2), 1.0f, 0, false, o, 0};
     int u = o / a.nslots;
     const int slot = o - u * a.nslots;
-    if (a.runs) {   // the u-th active unit
-      uint32_t m = active;
-      for (int i = 0; i < u; ++i) m &= m - 1;
-      u = __ffs(m) - 1;
-    }
+    if (a.runs) u = ulist[u];   // the u-th unit of this width
     int e = a.ids ? a.ids[u] : 0;   // no id list: every unit uses expert 0 (fused shards)
     const bool bad = e < 0 || e >= a.E;
     float scale = a.weights ? a.weights[u] : 1.0f;
@@ -306,7 +304,8 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap *maps, const GemvArg
   // Row arithmetic is 32-bit (the host keeps grid * total below 2^32): a
   // 64-bit division is a long software sequence on every path's start.
   const uint32_t TKU = (uint32_t)TK;
-  const uint32_t total = p.total, active = p.active;
+  const uint32_t total = p.total;
+  const int *ulist = p.ulist;
   const uint32_t t0 = me < grid ? range_start(me, total, grid) : 0;
   const uint32_t t1 = me < grid ? range_start(me + 1, total, grid) : 0;
   if (t0 >= t1) {
@@ -344,7 +343,7 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap *maps, const GemvArg
         const int tk_first = (int)(t - c * TKU), nrows = (int)(seg_end - t);
         const int op = GROUPED ? op_of_block(a, p, (int)c) : 0;
         const int tn0 = (GROUPED ? block_in_op(a, p, (int)c, op) : (int)c) * (S::CTA_COLS / 16);
-        const GemvOp Pp = gemv_op<GROUPED, F32OUT>(a, op, active);
+        const GemvOp Pp = gemv_op<GROUPED, F32OUT>(a, op, ulist);
         const int trow = Pp.trow + tk_first;
         const CUtensorMap *tmT = maps + Pp.map;
         for (int r0 = 0; r0 < nrows && !*s_abort; r0 += S::R) {
@@ -411,7 +410,7 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap *maps, const GemvArg
       const int c = (int)(t / TKU);   // block: op c / colblocks, column block c % colblocks
       const uint32_t seg_end = min(t1, (uint32_t)(c + 1) * TKU);
       const int op = GROUPED ? op_of_block(a, p, c) : 0;
-      const GemvOp P = gemv_op<GROUPED, F32OUT>(a, op, active);
+      const GemvOp P = gemv_op<GROUPED, F32OUT>(a, op, ulist);
       const int nop = GROUPED ? op_width(a, op) : a.n;
       const float *rs = rsum + (op - op0) * (a.k / 16);
       const int col0 = (GROUPED ? block_in_op(a, p, c, op) : c) * S::CTA_COLS;
@@ -587,7 +586,7 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap *maps, const GemvArg
     }
     for (int i = warp; i < nc; i += NCW) {
       const int jop = GROUPED ? i / KC : 0;               // op op0 + jop
-      const GemvOp P = gemv_op<GROUPED, F32OUT>(a, op0 + jop, active);
+      const GemvOp P = gemv_op<GROUPED, F32OUT>(a, op0 + jop, ulist);
       if (GROUPED && P.bad && lane == 0 && i % KC == 0) set_device_error(a.err, kErrExpertId);
       const int e0 = ((c0 + i - jop * KC) % KC) * 512 + lane * 16;
       const bool live = e0 < a.k;   // k is a multiple of 128: whole 8-lane groups
@@ -736,7 +735,7 @@ __device__ __forceinline__ void gemv_body(const CUtensorMap *maps, const GemvArg
 
 // The partition of a launch over one width: every CTA of the grid.
 __device__ __forceinline__ GemvPart gemv_whole_grid(const GemvArgs &a) {
-  return GemvPart{(int)blockIdx.x, (int)gridDim.x, a.total, a.op_rows, 0u, a.colblocks, a.stages, a.counters,
+  return GemvPart{(int)blockIdx.x, (int)gridDim.x, a.total, a.op_rows, nullptr, a.colblocks, a.stages, a.counters,
                   a.partials};
 }
 
@@ -764,21 +763,31 @@ static_assert(GemvShape<1>::THREADS == kGemvThreads && GemvShape<3>::THREADS == 
 
 // Routed experts of mixed widths for a few tokens, one launch per
 // projection: the runs (at most 8, their tensor maps in `maps`) have widths
-// run_K[r].  Every CTA finds the active units of each width (lane u of a
-// warp holds unit u), splits the grid over the widths in proportion to
-// their rows (at least one CTA each, and no more CTAs than rows), and runs
-// the decode of its width on its share; the widths' column blocks have their
+// run_K[r].  Every CTA counts the units of each width (warp ballots, 32
+// units at a time), splits the grid over the widths in proportion to their
+// weights (at least one CTA each, as many for every column block, no more
+// CTAs than rows), lists its width's units in shared memory and runs the
+// decode of its width on its share; the widths' column blocks have their
 // own arrival counters and partial slots.
 template <bool F32OUT>
 __global__ void __launch_bounds__(kGemvThreads, 1)
     gemv_widths_kernel(const __grid_constant__ GemvShardMaps maps, GemvArgs a) {
   const int lane = threadIdx.x & 31, me = blockIdx.x;
-  int ku = 0;   // width of unit `lane`'s expert (0: no run of this launch)
-  if (lane < a.units) {
-    const int e = a.ids[lane];
-    const int r = gemv_run_of(a, e);
-    if (r >= 0) ku = a.run_K[r];
-    if (me == 0 && threadIdx.x < 32 && (e < 0 || e >= a.E)) set_device_error(a.err, kErrExpertId);
+  // width of unit u's expert (0: no run of this launch)
+  auto width_of = [&](int u) -> int {
+    if (u >= a.units) return 0;
+    const int r = gemv_run_of(a, a.ids[u]);
+    return r >= 0 ? a.run_K[r] : 0;
+  };
+  uint32_t count[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};   // units of each width (every warp counts them all)
+  for (int base = 0; base < a.units; base += 32) {
+    const int ku = width_of(base + lane);
+    if (me == 0 && threadIdx.x < 32 && base + lane < a.units) {
+      const int e = a.ids[base + lane];
+      if (e < 0 || e >= a.E) set_device_error(a.err, kErrExpertId);
+    }
+#pragma unroll
+    for (int w = 1; w <= 8; ++w) count[w] += (uint32_t)__popc(__ballot_sync(0xffffffffu, ku == w));
   }
   // Rows of odd widths hold 256 columns, of even widths 128: the CTAs are
   // split in proportion to each width's weights, so that every CTA decodes
@@ -787,13 +796,12 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
                                    GemvShape<1>::CTA_COLS, GemvShape<2>::CTA_COLS, GemvShape<3>::CTA_COLS,
                                    GemvShape<4>::CTA_COLS, GemvShape<5>::CTA_COLS, GemvShape<6>::CTA_COLS,
                                    GemvShape<7>::CTA_COLS, GemvShape<8>::CTA_COLS};
-  uint32_t rows[9], mask[9];
+  uint32_t rows[9];
   unsigned long long weights[9], all = 0;
   int nw = 0;
 #pragma unroll
   for (int w = 1; w <= 8; ++w) {
-    mask[w] = __ballot_sync(0xffffffffu, ku == w);
-    rows[w] = (uint32_t)__popc(mask[w]) * (uint32_t)a.nslots * (uint32_t)a.wcolblocks[w] * (uint32_t)a.tiles_k;
+    rows[w] = count[w] * (uint32_t)a.nslots * (uint32_t)a.wcolblocks[w] * (uint32_t)a.tiles_k;
     weights[w] = (unsigned long long)rows[w] * cols_of[w];
     all += weights[w];
     nw += rows[w] > 0;
@@ -824,11 +832,24 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     if (me == 0) gemv_write_pos(a, threadIdx.x, kGemvThreads);
     return;
   }
+  // this width's units in unit order, past every width's shared-memory layout
+  extern __shared__ __align__(128) uint8_t gw_smem[];
+  int *ulist = reinterpret_cast<int *>(gw_smem + a.wlist_off);
+  if (threadIdx.x < 32) {
+    int pos = 0;
+    for (int base = 0; base < a.units; base += 32) {
+      const bool mine = width_of(base + lane) == wsel;
+      const uint32_t bal = __ballot_sync(0xffffffffu, mine);
+      if (mine) ulist[pos + __popc(bal & ((1u << lane) - 1u))] = base + lane;
+      pos += __popc(bal);
+    }
+  }
+  __syncthreads();
   GemvPart p;
   p.me = me - first;
   p.grid = (uint32_t)cnt < rows[wsel] ? cnt : (int)rows[wsel];   // every CTA taking part owns a row
   p.total = rows[wsel];
-  p.active = mask[wsel];
+  p.ulist = ulist;
   p.colblocks = a.wcolblocks[wsel];
   p.op_rows = (uint32_t)p.colblocks * (uint32_t)a.tiles_k;
   p.stages = a.wstages[wsel];
@@ -859,8 +880,8 @@ struct Launcher {
   static size_t xbytes(int k, int xops = kGemvMaxOps) {
     return (GROUPED ? xops : 1) * (4 * (size_t)k + (size_t)k / 4);
   }
-  static int stages(int k, int xops = kGemvMaxOps) {
-    const long avail = (long)kGemvSmemMax - S::FIXED_B - (long)xbytes(k, xops);
+  static int stages(int k, int xops = kGemvMaxOps, size_t reserve = 0) {
+    const long avail = (long)kGemvSmemMax - S::FIXED_B - (long)xbytes(k, xops) - (long)reserve;
     long st = avail / S::STAGE_B;
     if (st > kGemvMaxStages) st = kGemvMaxStages;
     return (int)st;
@@ -1125,9 +1146,13 @@ cudaError_t exl3_launch_moe_gemv(const uint16_t *x, const float *act_in, int *po
 // trellis + words[r]) as grouped M = 1 GEMVs, all widths in one launch.
 // Arguments otherwise as exl3_launch_moe_gemv (y [U * nslots][n] fp32).
 // partial_floats / counters_needed (optional): the sizes it uses.
+// Units the mixed-width kernel takes: its unit list lives in shared memory.
+constexpr int kGemvWidthsMaxUnits = 512;
+static size_t gemv_list_bytes(int U) { return ((size_t)U * sizeof(int) + 15) & ~(size_t)15; }
+
 bool exl3_moe_gemv_widths_plan(int U, int nslots, int k, int n, int runs, const int *K, int *grid,
-                               size_t *partial_floats, int *counters_needed) {
-  if (runs < 1 || runs > kGemvMaxShards || U < 1 || U > 32) return false;
+                               size_t *partial_floats, int *counters_needed, int *xops) {
+  if (runs < 1 || runs > kGemvMaxShards || U < 1 || U > kGemvWidthsMaxUnits) return false;
   const long long g = gemv_sm_count();
   bool seen[9] = {};
   int nw = 0;
@@ -1148,9 +1173,6 @@ bool exl3_moe_gemv_widths_plan(int U, int nslots, int k, int n, int runs, const 
     const long long rows = (long long)U * nslots * op_rows;
     max_rows += rows;
     if (rows * cc > max_weights) max_weights = rows * cc;
-    int st = 0;
-    EXL3_K_SWITCH(w, st = Launcher<KK, true, true>::stages(k));
-    if (st < 2) return false;
     pf += (size_t)(U * nslots * colblocks + g) * (size_t)cc;
     cnt += (int)(U * nslots * colblocks);
   }
@@ -1158,15 +1180,27 @@ bool exl3_moe_gemv_widths_plan(int U, int nslots, int k, int n, int runs, const 
   // weights, so a CTA of width w gets at most about (all weights) / (cols(w)
   // (g - nw)) rows; all weights are at most max_weights (units of one
   // width's weights add up to at most what all U units would have at the
-  // width with the most).  The share must touch no more than kGemvMaxOps ops.
+  // width with the most).  The x' slots cover the ops such a share touches
+  // (at least kGemvMaxOps, at most kGemvMaxOpsMoe), with two ring stages
+  // beside them and the unit list.
+  int xo = kGemvMaxOps;
   for (int w = 1; w <= 8; ++w) {
     if (!seen[w]) continue;
     const int cc = exl3_gemv_cta_cols(w);
     const long long op_rows = ((n + cc - 1) / cc) * (k / 16);
     const long long range = (max_weights + (long long)cc * (g - nw) - 1) / ((long long)cc * (g - nw)) + 1;
-    if ((range + op_rows - 1) / op_rows + 1 > kGemvMaxOps) return false;
+    const long long need = (range + op_rows - 1) / op_rows + 1;
+    if (need > kGemvMaxOpsMoe) return false;
+    if (need > xo) xo = (int)need;
     if ((unsigned long long)max_rows * (unsigned long long)g >= (1ull << 32)) return false;
   }
+  for (int w = 1; w <= 8; ++w) {
+    if (!seen[w]) continue;
+    int st = 0;
+    EXL3_K_SWITCH(w, st = Launcher<KK, true, true>::stages(k, xo, gemv_list_bytes(U)));
+    if (st < 2) return false;
+  }
+  if (xops) *xops = xo;
   *grid = (int)g;
   if (partial_floats) *partial_floats = pf;
   if (counters_needed) *counters_needed = cnt;
@@ -1180,8 +1214,8 @@ cudaError_t exl3_launch_moe_gemv_widths(const uint16_t *x, const float *act_in, 
                                         float *partials, int *counters, int *err, cudaStream_t s, bool prefetch) {
   auto fn = gemv_tmap_fn();
   if (!fn) return cudaErrorNotSupported;
-  int grid = 0;
-  if (!exl3_moe_gemv_widths_plan(U, nslots, k, n, runs, K, &grid, nullptr, nullptr)) return cudaErrorInvalidValue;
+  int grid = 0, xo = kGemvMaxOps;
+  if (!exl3_moe_gemv_widths_plan(U, nslots, k, n, runs, K, &grid, nullptr, nullptr, &xo)) return cudaErrorInvalidValue;
   GemvShardMaps maps;
   memset(&maps, 0, sizeof maps);
   GemvArgs a{};
@@ -1201,7 +1235,10 @@ cudaError_t exl3_launch_moe_gemv_widths(const uint16_t *x, const float *act_in, 
     a.run_K[r] = K[r];
   }
   // per width: column blocks, ring stages, and the first counter and
-  // partial slot of its blocks; the shared memory is the largest width's
+  // partial slot of its blocks; the shared memory is the largest width's,
+  // then the unit list
+  a.xops = xo;
+  const size_t list = gemv_list_bytes(U);
   size_t sm = 0;
   int cbase = 0;
   size_t pbase = 0;
@@ -1211,13 +1248,15 @@ cudaError_t exl3_launch_moe_gemv_widths(const uint16_t *x, const float *act_in, 
     if (!seen[w]) continue;
     const int cc = exl3_gemv_cta_cols(w);
     a.wcolblocks[w] = (n + cc - 1) / cc;
-    EXL3_K_SWITCH(w, a.wstages[w] = Launcher<KK, true, true>::stages(k);
-                  sm = std::max(sm, Launcher<KK, true, true>::smem(k, a.wstages[w])));
+    EXL3_K_SWITCH(w, a.wstages[w] = Launcher<KK, true, true>::stages(k, xo, list);
+                  sm = std::max(sm, Launcher<KK, true, true>::smem(k, a.wstages[w], xo)));
     a.wcounter_base[w] = cbase;
     a.wpartial_base[w] = (int)pbase;
     cbase += U * nslots * a.wcolblocks[w];
     pbase += (size_t)(U * nslots * a.wcolblocks[w] + grid) * (size_t)cc;
   }
+  a.wlist_off = (int)((sm + 15) & ~(size_t)15);
+  sm = (size_t)a.wlist_off + list;
   a.runs = runs;
   a.units = U;
   a.x = reinterpret_cast<const __half *>(x);
