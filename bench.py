@@ -76,7 +76,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # at k=5120 n=25600, with the hash of the kernel's sources at capture time; a
 # changed kernel source makes the recorded traffic stale (reported as null).
 TRAFFIC = {"files": ["trellis_quantized_gb300/csrc/gemv.cu", "trellis_quantized_gb300/csrc/gemv_core.cuh"],
-           "sha1": "284cfd7a8ebacb73ea130138a1c570c78f85a0cd", "bytes_per_launch": 65668608,
+           "sha1": "34067c50ee440772cca2e6a4266b32187a114944", "bytes_per_launch": 65668608,
            "workload": "k5120 n25600 K4 M1"}
 
 
