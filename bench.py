@@ -754,11 +754,11 @@ def bench_extras(only=None, moe_tokens=None):
             "row_invariant_k5120_n17408": inv, "moe_E256_top8_h2048_i512_K3": moe,
             "moe_mixed_E256_top8_h2048_i512_K3K4": mixed,
             "note": "MoE: device remap + gather/RHT + two grouped tcgen05 kernels decoding the experts' trellis "
-                    "on the fly + fixed-order combine (expert tiles of 32/128/256 rows by routed rows per "
-                    "expert); up to 32 routed rows, or up to one per expert: one grouped M=1 GEMV launch per "
-                    "projection + combine. "
-                    "Mixed widths: the tile kernels once per run of equal width (two runs here); up to 32 "
-                    "routed rows one grouped GEMV launch per projection over all runs"}
+                    "on the fly + fixed-order combine (expert tiles of 32/128/160/256 rows by routed rows per "
+                    "expert); up to 32 routed rows, or up to 1.25 per expert: one grouped M=1 GEMV launch per "
+                    "projection + combine. Mixed widths: the tile kernels once per run of equal width (two runs "
+                    "here); up to 32 routed rows, or up to one per expert, one grouped GEMV launch per "
+                    "projection over all widths"}
 
 
 # ---------------------------------------------------------------- pipe ceilings
