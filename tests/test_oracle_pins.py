@@ -9,6 +9,8 @@ attention", "MoE (routed experts)", "Adding a model"); "Bringing EXL3 Trellis
 Quantization to 35B MoE on Intel Arc 140V" (sections 1 and 2.B); "EXL3
 checkpoints on the native engine (tracker) #832".
 """
+from fractions import Fraction
+
 import numpy as np
 import pytest
 import scipy.linalg
@@ -187,11 +189,60 @@ def test_fwht_matches_matrix_product():
     assert np.max(np.abs(Hn @ Hn - np.eye(128))) < 1e-14
 
 
-def test_rht_in_f32_is_close_to_f64():
-    case = synth.linear_case(90, 0, 3, 512, 128, 2)
+U32 = 2.0 ** -24                                       # binary32 unit roundoff
+C_RHT = 2.0 ** -3.5                                    # 1/sqrt(128)
+
+
+def _tie_rows():
+    """fp16 rows whose Hadamard-domain sums S are chosen integers.
+
+    x = H.S / 128 is exact in fp16 (multiples of 1/128 below 16), so the
+    binary32 butterflies reproduce S exactly. Every row has S = 508 at
+    position 0 (its amax) and three entries S = +-2s, s odd, for which
+    127 * S / 508 = s / 2 is exactly halfway between two integers.
+    """
+    rows, sums = [], []
+    odd = list(range(1, 254, 2))
+    for i in range(0, len(odd), 3):
+        S = np.zeros(128, np.int64)
+        S[0] = 508
+        for j, s in enumerate(odd[i:i + 3]):
+            S[1 + 5 * j + i % 7] = 2 * s * (-1 if (i + j) % 2 else 1)
+        v = H128.astype(np.int64) @ S
+        assert np.abs(v).max() < 2048
+        rows.append(v / 128.0)
+        sums.append(S)
+    x = np.array(rows, dtype=np.float16)
+    assert np.array_equal(x.astype(np.float64), np.array(rows))
+    return x.view(np.uint16), np.ones(128, np.float16).view(np.uint16), np.array(sums)
+
+
+def test_rht_in_f32_exact_sums_are_one_rounding_from_the_definition():
+    # With exact butterflies the only errors are fp32(2^-3.5) and the final
+    # product, so every x' is within 2u (relative) of S * 2^-3.5, and a zero
+    # sum stays exactly zero. A wrong scale, sign or position fails this.
+    x, suh, S = _tie_rows()
+    a32 = oracle.rht_in_f32(x, suh).astype(np.float64)
+    exact = S * C_RHT
+    assert np.array_equal(a32 == 0, S == 0)
+    assert np.all(np.abs(a32 - exact) <= (2 * U32 + U32 * U32) * np.abs(exact))
+
+
+def test_rht_in_f32_within_the_pairwise_summation_bound():
+    # Forward error of a 7-level butterfly tree in binary32 (pairwise
+    # summation, Higham's gamma_7 bound) plus the two roundings of the scale:
+    #   |x'32 - x'| <= c * gamma_7 * (1 + 3u) * sum_j |x_j suh_j| + (2u + u^2) |x'|
+    # per element, with x' the float64 transform pinned above.
+    case = synth.linear_case(90, 0, 3, 512, 128, 2, outlier_rows=0.3)
     a64 = oracle.rht_in_f64(case.x, case.suh)
     a32 = oracle.rht_in_f32(case.x, case.suh).astype(np.float64)
-    assert np.max(np.abs(a32 - a64)) <= 1e-5 * np.max(np.abs(a64))
+    v = np.abs(case.x.astype(np.float64) * case.suh.astype(np.float64))
+    l1 = v.reshape(3, 4, 128).sum(axis=2).repeat(128, axis=1)
+    gamma7 = 7 * U32 / (1 - 7 * U32)
+    bound = C_RHT * gamma7 * (1 + 3 * U32) * l1 + (2 * U32 + U32 * U32) * np.abs(a64)
+    assert np.all(np.abs(a32 - a64) <= bound * (1 + 1e-9) + 1e-300)
+    # the bound is tight enough to matter: it sits far below the 1e-5 level
+    assert np.max(bound) < 1e-5 * np.max(np.abs(a64))
 
 
 # ------------------------------------------------------------ the linear -----
@@ -291,6 +342,45 @@ def test_int8_activation_quant_properties():
         assert np.float32(amax / 127) == a[r]
         assert np.abs(q[r]).max() == 127
         assert np.max(np.abs(q[r] * np.float64(a[r]) - xr[r])) <= 0.5 * a[r] * (1 + 1e-5)
+
+
+def _rne(t):
+    """Round-half-even of exact rationals (Fractions) to integers."""
+    out = []
+    for f in t:
+        lo = f.numerator // f.denominator
+        rem = f - lo
+        out.append(lo + (1 if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and lo % 2) else 0))
+    return np.array(out, dtype=np.float64)
+
+
+def test_int8_activation_quant_reading_is_multiply_by_fp32_inverse():
+    # Which of three plausible roundings the int8 path takes is a reading of
+    # "Prefill: int8 linears" (per-row absmax scale, codes in [-127, 127]):
+    #   (a) RNE(fp32(x' * fp32(127 / amax)))   -- this library's reading
+    #   (b) RNE(fp32(x' / a_r)), a_r = fp32(amax / 127)
+    #   (c) RNE of the exact rational x' * 127 / amax
+    # They agree except near halfway points. The rows of _tie_rows put 127
+    # elements exactly at halfway points of the definition, where fp32
+    # rounding decides; the oracle must match (a) everywhere and differ from
+    # (b) and (c) at many of these elements, so that the pin separates them.
+    x, suh, S = _tie_rows()
+    q, a = oracle.quant_act(x, suh)
+    xr = oracle.rht_in_f32(x, suh)
+    amax = np.abs(xr).max(axis=1)
+    assert np.array_equal(amax, np.abs(xr[:, 0]))
+    ties = S * 127 % 508 == 254                        # 127 S / 508 = m + 1/2
+    assert ties.sum() == 127
+    qa = np.rint(xr * (np.float32(127) / amax)[:, None]).astype(np.float64)
+    qb = np.rint(xr / (amax / np.float32(127))[:, None]).astype(np.float64)
+    qc = np.array([_rne([Fraction(float(t)) * 127 / Fraction(float(m)) for t in row])
+                   for row, m in zip(xr, amax)])
+    assert np.abs(qa).max() <= 127
+    assert np.array_equal(q.astype(np.float64), qa)
+    assert np.array_equal(qa[~ties], qc[~ties])        # off the ties all agree
+    assert (qa != qb)[ties].sum() >= 20
+    assert (qa != qc)[ties].sum() >= 20
+    assert np.array_equal(a, (amax / np.float32(127)).astype(np.float32))
 
 
 def test_int8_accumulators_and_output():
