@@ -13,6 +13,7 @@ import exl3_synth as synth
 import oracle
 import trellis_quantized_gb300 as tq
 from gpu_util import assert_close, dev, host
+from tie_rows import tie_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -51,6 +52,17 @@ def test_int8_config3_all_widths_and_rows(K, M):
     """Every (K, M) pair of the mixed-width layer through the int8 variant:
     q_x, row scales and accumulators bit-exact on every row."""
     _check(synth.config3(K, M))
+
+
+def test_int8_activation_codes_at_exact_ties():
+    """127 activations sit exactly halfway between two codes of the
+    definition, where only the fp32 rounding of x' * fp32(127 / amax) decides
+    the code: q_x, the row scales and the accumulators must still be
+    bit-exact."""
+    x, suh, _ = tie_rows()
+    case = synth.linear_case(22, 0, x.shape[0], 128, 256, 4)
+    case.x, case.suh = x, suh
+    _check(case)
 
 
 def test_int8_config4_sampled_rows():

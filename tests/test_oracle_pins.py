@@ -18,6 +18,7 @@ import scipy.special
 
 import exl3_synth as synth
 import oracle
+from tie_rows import tie_rows
 
 BOUND = 3.453125
 H128 = scipy.linalg.hadamard(128).astype(np.float64)   # Sylvester, natural order
@@ -193,35 +194,11 @@ U32 = 2.0 ** -24                                       # binary32 unit roundoff
 C_RHT = 2.0 ** -3.5                                    # 1/sqrt(128)
 
 
-def _tie_rows():
-    """fp16 rows whose Hadamard-domain sums S are chosen integers.
-
-    x = H.S / 128 is exact in fp16 (multiples of 1/128 below 16), so the
-    binary32 butterflies reproduce S exactly. Every row has S = 508 at
-    position 0 (its amax) and three entries S = +-2s, s odd, for which
-    127 * S / 508 = s / 2 is exactly halfway between two integers.
-    """
-    rows, sums = [], []
-    odd = list(range(1, 254, 2))
-    for i in range(0, len(odd), 3):
-        S = np.zeros(128, np.int64)
-        S[0] = 508
-        for j, s in enumerate(odd[i:i + 3]):
-            S[1 + 5 * j + i % 7] = 2 * s * (-1 if (i + j) % 2 else 1)
-        v = H128.astype(np.int64) @ S
-        assert np.abs(v).max() < 2048
-        rows.append(v / 128.0)
-        sums.append(S)
-    x = np.array(rows, dtype=np.float16)
-    assert np.array_equal(x.astype(np.float64), np.array(rows))
-    return x.view(np.uint16), np.ones(128, np.float16).view(np.uint16), np.array(sums)
-
-
 def test_rht_in_f32_exact_sums_are_one_rounding_from_the_definition():
     # With exact butterflies the only errors are fp32(2^-3.5) and the final
     # product, so every x' is within 2u (relative) of S * 2^-3.5, and a zero
     # sum stays exactly zero. A wrong scale, sign or position fails this.
-    x, suh, S = _tie_rows()
+    x, suh, S = tie_rows()
     a32 = oracle.rht_in_f32(x, suh).astype(np.float64)
     exact = S * C_RHT
     assert np.array_equal(a32 == 0, S == 0)
@@ -360,11 +337,11 @@ def test_int8_activation_quant_reading_is_multiply_by_fp32_inverse():
     #   (a) RNE(fp32(x' * fp32(127 / amax)))   -- this library's reading
     #   (b) RNE(fp32(x' / a_r)), a_r = fp32(amax / 127)
     #   (c) RNE of the exact rational x' * 127 / amax
-    # They agree except near halfway points. The rows of _tie_rows put 127
+    # They agree except near halfway points. The rows of tie_rows put 127
     # elements exactly at halfway points of the definition, where fp32
     # rounding decides; the oracle must match (a) everywhere and differ from
     # (b) and (c) at many of these elements, so that the pin separates them.
-    x, suh, S = _tie_rows()
+    x, suh, S = tie_rows()
     q, a = oracle.quant_act(x, suh)
     xr = oracle.rht_in_f32(x, suh)
     amax = np.abs(xr).max(axis=1)
