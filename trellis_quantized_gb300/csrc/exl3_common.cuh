@@ -113,6 +113,88 @@ __device__ __forceinline__ void fwht128_x8(float (&v)[16], int lane) {
   }
 }
 
+// FWHT-128 that exchanges half of the values per cross-lane stage (8
+// shuffles instead of 16), on packed pairs of fp32 lanes.  Eight lanes hold a
+// block as in fwht128_x8 (p[i] = elements 2i, 2i + 1 of the lane's 16),
+// except that a lane with l & 1 set holds its two 8-element halves swapped
+// (p[0..3] = elements 16 (l mod 8) + 8 ..15, loaded that way).  In each stage
+// h = 16, 32, 64 a lane keeps p[0..3], sends p[4..7] to its partner, and
+// computes the sum and the difference of eight of the sixteen pairs; the next
+// stage's lane bit decides which of p[0..3] / p[4..7] takes which, so no value
+// is ever selected.  A lane whose kept operand is the upper one of its pairs
+// computes b - a in place of a - b, so values carry a sign per lane;
+// fwht128_xh_signs gives the factors that restore them.  Stages h >= 2 run two
+// butterflies per packed instruction (add.rn.f32x2, or fma.rn.f32x2 with a
+// factor of +-1: one rounding of the sum or difference).  Every result is the
+// single rounding of fwht128_x8's (negation is exact), so the transform equals
+// fwht128_x8's except possibly for the sign of a zero.  On return lane l holds
+// block elements 8 (l mod 8) + 2i, +1 in p[i] and 64 + 8 (l mod 8) + 2i, +1
+// in p[4 + i] (i < 4), before the sign factors.
+__device__ __forceinline__ void fwht128_xh(float2 (&p)[8], int lane) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {                  // h = 1, inside each pair
+    const float a = p[i].x, b = p[i].y;
+    p[i] = make_float2(a + b, a - b);
+  }
+  const float2 neg = make_float2(-1.0f, -1.0f);
+#pragma unroll
+  for (int h = 1; h < 4; h <<= 1)                // h = 2, 4 (1, 2 pairs apart)
+#pragma unroll
+    for (int i = 0; i < 8; i += 2 * h)
+#pragma unroll
+      for (int j = i; j < i + h; ++j) {
+        const float2 a = p[j], b = p[j + h];
+        p[j] = __fadd2_rn(a, b);
+        p[j + h] = __ffma2_rn(neg, b, a);
+      }
+  {                                              // h = 8 on the swapped halves
+    const float s0 = (lane & 1) ? -1.0f : 1.0f;
+    const float2 sp = make_float2(s0, s0), sn = make_float2(-s0, -s0);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 lo = p[i], hi = p[i + 4];
+      p[i] = __ffma2_rn(sp, lo, hi);
+      p[i + 4] = __ffma2_rn(sn, hi, lo);
+    }
+  }
+#pragma unroll
+  for (int m = 1; m < 8; m <<= 1) {              // h = 16, 32, 64 with lane l ^ m
+    // where the results go: by the next stage's lane bit (the last stage puts
+    // the sum first)
+    const float c = (m < 4 && (lane & (2 * m))) ? -1.0f : 1.0f;
+    const float2 cp = make_float2(c, c), cn = make_float2(-c, -c);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 r = make_float2(__shfl_xor_sync(0xffffffffu, p[i + 4].x, m),
+                                   __shfl_xor_sync(0xffffffffu, p[i + 4].y, m));
+      const float2 k = p[i];
+      p[i] = __ffma2_rn(cp, r, k);
+      p[i + 4] = __ffma2_rn(cn, r, k);
+    }
+  }
+}
+
+// Sign factors of fwht128_xh's p[0..3] (lo) and p[4..7] (hi) on this lane.
+__device__ __forceinline__ void fwht128_xh_signs(int lane, float &lo, float &hi) {
+  const float s0 = (lane & 1) ? -1.0f : 1.0f, s1 = (lane & 2) ? -1.0f : 1.0f, s2 = (lane & 4) ? -1.0f : 1.0f;
+  lo = ((lane & 2) ? s0 : 1.0f) * ((lane & 4) ? s1 : 1.0f);
+  hi = lo * s2;
+}
+
+// The exact fp32 products of two pairs of binary16 values (a 22-bit product
+// always fits): one mixed-precision FMA per value, with a -0 addend so that a
+// zero product keeps its sign.
+__device__ __forceinline__ float2 mul_f16x2_exact(uint32_t x, uint32_t s) {
+  float lo, hi;
+  asm("{\n.reg .f16 xl, xh, sl, sh;\n.reg .b16 b0, b1, b2, b3;\n"
+      "mov.b32 {b0, b1}, %2;\nmov.b32 {b2, b3}, %3;\n"
+      "mov.b16 xl, b0;\nmov.b16 xh, b1;\nmov.b16 sl, b2;\nmov.b16 sh, b3;\n"
+      "fma.rn.f32.f16 %0, xl, sl, 0f80000000;\nfma.rn.f32.f16 %1, xh, sh, 0f80000000;\n}\n"
+      : "=f"(lo), "=f"(hi)
+      : "r"(x), "r"(s));
+  return make_float2(lo, hi);
+}
+
 // ------------------------------------------------------------ small helpers --
 
 __device__ __forceinline__ void set_device_error(int *err, int bit) {

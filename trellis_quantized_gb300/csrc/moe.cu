@@ -213,19 +213,22 @@ __global__ void __launch_bounds__(1024) remap_small_kernel(const int32_t *__rest
 // xg[i] = RHT(x_t . suh_gate[e]), xu[i] = RHT(x_t . suh_up[e]), t = perm[i] / topk.
 // One warp per sorted row: the row's unit and expert are looked up once, and
 // the row's 512-element chunks follow one another with the loads of chunk
-// c + 1 issued before chunk c is transformed (lane l holds 16 contiguous
-// elements of a chunk, the fwht128_x8 layout).
+// c + 1 issued before chunk c is transformed.  Lane l loads 16 contiguous
+// elements of a chunk, its two halves swapped on odd lanes, for fwht128_xh,
+// and stores the two 8-element runs that the transform leaves it.
 struct GatherIn {
   uint4 x[2], g[2], u[2];
 };
 
+// half q of the lane's 16 elements comes from col + 8 (q ^ sw)
 __device__ __forceinline__ void gather_load(GatherIn &in, const __half *xr, const __half *sg, const __half *su,
-                                            int col, bool live) {
+                                            int col, int sw, bool live) {
 #pragma unroll
   for (int q = 0; q < 2; ++q) {
-    in.x[q] = live ? *reinterpret_cast<const uint4 *>(xr + col + 8 * q) : make_uint4(0u, 0u, 0u, 0u);
-    in.g[q] = live ? __ldg(reinterpret_cast<const uint4 *>(sg + col + 8 * q)) : make_uint4(0u, 0u, 0u, 0u);
-    in.u[q] = live ? __ldg(reinterpret_cast<const uint4 *>(su + col + 8 * q)) : make_uint4(0u, 0u, 0u, 0u);
+    const int c = col + 8 * (q ^ sw);
+    in.x[q] = live ? *reinterpret_cast<const uint4 *>(xr + c) : make_uint4(0u, 0u, 0u, 0u);
+    in.g[q] = live ? __ldg(reinterpret_cast<const uint4 *>(sg + c)) : make_uint4(0u, 0u, 0u, 0u);
+    in.u[q] = live ? __ldg(reinterpret_cast<const uint4 *>(su + c)) : make_uint4(0u, 0u, 0u, 0u);
   }
 }
 
@@ -246,36 +249,43 @@ __global__ void __launch_bounds__(256) gather_rht_kernel(const __half *__restric
   const __half *sg = suh13 + (long)e * 2 * hidden, *su = sg + hidden;
   __half *dg = xg + i * hidden, *du = xu + i * hidden;
   const int chunks = (hidden + 511) / 512;
+  const int sw = lane & 1;
+  float slo, shi;
+  fwht128_xh_signs(lane, slo, shi);
+  const float2 klo = make_float2(slo * kRhtScale, slo * kRhtScale);   // the output scale with the sign factors
+  const float2 khi = make_float2(shi * kRhtScale, shi * kRhtScale);
+  const int olo = 128 * (lane >> 3) + 8 * (lane & 7);   // the lane's output runs in a chunk: olo, olo + 64
   GatherIn cur, nxt;
-  gather_load(cur, xr, sg, su, 16 * lane, 16 * lane < hidden);
+  gather_load(cur, xr, sg, su, 16 * lane, sw, 16 * lane < hidden);
 #pragma unroll 1
   for (int c = 0; c < chunks; ++c) {
     const int col = c * 512 + 16 * lane;
     const bool in = col < hidden;      // whole 128-blocks are in or out (hidden % 128 == 0)
-    if (c + 1 < chunks) gather_load(nxt, xr, sg, su, col + 512, col + 512 < hidden);
-    const __half *xh = reinterpret_cast<const __half *>(cur.x);
-    const __half *gh = reinterpret_cast<const __half *>(cur.g);
-    const __half *uh = reinterpret_cast<const __half *>(cur.u);
-    float a[16], b[16];
+    if (c + 1 < chunks) gather_load(nxt, xr, sg, su, col + 512, sw, col + 512 < hidden);
+    const uint32_t *xw = reinterpret_cast<const uint32_t *>(cur.x);
+    const uint32_t *gw = reinterpret_cast<const uint32_t *>(cur.g);
+    const uint32_t *uw = reinterpret_cast<const uint32_t *>(cur.u);
+    float2 a[8], b[8];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const float xx = __half2float(xh[j]);
-      a[j] = xx * __half2float(gh[j]);
-      b[j] = xx * __half2float(uh[j]);
+    for (int j = 0; j < 8; ++j) {
+      a[j] = mul_f16x2_exact(xw[j], gw[j]);
+      b[j] = mul_f16x2_exact(xw[j], uw[j]);
     }
-    fwht128_x8(a, lane);
-    fwht128_x8(b, lane);
+    fwht128_xh(a, lane);
+    fwht128_xh(b, lane);
     if (in) {
       __align__(16) __half2 og[8], ou[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        og[j] = __floats2half2_rn(a[2 * j] * kRhtScale, a[2 * j + 1] * kRhtScale);
-        ou[j] = __floats2half2_rn(b[2 * j] * kRhtScale, b[2 * j + 1] * kRhtScale);
+        const float2 k = j < 4 ? klo : khi;
+        og[j] = __float22half2_rn(__fmul2_rn(a[j], k));
+        ou[j] = __float22half2_rn(__fmul2_rn(b[j], k));
       }
+      const long o = (long)c * 512 + olo;
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
-        *reinterpret_cast<uint4 *>(dg + col + 8 * q) = reinterpret_cast<const uint4 *>(og)[q];
-        *reinterpret_cast<uint4 *>(du + col + 8 * q) = reinterpret_cast<const uint4 *>(ou)[q];
+        *reinterpret_cast<uint4 *>(dg + o + 64 * q) = reinterpret_cast<const uint4 *>(og)[q];
+        *reinterpret_cast<uint4 *>(du + o + 64 * q) = reinterpret_cast<const uint4 *>(ou)[q];
       }
     }
     cur = nxt;
