@@ -75,8 +75,9 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # dram bytes (read + write) per launch from an ncu capture of gemv_m1_kernel<4>
 # at k=5120 n=25600, with the hash of the kernel's sources at capture time; a
 # changed kernel source makes the recorded traffic stale (reported as null).
-TRAFFIC = {"files": ["trellis_quantized_gb300/csrc/gemv.cu", "trellis_quantized_gb300/csrc/gemv_core.cuh"],
-           "sha1": "34067c50ee440772cca2e6a4266b32187a114944", "bytes_per_launch": 65668608,
+TRAFFIC = {"files": ["trellis_quantized_gb300/csrc/gemv.cu", "trellis_quantized_gb300/csrc/gemv_core.cuh",
+                     "trellis_quantized_gb300/csrc/exl3_common.cuh"],
+           "sha1": "f2e2cc0efb10200a5f71703c019acfcba9b7827f", "bytes_per_launch": 65670400,
            "workload": "k5120 n25600 K4 M1"}
 
 

@@ -76,11 +76,13 @@ __device__ __forceinline__ void fwht128_warp(float v[4], int lane) {
   a = v[1]; b = v[3]; v[1] = a + b; v[3] = a - b;
 #pragma unroll
   for (int m = 1; m < 32; m <<= 1) {
-    const bool upper = (lane & m) != 0;
+    // lower lane: v + other; upper lane: other - v; both one rounding of
+    // fma(+-1, v, other), with no select between two results
+    const float sgn = (lane & m) ? -1.0f : 1.0f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      float other = __shfl_xor_sync(0xffffffffu, v[j], m);
-      v[j] = upper ? (other - v[j]) : (v[j] + other);
+      const float other = __shfl_xor_sync(0xffffffffu, v[j], m);
+      v[j] = fmaf(sgn, v[j], other);
     }
   }
 }
